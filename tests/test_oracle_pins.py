@@ -1,0 +1,339 @@
+"""Pins of the CPU oracle against facts fixed by the pages and by mathematics.
+
+Nothing here compares the oracle with itself: each check uses an independent
+library routine (numpy fancy indexing, matmul, tril_indices; torch CPU
+modules), a closed form, an invariant, exhaustive enumeration, or a
+hand-computed fixture under tests/golden/.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import dlrm_synth as synth
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _arr(x, dt):
+    return np.array(x, dtype=dt)
+
+
+# ---------------------------------------------------------------- pair map
+
+def test_pair_closed_form_exhaustive_f_le_256(oracle_lib):
+    """p -> (i, j) closed form equals the i-major enumeration for every F <= 256.
+
+    Luminal compare modal_ci_ready...vanilla-pytorch, commit message,
+    PairwiseDotLowerTriStackedKernel: pair (i, j) from p via (1+sqrt(1+8p))/2.
+    The enumeration for F is a prefix of that for F+1, so F = 256 covers all.
+    """
+    f = 256
+    ei, ej = oracle.pair_enumerate(f, oracle_lib)
+    # the enumeration itself is the strict lower triangle, row-major
+    ti, tj = np.tril_indices(f, -1)
+    np.testing.assert_array_equal(ei, ti)
+    np.testing.assert_array_equal(ej, tj)
+    for p in range(f * (f - 1) // 2):
+        assert oracle.pair_from_index(p, oracle_lib) == (ei[p], ej[p]), p
+
+
+def test_pair_counts_and_shape_invariants():
+    """F(F-1)/2 and ln_top[0] = D + P for the pages' mini shape and the workloads.
+
+    dlrm_megakernel.rs tests shape_invariants: F = 4 -> 6 pairs, ln_top[0] = m_spa + n_pairs.
+    """
+    mini = synth.get_config("mini_b2048_k3_d4")
+    assert mini.n_features == 4 and mini.n_pairs == 6
+    assert mini.ln_top[0] == mini.emb_dim + mini.n_pairs == 10
+    assert synth.get_config("b2048_k32").n_pairs == 528
+    assert synth.get_config("b65536_k26_zipf").n_pairs == 351
+    for name in ("tiny_b64_k3", "b2048_k3", "b2048_k32", "b65536_k26_zipf"):
+        c = synth.get_config(name)
+        assert c.ln_top[0] == c.emb_dim + c.n_pairs and c.ln_top[-1] == 1
+        assert c.ln_bot[-1] == c.emb_dim
+
+
+# ---------------------------------------------------------------- bag sum
+
+def test_bag_size_one_is_index_select(oracle_lib):
+    """With one index per bag the bag sum is a row lookup (index_select), bit-exact.
+
+    LessonsLearned 'EmbeddingBag translator gap': for bag size 1 it is just an
+    embedding lookup.
+    """
+    cfg = synth.sweep_config(257, 5)
+    cfg = synth.DlrmConfig("t", 257, cfg.ln_bot, (1000, 700, 1, 33, 5000), 24, 1, cfg.ln_top)
+    tables = [synth.make_table(cfg, 7, t) for t in range(cfg.n_tables)]
+    idx = synth.make_indices(cfg, 7)
+    off = synth.make_offsets(cfg)
+    e = oracle.embedding_bag_sum(tables, idx, off, lib=oracle_lib)
+    for t in range(cfg.n_tables):
+        expect = np.take(tables[t], idx[t], axis=0)
+        np.testing.assert_array_equal(e[:, t, :].astype(np.float32), expect)
+        np.testing.assert_array_equal(e[:, t, :], expect.astype(np.float64))
+
+
+def test_bag_sum_permutation_invariant(oracle_lib):
+    """Permuting indices inside each bag leaves the bag sum unchanged (<= 1 ulp in fp32)."""
+    cfg = synth.get_config("tiny_b64_k3")
+    cfg = synth.DlrmConfig("t", 96, cfg.ln_bot, (1000,) * 3, 16, 7, cfg.ln_top, 0.05)
+    tables = [synth.make_table(cfg, 3, t) for t in range(3)]
+    idx = synth.make_indices(cfg, 3)
+    off = synth.make_offsets(cfg)
+    base = oracle.embedding_bag_sum(tables, idx, off, lib=oracle_lib).astype(np.float32)
+    rng = np.random.default_rng(0)
+    perm = idx.copy().reshape(3, 96, 7)
+    for t in range(3):
+        for b in range(96):
+            perm[t, b] = perm[t, b][rng.permutation(7)]
+    assert not np.array_equal(perm.reshape(3, -1), idx)
+    got = oracle.embedding_bag_sum(tables, perm.reshape(3, -1), off,
+                                   lib=oracle_lib).astype(np.float32)
+    ulp = np.spacing(np.maximum(np.abs(base), np.abs(got)))
+    assert np.all(np.abs(got - base) <= ulp)
+
+
+def test_bag_sum_general_offsets_and_empty_bags(oracle_lib):
+    """General offsets: bag b spans offsets[b]..offsets[b+1] (last bag to N); empty bag = 0."""
+    table = np.arange(20, dtype=np.float32).reshape(10, 2)   # row r = [2r, 2r+1]
+    idx = np.array([[3, 1, 4, 1, 5, 9, 2, 6]], np.int64)
+    off = np.array([[0, 2, 2, 5]], np.int64)  # bags: {3,1}, {}, {4,1,5}, {9,2,6}
+    e = oracle.embedding_bag_sum([table], idx, off, lib=oracle_lib)
+    expect = np.array([[6 + 2, 7 + 3], [0, 0], [8 + 2 + 10, 9 + 3 + 11],
+                       [18 + 4 + 12, 19 + 5 + 13]], np.float64)
+    np.testing.assert_array_equal(e[:, 0, :], expect)
+
+
+def test_bag_sum_out_of_range_index_flags(oracle_lib):
+    """An index outside [0, rows) contributes zeros and reports INDEX_OOB."""
+    table = np.ones((4, 3), np.float32)
+    idx = np.array([[0, 7, -1, 2]], np.int64)
+    off = np.array([[0, 2]], np.int64)
+    e, rc = oracle.embedding_bag_sum([table], idx, off, allow_oob=True, lib=oracle_lib,
+                                     return_status=True)
+    assert rc == oracle.INDEX_OOB
+    np.testing.assert_array_equal(e[:, 0, :], [[1, 1, 1], [1, 1, 1]])
+    with pytest.raises(oracle.OracleError):
+        oracle.embedding_bag_sum([table], idx, off, lib=oracle_lib)
+
+
+def test_bag_sum_matches_torch_embedding_bag(oracle_lib):
+    """Library cross-check: torch.nn.functional.embedding_bag(mode='sum') in float64."""
+    torch = pytest.importorskip("torch")
+    cfg = synth.get_config("tiny_b64_k3")
+    inp = synth.make_inputs(cfg, seed=11)
+    e = oracle.embedding_bag_sum(inp["tables"], inp["indices"], inp["offsets"], lib=oracle_lib)
+    for t in range(cfg.n_tables):
+        ref = torch.nn.functional.embedding_bag(
+            torch.from_numpy(inp["indices"][t]), torch.from_numpy(inp["tables"][t]).double(),
+            torch.from_numpy(inp["offsets"][t]), mode="sum").numpy()
+        np.testing.assert_allclose(e[:, t, :], ref, rtol=1e-12, atol=1e-15)
+
+
+# ---------------------------------------------------------------- interaction
+
+@pytest.mark.parametrize("k,d", [(1, 8), (3, 16), (8, 5), (32, 64), (26, 128)])
+def test_interaction_is_lower_triangle_of_gram(oracle_lib, k, d):
+    """z equals the strict lower triangle of Z Z^T read row-major, and R = [x, z].
+
+    Luminal compare modal_ci_ready...vanilla-pytorch, commit message: the
+    interaction is Z[:, li, lj] over bmm(cat(...), permute(..., [0,2,1])).
+    """
+    rng = np.random.default_rng(k * 1000 + d)
+    b = 9
+    x = rng.standard_normal((b, d))
+    e = rng.standard_normal((b, k, d))
+    r = oracle.interaction(x, e, lib=oracle_lib)
+    z_stack = np.concatenate([x[:, None, :], e], axis=1)           # (B, F, D)
+    gram = np.matmul(z_stack, np.transpose(z_stack, (0, 2, 1)))    # (B, F, F)
+    li, lj = np.tril_indices(k + 1, -1)
+    np.testing.assert_allclose(r[:, d:], gram[:, li, lj], rtol=1e-12, atol=1e-12)
+    np.testing.assert_array_equal(r[:, :d], x)
+
+
+def test_interaction_hand_fixture(oracle_lib):
+    g = _golden("hand_interaction_f4.json")
+    r = oracle.interaction(_arr(g["x"], np.float64), _arr(g["emb"], np.float64), lib=oracle_lib)
+    np.testing.assert_array_equal(r, _arr(g["expected_R"], np.float64))
+    ei, ej = oracle.pair_enumerate(4, oracle_lib)
+    assert [list(p) for p in zip(ei.tolist(), ej.tolist())] == g["expected_pairs"]
+
+
+# ---------------------------------------------------------------- linear
+
+@pytest.mark.parametrize("act", [oracle.ACT_NONE, oracle.ACT_RELU, oracle.ACT_SIGMOID])
+def test_linear_matches_matmul(oracle_lib, act):
+    """y = act(x W^T + b) against numpy matmul; W is (out, in) as in nn.Linear."""
+    rng = np.random.default_rng(act)
+    x = rng.standard_normal((37, 19))
+    w = rng.standard_normal((11, 19)).astype(np.float32)
+    b = rng.standard_normal(11).astype(np.float32)
+    y = oracle.linear(x, w, b, act, lib=oracle_lib)
+    a = x @ w.astype(np.float64).T + b.astype(np.float64)
+    ref = {oracle.ACT_NONE: a, oracle.ACT_RELU: np.maximum(a, 0.0),
+           oracle.ACT_SIGMOID: 1.0 / (1.0 + np.exp(-a))}[act]
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-12)
+    y0 = oracle.linear(x, w, None, act, lib=oracle_lib)
+    a0 = x @ w.astype(np.float64).T
+    ref0 = {oracle.ACT_NONE: a0, oracle.ACT_RELU: np.maximum(a0, 0.0),
+            oracle.ACT_SIGMOID: 1.0 / (1.0 + np.exp(-a0))}[act]
+    np.testing.assert_allclose(y0, ref0, rtol=1e-12, atol=1e-12)
+
+
+def test_linear_non_square_orientation(oracle_lib):
+    """A transposed weight would not even match shapes; check one element by hand."""
+    x = np.array([[1.0, 2.0, 3.0]])
+    w = np.array([[1, 0, 0], [0, 0, 10]], np.float32)    # out 2, in 3
+    y = oracle.linear(x, w, np.array([0.5, -1], np.float32), oracle.ACT_NONE, lib=oracle_lib)
+    np.testing.assert_array_equal(y, [[1.5, 29.0]])
+
+
+# ---------------------------------------------------------------- forward
+
+def _golden_inputs(g):
+    return dict(
+        dense=_arr(g["dense"], np.float32),
+        tables=[_arr(t, np.float32) for t in g["tables"]],
+        indices=_arr(g["indices"], np.int64), offsets=_arr(g["offsets"], np.int64),
+        bot_w=[_arr(w, np.float32) for w in g["bot_w"]],
+        bot_b=[_arr(v, np.float32) for v in g["bot_b"]],
+        top_w=[_arr(w, np.float32) for w in g["top_w"]],
+        top_b=[_arr(v, np.float32) for v in g["top_b"]])
+
+
+def test_forward_hand_fixture(oracle_lib):
+    """Hand-computed forward: ReLU after the last bottom layer, bag sums, pair
+    order, concat position, top ReLU and final sigmoid all matter here."""
+    g = _golden("hand_forward_f3.json")
+    inp = _golden_inputs(g)
+    out = oracle.forward(inp, lib=oracle_lib)
+    np.testing.assert_allclose(out, g["expected_out"], rtol=0, atol=1e-15)
+    x = oracle.linear(inp["dense"], inp["bot_w"][0], inp["bot_b"][0], oracle.ACT_RELU,
+                      lib=oracle_lib)
+    np.testing.assert_array_equal(x, g["expected_x"])
+    e = oracle.embedding_bag_sum(inp["tables"], inp["indices"], inp["offsets"], lib=oracle_lib)
+    np.testing.assert_array_equal(e, g["expected_bags"])
+    np.testing.assert_array_equal(oracle.interaction(x, e, lib=oracle_lib), g["expected_R"])
+
+
+def test_forward_sample_subset_matches_full(oracle_lib):
+    cfg = synth.get_config("tiny_b64_k3")
+    inp = synth.make_inputs(cfg, seed=5)
+    full = oracle.forward(inp, lib=oracle_lib)
+    ids = np.array([63, 0, 17, 17, 40])
+    np.testing.assert_array_equal(oracle.forward(inp, sample_ids=ids, lib=oracle_lib), full[ids])
+    # single-threaded gives the same bits (no reduction is split across threads)
+    np.testing.assert_array_equal(oracle.forward(inp, threads=1, lib=oracle_lib), full)
+
+
+def test_forward_zero_last_top_layer_is_sigmoid_of_bias(oracle_lib):
+    """All-zero last top weights: out = sigmoid(b_last) for every sample; sigmoid(0) = 0.5."""
+    cfg = synth.get_config("tiny_b64_k3")
+    inp = synth.make_inputs(cfg, seed=9)
+    inp["top_w"][-1] = np.zeros_like(inp["top_w"][-1])
+    b_last = float(inp["top_b"][-1][0])
+    out = oracle.forward(inp, lib=oracle_lib)
+    np.testing.assert_allclose(out, 1.0 / (1.0 + math.exp(-b_last)), rtol=0, atol=1e-16)
+    inp["top_b"][-1] = np.zeros_like(inp["top_b"][-1])
+    np.testing.assert_array_equal(oracle.forward(inp, lib=oracle_lib), 0.5)
+
+
+def test_forward_selectors_pin_concat_and_pairs(oracle_lib):
+    """Identity bottom MLP and a one-hot single-layer top MLP read single entries of R.
+
+    With W_bot = I, b_bot = 0 and dense >= 0, x = dense. A top layer whose
+    weight is the unit vector e_c gives out = sigmoid(R[c]): c < D reads x[c],
+    c = D + p reads the dot of pair p = (i, j), checked against numpy.
+    """
+    d, k, b = 4, 3, 16
+    f = k + 1
+    p_count = f * (f - 1) // 2
+    rng = np.random.default_rng(1)
+    dense = np.abs(rng.standard_normal((b, d))).astype(np.float32)
+    tables = [rng.uniform(-1, 1, (50, d)).astype(np.float32) for _ in range(k)]
+    idx = rng.integers(0, 50, (k, b * 2)).astype(np.int64)
+    off = np.ascontiguousarray(np.broadcast_to(np.arange(b) * 2, (k, b))).astype(np.int64)
+    bags = np.stack([np.take(tables[t], idx[t].reshape(b, 2), axis=0).astype(np.float64).sum(1)
+                     for t in range(k)], axis=1)                          # (B, K, D)
+    feats = np.concatenate([dense.astype(np.float64)[:, None, :], bags], axis=1)
+    li, lj = np.tril_indices(f, -1)
+    for c in range(d + p_count):
+        w = np.zeros((1, d + p_count), np.float32)
+        w[0, c] = 1.0
+        inp = dict(dense=dense, tables=tables, indices=idx, offsets=off,
+                   bot_w=[np.eye(d, dtype=np.float32)], bot_b=[np.zeros(d, np.float32)],
+                   top_w=[w], top_b=[np.zeros(1, np.float32)])
+        out = oracle.forward(inp, lib=oracle_lib)
+        if c < d:
+            val = dense[:, c].astype(np.float64)
+        else:
+            p = c - d
+            val = np.einsum("bd,bd->b", feats[:, li[p]], feats[:, lj[p]])
+        np.testing.assert_allclose(out, 1.0 / (1.0 + np.exp(-val)), rtol=1e-13, atol=1e-15)
+
+
+def test_forward_matches_torch_modules(oracle_lib):
+    """Library cross-check on the tiny workload: torch CPU float64 built from
+    nn.functional.embedding_bag, linear, bmm and tril_indices."""
+    torch = pytest.importorskip("torch")
+    cfg = synth.get_config("tiny_b64_k3")
+    inp = synth.make_inputs(cfg, seed=21)
+    t64 = lambda a: torch.from_numpy(np.asarray(a)).double()
+    h = t64(inp["dense"])
+    for w, bb in zip(inp["bot_w"], inp["bot_b"]):
+        h = torch.relu(torch.nn.functional.linear(h, t64(w), t64(bb)))
+    embs = [torch.nn.functional.embedding_bag(torch.from_numpy(inp["indices"][t]),
+                                              t64(inp["tables"][t]),
+                                              torch.from_numpy(inp["offsets"][t]), mode="sum")
+            for t in range(cfg.n_tables)]
+    z = torch.stack([h] + embs, dim=1)
+    gram = torch.bmm(z, z.transpose(1, 2))
+    li, lj = torch.tril_indices(cfg.n_features, cfg.n_features, -1)
+    r = torch.cat([h, gram[:, li, lj]], dim=1)
+    for l, (w, bb) in enumerate(zip(inp["top_w"], inp["top_b"])):
+        r = torch.nn.functional.linear(r, t64(w), t64(bb))
+        r = torch.sigmoid(r) if l == len(inp["top_w"]) - 1 else torch.relu(r)
+    out = oracle.forward(inp, lib=oracle_lib)
+    np.testing.assert_allclose(out, r[:, 0].numpy(), rtol=1e-12, atol=1e-14)
+
+
+def test_forward_rejects_inconsistent_shapes(oracle_lib):
+    """validate(): ln_top[0] must be D + P and ln_top[-1] must be 1."""
+    g = _golden("hand_forward_f3.json")
+    inp = _golden_inputs(g)
+    inp["top_w"][0] = np.zeros((2, 6), np.float32)     # 6 != D + P = 5
+    with pytest.raises(oracle.OracleError):
+        oracle.forward(inp, lib=oracle_lib)
+
+
+# ---------------------------------------------------------------- generator
+
+def test_generator_splitmix_reference_value():
+    """SplitMix64 started at state 0 yields 0xE220A8397B1DCDAF first (Steele, Lea and
+    Flood, OOPSLA 2014, reference implementation); streams are deterministic."""
+    assert synth.raw(0, 0) == 0xE220A8397B1DCDAF
+    a = [synth.element(1234, 5, i) for i in range(4)]
+    assert len(set(a)) == 4 and a == [synth.element(1234, 5, i) for i in range(4)]
+    assert synth.element(1234, 6, 0) != a[0] and synth.element(1235, 5, 0) != a[0]
+
+
+def test_generator_distributions():
+    u = synth.fill_uniform(np.empty(1 << 18, np.float32), 1, 2, -0.01, 0.01)
+    assert u.min() >= -0.01 and u.max() <= 0.01 and abs(u.mean()) < 1e-4
+    n = synth.fill_normal(np.empty(1 << 18, np.float32), 1, 3)
+    assert abs(n.mean()) < 0.01 and abs(n.std() - 1) < 0.01
+    z = synth.fill_index_zipf(np.empty(1 << 18, np.int64), 1, 4, 1_000_000, 1.05)
+    ranks = np.arange(1, 1_000_001, dtype=np.float64)
+    w = ranks ** -1.05
+    head = w[:10_000].sum() / w.sum()
+    assert abs((z < 10_000).mean() - head) < 0.005
+    assert z.min() >= 0 and z.max() < 1_000_000
