@@ -1,0 +1,471 @@
+#!/usr/bin/env python
+"""Bench of the GB300 DLRMv1 inference forward (samples/s and us/batch).
+
+A step is one dlrm_forward over one batch of the named synthetic workload
+(default: batch 2048, bottom 13-512-256-64, 3 tables x 100k x 64, one index
+per bag, top 70-512-256-1, fp32). Timing: W untimed warm-up steps, then K
+steps, each preceded by an L2 flush (a 256 MB write, larger than the 129 MB
+L2) and timed with CUDA events on the launching stream; the K event times are
+summed. One JSON line on stdout (rank 0).
+
+Extra objects on the line:
+  e2e        the same metric through dlrm_forward_host (pinned host buffers,
+             H2D of dense/indices/offsets and D2H of the output in the timed
+             region)
+  graph      the forward captured once in a CUDA graph and replayed
+  stages_us  per-stage device time from the library's event profiling mode
+  roofline   the dominant stage against its bound (FP32 FFMA peak from SM
+             count x 128 lanes x 2 x 2070 MHz, or measured HBM GB/s)
+  gather_b65536_k26_zipf  the standalone multi-table gather on the 13.3 GB
+             26-table workload (bags of 20, Zipf(1.05)) plus a uniform-index
+             control, algorithmic GB/s against measured HBM GB/s
+  cpu_baseline  the CPU oracle (fp64, all host cores) on a bounded sample
+
+--impl reference times the CPU oracle as the reference arm (there is no
+runnable reference implementation; the pages hold no code for this path).
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "DLRM fwd samples/sec & µs/batch at bs=2048; gather HBM GB/s vs roofline"
+UNIT = "samples/s"
+FLUSH_BYTES = 256 << 20
+FP32_LANES_PER_SM = 128
+SM_MAX_MHZ_DEFAULT = 2070.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="b2048_k3")
+    ap.add_argument("--seed", type=int, default=1234)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-gather", action="store_true",
+                    help="skip the 13.3 GB standalone-gather measurement")
+    ap.add_argument("--profile-steps", type=int, default=200)
+    ap.add_argument("--only-forward", action="store_true",
+                    help="time the device forward only (for ncu launch lists)")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm_gbs=float(p["hbm_gbs"]), bf16_tflops=float(p["bf16_tflops"]),
+                    sm_max_mhz=float(p.get("sm_max_mhz", SM_MAX_MHZ_DEFAULT)), source="measured")
+    except Exception:
+        return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, sm_max_mhz=SM_MAX_MHZ_DEFAULT,
+                    source="fallback")
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.windows = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def mark(self, t0: float, t1: float):
+        self.windows.append((t0, t1))
+
+    def finish(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        rows = []
+        for rec in csv.reader(io.StringIO(out)):
+            if len(rec) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(rec[0].strip().split(".")[0],
+                                               "%Y/%m/%d %H:%M:%S"))
+                frac = float("0." + rec[0].strip().split(".")[1]) if "." in rec[0] else 0.0
+                rows.append(dict(t=ts + frac, sm=float(rec[2]), smax=float(rec[3]),
+                                 power=float(rec[4]) if rec[4].strip() not in ("", "[N/A]") else None,
+                                 hw=rec[6].strip(), hwt=rec[7].strip(), swt=rec[8].strip(),
+                                 swp=rec[9].strip()))
+            except Exception:
+                continue
+        inside = [r for r in rows if any(a - 0.15 <= r["t"] <= b + 0.15 for a, b in self.windows)]
+        used = inside if inside else rows
+        if not used:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        reasons = set()
+        for r in used:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in used),
+                "sm_max_mhz": max(r["smax"] for r in used),
+                "reasons": sorted(reasons), "samples": len(used),
+                "samples_in_timed_region": len(inside)}
+
+
+# ---------------------------------------------------------------- oracle timing
+
+def time_oracle(inp, batch, budget_s, max_samples=None):
+    """Oracle samples/s on a bounded sample: whole batches (or a prefix of one)
+    repeated until budget_s of CPU time has run."""
+    import numpy as np
+    import oracle
+    lib = oracle.load()
+    threads = os.cpu_count() or 1
+    probe_ids = np.arange(min(batch, 64))
+    t0 = time.perf_counter()
+    oracle.forward(inp, sample_ids=probe_ids, threads=threads, lib=lib)
+    per_sample = max((time.perf_counter() - t0) / len(probe_ids), 1e-7)
+    n = int(min(batch, max(1, budget_s / per_sample / 2)))
+    if max_samples:
+        n = min(n, max_samples)
+    ids = np.arange(n)
+    done, t_start = 0, time.perf_counter()
+    reps = 0
+    while True:
+        oracle.forward(inp, sample_ids=ids, threads=threads, lib=lib)
+        done += n
+        reps += 1
+        if time.perf_counter() - t_start >= budget_s:
+            break
+    dt = time.perf_counter() - t_start
+    return dict(value=done / dt, unit=UNIT, cores=threads, kind="oracle",
+                sample=f"{n} of {batch} samples x {reps} repetitions ({dt:.1f} s, fp64, "
+                       f"{threads} threads)")
+
+
+# ---------------------------------------------------------------- reference arm
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    import numpy as np
+    import dlrm_synth as synth
+    import oracle
+    cfg = synth.get_config(args.config)
+    inp = synth.make_inputs(cfg, seed=args.seed)
+    lib = oracle.load()
+    threads = os.cpu_count() or 1
+    probe = np.arange(min(cfg.batch, 32))
+    t0 = time.perf_counter()
+    oracle.forward(inp, sample_ids=probe, threads=threads, lib=lib)
+    per_sample = max((time.perf_counter() - t0) / len(probe), 1e-7)
+    budget = 120.0 / max(1, args.steps + args.warmup)       # whole run within ~2 minutes
+    n = int(max(1, min(cfg.batch, budget / per_sample)))
+    ids = np.arange(n)
+    for _ in range(args.warmup):
+        oracle.forward(inp, sample_ids=ids, threads=threads, lib=lib)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.forward(inp, sample_ids=ids, threads=threads, lib=lib)
+    dt = time.perf_counter() - t0
+    value = n * args.steps / dt
+    line = dict(metric=METRIC, value=value, unit=UNIT, impl="reference", n_gpus=world,
+                steps=args.steps, warmup=args.warmup, ms_per_step=dt * 1e3 / args.steps,
+                higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64",
+                data="synthetic (seeded SplitMix64 inputs)",
+                config=dict(workload=cfg.name, batch=cfg.batch),
+                cpu_baseline=dict(kind="oracle", cores=threads, value=value, unit=UNIT,
+                                  sample=f"{n} of {cfg.batch} samples per step (fp64 CPU "
+                                         f"oracle, {threads} threads)"),
+                e2e=dict(value=value, unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0),
+                note="reference arm = the CPU oracle; the pages ship no runnable code")
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- our arm
+
+def stage_work(cfg, name, batch):
+    """Algorithmic (flops, bytes) of one stage launch."""
+    k, d, l = cfg.n_tables, cfg.emb_dim, cfg.bag_size
+    f = k + 1
+    p = f * (f - 1) // 2
+    if name == "gather":
+        byts = batch * k * l * d * 4 + batch * k * l * 8 + batch * k * 8 + batch * k * d * 4
+        return batch * k * (l - 1) * d, byts
+    if name == "interaction":
+        return 2 * batch * p * d, batch * f * d * 4 + batch * (d + p) * 4
+    widths = cfg.ln_bot if name.startswith("bottom") else cfg.ln_top
+    i = int(name[len("bottom"):] if name.startswith("bottom") else name[len("top"):])
+    kin, nout = widths[i], widths[i + 1]
+    return 2 * batch * kin * nout, 4 * (batch * kin + kin * nout + nout + batch * nout)
+
+
+def gather_measure(torch, dl, synth, pk, steps=10):
+    """Standalone gather on the 26 x 1M x 128 workload (bags of 20), Zipf and uniform."""
+    import numpy as np
+    cfg = synth.get_config("b65536_k26_zipf")
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(1234)
+    tables = [torch.empty((cfg.rows[t], cfg.emb_dim), device="cuda").uniform_(
+        -cfg.table_range, cfg.table_range, generator=gen) for t in range(cfg.n_tables)]
+    off = torch.from_numpy(synth.make_offsets(cfg)).cuda()
+    out = torch.empty((cfg.batch, cfg.n_tables, cfg.emb_dim), device="cuda")
+    _, byts = stage_work(cfg, "gather", cfg.batch)
+    res = {}
+    for dist in ("zipf", "uniform"):
+        c = cfg if dist == "zipf" else synth.DlrmConfig(
+            cfg.name, cfg.batch, cfg.ln_bot, cfg.rows, cfg.emb_dim, cfg.bag_size, cfg.ln_top)
+        idx = torch.from_numpy(synth.make_indices(c, 1234)).cuda()
+        s = torch.cuda.current_stream()
+        for _ in range(3):
+            dl.embedding_bag_sum_multi(tables, idx, off, out, cfg.bag_size, stream=s)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        torch.cuda.synchronize()
+        for a, b in ev:
+            a.record(s)
+            dl.embedding_bag_sum_multi(tables, idx, off, out, cfg.bag_size, stream=s)
+            b.record(s)
+        torch.cuda.synchronize()
+        ms = sum(a.elapsed_time(b) for a, b in ev) / steps
+        gbs = byts / (ms * 1e-3) / 1e9
+        res[dist] = dict(ms_per_launch=ms, algorithmic_gbs=gbs,
+                         frac_of_measured_hbm=gbs / pk["hbm_gbs"], frac_of_nominal_8tbs=gbs / 8000.0)
+        del idx
+    del tables, out
+    torch.cuda.empty_cache()
+    return dict(workload="26 tables x 1M x 128 fp32 (13.3 GB), batch 65536, bags of 20",
+                bytes_per_launch=byts, launches_timed=steps,
+                note="inputs far larger than L2; algorithmic bytes = rows + indices + offsets "
+                     "+ output; Zipf hot rows are served partly from L2", **res)
+
+
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    import dlrm_embedding_interaction_gb300 as dl
+    import dlrm_synth as synth
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    pk = peaks()
+    cfg = synth.get_config(args.config)
+    inp = synth.make_inputs(cfg, seed=args.seed)
+    cu = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    model = dl.DlrmModel(cfg.ln_bot, cfg.ln_top, [cu(t) for t in inp["tables"]],
+                         [cu(w) for w in inp["bot_w"]], [cu(b) for b in inp["bot_b"]],
+                         [cu(w) for w in inp["top_w"]], [cu(b) for b in inp["top_b"]],
+                         cfg.bag_size, cfg.batch)
+    dense, idx, off = cu(inp["dense"]), cu(inp["indices"]), cu(inp["offsets"])
+    out = torch.empty(cfg.batch, device=dev)
+    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    n_stages = len(model.stage_names())
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    def timed(step_fn, k, w):
+        with torch.cuda.stream(stream):
+            for _ in range(w):
+                flush_buf.zero_()
+                step_fn()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(k)]
+            torch.cuda.synchronize()
+            barrier()
+            torch.cuda.synchronize()
+            t0 = time.time()
+            for a, b in ev:
+                flush_buf.zero_()
+                a.record(stream)
+                step_fn()
+                b.record(stream)
+            torch.cuda.synchronize()
+            barrier()
+            torch.cuda.synchronize()
+            t1 = time.time()
+        ms = [a.elapsed_time(b) for a, b in ev]
+        return ms, (t0, t1)
+
+    clocks = ClockSampler(local_rank)
+    time.sleep(1.0)          # let nvidia-smi start sampling
+
+    # device-resident forward (the headline value)
+    ms, win = timed(lambda: model.forward(dense, idx, off, out, stream=stream),
+                    args.steps, args.warmup)
+    clocks.mark(*win)
+    if model.error(stream) != dl.OK:
+        raise RuntimeError("device error during the timed forward")
+    if args.only_forward:
+        clocks.finish()
+        model.close()
+        if rank == 0:
+            print(json.dumps(dict(metric=METRIC, value=cfg.batch * args.steps / (sum(ms) * 1e-3),
+                                  unit=UNIT, us_per_batch=sum(ms) * 1e3 / args.steps,
+                                  config=dict(workload=cfg.name), mode="only-forward")))
+        return 0
+    total_ms = sum(ms)
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * cfg.batch * args.steps / (total_ms * 1e-3)
+
+    # end to end through the host-buffer C-ABI call
+    h_dense = torch.from_numpy(inp["dense"]).pin_memory()
+    h_idx = torch.from_numpy(inp["indices"]).pin_memory()
+    h_off = torch.from_numpy(inp["offsets"]).pin_memory()
+    h_out = torch.empty(cfg.batch).pin_memory()
+    e2e_steps = max(1, args.steps // 5)
+    ms_e2e, win = timed(lambda: model.forward_host(h_dense, h_idx, h_off, h_out, stream=stream),
+                        e2e_steps, max(3, args.warmup // 5))
+    clocks.mark(*win)
+    if model.error(stream) != dl.OK:
+        raise RuntimeError("device error during the e2e forward")
+    e2e_total = sum(ms_e2e)
+    if dist is not None:
+        t = torch.tensor([e2e_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_total = float(t.item())
+    h2d = (inp["dense"].nbytes + inp["indices"].nbytes + inp["offsets"].nbytes)
+    e2e = dict(value=world * cfg.batch * e2e_steps / (e2e_total * 1e-3), unit=UNIT,
+               us_per_batch=e2e_total * 1e3 / e2e_steps, steps=e2e_steps,
+               h2d_bytes_per_step=int(h2d), d2h_bytes_per_step=int(cfg.batch * 4),
+               api="dlrm_forward_host (pinned host buffers)")
+
+    # CUDA-graph replay of the same forward
+    with torch.cuda.stream(stream):
+        model.forward(dense, idx, off, out, stream=stream)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        model.forward(dense, idx, off, out, stream=stream)
+    ms_g, win = timed(graph.replay, max(1, args.steps // 5), 3)
+    clocks.mark(*win)
+    graph_us = statistics.median(ms_g) * 1e3
+    clock_info = clocks.finish()
+
+    # per-stage device times (library event profiling, flush before each call)
+    model.set_profiling(True)
+    with torch.cuda.stream(stream):
+        for _ in range(args.profile_steps):
+            flush_buf.zero_()
+            model.forward(dense, idx, off, out, stream=stream)
+    names, totals, calls = model.stage_times()
+    model.set_profiling(False)
+    stage_us = {n: t * 1e3 / max(calls, 1) for n, t in zip(names, totals)}
+    dom = max(stage_us, key=stage_us.get)
+    flops, byts = stage_work(cfg, dom, cfg.batch)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    fp32_peak = sms * FP32_LANES_PER_SM * 2 * pk["sm_max_mhz"] * 1e6 / 1e12
+    t_dom = stage_us[dom] * 1e-6
+    if dom in ("gather", "interaction") and byts / (pk["hbm_gbs"] * 1e9) >= flops / (fp32_peak * 1e12):
+        ach = byts / t_dom / 1e9
+        roof = dict(bound="hbm", achieved=ach, peak=pk["hbm_gbs"], unit="GB/s",
+                    frac=ach / pk["hbm_gbs"], traffic=None, kernel=dom,
+                    peak_source=f"{pk['source']} (MEASURED_PEAKS hbm_gbs)")
+    else:
+        ach = flops / t_dom / 1e12
+        roof = dict(bound="alu", achieved=ach, peak=fp32_peak, unit="TFLOP/s",
+                    frac=ach / fp32_peak, traffic=None, kernel=dom,
+                    peak_source=f"FP32 FFMA: {sms} SMs x 128 lanes x 2 x {pk['sm_max_mhz']:.0f} MHz")
+    roof["algorithmic_per_launch"] = flops if roof["bound"] == "alu" else byts
+
+    # whole-forward roofline fraction (slower of HBM bytes and FP32 flops)
+    tot_flops = sum(stage_work(cfg, n, cfg.batch)[0] for n in names)
+    w_bytes = 4 * sum(a * b + b for a, b in zip(cfg.ln_bot[:-1], cfg.ln_bot[1:]))
+    w_bytes += 4 * sum(a * b + b for a, b in zip(cfg.ln_top[:-1], cfg.ln_top[1:]))
+    k, d, l = cfg.n_tables, cfg.emb_dim, cfg.bag_size
+    fwd_bytes = (cfg.batch * (k * l * d * 4 + k * l * 8 + k * 8 + cfg.n_dense * 4 + 4) + w_bytes)
+    t_roof = max(fwd_bytes / (pk["hbm_gbs"] * 1e9), tot_flops / (fp32_peak * 1e12))
+    forward_roofline = dict(algorithmic_flops=tot_flops, algorithmic_bytes=fwd_bytes,
+                            roofline_us=t_roof * 1e6, frac=t_roof / (ms_per_step * 1e-3),
+                            bound="alu (FP32 FFMA)" if tot_flops / (fp32_peak * 1e12) >
+                            fwd_bytes / (pk["hbm_gbs"] * 1e9) else "hbm")
+
+    gather = None
+    cpu = None
+    if rank == 0 and world == 1:
+        if not args.no_gather:
+            del flush_buf
+            torch.cuda.empty_cache()
+            gather = gather_measure(torch, dl, synth, pk)
+        if not args.no_cpu_baseline:
+            cpu = time_oracle(inp, cfg.batch, args.cpu_seconds)
+
+    model.close()
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+    line = dict(
+        metric=METRIC, value=value, unit=UNIT, n_gpus=world, steps=args.steps,
+        warmup=args.warmup, ms_per_step=ms_per_step, us_per_batch=ms_per_step * 1e3,
+        us_per_batch_median=statistics.median(ms) * 1e3,
+        us_per_batch_p10_p90=[float(np.percentile(ms, 10) * 1e3), float(np.percentile(ms, 90) * 1e3)],
+        higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f32",
+        data="synthetic: seeded SplitMix64 inputs of the workload's shapes and distributions",
+        config=dict(workload=cfg.name, global_batch=cfg.batch * world, batch_per_gpu=cfg.batch,
+                    tables=cfg.n_tables, rows=cfg.rows[0], emb_dim=cfg.emb_dim,
+                    bag_size=cfg.bag_size, ln_bot=list(cfg.ln_bot), ln_top=list(cfg.ln_top),
+                    math="fp32", l2="flushed before every step (256 MB write)",
+                    parallelism="replicas" if world > 1 else "single GPU"),
+        e2e=e2e, gpu_launches=args.steps * n_stages, clocks=clock_info,
+        roofline=roof, forward_roofline=forward_roofline, stages_us=stage_us,
+        graph=dict(us_per_batch_median=graph_us, samples_per_s=cfg.batch / (graph_us * 1e-6)),
+        cpu_baseline=cpu)
+    line["gather_b65536_k26_zipf"] = gather
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    return run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

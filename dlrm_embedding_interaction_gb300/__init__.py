@@ -1,0 +1,342 @@
+"""Python binding of libdlrm_gb300.so, the GB300 DLRMv1 inference forward.
+
+Argument marshalling only: every step of the forward runs in the library's
+CUDA kernels (include/dlrm.h documents each entry point). PyTorch supplies
+device memory and streams. There is no CPU or PyTorch fallback: if the
+library is missing, loading it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdlrm_gb300.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_OOM, ERR_INDEX_OOB, ERR_TIMEOUT = range(7)
+MATH_FP32, MATH_TF32, MATH_BF16 = 0, 1, 2
+ACT_NONE, ACT_RELU, ACT_SIGMOID = 0, 1, 2
+ERRBIT_INDEX_OOB = 1 << ERR_INDEX_OOB
+ERRBIT_OFFSETS = 1 << ERR_UNSUPPORTED
+MAX_TABLES = 128
+MAX_LAYERS = 16
+
+# Every symbol include/dlrm.h declares.
+EXPORTS = ("dlrm_version", "dlrm_status_string", "dlrm_create", "dlrm_forward",
+           "dlrm_forward_host", "dlrm_get_error", "dlrm_workspace_bytes", "dlrm_destroy",
+           "dlrm_num_stages", "dlrm_stage_name", "dlrm_set_profiling", "dlrm_stage_times",
+           "embedding_bag_sum_multi", "pairwise_dot_lower_tri", "pairwise_pair_map",
+           "linear_bias_act")
+
+_lib = None
+
+
+class DlrmError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        msg = _status_string(status)
+        super().__init__(f"{where}: status {status} ({msg})")
+        self.status = status
+
+
+class _Config(ctypes.Structure):
+    _fields_ = [("n_bot", ctypes.c_int32), ("ln_bot", ctypes.POINTER(ctypes.c_int32)),
+                ("n_tables", ctypes.c_int32), ("rows", ctypes.POINTER(ctypes.c_int64)),
+                ("emb_dim", ctypes.c_int32), ("n_top", ctypes.c_int32),
+                ("ln_top", ctypes.POINTER(ctypes.c_int32)), ("bag_size", ctypes.c_int32),
+                ("max_batch", ctypes.c_int32), ("math", ctypes.c_int)]
+
+
+def _bind(lib):
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    st = ctypes.c_int
+    sig = {
+        "dlrm_version": ([], i32),
+        "dlrm_status_string": ([i32], ctypes.c_char_p),
+        "dlrm_create": ([ctypes.POINTER(_Config), vp, vp, vp, vp, vp, ctypes.POINTER(vp)], st),
+        "dlrm_forward": ([vp, vp, vp, vp, vp, i32, vp], st),
+        "dlrm_forward_host": ([vp, vp, vp, vp, vp, i32, vp], st),
+        "dlrm_get_error": ([vp, vp], st),
+        "dlrm_workspace_bytes": ([vp], i64),
+        "dlrm_destroy": ([vp], None),
+        "dlrm_num_stages": ([vp], i32),
+        "dlrm_stage_name": ([vp, i32], ctypes.c_char_p),
+        "dlrm_set_profiling": ([vp, i32], st),
+        "dlrm_stage_times": ([vp, ctypes.c_void_p, i32, ctypes.POINTER(i64)], i32),
+        "embedding_bag_sum_multi": ([vp, vp, i32, i32, vp, vp, i32, i32, vp, vp, vp], st),
+        "pairwise_dot_lower_tri": ([vp, i32, vp, i32, i32, i32, vp, i32, i32, vp], st),
+        "pairwise_pair_map": ([i32, vp, vp, vp], st),
+        "linear_bias_act": ([vp, i32, vp, vp, vp, i32, i32, i32, i32, st, st, vp], st),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    return lib
+
+
+def lib():
+    """The loaded library. Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with `python -m "
+                "dlrm_embedding_interaction_gb300.build` (nvcc, sm_103a). "
+                "There is no fallback path.")
+        _lib = _bind(ctypes.CDLL(LIB_PATH))
+    return _lib
+
+
+def _status_string(status: int) -> str:
+    try:
+        return lib().dlrm_status_string(status).decode()
+    except Exception:  # pragma: no cover - library not loadable
+        return "?"
+
+
+def _check(status: int, where: str) -> None:
+    if status != OK:
+        raise DlrmError(status, where)
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _ptr(t) -> ctypes.c_void_p:
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _need(t, dtype, name, cuda=True):
+    import torch
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if cuda and not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor")
+
+
+def _row_stride(t, name) -> int:
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError(f"{name}: expected a 2-D tensor with unit column stride")
+    return t.stride(0)
+
+
+def version() -> int:
+    return int(lib().dlrm_version())
+
+
+# ---------------------------------------------------------------- standalone ops
+
+def embedding_bag_sum_multi(tables: Sequence, indices, offsets, out, bag_size: int,
+                            err_flag=None, stream=None) -> None:
+    """out (B, K, D) = per-table bag sums; indices (K, B*L), offsets (K, B) int64."""
+    import torch
+    k = len(tables)
+    if k == 0:
+        raise ValueError("need at least one table")
+    d = tables[0].shape[1]
+    for i, t in enumerate(tables):
+        _need(t, torch.float32, f"tables[{i}]")
+        if t.dim() != 2 or t.shape[1] != d or not t.is_contiguous():
+            raise ValueError(f"tables[{i}]: expected contiguous (rows, {d})")
+    _need(indices, torch.int64, "indices")
+    _need(offsets, torch.int64, "offsets")
+    _need(out, torch.float32, "out")
+    b = offsets.shape[1]
+    if (tuple(indices.shape) != (k, b * bag_size) or tuple(offsets.shape) != (k, b)
+            or tuple(out.shape) != (b, k, d)):
+        raise ValueError("shape mismatch among indices/offsets/out")
+    if not (indices.is_contiguous() and offsets.is_contiguous() and out.is_contiguous()):
+        raise ValueError("indices, offsets and out must be contiguous")
+    if err_flag is not None:
+        _need(err_flag, torch.int32, "err_flag")
+    ptrs = (ctypes.c_void_p * k)(*[t.data_ptr() for t in tables])
+    rows = (ctypes.c_int64 * k)(*[t.shape[0] for t in tables])
+    _check(lib().embedding_bag_sum_multi(ptrs, rows, k, d, _ptr(indices), _ptr(offsets), b,
+                                         bag_size, _ptr(out), _ptr(err_flag), _stream(stream)),
+           "embedding_bag_sum_multi")
+
+
+def pairwise_dot_lower_tri(dense, emb, out, copy_dense: bool = True, stream=None) -> None:
+    """out[b] = [dense[b], z[b]] (copy_dense) or z[b]; dense (B, D), emb (B, K, D)."""
+    import torch
+    _need(dense, torch.float32, "dense")
+    _need(emb, torch.float32, "emb")
+    _need(out, torch.float32, "out")
+    b, d = dense.shape
+    if emb.dim() != 3 or emb.shape[0] != b or emb.shape[2] != d or not emb.is_contiguous():
+        raise ValueError("emb: expected contiguous (B, K, D)")
+    k = emb.shape[1]
+    ld_dense = _row_stride(dense, "dense")
+    ld_out = _row_stride(out, "out")
+    if out.shape[0] != b:
+        raise ValueError("out: batch mismatch")
+    _check(lib().pairwise_dot_lower_tri(_ptr(dense), ld_dense, _ptr(emb), b, k, d, _ptr(out),
+                                        ld_out, 1 if copy_dense else 0, _stream(stream)),
+           "pairwise_dot_lower_tri")
+
+
+def pairwise_pair_map(f: int, i_out, j_out, stream=None) -> None:
+    import torch
+    _need(i_out, torch.int32, "i_out")
+    _need(j_out, torch.int32, "j_out")
+    p = f * (f - 1) // 2
+    if i_out.numel() < p or j_out.numel() < p:
+        raise ValueError("i_out/j_out too small")
+    _check(lib().pairwise_pair_map(f, _ptr(i_out), _ptr(j_out), _stream(stream)),
+           "pairwise_pair_map")
+
+
+def linear_bias_act(x, w, bias, y, act: int = ACT_NONE, math: int = MATH_FP32,
+                    stream=None) -> None:
+    """y = act(x W^T + bias); x (M, K), W (N, K) contiguous, y (M, N)."""
+    import torch
+    _need(x, torch.float32, "x")
+    _need(w, torch.float32, "W")
+    _need(y, torch.float32, "y")
+    if bias is not None:
+        _need(bias, torch.float32, "bias")
+    m, k = x.shape
+    n = w.shape[0]
+    if w.dim() != 2 or w.shape[1] != k or not w.is_contiguous():
+        raise ValueError("W: expected contiguous (N, K)")
+    if y.shape[0] != m or y.shape[1] != n:
+        raise ValueError("y: expected (M, N)")
+    _check(lib().linear_bias_act(_ptr(x), _row_stride(x, "x"), _ptr(w), _ptr(bias), _ptr(y),
+                                 _row_stride(y, "y"), m, n, k, act, math, _stream(stream)),
+           "linear_bias_act")
+
+
+# ---------------------------------------------------------------- forward plan
+
+def dlrm_create(ln_bot: Sequence[int], ln_top: Sequence[int], tables: Sequence,
+                bot_w: Sequence, bot_b: Sequence, top_w: Sequence, top_b: Sequence,
+                bag_size: int, max_batch: int, math: int = MATH_FP32) -> int:
+    """Build a forward plan; returns the opaque handle (an int).
+
+    ``tables`` are CUDA tensors the handle borrows (keep them alive); the MLP
+    parameters may be CPU or CUDA float32 tensors and are copied.
+    """
+    k = len(tables)
+    d = int(tables[0].shape[1])
+    lb = (ctypes.c_int32 * len(ln_bot))(*ln_bot)
+    lt = (ctypes.c_int32 * len(ln_top))(*ln_top)
+    rows = (ctypes.c_int64 * k)(*[int(t.shape[0]) for t in tables])
+    cfg = _Config(len(ln_bot) - 1, lb, k, rows, d, len(ln_top) - 1, lt, bag_size, max_batch,
+                  math)
+
+    def arr(ts):
+        for t in ts:
+            if not t.is_contiguous():
+                raise ValueError("parameters must be contiguous")
+        return (ctypes.c_void_p * len(ts))(*[t.data_ptr() for t in ts])
+
+    h = ctypes.c_void_p()
+    _check(lib().dlrm_create(ctypes.byref(cfg), arr(tables), arr(bot_w), arr(bot_b),
+                             arr(top_w), arr(top_b), ctypes.byref(h)), "dlrm_create")
+    return h.value
+
+
+def dlrm_forward(h: int, dense, indices, offsets, out, stream=None) -> None:
+    batch = dense.shape[0]
+    _check(lib().dlrm_forward(ctypes.c_void_p(h), _ptr(dense), _ptr(indices), _ptr(offsets),
+                              _ptr(out), batch, _stream(stream)), "dlrm_forward")
+
+
+def dlrm_forward_host(h: int, dense, indices, offsets, out, stream=None) -> None:
+    """Host-buffer forward (pinned CPU tensors); asynchronous on ``stream``."""
+    batch = dense.shape[0]
+    _check(lib().dlrm_forward_host(ctypes.c_void_p(h), _ptr(dense), _ptr(indices),
+                                   _ptr(offsets), _ptr(out), batch, _stream(stream)),
+           "dlrm_forward_host")
+
+
+def dlrm_get_error(h: int, stream=None) -> int:
+    return int(lib().dlrm_get_error(ctypes.c_void_p(h), _stream(stream)))
+
+
+def dlrm_workspace_bytes(h: int) -> int:
+    return int(lib().dlrm_workspace_bytes(ctypes.c_void_p(h)))
+
+
+def dlrm_num_stages(h: int) -> int:
+    return int(lib().dlrm_num_stages(ctypes.c_void_p(h)))
+
+
+def dlrm_stage_name(h: int, i: int) -> str:
+    name = lib().dlrm_stage_name(ctypes.c_void_p(h), i)
+    return name.decode() if name is not None else ""
+
+
+def dlrm_set_profiling(h: int, enable: bool) -> None:
+    _check(lib().dlrm_set_profiling(ctypes.c_void_p(h), 1 if enable else 0),
+           "dlrm_set_profiling")
+
+
+def dlrm_stage_times(h: int):
+    """(names, total_ms per stage, profiled calls)."""
+    n = dlrm_num_stages(h)
+    buf = (ctypes.c_double * max(n, 1))()
+    calls = ctypes.c_int64()
+    lib().dlrm_stage_times(ctypes.c_void_p(h), buf, n, ctypes.byref(calls))
+    return [dlrm_stage_name(h, i) for i in range(n)], list(buf)[:n], calls.value
+
+
+def dlrm_destroy(h: Optional[int]) -> None:
+    if h:
+        lib().dlrm_destroy(ctypes.c_void_p(h))
+
+
+class DlrmModel:
+    """Owns a forward plan and keeps the borrowed tables alive."""
+
+    def __init__(self, ln_bot, ln_top, tables, bot_w, bot_b, top_w, top_b, bag_size: int,
+                 max_batch: int, math: int = MATH_FP32):
+        self.tables = list(tables)
+        self.ln_bot, self.ln_top = tuple(ln_bot), tuple(ln_top)
+        self.bag_size, self.max_batch, self.math = bag_size, max_batch, math
+        self.handle = dlrm_create(ln_bot, ln_top, self.tables, bot_w, bot_b, top_w, top_b,
+                                  bag_size, max_batch, math)
+
+    def forward(self, dense, indices, offsets, out=None, stream=None):
+        import torch
+        if out is None:
+            out = torch.empty(dense.shape[0], dtype=torch.float32, device=dense.device)
+        dlrm_forward(self.handle, dense, indices, offsets, out, stream)
+        return out
+
+    def forward_host(self, dense, indices, offsets, out, stream=None):
+        dlrm_forward_host(self.handle, dense, indices, offsets, out, stream)
+        return out
+
+    def error(self, stream=None) -> int:
+        return dlrm_get_error(self.handle, stream)
+
+    def workspace_bytes(self) -> int:
+        return dlrm_workspace_bytes(self.handle)
+
+    def stage_names(self):
+        return [dlrm_stage_name(self.handle, i) for i in range(dlrm_num_stages(self.handle))]
+
+    def set_profiling(self, enable: bool) -> None:
+        dlrm_set_profiling(self.handle, enable)
+
+    def stage_times(self):
+        return dlrm_stage_times(self.handle)
+
+    def close(self):
+        if self.handle:
+            dlrm_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,481 @@
+// C ABI of libdlrm_gb300.so (declared in include/dlrm.h): argument checks,
+// the forward plan (handle), its workspace, and the launch sequence.
+//
+// The forward follows Luminal compare dlrm-fused-kernels...dlrm-pt2-megakernel,
+// dlrm_megakernel.rs steps 1-6 (bottom MLP with ReLU after every layer,
+// lookups, i-major pairwise dots with Vec[0] = x, R = [x, z], top MLP with ReLU
+// then a final sigmoid), with the shape checks of its validate(). All device
+// memory of a handle is one arena allocated in dlrm_create; forward calls
+// allocate nothing and never synchronise.
+#include <algorithm>
+#include <atomic>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+
+namespace dlrm {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+std::atomic<int> g_smem_optin[kMaxDevices];
+
+int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  return dev;
+}
+
+}  // namespace
+
+int device_sm_count() {
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return 148;
+  int v = g_sm_count[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+      v = 148;
+    g_sm_count[dev].store(v, std::memory_order_relaxed);
+  }
+  return v;
+}
+
+size_t device_max_smem_optin() {
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return 48 * 1024;
+  int v = g_smem_optin[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+        v <= 0)
+      v = 48 * 1024;
+    g_smem_optin[dev].store(v, std::memory_order_relaxed);
+  }
+  return static_cast<size_t>(v);
+}
+
+}  // namespace dlrm
+
+using dlrm::round_up;
+
+struct dlrm_handle_s {
+  int device = 0;
+  int n_bot = 0, n_top = 0, k = 0, d = 0, bag = 0, max_batch = 0, n_dense = 0;
+  dlrm_math_t math = DLRM_MATH_FP32;
+  std::vector<int> ln_bot, ln_top;
+  dlrm::GatherTables tabs{};
+  // packed parameters: W as (N, ldw = round_up(K, 4)) zero-padded, bias (N)
+  std::vector<float*> bot_w, bot_b, top_w, top_b;
+  std::vector<int> bot_ldw, top_ldw;
+  // workspace
+  float* emb = nullptr;          // (max_batch, K, D)
+  float* act[2] = {nullptr, nullptr};
+  int ld_act = 0;                // widest hidden width, rounded to 4
+  float* r = nullptr;            // (max_batch, ld_r), R = [x, z]
+  int ld_r = 0;
+  int32_t* err = nullptr;        // device error word
+  // staging for dlrm_forward_host
+  float* dense_stage = nullptr;
+  int64_t* idx_stage = nullptr;
+  int64_t* off_stage = nullptr;
+  float* out_stage = nullptr;
+  void* arena = nullptr;
+  size_t arena_bytes = 0;
+  // per-stage profiling (dlrm_set_profiling)
+  std::vector<std::string> stage_names;
+  std::vector<cudaEvent_t> events;      // stage boundaries, empty when off
+  std::vector<double> stage_ms;
+  int64_t profiled_calls = 0;
+};
+
+namespace {
+
+dlrm_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? DLRM_OK : DLRM_ERR_CUDA; }
+
+// Bump allocator over one cudaMalloc'd arena; 256-byte aligned slices.
+struct ArenaPlan {
+  size_t bytes = 0;
+  template <class T>
+  size_t take(size_t count) {
+    const size_t off = bytes;
+    bytes = static_cast<size_t>(round_up(static_cast<int64_t>(off + count * sizeof(T)), 256));
+    return off;
+  }
+};
+
+bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + nb && b0 < a0 + na;
+}
+
+dlrm_status_t run_forward(dlrm_handle_t h, const float* dense, const int64_t* indices,
+                          const int64_t* offsets, float* out, int batch, cudaStream_t s) {
+  cudaError_t e;
+  const bool prof = !h->events.empty();
+  int stage = 0;
+  auto mark = [&]() -> bool {
+    return !prof || cudaEventRecord(h->events[stage++], s) == cudaSuccess;
+  };
+  if (!mark()) return DLRM_ERR_CUDA;
+  // [G] bag sums, all tables in one launch
+  e = dlrm::launch_gather(h->tabs, h->k, h->d, indices, offsets, batch, h->bag, h->emb, h->d,
+                          h->err, s);
+  if (e != cudaSuccess || !mark()) return DLRM_ERR_CUDA;
+  // [M1] bottom MLP, ReLU after every layer
+  const float* in = dense;
+  int ld_in = h->n_dense;
+  for (int l = 0; l < h->n_bot; ++l) {
+    float* o = h->act[l & 1];
+    e = dlrm::launch_linear_fp32(in, ld_in, h->bot_w[l], h->bot_ldw[l], h->bot_b[l], o, h->ld_act,
+                                 batch, h->ln_bot[l + 1], h->ln_bot[l], DLRM_ACT_RELU, s);
+    if (e != cudaSuccess || !mark()) return DLRM_ERR_CUDA;
+    in = o;
+    ld_in = h->ld_act;
+  }
+  // [I] interaction; R = [x, z]
+  e = dlrm::launch_interaction(in, ld_in, h->emb, batch, h->k, h->d, h->r, h->ld_r, 1, s);
+  if (e != cudaSuccess || !mark()) return DLRM_ERR_CUDA;
+  // [M2] top MLP: ReLU, ..., sigmoid into out
+  in = h->r;
+  ld_in = h->ld_r;
+  for (int l = 0; l < h->n_top; ++l) {
+    const bool last = (l == h->n_top - 1);
+    float* o = last ? out : h->act[l & 1];
+    const int ld_o = last ? 1 : h->ld_act;
+    e = dlrm::launch_linear_fp32(in, ld_in, h->top_w[l], h->top_ldw[l], h->top_b[l], o, ld_o,
+                                 batch, h->ln_top[l + 1], h->ln_top[l],
+                                 last ? DLRM_ACT_SIGMOID : DLRM_ACT_RELU, s);
+    if (e != cudaSuccess || !mark()) return DLRM_ERR_CUDA;
+    in = o;
+    ld_in = ld_o;
+  }
+  if (prof) {
+    if (cudaEventSynchronize(h->events.back()) != cudaSuccess) return DLRM_ERR_CUDA;
+    for (size_t i = 0; i + 1 < h->events.size(); ++i) {
+      float ms = 0.f;
+      if (cudaEventElapsedTime(&ms, h->events[i], h->events[i + 1]) != cudaSuccess)
+        return DLRM_ERR_CUDA;
+      h->stage_ms[i] += ms;
+    }
+    ++h->profiled_calls;
+  }
+  return DLRM_OK;
+}
+
+void destroy_events(dlrm_handle_t h) {
+  for (cudaEvent_t ev : h->events) cudaEventDestroy(ev);
+  h->events.clear();
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t dlrm_version(void) { return 100; }
+
+const char* dlrm_status_string(int32_t status) {
+  switch (status) {
+    case DLRM_OK: return "ok";
+    case DLRM_ERR_INVALID_ARG: return "invalid argument";
+    case DLRM_ERR_UNSUPPORTED: return "unsupported";
+    case DLRM_ERR_CUDA: return "CUDA error";
+    case DLRM_ERR_OOM: return "out of device memory";
+    case DLRM_ERR_INDEX_OOB: return "index out of range";
+    case DLRM_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+dlrm_status_t dlrm_create(const dlrm_config_t* cfg, const float* const* tables,
+                          const float* const* bot_w, const float* const* bot_b,
+                          const float* const* top_w, const float* const* top_b,
+                          dlrm_handle_t* out) {
+  if (!out) return DLRM_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!cfg || !tables || !bot_w || !bot_b || !top_w || !top_b) return DLRM_ERR_INVALID_ARG;
+  if (!cfg->ln_bot || !cfg->ln_top || !cfg->rows) return DLRM_ERR_INVALID_ARG;
+  // validate(): at least one layer each side, widths chain, ln_bot.last() = m_spa,
+  // ln_top[0] = m_spa + n_pairs, ln_top.last() = 1, batch > 0.
+  if (cfg->n_bot < 1 || cfg->n_top < 1) return DLRM_ERR_INVALID_ARG;
+  if (cfg->n_bot > DLRM_MAX_LAYERS || cfg->n_top > DLRM_MAX_LAYERS) return DLRM_ERR_UNSUPPORTED;
+  if (cfg->n_tables < 1 || cfg->emb_dim < 1 || cfg->bag_size < 1 || cfg->max_batch < 1)
+    return DLRM_ERR_INVALID_ARG;
+  if (cfg->n_tables > DLRM_MAX_TABLES) return DLRM_ERR_UNSUPPORTED;
+  for (int l = 0; l <= cfg->n_bot; ++l) if (cfg->ln_bot[l] < 1) return DLRM_ERR_INVALID_ARG;
+  for (int l = 0; l <= cfg->n_top; ++l) if (cfg->ln_top[l] < 1) return DLRM_ERR_INVALID_ARG;
+  const int64_t f = cfg->n_tables + 1;
+  const int64_t p = f * (f - 1) / 2;
+  if (cfg->ln_bot[cfg->n_bot] != cfg->emb_dim) return DLRM_ERR_INVALID_ARG;
+  if (cfg->ln_top[0] != cfg->emb_dim + p) return DLRM_ERR_INVALID_ARG;
+  if (cfg->ln_top[cfg->n_top] != 1) return DLRM_ERR_INVALID_ARG;
+  for (int t = 0; t < cfg->n_tables; ++t)
+    if (!tables[t] || cfg->rows[t] < 1) return DLRM_ERR_INVALID_ARG;
+  for (int l = 0; l < cfg->n_bot; ++l) if (!bot_w[l] || !bot_b[l]) return DLRM_ERR_INVALID_ARG;
+  for (int l = 0; l < cfg->n_top; ++l) if (!top_w[l] || !top_b[l]) return DLRM_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(cfg->max_batch) * cfg->bag_size > (int64_t(1) << 31))
+    return DLRM_ERR_UNSUPPORTED;
+  if (cfg->math != DLRM_MATH_FP32) return DLRM_ERR_UNSUPPORTED;
+  if (dlrm::interaction_smem_per_sample(cfg->n_tables, cfg->emb_dim) >
+      dlrm::device_max_smem_optin())
+    return DLRM_ERR_UNSUPPORTED;
+
+  dlrm_handle_t h = new (std::nothrow) dlrm_handle_s();
+  if (!h) return DLRM_ERR_OOM;
+  cudaGetDevice(&h->device);
+  h->n_bot = cfg->n_bot;
+  h->n_top = cfg->n_top;
+  h->k = cfg->n_tables;
+  h->d = cfg->emb_dim;
+  h->bag = cfg->bag_size;
+  h->max_batch = cfg->max_batch;
+  h->n_dense = cfg->ln_bot[0];
+  h->math = cfg->math;
+  h->ln_bot.assign(cfg->ln_bot, cfg->ln_bot + cfg->n_bot + 1);
+  h->ln_top.assign(cfg->ln_top, cfg->ln_top + cfg->n_top + 1);
+  for (int t = 0; t < h->k; ++t) {
+    h->tabs.ptr[t] = tables[t];
+    h->tabs.rows[t] = cfg->rows[t];
+  }
+  h->stage_names.push_back("gather");
+  for (int l = 0; l < h->n_bot; ++l) h->stage_names.push_back("bottom" + std::to_string(l));
+  h->stage_names.push_back("interaction");
+  for (int l = 0; l < h->n_top; ++l) h->stage_names.push_back("top" + std::to_string(l));
+  h->stage_ms.assign(h->stage_names.size(), 0.0);
+
+  // Layout of the arena.
+  int widest = 4;
+  for (int l = 1; l <= h->n_bot; ++l) widest = std::max(widest, h->ln_bot[l]);
+  for (int l = 1; l < h->n_top; ++l) widest = std::max(widest, h->ln_top[l]);
+  h->ld_act = static_cast<int>(round_up(widest, 4));
+  h->ld_r = static_cast<int>(round_up(h->ln_top[0], 4));
+  const size_t mb = static_cast<size_t>(h->max_batch);
+  ArenaPlan plan;
+  std::vector<size_t> off_bw(h->n_bot), off_bb(h->n_bot), off_tw(h->n_top), off_tb(h->n_top);
+  h->bot_ldw.resize(h->n_bot);
+  h->top_ldw.resize(h->n_top);
+  for (int l = 0; l < h->n_bot; ++l) {
+    h->bot_ldw[l] = static_cast<int>(round_up(h->ln_bot[l], 4));
+    off_bw[l] = plan.take<float>(static_cast<size_t>(h->ln_bot[l + 1]) * h->bot_ldw[l]);
+    off_bb[l] = plan.take<float>(h->ln_bot[l + 1]);
+  }
+  for (int l = 0; l < h->n_top; ++l) {
+    h->top_ldw[l] = static_cast<int>(round_up(h->ln_top[l], 4));
+    off_tw[l] = plan.take<float>(static_cast<size_t>(h->ln_top[l + 1]) * h->top_ldw[l]);
+    off_tb[l] = plan.take<float>(h->ln_top[l + 1]);
+  }
+  const size_t off_emb = plan.take<float>(mb * h->k * h->d);
+  const size_t off_a0 = plan.take<float>(mb * h->ld_act);
+  const size_t off_a1 = plan.take<float>(mb * h->ld_act);
+  const size_t off_r = plan.take<float>(mb * h->ld_r);
+  const size_t off_err = plan.take<int32_t>(4);
+  const size_t off_dense = plan.take<float>(mb * h->n_dense);
+  const size_t off_idx = plan.take<int64_t>(mb * h->k * h->bag);
+  const size_t off_off = plan.take<int64_t>(mb * h->k);
+  const size_t off_out = plan.take<float>(mb);
+
+  if (cudaMalloc(&h->arena, plan.bytes) != cudaSuccess) {
+    cudaGetLastError();
+    delete h;
+    return DLRM_ERR_OOM;
+  }
+  h->arena_bytes = plan.bytes;
+  char* base = static_cast<char*>(h->arena);
+  auto at = [&](size_t off) { return reinterpret_cast<float*>(base + off); };
+  dlrm_status_t st = cuda_status(cudaMemset(h->arena, 0, plan.bytes));
+  for (int l = 0; l < h->n_bot && st == DLRM_OK; ++l) {
+    h->bot_w.push_back(at(off_bw[l]));
+    h->bot_b.push_back(at(off_bb[l]));
+    st = cuda_status(cudaMemcpy2D(at(off_bw[l]), h->bot_ldw[l] * sizeof(float), bot_w[l],
+                                  h->ln_bot[l] * sizeof(float), h->ln_bot[l] * sizeof(float),
+                                  h->ln_bot[l + 1], cudaMemcpyDefault));
+    if (st == DLRM_OK)
+      st = cuda_status(cudaMemcpy(at(off_bb[l]), bot_b[l], h->ln_bot[l + 1] * sizeof(float),
+                                  cudaMemcpyDefault));
+  }
+  for (int l = 0; l < h->n_top && st == DLRM_OK; ++l) {
+    h->top_w.push_back(at(off_tw[l]));
+    h->top_b.push_back(at(off_tb[l]));
+    st = cuda_status(cudaMemcpy2D(at(off_tw[l]), h->top_ldw[l] * sizeof(float), top_w[l],
+                                  h->ln_top[l] * sizeof(float), h->ln_top[l] * sizeof(float),
+                                  h->ln_top[l + 1], cudaMemcpyDefault));
+    if (st == DLRM_OK)
+      st = cuda_status(cudaMemcpy(at(off_tb[l]), top_b[l], h->ln_top[l + 1] * sizeof(float),
+                                  cudaMemcpyDefault));
+  }
+  if (st == DLRM_OK) st = cuda_status(cudaDeviceSynchronize());
+  if (st != DLRM_OK) {
+    cudaGetLastError();
+    cudaFree(h->arena);
+    delete h;
+    return st;
+  }
+  h->emb = at(off_emb);
+  h->act[0] = at(off_a0);
+  h->act[1] = at(off_a1);
+  h->r = at(off_r);
+  h->err = reinterpret_cast<int32_t*>(base + off_err);
+  h->dense_stage = at(off_dense);
+  h->idx_stage = reinterpret_cast<int64_t*>(base + off_idx);
+  h->off_stage = reinterpret_cast<int64_t*>(base + off_off);
+  h->out_stage = at(off_out);
+  *out = h;
+  return DLRM_OK;
+}
+
+dlrm_status_t dlrm_forward(dlrm_handle_t h, const float* dense, const int64_t* indices,
+                           const int64_t* offsets, float* out, int32_t batch, void* stream) {
+  if (!h || !dense || !indices || !offsets || !out) return DLRM_ERR_INVALID_ARG;
+  if (batch < 1 || batch > h->max_batch) return DLRM_ERR_INVALID_ARG;
+  return run_forward(h, dense, indices, offsets, out, batch, static_cast<cudaStream_t>(stream));
+}
+
+dlrm_status_t dlrm_forward_host(dlrm_handle_t h, const float* dense_host,
+                                const int64_t* indices_host, const int64_t* offsets_host,
+                                float* out_host, int32_t batch, void* stream) {
+  if (!h || !dense_host || !indices_host || !offsets_host || !out_host)
+    return DLRM_ERR_INVALID_ARG;
+  if (batch < 1 || batch > h->max_batch) return DLRM_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t nb = static_cast<size_t>(batch);
+  if (cudaMemcpyAsync(h->dense_stage, dense_host, nb * h->n_dense * sizeof(float),
+                      cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(h->idx_stage, indices_host, nb * h->k * h->bag * sizeof(int64_t),
+                      cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(h->off_stage, offsets_host, nb * h->k * sizeof(int64_t),
+                      cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return DLRM_ERR_CUDA;
+  dlrm_status_t st = run_forward(h, h->dense_stage, h->idx_stage, h->off_stage, h->out_stage,
+                                 batch, s);
+  if (st != DLRM_OK) return st;
+  return cuda_status(cudaMemcpyAsync(out_host, h->out_stage, nb * sizeof(float),
+                                     cudaMemcpyDeviceToHost, s));
+}
+
+dlrm_status_t dlrm_get_error(dlrm_handle_t h, void* stream) {
+  if (!h) return DLRM_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DLRM_ERR_CUDA;
+  int32_t word = 0;
+  if (cudaMemcpy(&word, h->err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return DLRM_ERR_CUDA;
+  if (word != 0 && cudaMemset(h->err, 0, sizeof(int32_t)) != cudaSuccess) return DLRM_ERR_CUDA;
+  const uint32_t bits = static_cast<uint32_t>(word);
+  if (bits & DLRM_ERRBIT_INDEX_OOB) return DLRM_ERR_INDEX_OOB;
+  if (bits & DLRM_ERRBIT_OFFSETS) return DLRM_ERR_UNSUPPORTED;
+  if (bits & DLRM_ERRBIT_TIMEOUT) return DLRM_ERR_TIMEOUT;
+  return DLRM_OK;
+}
+
+int64_t dlrm_workspace_bytes(dlrm_handle_t h) {
+  return h ? static_cast<int64_t>(h->arena_bytes) : 0;
+}
+
+int32_t dlrm_num_stages(dlrm_handle_t h) {
+  return h ? static_cast<int32_t>(h->stage_names.size()) : 0;
+}
+
+const char* dlrm_stage_name(dlrm_handle_t h, int32_t i) {
+  if (!h || i < 0 || i >= static_cast<int32_t>(h->stage_names.size())) return nullptr;
+  return h->stage_names[i].c_str();
+}
+
+dlrm_status_t dlrm_set_profiling(dlrm_handle_t h, int32_t enable) {
+  if (!h) return DLRM_ERR_INVALID_ARG;
+  destroy_events(h);
+  h->stage_ms.assign(h->stage_names.size(), 0.0);
+  h->profiled_calls = 0;
+  if (!enable) return DLRM_OK;
+  for (size_t i = 0; i <= h->stage_names.size(); ++i) {
+    cudaEvent_t ev;
+    if (cudaEventCreate(&ev) != cudaSuccess) {
+      destroy_events(h);
+      return DLRM_ERR_CUDA;
+    }
+    h->events.push_back(ev);
+  }
+  return DLRM_OK;
+}
+
+int32_t dlrm_stage_times(dlrm_handle_t h, double* total_ms, int32_t capacity, int64_t* calls) {
+  if (!h) return -1;
+  const int32_t n = static_cast<int32_t>(h->stage_names.size());
+  for (int32_t i = 0; i < n && i < capacity && total_ms; ++i) total_ms[i] = h->stage_ms[i];
+  if (calls) *calls = h->profiled_calls;
+  return n;
+}
+
+void dlrm_destroy(dlrm_handle_t h) {
+  if (!h) return;
+  cudaDeviceSynchronize();
+  destroy_events(h);
+  if (h->arena) cudaFree(h->arena);
+  delete h;
+}
+
+dlrm_status_t embedding_bag_sum_multi(const float* const* tables, const int64_t* rows,
+                                      int32_t K, int32_t D, const int64_t* indices,
+                                      const int64_t* offsets, int32_t B, int32_t L, float* out,
+                                      int32_t* err_flag, void* stream) {
+  if (K < 1 || D < 1 || L < 1 || B < 0) return DLRM_ERR_INVALID_ARG;
+  if (K > DLRM_MAX_TABLES) return DLRM_ERR_UNSUPPORTED;
+  if (!tables || !rows) return DLRM_ERR_INVALID_ARG;
+  if (B == 0) return DLRM_OK;
+  if (!indices || !offsets || !out) return DLRM_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(B) * L > (int64_t(1) << 31)) return DLRM_ERR_UNSUPPORTED;
+  dlrm::GatherTables tabs{};
+  for (int t = 0; t < K; ++t) {
+    if (!tables[t] || rows[t] < 0) return DLRM_ERR_INVALID_ARG;
+    tabs.ptr[t] = tables[t];
+    tabs.rows[t] = rows[t];
+  }
+  return cuda_status(dlrm::launch_gather(tabs, K, D, indices, offsets, B, L, out, D, err_flag,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+dlrm_status_t pairwise_dot_lower_tri(const float* dense, int32_t ld_dense, const float* emb,
+                                     int32_t B, int32_t K, int32_t D, float* out,
+                                     int32_t ld_out, int32_t copy_dense, void* stream) {
+  if (B < 0 || K < 0 || D < 1 || ld_dense < D) return DLRM_ERR_INVALID_ARG;
+  const int64_t f = static_cast<int64_t>(K) + 1;
+  const int64_t p = f * (f - 1) / 2;
+  if (ld_out < (copy_dense ? D : 0) + p) return DLRM_ERR_INVALID_ARG;
+  if (B == 0) return DLRM_OK;
+  if (!dense || !out || (K > 0 && !emb)) return DLRM_ERR_INVALID_ARG;
+  if (p > (int64_t(1) << 30)) return DLRM_ERR_UNSUPPORTED;
+  if (dlrm::interaction_smem_per_sample(K, D) > dlrm::device_max_smem_optin())
+    return DLRM_ERR_UNSUPPORTED;
+  return cuda_status(dlrm::launch_interaction(dense, ld_dense, emb, B, K, D, out, ld_out,
+                                              copy_dense ? 1 : 0,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
+dlrm_status_t pairwise_pair_map(int32_t F, int32_t* i_out, int32_t* j_out, void* stream) {
+  if (F < 2 || F > 46341 || !i_out || !j_out) return DLRM_ERR_INVALID_ARG;
+  return cuda_status(dlrm::launch_pair_map(F, i_out, j_out, static_cast<cudaStream_t>(stream)));
+}
+
+dlrm_status_t linear_bias_act(const float* x, int32_t ld_x, const float* W, const float* bias,
+                              float* y, int32_t ld_y, int32_t M, int32_t N, int32_t K,
+                              dlrm_act_t act, dlrm_math_t math, void* stream) {
+  if (M < 0 || N < 1 || K < 1 || ld_x < K || ld_y < N) return DLRM_ERR_INVALID_ARG;
+  if (act != DLRM_ACT_NONE && act != DLRM_ACT_RELU && act != DLRM_ACT_SIGMOID)
+    return DLRM_ERR_INVALID_ARG;
+  if (math != DLRM_MATH_FP32 && math != DLRM_MATH_TF32 && math != DLRM_MATH_BF16)
+    return DLRM_ERR_INVALID_ARG;
+  if (M == 0) return DLRM_OK;
+  if (!x || !W || !y) return DLRM_ERR_INVALID_ARG;
+  const size_t ybytes = (static_cast<size_t>(M - 1) * ld_y + N) * sizeof(float);
+  const size_t xbytes = (static_cast<size_t>(M - 1) * ld_x + K) * sizeof(float);
+  const size_t wbytes = static_cast<size_t>(N) * K * sizeof(float);
+  if (ranges_overlap(y, ybytes, x, xbytes) || ranges_overlap(y, ybytes, W, wbytes))
+    return DLRM_ERR_INVALID_ARG;
+  if (math != DLRM_MATH_FP32) return DLRM_ERR_UNSUPPORTED;
+  return cuda_status(dlrm::launch_linear_fp32(x, ld_x, W, K, bias, y, ld_y, M, N, K, act,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,184 @@
+// Strict-lower-triangular pairwise-dot interaction with the concat fused.
+//
+// Per sample: Z = [x; e_0; ...; e_{K-1}] is (F, D), F = K + 1, and
+// z[p] = <Z_i, Z_j> for p = i(i-1)/2 + j, j < i (i-major), R = [x, z]
+// (Luminal compare dlrm-fused-kernels...dlrm-pt2-megakernel,
+// dlrm_megakernel.rs steps 4-5; compare modal_ci_ready...vanilla-pytorch,
+// commit message: PairwiseDotLowerTriStackedKernel, block-per-batch-row with
+// all F*D features cached in shared memory and (i, j) from the closed form).
+//
+// GB300 design: a block takes S consecutive samples (S = 1 for wide F, more
+// when F is small so the block has S * P >= blockDim pair tasks), stages
+// their S*F*D features in shared memory with 128-bit coalesced loads (rows
+// padded to D + 4 floats so the 16-byte reads of different rows fall in
+// different banks), then thread w computes pair tasks w, w + T, ... with a
+// float4 dot product. Consecutive threads take consecutive p, so the writes
+// of R are coalesced and the i row is a shared-memory broadcast.
+#include <atomic>
+
+#include "common.cuh"
+
+namespace dlrm {
+namespace {
+
+constexpr int kInteractThreads = 256;
+
+__host__ __device__ __forceinline__ int z_stride(int d) {
+  return static_cast<int>(round_up(d, 4)) + 4;
+}
+
+template <bool VEC>
+__global__ void __launch_bounds__(kInteractThreads)
+interaction_kernel(const float* __restrict__ dense, int ld_dense, const float* __restrict__ emb,
+                   int batch, int k_tables, int d, float* __restrict__ out, int ld_out,
+                   int copy_dense, int samples_per_block) {
+  extern __shared__ float4 smem_f4[];
+  float* zs = reinterpret_cast<float*>(smem_f4);
+  const int f = k_tables + 1;
+  const int p_count = f * (f - 1) / 2;
+  const int ldz = z_stride(d);
+  const int b0 = blockIdx.x * samples_per_block;
+  const int ns = min(samples_per_block, batch - b0);
+  const int tid = threadIdx.x;
+
+  // Stage Z for ns samples: row 0 from dense, rows 1..K from emb.
+  if (VEC) {
+    const int d4 = d / 4;
+    const int per_sample = f * d4;
+    for (int e = tid; e < ns * per_sample; e += blockDim.x) {
+      const int s = e / per_sample;
+      const int r = e - s * per_sample;
+      const int row = r / d4;
+      const int c4 = r - row * d4;
+      float4 v;
+      if (row == 0) {
+        v = __ldg(reinterpret_cast<const float4*>(dense + static_cast<int64_t>(b0 + s) * ld_dense) + c4);
+      } else {
+        v = __ldg(reinterpret_cast<const float4*>(emb) +
+                  (static_cast<int64_t>(b0 + s) * k_tables + (row - 1)) * d4 + c4);
+      }
+      *reinterpret_cast<float4*>(zs + (s * f + row) * ldz + c4 * 4) = v;
+    }
+  } else {
+    const int per_sample = f * d;
+    for (int e = tid; e < ns * per_sample; e += blockDim.x) {
+      const int s = e / per_sample;
+      const int r = e - s * per_sample;
+      const int row = r / d;
+      const int c = r - row * d;
+      const float v = (row == 0)
+          ? __ldg(dense + static_cast<int64_t>(b0 + s) * ld_dense + c)
+          : __ldg(emb + (static_cast<int64_t>(b0 + s) * k_tables + (row - 1)) * d + c);
+      zs[(s * f + row) * ldz + c] = v;
+    }
+  }
+  __syncthreads();
+
+  int col0 = 0;
+  if (copy_dense) {
+    for (int e = tid; e < ns * d; e += blockDim.x) {
+      const int s = e / d;
+      const int c = e - s * d;
+      out[static_cast<int64_t>(b0 + s) * ld_out + c] = zs[(s * f) * ldz + c];
+    }
+    col0 = d;
+  }
+  const int d4 = d / 4;
+  for (int w = tid; w < ns * p_count; w += blockDim.x) {
+    const int s = w / p_count;
+    const int p = w - s * p_count;
+    int i, j;
+    pair_from_index(p, i, j);
+    const float* zi = zs + (s * f + i) * ldz;
+    const float* zj = zs + (s * f + j) * ldz;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c4 = 0; c4 < d4; ++c4) {
+      const float4 u = *reinterpret_cast<const float4*>(zi + 4 * c4);
+      const float4 v = *reinterpret_cast<const float4*>(zj + 4 * c4);
+      a.x = fmaf(u.x, v.x, a.x);
+      a.y = fmaf(u.y, v.y, a.y);
+      a.z = fmaf(u.z, v.z, a.z);
+      a.w = fmaf(u.w, v.w, a.w);
+    }
+    float acc = (a.x + a.y) + (a.z + a.w);
+    for (int c = 4 * d4; c < d; ++c) acc = fmaf(zi[c], zj[c], acc);
+    out[static_cast<int64_t>(b0 + s) * ld_out + col0 + p] = acc;
+  }
+}
+
+__global__ void pair_map_kernel(int f, int32_t* i_out, int32_t* j_out) {
+  const int p_count = f * (f - 1) / 2;
+  for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < p_count; p += gridDim.x * blockDim.x) {
+    int i, j;
+    pair_from_index(p, i, j);
+    i_out[p] = i;
+    j_out[p] = j;
+  }
+}
+
+// Raise a kernel's dynamic shared-memory limit to the device maximum, once per
+// (kernel, device). Done on first use, outside any stream capture in practice
+// (the first call of a shape), and never again on later launches.
+template <class K>
+cudaError_t enable_large_smem(K kernel, int slot) {
+  static std::atomic<uint64_t> done[2];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = (dev < 64) ? (uint64_t(1) << dev) : 0;
+  if (bit && (done[slot].load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(device_max_smem_optin()));
+  if (e == cudaSuccess && bit) done[slot].fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
+}  // namespace
+
+size_t interaction_smem_per_sample(int k, int d) {
+  return static_cast<size_t>(k + 1) * z_stride(d) * sizeof(float);
+}
+
+cudaError_t launch_interaction(const float* dense, int ld_dense, const float* emb, int b,
+                               int k, int d, float* out, int ld_out, int copy_dense,
+                               cudaStream_t stream) {
+  if (b == 0) return cudaSuccess;
+  const int f = k + 1;
+  const int p_count = f * (f - 1) / 2;
+  const size_t per = interaction_smem_per_sample(k, d);
+  const size_t budget = 64 * 1024;
+  int s = p_count > 0 ? (kInteractThreads + p_count - 1) / p_count : kInteractThreads;
+  s = static_cast<int>(std::min<size_t>(static_cast<size_t>(s), std::max<size_t>(1, budget / per)));
+  // keep at least two blocks per SM when the batch allows it
+  const int sms = device_sm_count();
+  const int cap = std::max(1, (b + 2 * sms - 1) / (2 * sms));
+  s = std::max(1, std::min(s, cap));
+  const size_t smem = per * s;
+  const bool vec = (d % 4 == 0) && (ld_dense % 4 == 0) &&
+                   (reinterpret_cast<uintptr_t>(dense) % 16 == 0) &&
+                   (reinterpret_cast<uintptr_t>(emb) % 16 == 0);
+  const unsigned grid = static_cast<unsigned>((b + s - 1) / s);
+  if (smem > 48 * 1024) {
+    cudaError_t e = vec ? enable_large_smem(interaction_kernel<true>, 0)
+                        : enable_large_smem(interaction_kernel<false>, 1);
+    if (e != cudaSuccess) return e;
+  }
+  if (vec) {
+    interaction_kernel<true><<<grid, kInteractThreads, smem, stream>>>(
+        dense, ld_dense, emb, b, k, d, out, ld_out, copy_dense, s);
+  } else {
+    interaction_kernel<false><<<grid, kInteractThreads, smem, stream>>>(
+        dense, ld_dense, emb, b, k, d, out, ld_out, copy_dense, s);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pair_map(int f, int32_t* i_out, int32_t* j_out, cudaStream_t stream) {
+  const int p_count = f * (f - 1) / 2;
+  if (p_count == 0) return cudaSuccess;
+  const unsigned grid = static_cast<unsigned>(std::min(1024, (p_count + 255) / 256));
+  pair_map_kernel<<<grid, 256, 0, stream>>>(f, i_out, j_out);
+  return cudaGetLastError();
+}
+
+}  // namespace dlrm

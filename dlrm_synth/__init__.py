@@ -270,7 +270,7 @@ def make_offsets(cfg: DlrmConfig, batch: Optional[int] = None) -> np.ndarray:
     """Uniform-stride offsets, (K, B) int64: offsets[t][b] = b * L."""
     b = cfg.batch if batch is None else batch
     row = np.arange(b, dtype=np.int64) * cfg.bag_size
-    return np.ascontiguousarray(np.broadcast_to(row, (cfg.n_tables, b)))
+    return np.broadcast_to(row, (cfg.n_tables, b)).copy()
 
 
 def make_inputs(cfg: DlrmConfig, seed: int = 1234, batch: Optional[int] = None,

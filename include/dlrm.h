@@ -1,0 +1,230 @@
+/*
+ * dlrm.h -- C ABI of libdlrm_gb300.so, a single-GPU (GB300, sm_103a) DLRMv1
+ * inference forward: multi-table EmbeddingBag sum, bottom MLP, strict-lower-
+ * triangular pairwise-dot interaction with the dense vector concatenated in
+ * front, and a top MLP ending in a sigmoid.
+ *
+ * Sources (Luminal compare pages on the DLRMv1 forward):
+ *  [P1] compare modal_ci_ready...vanilla-pytorch, commit message "vanilla-
+ *       PyTorch DLRMv1 fast paths": multi_table_embedding_bag_sum (K tables in
+ *       one launch, (batch, num_tables, d) F32 out), pairwise-dot kernels
+ *       (block-per-batch, closed-form pair index), linear_bias_(relu|sigmoid).
+ *  [P4] compare dlrm-fused-kernels...dlrm-pt2-megakernel:
+ *       dlrm_megakernel.rs (shape struct, validate(), body steps 1-6),
+ *       LessonsLearned "EmbeddingBag translator gap", translate_embedding_bag.
+ *
+ * Conventions for every call below:
+ *  - Pointers are DEVICE pointers unless marked "host".
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream). Every call only enqueues work on it and never synchronises it,
+ *    except dlrm_get_error and dlrm_create/dlrm_destroy as documented.
+ *  - All float data is fp32, row-major; integer indices/offsets are int64.
+ *  - Argument problems detectable on the host are returned as a status
+ *    before anything is launched. Problems only visible on the device (an
+ *    index outside its table, offsets that are not the uniform stride) never
+ *    trap: the affected bag contributes zeros and a bit is set in a device
+ *    error word, read with dlrm_get_error (handle path) or by the caller
+ *    (standalone path, err_flag argument).
+ *  - Nothing here allocates except dlrm_create.
+ */
+#ifndef DLRM_GB300_H
+#define DLRM_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DLRM_OK = 0,
+  DLRM_ERR_INVALID_ARG = 1,  /* bad pointer, size, alignment or shape */
+  DLRM_ERR_UNSUPPORTED = 2,  /* valid request outside what is implemented */
+  DLRM_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
+  DLRM_ERR_OOM = 4,          /* device allocation failed (dlrm_create only) */
+  DLRM_ERR_INDEX_OOB = 5,    /* device saw an index outside [0, rows) */
+  DLRM_ERR_TIMEOUT = 6       /* a bounded device wait gave up */
+} dlrm_status_t;
+
+/* Arithmetic of the MLP GEMMs. FP32 (SIMT FFMA) is the parity mode. TF32 and
+ * BF16 run the MLPs on the tcgen05 tensor cores with fp32 accumulation in
+ * TMEM (opt-in; results within rel 2e-2 of fp32). */
+typedef enum { DLRM_MATH_FP32 = 0, DLRM_MATH_TF32 = 1, DLRM_MATH_BF16 = 2 } dlrm_math_t;
+
+/* Epilogue activation of linear_bias_act. */
+typedef enum { DLRM_ACT_NONE = 0, DLRM_ACT_RELU = 1, DLRM_ACT_SIGMOID = 2 } dlrm_act_t;
+
+/* Device error word bits (1u << code) set by kernels. */
+#define DLRM_ERRBIT_INDEX_OOB (1u << DLRM_ERR_INDEX_OOB)
+#define DLRM_ERRBIT_OFFSETS   (1u << DLRM_ERR_UNSUPPORTED)
+#define DLRM_ERRBIT_TIMEOUT   (1u << DLRM_ERR_TIMEOUT)
+
+#define DLRM_MAX_TABLES 128   /* K limit (kernel-parameter pointer table) */
+#define DLRM_MAX_LAYERS 16    /* Linear layers per MLP */
+
+/* Model shape ([P4] dlrm_megakernel.rs shape struct and validate()):
+ *   ln_bot  host, n_bot + 1 widths: ln_bot[0] = dense features,
+ *           ln_bot[n_bot] = emb_dim (the bottom output is the first feature
+ *           vector); ReLU follows every bottom layer, including the last.
+ *   rows    host, n_tables row counts (V_t); every table is (V_t, emb_dim).
+ *   ln_top  host, n_top + 1 widths: ln_top[0] = emb_dim + F(F-1)/2 with
+ *           F = n_tables + 1; ln_top[n_top] = 1. ReLU follows every top layer
+ *           but the last, which is followed by a sigmoid.
+ *   bag_size  L >= 1 indices per bag, uniform (offsets[t][b] = b * L).
+ *   max_batch largest batch a forward call may pass; sizes the workspace. */
+typedef struct {
+  int32_t n_bot;
+  const int32_t* ln_bot;
+  int32_t n_tables;
+  const int64_t* rows;
+  int32_t emb_dim;
+  int32_t n_top;
+  const int32_t* ln_top;
+  int32_t bag_size;
+  int32_t max_batch;
+  dlrm_math_t math;
+} dlrm_config_t;
+
+typedef struct dlrm_handle_s* dlrm_handle_t;
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int32_t dlrm_version(void);
+
+/* Static string for a status code. */
+const char* dlrm_status_string(int32_t status);
+
+/* Build a forward plan on the current CUDA device.
+ *   tables  host array of n_tables DEVICE pointers, each (rows[t], emb_dim)
+ *           fp32 row-major, 16-byte aligned. BORROWED: the handle keeps the
+ *           pointers and never copies the tables (a 13 GB table set stays
+ *           where the caller put it); the caller keeps them alive and
+ *           unchanged in shape until dlrm_destroy.
+ *   bot_w/bot_b/top_w/top_b  host arrays of n_bot / n_top pointers (host or
+ *           device memory, read with cudaMemcpyDefault) to the Linear weights
+ *           in PyTorch (out, in) row-major layout and their (out) biases. The
+ *           handle COPIES them (padded, and converted for TF32/BF16) into its
+ *           own device memory; the caller may free them afterwards.
+ * Allocates the handle's workspace for max_batch samples (bag sums, hidden
+ * activations, the interaction output, staging for dlrm_forward_host) and
+ * synchronises the device once. Returns INVALID_ARG for any shape violation
+ * of [P4] validate(), OOM if an allocation fails, UNSUPPORTED for
+ * n_tables > DLRM_MAX_TABLES or a math mode not built. */
+dlrm_status_t dlrm_create(const dlrm_config_t* cfg, const float* const* tables,
+                          const float* const* bot_w, const float* const* bot_b,
+                          const float* const* top_w, const float* const* top_b,
+                          dlrm_handle_t* out);
+
+/* One forward pass for `batch` samples ([P4] dlrm_megakernel.rs steps 1-6).
+ *   dense    (batch, ln_bot[0]) fp32
+ *   indices  (n_tables, batch * bag_size) int64, table-major
+ *   offsets  (n_tables, batch) int64, bag starts; must be b * bag_size
+ *            (include_last_offset = false, [P4] translate_embedding_bag)
+ *   out      (batch) fp32 click probabilities
+ * 1 <= batch <= max_batch. Enqueued on `stream`; no host synchronisation;
+ * capturable in a CUDA graph. Device-side problems (index out of range,
+ * non-uniform offsets) set the handle's error word (see dlrm_get_error).
+ * Calls on one handle must be serialised on one stream (shared workspace). */
+dlrm_status_t dlrm_forward(dlrm_handle_t h, const float* dense, const int64_t* indices,
+                           const int64_t* offsets, float* out, int32_t batch, void* stream);
+
+/* dlrm_forward from HOST buffers: enqueues the host-to-device copies of dense,
+ * indices and offsets into the handle's staging buffers, the forward, and the
+ * device-to-host copy of `out`, all on `stream`. Host buffers should be
+ * pinned for the copies to be asynchronous; they must stay valid and
+ * unchanged until the stream has passed this call (e.g. after
+ * cudaStreamSynchronize or dlrm_get_error). */
+dlrm_status_t dlrm_forward_host(dlrm_handle_t h, const float* dense_host,
+                                const int64_t* indices_host, const int64_t* offsets_host,
+                                float* out_host, int32_t batch, void* stream);
+
+/* Synchronises `stream`, returns the first error recorded on the device
+ * since the last call (INDEX_OOB before UNSUPPORTED before TIMEOUT; OK if
+ * none) and clears it. */
+dlrm_status_t dlrm_get_error(dlrm_handle_t h, void* stream);
+
+/* Bytes of device memory the handle owns (workspace + packed weights). */
+int64_t dlrm_workspace_bytes(dlrm_handle_t h);
+
+/* Number of kernel launches one dlrm_forward enqueues (its stages). */
+int32_t dlrm_num_stages(dlrm_handle_t h);
+
+/* Static name of stage i ("gather", "bottom0", ..., "interaction", "top0", ...),
+ * or NULL when i is out of range. */
+const char* dlrm_stage_name(dlrm_handle_t h, int32_t i);
+
+/* Per-stage timing (off by default). With enable != 0 the handle creates one
+ * CUDA event per stage boundary and every later dlrm_forward records them on
+ * its stream, then WAITS for its last event and adds each stage's
+ * event-to-event time to a running total; this mode synchronises the host
+ * and must not be used inside graph capture. enable = 0 destroys the events
+ * and clears the totals. */
+dlrm_status_t dlrm_set_profiling(dlrm_handle_t h, int32_t enable);
+
+/* Copies up to `capacity` per-stage totals (milliseconds, summed over the
+ * profiled forward calls) into total_ms and the number of profiled calls into
+ * *calls; returns the number of stages, or -1 for a null handle. */
+int32_t dlrm_stage_times(dlrm_handle_t h, double* total_ms, int32_t capacity, int64_t* calls);
+
+/* Synchronises the device and frees everything the handle owns (not the
+ * borrowed tables). Null is a no-op. */
+void dlrm_destroy(dlrm_handle_t h);
+
+/* Multi-table EmbeddingBag sum in one launch ([P1] MultiTableEmbeddingBagSum;
+ * [P4] LessonsLearned "EmbeddingBag translator gap"):
+ *   out[b][t][:] = sum_{l < L} tables[t][indices[t][offsets[t][b] + l]][:]
+ *   tables   host array of K device pointers, table t is (rows[t], D) fp32
+ *            row-major; rows is a host array of K row counts
+ *   indices  (K, B * L) int64 table-major;  offsets (K, B) int64
+ *   out      (B, K, D) fp32
+ *   err_flag device int32 error word or NULL; bits DLRM_ERRBIT_INDEX_OOB (an
+ *            index outside [0, rows[t]): that row contributes zeros) and
+ *            DLRM_ERRBIT_OFFSETS (offsets[t][b] != b * L: the bag is zeros)
+ *            are OR-ed in; it is never cleared here.
+ * Sum order within a bag is the index order, in fp32; with L = 1 the result
+ * is the row itself (an index_select), bit for bit.
+ * 1 <= K <= DLRM_MAX_TABLES, D >= 1, L >= 1, B >= 0 (B = 0 is a no-op). */
+dlrm_status_t embedding_bag_sum_multi(const float* const* tables, const int64_t* rows,
+                                      int32_t K, int32_t D, const int64_t* indices,
+                                      const int64_t* offsets, int32_t B, int32_t L, float* out,
+                                      int32_t* err_flag, void* stream);
+
+/* Strict-lower-triangular pairwise-dot interaction ([P1]
+ * PairwiseDotLowerTriStackedKernel; [P4] dlrm_megakernel.rs steps 4-5):
+ * per sample, Z = [dense; emb[0..K-1]] is (F, D) with F = K + 1, and
+ *   z[p] = <Z_i, Z_j>,  p = i(i-1)/2 + j,  0 <= j < i < F   (i-major order),
+ * so i = floor((1 + sqrt(1 + 8p)) / 2), j = p - i(i-1)/2.
+ *   dense  (B, D) fp32 with row stride ld_dense >= D
+ *   emb    (B, K, D) fp32 contiguous
+ *   out    (B, ld_out) fp32; copy_dense = 1 writes out[b] = [dense[b], z]
+ *          (the concat R = [x, z] fused; ld_out >= D + P), copy_dense = 0
+ *          writes out[b] = z (ld_out >= P). Columns past the written width
+ *          are left untouched.
+ * K >= 0 (K = 0 gives no pairs), D >= 1, B >= 0. Needs F * (D + 4) * 4 bytes
+ * of shared memory per sample (UNSUPPORTED if that exceeds the device). */
+dlrm_status_t pairwise_dot_lower_tri(const float* dense, int32_t ld_dense, const float* emb,
+                                     int32_t B, int32_t K, int32_t D, float* out,
+                                     int32_t ld_out, int32_t copy_dense, void* stream);
+
+/* Test-mode export of the device pair map used by pairwise_dot_lower_tri:
+ * i_out[p], j_out[p] (device int32, P = F(F-1)/2 entries each) for F >= 2. */
+dlrm_status_t pairwise_pair_map(int32_t F, int32_t* i_out, int32_t* j_out, void* stream);
+
+/* Fused Linear + bias + activation ([P1] linear_bias_(relu|sigmoid) over the
+ * fused Matmul2D kernel; [P4] body steps 2 and 6):
+ *   y[m][n] = act(sum_k x[m][k] * W[n][k] + bias[n])
+ *   x     (M, K) fp32, row stride ld_x >= K
+ *   W     (N, K) fp32 row-major (PyTorch nn.Linear layout), contiguous
+ *   bias  (N) fp32 or NULL (no bias)
+ *   y     (M, N) fp32, row stride ld_y >= N; must not overlap x or W
+ * act: DLRM_ACT_NONE / RELU / SIGMOID (1 / (1 + exp(-a))).
+ * math: DLRM_MATH_FP32 (parity) or an opt-in tensor-core mode.
+ * M >= 0 (0 is a no-op), N >= 1, K >= 1. */
+dlrm_status_t linear_bias_act(const float* x, int32_t ld_x, const float* W, const float* bias,
+                              float* y, int32_t ld_y, int32_t M, int32_t N, int32_t K,
+                              dlrm_act_t act, dlrm_math_t math, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DLRM_GB300_H */

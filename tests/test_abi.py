@@ -1,0 +1,107 @@
+"""The C-ABI library loads, exports every symbol include/dlrm.h declares, and
+rejects bad arguments on the host before touching the GPU (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import dlrm_embedding_interaction_gb300 as dl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dlrm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from dlrm_embedding_interaction_gb300 import build
+    build.build()
+    return dl.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z_][a-z0-9_]*)\s*\(",
+                       text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("dlrm_create", "dlrm_forward", "embedding_bag_sum_multi",
+                     "pairwise_dot_lower_tri", "linear_bias_act"):
+        assert required in names
+    assert sorted(dl.EXPORTS) == names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert dl.version() == 100
+
+
+def test_status_strings(lib):
+    assert lib.dlrm_status_string(dl.OK) == b"ok"
+    assert lib.dlrm_status_string(dl.ERR_INDEX_OOB) == b"index out of range"
+    assert lib.dlrm_status_string(99) == b"unknown status"
+
+
+def test_host_side_argument_checks(lib):
+    vp = ctypes.c_void_p
+    null = vp(0)
+    # linear_bias_act: N < 1, K < 1, ld_x < K, bad act
+    assert lib.linear_bias_act(null, 4, null, null, null, 4, 4, 0, 4, 0, 0, null) == dl.ERR_INVALID_ARG
+    assert lib.linear_bias_act(null, 4, null, null, null, 4, 4, 4, 0, 0, 0, null) == dl.ERR_INVALID_ARG
+    assert lib.linear_bias_act(null, 3, null, null, null, 4, 4, 4, 4, 0, 0, null) == dl.ERR_INVALID_ARG
+    assert lib.linear_bias_act(null, 4, null, null, null, 4, 4, 4, 4, 7, 0, null) == dl.ERR_INVALID_ARG
+    # M = 0 is a no-op
+    assert lib.linear_bias_act(null, 4, null, null, null, 4, 0, 4, 4, 0, 0, null) == dl.OK
+    # null pointers with M > 0
+    assert lib.linear_bias_act(null, 4, null, null, null, 4, 2, 4, 4, 0, 0, null) == dl.ERR_INVALID_ARG
+    # gather: K < 1, K > max, B = 0 no-op, null tables
+    assert lib.embedding_bag_sum_multi(null, null, 0, 4, null, null, 1, 1, null, null, null) == dl.ERR_INVALID_ARG
+    ptrs = (vp * 200)()
+    rows = (ctypes.c_int64 * 200)()
+    assert lib.embedding_bag_sum_multi(ptrs, rows, 200, 4, null, null, 1, 1, null, null, null) == dl.ERR_UNSUPPORTED
+    assert lib.embedding_bag_sum_multi(ptrs, rows, 3, 4, null, null, 0, 1, null, null, null) == dl.OK
+    assert lib.embedding_bag_sum_multi(ptrs, rows, 3, 4, null, null, 5, 1, null, null, null) == dl.ERR_INVALID_ARG
+    # interaction: ld_out too small for [x, z]; B = 0 no-op
+    assert lib.pairwise_dot_lower_tri(null, 4, null, 2, 3, 4, null, 9, 1, null) == dl.ERR_INVALID_ARG
+    assert lib.pairwise_dot_lower_tri(null, 4, null, 0, 3, 4, null, 10, 1, null) == dl.OK
+    assert lib.pairwise_pair_map(1, null, null, null) == dl.ERR_INVALID_ARG
+
+
+def _create(lib, ln_bot, ln_top, rows, d, bag=1, max_batch=8, math=0, tables_ok=True):
+    k = len(rows)
+    cfg = dl._Config(len(ln_bot) - 1, (ctypes.c_int32 * len(ln_bot))(*ln_bot), k,
+                     (ctypes.c_int64 * k)(*rows), d, len(ln_top) - 1,
+                     (ctypes.c_int32 * len(ln_top))(*ln_top), bag, max_batch, math)
+    fake = ctypes.c_void_p(0x1000 if tables_ok else 0)
+    tabs = (ctypes.c_void_p * k)(*([fake] * k))
+    w = (ctypes.c_void_p * 16)(*([ctypes.c_void_p(0x1000)] * 16))
+    h = ctypes.c_void_p()
+    return lib.dlrm_create(ctypes.byref(cfg), tabs, w, w, w, w, ctypes.byref(h)), h
+
+
+def test_create_validates_shapes(lib):
+    """dlrm_megakernel.rs validate(): ln_bot.last() = m_spa, ln_top[0] = m_spa + P,
+    ln_top.last() = 1; plus the ABI's own limits."""
+    assert _create(lib, [13, 8, 5], [10, 8, 1], [10, 20, 30], 4)[0] == dl.ERR_INVALID_ARG
+    assert _create(lib, [13, 8, 4], [11, 8, 1], [10, 20, 30], 4)[0] == dl.ERR_INVALID_ARG
+    assert _create(lib, [13, 8, 4], [10, 8, 2], [10, 20, 30], 4)[0] == dl.ERR_INVALID_ARG
+    assert _create(lib, [13, 8, 4], [10, 8, 1], [10, 20, 30], 4, bag=0)[0] == dl.ERR_INVALID_ARG
+    assert _create(lib, [13, 8, 4], [10, 8, 1], [10, 20, 30], 4, max_batch=0)[0] == dl.ERR_INVALID_ARG
+    assert _create(lib, [13, 8, 4], [10, 8, 1], [10, 0, 30], 4)[0] == dl.ERR_INVALID_ARG
+    assert _create(lib, [13, 8, 4], [10, 8, 1], [10, 20, 30], 4, tables_ok=False)[0] == dl.ERR_INVALID_ARG
+    assert _create(lib, [13, 8, 4], [10, 8, 1], [10, 20, 30], 4, math=5)[0] != dl.OK
+    assert lib.dlrm_create(None, None, None, None, None, None, None) == dl.ERR_INVALID_ARG
+
+
+def test_forward_rejects_null_handle(lib):
+    null = ctypes.c_void_p(0)
+    assert lib.dlrm_forward(null, null, null, null, null, 1, null) == dl.ERR_INVALID_ARG
+    assert lib.dlrm_forward_host(null, null, null, null, null, 1, null) == dl.ERR_INVALID_ARG
+    assert lib.dlrm_get_error(null, null) == dl.ERR_INVALID_ARG
+    assert lib.dlrm_workspace_bytes(null) == 0
+    lib.dlrm_destroy(null)

@@ -1,0 +1,367 @@
+"""GPU parity: every entry point of libdlrm_gb300.so against the CPU oracle.
+
+Inputs are seeded and synthetic (dlrm_synth). Tolerances: index, pair-map and
+bag-size-1 gather results are bit-exact; fp32 results must satisfy
+|gpu - oracle| <= 1e-5 + 1e-4 * |oracle| (oracle in fp64). Stage tests feed the
+oracle the same fp32 inputs the kernel consumed, so errors never compound.
+"""
+import numpy as np
+import pytest
+
+import dlrm_synth as synth
+import oracle
+
+torch = pytest.importorskip("torch")
+import dlrm_embedding_interaction_gb300 as dl  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+ATOL, RTOL = 1e-5, 1e-4
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    if not torch.cuda.is_available():
+        pytest.fail("the gpu tests need a CUDA device")
+    from dlrm_embedding_interaction_gb300 import build
+    build.build()
+    dl.lib()
+    torch.cuda.set_device(0)
+
+
+def cu(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def close(gpu, ref, atol=ATOL, rtol=RTOL):
+    np.testing.assert_allclose(np.asarray(gpu, dtype=np.float64), ref, atol=atol, rtol=rtol)
+
+
+# ---------------------------------------------------------------- gather
+
+GATHER_CASES = [
+    # name, B, rows, D, L, dist
+    ("tiny_b64_k3", 64, (1000,) * 3, 16, 2, "uniform"),
+    ("b2048_k3", 2048, (100_000,) * 3, 64, 1, "uniform"),
+    ("b2048_k32", 2048, (100_000,) * 32, 64, 1, "uniform"),
+    ("ragged_d24", 37, (5, 1000, 77), 24, 3, "uniform"),
+    ("scalar_d13", 19, (50, 50), 13, 4, "uniform"),
+    ("d128_l20_zipf", 301, (5000,) * 4, 128, 20, "zipf"),
+    ("d512", 9, (100, 100), 512, 5, "uniform"),
+    ("d1024_l1", 5, (64,), 1024, 1, "uniform"),
+    ("single", 1, (10,), 4, 1, "uniform"),
+    ("d4_l33", 130, (7, 9), 4, 33, "uniform"),
+]
+
+
+def _gather_inputs(b, rows, d, l, dist, seed=17):
+    cfg = synth.DlrmConfig("g", b, (13, d), tuple(rows), d, l, (d + 1,), 0.05, dist)
+    tables = [synth.make_table(cfg, seed, t) for t in range(len(rows))]
+    return cfg, tables, synth.make_indices(cfg, seed), synth.make_offsets(cfg)
+
+
+def _run_gather(tables, idx, off, l, err=None):
+    k, d = len(tables), tables[0].shape[1]
+    b = off.shape[1]
+    tdev = [cu(t) for t in tables]
+    out = torch.full((b, k, d), float("nan"), device="cuda")
+    dl.embedding_bag_sum_multi(tdev, cu(idx), cu(off), out, l, err_flag=err)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+@pytest.mark.parametrize("case", GATHER_CASES, ids=[c[0] for c in GATHER_CASES])
+def test_gather_matches_oracle(case):
+    _, b, rows, d, l, dist = case
+    cfg, tables, idx, off = _gather_inputs(b, rows, d, l, dist)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = _run_gather(tables, idx, off, l, err)
+    assert int(err.item()) == 0
+    if l == 1:
+        for t in range(len(rows)):   # bag size 1 is an index_select, bit for bit
+            np.testing.assert_array_equal(got[:, t, :], np.take(tables[t], idx[t], axis=0))
+    ref = oracle.embedding_bag_sum(tables, idx, off)
+    close(got, ref)
+
+
+def test_gather_empty_batch_is_noop():
+    t = cu(np.ones((4, 8), np.float32))
+    out = torch.empty((0, 1, 8), device="cuda")
+    dl.embedding_bag_sum_multi([t], torch.empty((1, 0), dtype=torch.int64, device="cuda"),
+                               torch.empty((1, 0), dtype=torch.int64, device="cuda"), out, 1)
+
+
+def test_gather_out_of_range_index_sets_flag_and_contributes_zero():
+    cfg, tables, idx, off = _gather_inputs(40, (100, 50), 16, 3, "uniform")
+    idx[0, 5] = -1
+    idx[1, 77] = 50
+    idx[1, 78] = 10 ** 12
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = _run_gather(tables, idx, off, 3, err)
+    assert int(err.item()) & dl.ERRBIT_INDEX_OOB
+    ref = oracle.embedding_bag_sum(tables, idx, off, allow_oob=True)
+    close(got, ref)
+
+
+def test_gather_non_uniform_offsets_flagged_and_zeroed():
+    cfg, tables, idx, off = _gather_inputs(12, (100,), 8, 2, "uniform")
+    off = off.copy()
+    off[0, 3] = 5     # not 3 * 2
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = _run_gather(tables, idx, off, 2, err)
+    assert int(err.item()) & dl.ERRBIT_OFFSETS
+    np.testing.assert_array_equal(got[3, 0], 0.0)
+    good = [b for b in range(12) if b != 3]
+    ref = oracle.embedding_bag_sum(tables, idx, synth.make_offsets(cfg))
+    close(got[good], ref[good])
+
+
+# ---------------------------------------------------------------- interaction
+
+INTERACT_CASES = [
+    (64, 3, 16), (2048, 3, 64), (2048, 32, 64), (300, 26, 128), (5, 0, 8),
+    (17, 7, 13), (3, 127, 4), (1, 1, 1), (33, 5, 6), (1000, 1, 64),
+]
+
+
+@pytest.mark.parametrize("b,k,d", INTERACT_CASES)
+@pytest.mark.parametrize("copy_dense", [True, False])
+@pytest.mark.parametrize("ld_pad", [0, 3, 4])
+def test_interaction_matches_oracle(b, k, d, copy_dense, ld_pad):
+    rng = np.random.default_rng(b * 131 + k * 7 + d)
+    ld_dense = d + ld_pad                 # 16-byte rows (vector staging) or not
+    dense_full = rng.standard_normal((b, ld_dense)).astype(np.float32)
+    x = dense_full[:, :d]
+    e = rng.uniform(-0.5, 0.5, (b, k, d)).astype(np.float32)
+    f = k + 1
+    p = f * (f - 1) // 2
+    width = (d if copy_dense else 0) + p
+    ld_out = width + 5
+    out = torch.full((b, ld_out), -7.0, device="cuda")
+    ddev = cu(dense_full)[:, :d]
+    dl.pairwise_dot_lower_tri(ddev, cu(e).reshape(b, k, d), out, copy_dense=copy_dense)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    ref = oracle.interaction(x.astype(np.float64), e.astype(np.float64))
+    if copy_dense:
+        np.testing.assert_array_equal(got[:, :d], x)          # the concat is a copy
+        close(got[:, :width], ref)
+    else:
+        close(got[:, :width], ref[:, d:])
+    np.testing.assert_array_equal(got[:, width:], -7.0)       # padding untouched
+
+
+@pytest.mark.parametrize("f", [2, 4, 27, 33, 256, 1500])
+def test_pair_map_is_bit_exact(f):
+    p = f * (f - 1) // 2
+    i_out = torch.full((p,), -1, dtype=torch.int32, device="cuda")
+    j_out = torch.full((p,), -1, dtype=torch.int32, device="cuda")
+    dl.pairwise_pair_map(f, i_out, j_out)
+    torch.cuda.synchronize()
+    ei, ej = oracle.pair_enumerate(f)
+    np.testing.assert_array_equal(i_out.cpu().numpy(), ei)
+    np.testing.assert_array_equal(j_out.cpu().numpy(), ej)
+
+
+# ---------------------------------------------------------------- linear
+
+LINEAR_CASES = [
+    # M, N, K, ld_x extra
+    (1, 1, 1, 0), (7, 13, 5, 0), (2048, 512, 13, 0), (2048, 256, 512, 0), (2048, 64, 256, 0),
+    (2048, 512, 70, 2), (2048, 512, 592, 0), (33, 1, 256, 0), (100, 17, 70, 3),
+    (257, 1024, 479, 1), (4096, 128, 64, 0), (65, 16, 16, 0), (3, 3, 1000, 0),
+]
+
+
+@pytest.mark.parametrize("m,n,k,pad", LINEAR_CASES)
+@pytest.mark.parametrize("act", [dl.ACT_NONE, dl.ACT_RELU, dl.ACT_SIGMOID])
+def test_linear_matches_oracle(m, n, k, pad, act):
+    rng = np.random.default_rng(m + 10 * n + 100 * k + act)
+    xf = rng.standard_normal((m, k + pad)).astype(np.float32)
+    bound = 1.0 / np.sqrt(k)
+    w = rng.uniform(-bound, bound, (n, k)).astype(np.float32)
+    bias = rng.uniform(-bound, bound, n).astype(np.float32)
+    y = torch.full((m, n), float("nan"), device="cuda")
+    dl.linear_bias_act(cu(xf)[:, :k], cu(w), cu(bias), y, act)
+    torch.cuda.synchronize()
+    ref = oracle.linear(xf[:, :k].astype(np.float64), w, bias, act)
+    close(y.cpu().numpy(), ref)
+
+
+def test_linear_without_bias():
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((300, 40)).astype(np.float32)
+    w = rng.standard_normal((48, 40)).astype(np.float32) * 0.1
+    y = torch.empty((300, 48), device="cuda")
+    dl.linear_bias_act(cu(x), cu(w), None, y, dl.ACT_RELU)
+    torch.cuda.synchronize()
+    close(y.cpu().numpy(), oracle.linear(x, w, None, oracle.ACT_RELU))
+
+
+def test_linear_rejects_overlapping_output():
+    x = torch.zeros((8, 8), device="cuda")
+    w = torch.zeros((8, 8), device="cuda")
+    with pytest.raises(dl.DlrmError):
+        dl.linear_bias_act(x, w, None, x, dl.ACT_NONE)
+
+
+# ---------------------------------------------------------------- full forward
+
+def make_model(cfg, inp, max_batch=None, math=dl.MATH_FP32):
+    tables = [cu(t) for t in inp["tables"]]
+    return dl.DlrmModel(cfg.ln_bot, cfg.ln_top, tables,
+                        [cu(w) for w in inp["bot_w"]], [cu(v) for v in inp["bot_b"]],
+                        [cu(w) for w in inp["top_w"]], [cu(v) for v in inp["top_b"]],
+                        cfg.bag_size, max_batch or cfg.batch, math)
+
+
+def run_forward(model, inp):
+    out = model.forward(cu(inp["dense"]), cu(inp["indices"]), cu(inp["offsets"]))
+    assert model.error() == dl.OK
+    return out.cpu().numpy()
+
+
+FORWARD_CASES = ["tiny_b64_k3", "mini_b2048_k3_d4", "b2048_k3", "b2048_k32",
+                 "sweep_b1_k1", "sweep_b8_k16", "sweep_b33_k3", "sweep_b4096_k8",
+                 "sweep_b8192_k32"]
+
+
+@pytest.mark.parametrize("name", FORWARD_CASES)
+def test_forward_matches_oracle(name):
+    cfg = synth.get_config(name)
+    inp = synth.make_inputs(cfg, seed=1234)
+    model = make_model(cfg, inp)
+    got = run_forward(model, inp)
+    close(got, oracle.forward(inp))
+    model.close()
+
+
+@pytest.mark.parametrize("seed", [1, 2, 3])
+def test_forward_tiny_seeds(seed):
+    cfg = synth.get_config("tiny_b64_k3")
+    inp = synth.make_inputs(cfg, seed=seed)
+    model = make_model(cfg, inp)
+    close(run_forward(model, inp), oracle.forward(inp))
+    model.close()
+
+
+def test_forward_hand_fixture():
+    import json, os
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden",
+                                    "hand_forward_f3.json")))
+    f32 = lambda a: np.array(a, np.float32)
+    inp = dict(dense=f32(g["dense"]), tables=[f32(t) for t in g["tables"]],
+               indices=np.array(g["indices"], np.int64), offsets=np.array(g["offsets"], np.int64),
+               bot_w=[f32(w) for w in g["bot_w"]], bot_b=[f32(v) for v in g["bot_b"]],
+               top_w=[f32(w) for w in g["top_w"]], top_b=[f32(v) for v in g["top_b"]])
+    cfg = synth.DlrmConfig("hand", 2, (2, 2), (3, 2), 2, 2, (5, 2, 1))
+    model = make_model(cfg, inp)
+    close(run_forward(model, inp), g["expected_out"], atol=1e-6, rtol=1e-6)
+    model.close()
+
+
+def test_forward_smaller_batches_than_max():
+    cfg = synth.get_config("b2048_k3")
+    inp = synth.make_inputs(cfg, seed=77)
+    model = make_model(cfg, inp, max_batch=2048)
+    for b in (1, 37, 1000):
+        sub = synth.make_inputs(cfg.with_batch(b), seed=78, with_tables=False)
+        sub.update(tables=inp["tables"], bot_w=inp["bot_w"], bot_b=inp["bot_b"],
+                   top_w=inp["top_w"], top_b=inp["top_b"])
+        close(run_forward(model, sub), oracle.forward(sub))
+    model.close()
+
+
+def test_forward_host_equals_device_forward():
+    cfg = synth.get_config("b2048_k3")
+    inp = synth.make_inputs(cfg, seed=5)
+    model = make_model(cfg, inp)
+    dev = run_forward(model, inp)
+    dense = torch.from_numpy(inp["dense"]).pin_memory()
+    idx = torch.from_numpy(inp["indices"]).pin_memory()
+    off = torch.from_numpy(inp["offsets"]).pin_memory()
+    out = torch.full((cfg.batch,), -1.0).pin_memory()
+    model.forward_host(dense, idx, off, out)
+    assert model.error() == dl.OK       # synchronises the stream
+    np.testing.assert_array_equal(out.numpy(), dev)
+    model.close()
+
+
+def test_forward_reports_device_errors_and_clears_them():
+    cfg = synth.get_config("tiny_b64_k3")
+    inp = synth.make_inputs(cfg, seed=8)
+    model = make_model(cfg, inp)
+    bad = dict(inp)
+    bad["indices"] = inp["indices"].copy()
+    bad["indices"][1, 9] = 1000           # rows = 1000
+    model.forward(cu(bad["dense"]), cu(bad["indices"]), cu(bad["offsets"]))
+    assert model.error() == dl.ERR_INDEX_OOB
+    assert model.error() == dl.OK         # cleared
+    got = model.forward(cu(bad["dense"]), cu(bad["indices"]), cu(bad["offsets"])).cpu().numpy()
+    assert model.error() == dl.ERR_INDEX_OOB
+    close(got, oracle.forward(bad, allow_oob=True))
+    bad_off = inp["offsets"].copy()
+    bad_off[2, 4] += 1
+    model.forward(cu(inp["dense"]), cu(inp["indices"]), cu(bad_off))
+    assert model.error() == dl.ERR_UNSUPPORTED
+    model.close()
+
+
+def test_forward_rejects_batch_above_max():
+    cfg = synth.get_config("tiny_b64_k3")
+    inp = synth.make_inputs(cfg, seed=8)
+    model = make_model(cfg, inp, max_batch=32)
+    with pytest.raises(dl.DlrmError) as ei:
+        model.forward(cu(inp["dense"]), cu(inp["indices"]), cu(inp["offsets"]))
+    assert ei.value.status == dl.ERR_INVALID_ARG
+    model.close()
+
+
+def test_forward_is_graph_capturable():
+    cfg = synth.get_config("b2048_k32")
+    inp = synth.make_inputs(cfg, seed=9)
+    model = make_model(cfg, inp)
+    dense, idx, off = cu(inp["dense"]), cu(inp["indices"]), cu(inp["offsets"])
+    out = torch.empty(cfg.batch, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        model.forward(dense, idx, off, out, stream=s)       # warm-up outside capture
+    s.synchronize()
+    ref = out.clone()
+    g = torch.cuda.CUDAGraph()
+    out.zero_()
+    with torch.cuda.graph(g, stream=s):
+        model.forward(dense, idx, off, out, stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    torch.testing.assert_close(out, ref, rtol=0, atol=0)
+    model.close()
+
+
+@pytest.mark.slow
+def test_forward_full_size_zipf_b65536_k26_sampled():
+    """The 13.3 GB workload at full size in the bench's launch configuration;
+    sampled outputs against the oracle, sampled bags against the oracle gather."""
+    cfg = synth.get_config("b65536_k26_zipf")
+    inp = synth.make_inputs(cfg, seed=1234)
+    model = make_model(cfg, inp)
+    dense, idx, off = cu(inp["dense"]), cu(inp["indices"]), cu(inp["offsets"])
+    got = model.forward(dense, idx, off)
+    assert model.error() == dl.OK
+    got = got.cpu().numpy()
+    assert np.all(np.isfinite(got)) and np.all((got > 0) & (got < 1))
+    ids = np.unique(np.concatenate([[0, cfg.batch - 1],
+                                    np.random.default_rng(0).integers(0, cfg.batch, 62)]))
+    close(got[ids], oracle.forward(inp, sample_ids=ids))
+    # sampled bags of the standalone gather over the same tables
+    emb = torch.empty((cfg.batch, cfg.n_tables, cfg.emb_dim), device="cuda")
+    dl.embedding_bag_sum_multi(model.tables, idx, off, emb, cfg.bag_size)
+    torch.cuda.synchronize()
+    l = cfg.bag_size
+    sub_idx = np.stack([np.concatenate([inp["indices"][t, b * l:(b + 1) * l] for b in ids])
+                        for t in range(cfg.n_tables)])
+    sub_off = np.ascontiguousarray(np.broadcast_to(np.arange(len(ids)) * l,
+                                                   (cfg.n_tables, len(ids)))).astype(np.int64)
+    ref = oracle.embedding_bag_sum(inp["tables"], sub_idx, sub_off)
+    close(emb[torch.from_numpy(ids).cuda()].cpu().numpy(), ref)
+    model.close()
