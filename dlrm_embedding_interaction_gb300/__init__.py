@@ -26,8 +26,10 @@ MAX_LAYERS = 16
 EXPORTS = ("dlrm_version", "dlrm_status_string", "dlrm_create", "dlrm_forward",
            "dlrm_forward_host", "dlrm_get_error", "dlrm_workspace_bytes", "dlrm_destroy",
            "dlrm_num_stages", "dlrm_stage_name", "dlrm_set_profiling", "dlrm_stage_times",
+           "dlrm_forward_noalloc",
            "embedding_bag_sum_multi", "pairwise_dot_lower_tri", "pairwise_pair_map",
            "linear_bias_act")
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _lib = None
 
@@ -63,6 +65,8 @@ def _bind(lib):
         "dlrm_stage_name": ([vp, i32], ctypes.c_char_p),
         "dlrm_set_profiling": ([vp, i32], st),
         "dlrm_stage_times": ([vp, ctypes.c_void_p, i32, ctypes.POINTER(i64)], i32),
+        "dlrm_forward_noalloc": ([ctypes.POINTER(_Config), vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                  i32, vp, vp], st),
         "embedding_bag_sum_multi": ([vp, vp, i32, i32, vp, vp, i32, i32, vp, vp, vp], st),
         "pairwise_dot_lower_tri": ([vp, i32, vp, i32, i32, i32, vp, i32, i32, vp], st),
         "pairwise_pair_map": ([i32, vp, vp, vp], st),
@@ -255,6 +259,37 @@ def dlrm_forward_host(h: int, dense, indices, offsets, out, stream=None) -> None
     _check(lib().dlrm_forward_host(ctypes.c_void_p(h), _ptr(dense), _ptr(indices),
                                    _ptr(offsets), _ptr(out), batch, _stream(stream)),
            "dlrm_forward_host")
+
+
+def dlrm_forward_noalloc(ln_bot: Sequence[int], ln_top: Sequence[int], tables: Sequence,
+                         bot_w: Sequence, bot_b: Sequence, top_w: Sequence, top_b: Sequence,
+                         bag_size: int, dense, indices, offsets, out, err_flag=None,
+                         stream=None) -> None:
+    """The forward with no handle and no device allocation (fixed library scratch).
+
+    For callers that must not allocate device memory when they run the model.
+    Every tensor is a CUDA tensor the caller owns; weights are (out, in)
+    contiguous. Calls share one scratch array: serialise them (one stream).
+    """
+    k = len(tables)
+    d = int(tables[0].shape[1])
+    lb = (ctypes.c_int32 * len(ln_bot))(*ln_bot)
+    lt = (ctypes.c_int32 * len(ln_top))(*ln_top)
+    rows = (ctypes.c_int64 * k)(*[int(t.shape[0]) for t in tables])
+    cfg = _Config(len(ln_bot) - 1, lb, k, rows, d, len(ln_top) - 1, lt, bag_size,
+                  int(dense.shape[0]), MATH_FP32)
+
+    def arr(ts):
+        for t in ts:
+            if not (t.is_cuda and t.is_contiguous()):
+                raise ValueError("tables and parameters must be contiguous CUDA tensors")
+        return (ctypes.c_void_p * len(ts))(*[t.data_ptr() for t in ts])
+
+    _check(lib().dlrm_forward_noalloc(ctypes.byref(cfg), arr(tables), arr(bot_w), arr(bot_b),
+                                      arr(top_w), arr(top_b), _ptr(dense), _ptr(indices),
+                                      _ptr(offsets), _ptr(out), int(dense.shape[0]),
+                                      _ptr(err_flag), _stream(stream)),
+           "dlrm_forward_noalloc")
 
 
 def dlrm_get_error(h: int, stream=None) -> int:

@@ -169,6 +169,45 @@ int32_t dlrm_stage_times(dlrm_handle_t h, double* total_ms, int32_t capacity, in
  * borrowed tables). Null is a no-op. */
 void dlrm_destroy(dlrm_handle_t h);
 
+/* Size of the fixed scratch array behind dlrm_forward_noalloc (16 MiB). */
+#define DLRM_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* The same forward as dlrm_forward, for callers that cannot allocate device
+ * memory when they run it. No counterpart exists on the pages; this is a
+ * service of this library. Typical callers: a plug-in inside another
+ * framework whose caching allocator owns the GPU's memory (a raw cudaMalloc
+ * there bypasses its accounting and limits), a serving loop that must never
+ * take cudaMalloc's implicit device-wide synchronisation, or code that runs
+ * under a device-memory budget fixed at start-up.
+ *
+ * There is no handle: the caller passes the shape (cfg; cfg->math must be
+ * DLRM_MATH_FP32, cfg->max_batch is ignored), the DEVICE pointers of the
+ * tables and of the Linear weights (PyTorch (out, in) layout, contiguous) and
+ * biases, and the inputs and output exactly as for dlrm_forward. err_flag is
+ * an optional device int32 word into which the DLRM_ERRBIT_* bits of this
+ * call are OR-ed (it is never cleared here).
+ *
+ * Scratch: the bag sums, hidden activations and the interaction output live
+ * in one file-scope __device__ array of DLRM_NOALLOC_SCRATCH_BYTES, which
+ * every GPU that uses this entry point holds until the process exits. A
+ * batch whose scratch would exceed it is rejected with DLRM_ERR_UNSUPPORTED
+ * before anything is launched (the 2048-sample, 3-table, 512-wide model needs
+ * about 10 MiB). Nothing in the scratch has to start at zero: every value a
+ * call reads was written earlier in the same call. All calls share the one
+ * array, so calls whose work overlaps on the GPU (different streams, or
+ * different host threads, without ordering between them) race and corrupt
+ * each other's results: serialise them, e.g. on one stream.
+ * Set-up: the first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, once per device, with that device current); make
+ * that first call before any stream capture. The call allocates nothing:
+ * no cudaMalloc, cudaFree or allocating library routine. */
+dlrm_status_t dlrm_forward_noalloc(const dlrm_config_t* cfg, const float* const* tables,
+                                   const float* const* bot_w, const float* const* bot_b,
+                                   const float* const* top_w, const float* const* top_b,
+                                   const float* dense, const int64_t* indices,
+                                   const int64_t* offsets, float* out, int32_t batch,
+                                   int32_t* err_flag, void* stream);
+
 /* Multi-table EmbeddingBag sum in one launch ([P1] MultiTableEmbeddingBagSum;
  * [P4] LessonsLearned "EmbeddingBag translator gap"):
  *   out[b][t][:] = sum_{l < L} tables[t][indices[t][offsets[t][b] + l]][:]
