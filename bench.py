@@ -221,10 +221,28 @@ def stage_work(cfg, name, batch):
         return batch * k * (l - 1) * d, byts
     if name == "interaction":
         return 2 * batch * p * d, batch * f * d * 4 + batch * (d + p) * 4
+    if name == "fused":
+        return forward_work(cfg, batch)
     widths = cfg.ln_bot if name.startswith("bottom") else cfg.ln_top
     i = int(name[len("bottom"):] if name.startswith("bottom") else name[len("top"):])
     kin, nout = widths[i], widths[i + 1]
     return 2 * batch * kin * nout, 4 * (batch * kin + kin * nout + nout + batch * nout)
+
+
+def forward_work(cfg, batch):
+    """Algorithmic (flops, bytes) of one whole forward: every GEMM's 2*M*N*K, the
+    pair dots and bag adds; HBM bytes of the inputs, tables rows, weights and output."""
+    k, d, l = cfg.n_tables, cfg.emb_dim, cfg.bag_size
+    f = k + 1
+    p = f * (f - 1) // 2
+    flops = batch * k * (l - 1) * d + 2 * batch * p * d
+    w_bytes = 0
+    for widths in (cfg.ln_bot, cfg.ln_top):
+        for a, b in zip(widths[:-1], widths[1:]):
+            flops += 2 * batch * a * b
+            w_bytes += 4 * (a * b + b)
+    byts = batch * (k * l * d * 4 + k * l * 8 + k * 8 + cfg.n_dense * 4 + 4) + w_bytes
+    return flops, byts
 
 
 def gather_measure(torch, dl, synth, pk, steps=10):
@@ -294,6 +312,7 @@ def run_ours(args, rank, world, local_rank):
     flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
     n_stages = len(model.stage_names())
+    path_used = model.path
 
     def barrier():
         if dist is not None:
@@ -390,6 +409,30 @@ def run_ours(args, rank, world, local_rank):
     names, totals, calls = model.stage_times()
     model.set_profiling(False)
     stage_us = {n: t * 1e3 / max(calls, 1) for n, t in zip(names, totals)}
+
+    # per-phase device time of the fused kernel (%globaltimer stamps per tile)
+    phases_us = None
+    if path_used == dl.PATH_FUSED:
+        tiles = None
+        buf = torch.zeros(((cfg.batch + 7) // 8) * dl.TRACE_SLOTS, dtype=torch.int64, device=dev)
+        rows = model.set_phase_trace(buf)
+        tiles = (cfg.batch + rows - 1) // rows
+        pnames = model.phase_names()
+        acc = np.zeros(len(pnames))
+        span = 0.0
+        reps = 20
+        with torch.cuda.stream(stream):
+            for _ in range(reps):
+                flush_buf.zero_()
+                buf.zero_()
+                model.forward(dense, idx, off, out, stream=stream)
+                stream.synchronize()
+                t = buf.view(-1, dl.TRACE_SLOTS)[:tiles, :len(pnames) + 1].cpu().numpy()
+                acc += np.diff(t, axis=1).mean(axis=0) / 1e3
+                span += (t[:, -1].max() - t[:, 0].min()) / 1e3
+        model.set_phase_trace(None)
+        phases_us = {n: float(v / reps) for n, v in zip(pnames, acc)}
+        phases_us["kernel_span"] = span / reps
     dom = max(stage_us, key=stage_us.get)
     flops, byts = stage_work(cfg, dom, cfg.batch)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
@@ -408,11 +451,7 @@ def run_ours(args, rank, world, local_rank):
     roof["algorithmic_per_launch"] = flops if roof["bound"] == "alu" else byts
 
     # whole-forward roofline fraction (slower of HBM bytes and FP32 flops)
-    tot_flops = sum(stage_work(cfg, n, cfg.batch)[0] for n in names)
-    w_bytes = 4 * sum(a * b + b for a, b in zip(cfg.ln_bot[:-1], cfg.ln_bot[1:]))
-    w_bytes += 4 * sum(a * b + b for a, b in zip(cfg.ln_top[:-1], cfg.ln_top[1:]))
-    k, d, l = cfg.n_tables, cfg.emb_dim, cfg.bag_size
-    fwd_bytes = (cfg.batch * (k * l * d * 4 + k * l * 8 + k * 8 + cfg.n_dense * 4 + 4) + w_bytes)
+    tot_flops, fwd_bytes = forward_work(cfg, cfg.batch)
     t_roof = max(fwd_bytes / (pk["hbm_gbs"] * 1e9), tot_flops / (fp32_peak * 1e12))
     forward_roofline = dict(algorithmic_flops=tot_flops, algorithmic_bytes=fwd_bytes,
                             roofline_us=t_roof * 1e6, frac=t_roof / (ms_per_step * 1e-3),
@@ -445,9 +484,12 @@ def run_ours(args, rank, world, local_rank):
                     tables=cfg.n_tables, rows=cfg.rows[0], emb_dim=cfg.emb_dim,
                     bag_size=cfg.bag_size, ln_bot=list(cfg.ln_bot), ln_top=list(cfg.ln_top),
                     math="fp32", l2="flushed before every step (256 MB write)",
+                    plan={dl.PATH_FUSED: "fused single launch",
+                          dl.PATH_LAYERWISE: "layer-wise launches"}[path_used],
                     parallelism="replicas" if world > 1 else "single GPU"),
         e2e=e2e, gpu_launches=args.steps * n_stages, clocks=clock_info,
         roofline=roof, forward_roofline=forward_roofline, stages_us=stage_us,
+        fused_phases_us=phases_us,
         graph=dict(us_per_batch_median=graph_us, samples_per_s=cfg.batch / (graph_us * 1e-6)),
         cpu_baseline=cpu)
     line["gather_b65536_k26_zipf"] = gather

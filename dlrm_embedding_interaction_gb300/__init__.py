@@ -16,6 +16,7 @@ LIB_PATH = os.path.join(_HERE, "libdlrm_gb300.so")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_OOM, ERR_INDEX_OOB, ERR_TIMEOUT = range(7)
 MATH_FP32, MATH_TF32, MATH_BF16 = 0, 1, 2
+PATH_AUTO, PATH_LAYERWISE, PATH_FUSED = 0, 1, 2
 ACT_NONE, ACT_RELU, ACT_SIGMOID = 0, 1, 2
 ERRBIT_INDEX_OOB = 1 << ERR_INDEX_OOB
 ERRBIT_OFFSETS = 1 << ERR_UNSUPPORTED
@@ -25,11 +26,12 @@ MAX_LAYERS = 16
 # Every symbol include/dlrm.h declares.
 EXPORTS = ("dlrm_version", "dlrm_status_string", "dlrm_create", "dlrm_forward",
            "dlrm_forward_host", "dlrm_get_error", "dlrm_workspace_bytes", "dlrm_destroy",
-           "dlrm_num_stages", "dlrm_stage_name", "dlrm_set_profiling", "dlrm_stage_times",
-           "dlrm_forward_noalloc",
+           "dlrm_path", "dlrm_num_stages", "dlrm_stage_name", "dlrm_set_profiling", "dlrm_stage_times",
+           "dlrm_forward_noalloc", "dlrm_set_phase_trace",
            "embedding_bag_sum_multi", "pairwise_dot_lower_tri", "pairwise_pair_map",
            "linear_bias_act")
 NOALLOC_SCRATCH_BYTES = 16 << 20
+TRACE_SLOTS = 40
 
 _lib = None
 
@@ -46,7 +48,7 @@ class _Config(ctypes.Structure):
                 ("n_tables", ctypes.c_int32), ("rows", ctypes.POINTER(ctypes.c_int64)),
                 ("emb_dim", ctypes.c_int32), ("n_top", ctypes.c_int32),
                 ("ln_top", ctypes.POINTER(ctypes.c_int32)), ("bag_size", ctypes.c_int32),
-                ("max_batch", ctypes.c_int32), ("math", ctypes.c_int)]
+                ("max_batch", ctypes.c_int32), ("math", ctypes.c_int), ("path", ctypes.c_int32)]
 
 
 def _bind(lib):
@@ -61,12 +63,14 @@ def _bind(lib):
         "dlrm_get_error": ([vp, vp], st),
         "dlrm_workspace_bytes": ([vp], i64),
         "dlrm_destroy": ([vp], None),
+        "dlrm_path": ([vp], i32),
         "dlrm_num_stages": ([vp], i32),
         "dlrm_stage_name": ([vp, i32], ctypes.c_char_p),
         "dlrm_set_profiling": ([vp, i32], st),
         "dlrm_stage_times": ([vp, ctypes.c_void_p, i32, ctypes.POINTER(i64)], i32),
         "dlrm_forward_noalloc": ([ctypes.POINTER(_Config), vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                   i32, vp, vp], st),
+        "dlrm_set_phase_trace": ([vp, vp, i64, ctypes.POINTER(i32)], st),
         "embedding_bag_sum_multi": ([vp, vp, i32, i32, vp, vp, i32, i32, vp, vp, vp], st),
         "pairwise_dot_lower_tri": ([vp, i32, vp, i32, i32, i32, vp, i32, i32, vp], st),
         "pairwise_pair_map": ([i32, vp, vp, vp], st),
@@ -221,7 +225,8 @@ def linear_bias_act(x, w, bias, y, act: int = ACT_NONE, math: int = MATH_FP32,
 
 def dlrm_create(ln_bot: Sequence[int], ln_top: Sequence[int], tables: Sequence,
                 bot_w: Sequence, bot_b: Sequence, top_w: Sequence, top_b: Sequence,
-                bag_size: int, max_batch: int, math: int = MATH_FP32) -> int:
+                bag_size: int, max_batch: int, math: int = MATH_FP32,
+                path: int = PATH_AUTO) -> int:
     """Build a forward plan; returns the opaque handle (an int).
 
     ``tables`` are CUDA tensors the handle borrows (keep them alive); the MLP
@@ -233,7 +238,7 @@ def dlrm_create(ln_bot: Sequence[int], ln_top: Sequence[int], tables: Sequence,
     lt = (ctypes.c_int32 * len(ln_top))(*ln_top)
     rows = (ctypes.c_int64 * k)(*[int(t.shape[0]) for t in tables])
     cfg = _Config(len(ln_bot) - 1, lb, k, rows, d, len(ln_top) - 1, lt, bag_size, max_batch,
-                  math)
+                  math, path)
 
     def arr(ts):
         for t in ts:
@@ -277,7 +282,7 @@ def dlrm_forward_noalloc(ln_bot: Sequence[int], ln_top: Sequence[int], tables: S
     lt = (ctypes.c_int32 * len(ln_top))(*ln_top)
     rows = (ctypes.c_int64 * k)(*[int(t.shape[0]) for t in tables])
     cfg = _Config(len(ln_bot) - 1, lb, k, rows, d, len(ln_top) - 1, lt, bag_size,
-                  int(dense.shape[0]), MATH_FP32)
+                  int(dense.shape[0]), MATH_FP32, PATH_AUTO)
 
     def arr(ts):
         for t in ts:
@@ -298,6 +303,10 @@ def dlrm_get_error(h: int, stream=None) -> int:
 
 def dlrm_workspace_bytes(h: int) -> int:
     return int(lib().dlrm_workspace_bytes(ctypes.c_void_p(h)))
+
+
+def dlrm_path(h: int) -> int:
+    return int(lib().dlrm_path(ctypes.c_void_p(h)))
 
 
 def dlrm_num_stages(h: int) -> int:
@@ -332,12 +341,12 @@ class DlrmModel:
     """Owns a forward plan and keeps the borrowed tables alive."""
 
     def __init__(self, ln_bot, ln_top, tables, bot_w, bot_b, top_w, top_b, bag_size: int,
-                 max_batch: int, math: int = MATH_FP32):
+                 max_batch: int, math: int = MATH_FP32, path: int = PATH_AUTO):
         self.tables = list(tables)
         self.ln_bot, self.ln_top = tuple(ln_bot), tuple(ln_top)
         self.bag_size, self.max_batch, self.math = bag_size, max_batch, math
         self.handle = dlrm_create(ln_bot, ln_top, self.tables, bot_w, bot_b, top_w, top_b,
-                                  bag_size, max_batch, math)
+                                  bag_size, max_batch, math, path)
 
     def forward(self, dense, indices, offsets, out=None, stream=None):
         import torch
@@ -356,6 +365,10 @@ class DlrmModel:
     def workspace_bytes(self) -> int:
         return dlrm_workspace_bytes(self.handle)
 
+    @property
+    def path(self) -> int:
+        return dlrm_path(self.handle)
+
     def stage_names(self):
         return [dlrm_stage_name(self.handle, i) for i in range(dlrm_num_stages(self.handle))]
 
@@ -364,6 +377,21 @@ class DlrmModel:
 
     def stage_times(self):
         return dlrm_stage_times(self.handle)
+
+    def set_phase_trace(self, buf) -> int:
+        """Fused plan only: per-tile phase stamps into ``buf`` (int64 CUDA tensor of at
+        least tiles * TRACE_SLOTS words) or off with None; returns the tile height."""
+        rows = ctypes.c_int32()
+        cap = 0 if buf is None else buf.numel()
+        _check(lib().dlrm_set_phase_trace(ctypes.c_void_p(self.handle), _ptr(buf), cap,
+                                          ctypes.byref(rows)), "dlrm_set_phase_trace")
+        return rows.value
+
+    def phase_names(self):
+        """Names of the trace phases 1.. (slot 0 is the kernel start)."""
+        nb, nt = len(self.ln_bot) - 1, len(self.ln_top) - 1
+        return (["prologue"] + [f"bottom{l}" for l in range(nb)] + ["interaction"]
+                + [f"top{l}" for l in range(nt - 1)] + [f"top{nt - 1}_sigmoid"])
 
     def close(self):
         if self.handle:

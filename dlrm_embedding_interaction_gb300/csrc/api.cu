@@ -16,6 +16,7 @@
 #include <vector>
 
 #include "common.cuh"
+#include "fused.cuh"
 
 namespace dlrm {
 
@@ -85,6 +86,11 @@ struct dlrm_handle_s {
   float* out_stage = nullptr;
   void* arena = nullptr;
   size_t arena_bytes = 0;
+  // kernel plan
+  int path = DLRM_PATH_LAYERWISE;
+  int fused_bm = 0;
+  dlrm::FusedParams fused{};     // per-call fields filled by run_forward
+  unsigned long long* trace = nullptr;
   // per-stage profiling (dlrm_set_profiling)
   std::vector<std::string> stage_names;
   std::vector<cudaEvent_t> events;      // stage boundaries, empty when off
@@ -121,6 +127,19 @@ dlrm_status_t run_forward(dlrm_handle_t h, const float* dense, const int64_t* in
     return !prof || cudaEventRecord(h->events[stage++], s) == cudaSuccess;
   };
   if (!mark()) return DLRM_ERR_CUDA;
+  if (h->path == DLRM_PATH_FUSED) {
+    // the whole forward in one launch
+    dlrm::FusedParams p = h->fused;
+    p.batch = batch;
+    p.dense = dense;
+    p.indices = indices;
+    p.offsets = offsets;
+    p.out = out;
+    p.err = h->err;
+    p.trace = h->trace;
+    e = dlrm::launch_fused(p, h->fused_bm, s);
+    if (e != cudaSuccess || !mark()) return DLRM_ERR_CUDA;
+  } else {
   // [G] bag sums, all tables in one launch
   e = dlrm::launch_gather(h->tabs, h->k, h->d, indices, offsets, batch, h->bag, h->emb, h->d,
                           h->err, s);
@@ -153,6 +172,7 @@ dlrm_status_t run_forward(dlrm_handle_t h, const float* dense, const int64_t* in
     in = o;
     ld_in = ld_o;
   }
+  }  // layer-wise
   if (prof) {
     if (cudaEventSynchronize(h->events.back()) != cudaSuccess) return DLRM_ERR_CUDA;
     for (size_t i = 0; i + 1 < h->events.size(); ++i) {
@@ -169,6 +189,30 @@ dlrm_status_t run_forward(dlrm_handle_t h, const float* dense, const int64_t* in
 void destroy_events(dlrm_handle_t h) {
   for (cudaEvent_t ev : h->events) cudaEventDestroy(ev);
   h->events.clear();
+}
+
+// Host copies of the (out, in) weights and biases (host or device pointers,
+// read with cudaMemcpyDefault), bottom layers then top, for the fused planner.
+bool host_params(dlrm_handle_t h, const float* const* bot_w, const float* const* bot_b,
+                 const float* const* top_w, const float* const* top_b,
+                 std::vector<std::vector<float>>* w, std::vector<std::vector<float>>* b) {
+  w->clear();
+  b->clear();
+  for (int side = 0; side < 2; ++side) {
+    const std::vector<int>& ln = side == 0 ? h->ln_bot : h->ln_top;
+    const float* const* ws = side == 0 ? bot_w : top_w;
+    const float* const* bs = side == 0 ? bot_b : top_b;
+    for (size_t l = 0; l + 1 < ln.size(); ++l) {
+      w->emplace_back(static_cast<size_t>(ln[l]) * ln[l + 1]);
+      b->emplace_back(ln[l + 1]);
+      if (cudaMemcpy(w->back().data(), ws[l], w->back().size() * sizeof(float),
+                     cudaMemcpyDefault) != cudaSuccess ||
+          cudaMemcpy(b->back().data(), bs[l], b->back().size() * sizeof(float),
+                     cudaMemcpyDefault) != cudaSuccess)
+        return false;
+    }
+  }
+  return true;
 }
 
 }  // namespace
@@ -240,10 +284,44 @@ dlrm_status_t dlrm_create(const dlrm_config_t* cfg, const float* const* tables,
     h->tabs.ptr[t] = tables[t];
     h->tabs.rows[t] = cfg->rows[t];
   }
-  h->stage_names.push_back("gather");
-  for (int l = 0; l < h->n_bot; ++l) h->stage_names.push_back("bottom" + std::to_string(l));
-  h->stage_names.push_back("interaction");
-  for (int l = 0; l < h->n_top; ++l) h->stage_names.push_back("top" + std::to_string(l));
+  // Kernel plan.
+  dlrm::FusedPlan fplan;
+  bool fused_fits = false;
+  if (cfg->path != DLRM_PATH_LAYERWISE && h->math == DLRM_MATH_FP32) {
+    std::vector<std::vector<float>> hw, hb;
+    if (!host_params(h, bot_w, bot_b, top_w, top_b, &hw, &hb)) {
+      cudaGetLastError();
+      delete h;
+      return DLRM_ERR_CUDA;
+    }
+    fused_fits = dlrm::fused_plan(h->n_dense, h->k, h->d, h->bag, h->ln_bot, h->ln_top, hw, hb,
+                                  h->tabs, dlrm::device_max_smem_optin(), &fplan);
+    h->fused_bm = fplan.bm;
+  }
+  const int64_t tiles = fused_fits ? (h->max_batch + h->fused_bm - 1) / h->fused_bm : 0;
+  if (cfg->path == DLRM_PATH_FUSED) {
+    if (!fused_fits) {
+      delete h;
+      return DLRM_ERR_UNSUPPORTED;
+    }
+    h->path = DLRM_PATH_FUSED;
+  } else if (cfg->path == DLRM_PATH_AUTO) {
+    h->path = (fused_fits && tiles <= 2 * dlrm::device_sm_count()) ? DLRM_PATH_FUSED
+                                                                   : DLRM_PATH_LAYERWISE;
+  } else if (cfg->path == DLRM_PATH_LAYERWISE) {
+    h->path = DLRM_PATH_LAYERWISE;
+  } else {
+    delete h;
+    return DLRM_ERR_INVALID_ARG;
+  }
+  if (h->path == DLRM_PATH_FUSED) {
+    h->stage_names.push_back("fused");
+  } else {
+    h->stage_names.push_back("gather");
+    for (int l = 0; l < h->n_bot; ++l) h->stage_names.push_back("bottom" + std::to_string(l));
+    h->stage_names.push_back("interaction");
+    for (int l = 0; l < h->n_top; ++l) h->stage_names.push_back("top" + std::to_string(l));
+  }
   h->stage_ms.assign(h->stage_names.size(), 0.0);
 
   // Layout of the arena.
@@ -276,6 +354,12 @@ dlrm_status_t dlrm_create(const dlrm_config_t* cfg, const float* const* tables,
   const size_t off_idx = plan.take<int64_t>(mb * h->k * h->bag);
   const size_t off_off = plan.take<int64_t>(mb * h->k);
   const size_t off_out = plan.take<float>(mb);
+  size_t off_fw = 0, off_fb = 0, off_fl = 0;      // fused weight stream, biases, last layer
+  if (h->path == DLRM_PATH_FUSED) {
+    off_fw = plan.take<float>(fplan.wstream.size());
+    off_fb = plan.take<float>(fplan.bias.size());
+    off_fl = plan.take<float>(fplan.wlast.size());
+  }
 
   if (cudaMalloc(&h->arena, plan.bytes) != cudaSuccess) {
     cudaGetLastError();
@@ -305,6 +389,21 @@ dlrm_status_t dlrm_create(const dlrm_config_t* cfg, const float* const* tables,
     if (st == DLRM_OK)
       st = cuda_status(cudaMemcpy(at(off_tb[l]), top_b[l], h->ln_top[l + 1] * sizeof(float),
                                   cudaMemcpyDefault));
+  }
+  if (h->path == DLRM_PATH_FUSED && st == DLRM_OK) {
+    st = cuda_status(cudaMemcpy(at(off_fw), fplan.wstream.data(),
+                                fplan.wstream.size() * sizeof(float), cudaMemcpyHostToDevice));
+    if (st == DLRM_OK)
+      st = cuda_status(cudaMemcpy(at(off_fb), fplan.bias.data(), fplan.bias.size() * sizeof(float),
+                                  cudaMemcpyHostToDevice));
+    if (st == DLRM_OK)
+      st = cuda_status(cudaMemcpy(at(off_fl), fplan.wlast.data(),
+                                  fplan.wlast.size() * sizeof(float), cudaMemcpyHostToDevice));
+    h->fused = fplan.params;
+    h->fused.wstream = at(off_fw);
+    h->fused.bias = at(off_fb);
+    h->fused.wlast = at(off_fl);
+    if (st == DLRM_OK) st = cuda_status(dlrm::fused_prepare(h->fused_bm));
   }
   if (st == DLRM_OK) st = cuda_status(cudaDeviceSynchronize());
   if (st != DLRM_OK) {
@@ -372,6 +471,24 @@ dlrm_status_t dlrm_get_error(dlrm_handle_t h, void* stream) {
 
 int64_t dlrm_workspace_bytes(dlrm_handle_t h) {
   return h ? static_cast<int64_t>(h->arena_bytes) : 0;
+}
+
+int32_t dlrm_path(dlrm_handle_t h) { return h ? h->path : -1; }
+
+dlrm_status_t dlrm_set_phase_trace(dlrm_handle_t h, uint64_t* buf, int64_t capacity,
+                                   int32_t* tile_rows) {
+  static_assert(DLRM_TRACE_SLOTS == dlrm::kFusedTraceSlots, "trace slot count");
+  if (!h) return DLRM_ERR_INVALID_ARG;
+  if (h->path != DLRM_PATH_FUSED) return DLRM_ERR_UNSUPPORTED;
+  if (tile_rows) *tile_rows = h->fused_bm;
+  if (!buf) {
+    h->trace = nullptr;
+    return DLRM_OK;
+  }
+  const int64_t tiles = (h->max_batch + h->fused_bm - 1) / h->fused_bm;
+  if (capacity < tiles * DLRM_TRACE_SLOTS) return DLRM_ERR_INVALID_ARG;
+  h->trace = reinterpret_cast<unsigned long long*>(buf);
+  return DLRM_OK;
 }
 
 int32_t dlrm_num_stages(dlrm_handle_t h) {

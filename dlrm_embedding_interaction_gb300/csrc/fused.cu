@@ -1,0 +1,711 @@
+// Fused single-launch DLRMv1 forward (fp32).
+//
+// One CTA runs the whole forward for a tile of BM samples (Luminal compare
+// dlrm-fused-kernels...dlrm-pt2-megakernel, dlrm_megakernel.rs steps 1-6:
+// bottom Linear+ReLU on every layer, lookups, i-major pairwise dots with
+// Vec[0] = x, R = [x, z], top Linear+ReLU then Linear+sigmoid).
+//
+// The pages' megakernel keeps one batch row per thread with activations in
+// registers; at 512-wide layers that cannot hold. Here the tile's activations
+// stay in shared memory for the whole forward and every layer is a CTA-wide
+// GEMM, with the work split by warp role:
+//  * one producer warp streams the weights of all layers, back to back, into
+//    a ring of 32 KB stages with 1-D bulk async copies (cp.async.bulk)
+//    completing on mbarriers. The stream is pre-packed at create time in
+//    consumption order, each stage one contiguous block whose 16-byte chunks
+//    are XOR-swizzled so the consumers' reads are bank-conflict free. The
+//    producer runs ahead across layer boundaries: no pipeline refill per layer.
+//  * eight consumer warps compute. A warp owns a 64-column tile; a thread owns
+//    BM/4 rows x 8 columns (rows lm + 4i, columns ln + 8j) and reads both
+//    operands with 128-bit shared loads (12 loads per 128 FFMA), ordering the
+//    FMAs component-outer so 8*BM/4 independent accumulators separate
+//    dependent ones. Layers narrower than 512 columns split K across warps
+//    (ksplit = 8 / column tiles) and reduce the partial sums in place in the
+//    output buffer.
+//  * biases, the last layer's weights and (bag size 1) the tile's embedding
+//    rows are fetched with cp.async at kernel start and land during the
+//    bottom MLP; bag sums and pair dots then run from shared memory and build
+//    R = [x, z] in place; the N = 1 sigmoid layer is a warp-per-row dot.
+// Every mbarrier wait is bounded (%globaltimer, 2 s): on expiry the kernel
+// sets DLRM_ERRBIT_TIMEOUT, stops waiting, finishes its control flow and the
+// producer waits (bounded) for its copies in flight before exiting.
+// Rows past the batch are computed on zeros and never stored.
+#include <atomic>
+
+#include "common.cuh"
+#include "fused.cuh"
+
+namespace dlrm {
+namespace {
+
+constexpr int kConsumers = kFusedConsumerWarps * kWarp;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Phase trace (profiling): the consumer leader stamps when the tile finishes
+// phase `slot`.
+__device__ __forceinline__ void stamp(const FusedParams& p, int slot) {
+  if (p.trace && threadIdx.x == 0)
+    p.trace[static_cast<size_t>(blockIdx.x) * kFusedTraceSlots + slot] = global_ns();
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(dst)), "l"(src));
+}
+
+// 16 zero bytes (src-size 0: nothing is read from src).
+__device__ __forceinline__ void cp_async16_zero(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, 0;\n" ::"r"(smem_u32(dst)), "l"(src));
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+}
+
+// Bounded wait for the phase with the given parity. Returns false when this or
+// another thread gave up (abort raised); the caller then carries on without
+// the data so every named barrier is still reached.
+__device__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  if (*abort_flag) return false;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 31) == 0) {
+      if (*abort_flag) return false;
+      if (global_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        if (err) atomicOr(reinterpret_cast<unsigned int*>(err), DLRM_ERRBIT_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ int gemm_rows(const FusedGemm& L, int pass) {
+  if (L.ksplit > 1) return L.n_pad;
+  const int left = L.n_pad / 64 - pass * kFusedConsumerWarps;
+  return 64 * (left < kFusedConsumerWarps ? left : kFusedConsumerWarps);
+}
+
+// ---------------------------------------------------------------- producer
+
+__device__ void produce(const FusedParams& p, float* stages, uint64_t* full, uint64_t* empty,
+                        volatile int* abort_flag) {
+  const uint32_t s_count = static_cast<uint32_t>(p.stages);
+  const float* src = p.wstream;
+  uint32_t it = 0;
+  bool ok = true;
+  for (int g = 0; g < p.n_gemm && ok; ++g) {
+    const FusedGemm& L = p.gemm[g];
+    const int ks = 16 * L.ksplit;
+    for (int pass = 0; pass < L.passes && ok; ++pass) {
+      const int rows = gemm_rows(L, pass);
+      const uint32_t bytes = static_cast<uint32_t>(rows * ks) * 4u;
+      for (int kst = 0; kst < L.n_kst; ++kst) {
+        const uint32_t slot = it % s_count;
+        if (it >= s_count &&
+            !wait_phase(smem_u32(&empty[slot]), ((it / s_count) - 1) & 1, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(smem_u32(&full[slot]), bytes);
+        bulk_g2s(smem_u32(stages + slot * kFusedStageFloats), src, bytes, smem_u32(&full[slot]));
+        src += rows * ks;
+        ++it;
+      }
+    }
+  }
+  // The copies still in flight must land before this CTA's shared memory is
+  // released: wait (bounded, regardless of abort) for the last stages issued.
+  const uint32_t first = it > s_count ? it - s_count : 0;
+  for (uint32_t j = first; j < it; ++j) {
+    const uint32_t bar = smem_u32(&full[j % s_count]);
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, (j / s_count) & 1)) {
+      if (global_ns() - t0 > kWaitLimitNs) {
+        if (p.err) atomicOr(reinterpret_cast<unsigned int*>(p.err), DLRM_ERRBIT_TIMEOUT);
+        break;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- consumers
+
+// C (BM x n_pad; zero beyond n) = act(A (BM x k_pad) W^T + b). `it` is the
+// stage counter shared with the producer's sequence. KSPLIT is a template
+// argument so the stage row length and the j offsets are immediates.
+template <int BM, int KSPLIT>
+__device__ void gemm_layer(const FusedGemm& L, const float* __restrict__ a_s, float* __restrict__ c_s,
+                           int lda, const float* __restrict__ bias_s, int act,
+                           const float* __restrict__ stages, uint64_t* full, uint64_t* empty,
+                           uint32_t& it, uint32_t s_count, volatile int* abort_flag, int32_t* err) {
+  constexpr int TM = BM / 4;
+  constexpr int ksplit = KSPLIT;
+  constexpr int KS = 16 * KSPLIT;
+  constexpr int NACT = kFusedConsumerWarps / KSPLIT;
+  const int tid = threadIdx.x;
+  const int warp = tid / kWarp;
+  const int lane = tid % kWarp;
+  const int lm = lane / 8;
+  const int ln = lane % 8;
+  const int ct = warp % NACT;
+  const int kslice = warp / NACT;
+  const int sw = (KS == 16) ? ((ln >> 1) & 3) : ln;     // chunk swizzle of this thread's rows
+  int ph[4];
+#pragma unroll
+  for (int s = 0; s < 4; ++s) ph[s] = ((kslice * 4 + s) ^ sw) * 4;
+  const int wj = 8 * KS;                                 // row distance of the j columns
+  const float* a_row = a_s + lm * lda + kslice * 16;
+
+  for (int pass = 0; pass < L.passes; ++pass) {
+    const int tiles_here = gemm_rows(L, pass) / 64;
+    const bool active = ct < tiles_here;
+    float acc[TM][8];
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+
+    for (int kst = 0; kst < L.n_kst; ++kst, ++it) {
+      const uint32_t slot = it % s_count;
+      wait_phase(smem_u32(&full[slot]), (it / s_count) & 1, abort_flag, err);
+      if (active) {
+        const float* ws = stages + slot * kFusedStageFloats + (ct * 64 + ln) * KS;
+        const float* as = a_row + kst * KS;
+        float4 av[2][TM], wv[2][8];
+#pragma unroll
+        for (int i = 0; i < TM; ++i) av[0][i] = *reinterpret_cast<const float4*>(as + 4 * i * lda);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          wv[0][j] = *reinterpret_cast<const float4*>(ws + j * wj + ph[0]);
+#pragma unroll
+        for (int step = 0; step < 4; ++step) {
+          const int cur = step & 1;
+          if (step < 3) {
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
+              av[cur ^ 1][i] = *reinterpret_cast<const float4*>(as + 4 * i * lda + 4 * (step + 1));
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              wv[cur ^ 1][j] = *reinterpret_cast<const float4*>(ws + j * wj + ph[step + 1]);
+          }
+#pragma unroll
+          for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[cur][i].x, wv[cur][j].x, acc[i][j]);
+#pragma unroll
+          for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[cur][i].y, wv[cur][j].y, acc[i][j]);
+#pragma unroll
+          for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[cur][i].z, wv[cur][j].z, acc[i][j]);
+#pragma unroll
+          for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[cur][i].w, wv[cur][j].w, acc[i][j]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
+    }
+
+    const int col0 = pass * kFusedConsumerWarps * 64;
+    if (ksplit == 1) {
+      if (active) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int n = col0 + ct * 64 + ln + 8 * j;
+          const float bv = bias_s[L.b_off + n];
+#pragma unroll
+          for (int i = 0; i < TM; ++i) {
+            const float v = apply_act(acc[i][j] + bv, act);
+            c_s[(lm + 4 * i) * lda + n] = (n < L.n) ? v : 0.f;
+          }
+        }
+      }
+    } else {
+      // partial sums of k-slice s go to columns [s * n_pad, (s + 1) * n_pad)
+#pragma unroll
+      for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          c_s[(lm + 4 * i) * lda + kslice * L.n_pad + ct * 64 + ln + 8 * j] = acc[i][j];
+      consumer_sync();
+      const int np = L.n_pad;
+      for (int e = tid; e < BM * np; e += kConsumers) {
+        const int m = e / np;
+        const int n = e - m * np;
+        float v = 0.f;
+        for (int s = 0; s < ksplit; ++s) v += c_s[m * lda + s * np + n];
+        v = apply_act(v + bias_s[L.b_off + n], act);
+        c_s[m * lda + n] = (n < L.n) ? v : 0.f;
+      }
+    }
+    consumer_sync();
+  }
+}
+
+template <int BM>
+__device__ void gemm_dispatch(const FusedGemm& L, const float* a_s, float* c_s, int lda,
+                              const float* bias_s, int act, int zero_to, const float* stages,
+                              uint64_t* full, uint64_t* empty, uint32_t& it, uint32_t s_count,
+                              volatile int* abort_flag, int32_t* err) {
+  switch (L.ksplit) {
+    case 1:
+      gemm_layer<BM, 1>(L, a_s, c_s, lda, bias_s, act, stages, full, empty, it, s_count, abort_flag, err);
+      break;
+    case 2:
+      gemm_layer<BM, 2>(L, a_s, c_s, lda, bias_s, act, stages, full, empty, it, s_count, abort_flag, err);
+      break;
+    case 4:
+      gemm_layer<BM, 4>(L, a_s, c_s, lda, bias_s, act, stages, full, empty, it, s_count, abort_flag, err);
+      break;
+    default:
+      gemm_layer<BM, 8>(L, a_s, c_s, lda, bias_s, act, stages, full, empty, it, s_count, abort_flag, err);
+      break;
+  }
+  const int extra = zero_to - L.n_pad;
+  for (int e = threadIdx.x; e < BM * extra; e += kConsumers) {
+    const int m = e / extra;
+    c_s[m * lda + L.n_pad + (e - m * extra)] = 0.f;
+  }
+  consumer_sync();
+}
+
+template <int BM>
+__device__ void consume(const FusedParams& p, float* stages, uint64_t* full, uint64_t* empty,
+                        volatile int* abort_flag, float* act0, float* act1, float* zs,
+                        float* bias_s, float* wlast_s) {
+  const int tid = threadIdx.x;
+  const int m0 = blockIdx.x * BM;
+  const int rows = min(BM, p.batch - m0);
+  const int k = p.k_tables, d = p.d, d4 = d / 4;
+  const int f = k + 1;
+  const int pairs = f * (f - 1) / 2;
+  bool oob = false, bad_off = false;
+
+  // Prologue: bias block + last-layer weights (group 0), then the tile's
+  // embedding rows when every bag is one row (group 1).
+  for (int c = tid; c < p.bias_floats / 4; c += kConsumers) cp_async16(bias_s + 4 * c, p.bias + 4 * c);
+  for (int c = tid; c < p.k_last / 4; c += kConsumers) cp_async16(wlast_s + 4 * c, p.wlast + 4 * c);
+  cp_async_commit();
+  if (p.prefetch_z) {
+    for (int e = tid; e < BM * k * d4; e += kConsumers) {
+      const int s = e / (k * d4);
+      const int rem = e - s * k * d4;
+      const int t = rem / d4;
+      const int c4 = rem - t * d4;
+      float* dst = zs + (s * k + t) * p.ldz + 4 * c4;
+      const float* table = p.tabs.ptr[t];
+      bool ok = false;
+      int64_t row = 0;
+      if (s < rows) {
+        const int64_t b = m0 + s;
+        const int64_t start = __ldg(p.offsets + static_cast<int64_t>(t) * p.batch + b);
+        row = __ldg(p.indices + static_cast<int64_t>(t) * p.batch + b);   // bag size 1
+        if (start != b) {
+          bad_off = true;
+        } else if (row < 0 || row >= p.tabs.rows[t]) {
+          oob = true;
+        } else {
+          ok = true;
+        }
+      }
+      if (ok) cp_async16(dst, table + row * d + 4 * c4);
+      else cp_async16_zero(dst, table);
+    }
+  }
+  cp_async_commit();
+
+  // dense features -> act0, zero-padded to the first layer's k_pad
+  {
+    const int kp = p.gemm[0].k_pad;
+    for (int e = tid; e < BM * kp; e += kConsumers) {
+      const int m = e / kp;
+      const int c = e - m * kp;
+      act0[m * p.lda + c] = (m < rows && c < p.n_dense)
+                                ? __ldg(p.dense + static_cast<int64_t>(m0 + m) * p.n_dense + c)
+                                : 0.f;
+    }
+  }
+  cp_async_wait<1>();
+  consumer_sync();
+  stamp(p, 1);
+
+  const uint32_t s_count = static_cast<uint32_t>(p.stages);
+  uint32_t it = 0;
+  float* in = act0;
+  float* out = act1;
+  for (int g = 0; g < p.n_bot; ++g) {
+    const int zero_to = (g + 1 < p.n_bot) ? p.gemm[g + 1].k_pad : p.gemm[g].n_pad;
+    gemm_dispatch<BM>(p.gemm[g], in, out, p.lda, bias_s, DLRM_ACT_RELU, zero_to, stages, full,
+                      empty, it, s_count, abort_flag, p.err);
+    float* t = in; in = out; out = t;
+    stamp(p, 2 + g);
+  }
+  const float* x = in;       // bottom output (BM, d)
+  float* r = out;            // R = [x, z]
+
+  // Interaction: R[m] = [x[m], z[m]], zero to the next layer's k_pad.
+  const int rk = (p.n_top > 1) ? p.gemm[p.n_bot].k_pad : p.k_last;
+  for (int e = tid; e < BM * rk; e += kConsumers) {
+    const int m = e / rk;
+    const int c = e - m * rk;
+    if (c < d) r[m * p.lda + c] = x[m * p.lda + c];
+    else if (c >= d + pairs) r[m * p.lda + c] = 0.f;
+  }
+  if (p.prefetch_z) cp_async_wait<0>();
+  for (int g0 = 0; g0 < BM; g0 += p.sg) {
+    const int ns = min(p.sg, BM - g0);
+    if (!p.prefetch_z) {
+      for (int e = tid; e < ns * k * d4; e += kConsumers) {
+        const int s = e / (k * d4);
+        const int rem = e - s * k * d4;
+        const int t = rem / d4;
+        const int c4 = rem - t * d4;
+        const int m = g0 + s;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (m < rows) {
+          const int64_t b = m0 + m;
+          const int64_t start = __ldg(p.offsets + static_cast<int64_t>(t) * p.batch + b);
+          if (start != b * p.bag) {
+            bad_off = true;
+          } else {
+            const int64_t* idx = p.indices + static_cast<int64_t>(t) * p.batch * p.bag + start;
+            const float4* table = reinterpret_cast<const float4*>(p.tabs.ptr[t]);
+            const int64_t nrows = p.tabs.rows[t];
+            for (int l = 0; l < p.bag; ++l) {
+              const int64_t row = __ldg(idx + l);
+              if (row >= 0 && row < nrows) {
+                const float4 u = __ldg(table + row * d4 + c4);
+                v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w;
+              } else {
+                oob = true;
+              }
+            }
+          }
+        }
+        *reinterpret_cast<float4*>(zs + (s * k + t) * p.ldz + 4 * c4) = v;
+      }
+    }
+    consumer_sync();
+    const float* zg = zs + (p.prefetch_z ? g0 * k * p.ldz : 0);
+    for (int e = tid; e < ns * pairs; e += kConsumers) {
+      const int s = e / pairs;
+      const int q = e - s * pairs;
+      int i, j;
+      pair_from_index(q, i, j);
+      const float* vi = (i == 0) ? x + (g0 + s) * p.lda : zg + (s * k + i - 1) * p.ldz;
+      const float* vj = (j == 0) ? x + (g0 + s) * p.lda : zg + (s * k + j - 1) * p.ldz;
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int c4 = 0; c4 < d4; ++c4) {
+        const float4 u = *reinterpret_cast<const float4*>(vi + 4 * c4);
+        const float4 w = *reinterpret_cast<const float4*>(vj + 4 * c4);
+        a.x = fmaf(u.x, w.x, a.x);
+        a.y = fmaf(u.y, w.y, a.y);
+        a.z = fmaf(u.z, w.z, a.z);
+        a.w = fmaf(u.w, w.w, a.w);
+      }
+      r[(g0 + s) * p.lda + d + q] = (a.x + a.y) + (a.z + a.w);
+    }
+    consumer_sync();
+  }
+  if (p.err) {
+    if (oob) atomicOr(reinterpret_cast<unsigned int*>(p.err), DLRM_ERRBIT_INDEX_OOB);
+    if (bad_off) atomicOr(reinterpret_cast<unsigned int*>(p.err), DLRM_ERRBIT_OFFSETS);
+  }
+
+  stamp(p, 2 + p.n_bot);
+  // Top MLP: ReLU layers, then the N = 1 sigmoid layer.
+  in = r;
+  out = (r == act0) ? act1 : act0;
+  for (int g = p.n_bot; g < p.n_gemm; ++g) {
+    const int zero_to = (g + 1 < p.n_gemm) ? p.gemm[g + 1].k_pad : p.k_last;
+    gemm_dispatch<BM>(p.gemm[g], in, out, p.lda, bias_s, DLRM_ACT_RELU, zero_to, stages, full,
+                      empty, it, s_count, abort_flag, p.err);
+    float* t = in; in = out; out = t;
+    stamp(p, 3 + g);
+  }
+  const int warp = tid / kWarp, lane = tid % kWarp;
+  const int k4 = p.k_last / 4;
+  const float bl = bias_s[p.b_last];
+  for (int m = warp; m < rows; m += kFusedConsumerWarps) {
+    float acc = 0.f;
+    for (int q = lane; q < k4; q += kWarp) {
+      const float4 a = *reinterpret_cast<const float4*>(in + m * p.lda + 4 * q);
+      const float4 w = *reinterpret_cast<const float4*>(wlast_s + 4 * q);
+      acc = fmaf(a.x, w.x, acc);
+      acc = fmaf(a.y, w.y, acc);
+      acc = fmaf(a.z, w.z, acc);
+      acc = fmaf(a.w, w.w, acc);
+    }
+#pragma unroll
+    for (int o = kWarp / 2; o > 0; o /= 2) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) p.out[m0 + m] = apply_act(acc + bl, DLRM_ACT_SIGMOID);
+  }
+  if (p.trace) {
+    consumer_sync();
+    stamp(p, 2 + p.n_gemm + 1);
+  }
+}
+
+template <int BM>
+__global__ void __launch_bounds__(kFusedThreads, 1)
+fused_forward_kernel(const __grid_constant__ FusedParams p) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  float* stages = reinterpret_cast<float*>(smem_raw);
+  float* act0 = reinterpret_cast<float*>(smem_raw + p.off_act0);
+  float* act1 = reinterpret_cast<float*>(smem_raw + p.off_act1);
+  float* zs = reinterpret_cast<float*>(smem_raw + p.off_z);
+  float* bias_s = reinterpret_cast<float*>(smem_raw + p.off_bias);
+  float* wlast_s = reinterpret_cast<float*>(smem_raw + p.off_wlast);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw + p.off_bar);
+  uint64_t* empty = full + p.stages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + p.stages);
+  const int warp = threadIdx.x / kWarp;
+  stamp(p, 0);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), kFusedConsumerWarps);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  __syncthreads();
+  if (warp == kFusedConsumerWarps) {
+    if (threadIdx.x % kWarp == 0) produce(p, stages, full, empty, abort_flag);
+    return;
+  }
+  consume<BM>(p, stages, full, empty, abort_flag, act0, act1, zs, bias_s, wlast_s);
+}
+
+template <int BM>
+cudaError_t enable_smem() {
+  static std::atomic<uint64_t> done{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(fused_forward_kernel<BM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(device_max_smem_optin()));
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
+}  // namespace
+
+cudaError_t fused_prepare(int bm) {
+  if (bm == 16) return enable_smem<16>();
+  if (bm == 8) return enable_smem<8>();
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_fused(const FusedParams& p, int bm, cudaStream_t stream) {
+  if (p.batch == 0) return cudaSuccess;
+  const unsigned grid = static_cast<unsigned>((p.batch + bm - 1) / bm);
+  cudaError_t e = fused_prepare(bm);
+  if (e != cudaSuccess) return e;
+  if (bm == 16)
+    fused_forward_kernel<16><<<grid, kFusedThreads, p.smem_bytes, stream>>>(p);
+  else
+    fused_forward_kernel<8><<<grid, kFusedThreads, p.smem_bytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- host plan
+
+namespace {
+
+int swizzle_of(int row, int ks) { return ks == 16 ? ((row >> 1) & 3) : (row & 7); }
+
+size_t align128(size_t x) { return (x + 127) / 128 * 128; }
+
+}  // namespace
+
+bool fused_plan(int n_dense, int k_tables, int d, int bag, const std::vector<int>& ln_bot,
+                const std::vector<int>& ln_top, const std::vector<std::vector<float>>& w,
+                const std::vector<std::vector<float>>& b, const GatherTables& tabs,
+                size_t smem_limit, FusedPlan* plan) {
+  const int n_bot = static_cast<int>(ln_bot.size()) - 1;
+  const int n_top = static_cast<int>(ln_top.size()) - 1;
+  const int n_gemm = n_bot + n_top - 1;
+  if (d % 4 != 0 || ln_top.back() != 1 || n_gemm > kFusedMaxGemm || n_bot < 1) return false;
+  for (int t = 0; t < k_tables; ++t)
+    if (reinterpret_cast<uintptr_t>(tabs.ptr[t]) % 16 != 0) return false;
+  FusedParams& p = plan->params;
+  p = FusedParams{};
+  p.n_dense = n_dense;
+  p.k_tables = k_tables;
+  p.d = d;
+  p.bag = bag;
+  p.n_bot = n_bot;
+  p.n_top = n_top;
+  p.n_gemm = n_gemm;
+  const int f = k_tables + 1;
+  const int pairs = f * (f - 1) / 2;
+
+  // layer shapes
+  std::vector<int> kin(n_gemm), nout(n_gemm);
+  for (int g = 0; g < n_gemm; ++g) {
+    kin[g] = g < n_bot ? ln_bot[g] : ln_top[g - n_bot];
+    nout[g] = g < n_bot ? ln_bot[g + 1] : ln_top[g - n_bot + 1];
+  }
+  int widest = 512;   // split-K partials span 512 columns
+  int bias_floats = 0;
+  for (int g = 0; g < n_gemm; ++g) {
+    FusedGemm& L = p.gemm[g];
+    int n_wt = (nout[g] + 63) / 64;
+    if (n_wt < kFusedConsumerWarps) {
+      int p2 = 1;
+      while (p2 < n_wt) p2 *= 2;
+      n_wt = p2;
+      L.ksplit = kFusedConsumerWarps / n_wt;
+      L.passes = 1;
+    } else {
+      L.ksplit = 1;
+      L.passes = (n_wt + kFusedConsumerWarps - 1) / kFusedConsumerWarps;
+    }
+    L.n = nout[g];
+    L.n_pad = 64 * n_wt;
+    L.k_pad = static_cast<int>(round_up(kin[g], 16 * L.ksplit));
+    L.n_kst = L.k_pad / (16 * L.ksplit);
+    L.b_off = bias_floats;
+    bias_floats += L.n_pad;
+    widest = std::max({widest, L.k_pad, L.n_pad});
+  }
+  p.k_last = static_cast<int>(round_up(ln_top[n_top - 1], 4));
+  p.b_last = bias_floats;
+  bias_floats += 4;
+  p.bias_floats = bias_floats;
+  widest = std::max({widest, p.k_last, d + pairs});
+  p.lda = static_cast<int>(round_up(widest, 32)) + 4;
+  p.ldz = static_cast<int>(round_up(d, 4)) + 4;
+
+  // shared-memory carve: stages | act0 | act1 | z | bias | wlast | barriers
+  const size_t per_sample_z = static_cast<size_t>(k_tables) * p.ldz * sizeof(float);
+  bool placed = false;
+  for (int bm : {16, 8}) {
+    for (int stages : {4, 3}) {
+      size_t off = static_cast<size_t>(stages) * kFusedStageFloats * sizeof(float);
+      const size_t act = align128(static_cast<size_t>(bm) * p.lda * sizeof(float));
+      const size_t tail = align128(bias_floats * sizeof(float)) +
+                          align128(p.k_last * sizeof(float)) + align128(2 * stages * 8 + 16);
+      const size_t fixed = off + 2 * act + tail;
+      if (fixed + per_sample_z > smem_limit) continue;
+      const int sg = static_cast<int>(std::min<size_t>(bm, (smem_limit - fixed) / per_sample_z));
+      if (sg < 1) continue;
+      p.stages = stages;
+      p.off_act0 = static_cast<int>(off);
+      p.off_act1 = static_cast<int>(off + act);
+      p.off_z = static_cast<int>(off + 2 * act);
+      const size_t zbytes = align128(static_cast<size_t>(sg) * per_sample_z);
+      p.off_bias = static_cast<int>(p.off_z + zbytes);
+      p.off_wlast = static_cast<int>(p.off_bias + align128(bias_floats * sizeof(float)));
+      p.off_bar = static_cast<int>(p.off_wlast + align128(p.k_last * sizeof(float)));
+      p.smem_bytes = static_cast<int>(p.off_bar + align128(2 * stages * 8 + 16));
+      p.sg = sg;
+      p.prefetch_z = (bag == 1 && sg == bm) ? 1 : 0;
+      plan->bm = bm;
+      placed = true;
+      break;
+    }
+    if (placed) break;
+  }
+  if (!placed || static_cast<size_t>(p.smem_bytes) > smem_limit) return false;
+
+  // packed weight stream, in the producer's order
+  plan->wstream.clear();
+  for (int g = 0; g < n_gemm; ++g) {
+    const FusedGemm& L = p.gemm[g];
+    const int ks = 16 * L.ksplit;
+    const std::vector<float>& W = w[g];
+    for (int pass = 0; pass < L.passes; ++pass) {
+      const int rows = (L.ksplit > 1) ? L.n_pad
+                                      : 64 * std::min(L.n_pad / 64 - pass * kFusedConsumerWarps,
+                                                      kFusedConsumerWarps);
+      for (int kst = 0; kst < L.n_kst; ++kst) {
+        const size_t base = plan->wstream.size();
+        plan->wstream.resize(base + static_cast<size_t>(rows) * ks, 0.f);
+        for (int rr = 0; rr < rows; ++rr) {
+          const int n = pass * kFusedConsumerWarps * 64 + rr;
+          if (n >= L.n) continue;
+          for (int kk = 0; kk < ks; ++kk) {
+            const int kg = kst * ks + kk;
+            if (kg >= kin[g]) break;
+            const int chunk = (kk / 4) ^ swizzle_of(rr, ks);
+            plan->wstream[base + static_cast<size_t>(rr) * ks + chunk * 4 + kk % 4] =
+                W[static_cast<size_t>(n) * kin[g] + kg];
+          }
+        }
+      }
+    }
+  }
+  plan->bias.assign(bias_floats, 0.f);
+  for (int g = 0; g < n_gemm; ++g)
+    for (int n = 0; n < nout[g]; ++n) plan->bias[p.gemm[g].b_off + n] = b[g][n];
+  plan->bias[p.b_last] = b[n_gemm][0];
+  plan->wlast.assign(p.k_last, 0.f);
+  for (int c = 0; c < ln_top[n_top - 1]; ++c) plan->wlast[c] = w[n_gemm][c];
+  p.tabs = tabs;
+  return true;
+}
+
+}  // namespace dlrm

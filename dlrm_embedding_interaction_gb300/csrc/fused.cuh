@@ -1,0 +1,75 @@
+// Parameter block and host planning of the fused single-launch forward
+// (fused.cu).
+#pragma once
+
+#include <vector>
+
+#include "common.cuh"
+
+namespace dlrm {
+
+constexpr int kFusedConsumerWarps = 8;
+constexpr int kFusedThreads = (kFusedConsumerWarps + 1) * 32;   // + one producer warp
+constexpr int kFusedStageFloats = 8192;                        // 32 KB weight stage
+constexpr int kFusedMaxGemm = 2 * DLRM_MAX_LAYERS;
+
+// One GEMM layer of the weight stream. Its weights occupy `passes * n_kst`
+// consecutive stages of the packed stream: pass p covers output rows
+// [512 p, 512 p + rows), stage s covers k in [s*KS, (s+1)*KS), KS = 16*ksplit,
+// stored row-major (rows x KS) with 16-byte chunk c of row r at position
+// c ^ swz(r) (swz = (r >> 1) & 3 when KS = 16, else r & 7).
+//   n      output width; n_pad = 64 * {1, 2, 4} (ksplit = 8, 4, 2) or a
+//          multiple of 64 >= 512 (ksplit = 1)
+//   k_pad  input width padded to a multiple of KS (zero weights)
+//   b_off  offset of the layer's zero-padded bias in the bias block
+struct FusedGemm {
+  int n, n_pad, k_pad, ksplit, passes, n_kst, b_off;
+};
+
+struct FusedParams {
+  int batch, n_dense, k_tables, d, bag, n_bot, n_top;
+  int n_gemm;        // n_bot + n_top - 1 (the last top layer is the N = 1 dot)
+  int lda;           // activation row stride (floats), >= 516, = 4 mod 32
+  int ldz;           // bag-sum row stride, round_up(d, 4) + 4
+  int sg;            // samples per gather/interaction group
+  int prefetch_z;    // 1: all BM samples' rows are fetched at kernel start (bag 1)
+  int stages;        // weight ring depth
+  int k_last;        // padded input width of the last (N = 1) layer
+  int b_last;        // its bias offset in the bias block
+  int bias_floats;   // bias block length (multiple of 4)
+  // shared-memory carve (bytes from the dynamic base)
+  int off_act0, off_act1, off_z, off_bias, off_wlast, off_bar;
+  int smem_bytes;
+  FusedGemm gemm[kFusedMaxGemm];
+  const float* wstream;    // packed weight stream
+  const float* bias;       // bias block
+  const float* wlast;      // last layer weights, k_last floats (zero-padded)
+  const float* dense;
+  const int64_t* indices;
+  const int64_t* offsets;
+  float* out;
+  int32_t* err;
+  unsigned long long* trace;   // optional phase stamps, kFusedTraceSlots per tile
+  GatherTables tabs;
+};
+
+constexpr int kFusedTraceSlots = 40;
+
+// Host plan: shapes, smem carve and the packed weight/bias images.
+struct FusedPlan {
+  FusedParams params{};
+  int bm = 0;
+  std::vector<float> wstream, bias, wlast;
+};
+
+// Builds the plan from host copies of the (out, in) weights and biases;
+// false when the model does not fit the fused kernel.
+bool fused_plan(int n_dense, int k_tables, int d, int bag, const std::vector<int>& ln_bot,
+                const std::vector<int>& ln_top, const std::vector<std::vector<float>>& w,
+                const std::vector<std::vector<float>>& b, const GatherTables& tabs,
+                size_t smem_limit, FusedPlan* plan);
+
+cudaError_t fused_prepare(int bm);
+cudaError_t launch_fused(const FusedParams& p, int bm, cudaStream_t stream);
+
+}  // namespace dlrm

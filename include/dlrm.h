@@ -51,6 +51,13 @@ typedef enum {
  * TMEM (opt-in; results within rel 2e-2 of fp32). */
 typedef enum { DLRM_MATH_FP32 = 0, DLRM_MATH_TF32 = 1, DLRM_MATH_BF16 = 2 } dlrm_math_t;
 
+/* Kernel plan of a forward handle. AUTO takes the fused single-launch forward
+ * when the shape fits it (activations of a tile of samples resident in shared
+ * memory) and the batch is at most two waves of tiles, else the layer-wise
+ * launches; FUSED fails dlrm_create with DLRM_ERR_UNSUPPORTED when the shape
+ * does not fit; LAYERWISE always launches one kernel per step. */
+typedef enum { DLRM_PATH_AUTO = 0, DLRM_PATH_LAYERWISE = 1, DLRM_PATH_FUSED = 2 } dlrm_path_t;
+
 /* Epilogue activation of linear_bias_act. */
 typedef enum { DLRM_ACT_NONE = 0, DLRM_ACT_RELU = 1, DLRM_ACT_SIGMOID = 2 } dlrm_act_t;
 
@@ -71,7 +78,8 @@ typedef enum { DLRM_ACT_NONE = 0, DLRM_ACT_RELU = 1, DLRM_ACT_SIGMOID = 2 } dlrm
  *           F = n_tables + 1; ln_top[n_top] = 1. ReLU follows every top layer
  *           but the last, which is followed by a sigmoid.
  *   bag_size  L >= 1 indices per bag, uniform (offsets[t][b] = b * L).
- *   max_batch largest batch a forward call may pass; sizes the workspace. */
+ *   max_batch largest batch a forward call may pass; sizes the workspace.
+ *   path      kernel plan (dlrm_path_t); ignored by dlrm_forward_noalloc. */
 typedef struct {
   int32_t n_bot;
   const int32_t* ln_bot;
@@ -83,6 +91,7 @@ typedef struct {
   int32_t bag_size;
   int32_t max_batch;
   dlrm_math_t math;
+  int32_t path;
 } dlrm_config_t;
 
 typedef struct dlrm_handle_s* dlrm_handle_t;
@@ -145,6 +154,10 @@ dlrm_status_t dlrm_get_error(dlrm_handle_t h, void* stream);
 /* Bytes of device memory the handle owns (workspace + packed weights). */
 int64_t dlrm_workspace_bytes(dlrm_handle_t h);
 
+/* The plan the handle resolved at create time: DLRM_PATH_LAYERWISE or
+ * DLRM_PATH_FUSED (-1 for a null handle). */
+int32_t dlrm_path(dlrm_handle_t h);
+
 /* Number of kernel launches one dlrm_forward enqueues (its stages). */
 int32_t dlrm_num_stages(dlrm_handle_t h);
 
@@ -159,6 +172,20 @@ const char* dlrm_stage_name(dlrm_handle_t h, int32_t i);
  * and must not be used inside graph capture. enable = 0 destroys the events
  * and clears the totals. */
 dlrm_status_t dlrm_set_profiling(dlrm_handle_t h, int32_t enable);
+
+/* Phase trace of the fused plan (profiling; off by default). With a non-null
+ * device buffer of `capacity` uint64 words, every later dlrm_forward on a
+ * fused handle writes, per tile t of 16 (or 8) samples, the %globaltimer
+ * nanoseconds at which the tile finished each phase to
+ * buf[t * DLRM_TRACE_SLOTS + s]: s = 0 kernel start, 1 prologue (biases and
+ * inputs loaded), 2 .. 1+n_bot the bottom layers, 2+n_bot the interaction,
+ * 3+n_bot .. 1+n_bot+n_top the top layers but the last, 2+n_bot+n_top the end
+ * (sigmoid layer written). Needs capacity >= tiles(max_batch) *
+ * DLRM_TRACE_SLOTS (INVALID_ARG otherwise; UNSUPPORTED on a layer-wise
+ * handle); NULL switches it off. Returns the tile height in *tile_rows. */
+#define DLRM_TRACE_SLOTS 40
+dlrm_status_t dlrm_set_phase_trace(dlrm_handle_t h, uint64_t* buf, int64_t capacity,
+                                   int32_t* tile_rows);
 
 /* Copies up to `capacity` per-stage totals (milliseconds, summed over the
  * profiled forward calls) into total_ms and the number of profiled calls into

@@ -76,7 +76,7 @@ def _create(lib, ln_bot, ln_top, rows, d, bag=1, max_batch=8, math=0, tables_ok=
     k = len(rows)
     cfg = dl._Config(len(ln_bot) - 1, (ctypes.c_int32 * len(ln_bot))(*ln_bot), k,
                      (ctypes.c_int64 * k)(*rows), d, len(ln_top) - 1,
-                     (ctypes.c_int32 * len(ln_top))(*ln_top), bag, max_batch, math)
+                     (ctypes.c_int32 * len(ln_top))(*ln_top), bag, max_batch, math, 0)
     fake = ctypes.c_void_p(0x1000 if tables_ok else 0)
     tabs = (ctypes.c_void_p * k)(*([fake] * k))
     w = (ctypes.c_void_p * 16)(*([ctypes.c_void_p(0x1000)] * 16))

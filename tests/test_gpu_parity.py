@@ -207,12 +207,24 @@ def test_linear_rejects_overlapping_output():
 
 # ---------------------------------------------------------------- full forward
 
-def make_model(cfg, inp, max_batch=None, math=dl.MATH_FP32):
+PATHS = [dl.PATH_LAYERWISE, dl.PATH_FUSED]
+PATH_IDS = ["layerwise", "fused"]
+
+
+def make_model(cfg, inp, max_batch=None, math=dl.MATH_FP32, path=dl.PATH_AUTO):
     tables = [cu(t) for t in inp["tables"]]
-    return dl.DlrmModel(cfg.ln_bot, cfg.ln_top, tables,
-                        [cu(w) for w in inp["bot_w"]], [cu(v) for v in inp["bot_b"]],
-                        [cu(w) for w in inp["top_w"]], [cu(v) for v in inp["top_b"]],
-                        cfg.bag_size, max_batch or cfg.batch, math)
+    try:
+        model = dl.DlrmModel(cfg.ln_bot, cfg.ln_top, tables,
+                             [cu(w) for w in inp["bot_w"]], [cu(v) for v in inp["bot_b"]],
+                             [cu(w) for w in inp["top_w"]], [cu(v) for v in inp["top_b"]],
+                             cfg.bag_size, max_batch or cfg.batch, math, path)
+    except dl.DlrmError as e:
+        if path == dl.PATH_FUSED and e.status == dl.ERR_UNSUPPORTED:
+            pytest.skip("shape does not fit the fused forward")
+        raise
+    if path != dl.PATH_AUTO:
+        assert model.path == path
+    return model
 
 
 def run_forward(model, inp):
@@ -226,21 +238,32 @@ FORWARD_CASES = ["tiny_b64_k3", "mini_b2048_k3_d4", "b2048_k3", "b2048_k32",
                  "sweep_b8192_k32"]
 
 
+@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
 @pytest.mark.parametrize("name", FORWARD_CASES)
-def test_forward_matches_oracle(name):
+def test_forward_matches_oracle(name, path):
     cfg = synth.get_config(name)
     inp = synth.make_inputs(cfg, seed=1234)
-    model = make_model(cfg, inp)
+    model = make_model(cfg, inp, path=path)
     got = run_forward(model, inp)
     close(got, oracle.forward(inp))
     model.close()
 
 
+def test_auto_path_picks_fused_for_the_2048_sample_workload():
+    cfg = synth.get_config("b2048_k3")
+    inp = synth.make_inputs(cfg, seed=3)
+    model = make_model(cfg, inp)
+    assert model.path == dl.PATH_FUSED
+    assert model.stage_names() == ["fused"]
+    model.close()
+
+
+@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
 @pytest.mark.parametrize("seed", [1, 2, 3])
-def test_forward_tiny_seeds(seed):
+def test_forward_tiny_seeds(seed, path):
     cfg = synth.get_config("tiny_b64_k3")
     inp = synth.make_inputs(cfg, seed=seed)
-    model = make_model(cfg, inp)
+    model = make_model(cfg, inp, path=path)
     close(run_forward(model, inp), oracle.forward(inp))
     model.close()
 
@@ -260,10 +283,11 @@ def test_forward_hand_fixture():
     model.close()
 
 
-def test_forward_smaller_batches_than_max():
+@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
+def test_forward_smaller_batches_than_max(path):
     cfg = synth.get_config("b2048_k3")
     inp = synth.make_inputs(cfg, seed=77)
-    model = make_model(cfg, inp, max_batch=2048)
+    model = make_model(cfg, inp, max_batch=2048, path=path)
     for b in (1, 37, 1000):
         sub = synth.make_inputs(cfg.with_batch(b), seed=78, with_tables=False)
         sub.update(tables=inp["tables"], bot_w=inp["bot_w"], bot_b=inp["bot_b"],
@@ -272,10 +296,11 @@ def test_forward_smaller_batches_than_max():
     model.close()
 
 
-def test_forward_host_equals_device_forward():
+@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
+def test_forward_host_equals_device_forward(path):
     cfg = synth.get_config("b2048_k3")
     inp = synth.make_inputs(cfg, seed=5)
-    model = make_model(cfg, inp)
+    model = make_model(cfg, inp, path=path)
     dev = run_forward(model, inp)
     dense = torch.from_numpy(inp["dense"]).pin_memory()
     idx = torch.from_numpy(inp["indices"]).pin_memory()
@@ -287,10 +312,11 @@ def test_forward_host_equals_device_forward():
     model.close()
 
 
-def test_forward_reports_device_errors_and_clears_them():
+@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
+def test_forward_reports_device_errors_and_clears_them(path):
     cfg = synth.get_config("tiny_b64_k3")
     inp = synth.make_inputs(cfg, seed=8)
-    model = make_model(cfg, inp)
+    model = make_model(cfg, inp, path=path)
     bad = dict(inp)
     bad["indices"] = inp["indices"].copy()
     bad["indices"][1, 9] = 1000           # rows = 1000
@@ -317,10 +343,11 @@ def test_forward_rejects_batch_above_max():
     model.close()
 
 
-def test_forward_is_graph_capturable():
+@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
+def test_forward_is_graph_capturable(path):
     cfg = synth.get_config("b2048_k32")
     inp = synth.make_inputs(cfg, seed=9)
-    model = make_model(cfg, inp)
+    model = make_model(cfg, inp, path=path)
     dense, idx, off = cu(inp["dense"]), cu(inp["indices"]), cu(inp["offsets"])
     out = torch.empty(cfg.batch, device="cuda")
     s = torch.cuda.Stream()
