@@ -147,10 +147,19 @@ dlrm_status_t run_forward(dlrm_handle_t h, const float* dense, const int64_t* in
   // [M1] bottom MLP, ReLU after every layer
   const float* in = dense;
   int ld_in = h->n_dense;
+  // GEMMs of the opt-in TF32/BF16 modes run on the tensor cores; the N = 1
+  // sigmoid layer (a dot product per row) stays on the fp32 GEMV.
+  auto linear = [&](const float* x, int ldx, const float* w, int ldw, const float* b, float* y,
+                    int ldy, int n, int k, int act) {
+    if (h->math != DLRM_MATH_FP32 && n >= 16)
+      return dlrm::launch_linear_tc(x, ldx, w, ldw, b, y, ldy, batch, n, k, act,
+                                    h->math == DLRM_MATH_BF16, h->err, s);
+    return dlrm::launch_linear_fp32(x, ldx, w, ldw, b, y, ldy, batch, n, k, act, s);
+  };
   for (int l = 0; l < h->n_bot; ++l) {
     float* o = h->act[l & 1];
-    e = dlrm::launch_linear_fp32(in, ld_in, h->bot_w[l], h->bot_ldw[l], h->bot_b[l], o, h->ld_act,
-                                 batch, h->ln_bot[l + 1], h->ln_bot[l], DLRM_ACT_RELU, s);
+    e = linear(in, ld_in, h->bot_w[l], h->bot_ldw[l], h->bot_b[l], o, h->ld_act,
+               h->ln_bot[l + 1], h->ln_bot[l], DLRM_ACT_RELU);
     if (e != cudaSuccess || !mark()) return DLRM_ERR_CUDA;
     in = o;
     ld_in = h->ld_act;
@@ -165,9 +174,8 @@ dlrm_status_t run_forward(dlrm_handle_t h, const float* dense, const int64_t* in
     const bool last = (l == h->n_top - 1);
     float* o = last ? out : h->act[l & 1];
     const int ld_o = last ? 1 : h->ld_act;
-    e = dlrm::launch_linear_fp32(in, ld_in, h->top_w[l], h->top_ldw[l], h->top_b[l], o, ld_o,
-                                 batch, h->ln_top[l + 1], h->ln_top[l],
-                                 last ? DLRM_ACT_SIGMOID : DLRM_ACT_RELU, s);
+    e = linear(in, ld_in, h->top_w[l], h->top_ldw[l], h->top_b[l], o, ld_o, h->ln_top[l + 1],
+               h->ln_top[l], last ? DLRM_ACT_SIGMOID : DLRM_ACT_RELU);
     if (e != cudaSuccess || !mark()) return DLRM_ERR_CUDA;
     in = o;
     ld_in = ld_o;
@@ -262,7 +270,10 @@ dlrm_status_t dlrm_create(const dlrm_config_t* cfg, const float* const* tables,
   for (int l = 0; l < cfg->n_top; ++l) if (!top_w[l] || !top_b[l]) return DLRM_ERR_INVALID_ARG;
   if (static_cast<int64_t>(cfg->max_batch) * cfg->bag_size > (int64_t(1) << 31))
     return DLRM_ERR_UNSUPPORTED;
-  if (cfg->math != DLRM_MATH_FP32) return DLRM_ERR_UNSUPPORTED;
+  if (cfg->math != DLRM_MATH_FP32 && cfg->math != DLRM_MATH_TF32 && cfg->math != DLRM_MATH_BF16)
+    return DLRM_ERR_INVALID_ARG;
+  // the fused plan is fp32 only; the opt-in tensor-core modes are layer-wise
+  if (cfg->math != DLRM_MATH_FP32 && cfg->path == DLRM_PATH_FUSED) return DLRM_ERR_UNSUPPORTED;
   if (dlrm::interaction_smem_per_sample(cfg->n_tables, cfg->emb_dim) >
       dlrm::device_max_smem_optin())
     return DLRM_ERR_UNSUPPORTED;
@@ -590,7 +601,10 @@ dlrm_status_t linear_bias_act(const float* x, int32_t ld_x, const float* W, cons
   const size_t wbytes = static_cast<size_t>(N) * K * sizeof(float);
   if (ranges_overlap(y, ybytes, x, xbytes) || ranges_overlap(y, ybytes, W, wbytes))
     return DLRM_ERR_INVALID_ARG;
-  if (math != DLRM_MATH_FP32) return DLRM_ERR_UNSUPPORTED;
+  if (math != DLRM_MATH_FP32)
+    return cuda_status(dlrm::launch_linear_tc(x, ld_x, W, K, bias, y, ld_y, M, N, K, act,
+                                              math == DLRM_MATH_BF16, nullptr,
+                                              static_cast<cudaStream_t>(stream)));
   return cuda_status(dlrm::launch_linear_fp32(x, ld_x, W, K, bias, y, ld_y, M, N, K, act,
                                               static_cast<cudaStream_t>(stream)));
 }

@@ -199,8 +199,15 @@ __device__ void gemm_layer(const FusedGemm& L, const float* __restrict__ a_s, fl
   const int tid = threadIdx.x;
   const int warp = tid / kWarp;
   const int lane = tid % kWarp;
-  const int lm = lane / 8;
-  const int ln = lane % 8;
+  // Lane -> (row group lm, column group ln). A 128-bit shared load is served
+  // per half-warp, and its two quarter-warps share one wavefront only when they
+  // touch disjoint banks (equal addresses still collide). So inside each half
+  // the quarters take complementary row groups {0,1} / {2,3} and complementary
+  // column groups {0..3} / {4..7}: every A and W load costs 2 wavefronts.
+  const int quarter = (lane >> 3) & 1;
+  const int half = lane >> 4;
+  const int lm = ((lane & 7) >> 2) + 2 * quarter;
+  const int ln = (lane & 3) + 4 * (quarter ^ half);
   const int ct = warp % NACT;
   const int kslice = warp / NACT;
   const int sw = (KS == 16) ? ((ln >> 1) & 3) : ln;     // chunk swizzle of this thread's rows

@@ -1,0 +1,122 @@
+"""Opt-in tensor-core modes (tcgen05, TF32 / BF16 operands, fp32 accumulation)
+against the fp64 oracle.
+
+Tolerance of these modes: rel 2e-2. For a GEMM output, where single elements
+can cancel to ~0, the bound is |gpu - ref| <= 2e-2 * (|ref| + rms(ref)) per
+element; for the forward's sigmoid outputs it is 2e-2 * |ref|.
+"""
+import numpy as np
+import pytest
+
+import dlrm_synth as synth
+import oracle
+
+torch = pytest.importorskip("torch")
+import dlrm_embedding_interaction_gb300 as dl  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+MODES = [dl.MATH_TF32, dl.MATH_BF16]
+MODE_IDS = ["tf32", "bf16"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    if not torch.cuda.is_available():
+        pytest.fail("the gpu tests need a CUDA device")
+    from dlrm_embedding_interaction_gb300 import build
+    build.build()
+    dl.lib()
+    torch.cuda.set_device(0)
+
+
+def cu(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def tc_close(got, ref, rel=2e-2):
+    got = np.asarray(got, np.float64)
+    rms = float(np.sqrt(np.mean(ref ** 2))) if ref.size else 0.0
+    err = np.abs(got - ref)
+    bound = rel * (np.abs(ref) + rms)
+    worst = np.argmax(err - bound) if err.size else 0
+    assert np.all(err <= bound), (
+        f"max excess {float((err - bound).flat[worst]):.3e} at {np.unravel_index(worst, err.shape)}: "
+        f"got {got.flat[worst]:.6f} ref {ref.flat[worst]:.6f}")
+    return float(np.max(err / (np.abs(ref) + rms))) if err.size else 0.0
+
+
+LINEAR_CASES = [
+    (1, 16, 1), (7, 16, 5), (128, 128, 32), (128, 128, 64), (300, 200, 70), (2048, 512, 13),
+    (2048, 256, 512), (2048, 64, 256), (257, 1024, 479), (65, 17, 16), (129, 130, 131),
+    (4096, 512, 592),
+]
+
+
+@pytest.mark.parametrize("mode", MODES, ids=MODE_IDS)
+@pytest.mark.parametrize("m,n,k", LINEAR_CASES)
+def test_linear_tensor_core_matches_oracle(m, n, k, mode):
+    rng = np.random.default_rng(m * 7 + n * 11 + k * 13 + mode)
+    x = rng.standard_normal((m, k)).astype(np.float32)
+    bound = 1.0 / np.sqrt(k)
+    w = rng.uniform(-bound, bound, (n, k)).astype(np.float32)
+    b = rng.uniform(-bound, bound, n).astype(np.float32)
+    y = torch.full((m, n), float("nan"), device="cuda")
+    dl.linear_bias_act(cu(x), cu(w), cu(b), y, dl.ACT_NONE, mode)
+    torch.cuda.synchronize()
+    ref = oracle.linear(x, w, b, oracle.ACT_NONE)
+    worst = tc_close(y.cpu().numpy(), ref)
+    if mode == dl.MATH_TF32:
+        assert worst < 5e-3     # tf32 keeps 10 mantissa bits: far inside the bound
+
+
+@pytest.mark.parametrize("mode", MODES, ids=MODE_IDS)
+@pytest.mark.parametrize("act", [dl.ACT_RELU, dl.ACT_SIGMOID])
+def test_linear_tensor_core_epilogue(mode, act):
+    rng = np.random.default_rng(act)
+    x = rng.standard_normal((333, 96)).astype(np.float32)
+    w = rng.uniform(-0.1, 0.1, (160, 96)).astype(np.float32)
+    b = rng.uniform(-0.1, 0.1, 160).astype(np.float32)
+    y = torch.empty((333, 160), device="cuda")
+    dl.linear_bias_act(cu(x), cu(w), cu(b), y, act, mode)
+    torch.cuda.synchronize()
+    tc_close(y.cpu().numpy(), oracle.linear(x, w, b, act))
+
+
+def test_linear_tensor_core_strided_rows_and_no_bias():
+    rng = np.random.default_rng(5)
+    xf = rng.standard_normal((200, 75)).astype(np.float32)
+    w = rng.uniform(-0.1, 0.1, (48, 70)).astype(np.float32)
+    y = torch.empty((200, 48), device="cuda")
+    dl.linear_bias_act(cu(xf)[:, :70], cu(w), None, y, dl.ACT_NONE, dl.MATH_TF32)
+    torch.cuda.synchronize()
+    tc_close(y.cpu().numpy(), oracle.linear(xf[:, :70], w, None, oracle.ACT_NONE))
+
+
+@pytest.mark.parametrize("mode", MODES, ids=MODE_IDS)
+@pytest.mark.parametrize("name", ["tiny_b64_k3", "b2048_k3", "b2048_k32", "sweep_b33_k8"])
+def test_forward_tensor_core_matches_oracle(name, mode):
+    cfg = synth.get_config(name)
+    inp = synth.make_inputs(cfg, seed=1234)
+    tables = [cu(t) for t in inp["tables"]]
+    model = dl.DlrmModel(cfg.ln_bot, cfg.ln_top, tables,
+                         [cu(w) for w in inp["bot_w"]], [cu(v) for v in inp["bot_b"]],
+                         [cu(w) for w in inp["top_w"]], [cu(v) for v in inp["top_b"]],
+                         cfg.bag_size, cfg.batch, mode)
+    assert model.path == dl.PATH_LAYERWISE
+    out = model.forward(cu(inp["dense"]), cu(inp["indices"]), cu(inp["offsets"]))
+    assert model.error() == dl.OK
+    ref = oracle.forward(inp)
+    np.testing.assert_allclose(out.cpu().numpy(), ref, rtol=2e-2, atol=0)
+    model.close()
+
+
+def test_fused_plan_rejects_tensor_core_modes():
+    cfg = synth.get_config("tiny_b64_k3")
+    inp = synth.make_inputs(cfg, seed=1)
+    with pytest.raises(dl.DlrmError) as ei:
+        dl.DlrmModel(cfg.ln_bot, cfg.ln_top, [cu(t) for t in inp["tables"]],
+                     [cu(w) for w in inp["bot_w"]], [cu(v) for v in inp["bot_b"]],
+                     [cu(w) for w in inp["top_w"]], [cu(v) for v in inp["top_b"]],
+                     cfg.bag_size, cfg.batch, dl.MATH_BF16, dl.PATH_FUSED)
+    assert ei.value.status == dl.ERR_UNSUPPORTED
