@@ -458,6 +458,24 @@ def run_ours(args, rank, world, local_rank):
                             bound="alu (FP32 FFMA)" if tot_flops / (fp32_peak * 1e12) >
                             fwd_bytes / (pk["hbm_gbs"] * 1e9) else "hbm")
 
+    # opt-in tensor-core modes (tcgen05), same inputs and weights, same timing rules
+    tc_modes = {}
+    for mode_name, mode in (("tf32", dl.MATH_TF32), ("bf16", dl.MATH_BF16)):
+        m2 = dl.DlrmModel(cfg.ln_bot, cfg.ln_top, model.tables,
+                          [cu(w) for w in inp["bot_w"]], [cu(b) for b in inp["bot_b"]],
+                          [cu(w) for w in inp["top_w"]], [cu(b) for b in inp["top_b"]],
+                          cfg.bag_size, cfg.batch, mode)
+        ms_tc, _ = timed(lambda: m2.forward(dense, idx, off, out, stream=stream),
+                         max(1, args.steps // 5), 10)
+        if m2.error(stream) != dl.OK:
+            raise RuntimeError(f"device error in the {mode_name} forward")
+        tot = sum(ms_tc)
+        tc_modes[mode_name] = dict(us_per_batch=tot * 1e3 / len(ms_tc),
+                                   samples_per_s=cfg.batch * len(ms_tc) / (tot * 1e-3),
+                                   plan="layer-wise launches, tcgen05 GEMMs",
+                                   tolerance="rel 2e-2 vs the fp64 oracle")
+        m2.close()
+
     gather = None
     cpu = None
     if rank == 0 and world == 1:
@@ -489,7 +507,7 @@ def run_ours(args, rank, world, local_rank):
                     parallelism="replicas" if world > 1 else "single GPU"),
         e2e=e2e, gpu_launches=args.steps * n_stages, clocks=clock_info,
         roofline=roof, forward_roofline=forward_roofline, stages_us=stage_us,
-        fused_phases_us=phases_us,
+        fused_phases_us=phases_us, opt_in_tensor_core=tc_modes,
         graph=dict(us_per_batch_median=graph_us, samples_per_s=cfg.batch / (graph_us * 1e-6)),
         cpu_baseline=cpu)
     line["gather_b65536_k26_zipf"] = gather

@@ -9,6 +9,7 @@
 // allocate nothing and never synchronise.
 #include <algorithm>
 #include <atomic>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -305,8 +306,9 @@ dlrm_status_t dlrm_create(const dlrm_config_t* cfg, const float* const* tables,
       delete h;
       return DLRM_ERR_CUDA;
     }
+    const int cw = 8;   // consumer warps of the fused kernel
     fused_fits = dlrm::fused_plan(h->n_dense, h->k, h->d, h->bag, h->ln_bot, h->ln_top, hw, hb,
-                                  h->tabs, dlrm::device_max_smem_optin(), &fplan);
+                                  h->tabs, dlrm::device_max_smem_optin(), cw, &fplan);
     h->fused_bm = fplan.bm;
   }
   const int64_t tiles = fused_fits ? (h->max_batch + h->fused_bm - 1) / h->fused_bm : 0;
@@ -414,7 +416,7 @@ dlrm_status_t dlrm_create(const dlrm_config_t* cfg, const float* const* tables,
     h->fused.wstream = at(off_fw);
     h->fused.bias = at(off_fb);
     h->fused.wlast = at(off_fl);
-    if (st == DLRM_OK) st = cuda_status(dlrm::fused_prepare(h->fused_bm));
+    if (st == DLRM_OK) st = cuda_status(dlrm::fused_prepare(h->fused_bm, h->fused.cw));
   }
   if (st == DLRM_OK) st = cuda_status(cudaDeviceSynchronize());
   if (st != DLRM_OK) {

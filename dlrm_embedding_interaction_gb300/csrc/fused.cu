@@ -38,7 +38,6 @@
 namespace dlrm {
 namespace {
 
-constexpr int kConsumers = kFusedConsumerWarps * kWarp;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -109,8 +108,9 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
+template <int CW>
 __device__ __forceinline__ void consumer_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+  asm volatile("bar.sync 1, %0;" ::"n"(CW * kWarp) : "memory");
 }
 
 // Bounded wait for the phase with the given parity. Returns false when this or
@@ -133,14 +133,17 @@ __device__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_fl
   }
 }
 
-__device__ __forceinline__ int gemm_rows(const FusedGemm& L, int pass) {
+// Weight rows of pass `pass` (CW = 8 warps, 64-column warp tiles).
+__host__ __device__ __forceinline__ int gemm_rows(const FusedGemm& L, int pass, int cw) {
   if (L.ksplit > 1) return L.n_pad;
-  const int left = L.n_pad / 64 - pass * kFusedConsumerWarps;
-  return 64 * (left < kFusedConsumerWarps ? left : kFusedConsumerWarps);
+  const int ct = 512 / cw;
+  const int left = L.n_pad / ct - pass * cw;
+  return ct * (left < cw ? left : cw);
 }
 
 // ---------------------------------------------------------------- producer
 
+template <int CW>
 __device__ void produce(const FusedParams& p, float* stages, uint64_t* full, uint64_t* empty,
                         volatile int* abort_flag) {
   const uint32_t s_count = static_cast<uint32_t>(p.stages);
@@ -151,7 +154,7 @@ __device__ void produce(const FusedParams& p, float* stages, uint64_t* full, uin
     const FusedGemm& L = p.gemm[g];
     const int ks = 16 * L.ksplit;
     for (int pass = 0; pass < L.passes && ok; ++pass) {
-      const int rows = gemm_rows(L, pass);
+      const int rows = gemm_rows(L, pass, CW);
       const uint32_t bytes = static_cast<uint32_t>(rows * ks) * 4u;
       for (int kst = 0; kst < L.n_kst; ++kst) {
         const uint32_t slot = it % s_count;
@@ -186,16 +189,28 @@ __device__ void produce(const FusedParams& p, float* stages, uint64_t* full, uin
 
 // C (BM x n_pad; zero beyond n) = act(A (BM x k_pad) W^T + b). `it` is the
 // stage counter shared with the producer's sequence. KSPLIT is a template
-// argument so the stage row length and the j offsets are immediates.
-template <int BM, int KSPLIT>
-__device__ void gemm_layer(const FusedGemm& L, const float* __restrict__ a_s, float* __restrict__ c_s,
+// argument so the staged row length and the column offsets are immediates.
+//
+// Thread tile: BM/4 rows (lm + 4i) x 8 columns (ln + 8j) of a 64-column warp
+// tile, 12 128-bit shared loads per 128 FFMA at BM = 16. Shared-load issue,
+// not bandwidth, bounds this loop (an isolated copy of it runs at ~42% of the
+// FFMA peak; an 8 x 8 tile reaches ~63% alone but at 16 rows per tile costs
+// split K on every layer and runs slower here). With split K the partial
+// sums of k-slice s go to output columns [s * n_pad, (s + 1) * n_pad).
+template <int BM, int KSPLIT, int CW>
+__device__ void gemm_layer(const FusedGemm& L, float* __restrict__ a_s, float* __restrict__ c_s,
                            int lda, const float* __restrict__ bias_s, int act,
                            const float* __restrict__ stages, uint64_t* full, uint64_t* empty,
                            uint32_t& it, uint32_t s_count, volatile int* abort_flag, int32_t* err) {
   constexpr int TM = BM / 4;
+  constexpr int TN = 8;
+  constexpr int CT = 64;
+  constexpr int KSL = 16;                                // k per warp slice per stage
+  constexpr int kConsumers = CW * kWarp;
   constexpr int ksplit = KSPLIT;
-  constexpr int KS = 16 * KSPLIT;
-  constexpr int NACT = kFusedConsumerWarps / KSPLIT;
+  constexpr int KS = KSL * KSPLIT;                       // k per stage
+  constexpr int CPR = KS / 4;                            // 16-byte chunks per staged row
+  constexpr int NACT = CW / KSPLIT;
   const int tid = threadIdx.x;
   const int warp = tid / kWarp;
   const int lane = tid % kWarp;
@@ -210,73 +225,73 @@ __device__ void gemm_layer(const FusedGemm& L, const float* __restrict__ a_s, fl
   const int ln = (lane & 3) + 4 * (quarter ^ half);
   const int ct = warp % NACT;
   const int kslice = warp / NACT;
-  const int sw = (KS == 16) ? ((ln >> 1) & 3) : ln;     // chunk swizzle of this thread's rows
+  const int sw = CPR == 4 ? ((ln >> 1) & 3) : (ln & 7);  // chunk swizzle of this thread's rows
   int ph[4];
 #pragma unroll
   for (int s = 0; s < 4; ++s) ph[s] = ((kslice * 4 + s) ^ sw) * 4;
-  const int wj = 8 * KS;                                 // row distance of the j columns
-  const float* a_row = a_s + lm * lda + kslice * 16;
+  const float* a_row = a_s + lm * lda + kslice * KSL;
 
   for (int pass = 0; pass < L.passes; ++pass) {
-    const int tiles_here = gemm_rows(L, pass) / 64;
+    const int tiles_here = gemm_rows(L, pass, CW) / CT;
     const bool active = ct < tiles_here;
-    float acc[TM][8];
+    float acc[TM][TN];
 #pragma unroll
     for (int i = 0; i < TM; ++i)
 #pragma unroll
-      for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+      for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
 
     for (int kst = 0; kst < L.n_kst; ++kst, ++it) {
       const uint32_t slot = it % s_count;
       wait_phase(smem_u32(&full[slot]), (it / s_count) & 1, abort_flag, err);
       if (active) {
-        const float* ws = stages + slot * kFusedStageFloats + (ct * 64 + ln) * KS;
+        const float* ws = stages + slot * kFusedStageFloats + (ct * CT + ln) * KS;
         const float* as = a_row + kst * KS;
-        float4 av[2][TM], wv[2][8];
+        float4 av[2][TM], wv[2][TN];
 #pragma unroll
         for (int i = 0; i < TM; ++i) av[0][i] = *reinterpret_cast<const float4*>(as + 4 * i * lda);
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          wv[0][j] = *reinterpret_cast<const float4*>(ws + j * wj + ph[0]);
+        for (int j = 0; j < TN; ++j)
+          wv[0][j] = *reinterpret_cast<const float4*>(ws + 8 * j * KS + ph[0]);
 #pragma unroll
         for (int step = 0; step < 4; ++step) {
           const int cur = step & 1;
-          if (step < 3) {
+          if (step < 3) {      // fragments of the next 4-wide k step
 #pragma unroll
             for (int i = 0; i < TM; ++i)
               av[cur ^ 1][i] = *reinterpret_cast<const float4*>(as + 4 * i * lda + 4 * (step + 1));
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              wv[cur ^ 1][j] = *reinterpret_cast<const float4*>(ws + j * wj + ph[step + 1]);
+            for (int j = 0; j < TN; ++j)
+              wv[cur ^ 1][j] = *reinterpret_cast<const float4*>(ws + 8 * j * KS + ph[step + 1]);
           }
+          // component-outer: TM*TN independent accumulators between dependent FMAs
 #pragma unroll
           for (int i = 0; i < TM; ++i)
 #pragma unroll
-            for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[cur][i].x, wv[cur][j].x, acc[i][j]);
+            for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(av[cur][i].x, wv[cur][j].x, acc[i][j]);
 #pragma unroll
           for (int i = 0; i < TM; ++i)
 #pragma unroll
-            for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[cur][i].y, wv[cur][j].y, acc[i][j]);
+            for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(av[cur][i].y, wv[cur][j].y, acc[i][j]);
 #pragma unroll
           for (int i = 0; i < TM; ++i)
 #pragma unroll
-            for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[cur][i].z, wv[cur][j].z, acc[i][j]);
+            for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(av[cur][i].z, wv[cur][j].z, acc[i][j]);
 #pragma unroll
           for (int i = 0; i < TM; ++i)
 #pragma unroll
-            for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[cur][i].w, wv[cur][j].w, acc[i][j]);
+            for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(av[cur][i].w, wv[cur][j].w, acc[i][j]);
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
     }
 
-    const int col0 = pass * kFusedConsumerWarps * 64;
+    const int col0 = pass * CW * CT;
     if (ksplit == 1) {
       if (active) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int n = col0 + ct * 64 + ln + 8 * j;
+        for (int j = 0; j < TN; ++j) {
+          const int n = col0 + ct * CT + ln + 8 * j;
           const float bv = bias_s[L.b_off + n];
 #pragma unroll
           for (int i = 0; i < TM; ++i) {
@@ -286,58 +301,68 @@ __device__ void gemm_layer(const FusedGemm& L, const float* __restrict__ a_s, fl
         }
       }
     } else {
-      // partial sums of k-slice s go to columns [s * n_pad, (s + 1) * n_pad)
 #pragma unroll
       for (int i = 0; i < TM; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          c_s[(lm + 4 * i) * lda + kslice * L.n_pad + ct * 64 + ln + 8 * j] = acc[i][j];
-      consumer_sync();
+        for (int j = 0; j < TN; ++j)
+          c_s[(lm + 4 * i) * lda + kslice * L.n_pad + ct * CT + ln + 8 * j] = acc[i][j];
+      consumer_sync<CW>();
+      // n_pad = 64 * 2^j: 4 columns per thread step, shifts instead of divisions
       const int np = L.n_pad;
-      for (int e = tid; e < BM * np; e += kConsumers) {
-        const int m = e / np;
-        const int n = e - m * np;
-        float v = 0.f;
-        for (int s = 0; s < ksplit; ++s) v += c_s[m * lda + s * np + n];
-        v = apply_act(v + bias_s[L.b_off + n], act);
-        c_s[m * lda + n] = (n < L.n) ? v : 0.f;
+      const int q_shift = 31 - __clz(np >> 2);           // log2(np / 4)
+      for (int e = tid; e < BM * (np >> 2); e += kConsumers) {
+        const int m = e >> q_shift;
+        const int n = (e - (m << q_shift)) << 2;
+        float4 v = *reinterpret_cast<const float4*>(c_s + m * lda + n);
+#pragma unroll
+        for (int s = 1; s < ksplit; ++s) {
+          const float4 u = *reinterpret_cast<const float4*>(c_s + m * lda + s * np + n);
+          v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w;
+        }
+        const float4 bv = *reinterpret_cast<const float4*>(bias_s + L.b_off + n);
+        v.x = (n + 0 < L.n) ? apply_act(v.x + bv.x, act) : 0.f;
+        v.y = (n + 1 < L.n) ? apply_act(v.y + bv.y, act) : 0.f;
+        v.z = (n + 2 < L.n) ? apply_act(v.z + bv.z, act) : 0.f;
+        v.w = (n + 3 < L.n) ? apply_act(v.w + bv.w, act) : 0.f;
+        *reinterpret_cast<float4*>(c_s + m * lda + n) = v;
       }
     }
-    consumer_sync();
+    consumer_sync<CW>();
   }
 }
 
-template <int BM>
-__device__ void gemm_dispatch(const FusedGemm& L, const float* a_s, float* c_s, int lda,
+template <int BM, int CW>
+__device__ void gemm_dispatch(const FusedGemm& L, float* a_s, float* c_s, int lda,
                               const float* bias_s, int act, int zero_to, const float* stages,
                               uint64_t* full, uint64_t* empty, uint32_t& it, uint32_t s_count,
                               volatile int* abort_flag, int32_t* err) {
   switch (L.ksplit) {
     case 1:
-      gemm_layer<BM, 1>(L, a_s, c_s, lda, bias_s, act, stages, full, empty, it, s_count, abort_flag, err);
+      gemm_layer<BM, 1, CW>(L, a_s, c_s, lda, bias_s, act, stages, full, empty, it, s_count, abort_flag, err);
       break;
     case 2:
-      gemm_layer<BM, 2>(L, a_s, c_s, lda, bias_s, act, stages, full, empty, it, s_count, abort_flag, err);
+      gemm_layer<BM, 2, CW>(L, a_s, c_s, lda, bias_s, act, stages, full, empty, it, s_count, abort_flag, err);
       break;
     case 4:
-      gemm_layer<BM, 4>(L, a_s, c_s, lda, bias_s, act, stages, full, empty, it, s_count, abort_flag, err);
+      gemm_layer<BM, 4, CW>(L, a_s, c_s, lda, bias_s, act, stages, full, empty, it, s_count, abort_flag, err);
       break;
     default:
-      gemm_layer<BM, 8>(L, a_s, c_s, lda, bias_s, act, stages, full, empty, it, s_count, abort_flag, err);
+      gemm_layer<BM, 8, CW>(L, a_s, c_s, lda, bias_s, act, stages, full, empty, it, s_count, abort_flag, err);
       break;
   }
   const int extra = zero_to - L.n_pad;
-  for (int e = threadIdx.x; e < BM * extra; e += kConsumers) {
+  for (int e = threadIdx.x; e < BM * extra; e += CW * kWarp) {
     const int m = e / extra;
     c_s[m * lda + L.n_pad + (e - m * extra)] = 0.f;
   }
-  consumer_sync();
+  consumer_sync<CW>();
 }
 
-template <int BM>
+template <int BM, int CW>
 __device__ void consume(const FusedParams& p, float* stages, uint64_t* full, uint64_t* empty,
                         volatile int* abort_flag, float* act0, float* act1, float* zs,
-                        float* bias_s, float* wlast_s) {
+                        int* rowidx_s, float* bias_s, float* wlast_s) {
+  constexpr int kConsumers = CW * kWarp;
   const int tid = threadIdx.x;
   const int m0 = blockIdx.x * BM;
   const int rows = min(BM, p.batch - m0);
@@ -376,6 +401,23 @@ __device__ void consume(const FusedParams& p, float* stages, uint64_t* full, uin
       if (ok) cp_async16(dst, table + row * d + 4 * c4);
       else cp_async16_zero(dst, table);
     }
+  } else if (p.zbuf == 2) {
+    // Bag size 1, rows streamed later: check every bag now and keep its row
+    // (or -1) in shared memory, so the streaming needs no dependent loads.
+    for (int e = tid; e < BM * k; e += kConsumers) {
+      const int s = e / k;
+      const int t = e - s * k;
+      int row32 = -1;
+      if (s < rows) {
+        const int64_t b = m0 + s;
+        const int64_t start = __ldg(p.offsets + static_cast<int64_t>(t) * p.batch + b);
+        const int64_t row = __ldg(p.indices + static_cast<int64_t>(t) * p.batch + b);
+        if (start != b) bad_off = true;
+        else if (row < 0 || row >= p.tabs.rows[t]) oob = true;
+        else row32 = static_cast<int>(row);
+      }
+      rowidx_s[e] = row32;
+    }
   }
   cp_async_commit();
 
@@ -391,8 +433,32 @@ __device__ void consume(const FusedParams& p, float* stages, uint64_t* full, uin
     }
   }
   cp_async_wait<1>();
-  consumer_sync();
+  consumer_sync<CW>();
   stamp(p, 1);
+
+  // Bag-size-1 rows streamed by sample group into two buffers (zbuf == 2).
+  auto issue_group = [&](int g0, int buf) {
+    float* zb = zs + buf * p.sg * k * p.ldz;
+    const int ns = min(p.sg, BM - g0);
+    for (int e = tid; e < ns * k * d4; e += kConsumers) {
+      const int s = e / (k * d4);
+      const int rem = e - s * k * d4;
+      const int t = rem / d4;
+      const int c4 = rem - t * d4;
+      const int row = rowidx_s[(g0 + s) * k + t];
+      float* dst = zb + (s * k + t) * p.ldz + 4 * c4;
+      const float* table = p.tabs.ptr[t];
+      if (row >= 0) cp_async16(dst, table + static_cast<int64_t>(row) * d + 4 * c4);
+      else cp_async16_zero(dst, table);
+    }
+    cp_async_commit();
+  };
+  if (p.zbuf == 2) {
+    // the first two groups land while the bottom MLP runs
+    issue_group(0, 0);
+    if (p.sg < BM) issue_group(p.sg, 1);
+    else cp_async_commit();
+  }
 
   const uint32_t s_count = static_cast<uint32_t>(p.stages);
   uint32_t it = 0;
@@ -400,7 +466,7 @@ __device__ void consume(const FusedParams& p, float* stages, uint64_t* full, uin
   float* out = act1;
   for (int g = 0; g < p.n_bot; ++g) {
     const int zero_to = (g + 1 < p.n_bot) ? p.gemm[g + 1].k_pad : p.gemm[g].n_pad;
-    gemm_dispatch<BM>(p.gemm[g], in, out, p.lda, bias_s, DLRM_ACT_RELU, zero_to, stages, full,
+    gemm_dispatch<BM, CW>(p.gemm[g], in, out, p.lda, bias_s, DLRM_ACT_RELU, zero_to, stages, full,
                       empty, it, s_count, abort_flag, p.err);
     float* t = in; in = out; out = t;
     stamp(p, 2 + g);
@@ -417,9 +483,13 @@ __device__ void consume(const FusedParams& p, float* stages, uint64_t* full, uin
     else if (c >= d + pairs) r[m * p.lda + c] = 0.f;
   }
   if (p.prefetch_z) cp_async_wait<0>();
-  for (int g0 = 0; g0 < BM; g0 += p.sg) {
+  // zbuf == 2: groups 0 and 1 were issued in the prologue; group g + 2
+  // streams into buffer g % 2 once group g's pair dots are done.
+  for (int g0 = 0, gi = 0; g0 < BM; g0 += p.sg, ++gi) {
     const int ns = min(p.sg, BM - g0);
-    if (!p.prefetch_z) {
+    if (p.zbuf == 2) {
+      cp_async_wait<1>();   // group gi has landed (only gi + 1 may be pending)
+    } else if (!p.prefetch_z) {
       for (int e = tid; e < ns * k * d4; e += kConsumers) {
         const int s = e / (k * d4);
         const int rem = e - s * k * d4;
@@ -450,8 +520,9 @@ __device__ void consume(const FusedParams& p, float* stages, uint64_t* full, uin
         *reinterpret_cast<float4*>(zs + (s * k + t) * p.ldz + 4 * c4) = v;
       }
     }
-    consumer_sync();
-    const float* zg = zs + (p.prefetch_z ? g0 * k * p.ldz : 0);
+    consumer_sync<CW>();
+    const float* zg = zs + (p.prefetch_z ? g0 * k * p.ldz
+                                         : (p.zbuf == 2 ? (gi & 1) * p.sg * k * p.ldz : 0));
     for (int e = tid; e < ns * pairs; e += kConsumers) {
       const int s = e / pairs;
       const int q = e - s * pairs;
@@ -460,6 +531,7 @@ __device__ void consume(const FusedParams& p, float* stages, uint64_t* full, uin
       const float* vi = (i == 0) ? x + (g0 + s) * p.lda : zg + (s * k + i - 1) * p.ldz;
       const float* vj = (j == 0) ? x + (g0 + s) * p.lda : zg + (s * k + j - 1) * p.ldz;
       float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
       for (int c4 = 0; c4 < d4; ++c4) {
         const float4 u = *reinterpret_cast<const float4*>(vi + 4 * c4);
         const float4 w = *reinterpret_cast<const float4*>(vj + 4 * c4);
@@ -470,7 +542,11 @@ __device__ void consume(const FusedParams& p, float* stages, uint64_t* full, uin
       }
       r[(g0 + s) * p.lda + d + q] = (a.x + a.y) + (a.z + a.w);
     }
-    consumer_sync();
+    consumer_sync<CW>();
+    if (p.zbuf == 2) {
+      if (g0 + 2 * p.sg < BM) issue_group(g0 + 2 * p.sg, gi & 1);
+      else cp_async_commit();
+    }
   }
   if (p.err) {
     if (oob) atomicOr(reinterpret_cast<unsigned int*>(p.err), DLRM_ERRBIT_INDEX_OOB);
@@ -483,7 +559,7 @@ __device__ void consume(const FusedParams& p, float* stages, uint64_t* full, uin
   out = (r == act0) ? act1 : act0;
   for (int g = p.n_bot; g < p.n_gemm; ++g) {
     const int zero_to = (g + 1 < p.n_gemm) ? p.gemm[g + 1].k_pad : p.k_last;
-    gemm_dispatch<BM>(p.gemm[g], in, out, p.lda, bias_s, DLRM_ACT_RELU, zero_to, stages, full,
+    gemm_dispatch<BM, CW>(p.gemm[g], in, out, p.lda, bias_s, DLRM_ACT_RELU, zero_to, stages, full,
                       empty, it, s_count, abort_flag, p.err);
     float* t = in; in = out; out = t;
     stamp(p, 3 + g);
@@ -491,7 +567,7 @@ __device__ void consume(const FusedParams& p, float* stages, uint64_t* full, uin
   const int warp = tid / kWarp, lane = tid % kWarp;
   const int k4 = p.k_last / 4;
   const float bl = bias_s[p.b_last];
-  for (int m = warp; m < rows; m += kFusedConsumerWarps) {
+  for (int m = warp; m < rows; m += CW) {
     float acc = 0.f;
     for (int q = lane; q < k4; q += kWarp) {
       const float4 a = *reinterpret_cast<const float4*>(in + m * p.lda + 4 * q);
@@ -506,13 +582,13 @@ __device__ void consume(const FusedParams& p, float* stages, uint64_t* full, uin
     if (lane == 0) p.out[m0 + m] = apply_act(acc + bl, DLRM_ACT_SIGMOID);
   }
   if (p.trace) {
-    consumer_sync();
+    consumer_sync<CW>();
     stamp(p, 2 + p.n_gemm + 1);
   }
 }
 
-template <int BM>
-__global__ void __launch_bounds__(kFusedThreads, 1)
+template <int BM, int CW>
+__global__ void __launch_bounds__((CW + 1) * 32, 1)
 fused_forward_kernel(const __grid_constant__ FusedParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   float* stages = reinterpret_cast<float*>(smem_raw);
@@ -529,21 +605,22 @@ fused_forward_kernel(const __grid_constant__ FusedParams p) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), kFusedConsumerWarps);
+      mbar_init(smem_u32(&empty[s]), CW);
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   __syncthreads();
-  if (warp == kFusedConsumerWarps) {
-    if (threadIdx.x % kWarp == 0) produce(p, stages, full, empty, abort_flag);
+  if (warp == CW) {
+    if (threadIdx.x % kWarp == 0) produce<CW>(p, stages, full, empty, abort_flag);
     return;
   }
-  consume<BM>(p, stages, full, empty, abort_flag, act0, act1, zs, bias_s, wlast_s);
+  int* rowidx_s = reinterpret_cast<int*>(smem_raw + p.off_rowidx);
+  consume<BM, CW>(p, stages, full, empty, abort_flag, act0, act1, zs, rowidx_s, bias_s, wlast_s);
 }
 
-template <int BM>
+template <int BM, int CW>
 cudaError_t enable_smem() {
   static std::atomic<uint64_t> done{0};
   int dev = 0;
@@ -551,7 +628,7 @@ cudaError_t enable_smem() {
   if (e != cudaSuccess) return e;
   const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
   if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
-  e = cudaFuncSetAttribute(fused_forward_kernel<BM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(fused_forward_kernel<BM, CW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(device_max_smem_optin()));
   if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
   return e;
@@ -559,21 +636,23 @@ cudaError_t enable_smem() {
 
 }  // namespace
 
-cudaError_t fused_prepare(int bm) {
-  if (bm == 16) return enable_smem<16>();
-  if (bm == 8) return enable_smem<8>();
+cudaError_t fused_prepare(int bm, int cw) {
+  if (cw != 8) return cudaErrorInvalidValue;
+  if (bm == 16) return enable_smem<16, 8>();
+  if (bm == 8) return enable_smem<8, 8>();
   return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_fused(const FusedParams& p, int bm, cudaStream_t stream) {
   if (p.batch == 0) return cudaSuccess;
   const unsigned grid = static_cast<unsigned>((p.batch + bm - 1) / bm);
-  cudaError_t e = fused_prepare(bm);
+  cudaError_t e = fused_prepare(bm, p.cw);
   if (e != cudaSuccess) return e;
+  const unsigned threads = static_cast<unsigned>((p.cw + 1) * kWarp);
   if (bm == 16)
-    fused_forward_kernel<16><<<grid, kFusedThreads, p.smem_bytes, stream>>>(p);
+    fused_forward_kernel<16, 8><<<grid, threads, p.smem_bytes, stream>>>(p);
   else
-    fused_forward_kernel<8><<<grid, kFusedThreads, p.smem_bytes, stream>>>(p);
+    fused_forward_kernel<8, 8><<<grid, threads, p.smem_bytes, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -581,7 +660,11 @@ cudaError_t launch_fused(const FusedParams& p, int bm, cudaStream_t stream) {
 
 namespace {
 
-int swizzle_of(int row, int ks) { return ks == 16 ? ((row >> 1) & 3) : (row & 7); }
+// Chunk swizzle of staged row `row` when a row holds `cpr` 16-byte chunks:
+// 8 consecutive rows then hit 8 distinct 16-byte bank groups.
+int swizzle_of(int row, int cpr) {
+  return cpr == 2 ? ((row >> 2) & 1) : (cpr == 4 ? ((row >> 1) & 3) : (row & 7));
+}
 
 size_t align128(size_t x) { return (x + 127) / 128 * 128; }
 
@@ -590,7 +673,10 @@ size_t align128(size_t x) { return (x + 127) / 128 * 128; }
 bool fused_plan(int n_dense, int k_tables, int d, int bag, const std::vector<int>& ln_bot,
                 const std::vector<int>& ln_top, const std::vector<std::vector<float>>& w,
                 const std::vector<std::vector<float>>& b, const GatherTables& tabs,
-                size_t smem_limit, FusedPlan* plan) {
+                size_t smem_limit, int cw, FusedPlan* plan) {
+  if (cw != 8) return false;
+  const int ctw = 512 / cw;     // column tile width (64)
+  const int ksl = 16;           // k per warp slice per stage
   const int n_bot = static_cast<int>(ln_bot.size()) - 1;
   const int n_top = static_cast<int>(ln_top.size()) - 1;
   const int n_gemm = n_bot + n_top - 1;
@@ -606,6 +692,7 @@ bool fused_plan(int n_dense, int k_tables, int d, int bag, const std::vector<int
   p.n_bot = n_bot;
   p.n_top = n_top;
   p.n_gemm = n_gemm;
+  p.cw = cw;
   const int f = k_tables + 1;
   const int pairs = f * (f - 1) / 2;
 
@@ -615,25 +702,25 @@ bool fused_plan(int n_dense, int k_tables, int d, int bag, const std::vector<int
     kin[g] = g < n_bot ? ln_bot[g] : ln_top[g - n_bot];
     nout[g] = g < n_bot ? ln_bot[g + 1] : ln_top[g - n_bot + 1];
   }
-  int widest = 512;   // split-K partials span 512 columns
+  int widest = 512;   // split-K partials span 512 columns of the output buffer
   int bias_floats = 0;
   for (int g = 0; g < n_gemm; ++g) {
     FusedGemm& L = p.gemm[g];
-    int n_wt = (nout[g] + 63) / 64;
-    if (n_wt < kFusedConsumerWarps) {
+    int n_wt = (nout[g] + ctw - 1) / ctw;
+    if (n_wt < cw) {
       int p2 = 1;
       while (p2 < n_wt) p2 *= 2;
       n_wt = p2;
-      L.ksplit = kFusedConsumerWarps / n_wt;
+      L.ksplit = cw / n_wt;
       L.passes = 1;
     } else {
       L.ksplit = 1;
-      L.passes = (n_wt + kFusedConsumerWarps - 1) / kFusedConsumerWarps;
+      L.passes = (n_wt + cw - 1) / cw;
     }
     L.n = nout[g];
-    L.n_pad = 64 * n_wt;
-    L.k_pad = static_cast<int>(round_up(kin[g], 16 * L.ksplit));
-    L.n_kst = L.k_pad / (16 * L.ksplit);
+    L.n_pad = ctw * n_wt;
+    L.k_pad = static_cast<int>(round_up(kin[g], ksl * L.ksplit));
+    L.n_kst = L.k_pad / (ksl * L.ksplit);
     L.b_off = bias_floats;
     bias_floats += L.n_pad;
     widest = std::max({widest, L.k_pad, L.n_pad});
@@ -646,35 +733,55 @@ bool fused_plan(int n_dense, int k_tables, int d, int bag, const std::vector<int
   p.lda = static_cast<int>(round_up(widest, 32)) + 4;
   p.ldz = static_cast<int>(round_up(d, 4)) + 4;
 
-  // shared-memory carve: stages | act0 | act1 | z | bias | wlast | barriers
+  // shared-memory carve: stages | act0 | act1 | z | rowidx | bias | wlast | barriers
+  // Preference: every bag row of the tile prefetched at kernel start (bag 1);
+  // else two group buffers streamed with cp.async (bag 1); else one group
+  // buffer filled with summed loads (bags of L > 1). The 16-row tile is kept
+  // first (one wave of tiles), then a weight stage is given up.
   const size_t per_sample_z = static_cast<size_t>(k_tables) * p.ldz * sizeof(float);
   bool placed = false;
   for (int bm : {16, 8}) {
-    for (int stages : {4, 3}) {
-      size_t off = static_cast<size_t>(stages) * kFusedStageFloats * sizeof(float);
-      const size_t act = align128(static_cast<size_t>(bm) * p.lda * sizeof(float));
-      const size_t tail = align128(bias_floats * sizeof(float)) +
-                          align128(p.k_last * sizeof(float)) + align128(2 * stages * 8 + 16);
-      const size_t fixed = off + 2 * act + tail;
-      if (fixed + per_sample_z > smem_limit) continue;
-      const int sg = static_cast<int>(std::min<size_t>(bm, (smem_limit - fixed) / per_sample_z));
-      if (sg < 1) continue;
-      p.stages = stages;
-      p.off_act0 = static_cast<int>(off);
-      p.off_act1 = static_cast<int>(off + act);
-      p.off_z = static_cast<int>(off + 2 * act);
-      const size_t zbytes = align128(static_cast<size_t>(sg) * per_sample_z);
-      p.off_bias = static_cast<int>(p.off_z + zbytes);
-      p.off_wlast = static_cast<int>(p.off_bias + align128(bias_floats * sizeof(float)));
-      p.off_bar = static_cast<int>(p.off_wlast + align128(p.k_last * sizeof(float)));
-      p.smem_bytes = static_cast<int>(p.off_bar + align128(2 * stages * 8 + 16));
-      p.sg = sg;
-      p.prefetch_z = (bag == 1 && sg == bm) ? 1 : 0;
-      plan->bm = bm;
-      placed = true;
-      break;
+    for (int mode = 0; mode < 3 && !placed; ++mode) {
+      if (bag != 1 && mode < 2) continue;
+      for (int stages : {4, 3}) {
+        const size_t off = static_cast<size_t>(stages) * kFusedStageFloats * sizeof(float);
+        const size_t act = align128(static_cast<size_t>(bm) * p.lda * sizeof(float));
+        const size_t rowidx = align128(static_cast<size_t>(bm) * k_tables * sizeof(int));
+        const size_t tail = rowidx + align128(bias_floats * sizeof(float)) +
+                            align128(p.k_last * sizeof(float)) + align128(2 * stages * 8 + 16);
+        const size_t fixed = off + 2 * act + tail;
+        if (fixed >= smem_limit) continue;
+        const size_t room = smem_limit - fixed;
+        int sg = 0, zbuf = 1;
+        if (mode == 0) {
+          if (room < bm * per_sample_z) continue;
+          sg = bm;
+        } else if (mode == 1) {
+          sg = static_cast<int>(std::min<size_t>(bm, room / (2 * per_sample_z)));
+          zbuf = 2;
+        } else {
+          sg = static_cast<int>(std::min<size_t>(bm, room / per_sample_z));
+        }
+        if (sg < 1) continue;
+        p.stages = stages;
+        p.off_act0 = static_cast<int>(off);
+        p.off_act1 = static_cast<int>(off + act);
+        p.off_z = static_cast<int>(off + 2 * act);
+        const size_t zbytes = align128(static_cast<size_t>(zbuf) * sg * per_sample_z);
+        p.off_rowidx = static_cast<int>(p.off_z + zbytes);
+        p.off_bias = static_cast<int>(p.off_rowidx + rowidx);
+        p.off_wlast = static_cast<int>(p.off_bias + align128(bias_floats * sizeof(float)));
+        p.off_bar = static_cast<int>(p.off_wlast + align128(p.k_last * sizeof(float)));
+        p.smem_bytes = static_cast<int>(p.off_bar + align128(2 * stages * 8 + 16));
+        p.sg = sg;
+        p.prefetch_z = mode == 0 ? 1 : 0;
+        p.zbuf = zbuf;
+        plan->bm = bm;
+        placed = true;
+        break;
+      }
+      if (placed) break;
     }
-    if (placed) break;
   }
   if (!placed || static_cast<size_t>(p.smem_bytes) > smem_limit) return false;
 
@@ -682,22 +789,20 @@ bool fused_plan(int n_dense, int k_tables, int d, int bag, const std::vector<int
   plan->wstream.clear();
   for (int g = 0; g < n_gemm; ++g) {
     const FusedGemm& L = p.gemm[g];
-    const int ks = 16 * L.ksplit;
+    const int ks = ksl * L.ksplit;
     const std::vector<float>& W = w[g];
     for (int pass = 0; pass < L.passes; ++pass) {
-      const int rows = (L.ksplit > 1) ? L.n_pad
-                                      : 64 * std::min(L.n_pad / 64 - pass * kFusedConsumerWarps,
-                                                      kFusedConsumerWarps);
+      const int rows = gemm_rows(L, pass, cw);
       for (int kst = 0; kst < L.n_kst; ++kst) {
         const size_t base = plan->wstream.size();
         plan->wstream.resize(base + static_cast<size_t>(rows) * ks, 0.f);
         for (int rr = 0; rr < rows; ++rr) {
-          const int n = pass * kFusedConsumerWarps * 64 + rr;
+          const int n = pass * cw * ctw + rr;
           if (n >= L.n) continue;
           for (int kk = 0; kk < ks; ++kk) {
             const int kg = kst * ks + kk;
             if (kg >= kin[g]) break;
-            const int chunk = (kk / 4) ^ swizzle_of(rr, ks);
+            const int chunk = (kk / 4) ^ swizzle_of(rr, ks / 4);
             plan->wstream[base + static_cast<size_t>(rr) * ks + chunk * 4 + kk % 4] =
                 W[static_cast<size_t>(n) * kin[g] + kg];
           }

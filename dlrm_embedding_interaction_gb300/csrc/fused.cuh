@@ -8,18 +8,19 @@
 
 namespace dlrm {
 
-constexpr int kFusedConsumerWarps = 8;
-constexpr int kFusedThreads = (kFusedConsumerWarps + 1) * 32;   // + one producer warp
+// Consumer warps per CTA: 8 (thread tile 4 rows x 8 columns, 64-column warp
+// tiles) or 16 (4 x 4, 32-column warp tiles); one more warp is the producer.
 constexpr int kFusedStageFloats = 8192;                        // 32 KB weight stage
 constexpr int kFusedMaxGemm = 2 * DLRM_MAX_LAYERS;
 
 // One GEMM layer of the weight stream. Its weights occupy `passes * n_kst`
 // consecutive stages of the packed stream: pass p covers output rows
-// [512 p, 512 p + rows), stage s covers k in [s*KS, (s+1)*KS), KS = 16*ksplit,
+// [CW*CT p, CW*CT p + rows) (CW consumer warps, CT = 512 / CW column tile),
+// stage s covers k in [s*KS, (s+1)*KS), KS = 16*ksplit,
 // stored row-major (rows x KS) with 16-byte chunk c of row r at position
 // c ^ swz(r) (swz = (r >> 1) & 3 when KS = 16, else r & 7).
-//   n      output width; n_pad = 64 * {1, 2, 4} (ksplit = 8, 4, 2) or a
-//          multiple of 64 >= 512 (ksplit = 1)
+//   n      output width; n_pad = CT * 2^j < 512 (ksplit = CW / (n_pad / CT))
+//          or a multiple of CT >= 512 (ksplit = 1)
 //   k_pad  input width padded to a multiple of KS (zero weights)
 //   b_off  offset of the layer's zero-padded bias in the bias block
 struct FusedGemm {
@@ -29,16 +30,18 @@ struct FusedGemm {
 struct FusedParams {
   int batch, n_dense, k_tables, d, bag, n_bot, n_top;
   int n_gemm;        // n_bot + n_top - 1 (the last top layer is the N = 1 dot)
+  int cw;            // consumer warps (8 or 16)
   int lda;           // activation row stride (floats), >= 516, = 4 mod 32
   int ldz;           // bag-sum row stride, round_up(d, 4) + 4
   int sg;            // samples per gather/interaction group
   int prefetch_z;    // 1: all BM samples' rows are fetched at kernel start (bag 1)
+  int zbuf;          // bag 1 without prefetch: 2 group buffers, rows streamed with cp.async
   int stages;        // weight ring depth
   int k_last;        // padded input width of the last (N = 1) layer
   int b_last;        // its bias offset in the bias block
   int bias_floats;   // bias block length (multiple of 4)
   // shared-memory carve (bytes from the dynamic base)
-  int off_act0, off_act1, off_z, off_bias, off_wlast, off_bar;
+  int off_act0, off_act1, off_z, off_bias, off_wlast, off_bar, off_rowidx;
   int smem_bytes;
   FusedGemm gemm[kFusedMaxGemm];
   const float* wstream;    // packed weight stream
@@ -67,9 +70,9 @@ struct FusedPlan {
 bool fused_plan(int n_dense, int k_tables, int d, int bag, const std::vector<int>& ln_bot,
                 const std::vector<int>& ln_top, const std::vector<std::vector<float>>& w,
                 const std::vector<std::vector<float>>& b, const GatherTables& tabs,
-                size_t smem_limit, FusedPlan* plan);
+                size_t smem_limit, int consumer_warps, FusedPlan* plan);
 
-cudaError_t fused_prepare(int bm);
+cudaError_t fused_prepare(int bm, int consumer_warps);
 cudaError_t launch_fused(const FusedParams& p, int bm, cudaStream_t stream);
 
 }  // namespace dlrm
