@@ -15,7 +15,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libdlrm_gb300.so")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_OOM, ERR_INDEX_OOB, ERR_TIMEOUT = range(7)
-MATH_FP32, MATH_TF32, MATH_BF16 = 0, 1, 2
+MATH_FP32, MATH_TF32, MATH_BF16, MATH_TF32X3 = 0, 1, 2, 3
 PATH_AUTO, PATH_LAYERWISE, PATH_FUSED = 0, 1, 2
 ACT_NONE, ACT_RELU, ACT_SIGMOID = 0, 1, 2
 ERRBIT_INDEX_OOB = 1 << ERR_INDEX_OOB

@@ -154,7 +154,7 @@ dlrm_status_t run_forward(dlrm_handle_t h, const float* dense, const int64_t* in
                     int ldy, int n, int k, int act) {
     if (h->math != DLRM_MATH_FP32 && n >= 16)
       return dlrm::launch_linear_tc(x, ldx, w, ldw, b, y, ldy, batch, n, k, act,
-                                    h->math == DLRM_MATH_BF16, h->err, s);
+                                    static_cast<int>(h->math), h->err, s);
     return dlrm::launch_linear_fp32(x, ldx, w, ldw, b, y, ldy, batch, n, k, act, s);
   };
   for (int l = 0; l < h->n_bot; ++l) {
@@ -271,7 +271,8 @@ dlrm_status_t dlrm_create(const dlrm_config_t* cfg, const float* const* tables,
   for (int l = 0; l < cfg->n_top; ++l) if (!top_w[l] || !top_b[l]) return DLRM_ERR_INVALID_ARG;
   if (static_cast<int64_t>(cfg->max_batch) * cfg->bag_size > (int64_t(1) << 31))
     return DLRM_ERR_UNSUPPORTED;
-  if (cfg->math != DLRM_MATH_FP32 && cfg->math != DLRM_MATH_TF32 && cfg->math != DLRM_MATH_BF16)
+  if (cfg->math != DLRM_MATH_FP32 && cfg->math != DLRM_MATH_TF32 &&
+      cfg->math != DLRM_MATH_BF16 && cfg->math != DLRM_MATH_TF32X3)
     return DLRM_ERR_INVALID_ARG;
   // the fused plan is fp32 only; the opt-in tensor-core modes are layer-wise
   if (cfg->math != DLRM_MATH_FP32 && cfg->path == DLRM_PATH_FUSED) return DLRM_ERR_UNSUPPORTED;
@@ -594,7 +595,8 @@ dlrm_status_t linear_bias_act(const float* x, int32_t ld_x, const float* W, cons
   if (M < 0 || N < 1 || K < 1 || ld_x < K || ld_y < N) return DLRM_ERR_INVALID_ARG;
   if (act != DLRM_ACT_NONE && act != DLRM_ACT_RELU && act != DLRM_ACT_SIGMOID)
     return DLRM_ERR_INVALID_ARG;
-  if (math != DLRM_MATH_FP32 && math != DLRM_MATH_TF32 && math != DLRM_MATH_BF16)
+  if (math != DLRM_MATH_FP32 && math != DLRM_MATH_TF32 && math != DLRM_MATH_BF16 &&
+      math != DLRM_MATH_TF32X3)
     return DLRM_ERR_INVALID_ARG;
   if (M == 0) return DLRM_OK;
   if (!x || !W || !y) return DLRM_ERR_INVALID_ARG;
@@ -605,7 +607,7 @@ dlrm_status_t linear_bias_act(const float* x, int32_t ld_x, const float* W, cons
     return DLRM_ERR_INVALID_ARG;
   if (math != DLRM_MATH_FP32)
     return cuda_status(dlrm::launch_linear_tc(x, ld_x, W, K, bias, y, ld_y, M, N, K, act,
-                                              math == DLRM_MATH_BF16, nullptr,
+                                              static_cast<int>(math), nullptr,
                                               static_cast<cudaStream_t>(stream)));
   return cuda_status(dlrm::launch_linear_fp32(x, ld_x, W, K, bias, y, ld_y, M, N, K, act,
                                               static_cast<cudaStream_t>(stream)));

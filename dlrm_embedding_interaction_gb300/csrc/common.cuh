@@ -60,10 +60,10 @@ cudaError_t launch_linear_fp32(const float* x, int ld_x, const float* w, int ld_
                                const float* bias, float* y, int ld_y, int m, int n, int k,
                                int act, cudaStream_t stream);
 
-// Tensor-core (tcgen05) Linear: TF32 (bf16 = false) or BF16 operands, fp32
+// Tensor-core (tcgen05) Linear, mode DLRM_MATH_TF32 / BF16 / TF32X3, fp32
 // accumulation; err (nullable) receives DLRM_ERRBIT_TIMEOUT on a stuck wait.
 cudaError_t launch_linear_tc(const float* x, int ld_x, const float* w, int ld_w, const float* bias,
-                             float* y, int ld_y, int m, int n, int k, int act, bool bf16,
+                             float* y, int ld_y, int m, int n, int k, int act, int mode,
                              int32_t* err, cudaStream_t stream);
 
 int device_sm_count();

@@ -48,8 +48,17 @@ typedef enum {
 
 /* Arithmetic of the MLP GEMMs. FP32 (SIMT FFMA) is the parity mode. TF32 and
  * BF16 run the MLPs on the tcgen05 tensor cores with fp32 accumulation in
- * TMEM (opt-in; results within rel 2e-2 of fp32). */
-typedef enum { DLRM_MATH_FP32 = 0, DLRM_MATH_TF32 = 1, DLRM_MATH_BF16 = 2 } dlrm_math_t;
+ * TMEM (opt-in; results within rel 2e-2 of fp32). TF32X3 splits every fp32
+ * operand into a tf32 head and its exact remainder and sums three tensor-core
+ * products (head*head + head*rest + rest*head): opt-in, on the tensor cores,
+ * with errors inside the fp32 parity tolerance (about 2^-21 relative per
+ * product). */
+typedef enum {
+  DLRM_MATH_FP32 = 0,
+  DLRM_MATH_TF32 = 1,
+  DLRM_MATH_BF16 = 2,
+  DLRM_MATH_TF32X3 = 3
+} dlrm_math_t;
 
 /* Kernel plan of a forward handle. AUTO takes the fused single-launch forward
  * when the shape fits it (activations of a tile of samples resident in shared

@@ -18,6 +18,8 @@ pytestmark = pytest.mark.gpu
 
 MODES = [dl.MATH_TF32, dl.MATH_BF16]
 MODE_IDS = ["tf32", "bf16"]
+ALL_MODES = MODES + [dl.MATH_TF32X3]
+ALL_IDS = MODE_IDS + ["tf32x3"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -53,7 +55,7 @@ LINEAR_CASES = [
 ]
 
 
-@pytest.mark.parametrize("mode", MODES, ids=MODE_IDS)
+@pytest.mark.parametrize("mode", ALL_MODES, ids=ALL_IDS)
 @pytest.mark.parametrize("m,n,k", LINEAR_CASES)
 def test_linear_tensor_core_matches_oracle(m, n, k, mode):
     rng = np.random.default_rng(m * 7 + n * 11 + k * 13 + mode)
@@ -65,12 +67,15 @@ def test_linear_tensor_core_matches_oracle(m, n, k, mode):
     dl.linear_bias_act(cu(x), cu(w), cu(b), y, dl.ACT_NONE, mode)
     torch.cuda.synchronize()
     ref = oracle.linear(x, w, b, oracle.ACT_NONE)
+    if mode == dl.MATH_TF32X3:     # fp32 parity tolerance
+        np.testing.assert_allclose(y.cpu().numpy(), ref, atol=1e-5, rtol=1e-4)
+        return
     worst = tc_close(y.cpu().numpy(), ref)
     if mode == dl.MATH_TF32:
         assert worst < 5e-3     # tf32 keeps 10 mantissa bits: far inside the bound
 
 
-@pytest.mark.parametrize("mode", MODES, ids=MODE_IDS)
+@pytest.mark.parametrize("mode", ALL_MODES, ids=ALL_IDS)
 @pytest.mark.parametrize("act", [dl.ACT_RELU, dl.ACT_SIGMOID])
 def test_linear_tensor_core_epilogue(mode, act):
     rng = np.random.default_rng(act)
@@ -93,7 +98,7 @@ def test_linear_tensor_core_strided_rows_and_no_bias():
     tc_close(y.cpu().numpy(), oracle.linear(xf[:, :70], w, None, oracle.ACT_NONE))
 
 
-@pytest.mark.parametrize("mode", MODES, ids=MODE_IDS)
+@pytest.mark.parametrize("mode", ALL_MODES, ids=ALL_IDS)
 @pytest.mark.parametrize("name", ["tiny_b64_k3", "b2048_k3", "b2048_k32", "sweep_b33_k8"])
 def test_forward_tensor_core_matches_oracle(name, mode):
     cfg = synth.get_config(name)
@@ -107,7 +112,10 @@ def test_forward_tensor_core_matches_oracle(name, mode):
     out = model.forward(cu(inp["dense"]), cu(inp["indices"]), cu(inp["offsets"]))
     assert model.error() == dl.OK
     ref = oracle.forward(inp)
-    np.testing.assert_allclose(out.cpu().numpy(), ref, rtol=2e-2, atol=0)
+    if mode == dl.MATH_TF32X3:     # fp32 parity tolerance
+        np.testing.assert_allclose(out.cpu().numpy(), ref, atol=1e-5, rtol=1e-4)
+    else:
+        np.testing.assert_allclose(out.cpu().numpy(), ref, rtol=2e-2, atol=0)
     model.close()
 
 
