@@ -16,6 +16,10 @@ Extra objects on the line:
   stages_us  per-stage device time from the library's event profiling mode
   roofline   the dominant stage against its bound (FP32 FFMA peak from SM
              count x 128 lanes x 2 x 2070 MHz, or measured HBM GB/s)
+  configs    the forward on the other workloads (64-sample 3-table, 2048-sample
+             32-table, the 11 x 5 batch x tables sweep, and the 65536-sample
+             26-table Zipf workload): us/batch, samples/s, plan, whole-forward
+             roofline fraction
   gather_b65536_k26_zipf  the standalone multi-table gather on the 13.3 GB
              26-table workload (bags of 20, Zipf(1.05)) plus a uniform-index
              control, algorithmic GB/s against measured HBM GB/s
@@ -56,6 +60,8 @@ def parse_args():
     ap.add_argument("--seed", type=int, default=1234)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other workloads' forward measurements")
     ap.add_argument("--no-gather", action="store_true",
                     help="skip the 13.3 GB standalone-gather measurement")
     ap.add_argument("--profile-steps", type=int, default=200)
@@ -245,14 +251,23 @@ def forward_work(cfg, batch):
     return flops, byts
 
 
-def gather_measure(torch, dl, synth, pk, steps=10):
+def device_tables(torch, synth, cfg, seed, n=None):
+    """The workload's first n tables from the seeded generator, filled on the host
+    one at a time into a reused pinned buffer and copied to the current device."""
+    n = cfg.n_tables if n is None else n
+    host = torch.empty((max(cfg.rows[:n]), cfg.emb_dim), dtype=torch.float32).pin_memory()
+    out = []
+    for t in range(n):
+        h = host[:cfg.rows[t]]
+        synth.make_table(cfg, seed, t, out=h.numpy())
+        out.append(h.to("cuda"))
+    del host
+    return out
+
+
+def gather_measure(torch, dl, synth, pk, tables, steps=10):
     """Standalone gather on the 26 x 1M x 128 workload (bags of 20), Zipf and uniform."""
-    import numpy as np
     cfg = synth.get_config("b65536_k26_zipf")
-    gen = torch.Generator(device="cuda")
-    gen.manual_seed(1234)
-    tables = [torch.empty((cfg.rows[t], cfg.emb_dim), device="cuda").uniform_(
-        -cfg.table_range, cfg.table_range, generator=gen) for t in range(cfg.n_tables)]
     off = torch.from_numpy(synth.make_offsets(cfg)).cuda()
     out = torch.empty((cfg.batch, cfg.n_tables, cfg.emb_dim), device="cuda")
     _, byts = stage_work(cfg, "gather", cfg.batch)
@@ -277,7 +292,7 @@ def gather_measure(torch, dl, synth, pk, steps=10):
         res[dist] = dict(ms_per_launch=ms, algorithmic_gbs=gbs,
                          frac_of_measured_hbm=gbs / pk["hbm_gbs"], frac_of_nominal_8tbs=gbs / 8000.0)
         del idx
-    del tables, out
+    del out
     torch.cuda.empty_cache()
     return dict(workload="26 tables x 1M x 128 fp32 (13.3 GB), batch 65536, bags of 20",
                 bytes_per_launch=byts, launches_timed=steps,
@@ -479,13 +494,63 @@ def run_ours(args, rank, world, local_rank):
                                               else "rel 2e-2 vs the fp64 oracle"))
         m2.close()
 
+    def forward_point(c, tabs, steps, warmup):
+        """One workload's forward through the library, same timing rules as the
+        headline: mean and median us per batch, samples/s, the plan taken and the
+        whole-forward roofline fraction."""
+        ci = synth.make_inputs(c, seed=args.seed, with_tables=False)
+        m = dl.DlrmModel(c.ln_bot, c.ln_top, tabs,
+                         [cu(w) for w in ci["bot_w"]], [cu(b) for b in ci["bot_b"]],
+                         [cu(w) for w in ci["top_w"]], [cu(b) for b in ci["top_b"]],
+                         c.bag_size, c.batch)
+        d_, i_, o_ = cu(ci["dense"]), cu(ci["indices"]), cu(ci["offsets"])
+        y_ = torch.empty(c.batch, device=dev)
+        ms_c, _ = timed(lambda: m.forward(d_, i_, o_, y_, stream=stream), steps, warmup)
+        ok = m.error(stream) == dl.OK
+        plan = "fused" if m.path == dl.PATH_FUSED else "layer-wise"
+        m.close()
+        if not ok:
+            raise RuntimeError(f"device error in the {c.name} forward")
+        t = sum(ms_c) / len(ms_c) * 1e-3
+        fl, by = forward_work(c, c.batch)
+        t_alu, t_hbm = fl / (fp32_peak * 1e12), by / (pk["hbm_gbs"] * 1e9)
+        return dict(us_per_batch=t * 1e6, us_median=statistics.median(ms_c) * 1e3,
+                    samples_per_s=c.batch / t, steps=len(ms_c), plan=plan,
+                    roofline_frac=max(t_alu, t_hbm) / t,
+                    bound="alu (FP32 FFMA)" if t_alu >= t_hbm else "hbm")
+
+    configs = None
     gather = None
     cpu = None
     if rank == 0 and world == 1:
-        if not args.no_gather:
-            del flush_buf
+        if not args.no_configs:
+            configs = {cfg.name: "this line"}
+            for name in ("tiny_b64_k3", "b2048_k32"):
+                if name != cfg.name:
+                    c = synth.get_config(name)
+                    tabs = device_tables(torch, synth, c, args.seed)
+                    configs[name] = forward_point(c, tabs, 200, 10)
+                    del tabs
+            # batch x tables sweep; table t is the same seeded stream for every K,
+            # so one set of 32 tables serves all cells
+            tabs = device_tables(torch, synth, synth.sweep_config(1, 32), args.seed)
+            sweep = {}
+            for k in synth.SWEEP_TABLES:
+                for b in synth.SWEEP_BATCHES:
+                    r = forward_point(synth.sweep_config(b, k), tabs[:k], 30, 5)
+                    sweep[f"b{b}_k{k}"] = {key: r[key] for key in
+                                           ("us_per_batch", "samples_per_s", "roofline_frac", "plan")}
+            configs["sweep_b1-8192_k1-32"] = sweep
+            del tabs
             torch.cuda.empty_cache()
-            gather = gather_measure(torch, dl, synth, pk)
+        if not args.no_gather:
+            c4 = synth.get_config("b65536_k26_zipf")
+            tabs = device_tables(torch, synth, c4, args.seed)
+            gather = gather_measure(torch, dl, synth, pk, tabs)
+            if configs is not None:
+                configs[c4.name] = forward_point(c4, tabs, 5, 3)
+            del tabs
+            torch.cuda.empty_cache()
         if not args.no_cpu_baseline:
             cpu = time_oracle(inp, cfg.batch, args.cpu_seconds)
 
@@ -510,7 +575,7 @@ def run_ours(args, rank, world, local_rank):
                     parallelism="replicas" if world > 1 else "single GPU"),
         e2e=e2e, gpu_launches=args.steps * n_stages, clocks=clock_info,
         roofline=roof, forward_roofline=forward_roofline, stages_us=stage_us,
-        fused_phases_us=phases_us, opt_in_tensor_core=tc_modes,
+        fused_phases_us=phases_us, opt_in_tensor_core=tc_modes, configs=configs,
         graph=dict(us_per_batch_median=graph_us, samples_per_s=cfg.batch / (graph_us * 1e-6)),
         cpu_baseline=cpu)
     line["gather_b65536_k26_zipf"] = gather

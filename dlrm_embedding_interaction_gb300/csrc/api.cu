@@ -309,7 +309,8 @@ dlrm_status_t dlrm_create(const dlrm_config_t* cfg, const float* const* tables,
     }
     const int cw = 8;   // consumer warps of the fused kernel
     fused_fits = dlrm::fused_plan(h->n_dense, h->k, h->d, h->bag, h->ln_bot, h->ln_top, hw, hb,
-                                  h->tabs, dlrm::device_max_smem_optin(), cw, &fplan);
+                                  h->tabs, h->max_batch, dlrm::device_sm_count(),
+                                  dlrm::device_max_smem_optin(), cw, &fplan);
     h->fused_bm = fplan.bm;
   }
   const int64_t tiles = fused_fits ? (h->max_batch + h->fused_bm - 1) / h->fused_bm : 0;
@@ -368,9 +369,11 @@ dlrm_status_t dlrm_create(const dlrm_config_t* cfg, const float* const* tables,
   const size_t off_idx = plan.take<int64_t>(mb * h->k * h->bag);
   const size_t off_off = plan.take<int64_t>(mb * h->k);
   const size_t off_out = plan.take<float>(mb);
-  size_t off_fw = 0, off_fb = 0, off_fl = 0;      // fused weight stream, biases, last layer
+  // fused weight stream, its stage table, biases, last layer
+  size_t off_fw = 0, off_ft = 0, off_fb = 0, off_fl = 0;
   if (h->path == DLRM_PATH_FUSED) {
     off_fw = plan.take<float>(fplan.wstream.size());
+    off_ft = plan.take<uint2>(fplan.stage_tab.size());
     off_fb = plan.take<float>(fplan.bias.size());
     off_fl = plan.take<float>(fplan.wlast.size());
   }
@@ -408,6 +411,9 @@ dlrm_status_t dlrm_create(const dlrm_config_t* cfg, const float* const* tables,
     st = cuda_status(cudaMemcpy(at(off_fw), fplan.wstream.data(),
                                 fplan.wstream.size() * sizeof(float), cudaMemcpyHostToDevice));
     if (st == DLRM_OK)
+      st = cuda_status(cudaMemcpy(at(off_ft), fplan.stage_tab.data(),
+                                  fplan.stage_tab.size() * sizeof(uint2), cudaMemcpyHostToDevice));
+    if (st == DLRM_OK)
       st = cuda_status(cudaMemcpy(at(off_fb), fplan.bias.data(), fplan.bias.size() * sizeof(float),
                                   cudaMemcpyHostToDevice));
     if (st == DLRM_OK)
@@ -415,6 +421,7 @@ dlrm_status_t dlrm_create(const dlrm_config_t* cfg, const float* const* tables,
                                   fplan.wlast.size() * sizeof(float), cudaMemcpyHostToDevice));
     h->fused = fplan.params;
     h->fused.wstream = at(off_fw);
+    h->fused.stage_tab = reinterpret_cast<const uint2*>(at(off_ft));
     h->fused.bias = at(off_fb);
     h->fused.wlast = at(off_fl);
     if (st == DLRM_OK) st = cuda_status(dlrm::fused_prepare(h->fused_bm, h->fused.cw));

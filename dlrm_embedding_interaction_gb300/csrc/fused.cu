@@ -8,27 +8,25 @@
 // The pages' megakernel keeps one batch row per thread with activations in
 // registers; at 512-wide layers that cannot hold. Here the tile's activations
 // stay in shared memory for the whole forward and every layer is a CTA-wide
-// GEMM, with the work split by warp role:
-//  * one producer warp streams the weights of all layers, back to back, into
-//    a ring of 32 KB stages with 1-D bulk async copies (cp.async.bulk)
-//    completing on mbarriers. The stream is pre-packed at create time in
-//    consumption order, each stage one contiguous block whose 16-byte chunks
-//    are XOR-swizzled so the consumers' reads are bank-conflict free. The
-//    producer runs ahead across layer boundaries: no pipeline refill per layer.
-//  * eight consumer warps compute. A warp owns a 64-column tile; a thread owns
-//    BM/4 rows x 8 columns (rows lm + 4i, columns ln + 8j) and reads both
-//    operands with 128-bit shared loads (12 loads per 128 FFMA), ordering the
-//    FMAs component-outer so 8*BM/4 independent accumulators separate
-//    dependent ones. Layers narrower than 512 columns split K across warps
-//    (ksplit = 8 / column tiles) and reduce the partial sums in place in the
-//    output buffer.
+// GEMM of the tile's rows against weights streamed through shared memory:
+//  * the weights of all layers form one stream, pre-packed at create time in
+//    consumption order, each 32 KB stage one contiguous block whose 16-byte
+//    chunks are XOR-swizzled so the warps' reads are bank-conflict free. It
+//    flows through a ring of stages filled by 1-D bulk async copies
+//    (cp.async.bulk) completing on mbarriers, issued by one producer warp
+//    that runs ahead across layer boundaries while eight warps compute.
+//  * a computing warp owns TM = 8 rows (4 for 4-row tiles), broadcast-read
+//    from the activation buffer, and 32 * TN columns (one column per lane,
+//    TN per thread) of one 16-wide k-slice of each stage; the register tile
+//    (8 x 4 at 16 rows) accumulates with packed fma.rn.f32x2, and the
+//    k-slices' partial sums meet in shared memory.
 //  * biases, the last layer's weights and (bag size 1) the tile's embedding
 //    rows are fetched with cp.async at kernel start and land during the
 //    bottom MLP; bag sums and pair dots then run from shared memory and build
 //    R = [x, z] in place; the N = 1 sigmoid layer is a warp-per-row dot.
 // Every mbarrier wait is bounded (%globaltimer, 2 s): on expiry the kernel
-// sets DLRM_ERRBIT_TIMEOUT, stops waiting, finishes its control flow and the
-// producer waits (bounded) for its copies in flight before exiting.
+// sets DLRM_ERRBIT_TIMEOUT, stops waiting and finishes its control flow;
+// before exiting it waits (bounded) for any copies still in flight.
 // Rows past the batch are computed on zeros and never stored.
 #include <atomic>
 
@@ -42,6 +40,10 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ uint64_t global_ns() {
@@ -61,10 +63,6 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
                "r"(bytes)
@@ -79,6 +77,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// As mbar_try_wait, but the thread may be suspended (not issuing) for up to
+// `ns` nanoseconds while the phase is incomplete; it resumes when the phase
+// completes or the hint runs out.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
       : "memory");
   return ok != 0;
 }
@@ -115,70 +128,80 @@ __device__ __forceinline__ void consumer_sync() {
 
 // Bounded wait for the phase with the given parity. Returns false when this or
 // another thread gave up (abort raised); the caller then carries on without
-// the data so every named barrier is still reached.
+// the data so every named barrier is still reached. While waiting, the thread
+// is suspended in the mbarrier (hint kSuspendNs) instead of spinning, so a
+// waiting warp takes no issue slots from the warps computing beside it.
+constexpr uint32_t kSuspendNs = 20000;
 __device__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err) {
   if (mbar_try_wait(bar, parity)) return true;
   if (*abort_flag) return false;
   const uint64_t t0 = global_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 31) == 0) {
-      if (*abort_flag) return false;
-      if (global_ns() - t0 > kWaitLimitNs) {
-        *abort_flag = 1;
-        if (err) atomicOr(reinterpret_cast<unsigned int*>(err), DLRM_ERRBIT_TIMEOUT);
-        return false;
-      }
+  for (;;) {
+    if (mbar_try_wait_suspend(bar, parity, kSuspendNs)) return true;
+    if (*abort_flag) return false;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      if (err) atomicOr(reinterpret_cast<unsigned int*>(err), DLRM_ERRBIT_TIMEOUT);
+      return false;
     }
   }
 }
 
-// Weight rows of pass `pass` (CW = 8 warps, 64-column warp tiles).
-__host__ __device__ __forceinline__ int gemm_rows(const FusedGemm& L, int pass, int cw) {
-  if (L.ksplit > 1) return L.n_pad;
-  const int ct = 512 / cw;
-  const int left = L.n_pad / ct - pass * cw;
-  return ct * (left < cw ? left : cw);
+// Output columns one pass covers: 2 / ksplit column groups of 32 * tn.
+__host__ __device__ __forceinline__ int gemm_cols_per_pass(const FusedGemm& L) {
+  return (2 / L.ksplit) * 32 * L.tn;
 }
 
-// ---------------------------------------------------------------- producer
+// Staged weight rows (output columns) of pass `pass`.
+__host__ __device__ __forceinline__ int gemm_rows(const FusedGemm& L, int pass) {
+  const int per_pass = gemm_cols_per_pass(L);
+  const int left = L.n_pad - pass * per_pass;
+  return left < per_pass ? left : per_pass;
+}
 
-template <int CW>
-__device__ void produce(const FusedParams& p, float* stages, uint64_t* full, uint64_t* empty,
-                        volatile int* abort_flag) {
-  const uint32_t s_count = static_cast<uint32_t>(p.stages);
-  const float* src = p.wstream;
-  uint32_t it = 0;
-  bool ok = true;
-  for (int g = 0; g < p.n_gemm && ok; ++g) {
-    const FusedGemm& L = p.gemm[g];
-    const int ks = 16 * L.ksplit;
-    for (int pass = 0; pass < L.passes && ok; ++pass) {
-      const int rows = gemm_rows(L, pass, CW);
-      const uint32_t bytes = static_cast<uint32_t>(rows * ks) * 4u;
-      for (int kst = 0; kst < L.n_kst; ++kst) {
-        const uint32_t slot = it % s_count;
-        if (it >= s_count &&
-            !wait_phase(smem_u32(&empty[slot]), ((it / s_count) - 1) & 1, abort_flag, p.err)) {
-          ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(smem_u32(&full[slot]), bytes);
-        bulk_g2s(smem_u32(stages + slot * kFusedStageFloats), src, bytes, smem_u32(&full[slot]));
-        src += rows * ks;
-        ++it;
-      }
-    }
+// ---------------------------------------------------------------- weight ring
+
+// The weight stream flows through a ring of s_count stages: stream stage j
+// lands in slot j % s_count, full[slot] completes when its bytes have arrived
+// and empty[slot] when all CW computing warps are done with it. One producer
+// warp (one elected thread) walks the stage table, waiting on empty before
+// refilling a slot; it runs ahead across layer boundaries.
+struct Ring {
+  float* stages;
+  uint64_t* full;
+  uint64_t* empty;
+  volatile int* abort_flag;
+  uint32_t s_count;
+  int32_t* err;
+};
+
+// The warp is done with stream stage j.
+__device__ __forceinline__ void ring_release(const Ring& r, uint32_t j) {
+  __syncwarp();
+  if ((threadIdx.x % kWarp) == 0) mbar_arrive(smem_u32(&r.empty[j % r.s_count]));
+}
+
+__device__ void produce(const Ring& r, const float* wstream, const uint2* tab, uint32_t n_stages) {
+  uint32_t j = 0;
+  for (; j < n_stages; ++j) {
+    const uint32_t slot = j % r.s_count;
+    if (j >= r.s_count &&
+        !wait_phase(smem_u32(&r.empty[slot]), ((j / r.s_count) - 1) & 1, r.abort_flag, r.err))
+      break;
+    const uint2 e = __ldg(tab + j);
+    mbar_arrive_expect_tx(smem_u32(&r.full[slot]), e.y);
+    bulk_g2s(smem_u32(r.stages + slot * kFusedStageFloats), wstream + e.x, e.y,
+             smem_u32(&r.full[slot]));
   }
   // The copies still in flight must land before this CTA's shared memory is
   // released: wait (bounded, regardless of abort) for the last stages issued.
-  const uint32_t first = it > s_count ? it - s_count : 0;
-  for (uint32_t j = first; j < it; ++j) {
-    const uint32_t bar = smem_u32(&full[j % s_count]);
+  const uint32_t first = j > r.s_count ? j - r.s_count : 0;
+  for (uint32_t q = first; q < j; ++q) {
+    const uint32_t bar = smem_u32(&r.full[q % r.s_count]);
     const uint64_t t0 = global_ns();
-    while (!mbar_try_wait(bar, (j / s_count) & 1)) {
+    while (!mbar_try_wait(bar, (q / r.s_count) & 1)) {
       if (global_ns() - t0 > kWaitLimitNs) {
-        if (p.err) atomicOr(reinterpret_cast<unsigned int*>(p.err), DLRM_ERRBIT_TIMEOUT);
+        if (r.err) atomicOr(reinterpret_cast<unsigned int*>(r.err), DLRM_ERRBIT_TIMEOUT);
         break;
       }
     }
@@ -188,168 +211,239 @@ __device__ void produce(const FusedParams& p, float* stages, uint64_t* full, uin
 // ---------------------------------------------------------------- consumers
 
 // C (BM x n_pad; zero beyond n) = act(A (BM x k_pad) W^T + b). `it` is the
-// stage counter shared with the producer's sequence. KSPLIT is a template
-// argument so the staged row length and the column offsets are immediates.
+// stage counter shared with the producer's sequence.
 //
-// Thread tile: BM/4 rows (lm + 4i) x 8 columns (ln + 8j) of a 64-column warp
-// tile, 12 128-bit shared loads per 128 FFMA at BM = 16. Shared-load issue,
-// not bandwidth, bounds this loop (an isolated copy of it runs at ~42% of the
-// FFMA peak; an 8 x 8 tile reaches ~63% alone but at 16 rows per tile costs
-// split K on every layer and runs slower here). With split K the partial
-// sums of k-slice s go to output columns [s * n_pad, (s + 1) * n_pad).
-template <int BM, int KSPLIT, int CW>
-__device__ void gemm_layer(const FusedGemm& L, float* __restrict__ a_s, float* __restrict__ c_s,
-                           int lda, const float* __restrict__ bias_s, int act,
-                           const float* __restrict__ stages, uint64_t* full, uint64_t* empty,
-                           uint32_t& it, uint32_t s_count, volatile int* abort_flag, int32_t* err) {
-  constexpr int TM = BM / 4;
-  constexpr int TN = 8;
-  constexpr int CT = 64;
-  constexpr int KSL = 16;                                // k per warp slice per stage
-  constexpr int kConsumers = CW * kWarp;
-  constexpr int ksplit = KSPLIT;
-  constexpr int KS = KSL * KSPLIT;                       // k per stage
-  constexpr int CPR = KS / 4;                            // 16-byte chunks per staged row
-  constexpr int NACT = CW / KSPLIT;
+// Warp roles: the BM rows form RG = BM / TM row groups of TM rows; warp w
+// takes row group w % RG and slot w / RG of the SLOTS = 8 / RG slots of its
+// group. A slot is a (column group, k-slice) pair: a stage holds KS = 16 *
+// ksplit values of k for `gemm_rows` output columns; it is cut into KSLICES =
+// 2 * ksplit slices of 8 k (two 4-wide steps) and SLOTS / KSLICES column
+// groups of 32 * TN columns. Every tile height reads the same packed stream.
+// All 32 lanes of a warp read the same activation rows, so those 128-bit
+// shared loads are broadcasts (2 wavefronts); lane l owns columns l + 32 j
+// (j < TN), whose staged weight rows are consecutive across lanes (the chunk
+// swizzle puts 8 consecutive rows on 8 distinct bank groups: 4 wavefronts per
+// load). Per 4-wide k step a thread issues TM + TN loads for 4 * TM * TN FMAs
+// as packed fma.rn.f32x2 (the even-k and odd-k partial sums of an output in
+// one float2). Shared-memory wavefronts, not FMA issue, bound this loop: per
+// packed FMA 2 / TM (weights) + 1 / TN (activations) + 1 / (2 BM) (the bulk
+// copy writing the stage), against 1/2 SM cycle of FMA pipe; TM = TN = 8
+// balances the two at BM = 16.
+// The k-slices' partial sums meet in shared memory (the output buffer and,
+// once every warp is done reading it, the input buffer) and all threads add
+// them, the bias and the activation.
+template <int BM, int TM, int TN, int KSL, int KSPLIT, int CW>
+__device__ void gemm_layer(const FusedGemm& L, float* a_s, float* c_s, int lda,
+                           const float* __restrict__ bias_s, int act, const Ring& r, uint32_t& it) {
+  constexpr int RG = BM / TM;
+  constexpr int SLOTS = CW / RG;               // warp slots per row group
+  constexpr int KS = 16 * KSPLIT;              // k per stage
+  constexpr int KSLICES = KS / KSL;
+  constexpr int CGS = SLOTS / KSLICES;         // column groups per pass
+  static_assert(CW == 8 && BM % TM == 0 && CGS >= 1 && KS % KSL == 0, "warp slots");
+  constexpr int STEPS = KSL / 4;               // 4-wide k steps per stage
+  constexpr int CPR = KS / 4;                  // 16-byte chunks per staged row
+  constexpr int WCOLS = 32 * TN;               // columns of one warp
+  // fragments of step s + 1 load while step s computes, when registers allow
+  constexpr bool kDoubleBuffer = TM * TN <= 32;
   const int tid = threadIdx.x;
   const int warp = tid / kWarp;
   const int lane = tid % kWarp;
-  // Lane -> (row group lm, column group ln). A 128-bit shared load is served
-  // per half-warp, and its two quarter-warps share one wavefront only when they
-  // touch disjoint banks (equal addresses still collide). So inside each half
-  // the quarters take complementary row groups {0,1} / {2,3} and complementary
-  // column groups {0..3} / {4..7}: every A and W load costs 2 wavefronts.
-  const int quarter = (lane >> 3) & 1;
-  const int half = lane >> 4;
-  const int lm = ((lane & 7) >> 2) + 2 * quarter;
-  const int ln = (lane & 3) + 4 * (quarter ^ half);
-  const int ct = warp % NACT;
-  const int kslice = warp / NACT;
-  const int sw = CPR == 4 ? ((ln >> 1) & 3) : (ln & 7);  // chunk swizzle of this thread's rows
-  int ph[4];
+  const int rg = warp % RG;
+  const int slot = warp / RG;
+  const int cg = slot % CGS;
+  const int kslice = slot / CGS;
+  const int sw = CPR == 4 ? ((lane >> 1) & 3) : (lane & 7);   // swizzle of rows lane + 32 j
+  int ph[STEPS];
 #pragma unroll
-  for (int s = 0; s < 4; ++s) ph[s] = ((kslice * 4 + s) ^ sw) * 4;
-  const float* a_row = a_s + lm * lda + kslice * KSL;
+  for (int s = 0; s < STEPS; ++s) ph[s] = ((kslice * STEPS + s) ^ sw) * 4;
+  const float* a_base = a_s + rg * TM * lda + kslice * KSL;
+  const int per_pass = CGS * WCOLS;
 
   for (int pass = 0; pass < L.passes; ++pass) {
-    const int tiles_here = gemm_rows(L, pass, CW) / CT;
-    const bool active = ct < tiles_here;
-    float acc[TM][TN];
+    const bool active = cg * WCOLS < gemm_rows(L, pass);
+    float2 acc[TM][TN];
 #pragma unroll
     for (int i = 0; i < TM; ++i)
 #pragma unroll
-      for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
+      for (int j = 0; j < TN; ++j) acc[i][j] = make_float2(0.f, 0.f);
 
     for (int kst = 0; kst < L.n_kst; ++kst, ++it) {
-      const uint32_t slot = it % s_count;
-      wait_phase(smem_u32(&full[slot]), (it / s_count) & 1, abort_flag, err);
+      const uint32_t st = it % r.s_count;
+      wait_phase(smem_u32(&r.full[st]), (it / r.s_count) & 1, r.abort_flag, r.err);
       if (active) {
-        const float* ws = stages + slot * kFusedStageFloats + (ct * CT + ln) * KS;
-        const float* as = a_row + kst * KS;
-        float4 av[2][TM], wv[2][TN];
+        const float* ws = r.stages + st * kFusedStageFloats + (cg * WCOLS + lane) * KS;
+        const float* as = a_base + kst * KS;
+        if (kDoubleBuffer) {
+          float4 wv[2][TN], av[2][TM];
 #pragma unroll
-        for (int i = 0; i < TM; ++i) av[0][i] = *reinterpret_cast<const float4*>(as + 4 * i * lda);
+          for (int j = 0; j < TN; ++j)
+            wv[0][j] = *reinterpret_cast<const float4*>(ws + 32 * j * KS + ph[0]);
 #pragma unroll
-        for (int j = 0; j < TN; ++j)
-          wv[0][j] = *reinterpret_cast<const float4*>(ws + 8 * j * KS + ph[0]);
+          for (int i = 0; i < TM; ++i) av[0][i] = *reinterpret_cast<const float4*>(as + i * lda);
 #pragma unroll
-        for (int step = 0; step < 4; ++step) {
-          const int cur = step & 1;
-          if (step < 3) {      // fragments of the next 4-wide k step
+          for (int step = 0; step < STEPS; ++step) {
+            const int cur = step & 1;
+            if (step + 1 < STEPS) {
+#pragma unroll
+              for (int j = 0; j < TN; ++j)
+                wv[cur ^ 1][j] =
+                    *reinterpret_cast<const float4*>(ws + 32 * j * KS + ph[step + 1]);
+#pragma unroll
+              for (int i = 0; i < TM; ++i)
+                av[cur ^ 1][i] = *reinterpret_cast<const float4*>(as + i * lda + 4 * (step + 1));
+            }
+            // component-outer: TM * TN independent accumulators between the
+            // two dependent updates of each
 #pragma unroll
             for (int i = 0; i < TM; ++i)
-              av[cur ^ 1][i] = *reinterpret_cast<const float4*>(as + 4 * i * lda + 4 * (step + 1));
+#pragma unroll
+              for (int j = 0; j < TN; ++j)
+                acc[i][j] = __ffma2_rn(make_float2(av[cur][i].x, av[cur][i].y),
+                                       make_float2(wv[cur][j].x, wv[cur][j].y), acc[i][j]);
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
+#pragma unroll
+              for (int j = 0; j < TN; ++j)
+                acc[i][j] = __ffma2_rn(make_float2(av[cur][i].z, av[cur][i].w),
+                                       make_float2(wv[cur][j].z, wv[cur][j].w), acc[i][j]);
+          }
+        } else {
+#pragma unroll
+          for (int step = 0; step < STEPS; ++step) {
+            float4 wv[TN];
 #pragma unroll
             for (int j = 0; j < TN; ++j)
-              wv[cur ^ 1][j] = *reinterpret_cast<const float4*>(ws + 8 * j * KS + ph[step + 1]);
+              wv[j] = *reinterpret_cast<const float4*>(ws + 32 * j * KS + ph[step]);
+#pragma unroll
+            for (int i = 0; i < TM; ++i) {
+              const float4 a = *reinterpret_cast<const float4*>(as + i * lda + 4 * step);
+#pragma unroll
+              for (int j = 0; j < TN; ++j)
+                acc[i][j] = __ffma2_rn(make_float2(a.x, a.y), make_float2(wv[j].x, wv[j].y),
+                                       acc[i][j]);
+#pragma unroll
+              for (int j = 0; j < TN; ++j)
+                acc[i][j] = __ffma2_rn(make_float2(a.z, a.w), make_float2(wv[j].z, wv[j].w),
+                                       acc[i][j]);
+            }
           }
-          // component-outer: TM*TN independent accumulators between dependent FMAs
-#pragma unroll
-          for (int i = 0; i < TM; ++i)
-#pragma unroll
-            for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(av[cur][i].x, wv[cur][j].x, acc[i][j]);
-#pragma unroll
-          for (int i = 0; i < TM; ++i)
-#pragma unroll
-            for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(av[cur][i].y, wv[cur][j].y, acc[i][j]);
-#pragma unroll
-          for (int i = 0; i < TM; ++i)
-#pragma unroll
-            for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(av[cur][i].z, wv[cur][j].z, acc[i][j]);
-#pragma unroll
-          for (int i = 0; i < TM; ++i)
-#pragma unroll
-            for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(av[cur][i].w, wv[cur][j].w, acc[i][j]);
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
+      ring_release(r, it);
     }
 
-    const int col0 = pass * CW * CT;
-    if (ksplit == 1) {
+    const int c0 = pass * per_pass + cg * WCOLS + lane;
+    if (KSLICES == 1) {
       if (active) {
 #pragma unroll
         for (int j = 0; j < TN; ++j) {
-          const int n = col0 + ct * CT + ln + 8 * j;
+          const int n = c0 + 32 * j;
           const float bv = bias_s[L.b_off + n];
 #pragma unroll
           for (int i = 0; i < TM; ++i) {
-            const float v = apply_act(acc[i][j] + bv, act);
-            c_s[(lm + 4 * i) * lda + n] = (n < L.n) ? v : 0.f;
+            const float v = apply_act((acc[i][j].x + acc[i][j].y) + bv, act);
+            c_s[(rg * TM + i) * lda + n] = (n < L.n) ? v : 0.f;
           }
         }
       }
-    } else {
-#pragma unroll
-      for (int i = 0; i < TM; ++i)
-#pragma unroll
-        for (int j = 0; j < TN; ++j)
-          c_s[(lm + 4 * i) * lda + kslice * L.n_pad + ct * CT + ln + 8 * j] = acc[i][j];
       consumer_sync<CW>();
-      // n_pad = 64 * 2^j: 4 columns per thread step, shifts instead of divisions
-      const int np = L.n_pad;
-      const int q_shift = 31 - __clz(np >> 2);           // log2(np / 4)
-      for (int e = tid; e < BM * (np >> 2); e += kConsumers) {
+    } else if (pass + 1 == L.passes) {
+      // Parallel reduction. Once every warp is past its k-loop the layer's
+      // input is dead: partial set q goes to the output buffer (q < KSPLIT)
+      // or the input buffer (q >= KSPLIT), at columns (q % KSPLIT) * n_pad
+      // + the pass's column; then all threads add the sets, add the bias and
+      // apply the activation. Single-pass layers have n_pad = per_pass and
+      // rows of lda >= KSPLIT * n_pad floats.
+      if (KSLICES > KSPLIT) consumer_sync<CW>();   // the input becomes scratch
+      if (active) {
+        float* dst = kslice < KSPLIT ? c_s + kslice * L.n_pad + c0
+                                     : a_s + (kslice - KSPLIT) * L.n_pad + c0 - pass * per_pass;
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+          for (int j = 0; j < TN; ++j) dst[(rg * TM + i) * lda + 32 * j] = acc[i][j].x + acc[i][j].y;
+      }
+      consumer_sync<CW>();
+      const int np = gemm_rows(L, pass);
+      const int col0 = pass * per_pass;
+      const int q_shift = 31 - __clz(np >> 2);          // np / 4 is a power of two
+      for (int e = tid; e < BM * (np >> 2); e += CW * kWarp) {
         const int m = e >> q_shift;
         const int n = (e - (m << q_shift)) << 2;
-        float4 v = *reinterpret_cast<const float4*>(c_s + m * lda + n);
+        const float* base_c = c_s + m * lda + n;
+        const float* base_a = a_s + m * lda + n;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int s = 1; s < ksplit; ++s) {
-          const float4 u = *reinterpret_cast<const float4*>(c_s + m * lda + s * np + n);
+        for (int q = 0; q < KSLICES; ++q) {
+          const float4 u = *reinterpret_cast<const float4*>(
+              (q < KSPLIT ? base_c : base_a) + (q % KSPLIT) * L.n_pad + (q < KSPLIT ? col0 : 0));
           v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w;
         }
-        const float4 bv = *reinterpret_cast<const float4*>(bias_s + L.b_off + n);
-        v.x = (n + 0 < L.n) ? apply_act(v.x + bv.x, act) : 0.f;
-        v.y = (n + 1 < L.n) ? apply_act(v.y + bv.y, act) : 0.f;
-        v.z = (n + 2 < L.n) ? apply_act(v.z + bv.z, act) : 0.f;
-        v.w = (n + 3 < L.n) ? apply_act(v.w + bv.w, act) : 0.f;
-        *reinterpret_cast<float4*>(c_s + m * lda + n) = v;
+        const int nn = col0 + n;
+        const float4 bv = *reinterpret_cast<const float4*>(bias_s + L.b_off + nn);
+        v.x = (nn + 0 < L.n) ? apply_act(v.x + bv.x, act) : 0.f;
+        v.y = (nn + 1 < L.n) ? apply_act(v.y + bv.y, act) : 0.f;
+        v.z = (nn + 2 < L.n) ? apply_act(v.z + bv.z, act) : 0.f;
+        v.w = (nn + 3 < L.n) ? apply_act(v.w + bv.w, act) : 0.f;
+        *reinterpret_cast<float4*>(c_s + m * lda + nn) = v;
+      }
+      consumer_sync<CW>();
+    } else {
+      // A pass before the last of a multi-pass layer (the input is still
+      // live): k-slice q adds its partial sums to those of slices 0 .. q-1
+      // in place, the last one adding the bias and applying the activation.
+#pragma unroll 1
+      for (int q = 0; q < KSLICES; ++q) {
+        if (kslice == q && active) {
+#pragma unroll
+          for (int j = 0; j < TN; ++j) {
+            const int n = c0 + 32 * j;
+            const float bv = bias_s[L.b_off + n];
+#pragma unroll
+            for (int i = 0; i < TM; ++i) {
+              float* dst = c_s + (rg * TM + i) * lda + n;
+              float v = acc[i][j].x + acc[i][j].y;
+              if (q > 0) v += *dst;
+              if (q == KSLICES - 1) v = (n < L.n) ? apply_act(v + bv, act) : 0.f;
+              *dst = v;
+            }
+          }
+        }
+        consumer_sync<CW>();
       }
     }
-    consumer_sync<CW>();
   }
 }
 
 template <int BM, int CW>
 __device__ void gemm_dispatch(const FusedGemm& L, float* a_s, float* c_s, int lda,
-                              const float* bias_s, int act, int zero_to, const float* stages,
-                              uint64_t* full, uint64_t* empty, uint32_t& it, uint32_t s_count,
-                              volatile int* abort_flag, int32_t* err) {
-  switch (L.ksplit) {
-    case 1:
-      gemm_layer<BM, 1, CW>(L, a_s, c_s, lda, bias_s, act, stages, full, empty, it, s_count, abort_flag, err);
-      break;
-    case 2:
-      gemm_layer<BM, 2, CW>(L, a_s, c_s, lda, bias_s, act, stages, full, empty, it, s_count, abort_flag, err);
-      break;
-    case 4:
-      gemm_layer<BM, 4, CW>(L, a_s, c_s, lda, bias_s, act, stages, full, empty, it, s_count, abort_flag, err);
-      break;
-    default:
-      gemm_layer<BM, 8, CW>(L, a_s, c_s, lda, bias_s, act, stages, full, empty, it, s_count, abort_flag, err);
-      break;
+                              const float* bias_s, int act, int zero_to, const Ring& r,
+                              uint32_t& it) {
+  // TM rows per warp (8 when the tile has 8 or more rows), k-slices of KSL.
+  // A pass covers 64 * tn / ksplit columns with SLOTS / (16 * ksplit / KSL)
+  // column groups, which fixes the lane width TN (at least 1).
+  constexpr int TM = BM >= 8 ? 8 : 4;
+  constexpr int KSL = 16;
+  constexpr int SLOTS = CW * TM / BM;
+#define DLRM_GEMM_TN(TN16_, KS_)                                                     \
+  ((2 * (TN16_) / (KS_)) / (SLOTS / (16 * (KS_) / KSL)) > 0                          \
+       ? (2 * (TN16_) / (KS_)) / (SLOTS / (16 * (KS_) / KSL))                        \
+       : 1)
+#define DLRM_GEMM_CASE(TN16_, KS_)                                                   \
+  gemm_layer<BM, TM, DLRM_GEMM_TN(TN16_, KS_), KSL, KS_, CW>(L, a_s, c_s, lda, bias_s, act, r, it)
+  if (L.ksplit == 1) {
+    DLRM_GEMM_CASE(8, 1);
+  } else {
+    switch (L.tn) {
+      case 8: DLRM_GEMM_CASE(8, 2); break;
+      case 4: DLRM_GEMM_CASE(4, 2); break;
+      case 2: DLRM_GEMM_CASE(2, 2); break;
+      default: DLRM_GEMM_CASE(1, 2); break;
+    }
   }
+#undef DLRM_GEMM_CASE
+#undef DLRM_GEMM_TN
   const int extra = zero_to - L.n_pad;
   for (int e = threadIdx.x; e < BM * extra; e += CW * kWarp) {
     const int m = e / extra;
@@ -359,8 +453,7 @@ __device__ void gemm_dispatch(const FusedGemm& L, float* a_s, float* c_s, int ld
 }
 
 template <int BM, int CW>
-__device__ void consume(const FusedParams& p, float* stages, uint64_t* full, uint64_t* empty,
-                        volatile int* abort_flag, float* act0, float* act1, float* zs,
+__device__ void consume(const FusedParams& p, const Ring& ring, float* act0, float* act1, float* zs,
                         int* rowidx_s, float* bias_s, float* wlast_s) {
   constexpr int kConsumers = CW * kWarp;
   const int tid = threadIdx.x;
@@ -460,14 +553,12 @@ __device__ void consume(const FusedParams& p, float* stages, uint64_t* full, uin
     else cp_async_commit();
   }
 
-  const uint32_t s_count = static_cast<uint32_t>(p.stages);
   uint32_t it = 0;
   float* in = act0;
   float* out = act1;
   for (int g = 0; g < p.n_bot; ++g) {
     const int zero_to = (g + 1 < p.n_bot) ? p.gemm[g + 1].k_pad : p.gemm[g].n_pad;
-    gemm_dispatch<BM, CW>(p.gemm[g], in, out, p.lda, bias_s, DLRM_ACT_RELU, zero_to, stages, full,
-                      empty, it, s_count, abort_flag, p.err);
+    gemm_dispatch<BM, CW>(p.gemm[g], in, out, p.lda, bias_s, DLRM_ACT_RELU, zero_to, ring, it);
     float* t = in; in = out; out = t;
     stamp(p, 2 + g);
   }
@@ -559,8 +650,7 @@ __device__ void consume(const FusedParams& p, float* stages, uint64_t* full, uin
   out = (r == act0) ? act1 : act0;
   for (int g = p.n_bot; g < p.n_gemm; ++g) {
     const int zero_to = (g + 1 < p.n_gemm) ? p.gemm[g + 1].k_pad : p.k_last;
-    gemm_dispatch<BM, CW>(p.gemm[g], in, out, p.lda, bias_s, DLRM_ACT_RELU, zero_to, stages, full,
-                      empty, it, s_count, abort_flag, p.err);
+    gemm_dispatch<BM, CW>(p.gemm[g], in, out, p.lda, bias_s, DLRM_ACT_RELU, zero_to, ring, it);
     float* t = in; in = out; out = t;
     stamp(p, 3 + g);
   }
@@ -597,9 +687,11 @@ fused_forward_kernel(const __grid_constant__ FusedParams p) {
   float* zs = reinterpret_cast<float*>(smem_raw + p.off_z);
   float* bias_s = reinterpret_cast<float*>(smem_raw + p.off_bias);
   float* wlast_s = reinterpret_cast<float*>(smem_raw + p.off_wlast);
+  int* rowidx_s = reinterpret_cast<int*>(smem_raw + p.off_rowidx);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw + p.off_bar);
   uint64_t* empty = full + p.stages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + p.stages);
+  const Ring r{stages, full, empty, abort_flag, static_cast<uint32_t>(p.stages), p.err};
   const int warp = threadIdx.x / kWarp;
   stamp(p, 0);
   if (threadIdx.x == 0) {
@@ -613,11 +705,11 @@ fused_forward_kernel(const __grid_constant__ FusedParams p) {
   }
   __syncthreads();
   if (warp == CW) {
-    if (threadIdx.x % kWarp == 0) produce<CW>(p, stages, full, empty, abort_flag);
+    if (threadIdx.x % kWarp == 0)
+      produce(r, p.wstream, p.stage_tab, static_cast<uint32_t>(p.n_stages));
     return;
   }
-  int* rowidx_s = reinterpret_cast<int*>(smem_raw + p.off_rowidx);
-  consume<BM, CW>(p, stages, full, empty, abort_flag, act0, act1, zs, rowidx_s, bias_s, wlast_s);
+  consume<BM, CW>(p, r, act0, act1, zs, rowidx_s, bias_s, wlast_s);
 }
 
 template <int BM, int CW>
@@ -640,6 +732,7 @@ cudaError_t fused_prepare(int bm, int cw) {
   if (cw != 8) return cudaErrorInvalidValue;
   if (bm == 16) return enable_smem<16, 8>();
   if (bm == 8) return enable_smem<8, 8>();
+  if (bm == 4) return enable_smem<4, 8>();
   return cudaErrorInvalidValue;
 }
 
@@ -651,8 +744,10 @@ cudaError_t launch_fused(const FusedParams& p, int bm, cudaStream_t stream) {
   const unsigned threads = static_cast<unsigned>((p.cw + 1) * kWarp);
   if (bm == 16)
     fused_forward_kernel<16, 8><<<grid, threads, p.smem_bytes, stream>>>(p);
-  else
+  else if (bm == 8)
     fused_forward_kernel<8, 8><<<grid, threads, p.smem_bytes, stream>>>(p);
+  else
+    fused_forward_kernel<4, 8><<<grid, threads, p.smem_bytes, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -673,9 +768,8 @@ size_t align128(size_t x) { return (x + 127) / 128 * 128; }
 bool fused_plan(int n_dense, int k_tables, int d, int bag, const std::vector<int>& ln_bot,
                 const std::vector<int>& ln_top, const std::vector<std::vector<float>>& w,
                 const std::vector<std::vector<float>>& b, const GatherTables& tabs,
-                size_t smem_limit, int cw, FusedPlan* plan) {
+                int max_batch, int sms, size_t smem_limit, int cw, FusedPlan* plan) {
   if (cw != 8) return false;
-  const int ctw = 512 / cw;     // column tile width (64)
   const int ksl = 16;           // k per warp slice per stage
   const int n_bot = static_cast<int>(ln_bot.size()) - 1;
   const int n_top = static_cast<int>(ln_top.size()) - 1;
@@ -702,28 +796,32 @@ bool fused_plan(int n_dense, int k_tables, int d, int bag, const std::vector<int
     kin[g] = g < n_bot ? ln_bot[g] : ln_top[g - n_bot];
     nout[g] = g < n_bot ? ln_bot[g + 1] : ln_top[g - n_bot + 1];
   }
-  int widest = 512;   // split-K partials span 512 columns of the output buffer
+  // Layer shapes. Wider than 256 columns: 32 x 8-column warps in two column
+  // groups per pass (ksplit 1), n_pad a multiple of 256. Otherwise one column
+  // group of n_pad = 32 * tn (a power of two >= 32) and two k-slices.
+  int widest = 0;
   int bias_floats = 0;
   for (int g = 0; g < n_gemm; ++g) {
     FusedGemm& L = p.gemm[g];
-    int n_wt = (nout[g] + ctw - 1) / ctw;
-    if (n_wt < cw) {
-      int p2 = 1;
-      while (p2 < n_wt) p2 *= 2;
-      n_wt = p2;
-      L.ksplit = cw / n_wt;
-      L.passes = 1;
-    } else {
-      L.ksplit = 1;
-      L.passes = (n_wt + cw - 1) / cw;
-    }
     L.n = nout[g];
-    L.n_pad = ctw * n_wt;
+    if (L.n > 256) {
+      L.tn = 8;
+      L.ksplit = 1;
+      L.n_pad = static_cast<int>(round_up(L.n, 256));
+      L.passes = (L.n_pad + 511) / 512;
+    } else {
+      int np = 32;
+      while (np < L.n) np *= 2;
+      L.n_pad = np;
+      L.tn = np / 32;
+      L.ksplit = 2;
+      L.passes = 1;
+    }
     L.k_pad = static_cast<int>(round_up(kin[g], ksl * L.ksplit));
     L.n_kst = L.k_pad / (ksl * L.ksplit);
     L.b_off = bias_floats;
     bias_floats += L.n_pad;
-    widest = std::max({widest, L.k_pad, L.n_pad});
+    widest = std::max({widest, L.k_pad, L.n_pad * L.ksplit});
   }
   p.k_last = static_cast<int>(round_up(ln_top[n_top - 1], 4));
   p.b_last = bias_floats;
@@ -740,7 +838,11 @@ bool fused_plan(int n_dense, int k_tables, int d, int bag, const std::vector<int
   // first (one wave of tiles), then a weight stage is given up.
   const size_t per_sample_z = static_cast<size_t>(k_tables) * p.ldz * sizeof(float);
   bool placed = false;
-  for (int bm : {16, 8}) {
+  int first_bm = 16;
+  if (max_batch <= 4 * sms) first_bm = 4;
+  else if (max_batch <= 8 * sms) first_bm = 8;
+  for (int bm : {16, 8, 4}) {
+    if (bm > first_bm) continue;
     for (int mode = 0; mode < 3 && !placed; ++mode) {
       if (bag != 1 && mode < 2) continue;
       for (int stages : {4, 3}) {
@@ -785,19 +887,23 @@ bool fused_plan(int n_dense, int k_tables, int d, int bag, const std::vector<int
   }
   if (!placed || static_cast<size_t>(p.smem_bytes) > smem_limit) return false;
 
-  // packed weight stream, in the producer's order
+  // packed weight stream in consumption order, and its stage table
   plan->wstream.clear();
+  plan->stage_tab.clear();
   for (int g = 0; g < n_gemm; ++g) {
     const FusedGemm& L = p.gemm[g];
     const int ks = ksl * L.ksplit;
     const std::vector<float>& W = w[g];
     for (int pass = 0; pass < L.passes; ++pass) {
-      const int rows = gemm_rows(L, pass, cw);
+      const int rows = gemm_rows(L, pass);
       for (int kst = 0; kst < L.n_kst; ++kst) {
         const size_t base = plan->wstream.size();
+        if (base > 0xffffffffu) return false;
+        plan->stage_tab.push_back(make_uint2(static_cast<unsigned>(base),
+                                             static_cast<unsigned>(rows * ks * sizeof(float))));
         plan->wstream.resize(base + static_cast<size_t>(rows) * ks, 0.f);
         for (int rr = 0; rr < rows; ++rr) {
-          const int n = pass * cw * ctw + rr;
+          const int n = pass * gemm_cols_per_pass(L) + rr;
           if (n >= L.n) continue;
           for (int kk = 0; kk < ks; ++kk) {
             const int kg = kst * ks + kk;
@@ -810,6 +916,7 @@ bool fused_plan(int n_dense, int k_tables, int d, int bag, const std::vector<int
       }
     }
   }
+  p.n_stages = static_cast<int>(plan->stage_tab.size());
   plan->bias.assign(bias_floats, 0.f);
   for (int g = 0; g < n_gemm; ++g)
     for (int n = 0; n < nout[g]; ++n) plan->bias[p.gemm[g].b_off + n] = b[g][n];

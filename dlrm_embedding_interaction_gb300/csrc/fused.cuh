@@ -8,43 +8,46 @@
 
 namespace dlrm {
 
-// Consumer warps per CTA: 8 (thread tile 4 rows x 8 columns, 64-column warp
-// tiles) or 16 (4 x 4, 32-column warp tiles); one more warp is the producer.
+// Warps per CTA: 8 computing warps and one producer warp.
 constexpr int kFusedStageFloats = 8192;                        // 32 KB weight stage
 constexpr int kFusedMaxGemm = 2 * DLRM_MAX_LAYERS;
 
 // One GEMM layer of the weight stream. Its weights occupy `passes * n_kst`
-// consecutive stages of the packed stream: pass p covers output rows
-// [CW*CT p, CW*CT p + rows) (CW consumer warps, CT = 512 / CW column tile),
-// stage s covers k in [s*KS, (s+1)*KS), KS = 16*ksplit,
-// stored row-major (rows x KS) with 16-byte chunk c of row r at position
-// c ^ swz(r) (swz = (r >> 1) & 3 when KS = 16, else r & 7).
-//   n      output width; n_pad = CT * 2^j < 512 (ksplit = CW / (n_pad / CT))
-//          or a multiple of CT >= 512 (ksplit = 1)
+// consecutive stages of the packed stream: pass p covers output columns
+// [P p, P p + rows), P = (2 / ksplit) * 32 * tn, stage s covers k in
+// [s*KS, (s+1)*KS), KS = 16*ksplit, stored row-major (rows x KS) with 16-byte
+// chunk c of row r at position c ^ swz(r) (swz = (r >> 1) & 3 when KS = 16,
+// else r & 7).
+//   n      output width; wider than 256: n_pad = round_up(n, 256), tn = 8,
+//          ksplit = 1; else n_pad = 32 * tn (tn a power of two), ksplit = 2
+//   tn     columns per lane when the tile's rows form 4 row groups
 //   k_pad  input width padded to a multiple of KS (zero weights)
 //   b_off  offset of the layer's zero-padded bias in the bias block
 struct FusedGemm {
-  int n, n_pad, k_pad, ksplit, passes, n_kst, b_off;
+  int n, n_pad, tn, k_pad, ksplit, passes, n_kst, b_off;
 };
 
 struct FusedParams {
   int batch, n_dense, k_tables, d, bag, n_bot, n_top;
   int n_gemm;        // n_bot + n_top - 1 (the last top layer is the N = 1 dot)
-  int cw;            // consumer warps (8 or 16)
+  int cw;            // computing warps (8)
   int lda;           // activation row stride (floats), >= 516, = 4 mod 32
   int ldz;           // bag-sum row stride, round_up(d, 4) + 4
   int sg;            // samples per gather/interaction group
   int prefetch_z;    // 1: all BM samples' rows are fetched at kernel start (bag 1)
   int zbuf;          // bag 1 without prefetch: 2 group buffers, rows streamed with cp.async
   int stages;        // weight ring depth
+  int n_stages;      // stages of the whole weight stream
   int k_last;        // padded input width of the last (N = 1) layer
   int b_last;        // its bias offset in the bias block
   int bias_floats;   // bias block length (multiple of 4)
   // shared-memory carve (bytes from the dynamic base)
   int off_act0, off_act1, off_z, off_bias, off_wlast, off_bar, off_rowidx;
+  // barriers block: full[stages], empty[stages] (u64), abort flag
   int smem_bytes;
   FusedGemm gemm[kFusedMaxGemm];
   const float* wstream;    // packed weight stream
+  const uint2* stage_tab;  // per stream stage: (offset in floats, bytes)
   const float* bias;       // bias block
   const float* wlast;      // last layer weights, k_last floats (zero-padded)
   const float* dense;
@@ -63,14 +66,18 @@ struct FusedPlan {
   FusedParams params{};
   int bm = 0;
   std::vector<float> wstream, bias, wlast;
+  std::vector<uint2> stage_tab;
 };
 
 // Builds the plan from host copies of the (out, in) weights and biases;
 // false when the model does not fit the fused kernel.
+// The tile height is the smallest of 4, 8, 16 rows whose tiles of max_batch
+// fit one wave on `sms` SMs (16 past that), falling back to smaller tiles when
+// the shared-memory carve does not fit.
 bool fused_plan(int n_dense, int k_tables, int d, int bag, const std::vector<int>& ln_bot,
                 const std::vector<int>& ln_top, const std::vector<std::vector<float>>& w,
                 const std::vector<std::vector<float>>& b, const GatherTables& tabs,
-                size_t smem_limit, int consumer_warps, FusedPlan* plan);
+                int max_batch, int sms, size_t smem_limit, int consumer_warps, FusedPlan* plan);
 
 cudaError_t fused_prepare(int bm, int consumer_warps);
 cudaError_t launch_fused(const FusedParams& p, int bm, cudaStream_t stream);
