@@ -433,7 +433,7 @@ def run_ours(args, rank, world, local_rank):
     phases_us = None
     if path_used == dl.PATH_FUSED:
         tiles = None
-        buf = torch.zeros(((cfg.batch + 7) // 8) * dl.TRACE_SLOTS, dtype=torch.int64, device=dev)
+        buf = torch.zeros(((cfg.batch + 3) // 4) * dl.TRACE_SLOTS, dtype=torch.int64, device=dev)
         rows = model.set_phase_trace(buf)
         tiles = (cfg.batch + rows - 1) // rows
         pnames = model.phase_names()

@@ -181,6 +181,24 @@ __device__ __forceinline__ void ring_release(const Ring& r, uint32_t j) {
   if ((threadIdx.x % kWarp) == 0) mbar_arrive(smem_u32(&r.empty[j % r.s_count]));
 }
 
+// Bring this CTA's 1/gridDim share of the weight stream (16-byte granules)
+// into L2 at kernel start: every CTA then finds each stage in L2, and a
+// stage consumed faster than HBM latency does not stall the ring.
+__device__ void prefetch_stream_l2(const float* wstream, size_t floats) {
+  const size_t granules = floats / 4;
+  const size_t per = (granules + gridDim.x - 1) / gridDim.x;
+  const size_t g0 = per * blockIdx.x;
+  if (g0 >= granules) return;
+  size_t left = (granules - g0 < per ? granules - g0 : per) * 16;
+  const char* src = reinterpret_cast<const char*>(wstream) + g0 * 16;
+  while (left > 0) {
+    const uint32_t chunk = static_cast<uint32_t>(left < 65536 ? left : 65536);
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(chunk) : "memory");
+    src += chunk;
+    left -= chunk;
+  }
+}
+
 __device__ void produce(const Ring& r, const float* wstream, const uint2* tab, uint32_t n_stages) {
   uint32_t j = 0;
   for (; j < n_stages; ++j) {
@@ -420,10 +438,11 @@ template <int BM, int CW>
 __device__ void gemm_dispatch(const FusedGemm& L, float* a_s, float* c_s, int lda,
                               const float* bias_s, int act, int zero_to, const Ring& r,
                               uint32_t& it) {
-  // TM rows per warp (8 when the tile has 8 or more rows), k-slices of KSL.
-  // A pass covers 64 * tn / ksplit columns with SLOTS / (16 * ksplit / KSL)
-  // column groups, which fixes the lane width TN (at least 1).
-  constexpr int TM = BM >= 8 ? 8 : 4;
+  // TM rows per warp (the whole tile up to 8 rows, else two row groups of
+  // BM / 2), k-slices of KSL. A pass covers 64 * tn / ksplit columns with
+  // SLOTS / (16 * ksplit / KSL) column groups, which fixes the lane width TN
+  // (at least 1).
+  constexpr int TM = BM <= 8 ? BM : BM / 2;
   constexpr int KSL = 16;
   constexpr int SLOTS = CW * TM / BM;
 #define DLRM_GEMM_TN(TN16_, KS_)                                                     \
@@ -705,8 +724,10 @@ fused_forward_kernel(const __grid_constant__ FusedParams p) {
   }
   __syncthreads();
   if (warp == CW) {
-    if (threadIdx.x % kWarp == 0)
+    if (threadIdx.x % kWarp == 0) {
+      prefetch_stream_l2(p.wstream, p.stream_floats);
       produce(r, p.wstream, p.stage_tab, static_cast<uint32_t>(p.n_stages));
+    }
     return;
   }
   consume<BM, CW>(p, r, act0, act1, zs, rowidx_s, bias_s, wlast_s);
@@ -730,10 +751,14 @@ cudaError_t enable_smem() {
 
 cudaError_t fused_prepare(int bm, int cw) {
   if (cw != 8) return cudaErrorInvalidValue;
-  if (bm == 16) return enable_smem<16, 8>();
-  if (bm == 8) return enable_smem<8, 8>();
-  if (bm == 4) return enable_smem<4, 8>();
-  return cudaErrorInvalidValue;
+  switch (bm) {
+    case 16: return enable_smem<16, 8>();
+    case 14: return enable_smem<14, 8>();
+    case 12: return enable_smem<12, 8>();
+    case 8: return enable_smem<8, 8>();
+    case 4: return enable_smem<4, 8>();
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_fused(const FusedParams& p, int bm, cudaStream_t stream) {
@@ -742,12 +767,13 @@ cudaError_t launch_fused(const FusedParams& p, int bm, cudaStream_t stream) {
   cudaError_t e = fused_prepare(bm, p.cw);
   if (e != cudaSuccess) return e;
   const unsigned threads = static_cast<unsigned>((p.cw + 1) * kWarp);
-  if (bm == 16)
-    fused_forward_kernel<16, 8><<<grid, threads, p.smem_bytes, stream>>>(p);
-  else if (bm == 8)
-    fused_forward_kernel<8, 8><<<grid, threads, p.smem_bytes, stream>>>(p);
-  else
-    fused_forward_kernel<4, 8><<<grid, threads, p.smem_bytes, stream>>>(p);
+  switch (bm) {
+    case 16: fused_forward_kernel<16, 8><<<grid, threads, p.smem_bytes, stream>>>(p); break;
+    case 14: fused_forward_kernel<14, 8><<<grid, threads, p.smem_bytes, stream>>>(p); break;
+    case 12: fused_forward_kernel<12, 8><<<grid, threads, p.smem_bytes, stream>>>(p); break;
+    case 8: fused_forward_kernel<8, 8><<<grid, threads, p.smem_bytes, stream>>>(p); break;
+    default: fused_forward_kernel<4, 8><<<grid, threads, p.smem_bytes, stream>>>(p); break;
+  }
   return cudaGetLastError();
 }
 
@@ -838,10 +864,15 @@ bool fused_plan(int n_dense, int k_tables, int d, int bag, const std::vector<int
   // first (one wave of tiles), then a weight stage is given up.
   const size_t per_sample_z = static_cast<size_t>(k_tables) * p.ldz * sizeof(float);
   bool placed = false;
+  // smallest tile height whose tiles of max_batch fit one wave (16 past that)
   int first_bm = 16;
-  if (max_batch <= 4 * sms) first_bm = 4;
-  else if (max_batch <= 8 * sms) first_bm = 8;
-  for (int bm : {16, 8, 4}) {
+  for (int bm : {4, 8, 12, 14}) {
+    if ((max_batch + bm - 1) / bm <= sms) {
+      first_bm = bm;
+      break;
+    }
+  }
+  for (int bm : {16, 14, 12, 8, 4}) {
     if (bm > first_bm) continue;
     for (int mode = 0; mode < 3 && !placed; ++mode) {
       if (bag != 1 && mode < 2) continue;
@@ -917,6 +948,7 @@ bool fused_plan(int n_dense, int k_tables, int d, int bag, const std::vector<int
     }
   }
   p.n_stages = static_cast<int>(plan->stage_tab.size());
+  p.stream_floats = plan->wstream.size();
   plan->bias.assign(bias_floats, 0.f);
   for (int g = 0; g < n_gemm; ++g)
     for (int n = 0; n < nout[g]; ++n) plan->bias[p.gemm[g].b_off + n] = b[g][n];

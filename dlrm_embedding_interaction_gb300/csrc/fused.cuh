@@ -48,6 +48,7 @@ struct FusedParams {
   FusedGemm gemm[kFusedMaxGemm];
   const float* wstream;    // packed weight stream
   const uint2* stage_tab;  // per stream stage: (offset in floats, bytes)
+  size_t stream_floats;    // length of the weight stream (a multiple of 4)
   const float* bias;       // bias block
   const float* wlast;      // last layer weights, k_last floats (zero-padded)
   const float* dense;
@@ -71,9 +72,9 @@ struct FusedPlan {
 
 // Builds the plan from host copies of the (out, in) weights and biases;
 // false when the model does not fit the fused kernel.
-// The tile height is the smallest of 4, 8, 16 rows whose tiles of max_batch
-// fit one wave on `sms` SMs (16 past that), falling back to smaller tiles when
-// the shared-memory carve does not fit.
+// The tile height is the smallest of 4, 8, 12, 14, 16 rows whose tiles of
+// max_batch fit one wave on `sms` SMs (16 past that), falling back to smaller
+// tiles when the shared-memory carve does not fit.
 bool fused_plan(int n_dense, int k_tables, int d, int bag, const std::vector<int>& ln_bot,
                 const std::vector<int>& ln_top, const std::vector<std::vector<float>>& w,
                 const std::vector<std::vector<float>>& b, const GatherTables& tabs,
