@@ -35,6 +35,56 @@ __device__ __forceinline__ void pair_from_index(int p, int& i, int& j) {
   j = p - ii * (ii - 1) / 2;
 }
 
+// Pair dots in 4 x 4 register blocks. The lower triangle of one sample's
+// Gram matrix Z Z^T (Z = F rows of d4 float4, in shared memory) is cut into
+// blocks (bi, bj), bi >= bj, of rows i in [4 bi, 4 bi + 4) and j in
+// [4 bj, 4 bj + 4), numbered i-major with the diagonal included: block q is
+// the strict pair (bi + 1, bj) of the same closed form. One thread computes
+// the 16 dots of a block from 8 128-bit shared loads per 4-wide step (64
+// FMA), against 2 loads per 4 FMA one pair at a time. Rows past F are
+// clamped to F - 1 (computed, never stored).
+__host__ __device__ __forceinline__ int gram_blocks(int f) {
+  const int nb = (f + 3) / 4;
+  return nb * (nb + 1) / 2;
+}
+
+template <class RowFn>
+__device__ __forceinline__ void gram_block(const RowFn& row, int f, int d4, int q, int& bi,
+                                           int& bj, float acc[4][4]) {
+  int ii, jj;
+  pair_from_index(q, ii, jj);
+  bi = ii - 1;
+  bj = jj;
+  const float* ri[4];
+  const float* rj[4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    ri[a] = row(min(4 * bi + a, f - 1));
+    rj[a] = row(min(4 * bj + a, f - 1));
+  }
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[a][c] = 0.f;
+  for (int c4 = 0; c4 < d4; ++c4) {
+    float4 u[4], v[4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      u[a] = *reinterpret_cast<const float4*>(ri[a] + 4 * c4);
+      v[a] = *reinterpret_cast<const float4*>(rj[a] + 4 * c4);
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        acc[a][c] = fmaf(u[a].x, v[c].x, acc[a][c]);
+        acc[a][c] = fmaf(u[a].y, v[c].y, acc[a][c]);
+        acc[a][c] = fmaf(u[a].z, v[c].z, acc[a][c]);
+        acc[a][c] = fmaf(u[a].w, v[c].w, acc[a][c]);
+      }
+  }
+}
+
 // Kernel-parameter table for the multi-table gather: K (pointer, rows) pairs
 // passed by value so a launch needs no device-side staging buffer.
 struct GatherTables {

@@ -633,24 +633,50 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
     consumer_sync<CW>();
     const float* zg = zs + (p.prefetch_z ? g0 * k * p.ldz
                                          : (p.zbuf == 2 ? (gi & 1) * p.sg * k * p.ldz : 0));
-    for (int e = tid; e < ns * pairs; e += kConsumers) {
-      const int s = e / pairs;
-      const int q = e - s * pairs;
-      int i, j;
-      pair_from_index(q, i, j);
-      const float* vi = (i == 0) ? x + (g0 + s) * p.lda : zg + (s * k + i - 1) * p.ldz;
-      const float* vj = (j == 0) ? x + (g0 + s) * p.lda : zg + (s * k + j - 1) * p.ldz;
-      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-      for (int c4 = 0; c4 < d4; ++c4) {
-        const float4 u = *reinterpret_cast<const float4*>(vi + 4 * c4);
-        const float4 w = *reinterpret_cast<const float4*>(vj + 4 * c4);
-        a.x = fmaf(u.x, w.x, a.x);
-        a.y = fmaf(u.y, w.y, a.y);
-        a.z = fmaf(u.z, w.z, a.z);
-        a.w = fmaf(u.w, w.w, a.w);
+    // Pair dots; row 0 is x. In 4 x 4 register blocks (gram_block) when the
+    // group has a block task for every thread, else one pair per thread.
+    const int nblk = gram_blocks(f);
+    if (ns * nblk >= kConsumers) {
+      for (int e = tid; e < ns * nblk; e += kConsumers) {
+        const int s = e / nblk;
+        const int q = e - s * nblk;
+        const float* xrow = x + (g0 + s) * p.lda;
+        const float* zsam = zg + s * k * p.ldz;
+        float acc[4][4];
+        int bi, bj;
+        gram_block([&](int rr) { return rr == 0 ? xrow : zsam + (rr - 1) * p.ldz; }, f, d4, q,
+                   bi, bj, acc);
+        float* o = r + (g0 + s) * p.lda + d;
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          const int i = 4 * bi + a;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int j = 4 * bj + c;
+            if (i < f && j < i) o[i * (i - 1) / 2 + j] = acc[a][c];
+          }
+        }
       }
-      r[(g0 + s) * p.lda + d + q] = (a.x + a.y) + (a.z + a.w);
+    } else {
+      for (int e = tid; e < ns * pairs; e += kConsumers) {
+        const int s = e / pairs;
+        const int q = e - s * pairs;
+        int i, j;
+        pair_from_index(q, i, j);
+        const float* vi = (i == 0) ? x + (g0 + s) * p.lda : zg + (s * k + i - 1) * p.ldz;
+        const float* vj = (j == 0) ? x + (g0 + s) * p.lda : zg + (s * k + j - 1) * p.ldz;
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+        for (int c4 = 0; c4 < d4; ++c4) {
+          const float4 u = *reinterpret_cast<const float4*>(vi + 4 * c4);
+          const float4 w = *reinterpret_cast<const float4*>(vj + 4 * c4);
+          a.x = fmaf(u.x, w.x, a.x);
+          a.y = fmaf(u.y, w.y, a.y);
+          a.z = fmaf(u.z, w.z, a.z);
+          a.w = fmaf(u.w, w.w, a.w);
+        }
+        r[(g0 + s) * p.lda + d + q] = (a.x + a.y) + (a.z + a.w);
+      }
     }
     consumer_sync<CW>();
     if (p.zbuf == 2) {

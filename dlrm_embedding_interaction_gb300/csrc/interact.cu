@@ -11,9 +11,9 @@
 // when F is small so the block has S * P >= blockDim pair tasks), stages
 // their S*F*D features in shared memory with 128-bit coalesced loads (rows
 // padded to D + 4 floats so the 16-byte reads of different rows fall in
-// different banks), then thread w computes pair tasks w, w + T, ... with a
-// float4 dot product. Consecutive threads take consecutive p, so the writes
-// of R are coalesced and the i row is a shared-memory broadcast.
+// different banks), then thread w computes tasks w, w + T, ...: with D a
+// multiple of 4 a task is a 4 x 4 block of pairs held in registers
+// (gram_block), a quarter of the shared-memory reads of one pair per thread.
 #include <atomic>
 
 #include "common.cuh"
@@ -31,7 +31,7 @@ template <bool VEC>
 __global__ void __launch_bounds__(kInteractThreads)
 interaction_kernel(const float* __restrict__ dense, int ld_dense, const float* __restrict__ emb,
                    int batch, int k_tables, int d, float* __restrict__ out, int ld_out,
-                   int copy_dense, int samples_per_block) {
+                   int copy_dense, int samples_per_block, int use_blocks) {
   extern __shared__ float4 smem_f4[];
   float* zs = reinterpret_cast<float*>(smem_f4);
   const int f = k_tables + 1;
@@ -83,26 +83,60 @@ interaction_kernel(const float* __restrict__ dense, int ld_dense, const float* _
     }
     col0 = d;
   }
-  const int d4 = d / 4;
-  for (int w = tid; w < ns * p_count; w += blockDim.x) {
-    const int s = w / p_count;
-    const int p = w - s * p_count;
-    int i, j;
-    pair_from_index(p, i, j);
-    const float* zi = zs + (s * f + i) * ldz;
-    const float* zj = zs + (s * f + j) * ldz;
-    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c4 = 0; c4 < d4; ++c4) {
-      const float4 u = *reinterpret_cast<const float4*>(zi + 4 * c4);
-      const float4 v = *reinterpret_cast<const float4*>(zj + 4 * c4);
-      a.x = fmaf(u.x, v.x, a.x);
-      a.y = fmaf(u.y, v.y, a.y);
-      a.z = fmaf(u.z, v.z, a.z);
-      a.w = fmaf(u.w, v.w, a.w);
+  const int nblk = gram_blocks(f);
+  if (VEC && use_blocks) {
+    // 4 x 4 register blocks of pairs (gram_block)
+    const int d4 = d / 4;
+    for (int w = tid; w < ns * nblk; w += blockDim.x) {
+      const int s = w / nblk;
+      const int q = w - s * nblk;
+      const float* zsam = zs + s * f * ldz;
+      float acc[4][4];
+      int bi, bj;
+      gram_block([&](int r) { return zsam + r * ldz; }, f, d4, q, bi, bj, acc);
+      float* o = out + static_cast<int64_t>(b0 + s) * ld_out + col0;
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        const int i = 4 * bi + a;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int j = 4 * bj + c;
+          if (i < f && j < i) o[i * (i - 1) / 2 + j] = acc[a][c];
+        }
+      }
     }
-    float acc = (a.x + a.y) + (a.z + a.w);
-    for (int c = 4 * d4; c < d; ++c) acc = fmaf(zi[c], zj[c], acc);
-    out[static_cast<int64_t>(b0 + s) * ld_out + col0 + p] = acc;
+  } else if (VEC) {
+    const int d4 = d / 4;
+    for (int w = tid; w < ns * p_count; w += blockDim.x) {
+      const int s = w / p_count;
+      const int p = w - s * p_count;
+      int i, j;
+      pair_from_index(p, i, j);
+      const float* zi = zs + (s * f + i) * ldz;
+      const float* zj = zs + (s * f + j) * ldz;
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int c4 = 0; c4 < d4; ++c4) {
+        const float4 u = *reinterpret_cast<const float4*>(zi + 4 * c4);
+        const float4 v = *reinterpret_cast<const float4*>(zj + 4 * c4);
+        a.x = fmaf(u.x, v.x, a.x);
+        a.y = fmaf(u.y, v.y, a.y);
+        a.z = fmaf(u.z, v.z, a.z);
+        a.w = fmaf(u.w, v.w, a.w);
+      }
+      out[static_cast<int64_t>(b0 + s) * ld_out + col0 + p] = (a.x + a.y) + (a.z + a.w);
+    }
+  } else {
+    for (int w = tid; w < ns * p_count; w += blockDim.x) {
+      const int s = w / p_count;
+      const int p = w - s * p_count;
+      int i, j;
+      pair_from_index(p, i, j);
+      const float* zi = zs + (s * f + i) * ldz;
+      const float* zj = zs + (s * f + j) * ldz;
+      float acc = 0.f;
+      for (int c = 0; c < d; ++c) acc = fmaf(zi[c], zj[c], acc);
+      out[static_cast<int64_t>(b0 + s) * ld_out + col0 + p] = acc;
+    }
   }
 }
 
@@ -147,16 +181,21 @@ cudaError_t launch_interaction(const float* dense, int ld_dense, const float* em
   const int p_count = f * (f - 1) / 2;
   const size_t per = interaction_smem_per_sample(k, d);
   const size_t budget = 64 * 1024;
-  int s = p_count > 0 ? (kInteractThreads + p_count - 1) / p_count : kInteractThreads;
+  const bool vec = (d % 4 == 0) && (ld_dense % 4 == 0) &&
+                   (reinterpret_cast<uintptr_t>(dense) % 16 == 0) &&
+                   (reinterpret_cast<uintptr_t>(emb) % 16 == 0);
+  // per-sample tasks: 4 x 4 pair blocks from F = 9 on (at least 6 blocks a
+  // sample), single pairs below, where blocks would leave threads idle
+  const int blocks4 = gram_blocks(f);
+  const int use_blocks = (vec && f >= 9) ? 1 : 0;
+  const int tasks = use_blocks ? blocks4 : p_count;
+  int s = tasks > 0 ? (kInteractThreads + tasks - 1) / tasks : kInteractThreads;
   s = static_cast<int>(std::min<size_t>(static_cast<size_t>(s), std::max<size_t>(1, budget / per)));
   // keep at least two blocks per SM when the batch allows it
   const int sms = device_sm_count();
   const int cap = std::max(1, (b + 2 * sms - 1) / (2 * sms));
   s = std::max(1, std::min(s, cap));
   const size_t smem = per * s;
-  const bool vec = (d % 4 == 0) && (ld_dense % 4 == 0) &&
-                   (reinterpret_cast<uintptr_t>(dense) % 16 == 0) &&
-                   (reinterpret_cast<uintptr_t>(emb) % 16 == 0);
   const unsigned grid = static_cast<unsigned>((b + s - 1) / s);
   if (smem > 48 * 1024) {
     cudaError_t e = vec ? enable_large_smem(interaction_kernel<true>, 0)
@@ -165,10 +204,10 @@ cudaError_t launch_interaction(const float* dense, int ld_dense, const float* em
   }
   if (vec) {
     interaction_kernel<true><<<grid, kInteractThreads, smem, stream>>>(
-        dense, ld_dense, emb, b, k, d, out, ld_out, copy_dense, s);
+        dense, ld_dense, emb, b, k, d, out, ld_out, copy_dense, s, use_blocks);
   } else {
     interaction_kernel<false><<<grid, kInteractThreads, smem, stream>>>(
-        dense, ld_dense, emb, b, k, d, out, ld_out, copy_dense, s);
+        dense, ld_dense, emb, b, k, d, out, ld_out, copy_dense, s, 0);
   }
   return cudaGetLastError();
 }
