@@ -18,6 +18,7 @@
 
 #include "common.cuh"
 #include "fused.cuh"
+#include "fused_tc.cuh"
 
 namespace dlrm {
 
@@ -91,6 +92,8 @@ struct dlrm_handle_s {
   int path = DLRM_PATH_LAYERWISE;
   int fused_bm = 0;
   dlrm::FusedParams fused{};     // per-call fields filled by run_forward
+  bool fused_tc = false;         // the fused plan runs on the tensor cores (TF32 / BF16)
+  dlrm::FusedTcParams tcp{};
   unsigned long long* trace = nullptr;
   // per-stage profiling (dlrm_set_profiling)
   std::vector<std::string> stage_names;
@@ -138,7 +141,19 @@ dlrm_status_t run_forward(dlrm_handle_t h, const float* dense, const int64_t* in
     p.out = out;
     p.err = h->err;
     p.trace = h->trace;
-    e = dlrm::launch_fused(p, h->fused_bm, s);
+    if (h->fused_tc) {
+      dlrm::FusedTcParams q = h->tcp;
+      q.batch = batch;
+      q.dense = dense;
+      q.indices = indices;
+      q.offsets = offsets;
+      q.out = out;
+      q.err = h->err;
+      q.trace = h->trace;
+      e = dlrm::launch_fused_tc(q, s);
+    } else {
+      e = dlrm::launch_fused(p, h->fused_bm, s);
+    }
     if (e != cudaSuccess || !mark()) return DLRM_ERR_CUDA;
   } else {
   // [G] bag sums, all tables in one launch
@@ -274,8 +289,9 @@ dlrm_status_t dlrm_create(const dlrm_config_t* cfg, const float* const* tables,
   if (cfg->math != DLRM_MATH_FP32 && cfg->math != DLRM_MATH_TF32 &&
       cfg->math != DLRM_MATH_BF16 && cfg->math != DLRM_MATH_TF32X3)
     return DLRM_ERR_INVALID_ARG;
-  // the fused plan is fp32 only; the opt-in tensor-core modes are layer-wise
-  if (cfg->math != DLRM_MATH_FP32 && cfg->path == DLRM_PATH_FUSED) return DLRM_ERR_UNSUPPORTED;
+  // fused plans: fp32 (SIMT) and the TF32 / BF16 tensor-core modes; TF32X3 is
+  // layer-wise only
+  if (cfg->math == DLRM_MATH_TF32X3 && cfg->path == DLRM_PATH_FUSED) return DLRM_ERR_UNSUPPORTED;
   if (dlrm::interaction_smem_per_sample(cfg->n_tables, cfg->emb_dim) >
       dlrm::device_max_smem_optin())
     return DLRM_ERR_UNSUPPORTED;
@@ -299,19 +315,29 @@ dlrm_status_t dlrm_create(const dlrm_config_t* cfg, const float* const* tables,
   }
   // Kernel plan.
   dlrm::FusedPlan fplan;
+  dlrm::FusedTcPlan tplan;
   bool fused_fits = false;
-  if (cfg->path != DLRM_PATH_LAYERWISE && h->math == DLRM_MATH_FP32) {
+  const bool tc_math = h->math == DLRM_MATH_TF32 || h->math == DLRM_MATH_BF16;
+  if (cfg->path != DLRM_PATH_LAYERWISE && (h->math == DLRM_MATH_FP32 || tc_math)) {
     std::vector<std::vector<float>> hw, hb;
     if (!host_params(h, bot_w, bot_b, top_w, top_b, &hw, &hb)) {
       cudaGetLastError();
       delete h;
       return DLRM_ERR_CUDA;
     }
-    const int cw = 8;   // consumer warps of the fused kernel
-    fused_fits = dlrm::fused_plan(h->n_dense, h->k, h->d, h->bag, h->ln_bot, h->ln_top, hw, hb,
-                                  h->tabs, h->max_batch, dlrm::device_sm_count(),
-                                  dlrm::device_max_smem_optin(), cw, &fplan);
-    h->fused_bm = fplan.bm;
+    if (tc_math) {
+      fused_fits = dlrm::fused_tc_plan(h->n_dense, h->k, h->d, h->bag, h->ln_bot, h->ln_top, hw,
+                                       hb, h->tabs, static_cast<int>(h->math),
+                                       dlrm::device_max_smem_optin(), &tplan);
+      h->fused_tc = fused_fits;
+      h->fused_bm = dlrm::kTcTile;
+    } else {
+      const int cw = 8;   // computing warps of the fused kernel
+      fused_fits = dlrm::fused_plan(h->n_dense, h->k, h->d, h->bag, h->ln_bot, h->ln_top, hw,
+                                    hb, h->tabs, h->max_batch, dlrm::device_sm_count(),
+                                    dlrm::device_max_smem_optin(), cw, &fplan);
+      h->fused_bm = fplan.bm;
+    }
   }
   const int64_t tiles = fused_fits ? (h->max_batch + h->fused_bm - 1) / h->fused_bm : 0;
   if (cfg->path == DLRM_PATH_FUSED) {
@@ -371,7 +397,11 @@ dlrm_status_t dlrm_create(const dlrm_config_t* cfg, const float* const* tables,
   const size_t off_out = plan.take<float>(mb);
   // fused weight stream, its stage table, biases, last layer
   size_t off_fw = 0, off_ft = 0, off_fb = 0, off_fl = 0;
-  if (h->path == DLRM_PATH_FUSED) {
+  if (h->path == DLRM_PATH_FUSED && h->fused_tc) {
+    off_fw = plan.take<unsigned char>(tplan.wstream.size());
+    off_fb = plan.take<float>(tplan.bias.size());
+    off_fl = plan.take<float>(tplan.wlast.size());
+  } else if (h->path == DLRM_PATH_FUSED) {
     off_fw = plan.take<float>(fplan.wstream.size());
     off_ft = plan.take<uint2>(fplan.stage_tab.size());
     off_fb = plan.take<float>(fplan.bias.size());
@@ -407,7 +437,21 @@ dlrm_status_t dlrm_create(const dlrm_config_t* cfg, const float* const* tables,
       st = cuda_status(cudaMemcpy(at(off_tb[l]), top_b[l], h->ln_top[l + 1] * sizeof(float),
                                   cudaMemcpyDefault));
   }
-  if (h->path == DLRM_PATH_FUSED && st == DLRM_OK) {
+  if (h->path == DLRM_PATH_FUSED && h->fused_tc && st == DLRM_OK) {
+    st = cuda_status(cudaMemcpy(at(off_fw), tplan.wstream.data(), tplan.wstream.size(),
+                                cudaMemcpyHostToDevice));
+    if (st == DLRM_OK)
+      st = cuda_status(cudaMemcpy(at(off_fb), tplan.bias.data(), tplan.bias.size() * sizeof(float),
+                                  cudaMemcpyHostToDevice));
+    if (st == DLRM_OK)
+      st = cuda_status(cudaMemcpy(at(off_fl), tplan.wlast.data(),
+                                  tplan.wlast.size() * sizeof(float), cudaMemcpyHostToDevice));
+    h->tcp = tplan.params;
+    h->tcp.wstream = reinterpret_cast<const unsigned char*>(at(off_fw));
+    h->tcp.bias = at(off_fb);
+    h->tcp.wlast = at(off_fl);
+    if (st == DLRM_OK) st = cuda_status(dlrm::fused_tc_prepare(h->tcp.bf16));
+  } else if (h->path == DLRM_PATH_FUSED && st == DLRM_OK) {
     st = cuda_status(cudaMemcpy(at(off_fw), fplan.wstream.data(),
                                 fplan.wstream.size() * sizeof(float), cudaMemcpyHostToDevice));
     if (st == DLRM_OK)

@@ -13,8 +13,10 @@
 //    consumption order, each 32 KB stage one contiguous block whose 16-byte
 //    chunks are XOR-swizzled so the warps' reads are bank-conflict free. It
 //    flows through a ring of stages filled by 1-D bulk async copies
-//    (cp.async.bulk) completing on mbarriers, issued by one producer warp
-//    that runs ahead across layer boundaries while eight warps compute.
+//    (cp.async.bulk) completing on mbarriers, issued by up to four lanes of
+//    one producer warp (one thread's copies are serialised), each refilling
+//    its own ring slots, running ahead across layer boundaries while eight
+//    warps compute.
 //  * a computing warp owns TM = 8 rows (4 for 4-row tiles), broadcast-read
 //    from the activation buffer, and 32 * TN columns (one column per lane,
 //    TN per thread) of one 16-wide k-slice of each stage; the register tile
@@ -199,9 +201,22 @@ __device__ void prefetch_stream_l2(const float* wstream, size_t floats) {
   }
 }
 
+// Issuing lanes of the producer warp: one thread's bulk copies run one after
+// another at about 45 GB/s, four threads reach ~150 GB/s per SM. Lane l
+// issues stream stages j = l, l + n, ... where n divides the ring depth, so
+// every slot is refilled by one lane only, in order: a lane never waits on
+// a slot's empty barrier more than one phase ahead (a parity wait cannot
+// tell phases two apart).
+__device__ __forceinline__ uint32_t issuer_count(uint32_t s_count) {
+  return s_count % 4 == 0 ? 4 : (s_count % 3 == 0 ? 3 : (s_count % 2 == 0 ? 2 : 1));
+}
+
 __device__ void produce(const Ring& r, const float* wstream, const uint2* tab, uint32_t n_stages) {
-  uint32_t j = 0;
-  for (; j < n_stages; ++j) {
+  const uint32_t lane = threadIdx.x % kWarp;
+  const uint32_t n_issuers = issuer_count(r.s_count);
+  if (lane >= n_issuers) return;
+  uint32_t j = lane;
+  for (; j < n_stages; j += n_issuers) {
     const uint32_t slot = j % r.s_count;
     if (j >= r.s_count &&
         !wait_phase(smem_u32(&r.empty[slot]), ((j / r.s_count) - 1) & 1, r.abort_flag, r.err))
@@ -211,10 +226,13 @@ __device__ void produce(const Ring& r, const float* wstream, const uint2* tab, u
     bulk_g2s(smem_u32(r.stages + slot * kFusedStageFloats), wstream + e.x, e.y,
              smem_u32(&r.full[slot]));
   }
-  // The copies still in flight must land before this CTA's shared memory is
-  // released: wait (bounded, regardless of abort) for the last stages issued.
-  const uint32_t first = j > r.s_count ? j - r.s_count : 0;
-  for (uint32_t q = first; q < j; ++q) {
+  // This lane's copies still in flight must land before the CTA's shared
+  // memory is released: wait (bounded, regardless of abort) for its stages
+  // issued within the last ring.
+  const uint32_t issued_end = j < n_stages ? j : n_stages;
+  const uint32_t first = issued_end > r.s_count ? issued_end - r.s_count : 0;
+  for (uint32_t q = first; q < issued_end; ++q) {
+    if (q % n_issuers != lane) continue;
     const uint32_t bar = smem_u32(&r.full[q % r.s_count]);
     const uint64_t t0 = global_ns();
     while (!mbar_try_wait(bar, (q / r.s_count) & 1)) {
@@ -750,10 +768,8 @@ fused_forward_kernel(const __grid_constant__ FusedParams p) {
   }
   __syncthreads();
   if (warp == CW) {
-    if (threadIdx.x % kWarp == 0) {
-      prefetch_stream_l2(p.wstream, p.stream_floats);
-      produce(r, p.wstream, p.stage_tab, static_cast<uint32_t>(p.n_stages));
-    }
+    if (threadIdx.x % kWarp == 0) prefetch_stream_l2(p.wstream, p.stream_floats);
+    produce(r, p.wstream, p.stage_tab, static_cast<uint32_t>(p.n_stages));
     return;
   }
   consume<BM, CW>(p, r, act0, act1, zs, rowidx_s, bias_s, wlast_s);

@@ -98,17 +98,34 @@ def test_linear_tensor_core_strided_rows_and_no_bias():
     tc_close(y.cpu().numpy(), oracle.linear(xf[:, :70], w, None, oracle.ACT_NONE))
 
 
+def _model(cfg, inp, mode, path):
+    return dl.DlrmModel(cfg.ln_bot, cfg.ln_top, [cu(t) for t in inp["tables"]],
+                        [cu(w) for w in inp["bot_w"]], [cu(v) for v in inp["bot_b"]],
+                        [cu(w) for w in inp["top_w"]], [cu(v) for v in inp["top_b"]],
+                        cfg.bag_size, cfg.batch, mode, path)
+
+
 @pytest.mark.parametrize("mode", ALL_MODES, ids=ALL_IDS)
-@pytest.mark.parametrize("name", ["tiny_b64_k3", "b2048_k3", "b2048_k32", "sweep_b33_k8"])
-def test_forward_tensor_core_matches_oracle(name, mode):
+@pytest.mark.parametrize("path", [dl.PATH_LAYERWISE, dl.PATH_FUSED], ids=["layerwise", "fused"])
+@pytest.mark.parametrize("name", ["tiny_b64_k3", "b2048_k3", "b2048_k32", "sweep_b33_k8",
+                                  "sweep_b1_k1", "sweep_b300_k16"])
+def test_forward_tensor_core_matches_oracle(name, path, mode):
+    """Both plans of the tensor-core modes against the oracle. The fused plan
+    takes bag size 1 and models whose tile fits shared memory; TF32X3 is
+    layer-wise only. Other requests must be refused with UNSUPPORTED."""
     cfg = synth.get_config(name)
     inp = synth.make_inputs(cfg, seed=1234)
-    tables = [cu(t) for t in inp["tables"]]
-    model = dl.DlrmModel(cfg.ln_bot, cfg.ln_top, tables,
-                         [cu(w) for w in inp["bot_w"]], [cu(v) for v in inp["bot_b"]],
-                         [cu(w) for w in inp["top_w"]], [cu(v) for v in inp["top_b"]],
-                         cfg.bag_size, cfg.batch, mode)
-    assert model.path == dl.PATH_LAYERWISE
+    if path == dl.PATH_FUSED and (mode == dl.MATH_TF32X3 or cfg.bag_size != 1):
+        with pytest.raises(dl.DlrmError) as ei:
+            _model(cfg, inp, mode, path)
+        assert ei.value.status == dl.ERR_UNSUPPORTED
+        return
+    try:
+        model = _model(cfg, inp, mode, path)
+    except dl.DlrmError as e:
+        assert path == dl.PATH_FUSED and e.status == dl.ERR_UNSUPPORTED
+        pytest.skip("model does not fit the fused tensor-core tile")
+    assert model.path == path
     out = model.forward(cu(inp["dense"]), cu(inp["indices"]), cu(inp["offsets"]))
     assert model.error() == dl.OK
     ref = oracle.forward(inp)
@@ -119,12 +136,27 @@ def test_forward_tensor_core_matches_oracle(name, mode):
     model.close()
 
 
-def test_fused_plan_rejects_tensor_core_modes():
-    cfg = synth.get_config("tiny_b64_k3")
+@pytest.mark.parametrize("mode", MODES, ids=MODE_IDS)
+def test_fused_tensor_core_is_auto_choice_and_flags_bad_indices(mode):
+    cfg = synth.get_config("b2048_k3")
+    inp = synth.make_inputs(cfg, seed=7)
+    model = _model(cfg, inp, mode, dl.PATH_AUTO)
+    assert model.path == dl.PATH_FUSED
+    idx = inp["indices"].copy()
+    idx[1, 100] = cfg.rows[1]            # one index past its table
+    out = model.forward(cu(inp["dense"]), cu(idx), cu(inp["offsets"]))
+    assert model.error() == dl.ERR_INDEX_OOB
+    # the bag with the bad index contributes zeros (the oracle's definition)
+    inp2 = dict(inp)
+    inp2["indices"] = idx
+    ref = oracle.forward(inp2, allow_oob=True)
+    np.testing.assert_allclose(out.cpu().numpy(), ref, rtol=2e-2, atol=0)
+    model.close()
+
+
+def test_fused_plan_rejects_tf32x3():
+    cfg = synth.get_config("b2048_k3")
     inp = synth.make_inputs(cfg, seed=1)
     with pytest.raises(dl.DlrmError) as ei:
-        dl.DlrmModel(cfg.ln_bot, cfg.ln_top, [cu(t) for t in inp["tables"]],
-                     [cu(w) for w in inp["bot_w"]], [cu(v) for v in inp["bot_b"]],
-                     [cu(w) for w in inp["top_w"]], [cu(v) for v in inp["top_b"]],
-                     cfg.bag_size, cfg.batch, dl.MATH_BF16, dl.PATH_FUSED)
+        _model(cfg, inp, dl.MATH_TF32X3, dl.PATH_FUSED)
     assert ei.value.status == dl.ERR_UNSUPPORTED
