@@ -51,7 +51,7 @@ SM_MAX_MHZ_DEFAULT = 2070.0
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
 # capture of the kernel as built now on the named workload; a kernel change
 # invalidates the entry.
-NCU_TRAFFIC = {("fused", "b2048_k3"): 3193344}
+NCU_TRAFFIC = {("fused", "b2048_k3"): 3191552}
 
 
 def parse_args():
@@ -61,6 +61,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="b2048_k3")
+    ap.add_argument("--math", choices=["fp32", "tf32", "bf16", "tf32x3"], default="fp32",
+                    help="arithmetic of the timed model's MLPs (fp32 is the parity mode)")
     ap.add_argument("--seed", type=int, default=1234)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -322,10 +324,12 @@ def run_ours(args, rank, world, local_rank):
     cfg = synth.get_config(args.config)
     inp = synth.make_inputs(cfg, seed=args.seed)
     cu = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    math = {"fp32": dl.MATH_FP32, "tf32": dl.MATH_TF32, "bf16": dl.MATH_BF16,
+            "tf32x3": dl.MATH_TF32X3}[args.math]
     model = dl.DlrmModel(cfg.ln_bot, cfg.ln_top, [cu(t) for t in inp["tables"]],
                          [cu(w) for w in inp["bot_w"]], [cu(b) for b in inp["bot_b"]],
                          [cu(w) for w in inp["top_w"]], [cu(b) for b in inp["top_b"]],
-                         cfg.bag_size, cfg.batch)
+                         cfg.bag_size, cfg.batch, math)
     dense, idx, off = cu(inp["dense"]), cu(inp["indices"]), cu(inp["offsets"])
     out = torch.empty(cfg.batch, device=dev)
     flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -375,7 +379,8 @@ def run_ours(args, rank, world, local_rank):
         if rank == 0:
             print(json.dumps(dict(metric=METRIC, value=cfg.batch * args.steps / (sum(ms) * 1e-3),
                                   unit=UNIT, us_per_batch=sum(ms) * 1e3 / args.steps,
-                                  config=dict(workload=cfg.name), mode="only-forward")))
+                                  config=dict(workload=cfg.name, math=args.math),
+                                  mode="only-forward")))
         return 0
     total_ms = sum(ms)
     if dist is not None:
@@ -462,13 +467,22 @@ def run_ours(args, rank, world, local_rank):
         roof = dict(bound="hbm", achieved=ach, peak=pk["hbm_gbs"], unit="GB/s",
                     frac=ach / pk["hbm_gbs"], traffic=None, kernel=dom,
                     peak_source=f"{pk['source']} (MEASURED_PEAKS hbm_gbs)")
+    elif args.math != "fp32" and dom in ("fused",) + tuple(
+            f"{w}{i}" for w in ("bottom", "top") for i in range(16)):
+        # tensor-pipe work: measured bf16 peak, tf32 at the nominal half rate
+        tpeak = pk["bf16_tflops"] * (1.0 if args.math == "bf16" else 0.5)
+        ach = flops / t_dom / 1e12
+        roof = dict(bound="tensor", achieved=ach, peak=tpeak, unit="TFLOP/s",
+                    frac=ach / tpeak, traffic=None, kernel=dom,
+                    peak_source=f"{pk['source']} bf16_tflops" +
+                    ("" if args.math == "bf16" else " x 0.5 (tf32 nominal ratio)"))
     else:
         ach = flops / t_dom / 1e12
         roof = dict(bound="alu", achieved=ach, peak=fp32_peak, unit="TFLOP/s",
                     frac=ach / fp32_peak, traffic=None, kernel=dom,
                     peak_source=f"FP32 FFMA: {sms} SMs x 128 lanes x 2 x {pk['sm_max_mhz']:.0f} MHz")
-    roof["algorithmic_per_launch"] = flops if roof["bound"] == "alu" else byts
-    roof["traffic"] = NCU_TRAFFIC.get((dom, cfg.name))
+    roof["algorithmic_per_launch"] = byts if roof["bound"] == "hbm" else flops
+    roof["traffic"] = NCU_TRAFFIC.get((dom, cfg.name)) if args.math == "fp32" else None
     roof["algorithmic_bytes_per_launch"] = byts
 
     # whole-forward roofline fraction (slower of HBM bytes and FP32 flops)
@@ -492,9 +506,11 @@ def run_ours(args, rank, world, local_rank):
         if m2.error(stream) != dl.OK:
             raise RuntimeError(f"device error in the {mode_name} forward")
         tot = sum(ms_tc)
+        tc_plan = ("fused single launch, tcgen05 MMAs" if m2.path == dl.PATH_FUSED
+                   else "layer-wise launches, tcgen05 GEMMs")
         tc_modes[mode_name] = dict(us_per_batch=tot * 1e3 / len(ms_tc),
                                    samples_per_s=cfg.batch * len(ms_tc) / (tot * 1e-3),
-                                   plan="layer-wise launches, tcgen05 GEMMs",
+                                   plan=tc_plan,
                                    tolerance=("fp32 parity (abs 1e-5, rel 1e-4)"
                                               if mode == dl.MATH_TF32X3
                                               else "rel 2e-2 vs the fp64 oracle"))
@@ -570,12 +586,13 @@ def run_ours(args, rank, world, local_rank):
         warmup=args.warmup, ms_per_step=ms_per_step, us_per_batch=ms_per_step * 1e3,
         us_per_batch_median=statistics.median(ms) * 1e3,
         us_per_batch_p10_p90=[float(np.percentile(ms, 10) * 1e3), float(np.percentile(ms, 90) * 1e3)],
-        higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f32",
+        higher_is_better=True, scaling="weak", vs_baseline=None,
+        dtype={"fp32": "f32", "tf32": "tf32", "bf16": "bf16", "tf32x3": "3xtf32"}[args.math],
         data="synthetic: seeded SplitMix64 inputs of the workload's shapes and distributions",
         config=dict(workload=cfg.name, global_batch=cfg.batch * world, batch_per_gpu=cfg.batch,
                     tables=cfg.n_tables, rows=cfg.rows[0], emb_dim=cfg.emb_dim,
                     bag_size=cfg.bag_size, ln_bot=list(cfg.ln_bot), ln_top=list(cfg.ln_top),
-                    math="fp32", l2="flushed before every step (256 MB write)",
+                    math=args.math, l2="flushed before every step (256 MB write)",
                     plan={dl.PATH_FUSED: "fused single launch",
                           dl.PATH_LAYERWISE: "layer-wise launches"}[path_used],
                     parallelism="replicas" if world > 1 else "single GPU"),

@@ -768,7 +768,9 @@ fused_forward_kernel(const __grid_constant__ FusedParams p) {
   }
   __syncthreads();
   if (warp == CW) {
-    if (threadIdx.x % kWarp == 0) prefetch_stream_l2(p.wstream, p.stream_floats);
+    // the L2 prefetch from a lane that issues no copies: a thread's bulk
+    // operations run one after another
+    if (threadIdx.x % kWarp == kWarp - 1) prefetch_stream_l2(p.wstream, p.stream_floats);
     produce(r, p.wstream, p.stage_tab, static_cast<uint32_t>(p.n_stages));
     return;
   }

@@ -165,9 +165,9 @@ constexpr int kIssuers = 4;
 __device__ void produce(const FusedTcParams& p, unsigned char* ring, uint64_t* full,
                         uint64_t* empty, volatile int* abort_flag) {
   const int lane = threadIdx.x % kWarp;
-  if (lane >= kIssuers) return;
-  // this CTA's share of the stream into L2 first
-  if (lane == 0) {
+  // this CTA's share of the stream into L2, from a lane that issues no copies
+  // (a thread's bulk operations run one after another)
+  if (lane == kWarp - 1) {
     const size_t bytes = static_cast<size_t>(p.n_tiles) * kTcTileBytes;
     const size_t per = ((bytes / 16 + gridDim.x - 1) / gridDim.x) * 16;
     const size_t b0 = per * blockIdx.x;
@@ -183,6 +183,7 @@ __device__ void produce(const FusedTcParams& p, unsigned char* ring, uint64_t* f
       }
     }
   }
+  if (lane >= kIssuers) return;
   const uint32_t s_count = static_cast<uint32_t>(p.stages);
   const uint32_t n = static_cast<uint32_t>(p.n_tiles);
   uint32_t j = lane;
