@@ -410,7 +410,20 @@ def run_ours(args, rank, world, local_rank):
     e2e = dict(value=world * cfg.batch * e2e_steps / (e2e_total * 1e-3), unit=UNIT,
                us_per_batch=e2e_total * 1e3 / e2e_steps, steps=e2e_steps,
                h2d_bytes_per_step=int(h2d), d2h_bytes_per_step=int(cfg.batch * 4),
-               api="dlrm_forward_host (pinned host buffers)")
+               api="dlrm_forward_host, pinned host buffers: the kernels read the inputs and "
+                   "write the output in host memory over NVLink-C2C (no staging copies)")
+    # the same call with pageable buffers: staged host<->device copies each step
+    p_dense, p_idx = torch.from_numpy(inp["dense"]).clone(), torch.from_numpy(inp["indices"]).clone()
+    p_off, p_out = torch.from_numpy(inp["offsets"]).clone(), torch.empty(cfg.batch)
+    ms_st, win = timed(lambda: model.forward_host(p_dense, p_idx, p_off, p_out, stream=stream),
+                       e2e_steps, max(3, args.warmup // 5))
+    clocks.mark(*win)
+    if model.error(stream) != dl.OK:
+        raise RuntimeError("device error during the staged e2e forward")
+    e2e["staged_copies"] = dict(us_per_batch=sum(ms_st) * 1e3 / len(ms_st),
+                                value=world * cfg.batch * len(ms_st) / (sum(ms_st) * 1e-3),
+                                api="dlrm_forward_host, pageable host buffers (cudaMemcpyAsync "
+                                    "to and from the handle's staging buffers)")
 
     # CUDA-graph replay of the same forward
     with torch.cuda.stream(stream):

@@ -497,6 +497,21 @@ dlrm_status_t dlrm_forward(dlrm_handle_t h, const float* dense, const int64_t* i
   return run_forward(h, dense, indices, offsets, out, batch, static_cast<cudaStream_t>(stream));
 }
 
+namespace {
+
+// Device address of a host buffer the GPU can reach directly (pinned and
+// mapped: on GB300 host memory is coherent over NVLink-C2C), else null.
+const void* device_view(const void* host) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, host) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return (a.type == cudaMemoryTypeHost && a.devicePointer) ? a.devicePointer : nullptr;
+}
+
+}  // namespace
+
 dlrm_status_t dlrm_forward_host(dlrm_handle_t h, const float* dense_host,
                                 const int64_t* indices_host, const int64_t* offsets_host,
                                 float* out_host, int32_t batch, void* stream) {
@@ -505,16 +520,32 @@ dlrm_status_t dlrm_forward_host(dlrm_handle_t h, const float* dense_host,
   if (batch < 1 || batch > h->max_batch) return DLRM_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t nb = static_cast<size_t>(batch);
-  if (cudaMemcpyAsync(h->dense_stage, dense_host, nb * h->n_dense * sizeof(float),
-                      cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      cudaMemcpyAsync(h->idx_stage, indices_host, nb * h->k * h->bag * sizeof(int64_t),
-                      cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      cudaMemcpyAsync(h->off_stage, offsets_host, nb * h->k * sizeof(int64_t),
-                      cudaMemcpyHostToDevice, s) != cudaSuccess)
-    return DLRM_ERR_CUDA;
-  dlrm_status_t st = run_forward(h, h->dense_stage, h->idx_stage, h->off_stage, h->out_stage,
-                                 batch, s);
-  if (st != DLRM_OK) return st;
+  // Pinned buffers are read and written in place by the kernels; any other
+  // buffer goes through the handle's staging area with one copy each way.
+  const float* dense = static_cast<const float*>(device_view(dense_host));
+  const int64_t* idx = static_cast<const int64_t*>(device_view(indices_host));
+  const int64_t* off = static_cast<const int64_t*>(device_view(offsets_host));
+  float* out = static_cast<float*>(const_cast<void*>(device_view(out_host)));
+  if (!dense) {
+    if (cudaMemcpyAsync(h->dense_stage, dense_host, nb * h->n_dense * sizeof(float),
+                        cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return DLRM_ERR_CUDA;
+    dense = h->dense_stage;
+  }
+  if (!idx) {
+    if (cudaMemcpyAsync(h->idx_stage, indices_host, nb * h->k * h->bag * sizeof(int64_t),
+                        cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return DLRM_ERR_CUDA;
+    idx = h->idx_stage;
+  }
+  if (!off) {
+    if (cudaMemcpyAsync(h->off_stage, offsets_host, nb * h->k * sizeof(int64_t),
+                        cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return DLRM_ERR_CUDA;
+    off = h->off_stage;
+  }
+  dlrm_status_t st = run_forward(h, dense, idx, off, out ? out : h->out_stage, batch, s);
+  if (st != DLRM_OK || out) return st;
   return cuda_status(cudaMemcpyAsync(out_host, h->out_stage, nb * sizeof(float),
                                      cudaMemcpyDeviceToHost, s));
 }

@@ -145,12 +145,13 @@ dlrm_status_t dlrm_create(const dlrm_config_t* cfg, const float* const* tables,
 dlrm_status_t dlrm_forward(dlrm_handle_t h, const float* dense, const int64_t* indices,
                            const int64_t* offsets, float* out, int32_t batch, void* stream);
 
-/* dlrm_forward from HOST buffers: enqueues the host-to-device copies of dense,
- * indices and offsets into the handle's staging buffers, the forward, and the
- * device-to-host copy of `out`, all on `stream`. Host buffers should be
- * pinned for the copies to be asynchronous; they must stay valid and
- * unchanged until the stream has passed this call (e.g. after
- * cudaStreamSynchronize or dlrm_get_error). */
+/* dlrm_forward from HOST buffers, all on `stream`. A pinned (page-locked,
+ * mapped) buffer is read or written in place by the kernels through its
+ * device address (on GB300 host memory is coherent over NVLink-C2C): no copy.
+ * Any other buffer is copied host-to-device into the handle's staging buffers
+ * before the forward (dense, indices, offsets) or device-to-host after it
+ * (out). Buffers must stay valid and unchanged until the stream has passed
+ * this call (e.g. after cudaStreamSynchronize or dlrm_get_error). */
 dlrm_status_t dlrm_forward_host(dlrm_handle_t h, const float* dense_host,
                                 const int64_t* indices_host, const int64_t* offsets_host,
                                 float* out_host, int32_t batch, void* stream);

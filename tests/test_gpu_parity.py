@@ -296,16 +296,21 @@ def test_forward_smaller_batches_than_max(path):
     model.close()
 
 
+@pytest.mark.parametrize("pinned", ["all", "none", "mixed"])
 @pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
-def test_forward_host_equals_device_forward(path):
+def test_forward_host_equals_device_forward(path, pinned):
+    """Pinned buffers are used in place by the kernels, pageable ones through
+    staging copies; every combination gives the device forward's result."""
     cfg = synth.get_config("b2048_k3")
     inp = synth.make_inputs(cfg, seed=5)
     model = make_model(cfg, inp, path=path)
     dev = run_forward(model, inp)
-    dense = torch.from_numpy(inp["dense"]).pin_memory()
-    idx = torch.from_numpy(inp["indices"]).pin_memory()
-    off = torch.from_numpy(inp["offsets"]).pin_memory()
-    out = torch.full((cfg.batch,), -1.0).pin_memory()
+    pin = {"all": (1, 1, 1, 1), "none": (0, 0, 0, 0), "mixed": (1, 0, 1, 0)}[pinned]
+    host = lambda t, p: t.pin_memory() if p else t.clone()
+    dense = host(torch.from_numpy(inp["dense"]), pin[0])
+    idx = host(torch.from_numpy(inp["indices"]), pin[1])
+    off = host(torch.from_numpy(inp["offsets"]), pin[2])
+    out = host(torch.full((cfg.batch,), -1.0), pin[3])
     model.forward_host(dense, idx, off, out)
     assert model.error() == dl.OK       # synchronises the stream
     np.testing.assert_array_equal(out.numpy(), dev)
