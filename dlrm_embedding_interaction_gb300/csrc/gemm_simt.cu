@@ -16,6 +16,7 @@
 //  * bias and ReLU/sigmoid are applied in registers before the single store.
 // N < 16 (the final 256 -> 1 sigmoid layer) runs a warp-per-row GEMV instead.
 #include <algorithm>
+#include <atomic>
 
 #include "common.cuh"
 
@@ -177,6 +178,124 @@ sgemm_bias_act_kernel(const float* __restrict__ x, int ldx, const float* __restr
   }
 }
 
+// Large-M tile (M >= 64 rows per block for at least two blocks per SM): the
+// broadcast-row register tile of the fused forward. Block 64 rows x 128
+// columns, 8 warps; warp w owns rows 8w .. 8w+7 (every lane reads the same
+// row values: broadcast shared loads) and lane l owns columns l + 32 j, j < 4,
+// accumulating the even-k and odd-k partial sums of each output in one float2
+// with fma.rn.f32x2. Per packed FMA the tile needs 2/8 + 1/4 shared
+// wavefronts, in balance with the FMA pipe. Tiles of 32 k stream through a
+// 3-stage cp.async ring (zero-filled past M, N and K); W rows are stored with
+// their 16-byte chunks XOR-swizzled by row so 8 consecutive lanes' rows fall
+// on 8 distinct bank groups.
+constexpr int kLmBM = 64, kLmBN = 128, kLmBK = 32, kLmStages = 3, kLmThreads = 256;
+constexpr int kLmStageFloats = (kLmBM + kLmBN) * kLmBK;
+
+__device__ __forceinline__ void lm_cp_async16(float* dst, const float* src, int bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(static_cast<uint32_t>(
+                   __cvta_generic_to_shared(dst))),
+               "l"(src), "r"(bytes)
+               : "memory");
+}
+
+template <int ACT>
+__global__ void __launch_bounds__(kLmThreads, 2)
+sgemm_large_m_kernel(const float* __restrict__ x, int ldx, const float* __restrict__ w, int ldw,
+                     const float* __restrict__ bias, float* __restrict__ y, int ldy, int m, int n,
+                     int k) {
+  extern __shared__ __align__(16) float lm_smem[];
+  const int tid = threadIdx.x;
+  const int warp = tid / kWarp;
+  const int lane = tid % kWarp;
+  const int m0 = blockIdx.x * kLmBM;
+  const int n0 = blockIdx.y * kLmBN;
+  const int k_tiles = (k + kLmBK - 1) / kLmBK;
+
+  // stage loader: A 64 rows x 8 chunks, W 128 rows x 8 chunks of 16 bytes
+  auto load_stage = [&](int kt, int s) {
+    float* as = lm_smem + s * kLmStageFloats;
+    float* ws = as + kLmBM * kLmBK;
+    const int k0 = kt * kLmBK;
+    for (int c = tid; c < (kLmBM + kLmBN) * 8; c += kLmThreads) {
+      const bool is_a = c < kLmBM * 8;
+      const int cc = is_a ? c : c - kLmBM * 8;
+      const int r = cc >> 3;
+      const int ch = cc & 7;
+      const int kk = k0 + ch * 4;
+      const int gr = (is_a ? m0 : n0) + r;
+      const int rows = is_a ? m : n;
+      const float* src = is_a ? x : w;
+      int bytes = 0;
+      if (gr < rows && kk < k) {
+        src += static_cast<int64_t>(gr) * (is_a ? ldx : ldw) + kk;
+        bytes = k - kk >= 4 ? 16 : 4 * (k - kk);
+      }
+      float* dst = is_a ? as + r * kLmBK + ch * 4 : ws + r * kLmBK + ((ch ^ (r & 7)) * 4);
+      lm_cp_async16(dst, src, bytes);
+    }
+  };
+
+  float2 acc[8][4];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = make_float2(0.f, 0.f);
+
+#pragma unroll
+  for (int s = 0; s < kLmStages - 1; ++s) {
+    if (s < k_tiles) load_stage(s, s);
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+  }
+  const int sw = lane & 7;
+  for (int kt = 0; kt < k_tiles; ++kt) {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(kLmStages - 2) : "memory");
+    __syncthreads();
+    // refill the stage read two tiles ago (every warp is past it)
+    if (kt + kLmStages - 1 < k_tiles) load_stage(kt + kLmStages - 1, (kt + kLmStages - 1) % kLmStages);
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+    const float* as = lm_smem + (kt % kLmStages) * kLmStageFloats + warp * 8 * kLmBK;
+    const float* ws = lm_smem + (kt % kLmStages) * kLmStageFloats + kLmBM * kLmBK + lane * kLmBK;
+#pragma unroll
+    for (int step = 0; step < kLmBK / 4; ++step) {
+      float4 wv[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        wv[j] = *reinterpret_cast<const float4*>(ws + 32 * j * kLmBK + ((step ^ sw) * 4));
+      float4 av[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) av[i] = *reinterpret_cast<const float4*>(as + i * kLmBK + step * 4);
+      // component-outer: 32 independent accumulators between the even-k and
+      // odd-k updates of each
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          acc[i][j] = __ffma2_rn(make_float2(av[i].x, av[i].y), make_float2(wv[j].x, wv[j].y),
+                                 acc[i][j]);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          acc[i][j] = __ffma2_rn(make_float2(av[i].z, av[i].w), make_float2(wv[j].z, wv[j].w),
+                                 acc[i][j]);
+    }
+  }
+  asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int gn = n0 + lane + 32 * j;
+    if (gn >= n) continue;
+    const float bv = bias ? __ldg(bias + gn) : 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int gm = m0 + warp * 8 + i;
+      if (gm < m)
+        y[static_cast<int64_t>(gm) * ldy + gn] = apply_act((acc[i][j].x + acc[i][j].y) + bv, ACT);
+    }
+  }
+}
+
 // Warp per row for N < 16: lanes stride K, butterfly reduction, lane 0 writes.
 template <int ACT>
 __global__ void __launch_bounds__(256)
@@ -251,6 +370,24 @@ cudaError_t launch_act(const float* x, int ldx, const float* w, int ldw, const f
   auto blocks = [&](int bm, int bn) {
     return static_cast<int64_t>((m + bm - 1) / bm) * ((n + bn - 1) / bn);
   };
+  if (va && vw && blocks(kLmBM, kLmBN) >= 2 * sms) {
+    static std::atomic<uint64_t> done{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+    constexpr int kSmem = kLmStages * kLmStageFloats * static_cast<int>(sizeof(float));
+    if (!bit || !(done.load(std::memory_order_acquire) & bit)) {
+      e = cudaFuncSetAttribute(sgemm_large_m_kernel<ACT>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+      if (e != cudaSuccess) return e;
+      if (bit) done.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    const dim3 grid((m + kLmBM - 1) / kLmBM, (n + kLmBN - 1) / kLmBN);
+    sgemm_large_m_kernel<ACT><<<grid, kLmThreads, kSmem, stream>>>(x, ldx, w, ldw, bias, y, ldy, m,
+                                                                  n, k);
+    return cudaGetLastError();
+  }
   if (blocks(128, 128) >= sms)
     return launch_tile<128, 128, 8, 8, ACT>(x, ldx, w, ldw, bias, y, ldy, m, n, k, va, vw, vy, stream);
   if (blocks(64, 64) >= sms)

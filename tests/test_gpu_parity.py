@@ -170,6 +170,8 @@ LINEAR_CASES = [
     (1, 1, 1, 0), (7, 13, 5, 0), (2048, 512, 13, 0), (2048, 256, 512, 0), (2048, 64, 256, 0),
     (2048, 512, 70, 2), (2048, 512, 592, 0), (33, 1, 256, 0), (100, 17, 70, 3),
     (257, 1024, 479, 1), (4096, 128, 64, 0), (65, 16, 16, 0), (3, 3, 1000, 0),
+    # large M (the 64 x 128 broadcast-row tile): ragged M, N and K tiles
+    (8192, 512, 512, 0), (9000, 300, 100, 4), (20000, 130, 64, 0),
 ]
 
 
