@@ -56,6 +56,15 @@ __device__ __forceinline__ uint64_t global_ns() {
 
 // Phase trace (profiling): the consumer leader stamps when the tile finishes
 // phase `slot`.
+// Profiling: where GEMM layer g's leader stamps the end of its k-loop
+// (trace slot 20 + g), or null.
+__device__ __forceinline__ unsigned long long* kloop_stamp(const FusedParams& p, int g) {
+  // slots 20.. are free only while the phase stamps (up to n_gemm + 3) end below
+  return (p.trace && p.n_gemm + 3 < 20 && 20 + g < kFusedTraceSlots)
+             ? p.trace + static_cast<size_t>(blockIdx.x) * kFusedTraceSlots + 20 + g
+             : nullptr;
+}
+
 __device__ __forceinline__ void stamp(const FusedParams& p, int slot) {
   if (p.trace && threadIdx.x == 0)
     p.trace[static_cast<size_t>(blockIdx.x) * kFusedTraceSlots + slot] = global_ns();
@@ -128,23 +137,40 @@ __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(CW * kWarp) : "memory");
 }
 
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity. Returns false when this or
 // another thread gave up (abort raised); the caller then carries on without
-// the data so every named barrier is still reached. While waiting, the thread
-// is suspended in the mbarrier (hint kSuspendNs) instead of spinning, so a
-// waiting warp takes no issue slots from the warps computing beside it.
+// the data so every named barrier is still reached. SPIN: poll without
+// suspending (computing warps, whose next stage is usually moments away);
+// otherwise the thread sleeps in the barrier between polls (the producer,
+// which shares a sub-partition with computing warps).
 constexpr uint32_t kSuspendNs = 20000;
+template <bool SPIN>
 __device__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_test_wait(bar, parity)) return true;
   if (*abort_flag) return false;
   const uint64_t t0 = global_ns();
-  for (;;) {
-    if (mbar_try_wait_suspend(bar, parity, kSuspendNs)) return true;
-    if (*abort_flag) return false;
-    if (global_ns() - t0 > kWaitLimitNs) {
-      *abort_flag = 1;
-      if (err) atomicOr(reinterpret_cast<unsigned int*>(err), DLRM_ERRBIT_TIMEOUT);
-      return false;
+  for (uint32_t i = 1;; ++i) {
+    if (SPIN ? mbar_test_wait(bar, parity) : mbar_try_wait_suspend(bar, parity, kSuspendNs))
+      return true;
+    if (!SPIN || (i & 63) == 0) {
+      if (*abort_flag) return false;
+      if (global_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        if (err) atomicOr(reinterpret_cast<unsigned int*>(err), DLRM_ERRBIT_TIMEOUT);
+        return false;
+      }
     }
   }
 }
@@ -219,7 +245,8 @@ __device__ void produce(const Ring& r, const float* wstream, const uint2* tab, u
   for (; j < n_stages; j += n_issuers) {
     const uint32_t slot = j % r.s_count;
     if (j >= r.s_count &&
-        !wait_phase(smem_u32(&r.empty[slot]), ((j / r.s_count) - 1) & 1, r.abort_flag, r.err))
+        !wait_phase<false>(smem_u32(&r.empty[slot]), ((j / r.s_count) - 1) & 1, r.abort_flag,
+                           r.err))
       break;
     const uint2 e = __ldg(tab + j);
     mbar_arrive_expect_tx(smem_u32(&r.full[slot]), e.y);
@@ -270,7 +297,8 @@ __device__ void produce(const Ring& r, const float* wstream, const uint2* tab, u
 // them, the bias and the activation.
 template <int BM, int TM, int TN, int KSL, int KSPLIT, int CW>
 __device__ void gemm_layer(const FusedGemm& L, float* a_s, float* c_s, int lda,
-                           const float* __restrict__ bias_s, int act, const Ring& r, uint32_t& it) {
+                           const float* __restrict__ bias_s, int act, const Ring& r, uint32_t& it,
+                           unsigned long long* kstamp) {
   constexpr int RG = BM / TM;
   constexpr int SLOTS = CW / RG;               // warp slots per row group
   constexpr int KS = 16 * KSPLIT;              // k per stage
@@ -306,7 +334,7 @@ __device__ void gemm_layer(const FusedGemm& L, float* a_s, float* c_s, int lda,
 
     for (int kst = 0; kst < L.n_kst; ++kst, ++it) {
       const uint32_t st = it % r.s_count;
-      wait_phase(smem_u32(&r.full[st]), (it / r.s_count) & 1, r.abort_flag, r.err);
+      wait_phase<true>(smem_u32(&r.full[st]), (it / r.s_count) & 1, r.abort_flag, r.err);
       if (active) {
         const float* ws = r.stages + st * kFusedStageFloats + (cg * WCOLS + lane) * KS;
         const float* as = a_base + kst * KS;
@@ -369,6 +397,8 @@ __device__ void gemm_layer(const FusedGemm& L, float* a_s, float* c_s, int lda,
       ring_release(r, it);
     }
 
+    // profiling: the leader stamps the end of the layer's k-loop
+    if (kstamp && pass + 1 == L.passes && threadIdx.x == 0) *kstamp = global_ns();
     const int c0 = pass * per_pass + cg * WCOLS + lane;
     if (KSLICES == 1) {
       if (active) {
@@ -455,7 +485,7 @@ __device__ void gemm_layer(const FusedGemm& L, float* a_s, float* c_s, int lda,
 template <int BM, int CW>
 __device__ void gemm_dispatch(const FusedGemm& L, float* a_s, float* c_s, int lda,
                               const float* bias_s, int act, int zero_to, const Ring& r,
-                              uint32_t& it) {
+                              uint32_t& it, unsigned long long* kstamp) {
   // TM rows per warp (the whole tile up to 8 rows, else two row groups of
   // BM / 2), k-slices of KSL. A pass covers 64 * tn / ksplit columns with
   // SLOTS / (16 * ksplit / KSL) column groups, which fixes the lane width TN
@@ -468,7 +498,8 @@ __device__ void gemm_dispatch(const FusedGemm& L, float* a_s, float* c_s, int ld
        ? (2 * (TN16_) / (KS_)) / (SLOTS / (16 * (KS_) / KSL))                        \
        : 1)
 #define DLRM_GEMM_CASE(TN16_, KS_)                                                   \
-  gemm_layer<BM, TM, DLRM_GEMM_TN(TN16_, KS_), KSL, KS_, CW>(L, a_s, c_s, lda, bias_s, act, r, it)
+  gemm_layer<BM, TM, DLRM_GEMM_TN(TN16_, KS_), KSL, KS_, CW>(L, a_s, c_s, lda, bias_s, act, r, it, \
+                                                            kstamp)
   if (L.ksplit == 1) {
     DLRM_GEMM_CASE(8, 1);
   } else {
@@ -595,7 +626,8 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
   float* out = act1;
   for (int g = 0; g < p.n_bot; ++g) {
     const int zero_to = (g + 1 < p.n_bot) ? p.gemm[g + 1].k_pad : p.gemm[g].n_pad;
-    gemm_dispatch<BM, CW>(p.gemm[g], in, out, p.lda, bias_s, DLRM_ACT_RELU, zero_to, ring, it);
+    gemm_dispatch<BM, CW>(p.gemm[g], in, out, p.lda, bias_s, DLRM_ACT_RELU, zero_to, ring, it,
+                          kloop_stamp(p, g));
     float* t = in; in = out; out = t;
     stamp(p, 2 + g);
   }
@@ -713,7 +745,8 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
   out = (r == act0) ? act1 : act0;
   for (int g = p.n_bot; g < p.n_gemm; ++g) {
     const int zero_to = (g + 1 < p.n_gemm) ? p.gemm[g + 1].k_pad : p.k_last;
-    gemm_dispatch<BM, CW>(p.gemm[g], in, out, p.lda, bias_s, DLRM_ACT_RELU, zero_to, ring, it);
+    gemm_dispatch<BM, CW>(p.gemm[g], in, out, p.lda, bias_s, DLRM_ACT_RELU, zero_to, ring, it,
+                          kloop_stamp(p, g));
     float* t = in; in = out; out = t;
     stamp(p, 3 + g);
   }

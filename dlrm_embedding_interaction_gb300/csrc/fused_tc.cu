@@ -251,7 +251,7 @@ __device__ void issue_mmas(const FusedTcParams& p, uint32_t tmem, unsigned char*
     mma_commit(smem_addr(acc_ready));             // the layer's accumulators are final
     // profiling: per layer, ns the MMA thread waited for its input
     // activations (slot 20 + 2g) and for landed weight tiles (21 + 2g)
-    if (p.trace && 21 + 2 * g < kTcTraceSlots) {
+    if (p.trace && p.n_gemm + 3 < 20 && 21 + 2 * g < kTcTraceSlots) {
       unsigned long long* t = p.trace + static_cast<size_t>(blockIdx.x) * kTcTraceSlots;
       t[20 + 2 * g] = act_wait;
       t[21 + 2 * g] = tile_wait;

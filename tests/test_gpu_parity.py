@@ -399,3 +399,53 @@ def test_forward_full_size_zipf_b65536_k26_sampled():
     ref = oracle.embedding_bag_sum(inp["tables"], sub_idx, sub_off)
     close(emb[torch.from_numpy(ids).cuda()].cpu().numpy(), ref)
     model.close()
+
+
+@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
+def test_forward_flags_non_uniform_offsets_and_zeroes_the_bag(path):
+    """A bag start other than b * L is flagged (UNSUPPORTED) and that bag
+    contributes zeros; every other sample is the oracle's."""
+    cfg = synth.get_config("b2048_k3")
+    inp = synth.make_inputs(cfg, seed=21)
+    model = make_model(cfg, inp, path=path)
+    off = inp["offsets"].copy()
+    off[1, 5] = 7                                   # sample 5, table 1
+    out = model.forward(cu(inp["dense"]), cu(inp["indices"]), cu(off)).cpu().numpy()
+    assert model.error() == dl.ERR_UNSUPPORTED
+    ref = oracle.forward(inp)
+    keep = np.arange(cfg.batch) != 5
+    close(out[keep], ref[keep])
+    # sample 5 as if its table-1 bag were empty (the oracle's empty bag is zeros)
+    bad = dict(inp)
+    bad["tables"] = list(inp["tables"])
+    bad["indices"] = inp["indices"].copy()
+    t1 = np.concatenate([inp["tables"][1], np.zeros((1, cfg.emb_dim), np.float32)])
+    bad["tables"][1] = t1
+    bad["indices"][1, 5] = cfg.rows[1]              # the appended zero row
+    close(out[5:6], oracle.forward(bad, sample_ids=np.array([5])))
+    model.close()
+
+
+@pytest.mark.parametrize("name", ["b2048_k3", "sweep_b300_k8", "sweep_b8_k1"])
+def test_fused_phase_trace_is_ordered(name):
+    """Per-tile phase stamps of the fused kernel rise phase by phase, and each
+    GEMM layer's k-loop stamp falls inside its layer."""
+    cfg = synth.get_config(name)
+    inp = synth.make_inputs(cfg, seed=2)
+    model = make_model(cfg, inp, path=dl.PATH_FUSED)
+    buf = torch.zeros(((cfg.batch + 3) // 4) * dl.TRACE_SLOTS, dtype=torch.int64, device="cuda")
+    rows = model.set_phase_trace(buf)
+    tiles = (cfg.batch + rows - 1) // rows
+    model.forward(cu(inp["dense"]), cu(inp["indices"]), cu(inp["offsets"]))
+    assert model.error() == dl.OK
+    t = buf.view(-1, dl.TRACE_SLOTS)[:tiles].cpu().numpy()
+    n = len(model.phase_names())
+    assert (t[:, :n + 1] > 0).all()
+    assert (np.diff(t[:, :n + 1], axis=1) >= 0).all()
+    nb, nt = len(cfg.ln_bot) - 1, len(cfg.ln_top) - 1
+    for g in range(nb + nt - 1):
+        start = t[:, 1 + g] if g < nb else (t[:, 2 + nb] if g == nb else t[:, 2 + g])
+        end = t[:, 2 + g] if g < nb else t[:, 3 + g]
+        assert ((t[:, 20 + g] >= start) & (t[:, 20 + g] <= end)).all()
+    model.set_phase_trace(None)
+    model.close()

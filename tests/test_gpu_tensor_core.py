@@ -160,3 +160,42 @@ def test_fused_plan_rejects_tf32x3():
     with pytest.raises(dl.DlrmError) as ei:
         _model(cfg, inp, dl.MATH_TF32X3, dl.PATH_FUSED)
     assert ei.value.status == dl.ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("mode", MODES, ids=MODE_IDS)
+def test_fused_tensor_core_flags_non_uniform_offsets(mode):
+    cfg = synth.get_config("b2048_k3")
+    inp = synth.make_inputs(cfg, seed=9)
+    model = _model(cfg, inp, mode, dl.PATH_FUSED)
+    off = inp["offsets"].copy()
+    off[2, 40] = 41
+    out = model.forward(cu(inp["dense"]), cu(inp["indices"]), cu(off)).cpu().numpy()
+    assert model.error() == dl.ERR_UNSUPPORTED
+    keep = np.arange(cfg.batch) != 40
+    np.testing.assert_allclose(out[keep], oracle.forward(inp)[keep], rtol=2e-2, atol=0)
+    model.close()
+
+
+@pytest.mark.parametrize("mode", MODES, ids=MODE_IDS)
+def test_fused_tensor_core_phase_trace_and_host_buffers(mode):
+    """The fused tensor-core plan's phase stamps rise phase by phase, and the
+    host-buffer call (pinned buffers used in place) equals the device call."""
+    cfg = synth.get_config("sweep_b300_k3")
+    inp = synth.make_inputs(cfg, seed=4)
+    model = _model(cfg, inp, mode, dl.PATH_FUSED)
+    buf = torch.zeros(((cfg.batch + 3) // 4) * dl.TRACE_SLOTS, dtype=torch.int64, device="cuda")
+    rows = model.set_phase_trace(buf)
+    assert rows == 16
+    dev = model.forward(cu(inp["dense"]), cu(inp["indices"]), cu(inp["offsets"])).cpu().numpy()
+    assert model.error() == dl.OK
+    tiles = (cfg.batch + rows - 1) // rows
+    t = buf.view(-1, dl.TRACE_SLOTS)[:tiles].cpu().numpy()
+    n = len(model.phase_names())
+    assert (t[:, :n + 1] > 0).all() and (np.diff(t[:, :n + 1], axis=1) >= 0).all()
+    model.set_phase_trace(None)
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    out = torch.full((cfg.batch,), -1.0).pin_memory()
+    model.forward_host(pin(inp["dense"]), pin(inp["indices"]), pin(inp["offsets"]), out)
+    assert model.error() == dl.OK
+    np.testing.assert_array_equal(out.numpy(), dev)
+    model.close()
