@@ -181,6 +181,24 @@ def time_oracle(inp, batch, budget_s, max_samples=None):
                        f"{threads} threads)")
 
 
+# ---------------------------------------------------------------- ranks
+
+def max_over_ranks(local_ms: float, dist=None, device=None) -> float:
+    """The slowest rank's timed total (every rank gets it); the local value
+    on a single process. NCCL ranks pass their CUDA device, gloo ranks none."""
+    if dist is None:
+        return local_ms
+    import torch
+    t = torch.tensor([float(local_ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, samples_per_rank: int, steps: int, total_ms: float) -> float:
+    """Whole-job samples/s: every rank's samples over the slowest rank's time."""
+    return world * samples_per_rank * steps / (total_ms * 1e-3)
+
+
 # ---------------------------------------------------------------- reference arm
 
 def run_reference(args, rank, world):
@@ -211,7 +229,11 @@ def run_reference(args, rank, world):
                 steps=args.steps, warmup=args.warmup, ms_per_step=dt * 1e3 / args.steps,
                 higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64",
                 data="synthetic (seeded SplitMix64 inputs)",
-                config=dict(workload=cfg.name, batch=cfg.batch),
+                config=dict(workload=cfg.name, global_batch=cfg.batch, batch_per_gpu=cfg.batch,
+                            tables=cfg.n_tables, rows=cfg.rows[0], emb_dim=cfg.emb_dim,
+                            bag_size=cfg.bag_size, ln_bot=list(cfg.ln_bot),
+                            ln_top=list(cfg.ln_top), math="fp64 (oracle)",
+                            parallelism="rank 0 only"),
                 cpu_baseline=dict(kind="oracle", cores=threads, value=value, unit=UNIT,
                                   sample=f"{n} of {cfg.batch} samples per step (fp64 CPU "
                                          f"oracle, {threads} threads)"),
@@ -382,13 +404,9 @@ def run_ours(args, rank, world, local_rank):
                                   config=dict(workload=cfg.name, math=args.math),
                                   mode="only-forward")))
         return 0
-    total_ms = sum(ms)
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(ms), dist, dev)
     ms_per_step = total_ms / args.steps
-    value = world * cfg.batch * args.steps / (total_ms * 1e-3)
+    value = job_throughput(world, cfg.batch, args.steps, total_ms)
 
     # end to end through the host-buffer C-ABI call
     h_dense = torch.from_numpy(inp["dense"]).pin_memory()
@@ -401,13 +419,9 @@ def run_ours(args, rank, world, local_rank):
     clocks.mark(*win)
     if model.error(stream) != dl.OK:
         raise RuntimeError("device error during the e2e forward")
-    e2e_total = sum(ms_e2e)
-    if dist is not None:
-        t = torch.tensor([e2e_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_total = float(t.item())
+    e2e_total = max_over_ranks(sum(ms_e2e), dist, dev)
     h2d = (inp["dense"].nbytes + inp["indices"].nbytes + inp["offsets"].nbytes)
-    e2e = dict(value=world * cfg.batch * e2e_steps / (e2e_total * 1e-3), unit=UNIT,
+    e2e = dict(value=job_throughput(world, cfg.batch, e2e_steps, e2e_total), unit=UNIT,
                us_per_batch=e2e_total * 1e3 / e2e_steps, steps=e2e_steps,
                h2d_bytes_per_step=int(h2d), d2h_bytes_per_step=int(cfg.batch * 4),
                api="dlrm_forward_host, pinned host buffers: the kernels read the inputs and "
@@ -420,8 +434,9 @@ def run_ours(args, rank, world, local_rank):
     clocks.mark(*win)
     if model.error(stream) != dl.OK:
         raise RuntimeError("device error during the staged e2e forward")
-    e2e["staged_copies"] = dict(us_per_batch=sum(ms_st) * 1e3 / len(ms_st),
-                                value=world * cfg.batch * len(ms_st) / (sum(ms_st) * 1e-3),
+    st_total = max_over_ranks(sum(ms_st), dist, dev)
+    e2e["staged_copies"] = dict(us_per_batch=st_total * 1e3 / len(ms_st),
+                                value=job_throughput(world, cfg.batch, len(ms_st), st_total),
                                 api="dlrm_forward_host, pageable host buffers (cudaMemcpyAsync "
                                     "to and from the handle's staging buffers)")
 
