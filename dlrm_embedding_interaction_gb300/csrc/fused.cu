@@ -13,10 +13,10 @@
 //    consumption order, each 32 KB stage one contiguous block whose 16-byte
 //    chunks are XOR-swizzled so the warps' reads are bank-conflict free. It
 //    flows through a ring of stages filled by 1-D bulk async copies
-//    (cp.async.bulk) completing on mbarriers, issued by up to four lanes of
-//    one producer warp (one thread's copies are serialised), each refilling
-//    its own ring slots, running ahead across layer boundaries while eight
-//    warps compute.
+//    (cp.async.bulk) completing on mbarriers, issued by four lanes of one
+//    producer warp that each copy a quarter of every stage (one thread's
+//    copies are serialised), running ahead across layer boundaries while
+//    eight warps compute.
 //  * a computing warp owns TM = 8 rows (4 for 4-row tiles), broadcast-read
 //    from the activation buffer, and 32 * TN columns (one column per lane,
 //    TN per thread) of one 16-wide k-slice of each stage; the register tile
@@ -157,7 +157,8 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 // which shares a sub-partition with computing warps).
 constexpr uint32_t kSuspendNs = 20000;
 template <bool SPIN>
-__device__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err) {
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                           int32_t* err) {
   if (mbar_test_wait(bar, parity)) return true;
   if (*abort_flag) return false;
   const uint64_t t0 = global_ns();
@@ -191,9 +192,9 @@ __host__ __device__ __forceinline__ int gemm_rows(const FusedGemm& L, int pass) 
 
 // The weight stream flows through a ring of s_count stages: stream stage j
 // lands in slot j % s_count, full[slot] completes when its bytes have arrived
-// and empty[slot] when all CW computing warps are done with it. One producer
-// warp (one elected thread) walks the stage table, waiting on empty before
-// refilling a slot; it runs ahead across layer boundaries.
+// and empty[slot] when all CW computing warps are done with it. The producer
+// warp walks the stage table, waiting on empty before refilling a slot; it
+// runs ahead across layer boundaries.
 struct Ring {
   float* stages;
   uint64_t* full;
@@ -203,10 +204,23 @@ struct Ring {
   int32_t* err;
 };
 
-// The warp is done with stream stage j.
-__device__ __forceinline__ void ring_release(const Ring& r, uint32_t j) {
+// A consumer's place in the stream: the slot of its next stage (stage % S)
+// and that stage's full-barrier parity ((stage / S) & 1), advanced in step
+// rather than divided out per stage.
+struct RingPos {
+  uint32_t slot = 0, phase = 0;
+  __device__ __forceinline__ void advance(uint32_t s_count) {
+    if (++slot == s_count) {
+      slot = 0;
+      phase ^= 1;
+    }
+  }
+};
+
+// The warp is done with the stage in `slot`.
+__device__ __forceinline__ void ring_release(const Ring& r, uint32_t slot) {
   __syncwarp();
-  if ((threadIdx.x % kWarp) == 0) mbar_arrive(smem_u32(&r.empty[j % r.s_count]));
+  if ((threadIdx.x % kWarp) == 0) mbar_arrive(smem_u32(&r.empty[slot]));
 }
 
 // Bring this CTA's 1/gridDim share of the weight stream (16-byte granules)
@@ -227,39 +241,44 @@ __device__ void prefetch_stream_l2(const float* wstream, size_t floats) {
   }
 }
 
-// Issuing lanes of the producer warp: one thread's bulk copies run one after
-// another at about 45 GB/s, four threads reach ~150 GB/s per SM. Lane l
-// issues stream stages j = l, l + n, ... where n divides the ring depth, so
-// every slot is refilled by one lane only, in order: a lane never waits on
-// a slot's empty barrier more than one phase ahead (a parity wait cannot
-// tell phases two apart).
-__device__ __forceinline__ uint32_t issuer_count(uint32_t s_count) {
-  return s_count % 4 == 0 ? 4 : (s_count % 3 == 0 ? 3 : (s_count % 2 == 0 ? 2 : 1));
-}
+// Issuing lanes of the producer warp. One thread's bulk copies run one after
+// another at about 45 GB/s, while several threads' copies overlap (four reach
+// ~150 GB/s per SM). So every stage is cut into kIssuers pieces, one per
+// lane, and lands about four times sooner than from a single thread. The
+// lanes stay converged on one stage at a time: they wait on the same empty
+// barrier, lane 0 posts the stage's byte count on its full barrier, then each
+// lane copies its piece (complete_tx on that barrier).
+constexpr uint32_t kIssuers = 4;
+constexpr unsigned kIssuerMask = (1u << kIssuers) - 1;
 
 __device__ void produce(const Ring& r, const float* wstream, const uint2* tab, uint32_t n_stages) {
   const uint32_t lane = threadIdx.x % kWarp;
-  const uint32_t n_issuers = issuer_count(r.s_count);
-  if (lane >= n_issuers) return;
-  uint32_t j = lane;
-  for (; j < n_stages; j += n_issuers) {
-    const uint32_t slot = j % r.s_count;
-    if (j >= r.s_count &&
-        !wait_phase<false>(smem_u32(&r.empty[slot]), ((j / r.s_count) - 1) & 1, r.abort_flag,
-                           r.err))
-      break;
+  if (lane >= kIssuers) return;
+  const char* src0 = reinterpret_cast<const char*>(wstream);
+  uint32_t j = 0, slot = 0, phase = 0;   // slot = j % S, phase = (j / S) & 1
+  for (; j < n_stages; ++j) {
+    const bool ok = j < r.s_count ||
+                    wait_phase<false>(smem_u32(&r.empty[slot]), phase ^ 1, r.abort_flag, r.err);
+    if (!__all_sync(kIssuerMask, ok)) break;
     const uint2 e = __ldg(tab + j);
-    mbar_arrive_expect_tx(smem_u32(&r.full[slot]), e.y);
-    bulk_g2s(smem_u32(r.stages + slot * kFusedStageFloats), wstream + e.x, e.y,
-             smem_u32(&r.full[slot]));
+    const uint32_t full = smem_u32(&r.full[slot]);
+    if (lane == 0) mbar_arrive_expect_tx(full, e.y);
+    __syncwarp(kIssuerMask);
+    const uint32_t piece = (e.y / 16 + kIssuers - 1) / kIssuers * 16;
+    const uint32_t off = lane * piece;
+    if (off < e.y)
+      bulk_g2s(smem_u32(r.stages + slot * kFusedStageFloats) + off,
+               src0 + static_cast<size_t>(e.x) * sizeof(float) + off, min(piece, e.y - off), full);
+    if (++slot == r.s_count) {
+      slot = 0;
+      phase ^= 1;
+    }
   }
-  // This lane's copies still in flight must land before the CTA's shared
-  // memory is released: wait (bounded, regardless of abort) for its stages
-  // issued within the last ring.
-  const uint32_t issued_end = j < n_stages ? j : n_stages;
-  const uint32_t first = issued_end > r.s_count ? issued_end - r.s_count : 0;
-  for (uint32_t q = first; q < issued_end; ++q) {
-    if (q % n_issuers != lane) continue;
+  // Copies still in flight must land before the CTA's shared memory is
+  // released: wait (bounded, regardless of abort) for the stages issued
+  // within the last ring.
+  const uint32_t first = j > r.s_count ? j - r.s_count : 0;
+  for (uint32_t q = first; q < j; ++q) {
     const uint32_t bar = smem_u32(&r.full[q % r.s_count]);
     const uint64_t t0 = global_ns();
     while (!mbar_try_wait(bar, (q / r.s_count) & 1)) {
@@ -273,14 +292,14 @@ __device__ void produce(const Ring& r, const float* wstream, const uint2* tab, u
 
 // ---------------------------------------------------------------- consumers
 
-// C (BM x n_pad; zero beyond n) = act(A (BM x k_pad) W^T + b). `it` is the
-// stage counter shared with the producer's sequence.
+// C (BM x n_pad; zero beyond n) = act(A (BM x k_pad) W^T + b). `pos` is the
+// warp's place in the stage sequence shared with the producer.
 //
 // Warp roles: the BM rows form RG = BM / TM row groups of TM rows; warp w
 // takes row group w % RG and slot w / RG of the SLOTS = 8 / RG slots of its
 // group. A slot is a (column group, k-slice) pair: a stage holds KS = 16 *
 // ksplit values of k for `gemm_rows` output columns; it is cut into KSLICES =
-// 2 * ksplit slices of 8 k (two 4-wide steps) and SLOTS / KSLICES column
+// KS / KSL slices of KSL k (KSL / 4 steps of 4) and SLOTS / KSLICES column
 // groups of 32 * TN columns. Every tile height reads the same packed stream.
 // All 32 lanes of a warp read the same activation rows, so those 128-bit
 // shared loads are broadcasts (2 wavefronts); lane l owns columns l + 32 j
@@ -297,7 +316,7 @@ __device__ void produce(const Ring& r, const float* wstream, const uint2* tab, u
 // them, the bias and the activation.
 template <int BM, int TM, int TN, int KSL, int KSPLIT, int CW>
 __device__ void gemm_layer(const FusedGemm& L, float* a_s, float* c_s, int lda,
-                           const float* __restrict__ bias_s, int act, const Ring& r, uint32_t& it,
+                           const float* __restrict__ bias_s, int act, const Ring& r, RingPos& pos,
                            unsigned long long* kstamp) {
   constexpr int RG = BM / TM;
   constexpr int SLOTS = CW / RG;               // warp slots per row group
@@ -305,6 +324,7 @@ __device__ void gemm_layer(const FusedGemm& L, float* a_s, float* c_s, int lda,
   constexpr int KSLICES = KS / KSL;
   constexpr int CGS = SLOTS / KSLICES;         // column groups per pass
   static_assert(CW == 8 && BM % TM == 0 && CGS >= 1 && KS % KSL == 0, "warp slots");
+  static_assert(KSLICES <= 2 * KSPLIT, "partial sets fit the output and input buffers");
   constexpr int STEPS = KSL / 4;               // 4-wide k steps per stage
   constexpr int CPR = KS / 4;                  // 16-byte chunks per staged row
   constexpr int WCOLS = 32 * TN;               // columns of one warp
@@ -332,9 +352,9 @@ __device__ void gemm_layer(const FusedGemm& L, float* a_s, float* c_s, int lda,
 #pragma unroll
       for (int j = 0; j < TN; ++j) acc[i][j] = make_float2(0.f, 0.f);
 
-    for (int kst = 0; kst < L.n_kst; ++kst, ++it) {
-      const uint32_t st = it % r.s_count;
-      wait_phase<true>(smem_u32(&r.full[st]), (it / r.s_count) & 1, r.abort_flag, r.err);
+    for (int kst = 0; kst < L.n_kst; ++kst, pos.advance(r.s_count)) {
+      const uint32_t st = pos.slot;
+      wait_phase<true>(smem_u32(&r.full[st]), pos.phase, r.abort_flag, r.err);
       if (active) {
         const float* ws = r.stages + st * kFusedStageFloats + (cg * WCOLS + lane) * KS;
         const float* as = a_base + kst * KS;
@@ -375,26 +395,26 @@ __device__ void gemm_layer(const FusedGemm& L, float* a_s, float* c_s, int lda,
         } else {
 #pragma unroll
           for (int step = 0; step < STEPS; ++step) {
-            float4 wv[TN];
+            float4 wf[TN];
 #pragma unroll
             for (int j = 0; j < TN; ++j)
-              wv[j] = *reinterpret_cast<const float4*>(ws + 32 * j * KS + ph[step]);
+              wf[j] = *reinterpret_cast<const float4*>(ws + 32 * j * KS + ph[step]);
 #pragma unroll
             for (int i = 0; i < TM; ++i) {
               const float4 a = *reinterpret_cast<const float4*>(as + i * lda + 4 * step);
 #pragma unroll
               for (int j = 0; j < TN; ++j)
-                acc[i][j] = __ffma2_rn(make_float2(a.x, a.y), make_float2(wv[j].x, wv[j].y),
+                acc[i][j] = __ffma2_rn(make_float2(a.x, a.y), make_float2(wf[j].x, wf[j].y),
                                        acc[i][j]);
 #pragma unroll
               for (int j = 0; j < TN; ++j)
-                acc[i][j] = __ffma2_rn(make_float2(a.z, a.w), make_float2(wv[j].z, wv[j].w),
+                acc[i][j] = __ffma2_rn(make_float2(a.z, a.w), make_float2(wf[j].z, wf[j].w),
                                        acc[i][j]);
             }
           }
         }
       }
-      ring_release(r, it);
+      ring_release(r, st);
     }
 
     // profiling: the leader stamps the end of the layer's k-loop
@@ -485,29 +505,29 @@ __device__ void gemm_layer(const FusedGemm& L, float* a_s, float* c_s, int lda,
 template <int BM, int CW>
 __device__ void gemm_dispatch(const FusedGemm& L, float* a_s, float* c_s, int lda,
                               const float* bias_s, int act, int zero_to, const Ring& r,
-                              uint32_t& it, unsigned long long* kstamp) {
+                              RingPos& pos, unsigned long long* kstamp) {
   // TM rows per warp (the whole tile up to 8 rows, else two row groups of
   // BM / 2), k-slices of KSL. A pass covers 64 * tn / ksplit columns with
   // SLOTS / (16 * ksplit / KSL) column groups, which fixes the lane width TN
-  // (at least 1).
+  // (at least 1). (8-wide k-slices for layers of 64 columns or fewer, where
+  // every warp spans all columns, measured slower at 14-row tiles.)
   constexpr int TM = BM <= 8 ? BM : BM / 2;
-  constexpr int KSL = 16;
   constexpr int SLOTS = CW * TM / BM;
-#define DLRM_GEMM_TN(TN16_, KS_)                                                     \
-  ((2 * (TN16_) / (KS_)) / (SLOTS / (16 * (KS_) / KSL)) > 0                          \
-       ? (2 * (TN16_) / (KS_)) / (SLOTS / (16 * (KS_) / KSL))                        \
+#define DLRM_GEMM_TN(TN16_, KS_, KSL_)                                               \
+  ((2 * (TN16_) / (KS_)) / (SLOTS / (16 * (KS_) / (KSL_))) > 0                       \
+       ? (2 * (TN16_) / (KS_)) / (SLOTS / (16 * (KS_) / (KSL_)))                     \
        : 1)
-#define DLRM_GEMM_CASE(TN16_, KS_)                                                   \
-  gemm_layer<BM, TM, DLRM_GEMM_TN(TN16_, KS_), KSL, KS_, CW>(L, a_s, c_s, lda, bias_s, act, r, it, \
-                                                            kstamp)
+#define DLRM_GEMM_CASE(TN16_, KS_, KSL_)                                             \
+  gemm_layer<BM, TM, DLRM_GEMM_TN(TN16_, KS_, KSL_), KSL_, KS_, CW>(L, a_s, c_s, lda, bias_s, \
+                                                                    act, r, pos, kstamp)
   if (L.ksplit == 1) {
-    DLRM_GEMM_CASE(8, 1);
+    DLRM_GEMM_CASE(8, 1, 16);
   } else {
     switch (L.tn) {
-      case 8: DLRM_GEMM_CASE(8, 2); break;
-      case 4: DLRM_GEMM_CASE(4, 2); break;
-      case 2: DLRM_GEMM_CASE(2, 2); break;
-      default: DLRM_GEMM_CASE(1, 2); break;
+      case 8: DLRM_GEMM_CASE(8, 2, 16); break;
+      case 4: DLRM_GEMM_CASE(4, 2, 16); break;
+      case 2: DLRM_GEMM_CASE(2, 2, 16); break;
+      default: DLRM_GEMM_CASE(1, 2, 16); break;
     }
   }
 #undef DLRM_GEMM_CASE
@@ -532,67 +552,65 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
   const int pairs = f * (f - 1) / 2;
   bool oob = false, bad_off = false;
 
-  // Prologue: bias block + last-layer weights (group 0), then the tile's
-  // embedding rows when every bag is one row (group 1).
+  // Prologue: bias block + last-layer weights (group 0); one pass of global
+  // loads that checks every bag of size 1 (its row, or -1, kept in shared
+  // memory) and fetches the dense features into act0 (zero-padded to the
+  // first layer's k_pad), all loads issued before any is used; then the
+  // tile's embedding rows when they are prefetched whole (group 1).
   for (int c = tid; c < p.bias_floats / 4; c += kConsumers) cp_async16(bias_s + 4 * c, p.bias + 4 * c);
   for (int c = tid; c < p.k_last / 4; c += kConsumers) cp_async16(wlast_s + 4 * c, p.wlast + 4 * c);
   cp_async_commit();
-  if (p.prefetch_z) {
-    for (int e = tid; e < BM * k * d4; e += kConsumers) {
-      const int s = e / (k * d4);
-      const int rem = e - s * k * d4;
-      const int t = rem / d4;
-      const int c4 = rem - t * d4;
-      float* dst = zs + (s * k + t) * p.ldz + 4 * c4;
-      const float* table = p.tabs.ptr[t];
-      bool ok = false;
-      int64_t row = 0;
-      if (s < rows) {
-        const int64_t b = m0 + s;
-        const int64_t start = __ldg(p.offsets + static_cast<int64_t>(t) * p.batch + b);
-        row = __ldg(p.indices + static_cast<int64_t>(t) * p.batch + b);   // bag size 1
-        if (start != b) {
-          bad_off = true;
-        } else if (row < 0 || row >= p.tabs.rows[t]) {
-          oob = true;
-        } else {
-          ok = true;
+  {
+    const int n_bag = (p.prefetch_z || p.zbuf == 2) ? BM * k : 0;
+    const int kp = p.gemm[0].k_pad;
+    const int n_dense = BM * kp;
+    const int n_all = n_bag > n_dense ? n_bag : n_dense;
+    for (int e = tid; e < n_all; e += kConsumers) {
+      int64_t start = 0, row = 0, b = 0;
+      int t = 0;
+      bool bag_here = false;
+      if (e < n_bag) {
+        const int s = e / k;
+        t = e - s * k;
+        if (s < rows) {
+          b = m0 + s;
+          start = __ldg(p.offsets + static_cast<int64_t>(t) * p.batch + b);
+          row = __ldg(p.indices + static_cast<int64_t>(t) * p.batch + b);
+          bag_here = true;
         }
       }
-      if (ok) cp_async16(dst, table + row * d + 4 * c4);
-      else cp_async16_zero(dst, table);
-    }
-  } else if (p.zbuf == 2) {
-    // Bag size 1, rows streamed later: check every bag now and keep its row
-    // (or -1) in shared memory, so the streaming needs no dependent loads.
-    for (int e = tid; e < BM * k; e += kConsumers) {
-      const int s = e / k;
-      const int t = e - s * k;
-      int row32 = -1;
-      if (s < rows) {
-        const int64_t b = m0 + s;
-        const int64_t start = __ldg(p.offsets + static_cast<int64_t>(t) * p.batch + b);
-        const int64_t row = __ldg(p.indices + static_cast<int64_t>(t) * p.batch + b);
-        if (start != b) bad_off = true;
-        else if (row < 0 || row >= p.tabs.rows[t]) oob = true;
-        else row32 = static_cast<int>(row);
+      float dv = 0.f;
+      int m = 0, c = 0;
+      if (e < n_dense) {
+        m = e / kp;
+        c = e - m * kp;
+        if (m < rows && c < p.n_dense) dv = __ldg(p.dense + static_cast<int64_t>(m0 + m) * p.n_dense + c);
       }
-      rowidx_s[e] = row32;
+      if (e < n_bag) {
+        int row32 = -1;
+        if (bag_here) {
+          if (start != b) bad_off = true;
+          else if (row < 0 || row >= p.tabs.rows[t]) oob = true;
+          else row32 = static_cast<int>(row);
+        }
+        rowidx_s[e] = row32;
+      }
+      if (e < n_dense) act0[m * p.lda + c] = dv;
+    }
+  }
+  consumer_sync<CW>();
+  if (p.prefetch_z) {
+    for (int e = tid; e < BM * k * d4; e += kConsumers) {
+      const int sk = e / d4;              // sample * k + table
+      const int c4 = e - sk * d4;
+      const float* table = p.tabs.ptr[sk % k];
+      float* dst = zs + sk * p.ldz + 4 * c4;
+      const int row = rowidx_s[sk];
+      if (row >= 0) cp_async16(dst, table + static_cast<int64_t>(row) * d + 4 * c4);
+      else cp_async16_zero(dst, table);
     }
   }
   cp_async_commit();
-
-  // dense features -> act0, zero-padded to the first layer's k_pad
-  {
-    const int kp = p.gemm[0].k_pad;
-    for (int e = tid; e < BM * kp; e += kConsumers) {
-      const int m = e / kp;
-      const int c = e - m * kp;
-      act0[m * p.lda + c] = (m < rows && c < p.n_dense)
-                                ? __ldg(p.dense + static_cast<int64_t>(m0 + m) * p.n_dense + c)
-                                : 0.f;
-    }
-  }
   cp_async_wait<1>();
   consumer_sync<CW>();
   stamp(p, 1);
@@ -621,12 +639,12 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
     else cp_async_commit();
   }
 
-  uint32_t it = 0;
+  RingPos pos;
   float* in = act0;
   float* out = act1;
   for (int g = 0; g < p.n_bot; ++g) {
     const int zero_to = (g + 1 < p.n_bot) ? p.gemm[g + 1].k_pad : p.gemm[g].n_pad;
-    gemm_dispatch<BM, CW>(p.gemm[g], in, out, p.lda, bias_s, DLRM_ACT_RELU, zero_to, ring, it,
+    gemm_dispatch<BM, CW>(p.gemm[g], in, out, p.lda, bias_s, DLRM_ACT_RELU, zero_to, ring, pos,
                           kloop_stamp(p, g));
     float* t = in; in = out; out = t;
     stamp(p, 2 + g);
@@ -745,7 +763,7 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
   out = (r == act0) ? act1 : act0;
   for (int g = p.n_bot; g < p.n_gemm; ++g) {
     const int zero_to = (g + 1 < p.n_gemm) ? p.gemm[g + 1].k_pad : p.k_last;
-    gemm_dispatch<BM, CW>(p.gemm[g], in, out, p.lda, bias_s, DLRM_ACT_RELU, zero_to, ring, it,
+    gemm_dispatch<BM, CW>(p.gemm[g], in, out, p.lda, bias_s, DLRM_ACT_RELU, zero_to, ring, pos,
                           kloop_stamp(p, g));
     float* t = in; in = out; out = t;
     stamp(p, 3 + g);
