@@ -236,8 +236,8 @@ def run_forward(model, inp):
 
 
 FORWARD_CASES = ["tiny_b64_k3", "mini_b2048_k3_d4", "b2048_k3", "b2048_k32",
-                 "sweep_b1_k1", "sweep_b8_k16", "sweep_b33_k3", "sweep_b4096_k8",
-                 "sweep_b8192_k32"]
+                 "sweep_b1_k1", "sweep_b8_k16", "sweep_b33_k3", "sweep_b1500_k3",
+                 "sweep_b4096_k8", "sweep_b8192_k32"]
 
 
 @pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
@@ -248,6 +248,18 @@ def test_forward_matches_oracle(name, path):
     model = make_model(cfg, inp, path=path)
     got = run_forward(model, inp)
     close(got, oracle.forward(inp))
+    model.close()
+
+
+@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
+def test_forward_odd_widths_matches_oracle(path):
+    """Layers wider than 512 (two column passes), and 128-, 100- and 32-wide
+    layers, at 2048 samples: every weight-tile form of the fused GEMM."""
+    cfg = synth.DlrmConfig("odd_widths_b2048", 2048, (13, 600, 128, 32), (1000, 1000, 1000), 32,
+                           1, (38, 600, 100, 1))
+    inp = synth.make_inputs(cfg, seed=99)
+    model = make_model(cfg, inp, path=path)
+    close(run_forward(model, inp), oracle.forward(inp))
     model.close()
 
 
