@@ -471,6 +471,12 @@ def run_ours(args, rank, world, local_rank):
         tiles = (cfg.batch + rows - 1) // rows
         pnames = model.phase_names()
         acc = np.zeros(len(pnames))
+        # fp32 kernel: the leader also stamps the end of every GEMM's k-loop
+        # (slot 20 + g) while the phase stamps end below slot 20
+        n_bot = len(cfg.ln_bot) - 1
+        n_gemm = n_bot + len(cfg.ln_top) - 2
+        split = args.math == "fp32" and n_gemm + 3 < 20
+        kacc = np.zeros((n_gemm, 2))
         span = 0.0
         reps = 20
         with torch.cuda.stream(stream):
@@ -479,12 +485,23 @@ def run_ours(args, rank, world, local_rank):
                 buf.zero_()
                 model.forward(dense, idx, off, out, stream=stream)
                 stream.synchronize()
-                t = buf.view(-1, dl.TRACE_SLOTS)[:tiles, :len(pnames) + 1].cpu().numpy()
+                full = buf.view(-1, dl.TRACE_SLOTS)[:tiles].cpu().numpy()
+                t = full[:, :len(pnames) + 1]
                 acc += np.diff(t, axis=1).mean(axis=0) / 1e3
                 span += (t[:, -1].max() - t[:, 0].min()) / 1e3
+                if split:
+                    for g in range(n_gemm):
+                        first = 1 + g if g < n_bot else 2 + g    # stamp before the layer
+                        kend = full[:, 20 + g]
+                        kacc[g, 0] += (kend - full[:, first]).mean() / 1e3
+                        kacc[g, 1] += (full[:, first + 1] - kend).mean() / 1e3
         model.set_phase_trace(None)
         phases_us = {n: float(v / reps) for n, v in zip(pnames, acc)}
         phases_us["kernel_span"] = span / reps
+        if split:
+            names_g = [pnames[1 + g] if g < n_bot else pnames[2 + g] for g in range(n_gemm)]
+            phases_us["gemm_kloop_epilogue"] = {
+                n: [float(kacc[g, 0] / reps), float(kacc[g, 1] / reps)] for g, n in enumerate(names_g)}
     dom = max(stage_us, key=stage_us.get)
     flops, byts = stage_work(cfg, dom, cfg.batch)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
