@@ -270,8 +270,9 @@ __device__ void issue_mmas(const FusedTcParams& p, uint32_t tmem, unsigned char*
 
 template <bool BF16>
 __device__ void epilogue(const FusedTcParams& p, uint32_t tmem, unsigned char* const act[2],
-                         float* xf, float* hf, float* zs, float* bias_s, float* wlast_s,
-                         uint64_t* acc_ready, uint64_t* act_ready, volatile int* abort_flag) {
+                         float* xf, float* hf, float* zs, int* rowidx_s, float* bias_s,
+                         float* wlast_s, uint64_t* acc_ready, uint64_t* act_ready,
+                         volatile int* abort_flag) {
   constexpr int KB = BF16 ? 64 : 32;
   const int tid = threadIdx.x;                 // 0 .. 127
   const int warp = tid / kWarp;
@@ -283,47 +284,62 @@ __device__ void epilogue(const FusedTcParams& p, uint32_t tmem, unsigned char* c
   const int pairs = f * (f - 1) / 2;
   bool oob = false, bad_off = false;
 
-  // ---- prologue: bag rows (cp.async), biases, last-layer weights, dense rows
-  for (int e = tid; e < kTcTile * k * d4; e += kEpiWarps * kWarp) {
-    const int s = e / (k * d4);
-    const int rem = e - s * (k * d4);
-    const int t = rem / d4;
-    const int c4 = rem - t * d4;
-    float* dst = zs + (s * k + t) * p.ldz + 4 * c4;
-    const float* table = p.tabs.ptr[t];
-    const float* src = table;
-    int bytes = 0;
-    if (s < rows) {
-      const int64_t b = m0 + s;
-      const int64_t start = __ldg(p.offsets + static_cast<int64_t>(t) * p.batch + b);
-      const int64_t row = __ldg(p.indices + static_cast<int64_t>(t) * p.batch + b);  // bag 1
-      if (start != b) {
-        bad_off = true;
-      } else if (row < 0 || row >= p.tabs.rows[t]) {
-        oob = true;
-      } else {
-        src = table + row * d + 4 * c4;
-        bytes = 16;
-      }
-    }
-    cp_async16(dst, src, bytes);
-  }
-  for (int c = tid; c < p.bias_floats / 4; c += kEpiWarps * kWarp)
-    cp_async16(bias_s + 4 * c, p.bias + 4 * c, 16);
-  for (int c = tid; c < p.k_last / 4; c += kEpiWarps * kWarp)
-    cp_async16(wlast_s + 4 * c, p.wlast + 4 * c, 16);
-  asm volatile("cp.async.commit_group;\n" ::: "memory");
+  // ---- prologue. Biases and last-layer weights by cp.async; then one pass
+  // of global loads, all issued before any is used: every bag (size 1)
+  // checked, its row (or -1) kept in shared memory, and the dense features
+  // written as layer 0's operand (zero-padded); then the bag rows by cp.async.
+  constexpr int kEpi = kEpiWarps * kWarp;
+  for (int c = tid; c < p.bias_floats / 4; c += kEpi) cp_async16(bias_s + 4 * c, p.bias + 4 * c, 16);
+  for (int c = tid; c < p.k_last / 4; c += kEpi) cp_async16(wlast_s + 4 * c, p.wlast + 4 * c, 16);
   {
+    const int n_bag = kTcTile * k;
     const int kw = p.gemm[0].kbs * KB;          // layer 0 input width, zero padded
-    for (int e = tid; e < kTcTile * kw; e += kEpiWarps * kWarp) {
-      const int s = e / kw;
-      const int c = e - s * kw;
-      const float v = (s < rows && c < p.n_dense)
-                          ? __ldg(p.dense + static_cast<int64_t>(m0 + s) * p.n_dense + c)
-                          : 0.f;
-      put_operand<BF16>(act[0], s, c, v);
+    const int n_dense = kTcTile * kw;
+    const int n_all = n_bag > n_dense ? n_bag : n_dense;
+    for (int e = tid; e < n_all; e += kEpi) {
+      int64_t start = 0, row = 0, b = 0;
+      int t = 0;
+      bool bag_here = false;
+      if (e < n_bag) {
+        const int s = e / k;
+        t = e - s * k;
+        if (s < rows) {
+          b = m0 + s;
+          start = __ldg(p.offsets + static_cast<int64_t>(t) * p.batch + b);
+          row = __ldg(p.indices + static_cast<int64_t>(t) * p.batch + b);
+          bag_here = true;
+        }
+      }
+      float dv = 0.f;
+      int ds = 0, dc = 0;
+      if (e < n_dense) {
+        ds = e / kw;
+        dc = e - ds * kw;
+        if (ds < rows && dc < p.n_dense)
+          dv = __ldg(p.dense + static_cast<int64_t>(m0 + ds) * p.n_dense + dc);
+      }
+      if (e < n_bag) {
+        int row32 = -1;
+        if (bag_here) {
+          if (start != b) bad_off = true;
+          else if (row < 0 || row >= p.tabs.rows[t]) oob = true;
+          else row32 = static_cast<int>(row);
+        }
+        rowidx_s[e] = row32;
+      }
+      if (e < n_dense) put_operand<BF16>(act[0], ds, dc, dv);
     }
   }
+  epi_sync();
+  for (int e = tid; e < kTcTile * k * d4; e += kEpi) {
+    const int sk = e / d4;                      // sample * k + table
+    const int c4 = e - sk * d4;
+    const float* table = p.tabs.ptr[sk % k];
+    const int row = rowidx_s[sk];
+    cp_async16(zs + sk * p.ldz + 4 * c4, row >= 0 ? table + static_cast<int64_t>(row) * d + 4 * c4 : table,
+               row >= 0 ? 16 : 0);
+  }
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   epi_sync();
   if (tid == 0) mbar_arrive(smem_addr(act_ready));
@@ -341,24 +357,27 @@ __device__ void epilogue(const FusedTcParams& p, uint32_t tmem, unsigned char* c
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     unsigned char* out = act[(g + 1) & 1];
     for (int mt = 0; mt < L.mts; ++mt) {
-      float acc[kTcTile];
+      // the four K-step partial sums of this M-tile: four loads, one wait
+      uint32_t r[4][kTcTile];
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
-        uint32_t r[kTcTile];
         const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16) +
                                static_cast<uint32_t>((mt * 4 + ks) * kTcTile);
         asm volatile(
             "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, "
             "%10, %11, %12, %13, %14, %15}, [%16];"
-            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-              "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-              "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+            : "=r"(r[ks][0]), "=r"(r[ks][1]), "=r"(r[ks][2]), "=r"(r[ks][3]), "=r"(r[ks][4]),
+              "=r"(r[ks][5]), "=r"(r[ks][6]), "=r"(r[ks][7]), "=r"(r[ks][8]), "=r"(r[ks][9]),
+              "=r"(r[ks][10]), "=r"(r[ks][11]), "=r"(r[ks][12]), "=r"(r[ks][13]),
+              "=r"(r[ks][14]), "=r"(r[ks][15])
             : "r"(taddr));
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-        for (int c = 0; c < kTcTile; ++c)
-          acc[c] = ks == 0 ? __uint_as_float(r[c]) : acc[c] + __uint_as_float(r[c]);
       }
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      float acc[kTcTile];
+#pragma unroll
+      for (int c = 0; c < kTcTile; ++c)
+        acc[c] = (__uint_as_float(r[0][c]) + __uint_as_float(r[1][c])) +
+                 (__uint_as_float(r[2][c]) + __uint_as_float(r[3][c]));
       const int feat = mt * 128 + warp * 32 + lane;
       const bool live = feat < L.n;
       const float bv = live ? bias_s[L.b_off + feat] : 0.f;
@@ -379,28 +398,31 @@ __device__ void epilogue(const FusedTcParams& p, uint32_t tmem, unsigned char* c
       asm volatile("cp.async.wait_all;\n" ::: "memory");
       epi_sync();
       stamp(p, 2 + g);
+      // one (sample, pair) dot per thread, then zeros to the padded width
       const int kw = p.gemm[g + 1].kbs * KB;
-      for (int e = tid; e < kTcTile * (kw - d); e += kEpiWarps * kWarp) {
-        const int s = e / (kw - d);
-        const int q = e - s * (kw - d);
-        float v = 0.f;
-        if (q < pairs) {
-          int i, jj;
-          pair_from_index(q, i, jj);
-          const float* vi = (i == 0) ? xf + s * d : zs + (s * k + i - 1) * p.ldz;
-          const float* vj = (jj == 0) ? xf + s * d : zs + (s * k + jj - 1) * p.ldz;
-          float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int c4 = 0; c4 < d4; ++c4) {
-            const float4 u = *reinterpret_cast<const float4*>(vi + 4 * c4);
-            const float4 w = *reinterpret_cast<const float4*>(vj + 4 * c4);
-            a.x = fmaf(u.x, w.x, a.x);
-            a.y = fmaf(u.y, w.y, a.y);
-            a.z = fmaf(u.z, w.z, a.z);
-            a.w = fmaf(u.w, w.w, a.w);
-          }
-          v = (a.x + a.y) + (a.z + a.w);
+      for (int e = tid; e < kTcTile * pairs; e += kEpiWarps * kWarp) {
+        const int s = e / pairs;
+        const int q = e - s * pairs;
+        int i, jj;
+        pair_from_index(q, i, jj);
+        const float* vi = (i == 0) ? xf + s * d : zs + (s * k + i - 1) * p.ldz;
+        const float* vj = (jj == 0) ? xf + s * d : zs + (s * k + jj - 1) * p.ldz;
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+        for (int c4 = 0; c4 < d4; ++c4) {
+          const float4 u = *reinterpret_cast<const float4*>(vi + 4 * c4);
+          const float4 w = *reinterpret_cast<const float4*>(vj + 4 * c4);
+          a.x = fmaf(u.x, w.x, a.x);
+          a.y = fmaf(u.y, w.y, a.y);
+          a.z = fmaf(u.z, w.z, a.z);
+          a.w = fmaf(u.w, w.w, a.w);
         }
-        put_operand<BF16>(out, s, d + q, v);
+        put_operand<BF16>(out, s, d + q, (a.x + a.y) + (a.z + a.w));
+      }
+      const int pad = kw - d - pairs;
+      for (int e = tid; e < kTcTile * pad; e += kEpiWarps * kWarp) {
+        const int s = e / pad;
+        put_operand<BF16>(out, s, d + pairs + (e - s * pad), 0.f);
       }
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -446,6 +468,7 @@ fused_tc_kernel(const __grid_constant__ FusedTcParams p) {
   float* xf = reinterpret_cast<float*>(base + p.off_xf);
   float* hf = reinterpret_cast<float*>(base + p.off_hf);
   float* zs = reinterpret_cast<float*>(base + p.off_z);
+  int* rowidx_s = reinterpret_cast<int*>(base + p.off_rowidx);
   float* bias_s = reinterpret_cast<float*>(base + p.off_bias);
   float* wlast_s = reinterpret_cast<float*>(base + p.off_wlast);
   uint64_t* full = reinterpret_cast<uint64_t*>(base + p.off_bar);
@@ -484,7 +507,8 @@ fused_tc_kernel(const __grid_constant__ FusedTcParams p) {
     if (threadIdx.x % kWarp == 0)
       issue_mmas<BF16>(p, tmem, ring, act, full, empty, acc_ready, act_ready, abort_flag);
   } else {
-    epilogue<BF16>(p, tmem, act, xf, hf, zs, bias_s, wlast_s, acc_ready, act_ready, abort_flag);
+    epilogue<BF16>(p, tmem, act, xf, hf, zs, rowidx_s, bias_s, wlast_s, acc_ready, act_ready,
+                   abort_flag);
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
@@ -601,6 +625,7 @@ bool fused_tc_plan(int n_dense, int k_tables, int d, int bag, const std::vector<
       2 * static_cast<size_t>(p.act_bytes) + align_up(static_cast<size_t>(kTcTile) * d * 4, 128) +
       align_up(static_cast<size_t>(kTcTile) * p.k_last * 4, 128) +
       align_up(static_cast<size_t>(kTcTile) * k_tables * p.ldz * 4, 128) +
+      align_up(static_cast<size_t>(kTcTile) * k_tables * 4, 128) +
       align_up(static_cast<size_t>(bias_floats) * 4, 128) + align_up(p.k_last * 4, 128);
   int stages = 0;
   for (int s = 12; s >= 2; --s) {         // the deepest ring that fits
@@ -623,6 +648,8 @@ bool fused_tc_plan(int n_dense, int k_tables, int d, int bag, const std::vector<
   off += align_up(static_cast<size_t>(kTcTile) * p.k_last * 4, 128);
   p.off_z = static_cast<int>(off);
   off += align_up(static_cast<size_t>(kTcTile) * k_tables * p.ldz * 4, 128);
+  p.off_rowidx = static_cast<int>(off);
+  off += align_up(static_cast<size_t>(kTcTile) * k_tables * 4, 128);
   p.off_bias = static_cast<int>(off);
   off += align_up(static_cast<size_t>(bias_floats) * 4, 128);
   p.off_wlast = static_cast<int>(off);

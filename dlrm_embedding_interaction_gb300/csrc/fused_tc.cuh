@@ -32,7 +32,7 @@ struct FusedTcParams {
   int b_last;          // its bias offset in the bias block
   int bias_floats;
   // shared-memory carve (bytes from the 1024-aligned base)
-  int off_act0, off_act1, off_xf, off_hf, off_z, off_bias, off_wlast, off_bar;
+  int off_act0, off_act1, off_xf, off_hf, off_z, off_rowidx, off_bias, off_wlast, off_bar;
   int act_bytes;       // one activation buffer
   int smem_bytes;      // dynamic shared memory requested (base alignment included)
   TcGemm gemm[kTcMaxGemm];
