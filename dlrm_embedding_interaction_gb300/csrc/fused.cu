@@ -552,10 +552,10 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
   const int pairs = f * (f - 1) / 2;
   bool oob = false, bad_off = false;
 
-  // Prologue: bias block + last-layer weights (group 0); one pass of global
-  // loads that checks every bag of size 1 (its row, or -1, kept in shared
-  // memory) and fetches the dense features into act0 (zero-padded to the
-  // first layer's k_pad), all loads issued before any is used; then the
+  // Prologue: bias block + last-layer weights (group 0); global loads, two
+  // per thread in flight before either is used, that check every bag of
+  // size 1 (its row, or -1, kept in shared memory) and fetch the dense
+  // features into act0 (zero-padded to the first layer's k_pad); then the
   // tile's embedding rows when they are prefetched whole (group 1).
   for (int c = tid; c < p.bias_floats / 4; c += kConsumers) cp_async16(bias_s + 4 * c, p.bias + 4 * c);
   for (int c = tid; c < p.k_last / 4; c += kConsumers) cp_async16(wlast_s + 4 * c, p.wlast + 4 * c);
@@ -565,37 +565,46 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
     const int kp = p.gemm[0].k_pad;
     const int n_dense = BM * kp;
     const int n_all = n_bag > n_dense ? n_bag : n_dense;
-    for (int e = tid; e < n_all; e += kConsumers) {
-      int64_t start = 0, row = 0, b = 0;
-      int t = 0;
-      bool bag_here = false;
-      if (e < n_bag) {
-        const int s = e / k;
-        t = e - s * k;
-        if (s < rows) {
-          b = m0 + s;
-          start = __ldg(p.offsets + static_cast<int64_t>(t) * p.batch + b);
-          row = __ldg(p.indices + static_cast<int64_t>(t) * p.batch + b);
-          bag_here = true;
+    // two elements per thread, both loads in flight before either is used
+    for (int e0 = 0; e0 < n_all; e0 += 2 * kConsumers) {
+      int64_t start[2], row[2];
+      float dv[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int e = e0 + h * kConsumers + tid;
+        start[h] = row[h] = 0;
+        dv[h] = 0.f;
+        if (e < n_bag) {
+          const int s = e / k, t = e - s * k;
+          if (s < rows) {
+            start[h] = __ldg(p.offsets + static_cast<int64_t>(t) * p.batch + m0 + s);
+            row[h] = __ldg(p.indices + static_cast<int64_t>(t) * p.batch + m0 + s);
+          }
+        }
+        if (e < n_dense) {
+          const int m = e / kp, c = e - m * kp;
+          if (m < rows && c < p.n_dense)
+            dv[h] = __ldg(p.dense + static_cast<int64_t>(m0 + m) * p.n_dense + c);
         }
       }
-      float dv = 0.f;
-      int m = 0, c = 0;
-      if (e < n_dense) {
-        m = e / kp;
-        c = e - m * kp;
-        if (m < rows && c < p.n_dense) dv = __ldg(p.dense + static_cast<int64_t>(m0 + m) * p.n_dense + c);
-      }
-      if (e < n_bag) {
-        int row32 = -1;
-        if (bag_here) {
-          if (start != b) bad_off = true;
-          else if (row < 0 || row >= p.tabs.rows[t]) oob = true;
-          else row32 = static_cast<int>(row);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int e = e0 + h * kConsumers + tid;
+        if (e < n_bag) {
+          const int s = e / k, t = e - s * k;
+          int row32 = -1;
+          if (s < rows) {
+            if (start[h] != m0 + s) bad_off = true;
+            else if (row[h] < 0 || row[h] >= p.tabs.rows[t]) oob = true;
+            else row32 = static_cast<int>(row[h]);
+          }
+          rowidx_s[e] = row32;
         }
-        rowidx_s[e] = row32;
+        if (e < n_dense) {
+          const int m = e / kp;
+          act0[m * p.lda + (e - m * kp)] = dv[h];
+        }
       }
-      if (e < n_dense) act0[m * p.lda + c] = dv;
     }
   }
   consumer_sync<CW>();

@@ -284,53 +284,68 @@ __device__ void epilogue(const FusedTcParams& p, uint32_t tmem, unsigned char* c
   const int pairs = f * (f - 1) / 2;
   bool oob = false, bad_off = false;
 
-  // ---- prologue. Biases and last-layer weights by cp.async; then one pass
-  // of global loads, all issued before any is used: every bag (size 1)
-  // checked, its row (or -1) kept in shared memory, and the dense features
-  // written as layer 0's operand (zero-padded); then the bag rows by cp.async.
+  // ---- prologue. Biases and last-layer weights by cp.async. Then global
+  // loads, two per thread in flight before either is used: every bag (size
+  // 1) checked and its row (or -1) kept in shared memory, and the dense
+  // features written as layer 0's operand (the padding is zeroed apart). The
+  // MMA warp may start once the operand is complete; the bag rows follow by
+  // cp.async and land while layer 0 runs.
   constexpr int kEpi = kEpiWarps * kWarp;
   for (int c = tid; c < p.bias_floats / 4; c += kEpi) cp_async16(bias_s + 4 * c, p.bias + 4 * c, 16);
   for (int c = tid; c < p.k_last / 4; c += kEpi) cp_async16(wlast_s + 4 * c, p.wlast + 4 * c, 16);
   {
     const int n_bag = kTcTile * k;
+    const int n_dn = kTcTile * p.n_dense;
+    const int n_all = n_bag > n_dn ? n_bag : n_dn;
+    for (int e0 = 0; e0 < n_all; e0 += 2 * kEpi) {
+      int64_t start[2], row[2];
+      float dv[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int e = e0 + h * kEpi + tid;
+        start[h] = row[h] = 0;
+        dv[h] = 0.f;
+        if (e < n_bag) {
+          const int s = e / k, t = e - s * k;
+          if (s < rows) {
+            start[h] = __ldg(p.offsets + static_cast<int64_t>(t) * p.batch + m0 + s);
+            row[h] = __ldg(p.indices + static_cast<int64_t>(t) * p.batch + m0 + s);
+          }
+        }
+        if (e < n_dn) {
+          const int s = e / p.n_dense;
+          if (s < rows) dv[h] = __ldg(p.dense + static_cast<int64_t>(m0) * p.n_dense + e);
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int e = e0 + h * kEpi + tid;
+        if (e < n_bag) {
+          const int s = e / k, t = e - s * k;
+          int row32 = -1;
+          if (s < rows) {
+            if (start[h] != m0 + s) bad_off = true;
+            else if (row[h] < 0 || row[h] >= p.tabs.rows[t]) oob = true;
+            else row32 = static_cast<int>(row[h]);
+          }
+          rowidx_s[e] = row32;
+        }
+        if (e < n_dn) {
+          const int s = e / p.n_dense;
+          put_operand<BF16>(act[0], s, e - s * p.n_dense, dv[h]);
+        }
+      }
+    }
     const int kw = p.gemm[0].kbs * KB;          // layer 0 input width, zero padded
-    const int n_dense = kTcTile * kw;
-    const int n_all = n_bag > n_dense ? n_bag : n_dense;
-    for (int e = tid; e < n_all; e += kEpi) {
-      int64_t start = 0, row = 0, b = 0;
-      int t = 0;
-      bool bag_here = false;
-      if (e < n_bag) {
-        const int s = e / k;
-        t = e - s * k;
-        if (s < rows) {
-          b = m0 + s;
-          start = __ldg(p.offsets + static_cast<int64_t>(t) * p.batch + b);
-          row = __ldg(p.indices + static_cast<int64_t>(t) * p.batch + b);
-          bag_here = true;
-        }
-      }
-      float dv = 0.f;
-      int ds = 0, dc = 0;
-      if (e < n_dense) {
-        ds = e / kw;
-        dc = e - ds * kw;
-        if (ds < rows && dc < p.n_dense)
-          dv = __ldg(p.dense + static_cast<int64_t>(m0 + ds) * p.n_dense + dc);
-      }
-      if (e < n_bag) {
-        int row32 = -1;
-        if (bag_here) {
-          if (start != b) bad_off = true;
-          else if (row < 0 || row >= p.tabs.rows[t]) oob = true;
-          else row32 = static_cast<int>(row);
-        }
-        rowidx_s[e] = row32;
-      }
-      if (e < n_dense) put_operand<BF16>(act[0], ds, dc, dv);
+    const int pad = kw - p.n_dense;
+    for (int e = tid; e < kTcTile * pad; e += kEpi) {
+      const int s = e / pad;
+      put_operand<BF16>(act[0], s, p.n_dense + (e - s * pad), 0.f);
     }
   }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   epi_sync();
+  if (tid == 0) mbar_arrive(smem_addr(act_ready));
   for (int e = tid; e < kTcTile * k * d4; e += kEpi) {
     const int sk = e / d4;                      // sample * k + table
     const int c4 = e - sk * d4;
@@ -340,9 +355,6 @@ __device__ void epilogue(const FusedTcParams& p, uint32_t tmem, unsigned char* c
                row >= 0 ? 16 : 0);
   }
   asm volatile("cp.async.commit_group;\n" ::: "memory");
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  epi_sync();
-  if (tid == 0) mbar_arrive(smem_addr(act_ready));
   // biases, last-layer weights and bag rows land while layer 0 runs
   asm volatile("cp.async.wait_all;\n" ::: "memory");
   epi_sync();
