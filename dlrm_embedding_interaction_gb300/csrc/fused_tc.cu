@@ -151,6 +151,33 @@ __device__ __forceinline__ void put_operand(unsigned char* buf, int s, int f, fl
   }
 }
 
+// Zeros features [f0, f1) of every sample of a B-operand buffer: the 16-byte
+// chunks wholly inside the range by one vector store each, the partial
+// chunks at either end element by element.
+template <bool BF16>
+__device__ void zero_operand(unsigned char* buf, int f0, int f1, int tid, int nthreads) {
+  constexpr int EPC = BF16 ? 8 : 4;             // elements per 16-byte chunk
+  constexpr int KB = BF16 ? 64 : 32;
+  const int c0 = (f0 + EPC - 1) / EPC, c1 = f1 / EPC;   // whole chunks [c0, c1)
+  if (c0 >= c1) {
+    for (int e = tid; e < kTcTile * (f1 - f0); e += nthreads)
+      put_operand<BF16>(buf, e / (f1 - f0), f0 + e % (f1 - f0), 0.f);
+    return;
+  }
+  const int head = c0 * EPC - f0, tail = f1 - c1 * EPC;
+  for (int e = tid; e < kTcTile * (head + tail); e += nthreads) {
+    const int s = e / (head + tail), q = e % (head + tail);
+    put_operand<BF16>(buf, s, q < head ? f0 + q : c1 * EPC + (q - head), 0.f);
+  }
+  const int nch = c1 - c0;
+  for (int e = tid; e < kTcTile * nch; e += nthreads) {
+    const int s = e / nch, c = c0 + e % nch;      // chunk c of the feature axis
+    const int f = c * EPC;
+    *reinterpret_cast<uint4*>(buf + (f / KB) * kActBlock + swz_offset(s, (f % KB) * (BF16 ? 2 : 4) >> 4)) =
+        make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
 // ---------------------------------------------------------------- roles
 
 
@@ -336,12 +363,8 @@ __device__ void epilogue(const FusedTcParams& p, uint32_t tmem, unsigned char* c
         }
       }
     }
-    const int kw = p.gemm[0].kbs * KB;          // layer 0 input width, zero padded
-    const int pad = kw - p.n_dense;
-    for (int e = tid; e < kTcTile * pad; e += kEpi) {
-      const int s = e / pad;
-      put_operand<BF16>(act[0], s, p.n_dense + (e - s * pad), 0.f);
-    }
+    // layer 0 input, zero-padded to its K-blocks
+    zero_operand<BF16>(act[0], p.n_dense, p.gemm[0].kbs * KB, tid, kEpi);
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   epi_sync();
@@ -431,11 +454,7 @@ __device__ void epilogue(const FusedTcParams& p, uint32_t tmem, unsigned char* c
         }
         put_operand<BF16>(out, s, d + q, (a.x + a.y) + (a.z + a.w));
       }
-      const int pad = kw - d - pairs;
-      for (int e = tid; e < kTcTile * pad; e += kEpiWarps * kWarp) {
-        const int s = e / pad;
-        put_operand<BF16>(out, s, d + pairs + (e - s * pad), 0.f);
-      }
+      zero_operand<BF16>(out, d + pairs, kw, tid, kEpiWarps * kWarp);
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     if (!last_hidden) {
@@ -451,13 +470,29 @@ __device__ void epilogue(const FusedTcParams& p, uint32_t tmem, unsigned char* c
   }
 
   // ---- last layer: fp32 dot and sigmoid, a warp per sample
+  // (warp w takes samples w, w + 4, w + 8, w + 12 together: four
+  // independent sums per lane)
   const float bl = bias_s[p.b_last];
-  for (int s = warp; s < rows; s += kEpiWarps) {
-    float acc = 0.f;
-    for (int q = lane; q < p.k_last; q += kWarp) acc = fmaf(hf[s * p.k_last + q], wlast_s[q], acc);
+  {
+    constexpr int kPer = kTcTile / kEpiWarps;
+    static_assert(kTcTile % kEpiWarps == 0, "whole samples per warp");
+    float acc[kPer];
 #pragma unroll
-    for (int o = kWarp / 2; o > 0; o /= 2) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) p.out[m0 + s] = 1.0f / (1.0f + expf(-(acc + bl)));
+    for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
+    for (int q = lane; q < p.k_last; q += kWarp) {
+      const float wq = wlast_s[q];
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) acc[i] = fmaf(hf[(warp + i * kEpiWarps) * p.k_last + q], wq, acc[i]);
+    }
+#pragma unroll
+    for (int o = kWarp / 2; o > 0; o /= 2)
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], o);
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int s = warp + i * kEpiWarps;
+      if (lane == 0 && s < rows) p.out[m0 + s] = 1.0f / (1.0f + expf(-(acc[i] + bl)));
+    }
   }
   if (p.err) {
     if (oob) atomicOr(reinterpret_cast<unsigned int*>(p.err), DLRM_ERRBIT_INDEX_OOB);
