@@ -321,7 +321,7 @@ __device__ void epilogue(const FusedTcParams& p, uint32_t tmem, unsigned char* c
   for (int c = tid; c < p.bias_floats / 4; c += kEpi) cp_async16(bias_s + 4 * c, p.bias + 4 * c, 16);
   for (int c = tid; c < p.k_last / 4; c += kEpi) cp_async16(wlast_s + 4 * c, p.wlast + 4 * c, 16);
   {
-    const int n_bag = kTcTile * k;
+    const int n_bag = p.bag == 1 ? kTcTile * k : 0;
     const int n_dn = kTcTile * p.n_dense;
     const int n_all = n_bag > n_dn ? n_bag : n_dn;
     for (int e0 = 0; e0 < n_all; e0 += 2 * kEpi) {
@@ -369,13 +369,44 @@ __device__ void epilogue(const FusedTcParams& p, uint32_t tmem, unsigned char* c
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   epi_sync();
   if (tid == 0) mbar_arrive(smem_addr(act_ready));
-  for (int e = tid; e < kTcTile * k * d4; e += kEpi) {
-    const int sk = e / d4;                      // sample * k + table
-    const int c4 = e - sk * d4;
-    const float* table = p.tabs.ptr[sk % k];
-    const int row = rowidx_s[sk];
-    cp_async16(zs + sk * p.ldz + 4 * c4, row >= 0 ? table + static_cast<int64_t>(row) * d + 4 * c4 : table,
-               row >= 0 ? 16 : 0);
+  if (p.bag == 1) {
+    for (int e = tid; e < kTcTile * k * d4; e += kEpi) {
+      const int sk = e / d4;                    // sample * k + table
+      const int c4 = e - sk * d4;
+      const float* table = p.tabs.ptr[sk % k];
+      const int row = rowidx_s[sk];
+      cp_async16(zs + sk * p.ldz + 4 * c4,
+                 row >= 0 ? table + static_cast<int64_t>(row) * d + 4 * c4 : table, row >= 0 ? 16 : 0);
+    }
+  } else {
+    // bags of p.bag rows at offsets b * bag: summed in registers (an
+    // out-of-range row adds nothing and raises the flag)
+    for (int e = tid; e < kTcTile * k * d4; e += kEpi) {
+      const int sk = e / d4;
+      const int c4 = e - sk * d4;
+      const int s = sk / k, t = sk - s * k;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (s < rows) {
+        const int64_t b = m0 + s;
+        const int64_t start = __ldg(p.offsets + static_cast<int64_t>(t) * p.batch + b);
+        if (start != b * p.bag) {
+          bad_off = true;
+        } else {
+          const int64_t* idx = p.indices + static_cast<int64_t>(t) * p.batch * p.bag + start;
+          const float4* table = reinterpret_cast<const float4*>(p.tabs.ptr[t]);
+          for (int l = 0; l < p.bag; ++l) {
+            const int64_t row = __ldg(idx + l);
+            if (row >= 0 && row < p.tabs.rows[t]) {
+              const float4 u = __ldg(table + row * d4 + c4);
+              v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w;
+            } else {
+              oob = true;
+            }
+          }
+        }
+      }
+      *reinterpret_cast<float4*>(zs + sk * p.ldz + 4 * c4) = v;
+    }
   }
   asm volatile("cp.async.commit_group;\n" ::: "memory");
   // biases, last-layer weights and bag rows land while layer 0 runs
@@ -618,7 +649,7 @@ bool fused_tc_plan(int n_dense, int k_tables, int d, int bag, const std::vector<
   const int n_bot = static_cast<int>(ln_bot.size()) - 1;
   const int n_top = static_cast<int>(ln_top.size()) - 1;
   const int n_gemm = n_bot + n_top - 1;
-  if (bag != 1 || d % 4 != 0 || n_bot < 1 || n_top < 2 || ln_top.back() != 1 ||
+  if (bag < 1 || d % 4 != 0 || n_bot < 1 || n_top < 2 || ln_top.back() != 1 ||
       n_gemm > kTcMaxGemm)
     return false;
   for (int t = 0; t < k_tables; ++t)
@@ -628,6 +659,7 @@ bool fused_tc_plan(int n_dense, int k_tables, int d, int bag, const std::vector<
   p.n_dense = n_dense;
   p.k_tables = k_tables;
   p.d = d;
+  p.bag = bag;
   p.n_bot = n_bot;
   p.n_top = n_top;
   p.n_gemm = n_gemm;

@@ -21,7 +21,7 @@ struct TcGemm {
 };
 
 struct FusedTcParams {
-  int batch, n_dense, k_tables, d, n_bot, n_top;
+  int batch, n_dense, k_tables, d, bag, n_bot, n_top;
   int n_gemm;          // n_bot + n_top - 1 (the last top layer is an fp32 dot)
   int bf16;            // operand type: 0 tf32, 1 bf16
   int stages;          // weight ring depth
@@ -56,7 +56,7 @@ struct FusedTcPlan {
 
 // Builds the plan for math DLRM_MATH_TF32 or DLRM_MATH_BF16 from host copies
 // of the (out, in) weights and biases; false when the model does not fit
-// (bag size other than 1, tables not 16-byte aligned, shared memory).
+// (tables not 16-byte aligned, shared memory, tensor memory).
 bool fused_tc_plan(int n_dense, int k_tables, int d, int bag, const std::vector<int>& ln_bot,
                    const std::vector<int>& ln_top, const std::vector<std::vector<float>>& w,
                    const std::vector<std::vector<float>>& b, const GatherTables& tabs, int math,

@@ -111,11 +111,11 @@ def _model(cfg, inp, mode, path):
                                   "sweep_b1_k1", "sweep_b300_k16"])
 def test_forward_tensor_core_matches_oracle(name, path, mode):
     """Both plans of the tensor-core modes against the oracle. The fused plan
-    takes bag size 1 and models whose tile fits shared memory; TF32X3 is
-    layer-wise only. Other requests must be refused with UNSUPPORTED."""
+    takes models whose tile fits shared memory; TF32X3 is layer-wise only.
+    Other requests must be refused with UNSUPPORTED."""
     cfg = synth.get_config(name)
     inp = synth.make_inputs(cfg, seed=1234)
-    if path == dl.PATH_FUSED and (mode == dl.MATH_TF32X3 or cfg.bag_size != 1):
+    if path == dl.PATH_FUSED and mode == dl.MATH_TF32X3:
         with pytest.raises(dl.DlrmError) as ei:
             _model(cfg, inp, mode, path)
         assert ei.value.status == dl.ERR_UNSUPPORTED
@@ -151,6 +151,32 @@ def test_fused_tensor_core_is_auto_choice_and_flags_bad_indices(mode):
     inp2["indices"] = idx
     ref = oracle.forward(inp2, allow_oob=True)
     np.testing.assert_allclose(out.cpu().numpy(), ref, rtol=2e-2, atol=0)
+    model.close()
+
+
+@pytest.mark.parametrize("mode", MODES, ids=MODE_IDS)
+def test_fused_tensor_core_bags_of_two_flag_bad_index_and_offsets(mode):
+    """Bags of two rows (the 64-sample model): an index past its table adds
+    nothing to its bag and raises INDEX_OOB; an offset off the uniform stride
+    zeroes that bag and raises the offsets flag."""
+    cfg = synth.get_config("tiny_b64_k3")
+    assert cfg.bag_size == 2
+    inp = synth.make_inputs(cfg, seed=21)
+    model = _model(cfg, inp, mode, dl.PATH_FUSED)
+    idx = inp["indices"].copy()
+    idx[0, 2 * 5 + 1] = -3                 # second row of sample 5's bag in table 0
+    out = model.forward(cu(inp["dense"]), cu(idx), cu(inp["offsets"]))
+    assert model.error() == dl.ERR_INDEX_OOB
+    inp2 = dict(inp)
+    inp2["indices"] = idx
+    np.testing.assert_allclose(out.cpu().numpy(), oracle.forward(inp2, allow_oob=True),
+                               rtol=2e-2, atol=0)
+    off = inp["offsets"].copy()
+    off[1, 9] = 2 * 9 + 1
+    out = model.forward(cu(inp["dense"]), cu(inp["indices"]), cu(off)).cpu().numpy()
+    assert model.error() == dl.ERR_UNSUPPORTED
+    keep = np.arange(cfg.batch) != 9
+    np.testing.assert_allclose(out[keep], oracle.forward(inp)[keep], rtol=2e-2, atol=0)
     model.close()
 
 
