@@ -48,12 +48,13 @@ def _bind(lib):
     lib.oracle_pair_enumerate.argtypes = [i32, vp, vp]
     lib.oracle_pair_enumerate.restype = None
     lib.oracle_embedding_bag_sum.argtypes = [i32, vp, vp, i32, vp, i64, vp, i64, vp, i32]
+    lib.oracle_embedding_bag.argtypes = [i32, vp, vp, i32, vp, i64, vp, i64, i32, vp, vp, i32]
     lib.oracle_linear.argtypes = [i64, i32, i32, vp, vp, vp, i32, vp, i32]
     lib.oracle_interaction.argtypes = [i64, i32, i32, vp, vp, vp, i32]
     lib.oracle_forward.argtypes = [i64, i32, vp, vp, vp, i32, vp, vp, i32, vp, i64, vp,
                                    i32, vp, vp, vp, vp, vp, i64, vp, i32]
-    for f in (lib.oracle_embedding_bag_sum, lib.oracle_linear, lib.oracle_interaction,
-              lib.oracle_forward):
+    for f in (lib.oracle_embedding_bag_sum, lib.oracle_embedding_bag, lib.oracle_linear,
+              lib.oracle_interaction, lib.oracle_forward):
         f.restype = ctypes.c_int
     return lib
 
@@ -132,6 +133,38 @@ def embedding_bag_sum(tables, indices, offsets, allow_oob: bool = False,
                                       _threads(threads))
     rc = _check(rc, "embedding_bag_sum", allow_oob)
     return (out, rc) if return_status else out
+
+
+BAG_SUM, BAG_MEAN, BAG_MAX = 0, 1, 2
+BAG_FLAG_OOB, BAG_FLAG_OFFSETS = 1, 2
+
+
+def embedding_bag(tables, indices, offsets, mode: int = BAG_SUM,
+                  threads: Optional[int] = None, lib=None):
+    """Bags under a reduction mode over general offsets: ((B, K, D) float64, flags).
+
+    Bag b of table t is indices[t][offsets[t][b] : offsets[t][b+1]] (the last
+    bag ends at N = indices.shape[1]); mode BAG_SUM, BAG_MEAN or BAG_MAX. An
+    index out of range is left out of its bag (flag BAG_FLAG_OOB); mean divides
+    by the rows kept; a bag with no rows is zeros; bad bounds (begin < 0,
+    end > N, begin > end) give zeros and flag BAG_FLAG_OFFSETS.
+    """
+    lib = lib or load()
+    tables = [_f32(t) for t in tables]
+    indices, offsets = _i64(indices), _i64(offsets)
+    k = len(tables)
+    d = tables[0].shape[1]
+    b = offsets.shape[1]
+    rows = np.array([t.shape[0] for t in tables], np.int64)
+    out = np.zeros((b, k, d), np.float64)
+    flags = ctypes.c_int(0)
+    rc = lib.oracle_embedding_bag(k, _ptr_array(tables), rows.ctypes.data, d,
+                                  indices.ctypes.data, indices.shape[1], offsets.ctypes.data, b,
+                                  int(mode), out.ctypes.data, ctypes.byref(flags),
+                                  _threads(threads))
+    if rc != OK:
+        raise OracleError(rc, "embedding_bag")
+    return out, flags.value
 
 
 def linear(x, w, b=None, act: int = ACT_NONE, threads: Optional[int] = None, lib=None):

@@ -76,6 +76,40 @@ int bag_sum(const float* table, int64_t rows, int d, const int64_t* idx, int64_t
   return status;
 }
 
+// One (sample, table) bag under a reduction mode, over general offsets
+// ([P4] LessonsLearned "EmbeddingBag translator gap": output[b] =
+// reduce_op(weight[indices[offsets[b]:offsets[b+1]]]), reduce_op one of
+// sum / mean / max). Readings where the pages are silent: the last bag ends
+// at N; an index outside [0, rows) is left out of its bag (flag bit 1); mean
+// divides by the number of rows kept; a bag with no rows kept is zeros in
+// every mode; bounds with begin < 0, end > N or begin > end make the bag
+// zeros (flag bit 2). Returns the flag bits.
+enum { BAG_SUM = 0, BAG_MEAN = 1, BAG_MAX = 2 };
+enum { BAG_FLAG_OOB = 1, BAG_FLAG_OFFSETS = 2 };
+int bag_reduce(const float* table, int64_t rows, int d, const int64_t* idx, int64_t n_idx,
+               const int64_t* off, int64_t batch, int64_t b, int mode, double* out) {
+  for (int c = 0; c < d; ++c) out[c] = 0.0;
+  const int64_t begin = off[b];
+  const int64_t end = (b + 1 < batch) ? off[b + 1] : n_idx;
+  if (begin < 0 || end > n_idx || begin > end) return BAG_FLAG_OFFSETS;
+  int flags = 0;
+  int64_t kept = 0;
+  for (int64_t n = begin; n < end; ++n) {
+    const int64_t r = idx[n];
+    if (r < 0 || r >= rows) { flags |= BAG_FLAG_OOB; continue; }
+    const float* row = table + r * d;
+    for (int c = 0; c < d; ++c) {
+      const double v = static_cast<double>(row[c]);
+      if (mode == BAG_MAX) out[c] = (kept == 0 || v > out[c]) ? v : out[c];
+      else out[c] += v;
+    }
+    ++kept;
+  }
+  if (mode == BAG_MEAN && kept > 0)
+    for (int c = 0; c < d; ++c) out[c] /= static_cast<double>(kept);
+  return flags;
+}
+
 // Strict lower triangle of the Gram matrix of the F feature vectors, i-major
 // then j ([P4] dlrm_megakernel.rs step 4: "for i in 0..n_feat for j in 0..i",
 // Vec[0] = x, Vec[k+1] = table k). z must hold F(F-1)/2 values.
@@ -107,7 +141,7 @@ void parallel_for(int64_t n, int threads, Fn fn) {
 
 extern "C" {
 
-int oracle_version() { return 1; }
+int oracle_version() { return 2; }
 
 // Pair index p -> (i, j), i > j >= 0 ([P1] PairwiseDotLowerTriStackedKernel:
 // "(1+sqrt(1+8p))/2"; the floor and j = p - i(i-1)/2 are the reading).
@@ -144,6 +178,27 @@ int oracle_embedding_bag_sum(int k_tables, const float* const* tables, const int
     }
   });
   for (int64_t b = 0; b < batch; ++b) if (status[b] != ORACLE_OK) return status[b];
+  return ORACLE_OK;
+}
+
+// Multi-table EmbeddingBag with a reduction mode (0 sum, 1 mean, 2 max) over
+// general offsets: out (B, K, D) double; *flags receives the OR of the bags'
+// flag bits (1: an index out of range, 2: bad bag bounds).
+int oracle_embedding_bag(int k_tables, const float* const* tables, const int64_t* rows, int d,
+                         const int64_t* indices, int64_t n_idx, const int64_t* offsets,
+                         int64_t batch, int mode, double* out, int* flags, int threads) {
+  if (k_tables <= 0 || d <= 0 || batch < 0 || n_idx < 0 || mode < BAG_SUM || mode > BAG_MAX)
+    return ORACLE_INVALID;
+  std::vector<int> f(batch, 0);
+  parallel_for(batch, threads, [&](int64_t b) {
+    for (int t = 0; t < k_tables; ++t)
+      f[b] |= bag_reduce(tables[t], rows[t], d, indices + (int64_t)t * n_idx, n_idx,
+                         offsets + (int64_t)t * batch, batch, b, mode,
+                         out + (b * k_tables + t) * d);
+  });
+  int all = 0;
+  for (int64_t b = 0; b < batch; ++b) all |= f[b];
+  if (flags) *flags = all;
   return ORACLE_OK;
 }
 

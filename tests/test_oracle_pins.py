@@ -139,6 +139,123 @@ def test_bag_sum_matches_torch_embedding_bag(oracle_lib):
         np.testing.assert_allclose(e[:, t, :], ref, rtol=1e-12, atol=1e-15)
 
 
+# ---------------------------------------------------------------- bag modes
+
+MODES = [("sum", oracle.BAG_SUM), ("mean", oracle.BAG_MEAN), ("max", oracle.BAG_MAX)]
+
+
+def _variable_bags(rng, k, b, v, max_len, empty_every=7):
+    """(K, N) indices and (K, B) offsets of bags of random lengths in [0, max_len],
+    with every `empty_every`-th bag empty. All tables share N, so the last bag
+    of a table with fewer indices runs on to N (include_last_offset = false)."""
+    lens = rng.integers(1, max_len + 1, size=(k, b))
+    lens[:, ::empty_every] = 0
+    n = int(lens.sum(axis=1).max())
+    idx = rng.integers(0, v, size=(k, n)).astype(np.int64)
+    off = np.zeros((k, b), np.int64)
+    for t in range(k):
+        off[t, 1:] = np.cumsum(lens[t])[:-1]
+    return idx, off, lens
+
+
+def test_bag_modes_hand_fixture(oracle_lib):
+    """Sum, mean and max over general offsets, worked by hand (tests/golden)."""
+    g = _golden("hand_bag_modes.json")
+    table = _arr(g["table"], np.float32)
+    for case in g["cases"]:
+        idx = _arr([case["indices"]], np.int64)
+        off = _arr([case["offsets"]], np.int64)
+        for name, mode in MODES:
+            e, flags = oracle.embedding_bag([table], idx, off, mode, lib=oracle_lib)
+            np.testing.assert_array_equal(e[:, 0, :], _arr(case[name], np.float64))
+            assert flags == case["flags"], (name, flags)
+
+
+@pytest.mark.parametrize("name,mode", MODES)
+def test_bag_modes_match_torch_embedding_bag(oracle_lib, name, mode):
+    """Library cross-check: torch.nn.functional.embedding_bag(mode=...) in float64 on
+    bags of random lengths 0..9 over general offsets (the last bag runs to N)."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(41)
+    k, b, v, d = 3, 50, 300, 12
+    tables = [rng.uniform(-1, 1, (v, d)).astype(np.float32) for _ in range(k)]
+    idx, off, _ = _variable_bags(rng, k, b, v, 9)
+    e, flags = oracle.embedding_bag(tables, idx, off, mode, lib=oracle_lib)
+    assert flags == 0
+    for t in range(k):
+        ref = torch.nn.functional.embedding_bag(
+            torch.from_numpy(idx[t]), torch.from_numpy(tables[t]).double(),
+            torch.from_numpy(off[t]), mode=name).numpy()
+        if mode == oracle.BAG_MAX:
+            np.testing.assert_array_equal(e[:, t, :], ref)
+        else:
+            np.testing.assert_allclose(e[:, t, :], ref, rtol=1e-13, atol=1e-15)
+
+
+def test_bag_modes_selection_matrix_brute_force(oracle_lib):
+    """Brute force on tiny inputs in matrix form: with S[b, n] = 1 when index n lies
+    in bag b and G = table[indices], sum = S G, mean = S G / |bag|, max = the column
+    max of G over the rows S selects; empty bags are zeros."""
+    rng = np.random.default_rng(5)
+    v, d, b = 40, 6, 9
+    table = rng.uniform(-2, 2, (v, d)).astype(np.float32)
+    idx, off, _ = _variable_bags(rng, 1, b, v, 6, empty_every=4)
+    n = idx.shape[1]
+    ends = np.append(off[0, 1:], n)
+    sel = np.zeros((b, n))
+    for bb in range(b):
+        sel[bb, off[0, bb]:ends[bb]] = 1.0
+    g = table[idx[0]].astype(np.float64)
+    count = sel.sum(axis=1)
+    want_sum = sel @ g
+    want_mean = np.where(count[:, None] > 0, want_sum / np.maximum(count, 1)[:, None], 0.0)
+    masked = np.where(sel[:, :, None] > 0, g[None, :, :], -np.inf)
+    want_max = np.where(count[:, None] > 0, masked.max(axis=1), 0.0)
+    for (name, mode), want in zip(MODES, (want_sum, want_mean, want_max)):
+        e, _ = oracle.embedding_bag([table], idx, off, mode, lib=oracle_lib)
+        if mode == oracle.BAG_MAX:
+            np.testing.assert_array_equal(e[:, 0, :], want)
+        else:
+            np.testing.assert_allclose(e[:, 0, :], want, rtol=1e-13, atol=1e-14)
+
+
+@pytest.mark.parametrize("name,mode", MODES)
+def test_bag_modes_permutation_invariant(oracle_lib, name, mode):
+    """Permuting indices inside each bag leaves every mode unchanged: max exactly,
+    sum and mean within 1 ulp once rounded to fp32."""
+    rng = np.random.default_rng(17)
+    k, b, v, d = 2, 40, 500, 8
+    tables = [rng.uniform(-1, 1, (v, d)).astype(np.float32) for _ in range(k)]
+    idx, off, lens = _variable_bags(rng, k, b, v, 12)
+    base, _ = oracle.embedding_bag(tables, idx, off, mode, lib=oracle_lib)
+    perm = idx.copy()
+    for t in range(k):
+        for bb in range(b):
+            lo = off[t, bb]
+            hi = off[t, bb + 1] if bb + 1 < b else idx.shape[1]
+            perm[t, lo:hi] = perm[t, lo:hi][rng.permutation(hi - lo)]
+    assert not np.array_equal(perm, idx)
+    got, _ = oracle.embedding_bag(tables, perm, off, mode, lib=oracle_lib)
+    if mode == oracle.BAG_MAX:
+        np.testing.assert_array_equal(got, base)
+    else:
+        b32, g32 = base.astype(np.float32), got.astype(np.float32)
+        ulp = np.spacing(np.maximum(np.abs(b32), np.abs(g32)))
+        assert np.all(np.abs(g32 - b32) <= ulp)
+
+
+def test_bag_mean_of_one_repeated_row_is_that_row(oracle_lib):
+    """Closed form: the mean of L copies of row r is row r, exactly."""
+    rng = np.random.default_rng(2)
+    table = rng.uniform(-1, 1, (30, 5)).astype(np.float32)
+    rows = np.array([3, 17, 0, 29])
+    lens = np.array([1, 7, 20, 3])
+    idx = np.repeat(rows, lens)[None, :].astype(np.int64)
+    off = np.concatenate([[0], np.cumsum(lens)[:-1]])[None, :].astype(np.int64)
+    e, _ = oracle.embedding_bag([table], idx, off, oracle.BAG_MEAN, lib=oracle_lib)
+    np.testing.assert_array_equal(e[:, 0, :], table[rows].astype(np.float64))
+
+
 # ---------------------------------------------------------------- interaction
 
 @pytest.mark.parametrize("k,d", [(1, 8), (3, 16), (8, 5), (32, 64), (26, 128)])
