@@ -22,7 +22,9 @@ Extra objects on the line:
              roofline fraction
   gather_b65536_k26_zipf  the standalone multi-table gather on the 13.3 GB
              26-table workload (bags of 20, Zipf(1.05)) plus a uniform-index
-             control, algorithmic GB/s against measured HBM GB/s
+             control, algorithmic GB/s against measured HBM GB/s; under
+             "general_bags" the same tables through embedding_bag_multi with
+             bags of random lengths 0..40 over general offsets, sum / mean / max
   cpu_baseline  the CPU oracle (fp64, all host cores) on a bounded sample
 
 --impl reference times the CPU oracle as the reference arm (there is no
@@ -328,6 +330,51 @@ def gather_measure(torch, dl, synth, pk, tables, steps=10):
                      "+ output; Zipf hot rows are served partly from L2", **res)
 
 
+def bag_modes_measure(torch, dl, synth, pk, tables, steps=10):
+    """embedding_bag_multi on the 26 x 1M x 128 tables: bags of random lengths 0..40
+    (mean 20, empty bags included) over general offsets, sum / mean / max, Zipf and
+    uniform indices."""
+    cfg = synth.get_config("b65536_k26_zipf")
+    out = torch.empty((cfg.batch, cfg.n_tables, cfg.emb_dim), device="cuda")
+    modes = {"sum": dl.BAG_SUM, "mean": dl.BAG_MEAN, "max": dl.BAG_MAX}
+    res = {}
+    for dist in ("zipf", "uniform"):
+        c = cfg if dist == "zipf" else synth.DlrmConfig(
+            cfg.name, cfg.batch, cfg.ln_bot, cfg.rows, cfg.emb_dim, cfg.bag_size, cfg.ln_top)
+        idx_h, off_h, lens = synth.make_variable_bags(c, 1234, 40)
+        n_idx = idx_h.shape[1]
+        rows_read = int(lens.sum())
+        # algorithmic bytes: rows read + all indices + offsets + the (B, K, D) output
+        byts = (rows_read * cfg.emb_dim * 4 + cfg.n_tables * n_idx * 8
+                + cfg.n_tables * cfg.batch * 8 + cfg.batch * cfg.n_tables * cfg.emb_dim * 4)
+        idx, off = torch.from_numpy(idx_h).cuda(), torch.from_numpy(off_h).cuda()
+        del idx_h, off_h
+        s = torch.cuda.current_stream()
+        per = {}
+        for name, mode in modes.items():
+            for _ in range(3):
+                dl.embedding_bag_multi(tables, idx, off, out, mode, stream=s)
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(steps)]
+            torch.cuda.synchronize()
+            for a, b in ev:
+                a.record(s)
+                dl.embedding_bag_multi(tables, idx, off, out, mode, stream=s)
+                b.record(s)
+            torch.cuda.synchronize()
+            ms = sum(a.elapsed_time(b) for a, b in ev) / steps
+            gbs = byts / (ms * 1e-3) / 1e9
+            per[name] = dict(ms_per_launch=ms, algorithmic_gbs=gbs,
+                             frac_of_measured_hbm=gbs / pk["hbm_gbs"])
+        res[dist] = dict(bytes_per_launch=byts, mean_bag=rows_read / (cfg.batch * cfg.n_tables),
+                         **per)
+        del idx, off
+    del out
+    torch.cuda.empty_cache()
+    return dict(workload="26 tables x 1M x 128 fp32, batch 65536, bag lengths uniform on "
+                         "0..40 (general offsets)", launches_timed=steps, **res)
+
+
 def run_ours(args, rank, world, local_rank):
     import numpy as np
     import torch
@@ -614,6 +661,7 @@ def run_ours(args, rank, world, local_rank):
             c4 = synth.get_config("b65536_k26_zipf")
             tabs = device_tables(torch, synth, c4, args.seed)
             gather = gather_measure(torch, dl, synth, pk, tabs)
+            gather["general_bags"] = bag_modes_measure(torch, dl, synth, pk, tabs)
             if configs is not None:
                 configs[c4.name] = forward_point(c4, tabs, 5, 3)
             del tabs

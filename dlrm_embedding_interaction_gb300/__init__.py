@@ -28,8 +28,8 @@ EXPORTS = ("dlrm_version", "dlrm_status_string", "dlrm_create", "dlrm_forward",
            "dlrm_forward_host", "dlrm_get_error", "dlrm_workspace_bytes", "dlrm_destroy",
            "dlrm_path", "dlrm_num_stages", "dlrm_stage_name", "dlrm_set_profiling", "dlrm_stage_times",
            "dlrm_forward_noalloc", "dlrm_set_phase_trace",
-           "embedding_bag_sum_multi", "pairwise_dot_lower_tri", "pairwise_pair_map",
-           "linear_bias_act")
+           "embedding_bag_sum_multi", "embedding_bag_multi", "pairwise_dot_lower_tri",
+           "pairwise_pair_map", "linear_bias_act")
 NOALLOC_SCRATCH_BYTES = 16 << 20
 TRACE_SLOTS = 40
 
@@ -72,6 +72,7 @@ def _bind(lib):
                                   i32, vp, vp], st),
         "dlrm_set_phase_trace": ([vp, vp, i64, ctypes.POINTER(i32)], st),
         "embedding_bag_sum_multi": ([vp, vp, i32, i32, vp, vp, i32, i32, vp, vp, vp], st),
+        "embedding_bag_multi": ([vp, vp, i32, i32, vp, i64, vp, i32, i32, vp, vp, vp], st),
         "pairwise_dot_lower_tri": ([vp, i32, vp, i32, i32, i32, vp, i32, i32, vp], st),
         "pairwise_pair_map": ([i32, vp, vp, vp], st),
         "linear_bias_act": ([vp, i32, vp, vp, vp, i32, i32, i32, i32, st, st, vp], st),
@@ -169,6 +170,44 @@ def embedding_bag_sum_multi(tables: Sequence, indices, offsets, out, bag_size: i
     _check(lib().embedding_bag_sum_multi(ptrs, rows, k, d, _ptr(indices), _ptr(offsets), b,
                                          bag_size, _ptr(out), _ptr(err_flag), _stream(stream)),
            "embedding_bag_sum_multi")
+
+
+BAG_SUM, BAG_MEAN, BAG_MAX = 0, 1, 2
+
+
+def embedding_bag_multi(tables: Sequence, indices, offsets, out, mode: int = BAG_SUM,
+                        err_flag=None, stream=None) -> None:
+    """out (B, K, D) = per-table bag reductions over general offsets.
+
+    indices (K, N) int64; offsets (K, B) int64 bag starts (the last bag runs
+    to N); mode BAG_SUM, BAG_MEAN or BAG_MAX.
+    """
+    import torch
+    k = len(tables)
+    if k == 0:
+        raise ValueError("need at least one table")
+    d = tables[0].shape[1]
+    for i, t in enumerate(tables):
+        _need(t, torch.float32, f"tables[{i}]")
+        if t.dim() != 2 or t.shape[1] != d or not t.is_contiguous():
+            raise ValueError(f"tables[{i}]: expected contiguous (rows, {d})")
+    _need(indices, torch.int64, "indices")
+    _need(offsets, torch.int64, "offsets")
+    _need(out, torch.float32, "out")
+    b = offsets.shape[1]
+    if (indices.dim() != 2 or indices.shape[0] != k or tuple(offsets.shape) != (k, b)
+            or tuple(out.shape) != (b, k, d)):
+        raise ValueError("shape mismatch among indices/offsets/out")
+    if not (indices.is_contiguous() and offsets.is_contiguous() and out.is_contiguous()):
+        raise ValueError("indices, offsets and out must be contiguous")
+    if err_flag is not None:
+        _need(err_flag, torch.int32, "err_flag")
+    ptrs = (ctypes.c_void_p * k)(*[t.data_ptr() for t in tables])
+    rows = (ctypes.c_int64 * k)(*[t.shape[0] for t in tables])
+    _check(lib().embedding_bag_multi(ptrs, rows, k, d, _ptr(indices), indices.shape[1],
+                                     _ptr(offsets), b, int(mode), _ptr(out), _ptr(err_flag),
+                                     _stream(stream)),
+           "embedding_bag_multi")
 
 
 def pairwise_dot_lower_tri(dense, emb, out, copy_dense: bool = True, stream=None) -> None:

@@ -649,6 +649,28 @@ dlrm_status_t embedding_bag_sum_multi(const float* const* tables, const int64_t*
                                          static_cast<cudaStream_t>(stream)));
 }
 
+dlrm_status_t embedding_bag_multi(const float* const* tables, const int64_t* rows, int32_t K,
+                                  int32_t D, const int64_t* indices, int64_t n_idx,
+                                  const int64_t* offsets, int32_t B, int32_t mode, float* out,
+                                  int32_t* err_flag, void* stream) {
+  if (K < 1 || D < 1 || B < 0 || n_idx < 0) return DLRM_ERR_INVALID_ARG;
+  if (mode != DLRM_BAG_SUM && mode != DLRM_BAG_MEAN && mode != DLRM_BAG_MAX)
+    return DLRM_ERR_INVALID_ARG;
+  if (K > DLRM_MAX_TABLES) return DLRM_ERR_UNSUPPORTED;
+  if (!tables || !rows) return DLRM_ERR_INVALID_ARG;
+  if (B == 0) return DLRM_OK;
+  if ((n_idx > 0 && !indices) || !offsets || !out) return DLRM_ERR_INVALID_ARG;
+  dlrm::GatherTables tabs{};
+  for (int t = 0; t < K; ++t) {
+    if (!tables[t] || rows[t] < 0) return DLRM_ERR_INVALID_ARG;
+    tabs.ptr[t] = tables[t];
+    tabs.rows[t] = rows[t];
+  }
+  return cuda_status(dlrm::launch_gather_general(tabs, K, D, indices, n_idx, offsets, B, mode,
+                                                 out, err_flag,
+                                                 static_cast<cudaStream_t>(stream)));
+}
+
 dlrm_status_t pairwise_dot_lower_tri(const float* dense, int32_t ld_dense, const float* emb,
                                      int32_t B, int32_t K, int32_t D, float* out,
                                      int32_t ld_out, int32_t copy_dense, void* stream) {

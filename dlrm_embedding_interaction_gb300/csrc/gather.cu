@@ -23,6 +23,14 @@
 // zeros and sets DLRM_ERRBIT_INDEX_OOB. The bag start must equal b * L (the
 // uniform stride), which also keeps every index read inside (K, B*L); a bag
 // whose offset differs is written as zeros with DLRM_ERRBIT_OFFSETS.
+//
+// The general form (embedding_bag_multi) is the runtime segment reduction the
+// same LessonsLearned entry names as the follow-up: bag b of table t spans
+// indices[t][offsets[t][b] : offsets[t][b+1]] (the last bag runs to N), with
+// reduce_op sum, mean or max. The same lane groups walk bags of any length;
+// an out-of-range index is left out of its bag, mean divides by the rows
+// kept, a bag with no rows is zeros, and bounds outside [0, N] or reversed
+// give zeros with DLRM_ERRBIT_OFFSETS.
 #include "common.cuh"
 
 namespace dlrm {
@@ -39,14 +47,19 @@ __device__ __forceinline__ void add4(float4& a, const float4& v) {
   a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
 }
 
+__device__ __forceinline__ void max4(float4& a, const float4& v) {
+  a.x = fmaxf(a.x, v.x); a.y = fmaxf(a.y, v.y); a.z = fmaxf(a.z, v.z); a.w = fmaxf(a.w, v.w);
+}
+
 // Vector path: D % 4 == 0, tables and out 16-byte aligned.
 // TPB lanes per bag (power of two <= 32); each lane owns CHUNKS float4 columns
-// col4 = lane + c * TPB (< D/4).
-template <int TPB, int CHUNKS>
+// col4 = lane + c * TPB (< D/4). GENERAL: bag bounds from consecutive offsets
+// (else the uniform stride L); MODE: DLRM_BAG_SUM, _MEAN or _MAX.
+template <int TPB, int CHUNKS, int MODE, bool GENERAL>
 __global__ void __launch_bounds__(kGatherThreads)
 gather_vec_kernel(const __grid_constant__ GatherTables tabs, int k_tables, int d4,
                   const int64_t* __restrict__ indices, const int64_t* __restrict__ offsets,
-                  int batch, int bag, float* __restrict__ out, int32_t* err) {
+                  int batch, int bag, int64_t n_idx, float* __restrict__ out, int32_t* err) {
   const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t bag_id = gtid / TPB;
   const int lane = threadIdx.x & (TPB - 1);
@@ -57,24 +70,36 @@ gather_vec_kernel(const __grid_constant__ GatherTables tabs, int k_tables, int d
   const int b = static_cast<int>(bag_id / k_tables);
   const int t = static_cast<int>(bag_id - static_cast<int64_t>(b) * k_tables);
 
-  float4* dst = reinterpret_cast<float4*>(out) + bag_id * d4;
+  const float init = MODE == DLRM_BAG_MAX ? -INFINITY : 0.f;
   float4 acc[CHUNKS];
 #pragma unroll
-  for (int c = 0; c < CHUNKS; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int c = 0; c < CHUNKS; ++c) acc[c] = make_float4(init, init, init, init);
 
-  const int64_t n_idx = static_cast<int64_t>(batch) * bag;
-  const int64_t start = offsets[static_cast<int64_t>(t) * batch + b];
-  if (start != static_cast<int64_t>(b) * bag) {
+  const int64_t* offs = offsets + static_cast<int64_t>(t) * batch;
+  const int64_t start = offs[b];
+  int len = bag;
+  bool good;
+  if (GENERAL) {
+    const int64_t end = (b + 1 < batch) ? offs[b + 1] : n_idx;
+    good = start >= 0 && end <= n_idx && start <= end && end - start <= INT32_MAX;
+    len = static_cast<int>(end - start);
+  } else {
+    good = start == static_cast<int64_t>(b) * bag;
+  }
+  int kept = 0;
+  if (!good) {
     if (lane == 0) flag_error(err, DLRM_ERRBIT_OFFSETS);
   } else {
     const int64_t* idx = indices + static_cast<int64_t>(t) * n_idx + start;
     const float4* table = reinterpret_cast<const float4*>(tabs.ptr[t]);
     const int64_t rows = tabs.rows[t];
     bool oob = false;
-    for (int l0 = 0; l0 < bag; l0 += TPB) {
-      const int cnt = min(TPB, bag - l0);
+    for (int l0 = 0; l0 < len; l0 += TPB) {
+      const int cnt = min(TPB, len - l0);
       const int64_t mine = (lane < cnt) ? __ldg(idx + l0 + lane) : 0;
       for (int u0 = 0; u0 < cnt; u0 += kUnroll) {
+        // a row left out (past the bag or out of range) loads the identity of
+        // the reduction: 0 for sums, -inf for max
         float4 v[kUnroll][CHUNKS];
 #pragma unroll
         for (int q = 0; q < kUnroll; ++q) {
@@ -82,34 +107,50 @@ gather_vec_kernel(const __grid_constant__ GatherTables tabs, int k_tables, int d
           const bool live = (u0 + q) < cnt;
           const bool ok = live && r >= 0 && r < rows;
           oob |= live && !ok;
+          if (MODE != DLRM_BAG_SUM) kept += ok ? 1 : 0;
 #pragma unroll
           for (int c = 0; c < CHUNKS; ++c) {
             const int col4 = lane + c * TPB;
             v[q][c] = (ok && col4 < d4) ? __ldg(table + r * d4 + col4)
-                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+                                        : make_float4(init, init, init, init);
           }
         }
 #pragma unroll
         for (int q = 0; q < kUnroll; ++q)
 #pragma unroll
-          for (int c = 0; c < CHUNKS; ++c) add4(acc[c], v[q][c]);
+          for (int c = 0; c < CHUNKS; ++c) {
+            if (MODE == DLRM_BAG_MAX) max4(acc[c], v[q][c]);
+            else add4(acc[c], v[q][c]);
+          }
       }
     }
     if (oob && lane == 0) flag_error(err, DLRM_ERRBIT_INDEX_OOB);
   }
+  // no rows kept: zeros in every mode (a sum of none is already zero); mean
+  // divides by the rows kept
+  float4* dst = reinterpret_cast<float4*>(out) + bag_id * d4;
 #pragma unroll
   for (int c = 0; c < CHUNKS; ++c) {
     const int col4 = lane + c * TPB;
-    if (col4 < d4) dst[col4] = acc[c];
+    if (col4 >= d4) continue;
+    float4 r = acc[c];
+    if (MODE != DLRM_BAG_SUM && kept == 0) {
+      r = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else if (MODE == DLRM_BAG_MEAN) {
+      r = make_float4(r.x / static_cast<float>(kept), r.y / static_cast<float>(kept),
+                      r.z / static_cast<float>(kept), r.w / static_cast<float>(kept));
+    }
+    dst[col4] = r;
   }
 }
 
 // Scalar path for any D and alignment: TPB = 32 lanes per bag, lane owns
 // columns lane, lane + 32, ...; indices re-read per column from L1.
+template <int MODE, bool GENERAL>
 __global__ void __launch_bounds__(kGatherThreads)
 gather_scalar_kernel(const __grid_constant__ GatherTables tabs, int k_tables, int d,
                      const int64_t* __restrict__ indices, const int64_t* __restrict__ offsets,
-                     int batch, int bag, float* __restrict__ out, int32_t* err) {
+                     int batch, int bag, int64_t n_idx, float* __restrict__ out, int32_t* err) {
   const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t bag_id = gtid / kWarp;
   const int lane = threadIdx.x & (kWarp - 1);
@@ -117,9 +158,18 @@ gather_scalar_kernel(const __grid_constant__ GatherTables tabs, int k_tables, in
   const int b = static_cast<int>(bag_id / k_tables);
   const int t = static_cast<int>(bag_id - static_cast<int64_t>(b) * k_tables);
   float* dst = out + bag_id * d;
-  const int64_t n_idx = static_cast<int64_t>(batch) * bag;
-  const int64_t start = offsets[static_cast<int64_t>(t) * batch + b];
-  if (start != static_cast<int64_t>(b) * bag) {
+  const int64_t* offs = offsets + static_cast<int64_t>(t) * batch;
+  const int64_t start = offs[b];
+  int len = bag;
+  bool good;
+  if (GENERAL) {
+    const int64_t end = (b + 1 < batch) ? offs[b + 1] : n_idx;
+    good = start >= 0 && end <= n_idx && start <= end && end - start <= INT32_MAX;
+    len = static_cast<int>(end - start);
+  } else {
+    good = start == static_cast<int64_t>(b) * bag;
+  }
+  if (!good) {
     if (lane == 0) flag_error(err, DLRM_ERRBIT_OFFSETS);
     for (int c = lane; c < d; c += kWarp) dst[c] = 0.f;
     return;
@@ -129,27 +179,66 @@ gather_scalar_kernel(const __grid_constant__ GatherTables tabs, int k_tables, in
   const int64_t rows = tabs.rows[t];
   bool oob = false;
   for (int c = lane; c < d; c += kWarp) {
-    float acc = 0.f;
-    for (int l = 0; l < bag; ++l) {
+    float acc = MODE == DLRM_BAG_MAX ? -INFINITY : 0.f;
+    int kept = 0;
+    for (int l = 0; l < len; ++l) {
       const int64_t r = __ldg(idx + l);
-      if (r >= 0 && r < rows) acc += __ldg(table + r * d + c);
-      else oob = true;
+      if (r >= 0 && r < rows) {
+        const float v = __ldg(table + r * d + c);
+        acc = MODE == DLRM_BAG_MAX ? fmaxf(acc, v) : acc + v;
+        ++kept;
+      } else {
+        oob = true;
+      }
     }
+    if (kept == 0) acc = 0.f;
+    else if (MODE == DLRM_BAG_MEAN) acc = acc / static_cast<float>(kept);
     dst[c] = acc;
   }
   if (d == 0) return;
   if (__any_sync(0xffffffffu, oob) && lane == 0) flag_error(err, DLRM_ERRBIT_INDEX_OOB);
 }
 
-template <int TPB, int CHUNKS>
+template <int TPB, int CHUNKS, int MODE, bool GENERAL>
 cudaError_t launch_vec(const GatherTables& tabs, int k, int d, const int64_t* indices,
-                       const int64_t* offsets, int b, int l, float* out, int32_t* err,
-                       cudaStream_t stream) {
+                       const int64_t* offsets, int b, int l, int64_t n_idx, float* out,
+                       int32_t* err, cudaStream_t stream) {
   const int64_t bags = static_cast<int64_t>(b) * k;
   const int64_t per_block = kGatherThreads / TPB;
   const int64_t grid = (bags + per_block - 1) / per_block;
-  gather_vec_kernel<TPB, CHUNKS><<<static_cast<unsigned>(grid), kGatherThreads, 0, stream>>>(
-      tabs, k, d / 4, indices, offsets, b, l, out, err);
+  gather_vec_kernel<TPB, CHUNKS, MODE, GENERAL>
+      <<<static_cast<unsigned>(grid), kGatherThreads, 0, stream>>>(tabs, k, d / 4, indices,
+                                                                   offsets, b, l, n_idx, out, err);
+  return cudaGetLastError();
+}
+
+// Lane-group width and columns per lane by D, vector or scalar path.
+template <int MODE, bool GENERAL>
+cudaError_t launch_any(const GatherTables& tabs, int k, int d, const int64_t* indices,
+                       const int64_t* offsets, int b, int l, int64_t n_idx, float* out,
+                       int32_t* err, cudaStream_t stream) {
+  bool vec = (d % 4 == 0) && (reinterpret_cast<uintptr_t>(out) % 16 == 0);
+  for (int t = 0; t < k && vec; ++t) vec = reinterpret_cast<uintptr_t>(tabs.ptr[t]) % 16 == 0;
+  const int d4 = d / 4;
+#define DLRM_VEC(TPB_, CH_) \
+  launch_vec<TPB_, CH_, MODE, GENERAL>(tabs, k, d, indices, offsets, b, l, n_idx, out, err, stream)
+  if (vec && d4 <= 256) {
+    if (d4 <= 1) return DLRM_VEC(1, 1);
+    if (d4 <= 2) return DLRM_VEC(2, 1);
+    if (d4 <= 4) return DLRM_VEC(4, 1);
+    if (d4 <= 8) return DLRM_VEC(8, 1);
+    if (d4 <= 16) return DLRM_VEC(16, 1);
+    if (d4 <= 32) return DLRM_VEC(32, 1);
+    if (d4 <= 64) return DLRM_VEC(32, 2);
+    if (d4 <= 128) return DLRM_VEC(32, 4);
+    return DLRM_VEC(32, 8);
+  }
+#undef DLRM_VEC
+  const int64_t bags = static_cast<int64_t>(b) * k;
+  const int64_t per_block = kGatherThreads / kWarp;
+  const int64_t grid = (bags + per_block - 1) / per_block;
+  gather_scalar_kernel<MODE, GENERAL><<<static_cast<unsigned>(grid), kGatherThreads, 0, stream>>>(
+      tabs, k, d, indices, offsets, b, l, n_idx, out, err);
   return cudaGetLastError();
 }
 
@@ -159,26 +248,27 @@ cudaError_t launch_gather(const GatherTables& tabs, int k, int d, const int64_t*
                           const int64_t* offsets, int b, int l, float* out, int /*unused*/,
                           int32_t* err, cudaStream_t stream) {
   if (b == 0) return cudaSuccess;
-  bool vec = (d % 4 == 0) && (reinterpret_cast<uintptr_t>(out) % 16 == 0);
-  for (int t = 0; t < k && vec; ++t) vec = reinterpret_cast<uintptr_t>(tabs.ptr[t]) % 16 == 0;
-  const int d4 = d / 4;
-  if (vec && d4 <= 256) {
-    if (d4 <= 1) return launch_vec<1, 1>(tabs, k, d, indices, offsets, b, l, out, err, stream);
-    if (d4 <= 2) return launch_vec<2, 1>(tabs, k, d, indices, offsets, b, l, out, err, stream);
-    if (d4 <= 4) return launch_vec<4, 1>(tabs, k, d, indices, offsets, b, l, out, err, stream);
-    if (d4 <= 8) return launch_vec<8, 1>(tabs, k, d, indices, offsets, b, l, out, err, stream);
-    if (d4 <= 16) return launch_vec<16, 1>(tabs, k, d, indices, offsets, b, l, out, err, stream);
-    if (d4 <= 32) return launch_vec<32, 1>(tabs, k, d, indices, offsets, b, l, out, err, stream);
-    if (d4 <= 64) return launch_vec<32, 2>(tabs, k, d, indices, offsets, b, l, out, err, stream);
-    if (d4 <= 128) return launch_vec<32, 4>(tabs, k, d, indices, offsets, b, l, out, err, stream);
-    return launch_vec<32, 8>(tabs, k, d, indices, offsets, b, l, out, err, stream);
+  return launch_any<DLRM_BAG_SUM, false>(tabs, k, d, indices, offsets, b, l,
+                                         static_cast<int64_t>(b) * l, out, err, stream);
+}
+
+cudaError_t launch_gather_general(const GatherTables& tabs, int k, int d, const int64_t* indices,
+                                  int64_t n_idx, const int64_t* offsets, int b, int mode,
+                                  float* out, int32_t* err, cudaStream_t stream) {
+  if (b == 0) return cudaSuccess;
+  switch (mode) {
+    case DLRM_BAG_SUM:
+      return launch_any<DLRM_BAG_SUM, true>(tabs, k, d, indices, offsets, b, 0, n_idx, out, err,
+                                            stream);
+    case DLRM_BAG_MEAN:
+      return launch_any<DLRM_BAG_MEAN, true>(tabs, k, d, indices, offsets, b, 0, n_idx, out, err,
+                                             stream);
+    case DLRM_BAG_MAX:
+      return launch_any<DLRM_BAG_MAX, true>(tabs, k, d, indices, offsets, b, 0, n_idx, out, err,
+                                            stream);
+    default:
+      return cudaErrorInvalidValue;
   }
-  const int64_t bags = static_cast<int64_t>(b) * k;
-  const int64_t per_block = kGatherThreads / kWarp;
-  const int64_t grid = (bags + per_block - 1) / per_block;
-  gather_scalar_kernel<<<static_cast<unsigned>(grid), kGatherThreads, 0, stream>>>(
-      tabs, k, d, indices, offsets, b, l, out, err);
-  return cudaGetLastError();
 }
 
 }  // namespace dlrm

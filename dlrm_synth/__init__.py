@@ -48,6 +48,7 @@ STREAM_TABLE = 1000
 STREAM_INDEX = 2000
 STREAM_BOT = 3000
 STREAM_TOP = 4000
+STREAM_BAG_LEN = 5000
 
 
 def build(force: bool = False) -> str:
@@ -271,6 +272,40 @@ def make_offsets(cfg: DlrmConfig, batch: Optional[int] = None) -> np.ndarray:
     b = cfg.batch if batch is None else batch
     row = np.arange(b, dtype=np.int64) * cfg.bag_size
     return np.broadcast_to(row, (cfg.n_tables, b)).copy()
+
+
+def make_variable_bags(cfg: DlrmConfig, seed: int, max_len: int, batch: Optional[int] = None,
+                       threads: Optional[int] = None):
+    """Bags of random lengths for the general-offsets EmbeddingBag.
+
+    Table 0's bag lengths are uniform on 0..max_len (stream STREAM_BAG_LEN);
+    every other table t takes the same lengths in its own order (sorted by keys
+    from stream STREAM_BAG_LEN + t), so all tables hold the same number N of
+    indices and no bag absorbs a remainder. Indices follow cfg.index_dist
+    (stream STREAM_INDEX + t). Returns ((K, N) int64 indices, (K, B) int64
+    offsets, (K, B) int64 lengths).
+    """
+    b = cfg.batch if batch is None else batch
+    k = cfg.n_tables
+    lens = np.empty((k, b), np.int64)
+    fill_index_uniform(lens[0], seed, STREAM_BAG_LEN, max_len + 1, threads)
+    keys = np.empty(b, np.int64)
+    for t in range(1, k):
+        fill_index_uniform(keys, seed, STREAM_BAG_LEN + t, 0xFFFFFFFF, threads)
+        lens[t] = lens[0][np.argsort(keys, kind="stable")]
+    n = int(lens[0].sum()) if b > 0 else 0
+    offsets = np.zeros((k, b), np.int64)
+    if b > 0:
+        offsets[:, 1:] = np.cumsum(lens, axis=1)[:, :-1]
+    indices = np.empty((k, n), np.int64)
+    for t in range(k):
+        if n == 0:
+            continue
+        if cfg.index_dist == "zipf":
+            fill_index_zipf(indices[t], seed, STREAM_INDEX + t, cfg.rows[t], cfg.zipf_s, threads)
+        else:
+            fill_index_uniform(indices[t], seed, STREAM_INDEX + t, cfg.rows[t], threads)
+    return indices, offsets, lens
 
 
 def make_inputs(cfg: DlrmConfig, seed: int = 1234, batch: Optional[int] = None,

@@ -70,6 +70,9 @@ typedef enum { DLRM_PATH_AUTO = 0, DLRM_PATH_LAYERWISE = 1, DLRM_PATH_FUSED = 2 
 /* Epilogue activation of linear_bias_act. */
 typedef enum { DLRM_ACT_NONE = 0, DLRM_ACT_RELU = 1, DLRM_ACT_SIGMOID = 2 } dlrm_act_t;
 
+/* Reduction of embedding_bag_multi over the rows of a bag. */
+typedef enum { DLRM_BAG_SUM = 0, DLRM_BAG_MEAN = 1, DLRM_BAG_MAX = 2 } dlrm_bag_mode_t;
+
 /* Device error word bits (1u << code) set by kernels. */
 #define DLRM_ERRBIT_INDEX_OOB (1u << DLRM_ERR_INDEX_OOB)
 #define DLRM_ERRBIT_OFFSETS   (1u << DLRM_ERR_UNSUPPORTED)
@@ -263,6 +266,31 @@ dlrm_status_t embedding_bag_sum_multi(const float* const* tables, const int64_t*
                                       int32_t K, int32_t D, const int64_t* indices,
                                       const int64_t* offsets, int32_t B, int32_t L, float* out,
                                       int32_t* err_flag, void* stream);
+
+/* Multi-table EmbeddingBag over general offsets, in one launch: the runtime
+ * segment reduction of [P4] LessonsLearned "EmbeddingBag translator gap",
+ *   out[b][t][:] = reduce_op(tables[t][indices[t][n]][:] for n in bag(t, b)),
+ *   bag(t, b) = [offsets[t][b], offsets[t][b+1])  (the last bag ends at N),
+ * reduce_op = sum, mean or max (mode).
+ *   tables   host array of K device pointers, table t is (rows[t], D) fp32
+ *            row-major; rows is a host array of K row counts
+ *   indices  (K, N) int64 table-major, N = n_idx >= 0 indices per table
+ *   offsets  (K, B) int64 bag starts (PyTorch include_last_offset = false)
+ *   out      (B, K, D) fp32
+ *   err_flag device int32 error word or NULL; bits DLRM_ERRBIT_INDEX_OOB (an
+ *            index outside [0, rows[t]) is left out of its bag) and
+ *            DLRM_ERRBIT_OFFSETS (a bag with begin < 0, end > N or
+ *            begin > end is written as zeros) are OR-ed in, never cleared.
+ * A bag with no rows kept is zeros in every mode; mean divides by the rows
+ * kept; sums run in index order in fp32; max is exact (fmaxf).
+ * Returns DLRM_ERR_INVALID_ARG for null pointers, K < 1, D < 1, B < 0,
+ * n_idx < 0 or an unknown mode; DLRM_ERR_UNSUPPORTED for K > DLRM_MAX_TABLES;
+ * DLRM_ERR_CUDA if the launch fails. B = 0 is a no-op. Asynchronous on
+ * stream; pointers are borrowed for the call only. */
+dlrm_status_t embedding_bag_multi(const float* const* tables, const int64_t* rows, int32_t K,
+                                  int32_t D, const int64_t* indices, int64_t n_idx,
+                                  const int64_t* offsets, int32_t B, int32_t mode, float* out,
+                                  int32_t* err_flag, void* stream);
 
 /* Strict-lower-triangular pairwise-dot interaction ([P1]
  * PairwiseDotLowerTriStackedKernel; [P4] dlrm_megakernel.rs steps 4-5):
