@@ -73,6 +73,12 @@ def parse_args():
     ap.add_argument("--no-gather", action="store_true",
                     help="skip the 13.3 GB standalone-gather measurement")
     ap.add_argument("--profile-steps", type=int, default=200)
+    ap.add_argument("--only-gather", action="store_true",
+                    help="time only the standalone gathers of the 26-table workload "
+                         "(uniform bags of 20 and general bags, Zipf and uniform indices)")
+    ap.add_argument("--gather-rows", type=int, default=0,
+                    help="rows per table for --only-gather (default: the workload's 1M; "
+                         "smaller tables keep an ncu capture to a few GB)")
     ap.add_argument("--only-forward", action="store_true",
                     help="time the device forward only (for ncu launch lists)")
     return ap.parse_args()
@@ -295,9 +301,9 @@ def device_tables(torch, synth, cfg, seed, n=None):
     return out
 
 
-def gather_measure(torch, dl, synth, pk, tables, steps=10):
+def gather_measure(torch, dl, synth, pk, tables, steps=10, cfg=None):
     """Standalone gather on the 26 x 1M x 128 workload (bags of 20), Zipf and uniform."""
-    cfg = synth.get_config("b65536_k26_zipf")
+    cfg = cfg or synth.get_config("b65536_k26_zipf")
     off = torch.from_numpy(synth.make_offsets(cfg)).cuda()
     out = torch.empty((cfg.batch, cfg.n_tables, cfg.emb_dim), device="cuda")
     _, byts = stage_work(cfg, "gather", cfg.batch)
@@ -324,17 +330,19 @@ def gather_measure(torch, dl, synth, pk, tables, steps=10):
         del idx
     del out
     torch.cuda.empty_cache()
-    return dict(workload="26 tables x 1M x 128 fp32 (13.3 GB), batch 65536, bags of 20",
+    return dict(workload=f"{cfg.n_tables} tables x {cfg.rows[0]} x {cfg.emb_dim} fp32 "
+                         f"({cfg.n_tables * cfg.rows[0] * cfg.emb_dim * 4 / 1e9:.1f} GB), "
+                         f"batch {cfg.batch}, bags of {cfg.bag_size}",
                 bytes_per_launch=byts, launches_timed=steps,
                 note="inputs far larger than L2; algorithmic bytes = rows + indices + offsets "
                      "+ output; Zipf hot rows are served partly from L2", **res)
 
 
-def bag_modes_measure(torch, dl, synth, pk, tables, steps=10):
+def bag_modes_measure(torch, dl, synth, pk, tables, steps=10, cfg=None):
     """embedding_bag_multi on the 26 x 1M x 128 tables: bags of random lengths 0..40
     (mean 20, empty bags included) over general offsets, sum / mean / max, Zipf and
     uniform indices."""
-    cfg = synth.get_config("b65536_k26_zipf")
+    cfg = cfg or synth.get_config("b65536_k26_zipf")
     out = torch.empty((cfg.batch, cfg.n_tables, cfg.emb_dim), device="cuda")
     modes = {"sum": dl.BAG_SUM, "mean": dl.BAG_MEAN, "max": dl.BAG_MAX}
     res = {}
@@ -371,8 +379,9 @@ def bag_modes_measure(torch, dl, synth, pk, tables, steps=10):
         del idx, off
     del out
     torch.cuda.empty_cache()
-    return dict(workload="26 tables x 1M x 128 fp32, batch 65536, bag lengths uniform on "
-                         "0..40 (general offsets)", launches_timed=steps, **res)
+    return dict(workload=f"{cfg.n_tables} tables x {cfg.rows[0]} x {cfg.emb_dim} fp32, batch "
+                         f"{cfg.batch}, bag lengths uniform on 0..40 (general offsets)",
+                launches_timed=steps, **res)
 
 
 def run_ours(args, rank, world, local_rank):
@@ -390,6 +399,21 @@ def run_ours(args, rank, world, local_rank):
         dist.init_process_group("nccl", device_id=dev)
 
     pk = peaks()
+    if args.only_gather:
+        c4 = synth.get_config("b65536_k26_zipf")
+        if args.gather_rows > 0:
+            c4 = synth.DlrmConfig(c4.name, c4.batch, c4.ln_bot, (args.gather_rows,) * c4.n_tables,
+                                  c4.emb_dim, c4.bag_size, c4.ln_top, c4.table_range,
+                                  c4.index_dist, c4.zipf_s)
+        tabs = device_tables(torch, synth, c4, args.seed)
+        gather = gather_measure(torch, dl, synth, pk, tabs, cfg=c4)
+        gather["general_bags"] = bag_modes_measure(torch, dl, synth, pk, tabs, cfg=c4)
+        if rank == 0:
+            print(json.dumps(dict(metric=METRIC, mode="only-gather",
+                                  gather_b65536_k26_zipf=gather)), flush=True)
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
     cfg = synth.get_config(args.config)
     inp = synth.make_inputs(cfg, seed=args.seed)
     cu = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
