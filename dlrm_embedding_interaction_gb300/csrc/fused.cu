@@ -54,20 +54,20 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
-// Phase trace (profiling): the consumer leader stamps when the tile finishes
-// phase `slot`.
+// Phase trace (profiling): the consumer leader stamps when tile `tile`
+// finishes phase `slot`.
 // Profiling: where GEMM layer g's leader stamps the end of its k-loop
 // (trace slot 20 + g), or null.
-__device__ __forceinline__ unsigned long long* kloop_stamp(const FusedParams& p, int g) {
+__device__ __forceinline__ unsigned long long* kloop_stamp(const FusedParams& p, int tile, int g) {
   // slots 20.. are free only while the phase stamps (up to n_gemm + 3) end below
   return (p.trace && p.n_gemm + 3 < 20 && 20 + g < kFusedTraceSlots)
-             ? p.trace + static_cast<size_t>(blockIdx.x) * kFusedTraceSlots + 20 + g
+             ? p.trace + static_cast<size_t>(tile) * kFusedTraceSlots + 20 + g
              : nullptr;
 }
 
-__device__ __forceinline__ void stamp(const FusedParams& p, int slot) {
+__device__ __forceinline__ void stamp(const FusedParams& p, int tile, int slot) {
   if (p.trace && threadIdx.x == 0)
-    p.trace[static_cast<size_t>(blockIdx.x) * kFusedTraceSlots + slot] = global_ns();
+    p.trace[static_cast<size_t>(tile) * kFusedTraceSlots + slot] = global_ns();
 }
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -251,16 +251,21 @@ __device__ void prefetch_stream_l2(const float* wstream, size_t floats) {
 constexpr uint32_t kIssuers = 4;
 constexpr unsigned kIssuerMask = (1u << kIssuers) - 1;
 
-__device__ void produce(const Ring& r, const float* wstream, const uint2* tab, uint32_t n_stages) {
+// The stage table runs once per tile of the CTA (n_tiles passes).
+__device__ void produce(const Ring& r, const float* wstream, const uint2* tab, uint32_t n_tab,
+                        uint32_t n_tiles) {
   const uint32_t lane = threadIdx.x % kWarp;
   if (lane >= kIssuers) return;
   const char* src0 = reinterpret_cast<const char*>(wstream);
+  const uint32_t n_stages = n_tab * n_tiles;
   uint32_t j = 0, slot = 0, phase = 0;   // slot = j % S, phase = (j / S) & 1
+  uint32_t jt = 0;                       // j % n_tab
   for (; j < n_stages; ++j) {
     const bool ok = j < r.s_count ||
                     wait_phase<false>(smem_u32(&r.empty[slot]), phase ^ 1, r.abort_flag, r.err);
     if (!__all_sync(kIssuerMask, ok)) break;
-    const uint2 e = __ldg(tab + j);
+    const uint2 e = __ldg(tab + jt);
+    if (++jt == n_tab) jt = 0;
     const uint32_t full = smem_u32(&r.full[slot]);
     if (lane == 0) mbar_arrive_expect_tx(full, e.y);
     __syncwarp(kIssuerMask);
@@ -540,12 +545,17 @@ __device__ void gemm_dispatch(const FusedGemm& L, float* a_s, float* c_s, int ld
   consumer_sync<CW>();
 }
 
+// One tile of BM samples, rows m0 = tile * BM on. `first`: the CTA's first
+// tile, which also fetches the biases and last-layer weights (they stay in
+// shared memory for the CTA's later tiles). `pos` carries the CTA's place in
+// the weight stream from tile to tile.
 template <int BM, int CW>
 __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, float* act1, float* zs,
-                        int* rowidx_s, float* bias_s, float* wlast_s) {
+                        int* rowidx_s, float* bias_s, float* wlast_s, int tile, bool first,
+                        RingPos& pos) {
   constexpr int kConsumers = CW * kWarp;
   const int tid = threadIdx.x;
-  const int m0 = blockIdx.x * BM;
+  const int m0 = tile * BM;
   const int rows = min(BM, p.batch - m0);
   const int k = p.k_tables, d = p.d, d4 = d / 4;
   const int f = k + 1;
@@ -557,8 +567,12 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
   // size 1 (its row, or -1, kept in shared memory) and fetch the dense
   // features into act0 (zero-padded to the first layer's k_pad); then the
   // tile's embedding rows when they are prefetched whole (group 1).
-  for (int c = tid; c < p.bias_floats / 4; c += kConsumers) cp_async16(bias_s + 4 * c, p.bias + 4 * c);
-  for (int c = tid; c < p.k_last / 4; c += kConsumers) cp_async16(wlast_s + 4 * c, p.wlast + 4 * c);
+  stamp(p, tile, 0);
+  if (first) {
+    for (int c = tid; c < p.bias_floats / 4; c += kConsumers)
+      cp_async16(bias_s + 4 * c, p.bias + 4 * c);
+    for (int c = tid; c < p.k_last / 4; c += kConsumers) cp_async16(wlast_s + 4 * c, p.wlast + 4 * c);
+  }
   cp_async_commit();
   {
     const int n_bag = (p.prefetch_z || p.zbuf == 2) ? BM * k : 0;
@@ -622,7 +636,7 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
   cp_async_commit();
   cp_async_wait<1>();
   consumer_sync<CW>();
-  stamp(p, 1);
+  stamp(p, tile, 1);
 
   // Bag-size-1 rows streamed by sample group into two buffers (zbuf == 2).
   auto issue_group = [&](int g0, int buf) {
@@ -648,15 +662,14 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
     else cp_async_commit();
   }
 
-  RingPos pos;
   float* in = act0;
   float* out = act1;
   for (int g = 0; g < p.n_bot; ++g) {
     const int zero_to = (g + 1 < p.n_bot) ? p.gemm[g + 1].k_pad : p.gemm[g].n_pad;
     gemm_dispatch<BM, CW>(p.gemm[g], in, out, p.lda, bias_s, DLRM_ACT_RELU, zero_to, ring, pos,
-                          kloop_stamp(p, g));
+                          kloop_stamp(p, tile, g));
     float* t = in; in = out; out = t;
-    stamp(p, 2 + g);
+    stamp(p, tile, 2 + g);
   }
   const float* x = in;       // bottom output (BM, d)
   float* r = out;            // R = [x, z]
@@ -766,16 +779,16 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
     if (bad_off) atomicOr(reinterpret_cast<unsigned int*>(p.err), DLRM_ERRBIT_OFFSETS);
   }
 
-  stamp(p, 2 + p.n_bot);
+  stamp(p, tile, 2 + p.n_bot);
   // Top MLP: ReLU layers, then the N = 1 sigmoid layer.
   in = r;
   out = (r == act0) ? act1 : act0;
   for (int g = p.n_bot; g < p.n_gemm; ++g) {
     const int zero_to = (g + 1 < p.n_gemm) ? p.gemm[g + 1].k_pad : p.k_last;
     gemm_dispatch<BM, CW>(p.gemm[g], in, out, p.lda, bias_s, DLRM_ACT_RELU, zero_to, ring, pos,
-                          kloop_stamp(p, g));
+                          kloop_stamp(p, tile, g));
     float* t = in; in = out; out = t;
-    stamp(p, 3 + g);
+    stamp(p, tile, 3 + g);
   }
   const int warp = tid / kWarp, lane = tid % kWarp;
   const int k4 = p.k_last / 4;
@@ -794,10 +807,9 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
     for (int o = kWarp / 2; o > 0; o /= 2) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (lane == 0) p.out[m0 + m] = apply_act(acc + bl, DLRM_ACT_SIGMOID);
   }
-  if (p.trace) {
-    consumer_sync<CW>();
-    stamp(p, 2 + p.n_gemm + 1);
-  }
+  // the next tile overwrites the activation, bag-row and row-index buffers
+  consumer_sync<CW>();
+  stamp(p, tile, 2 + p.n_gemm + 1);
 }
 
 template <int BM, int CW>
@@ -816,7 +828,9 @@ fused_forward_kernel(const __grid_constant__ FusedParams p) {
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + p.stages);
   const Ring r{stages, full, empty, abort_flag, static_cast<uint32_t>(p.stages), p.err};
   const int warp = threadIdx.x / kWarp;
-  stamp(p, 0);
+  // persistent: CTA c runs tiles c, c + gridDim.x, ...
+  const int n_tiles = (p.batch + BM - 1) / BM;
+  const int my_tiles = (n_tiles - static_cast<int>(blockIdx.x) + gridDim.x - 1) / gridDim.x;
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
@@ -831,10 +845,14 @@ fused_forward_kernel(const __grid_constant__ FusedParams p) {
     // the L2 prefetch from a lane that issues no copies: a thread's bulk
     // operations run one after another
     if (threadIdx.x % kWarp == kWarp - 1) prefetch_stream_l2(p.wstream, p.stream_floats);
-    produce(r, p.wstream, p.stage_tab, static_cast<uint32_t>(p.n_stages));
+    produce(r, p.wstream, p.stage_tab, static_cast<uint32_t>(p.n_stages),
+            static_cast<uint32_t>(my_tiles));
     return;
   }
-  consume<BM, CW>(p, r, act0, act1, zs, rowidx_s, bias_s, wlast_s);
+  RingPos pos;
+  for (int i = 0; i < my_tiles; ++i)
+    consume<BM, CW>(p, r, act0, act1, zs, rowidx_s, bias_s, wlast_s,
+                    static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x), i == 0, pos);
 }
 
 template <int BM, int CW>
@@ -867,7 +885,9 @@ cudaError_t fused_prepare(int bm, int cw) {
 
 cudaError_t launch_fused(const FusedParams& p, int bm, cudaStream_t stream) {
   if (p.batch == 0) return cudaSuccess;
-  const unsigned grid = static_cast<unsigned>((p.batch + bm - 1) / bm);
+  // persistent: at most one CTA per SM, each looping over its tiles
+  const int64_t tiles = (p.batch + bm - 1) / bm;
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(tiles, device_sm_count()));
   cudaError_t e = fused_prepare(bm, p.cw);
   if (e != cudaSuccess) return e;
   const unsigned threads = static_cast<unsigned>((p.cw + 1) * kWarp);
@@ -968,12 +988,20 @@ bool fused_plan(int n_dense, int k_tables, int d, int bag, const std::vector<int
   // first (one wave of tiles), then a weight stage is given up.
   const size_t per_sample_z = static_cast<size_t>(k_tables) * p.ldz * sizeof(float);
   bool placed = false;
-  // smallest tile height whose tiles of max_batch fit one wave (16 past that)
-  int first_bm = 16;
-  for (int bm : {4, 8, 12, 14}) {
-    if ((max_batch + bm - 1) / bm <= sms) {
+  // Tile height: the kernel is persistent (one CTA per SM looping over
+  // tiles), so a launch takes rounds = ceil(tiles / SMs) tile times. A tile's
+  // time grows about linearly with its rows, as if it had ~12 rows more (2048
+  // samples: ~24 us at 4 rows, ~42 us at 14). Take the height with the least
+  // rounds x (rows + 12), the smaller on a tie.
+  int first_bm = 4;
+  int64_t best = INT64_MAX;
+  for (int bm : {4, 8, 12, 14, 16}) {
+    const int64_t tiles = (max_batch + bm - 1) / bm;
+    const int64_t rounds = (tiles + sms - 1) / std::max(sms, 1);
+    const int64_t cost = rounds * (bm + 12);
+    if (cost < best) {
+      best = cost;
       first_bm = bm;
-      break;
     }
   }
   for (int bm : {16, 14, 12, 8, 4}) {

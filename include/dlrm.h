@@ -62,9 +62,11 @@ typedef enum {
 
 /* Kernel plan of a forward handle. AUTO takes the fused single-launch forward
  * when the shape fits it (activations of a tile of samples resident in shared
- * memory) and the batch is at most two waves of tiles, else the layer-wise
- * launches; FUSED fails dlrm_create with DLRM_ERR_UNSUPPORTED when the shape
- * does not fit; LAYERWISE always launches one kernel per step. */
+ * memory) and either the math is fp32 with bags of one row (the fp32 fused
+ * kernel is persistent, one CTA per SM looping over tiles, so any batch) or
+ * the batch is at most two waves of tiles; else the layer-wise launches.
+ * FUSED fails dlrm_create with DLRM_ERR_UNSUPPORTED when the shape does not
+ * fit; LAYERWISE always launches one kernel per step. */
 typedef enum { DLRM_PATH_AUTO = 0, DLRM_PATH_LAYERWISE = 1, DLRM_PATH_FUSED = 2 } dlrm_path_t;
 
 /* Epilogue activation of linear_bias_act. */
