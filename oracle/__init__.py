@@ -48,7 +48,8 @@ def _bind(lib):
     lib.oracle_pair_enumerate.argtypes = [i32, vp, vp]
     lib.oracle_pair_enumerate.restype = None
     lib.oracle_embedding_bag_sum.argtypes = [i32, vp, vp, i32, vp, i64, vp, i64, vp, i32]
-    lib.oracle_embedding_bag.argtypes = [i32, vp, vp, i32, vp, i64, vp, i64, i32, vp, vp, i32]
+    lib.oracle_embedding_bag.argtypes = [i32, vp, vp, i32, vp, i64, vp, i64, i32, vp, i64, vp,
+                                         vp, i32]
     lib.oracle_linear.argtypes = [i64, i32, i32, vp, vp, vp, i32, vp, i32]
     lib.oracle_interaction.argtypes = [i64, i32, i32, vp, vp, vp, i32]
     lib.oracle_forward.argtypes = [i64, i32, vp, vp, vp, i32, vp, vp, i32, vp, i64, vp,
@@ -139,8 +140,8 @@ BAG_SUM, BAG_MEAN, BAG_MAX = 0, 1, 2
 BAG_FLAG_OOB, BAG_FLAG_OFFSETS = 1, 2
 
 
-def embedding_bag(tables, indices, offsets, mode: int = BAG_SUM,
-                  threads: Optional[int] = None, lib=None):
+def embedding_bag(tables, indices, offsets, mode: int = BAG_SUM, per_sample_weights=None,
+                  padding_idx: int = -1, threads: Optional[int] = None, lib=None):
     """Bags under a reduction mode over general offsets: ((B, K, D) float64, flags).
 
     Bag b of table t is indices[t][offsets[t][b] : offsets[t][b+1]] (the last
@@ -148,6 +149,8 @@ def embedding_bag(tables, indices, offsets, mode: int = BAG_SUM,
     index out of range is left out of its bag (flag BAG_FLAG_OOB); mean divides
     by the rows kept; a bag with no rows is zeros; bad bounds (begin < 0,
     end > N, begin > end) give zeros and flag BAG_FLAG_OFFSETS.
+    per_sample_weights (K, N) float scales each row (sum only); an index equal
+    to padding_idx (>= 0) is left out without a flag.
     """
     lib = lib or load()
     tables = [_f32(t) for t in tables]
@@ -158,9 +161,13 @@ def embedding_bag(tables, indices, offsets, mode: int = BAG_SUM,
     rows = np.array([t.shape[0] for t in tables], np.int64)
     out = np.zeros((b, k, d), np.float64)
     flags = ctypes.c_int(0)
+    psw = None if per_sample_weights is None else _f32(per_sample_weights)
+    if psw is not None and psw.shape != indices.shape:
+        raise ValueError("per_sample_weights must match indices")
     rc = lib.oracle_embedding_bag(k, _ptr_array(tables), rows.ctypes.data, d,
                                   indices.ctypes.data, indices.shape[1], offsets.ctypes.data, b,
-                                  int(mode), out.ctypes.data, ctypes.byref(flags),
+                                  int(mode), None if psw is None else psw.ctypes.data,
+                                  int(padding_idx), out.ctypes.data, ctypes.byref(flags),
                                   _threads(threads))
     if rc != OK:
         raise OracleError(rc, "embedding_bag")

@@ -86,8 +86,15 @@ int bag_sum(const float* table, int64_t rows, int d, const int64_t* idx, int64_t
 // zeros (flag bit 2). Returns the flag bits.
 enum { BAG_SUM = 0, BAG_MEAN = 1, BAG_MAX = 2 };
 enum { BAG_FLAG_OOB = 1, BAG_FLAG_OFFSETS = 2 };
+//
+// PyTorch's per_sample_weights and padding_idx ([P4] LessonsLearned and the
+// translator's guards name both as cases the pages leave out): with weights
+// (sum only) row n is scaled by w[n] before it is added; an index equal to
+// padding_idx (>= 0) is left out of its bag like an out-of-range one, but
+// without a flag.
 int bag_reduce(const float* table, int64_t rows, int d, const int64_t* idx, int64_t n_idx,
-               const int64_t* off, int64_t batch, int64_t b, int mode, double* out) {
+               const int64_t* off, int64_t batch, int64_t b, int mode, const float* psw,
+               int64_t padding_idx, double* out) {
   for (int c = 0; c < d; ++c) out[c] = 0.0;
   const int64_t begin = off[b];
   const int64_t end = (b + 1 < batch) ? off[b + 1] : n_idx;
@@ -96,10 +103,12 @@ int bag_reduce(const float* table, int64_t rows, int d, const int64_t* idx, int6
   int64_t kept = 0;
   for (int64_t n = begin; n < end; ++n) {
     const int64_t r = idx[n];
+    if (padding_idx >= 0 && r == padding_idx) continue;
     if (r < 0 || r >= rows) { flags |= BAG_FLAG_OOB; continue; }
     const float* row = table + r * d;
+    const double w = psw ? static_cast<double>(psw[n]) : 1.0;
     for (int c = 0; c < d; ++c) {
-      const double v = static_cast<double>(row[c]);
+      const double v = w * static_cast<double>(row[c]);
       if (mode == BAG_MAX) out[c] = (kept == 0 || v > out[c]) ? v : out[c];
       else out[c] += v;
     }
@@ -141,7 +150,7 @@ void parallel_for(int64_t n, int threads, Fn fn) {
 
 extern "C" {
 
-int oracle_version() { return 2; }
+int oracle_version() { return 3; }
 
 // Pair index p -> (i, j), i > j >= 0 ([P1] PairwiseDotLowerTriStackedKernel:
 // "(1+sqrt(1+8p))/2"; the floor and j = p - i(i-1)/2 are the reading).
@@ -184,16 +193,21 @@ int oracle_embedding_bag_sum(int k_tables, const float* const* tables, const int
 // Multi-table EmbeddingBag with a reduction mode (0 sum, 1 mean, 2 max) over
 // general offsets: out (B, K, D) double; *flags receives the OR of the bags'
 // flag bits (1: an index out of range, 2: bad bag bounds).
+//   psw: (K, n_idx) float per-sample weights or null (sum mode only)
+//   padding_idx: a row index left out of every bag, or < 0 for none
 int oracle_embedding_bag(int k_tables, const float* const* tables, const int64_t* rows, int d,
                          const int64_t* indices, int64_t n_idx, const int64_t* offsets,
-                         int64_t batch, int mode, double* out, int* flags, int threads) {
+                         int64_t batch, int mode, const float* psw, int64_t padding_idx,
+                         double* out, int* flags, int threads) {
   if (k_tables <= 0 || d <= 0 || batch < 0 || n_idx < 0 || mode < BAG_SUM || mode > BAG_MAX)
     return ORACLE_INVALID;
+  if (psw && mode != BAG_SUM) return ORACLE_INVALID;
   std::vector<int> f(batch, 0);
   parallel_for(batch, threads, [&](int64_t b) {
     for (int t = 0; t < k_tables; ++t)
       f[b] |= bag_reduce(tables[t], rows[t], d, indices + (int64_t)t * n_idx, n_idx,
                          offsets + (int64_t)t * batch, batch, b, mode,
+                         psw ? psw + (int64_t)t * n_idx : nullptr, padding_idx,
                          out + (b * k_tables + t) * d);
   });
   int all = 0;

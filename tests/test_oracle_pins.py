@@ -244,6 +244,76 @@ def test_bag_modes_permutation_invariant(oracle_lib, name, mode):
         assert np.all(np.abs(g32 - b32) <= ulp)
 
 
+def test_bag_weighted_sum_and_padding_match_torch(oracle_lib):
+    """Library cross-check of per_sample_weights (sum) and padding_idx (all modes):
+    torch.nn.functional.embedding_bag in float64 over general offsets."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(23)
+    k, b, v, d = 2, 40, 60, 7
+    tables = [rng.uniform(-1, 1, (v, d)).astype(np.float32) for _ in range(k)]
+    idx, off, _ = _variable_bags(rng, k, b, v, 8)
+    idx[:, ::5] = 3                         # plenty of the padding row
+    w = rng.uniform(-2, 2, idx.shape).astype(np.float32)
+    e, flags = oracle.embedding_bag(tables, idx, off, oracle.BAG_SUM, per_sample_weights=w,
+                                    lib=oracle_lib)
+    assert flags == 0
+    for t in range(k):
+        ref = torch.nn.functional.embedding_bag(
+            torch.from_numpy(idx[t]), torch.from_numpy(tables[t]).double(),
+            torch.from_numpy(off[t]), mode="sum",
+            per_sample_weights=torch.from_numpy(w[t]).double()).numpy()
+        np.testing.assert_allclose(e[:, t, :], ref, rtol=1e-13, atol=1e-14)
+    for name, mode in MODES:
+        e, _ = oracle.embedding_bag(tables, idx, off, mode, padding_idx=3, lib=oracle_lib)
+        for t in range(k):
+            ref = torch.nn.functional.embedding_bag(
+                torch.from_numpy(idx[t]), torch.from_numpy(tables[t]).double(),
+                torch.from_numpy(off[t]), mode=name, padding_idx=3).numpy()
+            if mode == oracle.BAG_MAX:
+                np.testing.assert_array_equal(e[:, t, :], ref)
+            else:
+                np.testing.assert_allclose(e[:, t, :], ref, rtol=1e-13, atol=1e-14)
+
+
+def test_bag_weighted_sum_selection_matrix(oracle_lib):
+    """Brute force: the weighted sum is S diag(w) G; padding rows drop out of S."""
+    rng = np.random.default_rng(8)
+    v, d, b = 30, 5, 8
+    table = rng.uniform(-1, 1, (v, d)).astype(np.float32)
+    idx, off, _ = _variable_bags(rng, 1, b, v, 5, empty_every=3)
+    idx[0, 1::4] = 0
+    n = idx.shape[1]
+    w = rng.uniform(-1, 1, (1, n)).astype(np.float32)
+    ends = np.append(off[0, 1:], n)
+    sel = np.zeros((b, n))
+    for bb in range(b):
+        sel[bb, off[0, bb]:ends[bb]] = 1.0
+    sel[:, idx[0] == 0] = 0.0                 # padding_idx = 0
+    want = sel @ (w[0][:, None].astype(np.float64) * table[idx[0]].astype(np.float64))
+    e, _ = oracle.embedding_bag([table], idx, off, oracle.BAG_SUM, per_sample_weights=w,
+                                padding_idx=0, lib=oracle_lib)
+    np.testing.assert_allclose(e[:, 0, :], want, rtol=1e-13, atol=1e-14)
+
+
+def test_bag_padding_hand_case(oracle_lib):
+    """Hand-worked: padding rows leave the bag without a flag; mean counts the rest."""
+    g = _golden("hand_bag_modes.json")
+    table = _arr(g["table"], np.float32)
+    idx = _arr([[2, 0, 4, 1, 0, 0, 2]], np.int64)
+    off = _arr([[0, 2, 4, 6]], np.int64)     # bags {2,0}, {4,1}, {0,0}, {2}
+    e, flags = oracle.embedding_bag([table], idx, off, oracle.BAG_MEAN, padding_idx=0,
+                                    lib=oracle_lib)
+    assert flags == 0
+    np.testing.assert_array_equal(e[:, 0, :], [[5, 0], [-0.5, 3], [0, 0], [5, 0]])
+    w = _arr([[2, 10, 0.5, -1, 3, 3, 1]], np.float32)
+    e, _ = oracle.embedding_bag([table], idx, off, oracle.BAG_SUM, per_sample_weights=w,
+                                padding_idx=0, lib=oracle_lib)
+    np.testing.assert_array_equal(e[:, 0, :], [[10, 0], [4, -3], [0, 0], [5, 0]])
+    with pytest.raises(oracle.OracleError):
+        oracle.embedding_bag([table], idx, off, oracle.BAG_MAX, per_sample_weights=w,
+                             lib=oracle_lib)
+
+
 def test_bag_mean_of_one_repeated_row_is_that_row(oracle_lib):
     """Closed form: the mean of L copies of row r is row r, exactly."""
     rng = np.random.default_rng(2)
