@@ -28,7 +28,8 @@ EXPORTS = ("dlrm_version", "dlrm_status_string", "dlrm_create", "dlrm_forward",
            "dlrm_forward_host", "dlrm_get_error", "dlrm_workspace_bytes", "dlrm_destroy",
            "dlrm_path", "dlrm_num_stages", "dlrm_stage_name", "dlrm_set_profiling", "dlrm_stage_times",
            "dlrm_forward_noalloc", "dlrm_set_phase_trace",
-           "embedding_bag_sum_multi", "embedding_bag_multi", "pairwise_dot_lower_tri",
+           "embedding_bag_sum_multi", "embedding_bag_multi", "embedding_bag_multi_ex",
+           "pairwise_dot_lower_tri",
            "pairwise_pair_map", "linear_bias_act")
 NOALLOC_SCRATCH_BYTES = 16 << 20
 TRACE_SLOTS = 40
@@ -41,6 +42,11 @@ class DlrmError(RuntimeError):
         msg = _status_string(status)
         super().__init__(f"{where}: status {status} ({msg})")
         self.status = status
+
+
+class _BagOptions(ctypes.Structure):
+    _fields_ = [("mode", ctypes.c_int32), ("index_bits", ctypes.c_int32),
+                ("per_sample_weights", ctypes.c_void_p), ("padding_idx", ctypes.c_int64)]
 
 
 class _Config(ctypes.Structure):
@@ -73,6 +79,8 @@ def _bind(lib):
         "dlrm_set_phase_trace": ([vp, vp, i64, ctypes.POINTER(i32)], st),
         "embedding_bag_sum_multi": ([vp, vp, i32, i32, vp, vp, i32, i32, vp, vp, vp], st),
         "embedding_bag_multi": ([vp, vp, i32, i32, vp, i64, vp, i32, i32, vp, vp, vp], st),
+        "embedding_bag_multi_ex": ([vp, vp, i32, i32, vp, i64, vp, i32,
+                                    ctypes.POINTER(_BagOptions), vp, vp, vp], st),
         "pairwise_dot_lower_tri": ([vp, i32, vp, i32, i32, i32, vp, i32, i32, vp], st),
         "pairwise_pair_map": ([i32, vp, vp, vp], st),
         "linear_bias_act": ([vp, i32, vp, vp, vp, i32, i32, i32, i32, st, st, vp], st),
@@ -176,11 +184,14 @@ BAG_SUM, BAG_MEAN, BAG_MAX = 0, 1, 2
 
 
 def embedding_bag_multi(tables: Sequence, indices, offsets, out, mode: int = BAG_SUM,
-                        err_flag=None, stream=None) -> None:
+                        per_sample_weights=None, padding_idx: int = -1, err_flag=None,
+                        stream=None) -> None:
     """out (B, K, D) = per-table bag reductions over general offsets.
 
-    indices (K, N) int64; offsets (K, B) int64 bag starts (the last bag runs
-    to N); mode BAG_SUM, BAG_MEAN or BAG_MAX.
+    indices (K, N) and offsets (K, B), both int64 or both int32; offsets are bag
+    starts (the last bag runs to N); mode BAG_SUM, BAG_MEAN or BAG_MAX.
+    per_sample_weights (K, N) fp32 scales each row (BAG_SUM only); an index equal
+    to padding_idx (>= 0) is left out of its bag.
     """
     import torch
     k = len(tables)
@@ -191,8 +202,10 @@ def embedding_bag_multi(tables: Sequence, indices, offsets, out, mode: int = BAG
         _need(t, torch.float32, f"tables[{i}]")
         if t.dim() != 2 or t.shape[1] != d or not t.is_contiguous():
             raise ValueError(f"tables[{i}]: expected contiguous (rows, {d})")
-    _need(indices, torch.int64, "indices")
-    _need(offsets, torch.int64, "offsets")
+    if indices.dtype not in (torch.int64, torch.int32) or offsets.dtype != indices.dtype:
+        raise ValueError("indices and offsets must both be int64 or both int32")
+    _need(indices, indices.dtype, "indices")
+    _need(offsets, offsets.dtype, "offsets")
     _need(out, torch.float32, "out")
     b = offsets.shape[1]
     if (indices.dim() != 2 or indices.shape[0] != k or tuple(offsets.shape) != (k, b)
@@ -200,14 +213,21 @@ def embedding_bag_multi(tables: Sequence, indices, offsets, out, mode: int = BAG
         raise ValueError("shape mismatch among indices/offsets/out")
     if not (indices.is_contiguous() and offsets.is_contiguous() and out.is_contiguous()):
         raise ValueError("indices, offsets and out must be contiguous")
+    if per_sample_weights is not None:
+        _need(per_sample_weights, torch.float32, "per_sample_weights")
+        if (tuple(per_sample_weights.shape) != tuple(indices.shape)
+                or not per_sample_weights.is_contiguous()):
+            raise ValueError("per_sample_weights must be a contiguous tensor shaped like indices")
     if err_flag is not None:
         _need(err_flag, torch.int32, "err_flag")
     ptrs = (ctypes.c_void_p * k)(*[t.data_ptr() for t in tables])
     rows = (ctypes.c_int64 * k)(*[t.shape[0] for t in tables])
-    _check(lib().embedding_bag_multi(ptrs, rows, k, d, _ptr(indices), indices.shape[1],
-                                     _ptr(offsets), b, int(mode), _ptr(out), _ptr(err_flag),
-                                     _stream(stream)),
-           "embedding_bag_multi")
+    opt = _BagOptions(int(mode), 64 if indices.dtype == torch.int64 else 32,
+                      _ptr(per_sample_weights), int(padding_idx))
+    _check(lib().embedding_bag_multi_ex(ptrs, rows, k, d, _ptr(indices), indices.shape[1],
+                                        _ptr(offsets), b, ctypes.byref(opt), _ptr(out),
+                                        _ptr(err_flag), _stream(stream)),
+           "embedding_bag_multi_ex")
 
 
 def pairwise_dot_lower_tri(dense, emb, out, copy_dense: bool = True, stream=None) -> None:

@@ -655,13 +655,19 @@ dlrm_status_t embedding_bag_sum_multi(const float* const* tables, const int64_t*
                                          static_cast<cudaStream_t>(stream)));
 }
 
-dlrm_status_t embedding_bag_multi(const float* const* tables, const int64_t* rows, int32_t K,
-                                  int32_t D, const int64_t* indices, int64_t n_idx,
-                                  const int64_t* offsets, int32_t B, int32_t mode, float* out,
-                                  int32_t* err_flag, void* stream) {
+dlrm_status_t embedding_bag_multi_ex(const float* const* tables, const int64_t* rows, int32_t K,
+                                     int32_t D, const void* indices, int64_t n_idx,
+                                     const void* offsets, int32_t B,
+                                     const dlrm_bag_options_t* options, float* out,
+                                     int32_t* err_flag, void* stream) {
+  if (!options) return DLRM_ERR_INVALID_ARG;
+  const int mode = options->mode;
   if (K < 1 || D < 1 || B < 0 || n_idx < 0) return DLRM_ERR_INVALID_ARG;
   if (mode != DLRM_BAG_SUM && mode != DLRM_BAG_MEAN && mode != DLRM_BAG_MAX)
     return DLRM_ERR_INVALID_ARG;
+  if (options->index_bits != 32 && options->index_bits != 64) return DLRM_ERR_INVALID_ARG;
+  if (options->index_bits == 32 && n_idx > INT32_MAX) return DLRM_ERR_INVALID_ARG;
+  if (options->per_sample_weights && mode != DLRM_BAG_SUM) return DLRM_ERR_INVALID_ARG;
   if (K > DLRM_MAX_TABLES) return DLRM_ERR_UNSUPPORTED;
   if (!tables || !rows) return DLRM_ERR_INVALID_ARG;
   if (B == 0) return DLRM_OK;
@@ -672,9 +678,19 @@ dlrm_status_t embedding_bag_multi(const float* const* tables, const int64_t* row
     tabs.ptr[t] = tables[t];
     tabs.rows[t] = rows[t];
   }
-  return cuda_status(dlrm::launch_gather_general(tabs, K, D, indices, n_idx, offsets, B, mode,
-                                                 out, err_flag,
-                                                 static_cast<cudaStream_t>(stream)));
+  const int64_t padding = options->padding_idx >= 0 ? options->padding_idx : -1;
+  return cuda_status(dlrm::launch_gather_general(
+      tabs, K, D, indices, n_idx, offsets, options->index_bits, B, mode,
+      options->per_sample_weights, padding, out, err_flag, static_cast<cudaStream_t>(stream)));
+}
+
+dlrm_status_t embedding_bag_multi(const float* const* tables, const int64_t* rows, int32_t K,
+                                  int32_t D, const int64_t* indices, int64_t n_idx,
+                                  const int64_t* offsets, int32_t B, int32_t mode, float* out,
+                                  int32_t* err_flag, void* stream) {
+  const dlrm_bag_options_t opt{mode, 64, nullptr, -1};
+  return embedding_bag_multi_ex(tables, rows, K, D, indices, n_idx, offsets, B, &opt, out,
+                                err_flag, stream);
 }
 
 dlrm_status_t pairwise_dot_lower_tri(const float* dense, int32_t ld_dense, const float* emb,

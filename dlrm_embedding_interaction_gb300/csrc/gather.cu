@@ -47,19 +47,48 @@ __device__ __forceinline__ void add4(float4& a, const float4& v) {
   a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
 }
 
+__device__ __forceinline__ void fma4(float4& a, float w, const float4& v) {
+  a.x = fmaf(w, v.x, a.x); a.y = fmaf(w, v.y, a.y); a.z = fmaf(w, v.z, a.z); a.w = fmaf(w, v.w, a.w);
+}
+
 __device__ __forceinline__ void max4(float4& a, const float4& v) {
   a.x = fmaxf(a.x, v.x); a.y = fmaxf(a.y, v.y); a.z = fmaxf(a.z, v.z); a.w = fmaxf(a.w, v.w);
+}
+
+// The weighted sum (per_sample_weights) is a fourth, internal reduction.
+constexpr int kBagWeightedSum = 3;
+
+// Bag bounds: the uniform stride (GENERAL false: start must equal b * bag)
+// or consecutive offsets with the last bag running to N.
+template <bool GENERAL, typename IDX>
+__device__ __forceinline__ bool bag_bounds(const IDX* offs, int b, int batch, int bag,
+                                           int64_t n_idx, int64_t& start, int& len) {
+  start = static_cast<int64_t>(offs[b]);
+  if (!GENERAL) {
+    len = bag;
+    return start == static_cast<int64_t>(b) * bag;
+  }
+  const int64_t end = (b + 1 < batch) ? static_cast<int64_t>(offs[b + 1]) : n_idx;
+  len = static_cast<int>(end - start);
+  return start >= 0 && end <= n_idx && start <= end && end - start <= INT32_MAX;
 }
 
 // Vector path: D % 4 == 0, tables and out 16-byte aligned.
 // TPB lanes per bag (power of two <= 32); each lane owns CHUNKS float4 columns
 // col4 = lane + c * TPB (< D/4). GENERAL: bag bounds from consecutive offsets
-// (else the uniform stride L); MODE: DLRM_BAG_SUM, _MEAN or _MAX.
-template <int TPB, int CHUNKS, int MODE, bool GENERAL>
-__global__ void __launch_bounds__(kGatherThreads)
+// (else the uniform stride L); MODE: DLRM_BAG_SUM, _MEAN, _MAX or the weighted
+// sum; IDX: the index and offset type. An index equal to `padding`, when that
+// is >= 0, is left out of its bag without a flag (a negative `padding` is none).
+// Six CTAs of 256 threads per SM (at most 40 registers a thread) keep the
+// most rows in flight; ptxas spills a few bytes outside the row loop rather
+// than fall to five.
+template <int TPB, int CHUNKS, int MODE, bool GENERAL, typename IDX>
+__global__ void __launch_bounds__(kGatherThreads, CHUNKS == 1 ? 6 : 1)
 gather_vec_kernel(const __grid_constant__ GatherTables tabs, int k_tables, int d4,
-                  const int64_t* __restrict__ indices, const int64_t* __restrict__ offsets,
-                  int batch, int bag, int64_t n_idx, float* __restrict__ out, int32_t* err) {
+                  const IDX* __restrict__ indices, const IDX* __restrict__ offsets,
+                  const float* __restrict__ psw, int64_t padding, int batch, int bag,
+                  int64_t n_idx, float* __restrict__ out, int32_t* err) {
+  constexpr bool kWeighted = MODE == kBagWeightedSum;
   const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t bag_id = gtid / TPB;
   const int lane = threadIdx.x & (TPB - 1);
@@ -75,39 +104,36 @@ gather_vec_kernel(const __grid_constant__ GatherTables tabs, int k_tables, int d
 #pragma unroll
   for (int c = 0; c < CHUNKS; ++c) acc[c] = make_float4(init, init, init, init);
 
-  const int64_t* offs = offsets + static_cast<int64_t>(t) * batch;
-  const int64_t start = offs[b];
-  int len = bag;
-  bool good;
-  if (GENERAL) {
-    const int64_t end = (b + 1 < batch) ? offs[b + 1] : n_idx;
-    good = start >= 0 && end <= n_idx && start <= end && end - start <= INT32_MAX;
-    len = static_cast<int>(end - start);
-  } else {
-    good = start == static_cast<int64_t>(b) * bag;
-  }
+  int64_t start;
+  int len;
+  const bool good =
+      bag_bounds<GENERAL>(offsets + static_cast<int64_t>(t) * batch, b, batch, bag, n_idx, start, len);
   int kept = 0;
   if (!good) {
     if (lane == 0) flag_error(err, DLRM_ERRBIT_OFFSETS);
   } else {
-    const int64_t* idx = indices + static_cast<int64_t>(t) * n_idx + start;
+    const int64_t base = static_cast<int64_t>(t) * n_idx + start;
+    const IDX* idx = indices + base;
     const float4* table = reinterpret_cast<const float4*>(tabs.ptr[t]);
     const int64_t rows = tabs.rows[t];
     bool oob = false;
     for (int l0 = 0; l0 < len; l0 += TPB) {
       const int cnt = min(TPB, len - l0);
-      const int64_t mine = (lane < cnt) ? __ldg(idx + l0 + lane) : 0;
+      const int64_t mine = (lane < cnt) ? static_cast<int64_t>(__ldg(idx + l0 + lane)) : 0;
+      const float mine_w = (kWeighted && lane < cnt) ? __ldg(psw + base + l0 + lane) : 1.f;
       for (int u0 = 0; u0 < cnt; u0 += kUnroll) {
-        // a row left out (past the bag or out of range) loads the identity of
-        // the reduction: 0 for sums, -inf for max
+        // a row left out (past the bag, padding or out of range) loads the
+        // identity of the reduction: 0 for sums, -inf for max
         float4 v[kUnroll][CHUNKS];
+        float wq[kUnroll];
 #pragma unroll
         for (int q = 0; q < kUnroll; ++q) {
           const int64_t r = __shfl_sync(gmask, mine, (u0 + q) & (TPB - 1), TPB);
-          const bool live = (u0 + q) < cnt;
+          if (kWeighted) wq[q] = __shfl_sync(gmask, mine_w, (u0 + q) & (TPB - 1), TPB);
+          const bool live = (u0 + q) < cnt && !(GENERAL && padding >= 0 && r == padding);
           const bool ok = live && r >= 0 && r < rows;
           oob |= live && !ok;
-          if (MODE != DLRM_BAG_SUM) kept += ok ? 1 : 0;
+          if (MODE == DLRM_BAG_MEAN || MODE == DLRM_BAG_MAX) kept += ok ? 1 : 0;
 #pragma unroll
           for (int c = 0; c < CHUNKS; ++c) {
             const int col4 = lane + c * TPB;
@@ -120,6 +146,7 @@ gather_vec_kernel(const __grid_constant__ GatherTables tabs, int k_tables, int d
 #pragma unroll
           for (int c = 0; c < CHUNKS; ++c) {
             if (MODE == DLRM_BAG_MAX) max4(acc[c], v[q][c]);
+            else if (kWeighted) fma4(acc[c], wq[q], v[q][c]);
             else add4(acc[c], v[q][c]);
           }
       }
@@ -134,7 +161,7 @@ gather_vec_kernel(const __grid_constant__ GatherTables tabs, int k_tables, int d
     const int col4 = lane + c * TPB;
     if (col4 >= d4) continue;
     float4 r = acc[c];
-    if (MODE != DLRM_BAG_SUM && kept == 0) {
+    if ((MODE == DLRM_BAG_MEAN || MODE == DLRM_BAG_MAX) && kept == 0) {
       r = make_float4(0.f, 0.f, 0.f, 0.f);
     } else if (MODE == DLRM_BAG_MEAN) {
       r = make_float4(r.x / static_cast<float>(kept), r.y / static_cast<float>(kept),
@@ -146,11 +173,12 @@ gather_vec_kernel(const __grid_constant__ GatherTables tabs, int k_tables, int d
 
 // Scalar path for any D and alignment: TPB = 32 lanes per bag, lane owns
 // columns lane, lane + 32, ...; indices re-read per column from L1.
-template <int MODE, bool GENERAL>
+template <int MODE, bool GENERAL, typename IDX>
 __global__ void __launch_bounds__(kGatherThreads)
 gather_scalar_kernel(const __grid_constant__ GatherTables tabs, int k_tables, int d,
-                     const int64_t* __restrict__ indices, const int64_t* __restrict__ offsets,
-                     int batch, int bag, int64_t n_idx, float* __restrict__ out, int32_t* err) {
+                     const IDX* __restrict__ indices, const IDX* __restrict__ offsets,
+                     const float* __restrict__ psw, int64_t padding, int batch, int bag,
+                     int64_t n_idx, float* __restrict__ out, int32_t* err) {
   const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t bag_id = gtid / kWarp;
   const int lane = threadIdx.x & (kWarp - 1);
@@ -158,23 +186,16 @@ gather_scalar_kernel(const __grid_constant__ GatherTables tabs, int k_tables, in
   const int b = static_cast<int>(bag_id / k_tables);
   const int t = static_cast<int>(bag_id - static_cast<int64_t>(b) * k_tables);
   float* dst = out + bag_id * d;
-  const int64_t* offs = offsets + static_cast<int64_t>(t) * batch;
-  const int64_t start = offs[b];
-  int len = bag;
-  bool good;
-  if (GENERAL) {
-    const int64_t end = (b + 1 < batch) ? offs[b + 1] : n_idx;
-    good = start >= 0 && end <= n_idx && start <= end && end - start <= INT32_MAX;
-    len = static_cast<int>(end - start);
-  } else {
-    good = start == static_cast<int64_t>(b) * bag;
-  }
-  if (!good) {
+  int64_t start;
+  int len;
+  if (!bag_bounds<GENERAL>(offsets + static_cast<int64_t>(t) * batch, b, batch, bag, n_idx, start,
+                           len)) {
     if (lane == 0) flag_error(err, DLRM_ERRBIT_OFFSETS);
     for (int c = lane; c < d; c += kWarp) dst[c] = 0.f;
     return;
   }
-  const int64_t* idx = indices + static_cast<int64_t>(t) * n_idx + start;
+  const int64_t base = static_cast<int64_t>(t) * n_idx + start;
+  const IDX* idx = indices + base;
   const float* table = tabs.ptr[t];
   const int64_t rows = tabs.rows[t];
   bool oob = false;
@@ -182,10 +203,13 @@ gather_scalar_kernel(const __grid_constant__ GatherTables tabs, int k_tables, in
     float acc = MODE == DLRM_BAG_MAX ? -INFINITY : 0.f;
     int kept = 0;
     for (int l = 0; l < len; ++l) {
-      const int64_t r = __ldg(idx + l);
+      const int64_t r = static_cast<int64_t>(__ldg(idx + l));
+      if (GENERAL && padding >= 0 && r == padding) continue;
       if (r >= 0 && r < rows) {
         const float v = __ldg(table + r * d + c);
-        acc = MODE == DLRM_BAG_MAX ? fmaxf(acc, v) : acc + v;
+        if (MODE == DLRM_BAG_MAX) acc = fmaxf(acc, v);
+        else if (MODE == kBagWeightedSum) acc = fmaf(__ldg(psw + base + l), v, acc);
+        else acc += v;
         ++kept;
       } else {
         oob = true;
@@ -199,29 +223,30 @@ gather_scalar_kernel(const __grid_constant__ GatherTables tabs, int k_tables, in
   if (__any_sync(0xffffffffu, oob) && lane == 0) flag_error(err, DLRM_ERRBIT_INDEX_OOB);
 }
 
-template <int TPB, int CHUNKS, int MODE, bool GENERAL>
-cudaError_t launch_vec(const GatherTables& tabs, int k, int d, const int64_t* indices,
-                       const int64_t* offsets, int b, int l, int64_t n_idx, float* out,
-                       int32_t* err, cudaStream_t stream) {
+template <int TPB, int CHUNKS, int MODE, bool GENERAL, typename IDX>
+cudaError_t launch_vec(const GatherTables& tabs, int k, int d, const IDX* indices,
+                       const IDX* offsets, const float* psw, int64_t padding, int b, int l,
+                       int64_t n_idx, float* out, int32_t* err, cudaStream_t stream) {
   const int64_t bags = static_cast<int64_t>(b) * k;
   const int64_t per_block = kGatherThreads / TPB;
   const int64_t grid = (bags + per_block - 1) / per_block;
-  gather_vec_kernel<TPB, CHUNKS, MODE, GENERAL>
-      <<<static_cast<unsigned>(grid), kGatherThreads, 0, stream>>>(tabs, k, d / 4, indices,
-                                                                   offsets, b, l, n_idx, out, err);
+  gather_vec_kernel<TPB, CHUNKS, MODE, GENERAL, IDX>
+      <<<static_cast<unsigned>(grid), kGatherThreads, 0, stream>>>(
+          tabs, k, d / 4, indices, offsets, psw, padding, b, l, n_idx, out, err);
   return cudaGetLastError();
 }
 
 // Lane-group width and columns per lane by D, vector or scalar path.
-template <int MODE, bool GENERAL>
-cudaError_t launch_any(const GatherTables& tabs, int k, int d, const int64_t* indices,
-                       const int64_t* offsets, int b, int l, int64_t n_idx, float* out,
-                       int32_t* err, cudaStream_t stream) {
+template <int MODE, bool GENERAL, typename IDX>
+cudaError_t launch_any(const GatherTables& tabs, int k, int d, const IDX* indices,
+                       const IDX* offsets, const float* psw, int64_t padding, int b, int l,
+                       int64_t n_idx, float* out, int32_t* err, cudaStream_t stream) {
   bool vec = (d % 4 == 0) && (reinterpret_cast<uintptr_t>(out) % 16 == 0);
   for (int t = 0; t < k && vec; ++t) vec = reinterpret_cast<uintptr_t>(tabs.ptr[t]) % 16 == 0;
   const int d4 = d / 4;
-#define DLRM_VEC(TPB_, CH_) \
-  launch_vec<TPB_, CH_, MODE, GENERAL>(tabs, k, d, indices, offsets, b, l, n_idx, out, err, stream)
+#define DLRM_VEC(TPB_, CH_)                                                                     \
+  launch_vec<TPB_, CH_, MODE, GENERAL, IDX>(tabs, k, d, indices, offsets, psw, padding, b, l, \
+                                            n_idx, out, err, stream)
   if (vec && d4 <= 256) {
     if (d4 <= 1) return DLRM_VEC(1, 1);
     if (d4 <= 2) return DLRM_VEC(2, 1);
@@ -237,9 +262,34 @@ cudaError_t launch_any(const GatherTables& tabs, int k, int d, const int64_t* in
   const int64_t bags = static_cast<int64_t>(b) * k;
   const int64_t per_block = kGatherThreads / kWarp;
   const int64_t grid = (bags + per_block - 1) / per_block;
-  gather_scalar_kernel<MODE, GENERAL><<<static_cast<unsigned>(grid), kGatherThreads, 0, stream>>>(
-      tabs, k, d, indices, offsets, b, l, n_idx, out, err);
+  gather_scalar_kernel<MODE, GENERAL, IDX><<<static_cast<unsigned>(grid), kGatherThreads, 0,
+                                             stream>>>(tabs, k, d, indices, offsets, psw, padding,
+                                                       b, l, n_idx, out, err);
   return cudaGetLastError();
+}
+
+template <typename IDX>
+cudaError_t launch_general(const GatherTables& tabs, int k, int d, const IDX* indices,
+                           int64_t n_idx, const IDX* offsets, int b, int mode, const float* psw,
+                           int64_t padding, float* out, int32_t* err, cudaStream_t stream) {
+  if (psw) {
+    if (mode != DLRM_BAG_SUM) return cudaErrorInvalidValue;
+    return launch_any<kBagWeightedSum, true, IDX>(tabs, k, d, indices, offsets, psw, padding, b,
+                                                  0, n_idx, out, err, stream);
+  }
+  switch (mode) {
+    case DLRM_BAG_SUM:
+      return launch_any<DLRM_BAG_SUM, true, IDX>(tabs, k, d, indices, offsets, nullptr, padding,
+                                                 b, 0, n_idx, out, err, stream);
+    case DLRM_BAG_MEAN:
+      return launch_any<DLRM_BAG_MEAN, true, IDX>(tabs, k, d, indices, offsets, nullptr, padding,
+                                                  b, 0, n_idx, out, err, stream);
+    case DLRM_BAG_MAX:
+      return launch_any<DLRM_BAG_MAX, true, IDX>(tabs, k, d, indices, offsets, nullptr, padding,
+                                                 b, 0, n_idx, out, err, stream);
+    default:
+      return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
@@ -248,27 +298,22 @@ cudaError_t launch_gather(const GatherTables& tabs, int k, int d, const int64_t*
                           const int64_t* offsets, int b, int l, float* out, int /*unused*/,
                           int32_t* err, cudaStream_t stream) {
   if (b == 0) return cudaSuccess;
-  return launch_any<DLRM_BAG_SUM, false>(tabs, k, d, indices, offsets, b, l,
-                                         static_cast<int64_t>(b) * l, out, err, stream);
+  return launch_any<DLRM_BAG_SUM, false, int64_t>(tabs, k, d, indices, offsets, nullptr, -1, b, l,
+                                                  static_cast<int64_t>(b) * l, out, err, stream);
 }
 
-cudaError_t launch_gather_general(const GatherTables& tabs, int k, int d, const int64_t* indices,
-                                  int64_t n_idx, const int64_t* offsets, int b, int mode,
-                                  float* out, int32_t* err, cudaStream_t stream) {
+cudaError_t launch_gather_general(const GatherTables& tabs, int k, int d, const void* indices,
+                                  int64_t n_idx, const void* offsets, int index_bits, int b,
+                                  int mode, const float* psw, int64_t padding, float* out,
+                                  int32_t* err, cudaStream_t stream) {
   if (b == 0) return cudaSuccess;
-  switch (mode) {
-    case DLRM_BAG_SUM:
-      return launch_any<DLRM_BAG_SUM, true>(tabs, k, d, indices, offsets, b, 0, n_idx, out, err,
-                                            stream);
-    case DLRM_BAG_MEAN:
-      return launch_any<DLRM_BAG_MEAN, true>(tabs, k, d, indices, offsets, b, 0, n_idx, out, err,
-                                             stream);
-    case DLRM_BAG_MAX:
-      return launch_any<DLRM_BAG_MAX, true>(tabs, k, d, indices, offsets, b, 0, n_idx, out, err,
-                                            stream);
-    default:
-      return cudaErrorInvalidValue;
-  }
+  if (index_bits == 32)
+    return launch_general<int32_t>(tabs, k, d, static_cast<const int32_t*>(indices), n_idx,
+                                   static_cast<const int32_t*>(offsets), b, mode, psw, padding,
+                                   out, err, stream);
+  return launch_general<int64_t>(tabs, k, d, static_cast<const int64_t*>(indices), n_idx,
+                                 static_cast<const int64_t*>(offsets), b, mode, psw, padding, out,
+                                 err, stream);
 }
 
 }  // namespace dlrm

@@ -49,6 +49,7 @@ STREAM_INDEX = 2000
 STREAM_BOT = 3000
 STREAM_TOP = 4000
 STREAM_BAG_LEN = 5000
+STREAM_BAG_WEIGHT = 6000
 
 
 def build(force: bool = False) -> str:
@@ -306,6 +307,15 @@ def make_variable_bags(cfg: DlrmConfig, seed: int, max_len: int, batch: Optional
         else:
             fill_index_uniform(indices[t], seed, STREAM_INDEX + t, cfg.rows[t], threads)
     return indices, offsets, lens
+
+
+def make_bag_weights(shape, seed: int, lo: float = -2.0, hi: float = 2.0,
+                     threads: Optional[int] = None) -> np.ndarray:
+    """Per-sample weights (K, N) fp32, uniform on [lo, hi) (stream STREAM_BAG_WEIGHT + t)."""
+    out = np.empty(shape, np.float32)
+    for t in range(shape[0]):
+        fill_uniform(out[t], seed, STREAM_BAG_WEIGHT + t, lo, hi, threads)
+    return out
 
 
 def make_inputs(cfg: DlrmConfig, seed: int = 1234, batch: Optional[int] = None,

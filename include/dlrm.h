@@ -294,6 +294,35 @@ dlrm_status_t embedding_bag_multi(const float* const* tables, const int64_t* row
                                   const int64_t* offsets, int32_t B, int32_t mode, float* out,
                                   int32_t* err_flag, void* stream);
 
+/* Options of embedding_bag_multi_ex, PyTorch's EmbeddingBag arguments beyond
+ * the mode.
+ *   mode                DLRM_BAG_SUM, DLRM_BAG_MEAN or DLRM_BAG_MAX
+ *   index_bits          64: indices and offsets are int64_t; 32: int32_t
+ *   per_sample_weights  device (K, N) fp32 or NULL: with DLRM_BAG_SUM,
+ *                       out[b][t] = sum_n w[t][n] * tables[t][indices[t][n]]
+ *                       (fp32 fused multiply-adds in index order); any other
+ *                       mode with weights is DLRM_ERR_INVALID_ARG
+ *   padding_idx         a row index (>= 0) left out of every bag without a
+ *                       flag (not counted by mean), or -1 for none */
+typedef struct {
+  int32_t mode;
+  int32_t index_bits;
+  const float* per_sample_weights;
+  int64_t padding_idx;
+} dlrm_bag_options_t;
+
+/* embedding_bag_multi with options: the same operation and error behaviour,
+ * indices and offsets of either width, per-sample weights and a padding row.
+ * indices and offsets point to (K, N) and (K, B) arrays of the type
+ * index_bits names. Returns DLRM_ERR_INVALID_ARG for a null options pointer,
+ * index_bits other than 32 or 64, N > INT32_MAX with 32-bit indices, or the
+ * cases of embedding_bag_multi. */
+dlrm_status_t embedding_bag_multi_ex(const float* const* tables, const int64_t* rows, int32_t K,
+                                     int32_t D, const void* indices, int64_t n_idx,
+                                     const void* offsets, int32_t B,
+                                     const dlrm_bag_options_t* options, float* out,
+                                     int32_t* err_flag, void* stream);
+
 /* Strict-lower-triangular pairwise-dot interaction ([P1]
  * PairwiseDotLowerTriStackedKernel; [P4] dlrm_megakernel.rs steps 4-5):
  * per sample, Z = [dense; emb[0..K-1]] is (F, D) with F = K + 1, and

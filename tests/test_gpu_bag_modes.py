@@ -205,3 +205,102 @@ def test_zipf_bags_of_the_large_workload_sampled(mode, omode):
     ref, flags = oracle.embedding_bag(tables, idx, off, omode)
     assert err == 0 and flags == 0
     _compare(got, ref, mode)
+
+
+# ---------------------------------------------------------------- options
+
+def _run_ex(tables, idx, off, mode, psw=None, padding_idx=-1, out=None):
+    k, d = len(tables), tables[0].shape[1]
+    b = off.shape[1]
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    if out is None:
+        out = torch.full((b, k, d), float("nan"), device="cuda")
+    dl.embedding_bag_multi([cu(t) for t in tables], cu(idx), cu(off), out, mode,
+                           per_sample_weights=None if psw is None else cu(psw),
+                           padding_idx=padding_idx, err_flag=err)
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), int(err.item())
+
+
+@pytest.mark.parametrize("mode,omode", MODES, ids=MODE_IDS)
+@pytest.mark.parametrize("d", [64, 13])
+def test_int32_indices_and_offsets(mode, omode, d):
+    """32-bit indices and offsets give what 64-bit ones give (and the oracle)."""
+    cfg, tables = _tables((3000, 2000), d, seed=31)
+    idx, off, _ = synth.make_variable_bags(cfg.with_batch(150), seed=32, max_len=15)
+    got32, err = _run_ex(tables, idx.astype(np.int32), off.astype(np.int32), mode)
+    got64, _ = _run_ex(tables, idx, off, mode)
+    ref, _ = oracle.embedding_bag(tables, idx, off, omode)
+    assert err == 0
+    np.testing.assert_array_equal(got32, got64)
+    _compare(got32, ref, mode)
+
+
+@pytest.mark.parametrize("bits", [64, 32])
+@pytest.mark.parametrize("d", [128, 24, 7])
+def test_per_sample_weights(bits, d):
+    cfg, tables = _tables((4000, 300, 50), d, seed=41)
+    idx, off, _ = synth.make_variable_bags(cfg.with_batch(120), seed=42, max_len=20)
+    w = synth.make_bag_weights(idx.shape, 43)
+    dt = np.int64 if bits == 64 else np.int32
+    got, err = _run_ex(tables, idx.astype(dt), off.astype(dt), dl.BAG_SUM, psw=w)
+    ref, flags = oracle.embedding_bag(tables, idx, off, oracle.BAG_SUM, per_sample_weights=w)
+    assert err == 0 and flags == 0
+    _compare(got, ref, dl.BAG_SUM)
+
+
+@pytest.mark.parametrize("mode,omode", MODES, ids=MODE_IDS)
+def test_padding_idx_leaves_rows_out_without_a_flag(mode, omode):
+    cfg, tables = _tables((500, 500), 32, seed=51)
+    idx, off, _ = synth.make_variable_bags(cfg.with_batch(80), seed=52, max_len=6)
+    idx = idx.copy()
+    idx[:, ::3] = 7                     # a third of all entries are the padding row
+    got, err = _run_ex(tables, idx, off, mode, padding_idx=7)
+    ref, flags = oracle.embedding_bag(tables, idx, off, omode, padding_idx=7)
+    assert err == 0 and flags == 0
+    _compare(got, ref, mode)
+    # and without padding_idx the same rows count
+    got2, _ = _run_ex(tables, idx, off, mode)
+    ref2, _ = oracle.embedding_bag(tables, idx, off, omode)
+    _compare(got2, ref2, mode)
+
+
+@pytest.mark.parametrize("mode,omode", MODES, ids=MODE_IDS)
+def test_minus_one_is_out_of_range_without_padding(mode, omode):
+    """With no padding row, an index of -1 is out of range: left out and flagged."""
+    cfg, tables = _tables((200,), 16, seed=71)
+    idx, off, _ = synth.make_variable_bags(cfg.with_batch(30), seed=72, max_len=5)
+    idx = idx.copy()
+    idx[0, 4] = -1
+    got, err = _run_ex(tables, idx, off, mode)
+    ref, flags = oracle.embedding_bag(tables, idx, off, omode)
+    assert flags == oracle.BAG_FLAG_OOB and _flags(err) == flags
+    _compare(got, ref, mode)
+
+
+def test_weights_padding_and_bad_rows_together():
+    cfg, tables = _tables((600,), 16, seed=61)
+    idx, off, _ = synth.make_variable_bags(cfg.with_batch(64), seed=62, max_len=9)
+    idx = idx.copy()
+    idx[0, ::5] = 0
+    idx[0, 3] = 600
+    w = np.linspace(-1, 1, idx.size, dtype=np.float32).reshape(idx.shape)
+    got, err = _run_ex(tables, idx, off, dl.BAG_SUM, psw=w, padding_idx=0)
+    ref, flags = oracle.embedding_bag(tables, idx, off, oracle.BAG_SUM, per_sample_weights=w,
+                                      padding_idx=0)
+    assert flags == oracle.BAG_FLAG_OOB and _flags(err) == flags
+    _compare(got, ref, dl.BAG_SUM)
+
+
+def test_weights_need_sum_mode_and_matching_index_types():
+    _, tables = _tables((10,), 8, seed=1)
+    idx = cu(np.zeros((1, 4), np.int64))
+    off = cu(np.zeros((1, 2), np.int64))
+    out = torch.empty((2, 1, 8), device="cuda")
+    w = torch.ones((1, 4), device="cuda")
+    for mode in (dl.BAG_MEAN, dl.BAG_MAX):
+        with pytest.raises(dl.DlrmError) as ei:
+            dl.embedding_bag_multi([cu(tables[0])], idx, off, out, mode, per_sample_weights=w)
+        assert ei.value.status == dl.ERR_INVALID_ARG
+    with pytest.raises(ValueError):
+        dl.embedding_bag_multi([cu(tables[0])], idx, off.int(), out, dl.BAG_SUM)
