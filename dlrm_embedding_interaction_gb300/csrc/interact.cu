@@ -23,6 +23,15 @@ namespace {
 
 constexpr int kInteractThreads = 256;
 
+// 16-byte global -> shared copy that does not hold the thread (cp.async), so
+// every row of the block's samples is in flight at once.
+__device__ __forceinline__ void copy16_async(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src)
+               : "memory");
+}
+
 __host__ __device__ __forceinline__ int z_stride(int d) {
   return static_cast<int>(round_up(d, 4)) + 4;
 }
@@ -50,15 +59,13 @@ interaction_kernel(const float* __restrict__ dense, int ld_dense, const float* _
       const int r = e - s * per_sample;
       const int row = r / d4;
       const int c4 = r - row * d4;
-      float4 v;
-      if (row == 0) {
-        v = __ldg(reinterpret_cast<const float4*>(dense + static_cast<int64_t>(b0 + s) * ld_dense) + c4);
-      } else {
-        v = __ldg(reinterpret_cast<const float4*>(emb) +
-                  (static_cast<int64_t>(b0 + s) * k_tables + (row - 1)) * d4 + c4);
-      }
-      *reinterpret_cast<float4*>(zs + (s * f + row) * ldz + c4 * 4) = v;
+      const float4* src =
+          row == 0 ? reinterpret_cast<const float4*>(dense + static_cast<int64_t>(b0 + s) * ld_dense) + c4
+                   : reinterpret_cast<const float4*>(emb) +
+                         (static_cast<int64_t>(b0 + s) * k_tables + (row - 1)) * d4 + c4;
+      copy16_async(zs + (s * f + row) * ldz + c4 * 4, src);
     }
+    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
   } else {
     const int per_sample = f * d;
     for (int e = tid; e < ns * per_sample; e += blockDim.x) {
