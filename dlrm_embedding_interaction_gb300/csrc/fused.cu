@@ -1,9 +1,11 @@
 // Fused single-launch DLRMv1 forward (fp32).
 //
-// One CTA runs the whole forward for a tile of BM samples (Luminal compare
+// A CTA runs the whole forward for a tile of BM samples (Luminal compare
 // dlrm-fused-kernels...dlrm-pt2-megakernel, dlrm_megakernel.rs steps 1-6:
 // bottom Linear+ReLU on every layer, lookups, i-major pairwise dots with
-// Vec[0] = x, R = [x, z], top Linear+ReLU then Linear+sigmoid).
+// Vec[0] = x, R = [x, z], top Linear+ReLU then Linear+sigmoid). The launch is
+// persistent: at most one CTA per SM, each taking tiles c, c + grid, ... in
+// turn while the weight stream flows on through the same ring.
 //
 // The pages' megakernel keeps one batch row per thread with activations in
 // registers; at 512-wide layers that cannot hold. Here the tile's activations
@@ -17,15 +19,18 @@
 //    producer warp that each copy a quarter of every stage (one thread's
 //    copies are serialised), running ahead across layer boundaries while
 //    eight warps compute.
-//  * a computing warp owns TM = 8 rows (4 for 4-row tiles), broadcast-read
-//    from the activation buffer, and 32 * TN columns (one column per lane,
-//    TN per thread) of one 16-wide k-slice of each stage; the register tile
-//    (8 x 4 at 16 rows) accumulates with packed fma.rn.f32x2, and the
-//    k-slices' partial sums meet in shared memory.
-//  * biases, the last layer's weights and (bag size 1) the tile's embedding
-//    rows are fetched with cp.async at kernel start and land during the
-//    bottom MLP; bag sums and pair dots then run from shared memory and build
-//    R = [x, z] in place; the N = 1 sigmoid layer is a warp-per-row dot.
+//  * a computing warp owns TM rows (the whole tile up to 8 rows, else half
+//    of it: 7 at 14-row tiles), broadcast-read from the activation buffer,
+//    and 32 * TN columns (one column per lane, TN per thread) of one 16-wide
+//    k-slice of each stage; the register tile (7 x 4 at 14 rows)
+//    accumulates with packed fma.rn.f32x2, and the k-slices' partial sums
+//    meet in shared memory.
+//  * biases and the last layer's weights are fetched with cp.async once per
+//    CTA; per tile, one round of global loads checks the bags and fetches
+//    the dense rows, and (bag size 1) the tile's embedding rows follow by
+//    cp.async and land during the bottom MLP; bag sums and pair dots then run
+//    from shared memory and build R = [x, z] in place; the N = 1 sigmoid
+//    layer is a warp-per-row dot.
 // Every mbarrier wait is bounded (%globaltimer, 2 s): on expiry the kernel
 // sets DLRM_ERRBIT_TIMEOUT, stops waiting and finishes its control flow;
 // before exiting it waits (bounded) for any copies still in flight.

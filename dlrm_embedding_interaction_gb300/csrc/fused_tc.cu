@@ -22,9 +22,11 @@
 //    swizzled K-major layout, ping-ponging between two buffers.
 //  * four epilogue warps (one per 32-lane quarter of tensor memory) read
 //    the accumulators with tcgen05.ld, add the bias, apply ReLU and write the
-//    next layer's operand; they also fetch the tile's bag rows at kernel
-//    start, compute the pair dots into R (fp32, from an fp32 copy of x) and
-//    the last layer's fp32 dot and sigmoid.
+//    next layer's operand; at kernel start they check the bags and write the
+//    dense rows as layer 0's operand in one round of global loads, signal the
+//    MMA warp, then fetch the bag rows (cp.async for bags of one row, sums in
+//    registers for longer bags); they compute the pair dots into R (fp32,
+//    from an fp32 copy of x) and the last layer's fp32 dot and sigmoid.
 // Every wait is bounded (%globaltimer, 2 s): on expiry the kernel sets
 // DLRM_ERRBIT_TIMEOUT, stops issuing and waiting, and still frees its tensor
 // memory and waits (bounded) for its copies in flight.
