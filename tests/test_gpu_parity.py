@@ -438,7 +438,33 @@ def test_forward_flags_non_uniform_offsets_and_zeroes_the_bag(path):
     model.close()
 
 
-@pytest.mark.parametrize("name", ["b2048_k3", "sweep_b300_k8", "sweep_b8_k1"])
+def test_persistent_fused_takes_several_tiles_per_cta_with_long_bags():
+    """The fused plan on bags of two rows at 6000 samples: every CTA of the
+    persistent launch takes several tiles (bag sums gathered in the kernel)."""
+    cfg = synth.get_config("tiny_b64_k3").with_batch(6000)
+    inp = synth.make_inputs(cfg, seed=5)
+    model = make_model(cfg, inp, path=dl.PATH_FUSED)
+    close(run_forward(model, inp), oracle.forward(inp))
+    model.close()
+
+
+def test_persistent_fused_flags_a_bad_index_in_a_late_tile():
+    """An out-of-range index in the last tile of a CTA with several tiles is flagged,
+    contributes zeros, and leaves every other sample exact."""
+    cfg = synth.get_config("sweep_b8192_k3")
+    inp = synth.make_inputs(cfg, seed=6)
+    model = make_model(cfg, inp, path=dl.PATH_FUSED)
+    idx = inp["indices"].copy()
+    idx[2, 8191] = cfg.rows[2] + 5
+    out = model.forward(cu(inp["dense"]), cu(idx), cu(inp["offsets"])).cpu().numpy()
+    assert model.error() == dl.ERR_INDEX_OOB
+    bad = dict(inp)
+    bad["indices"] = idx
+    close(out, oracle.forward(bad, allow_oob=True))
+    model.close()
+
+
+@pytest.mark.parametrize("name", ["b2048_k3", "sweep_b300_k8", "sweep_b8_k1", "sweep_b8192_k3"])
 def test_fused_phase_trace_is_ordered(name):
     """Per-tile phase stamps of the fused kernel rise phase by phase, and each
     GEMM layer's k-loop stamp falls inside its layer."""
