@@ -9,6 +9,7 @@
 // allocate nothing and never synchronise.
 #include <algorithm>
 #include <atomic>
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -100,6 +101,7 @@ struct dlrm_handle_s {
   std::vector<cudaEvent_t> events;      // stage boundaries, empty when off
   std::vector<double> stage_ms;
   int64_t profiled_calls = 0;
+  bool report_on_destroy = false;   // DLRM_PROFILE=1 at dlrm_create
 };
 
 namespace {
@@ -492,6 +494,16 @@ dlrm_status_t dlrm_create(const dlrm_config_t* cfg, const float* const* tables,
   h->idx_stage = reinterpret_cast<int64_t*>(base + off_idx);
   h->off_stage = reinterpret_cast<int64_t*>(base + off_off);
   h->out_stage = at(off_out);
+  // DLRM_PROFILE=1: per-stage timing from the first forward on, reported on
+  // stderr by dlrm_destroy (the same counters dlrm_stage_times returns)
+  const char* prof = std::getenv("DLRM_PROFILE");
+  if (prof && prof[0] == '1' && prof[1] == '\0') {
+    if (dlrm_set_profiling(h, 1) != DLRM_OK) {
+      dlrm_destroy(h);
+      return DLRM_ERR_CUDA;
+    }
+    h->report_on_destroy = true;
+  }
   *out = h;
   return DLRM_OK;
 }
@@ -630,6 +642,14 @@ int32_t dlrm_stage_times(dlrm_handle_t h, double* total_ms, int32_t capacity, in
 void dlrm_destroy(dlrm_handle_t h) {
   if (!h) return;
   cudaDeviceSynchronize();
+  if (h->report_on_destroy && h->profiled_calls > 0) {
+    std::fprintf(stderr, "dlrm profile: %lld forward calls, %s plan; mean ms per call:\n",
+                 static_cast<long long>(h->profiled_calls),
+                 h->path == DLRM_PATH_FUSED ? "fused" : "layer-wise");
+    for (size_t i = 0; i < h->stage_names.size(); ++i)
+      std::fprintf(stderr, "  %-14s %10.4f\n", h->stage_names[i].c_str(),
+                   h->stage_ms[i] / static_cast<double>(h->profiled_calls));
+  }
   destroy_events(h);
   if (h->arena) cudaFree(h->arena);
   delete h;

@@ -185,7 +185,9 @@ const char* dlrm_stage_name(dlrm_handle_t h, int32_t i);
  * its stream, then WAITS for its last event and adds each stage's
  * event-to-event time to a running total; this mode synchronises the host
  * and must not be used inside graph capture. enable = 0 destroys the events
- * and clears the totals. */
+ * and clears the totals. With DLRM_PROFILE=1 in the environment, dlrm_create
+ * turns it on and dlrm_destroy prints the mean time per call of every stage
+ * to stderr. */
 dlrm_status_t dlrm_set_profiling(dlrm_handle_t h, int32_t enable);
 
 /* Phase trace of the fused plan (profiling; off by default). With a non-null

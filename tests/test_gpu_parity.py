@@ -438,6 +438,25 @@ def test_forward_flags_non_uniform_offsets_and_zeroes_the_bag(path):
     model.close()
 
 
+@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
+def test_profile_environment_switch(path, monkeypatch, capfd):
+    """DLRM_PROFILE=1 at create turns per-stage timing on; destroy reports it on stderr."""
+    monkeypatch.setenv("DLRM_PROFILE", "1")
+    cfg = synth.get_config("tiny_b64_k3")
+    inp = synth.make_inputs(cfg, seed=4)
+    model = make_model(cfg, inp, path=path)
+    monkeypatch.delenv("DLRM_PROFILE")
+    for _ in range(3):
+        run_forward(model, inp)
+    names, totals, calls = model.stage_times()
+    assert calls == 3 and len(names) == len(totals) and all(t > 0 for t in totals)
+    model.close()
+    err = capfd.readouterr().err
+    assert "dlrm profile: 3 forward calls" in err
+    for n in names:
+        assert n in err
+
+
 def test_persistent_fused_takes_several_tiles_per_cta_with_long_bags():
     """The fused plan on bags of two rows at 6000 samples: every CTA of the
     persistent launch takes several tiles (bag sums gathered in the kernel)."""
