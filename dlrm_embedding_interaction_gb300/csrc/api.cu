@@ -158,46 +158,46 @@ dlrm_status_t run_forward(dlrm_handle_t h, const float* dense, const int64_t* in
     }
     if (e != cudaSuccess || !mark()) return DLRM_ERR_CUDA;
   } else {
-  // [G] bag sums, all tables in one launch
-  e = dlrm::launch_gather(h->tabs, h->k, h->d, indices, offsets, batch, h->bag, h->emb, h->d,
-                          h->err, s);
-  if (e != cudaSuccess || !mark()) return DLRM_ERR_CUDA;
-  // [M1] bottom MLP, ReLU after every layer
-  const float* in = dense;
-  int ld_in = h->n_dense;
-  // GEMMs of the opt-in TF32/BF16 modes run on the tensor cores; the N = 1
-  // sigmoid layer (a dot product per row) stays on the fp32 GEMV.
-  auto linear = [&](const float* x, int ldx, const float* w, int ldw, const float* b, float* y,
-                    int ldy, int n, int k, int act) {
-    if (h->math != DLRM_MATH_FP32 && n >= 16)
-      return dlrm::launch_linear_tc(x, ldx, w, ldw, b, y, ldy, batch, n, k, act,
-                                    static_cast<int>(h->math), h->err, s);
-    return dlrm::launch_linear_fp32(x, ldx, w, ldw, b, y, ldy, batch, n, k, act, s);
-  };
-  for (int l = 0; l < h->n_bot; ++l) {
-    float* o = h->act[l & 1];
-    e = linear(in, ld_in, h->bot_w[l], h->bot_ldw[l], h->bot_b[l], o, h->ld_act,
-               h->ln_bot[l + 1], h->ln_bot[l], DLRM_ACT_RELU);
+    // [G] bag sums, all tables in one launch
+    e = dlrm::launch_gather(h->tabs, h->k, h->d, indices, offsets, batch, h->bag, h->emb,
+                            h->err, s);
     if (e != cudaSuccess || !mark()) return DLRM_ERR_CUDA;
-    in = o;
-    ld_in = h->ld_act;
-  }
-  // [I] interaction; R = [x, z]
-  e = dlrm::launch_interaction(in, ld_in, h->emb, batch, h->k, h->d, h->r, h->ld_r, 1, s);
-  if (e != cudaSuccess || !mark()) return DLRM_ERR_CUDA;
-  // [M2] top MLP: ReLU, ..., sigmoid into out
-  in = h->r;
-  ld_in = h->ld_r;
-  for (int l = 0; l < h->n_top; ++l) {
-    const bool last = (l == h->n_top - 1);
-    float* o = last ? out : h->act[l & 1];
-    const int ld_o = last ? 1 : h->ld_act;
-    e = linear(in, ld_in, h->top_w[l], h->top_ldw[l], h->top_b[l], o, ld_o, h->ln_top[l + 1],
-               h->ln_top[l], last ? DLRM_ACT_SIGMOID : DLRM_ACT_RELU);
+    // [M1] bottom MLP, ReLU after every layer
+    const float* in = dense;
+    int ld_in = h->n_dense;
+    // GEMMs of the opt-in TF32/BF16 modes run on the tensor cores; the N = 1
+    // sigmoid layer (a dot product per row) stays on the fp32 GEMV.
+    auto linear = [&](const float* x, int ldx, const float* w, int ldw, const float* b, float* y,
+                      int ldy, int n, int k, int act) {
+      if (h->math != DLRM_MATH_FP32 && n >= 16)
+        return dlrm::launch_linear_tc(x, ldx, w, ldw, b, y, ldy, batch, n, k, act,
+                                      static_cast<int>(h->math), h->err, s);
+      return dlrm::launch_linear_fp32(x, ldx, w, ldw, b, y, ldy, batch, n, k, act, s);
+    };
+    for (int l = 0; l < h->n_bot; ++l) {
+      float* o = h->act[l & 1];
+      e = linear(in, ld_in, h->bot_w[l], h->bot_ldw[l], h->bot_b[l], o, h->ld_act,
+                 h->ln_bot[l + 1], h->ln_bot[l], DLRM_ACT_RELU);
+      if (e != cudaSuccess || !mark()) return DLRM_ERR_CUDA;
+      in = o;
+      ld_in = h->ld_act;
+    }
+    // [I] interaction; R = [x, z]
+    e = dlrm::launch_interaction(in, ld_in, h->emb, batch, h->k, h->d, h->r, h->ld_r, 1, s);
     if (e != cudaSuccess || !mark()) return DLRM_ERR_CUDA;
-    in = o;
-    ld_in = ld_o;
-  }
+    // [M2] top MLP: ReLU, ..., sigmoid into out
+    in = h->r;
+    ld_in = h->ld_r;
+    for (int l = 0; l < h->n_top; ++l) {
+      const bool last = (l == h->n_top - 1);
+      float* o = last ? out : h->act[l & 1];
+      const int ld_o = last ? 1 : h->ld_act;
+      e = linear(in, ld_in, h->top_w[l], h->top_ldw[l], h->top_b[l], o, ld_o, h->ln_top[l + 1],
+                 h->ln_top[l], last ? DLRM_ACT_SIGMOID : DLRM_ACT_RELU);
+      if (e != cudaSuccess || !mark()) return DLRM_ERR_CUDA;
+      in = o;
+      ld_in = ld_o;
+    }
   }  // layer-wise
   if (prof) {
     if (cudaEventSynchronize(h->events.back()) != cudaSuccess) return DLRM_ERR_CUDA;
@@ -671,7 +671,7 @@ dlrm_status_t embedding_bag_sum_multi(const float* const* tables, const int64_t*
     tabs.ptr[t] = tables[t];
     tabs.rows[t] = rows[t];
   }
-  return cuda_status(dlrm::launch_gather(tabs, K, D, indices, offsets, B, L, out, D, err_flag,
+  return cuda_status(dlrm::launch_gather(tabs, K, D, indices, offsets, B, L, out, err_flag,
                                          static_cast<cudaStream_t>(stream)));
 }
 

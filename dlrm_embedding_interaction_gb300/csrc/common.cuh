@@ -95,8 +95,8 @@ struct GatherTables {
 // ---- launchers (each returns cudaGetLastError() of its launch) ----------
 
 cudaError_t launch_gather(const GatherTables& tabs, int k, int d, const int64_t* indices,
-                          const int64_t* offsets, int b, int l, float* out, int ld_out_row,
-                          int32_t* err_flag, cudaStream_t stream);
+                          const int64_t* offsets, int b, int l, float* out, int32_t* err_flag,
+                          cudaStream_t stream);
 cudaError_t launch_gather_general(const GatherTables& tabs, int k, int d, const void* indices,
                                   int64_t n_idx, const void* offsets, int index_bits, int b,
                                   int mode, const float* per_sample_weights, int64_t padding_idx,

@@ -295,8 +295,8 @@ cudaError_t launch_general(const GatherTables& tabs, int k, int d, const IDX* in
 }  // namespace
 
 cudaError_t launch_gather(const GatherTables& tabs, int k, int d, const int64_t* indices,
-                          const int64_t* offsets, int b, int l, float* out, int /*unused*/,
-                          int32_t* err, cudaStream_t stream) {
+                          const int64_t* offsets, int b, int l, float* out, int32_t* err,
+                          cudaStream_t stream) {
   if (b == 0) return cudaSuccess;
   return launch_any<DLRM_BAG_SUM, false, int64_t>(tabs, k, d, indices, offsets, nullptr, -1, b, l,
                                                   static_cast<int64_t>(b) * l, out, err, stream);

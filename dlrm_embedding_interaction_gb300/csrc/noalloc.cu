@@ -98,7 +98,7 @@ extern "C" dlrm_status_t dlrm_forward_noalloc(
   float* r = reinterpret_cast<float*>(base + off_r);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-  if (dlrm::launch_gather(tabs, k, d, indices, offsets, batch, bag, emb, d, err_flag, s) !=
+  if (dlrm::launch_gather(tabs, k, d, indices, offsets, batch, bag, emb, err_flag, s) !=
       cudaSuccess)
     return DLRM_ERR_CUDA;
   const float* in = dense;
