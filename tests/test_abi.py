@@ -105,3 +105,65 @@ def test_forward_rejects_null_handle(lib):
     assert lib.dlrm_get_error(null, null) == dl.ERR_INVALID_ARG
     assert lib.dlrm_workspace_bytes(null) == 0
     lib.dlrm_destroy(null)
+
+
+def test_bag_calls_check_arguments_on_the_host(lib):
+    """embedding_bag_multi(_ex) refuse bad shapes, modes, index widths and weight use
+    before any launch; a batch of zero returns at once."""
+    vp = ctypes.c_void_p
+    null = vp(0)
+    tabs = (vp * 2)(vp(16), vp(16))
+    rows = (ctypes.c_int64 * 2)(10, 10)
+    f = lib.embedding_bag_multi
+    f.argtypes = [vp, vp, ctypes.c_int32, ctypes.c_int32, vp, ctypes.c_int64, vp,
+                  ctypes.c_int32, ctypes.c_int32, vp, vp, vp]
+    assert f(tabs, rows, 0, 8, null, 4, null, 2, 0, null, null, null) == dl.ERR_INVALID_ARG
+    assert f(tabs, rows, 2, 0, null, 4, null, 2, 0, null, null, null) == dl.ERR_INVALID_ARG
+    assert f(tabs, rows, 2, 8, null, -1, null, 2, 0, null, null, null) == dl.ERR_INVALID_ARG
+    assert f(tabs, rows, 2, 8, null, 4, null, -1, 0, null, null, null) == dl.ERR_INVALID_ARG
+    assert f(tabs, rows, 2, 8, null, 4, null, 2, 3, null, null, null) == dl.ERR_INVALID_ARG
+    assert f(tabs, rows, 129, 8, null, 4, null, 2, 0, null, null, null) == dl.ERR_UNSUPPORTED
+    assert f(null, rows, 2, 8, null, 4, null, 2, 0, null, null, null) == dl.ERR_INVALID_ARG
+    assert f(tabs, rows, 2, 8, null, 4, null, 2, 0, null, null, null) == dl.ERR_INVALID_ARG
+    assert f(tabs, rows, 2, 8, null, 4, null, 0, 0, null, null, null) == dl.OK
+    g = lib.embedding_bag_multi_ex
+    g.argtypes = [vp, vp, ctypes.c_int32, ctypes.c_int32, vp, ctypes.c_int64, vp,
+                  ctypes.c_int32, ctypes.POINTER(dl._BagOptions), vp, vp, vp]
+    g.restype = ctypes.c_int
+
+    def ex(mode, bits, weights, n_idx=4, b=2):
+        opt = dl._BagOptions(mode, bits, weights, -1)
+        return g(tabs, rows, 2, 8, null, n_idx, null, b, ctypes.byref(opt), null, null, null)
+
+    assert g(tabs, rows, 2, 8, null, 4, null, 2, None, null, null, null) == dl.ERR_INVALID_ARG
+    assert ex(0, 16, None) == dl.ERR_INVALID_ARG
+    assert ex(1, 64, 16) == dl.ERR_INVALID_ARG          # weights with mean
+    assert ex(2, 32, 16) == dl.ERR_INVALID_ARG          # weights with max
+    assert ex(0, 32, None, n_idx=1 << 31) == dl.ERR_INVALID_ARG
+    assert ex(0, 32, 16, b=0) == dl.OK
+
+
+def test_header_is_plain_c_and_links(tmp_path, lib):
+    """include/dlrm.h compiles as C11 and a C program links against the library."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use.c"
+    src.write_text(
+        '#include "dlrm.h"\n'
+        "int main(void) {\n"
+        "  dlrm_bag_options_t o = {DLRM_BAG_MEAN, 64, 0, -1};\n"
+        "  (void)o;\n"
+        "  return dlrm_version() == 100 ? 0 : 1;\n"
+        "}\n")
+    cuda_inc = "/usr/local/cuda/include"
+    exe = tmp_path / "use"
+    libdir = os.path.dirname(dl.LIB_PATH)
+    r = subprocess.run([cc, "-std=c11", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        "-I", cuda_inc, str(src), "-o", str(exe), "-L", libdir, "-ldlrm_gb300",
+                        f"-Wl,-rpath,{libdir}"], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert run.returncode == 0, run.stderr
