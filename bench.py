@@ -263,11 +263,6 @@ def stage_work(cfg, name, batch):
         return batch * k * (l - 1) * d, byts
     if name == "interaction":
         return 2 * batch * p * d, batch * f * d * 4 + batch * (d + p) * 4
-    if name == "gather_interaction":
-        # rows, indices and offsets read, x read, R = [x, z] written
-        byts = (batch * k * l * d * 4 + batch * k * l * 8 + batch * k * 8 + batch * d * 4
-                + batch * (d + p) * 4)
-        return batch * k * (l - 1) * d + 2 * batch * p * d, byts
     if name == "fused":
         return forward_work(cfg, batch)
     widths = cfg.ln_bot if name.startswith("bottom") else cfg.ln_top
@@ -583,8 +578,7 @@ def run_ours(args, rank, world, local_rank):
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     fp32_peak = sms * FP32_LANES_PER_SM * 2 * pk["sm_max_mhz"] * 1e6 / 1e12
     t_dom = stage_us[dom] * 1e-6
-    if (dom in ("gather", "interaction", "gather_interaction")
-            and byts / (pk["hbm_gbs"] * 1e9) >= flops / (fp32_peak * 1e12)):
+    if dom in ("gather", "interaction") and byts / (pk["hbm_gbs"] * 1e9) >= flops / (fp32_peak * 1e12):
         ach = byts / t_dom / 1e9
         roof = dict(bound="hbm", achieved=ach, peak=pk["hbm_gbs"], unit="GB/s",
                     frac=ach / pk["hbm_gbs"], traffic=None, kernel=dom,

@@ -94,7 +94,6 @@ struct dlrm_handle_s {
   int fused_bm = 0;
   dlrm::FusedParams fused{};     // per-call fields filled by run_forward
   bool fused_tc = false;         // the fused plan runs on the tensor cores (TF32 / BF16)
-  bool gather_interact = false;  // layer-wise: bag sums and interaction in one launch
   dlrm::FusedTcParams tcp{};
   unsigned long long* trace = nullptr;
   // per-stage profiling (dlrm_set_profiling)
@@ -159,12 +158,10 @@ dlrm_status_t run_forward(dlrm_handle_t h, const float* dense, const int64_t* in
     }
     if (e != cudaSuccess || !mark()) return DLRM_ERR_CUDA;
   } else {
-    // [G] bag sums, all tables in one launch (unless fused with [I] below)
-    if (!h->gather_interact) {
-      e = dlrm::launch_gather(h->tabs, h->k, h->d, indices, offsets, batch, h->bag, h->emb,
-                              h->err, s);
-      if (e != cudaSuccess || !mark()) return DLRM_ERR_CUDA;
-    }
+    // [G] bag sums, all tables in one launch
+    e = dlrm::launch_gather(h->tabs, h->k, h->d, indices, offsets, batch, h->bag, h->emb,
+                            h->err, s);
+    if (e != cudaSuccess || !mark()) return DLRM_ERR_CUDA;
     // [M1] bottom MLP, ReLU after every layer
     const float* in = dense;
     int ld_in = h->n_dense;
@@ -185,12 +182,8 @@ dlrm_status_t run_forward(dlrm_handle_t h, const float* dense, const int64_t* in
       in = o;
       ld_in = h->ld_act;
     }
-    // [I] interaction; R = [x, z] (with the bag sums [G] in the same launch)
-    if (h->gather_interact)
-      e = dlrm::launch_gather_interaction(h->tabs, h->k, h->d, indices, offsets, batch, h->bag,
-                                          in, ld_in, h->r, h->ld_r, h->err, s);
-    else
-      e = dlrm::launch_interaction(in, ld_in, h->emb, batch, h->k, h->d, h->r, h->ld_r, 1, s);
+    // [I] interaction; R = [x, z]
+    e = dlrm::launch_interaction(in, ld_in, h->emb, batch, h->k, h->d, h->r, h->ld_r, 1, s);
     if (e != cudaSuccess || !mark()) return DLRM_ERR_CUDA;
     // [M2] top MLP: ReLU, ..., sigmoid into out
     in = h->r;
@@ -372,12 +365,6 @@ dlrm_status_t dlrm_create(const dlrm_config_t* cfg, const float* const* tables,
   }
   if (h->path == DLRM_PATH_FUSED) {
     h->stage_names.push_back("fused");
-  } else if (dlrm::gather_interaction_fits(h->tabs, h->k, h->d)) {
-    // the bottom MLP first, then the bag sums and interaction in one launch
-    h->gather_interact = true;
-    for (int l = 0; l < h->n_bot; ++l) h->stage_names.push_back("bottom" + std::to_string(l));
-    h->stage_names.push_back("gather_interaction");
-    for (int l = 0; l < h->n_top; ++l) h->stage_names.push_back("top" + std::to_string(l));
   } else {
     h->stage_names.push_back("gather");
     for (int l = 0; l < h->n_bot; ++l) h->stage_names.push_back("bottom" + std::to_string(l));
@@ -407,9 +394,7 @@ dlrm_status_t dlrm_create(const dlrm_config_t* cfg, const float* const* tables,
     off_tw[l] = plan.take<float>(static_cast<size_t>(h->ln_top[l + 1]) * h->top_ldw[l]);
     off_tb[l] = plan.take<float>(h->ln_top[l + 1]);
   }
-  // (B, K, D) bag sums: only the layer-wise plan with separate launches needs them
-  const bool need_emb = h->path != DLRM_PATH_FUSED && !h->gather_interact;
-  const size_t off_emb = plan.take<float>(need_emb ? mb * h->k * h->d : 0);
+  const size_t off_emb = plan.take<float>(mb * h->k * h->d);
   const size_t off_a0 = plan.take<float>(mb * h->ld_act);
   const size_t off_a1 = plan.take<float>(mb * h->ld_act);
   const size_t off_r = plan.take<float>(mb * h->ld_r);

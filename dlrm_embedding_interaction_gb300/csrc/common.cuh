@@ -97,15 +97,6 @@ struct GatherTables {
 cudaError_t launch_gather(const GatherTables& tabs, int k, int d, const int64_t* indices,
                           const int64_t* offsets, int b, int l, float* out, int32_t* err_flag,
                           cudaStream_t stream);
-// The layer-wise plan's bag sums and interaction in one launch. It fits D a
-// multiple of 4 up to 512 with 16-byte aligned tables and one sample's rows
-// within shared memory; x and out must be 16-byte aligned with row strides
-// that are multiples of 4 floats.
-bool gather_interaction_fits(const GatherTables& tabs, int k, int d);
-cudaError_t launch_gather_interaction(const GatherTables& tabs, int k, int d,
-                                      const int64_t* indices, const int64_t* offsets, int b,
-                                      int l, const float* x, int ld_x, float* out, int ld_out,
-                                      int32_t* err, cudaStream_t stream);
 cudaError_t launch_gather_general(const GatherTables& tabs, int k, int d, const void* indices,
                                   int64_t n_idx, const void* offsets, int index_bits, int b,
                                   int mode, const float* per_sample_weights, int64_t padding_idx,

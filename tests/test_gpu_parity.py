@@ -263,26 +263,6 @@ def test_forward_odd_widths_matches_oracle(path):
     model.close()
 
 
-def test_layerwise_plan_forms():
-    """The layer-wise plan sums bags inside the interaction launch when D is a
-    multiple of 4 (stages bottom.., gather_interaction, top..), and keeps the
-    separate gather and interaction launches otherwise (D = 6 here); both match
-    the oracle."""
-    for d, want in ((16, "gather_interaction"), (6, "interaction")):
-        f = 4
-        cfg = synth.DlrmConfig(f"lw_d{d}", 300, (13, 32, d), (500, 400, 300), d, 3,
-                               (d + f * (f - 1) // 2, 24, 1), 0.05)
-        inp = synth.make_inputs(cfg, seed=d)
-        model = make_model(cfg, inp, path=dl.PATH_LAYERWISE)
-        names = model.stage_names()
-        if want == "gather_interaction":
-            assert names == ["bottom0", "bottom1", "gather_interaction", "top0", "top1"]
-        else:
-            assert names == ["gather", "bottom0", "bottom1", "interaction", "top0", "top1"]
-        close(run_forward(model, inp), oracle.forward(inp))
-        model.close()
-
-
 def test_auto_path_picks_fused_for_the_2048_sample_workload():
     cfg = synth.get_config("b2048_k3")
     inp = synth.make_inputs(cfg, seed=3)
