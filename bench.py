@@ -73,6 +73,8 @@ def parse_args():
     ap.add_argument("--no-gather", action="store_true",
                     help="skip the 13.3 GB standalone-gather measurement")
     ap.add_argument("--profile-steps", type=int, default=200)
+    ap.add_argument("--path", choices=["auto", "fused", "layerwise"], default="auto",
+                    help="kernel plan of the forward handle (default: the library's choice)")
     ap.add_argument("--only-gather", action="store_true",
                     help="time only the standalone gathers of the 26-table workload "
                          "(uniform bags of 20 and general bags, Zipf and uniform indices)")
@@ -419,10 +421,11 @@ def run_ours(args, rank, world, local_rank):
     cu = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
     math = {"fp32": dl.MATH_FP32, "tf32": dl.MATH_TF32, "bf16": dl.MATH_BF16,
             "tf32x3": dl.MATH_TF32X3}[args.math]
+    plan = {"auto": dl.PATH_AUTO, "fused": dl.PATH_FUSED, "layerwise": dl.PATH_LAYERWISE}[args.path]
     model = dl.DlrmModel(cfg.ln_bot, cfg.ln_top, [cu(t) for t in inp["tables"]],
                          [cu(w) for w in inp["bot_w"]], [cu(b) for b in inp["bot_b"]],
                          [cu(w) for w in inp["top_w"]], [cu(b) for b in inp["top_b"]],
-                         cfg.bag_size, cfg.batch, math)
+                         cfg.bag_size, cfg.batch, math, plan)
     dense, idx, off = cu(inp["dense"]), cu(inp["indices"]), cu(inp["offsets"])
     out = torch.empty(cfg.batch, device=dev)
     flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
