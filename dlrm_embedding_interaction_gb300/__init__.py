@@ -27,7 +27,7 @@ MAX_LAYERS = 16
 EXPORTS = ("dlrm_version", "dlrm_status_string", "dlrm_create", "dlrm_forward",
            "dlrm_forward_host", "dlrm_get_error", "dlrm_workspace_bytes", "dlrm_destroy",
            "dlrm_path", "dlrm_num_stages", "dlrm_stage_name", "dlrm_set_profiling", "dlrm_stage_times",
-           "dlrm_forward_noalloc", "dlrm_set_phase_trace",
+           "dlrm_forward_noalloc", "dlrm_set_phase_trace", "dlrm_plan_query",
            "embedding_bag_sum_multi", "embedding_bag_multi", "embedding_bag_multi_ex",
            "pairwise_dot_lower_tri",
            "pairwise_pair_map", "linear_bias_act")
@@ -57,6 +57,14 @@ class _Config(ctypes.Structure):
                 ("max_batch", ctypes.c_int32), ("math", ctypes.c_int), ("path", ctypes.c_int32)]
 
 
+class _PlanInfo(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int32), ("fused_fits", ctypes.c_int32),
+                ("tensor_core", ctypes.c_int32), ("tile_samples", ctypes.c_int32),
+                ("tiles", ctypes.c_int64), ("grid", ctypes.c_int32),
+                ("smem_bytes", ctypes.c_int32), ("ring_stages", ctypes.c_int32),
+                ("stream_copies", ctypes.c_int32), ("stream_bytes", ctypes.c_int64)]
+
+
 def _bind(lib):
     vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
     st = ctypes.c_int
@@ -77,6 +85,7 @@ def _bind(lib):
         "dlrm_forward_noalloc": ([ctypes.POINTER(_Config), vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                   i32, vp, vp], st),
         "dlrm_set_phase_trace": ([vp, vp, i64, ctypes.POINTER(i32)], st),
+        "dlrm_plan_query": ([ctypes.POINTER(_Config), i32, i64, ctypes.POINTER(_PlanInfo)], st),
         "embedding_bag_sum_multi": ([vp, vp, i32, i32, vp, vp, i32, i32, vp, vp, vp], st),
         "embedding_bag_multi": ([vp, vp, i32, i32, vp, i64, vp, i32, i32, vp, vp, vp], st),
         "embedding_bag_multi_ex": ([vp, vp, i32, i32, vp, i64, vp, i32,
@@ -309,6 +318,30 @@ def dlrm_create(ln_bot: Sequence[int], ln_top: Sequence[int], tables: Sequence,
     _check(lib().dlrm_create(ctypes.byref(cfg), arr(tables), arr(bot_w), arr(bot_b),
                              arr(top_w), arr(top_b), ctypes.byref(h)), "dlrm_create")
     return h.value
+
+
+GB300_SMS = 152
+GB300_SMEM_PER_BLOCK = 232448
+
+
+def dlrm_plan_query(ln_bot: Sequence[int], ln_top: Sequence[int], rows: Sequence[int],
+                    emb_dim: int, bag_size: int, max_batch: int, math: int = MATH_FP32,
+                    path: int = PATH_AUTO, sm_count: int = GB300_SMS,
+                    smem_per_block: int = GB300_SMEM_PER_BLOCK) -> dict:
+    """The plan ``dlrm_create`` would take for this model on a device with
+    ``sm_count`` SMs and ``smem_per_block`` bytes of opt-in shared memory per
+    block (a GB300's by default), as a dict of the header's plan fields.
+    Host-only: no device and no weights are needed."""
+    k = len(rows)
+    lb = (ctypes.c_int32 * len(ln_bot))(*ln_bot)
+    lt = (ctypes.c_int32 * len(ln_top))(*ln_top)
+    rw = (ctypes.c_int64 * k)(*rows)
+    cfg = _Config(len(ln_bot) - 1, lb, k, rw, emb_dim, len(ln_top) - 1, lt, bag_size, max_batch,
+                  math, path)
+    info = _PlanInfo()
+    _check(lib().dlrm_plan_query(ctypes.byref(cfg), sm_count, smem_per_block, ctypes.byref(info)),
+           "dlrm_plan_query")
+    return {name: getattr(info, name) for name, _ in _PlanInfo._fields_}
 
 
 def dlrm_forward(h: int, dense, indices, offsets, out, stream=None) -> None:

@@ -241,6 +241,104 @@ bool host_params(dlrm_handle_t h, const float* const* bot_w, const float* const*
   return true;
 }
 
+// validate() shape rules ([P4] dlrm_megakernel.rs) and the library's own
+// limits, on the config alone: at least one layer each side, widths chain,
+// ln_bot.last() = m_spa, ln_top[0] = m_spa + n_pairs, ln_top.last() = 1.
+dlrm_status_t check_config(const dlrm_config_t* cfg, size_t smem_limit) {
+  if (!cfg->ln_bot || !cfg->ln_top || !cfg->rows) return DLRM_ERR_INVALID_ARG;
+  if (cfg->n_bot < 1 || cfg->n_top < 1) return DLRM_ERR_INVALID_ARG;
+  if (cfg->n_bot > DLRM_MAX_LAYERS || cfg->n_top > DLRM_MAX_LAYERS) return DLRM_ERR_UNSUPPORTED;
+  if (cfg->n_tables < 1 || cfg->emb_dim < 1 || cfg->bag_size < 1 || cfg->max_batch < 1)
+    return DLRM_ERR_INVALID_ARG;
+  if (cfg->n_tables > DLRM_MAX_TABLES) return DLRM_ERR_UNSUPPORTED;
+  for (int l = 0; l <= cfg->n_bot; ++l) if (cfg->ln_bot[l] < 1) return DLRM_ERR_INVALID_ARG;
+  for (int l = 0; l <= cfg->n_top; ++l) if (cfg->ln_top[l] < 1) return DLRM_ERR_INVALID_ARG;
+  const int64_t f = cfg->n_tables + 1;
+  const int64_t p = f * (f - 1) / 2;
+  if (cfg->ln_bot[cfg->n_bot] != cfg->emb_dim) return DLRM_ERR_INVALID_ARG;
+  if (cfg->ln_top[0] != cfg->emb_dim + p) return DLRM_ERR_INVALID_ARG;
+  if (cfg->ln_top[cfg->n_top] != 1) return DLRM_ERR_INVALID_ARG;
+  for (int t = 0; t < cfg->n_tables; ++t) if (cfg->rows[t] < 1) return DLRM_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(cfg->max_batch) * cfg->bag_size > (int64_t(1) << 31))
+    return DLRM_ERR_UNSUPPORTED;
+  if (cfg->math != DLRM_MATH_FP32 && cfg->math != DLRM_MATH_TF32 &&
+      cfg->math != DLRM_MATH_BF16 && cfg->math != DLRM_MATH_TF32X3)
+    return DLRM_ERR_INVALID_ARG;
+  if (cfg->path != DLRM_PATH_AUTO && cfg->path != DLRM_PATH_LAYERWISE &&
+      cfg->path != DLRM_PATH_FUSED)
+    return DLRM_ERR_INVALID_ARG;
+  // fused plans: fp32 (SIMT) and the TF32 / BF16 tensor-core modes; TF32X3 is
+  // layer-wise only
+  if (cfg->math == DLRM_MATH_TF32X3 && cfg->path == DLRM_PATH_FUSED) return DLRM_ERR_UNSUPPORTED;
+  if (dlrm::interaction_smem_per_sample(cfg->n_tables, cfg->emb_dim) > smem_limit)
+    return DLRM_ERR_UNSUPPORTED;
+  return DLRM_OK;
+}
+
+bool tensor_core_math(int math) { return math == DLRM_MATH_TF32 || math == DLRM_MATH_BF16; }
+
+// The fused planner is consulted unless the layer-wise plan was asked for or
+// the math has no fused kernel (TF32X3).
+bool wants_fused_plan(const dlrm_config_t* cfg) {
+  return cfg->path != DLRM_PATH_LAYERWISE &&
+         (cfg->math == DLRM_MATH_FP32 || tensor_core_math(cfg->math));
+}
+
+struct PlanChoice {
+  int path = DLRM_PATH_LAYERWISE;
+  bool fused_fits = false;
+  bool fused_tc = false;    // the fused plan runs on the tensor cores
+  int fused_bm = 0;         // samples per fused tile
+  int64_t tiles = 0;        // fused tiles of max_batch
+};
+
+// The kernel plan of a checked config, from host copies of the weights and
+// biases (bottom layers then top; their values only fill the packed images)
+// and the device's SM count and opt-in shared memory per block. The same
+// call serves dlrm_create and dlrm_plan_query.
+dlrm_status_t choose_plan(const dlrm_config_t* cfg, const std::vector<std::vector<float>>& hw,
+                          const std::vector<std::vector<float>>& hb,
+                          const dlrm::GatherTables& tabs, int sms, size_t smem_limit,
+                          dlrm::FusedPlan* fplan, dlrm::FusedTcPlan* tplan, PlanChoice* c) {
+  *c = PlanChoice{};
+  const std::vector<int> ln_bot(cfg->ln_bot, cfg->ln_bot + cfg->n_bot + 1);
+  const std::vector<int> ln_top(cfg->ln_top, cfg->ln_top + cfg->n_top + 1);
+  const bool tc_math = tensor_core_math(cfg->math);
+  if (wants_fused_plan(cfg)) {
+    if (tc_math) {
+      c->fused_fits = dlrm::fused_tc_plan(ln_bot[0], cfg->n_tables, cfg->emb_dim, cfg->bag_size,
+                                          ln_bot, ln_top, hw, hb, tabs,
+                                          static_cast<int>(cfg->math), smem_limit, tplan);
+      c->fused_tc = c->fused_fits;
+      c->fused_bm = dlrm::kTcTile;
+    } else {
+      const int cw = 8;   // computing warps of the fused kernel
+      c->fused_fits = dlrm::fused_plan(ln_bot[0], cfg->n_tables, cfg->emb_dim, cfg->bag_size,
+                                       ln_bot, ln_top, hw, hb, tabs, cfg->max_batch, sms,
+                                       smem_limit, cw, fplan);
+      c->fused_bm = fplan->bm;
+    }
+  }
+  c->tiles = c->fused_fits ? (cfg->max_batch + c->fused_bm - 1) / c->fused_bm : 0;
+  if (cfg->path == DLRM_PATH_FUSED) {
+    if (!c->fused_fits) return DLRM_ERR_UNSUPPORTED;
+    c->path = DLRM_PATH_FUSED;
+  } else if (cfg->path == DLRM_PATH_AUTO) {
+    // The fp32 fused kernel is persistent and beats the layer-wise launches at
+    // every batch when bags hold one row (8192 samples: 171 vs 238 us); with
+    // longer bags, gathered one row at a time inside the kernel, and for the
+    // tensor-core kernel (one CTA per tile), it is kept to two waves of tiles.
+    const bool persistent = !tc_math && cfg->bag_size == 1;
+    c->path = (c->fused_fits && (persistent || c->tiles <= 2 * static_cast<int64_t>(sms)))
+                  ? DLRM_PATH_FUSED
+                  : DLRM_PATH_LAYERWISE;
+  } else {
+    c->path = DLRM_PATH_LAYERWISE;
+  }
+  if (c->path != DLRM_PATH_FUSED) c->fused_tc = false;
+  return DLRM_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -267,36 +365,11 @@ dlrm_status_t dlrm_create(const dlrm_config_t* cfg, const float* const* tables,
   if (!out) return DLRM_ERR_INVALID_ARG;
   *out = nullptr;
   if (!cfg || !tables || !bot_w || !bot_b || !top_w || !top_b) return DLRM_ERR_INVALID_ARG;
-  if (!cfg->ln_bot || !cfg->ln_top || !cfg->rows) return DLRM_ERR_INVALID_ARG;
-  // validate(): at least one layer each side, widths chain, ln_bot.last() = m_spa,
-  // ln_top[0] = m_spa + n_pairs, ln_top.last() = 1, batch > 0.
-  if (cfg->n_bot < 1 || cfg->n_top < 1) return DLRM_ERR_INVALID_ARG;
-  if (cfg->n_bot > DLRM_MAX_LAYERS || cfg->n_top > DLRM_MAX_LAYERS) return DLRM_ERR_UNSUPPORTED;
-  if (cfg->n_tables < 1 || cfg->emb_dim < 1 || cfg->bag_size < 1 || cfg->max_batch < 1)
-    return DLRM_ERR_INVALID_ARG;
-  if (cfg->n_tables > DLRM_MAX_TABLES) return DLRM_ERR_UNSUPPORTED;
-  for (int l = 0; l <= cfg->n_bot; ++l) if (cfg->ln_bot[l] < 1) return DLRM_ERR_INVALID_ARG;
-  for (int l = 0; l <= cfg->n_top; ++l) if (cfg->ln_top[l] < 1) return DLRM_ERR_INVALID_ARG;
-  const int64_t f = cfg->n_tables + 1;
-  const int64_t p = f * (f - 1) / 2;
-  if (cfg->ln_bot[cfg->n_bot] != cfg->emb_dim) return DLRM_ERR_INVALID_ARG;
-  if (cfg->ln_top[0] != cfg->emb_dim + p) return DLRM_ERR_INVALID_ARG;
-  if (cfg->ln_top[cfg->n_top] != 1) return DLRM_ERR_INVALID_ARG;
-  for (int t = 0; t < cfg->n_tables; ++t)
-    if (!tables[t] || cfg->rows[t] < 1) return DLRM_ERR_INVALID_ARG;
+  const dlrm_status_t checked = check_config(cfg, dlrm::device_max_smem_optin());
+  if (checked != DLRM_OK) return checked;
+  for (int t = 0; t < cfg->n_tables; ++t) if (!tables[t]) return DLRM_ERR_INVALID_ARG;
   for (int l = 0; l < cfg->n_bot; ++l) if (!bot_w[l] || !bot_b[l]) return DLRM_ERR_INVALID_ARG;
   for (int l = 0; l < cfg->n_top; ++l) if (!top_w[l] || !top_b[l]) return DLRM_ERR_INVALID_ARG;
-  if (static_cast<int64_t>(cfg->max_batch) * cfg->bag_size > (int64_t(1) << 31))
-    return DLRM_ERR_UNSUPPORTED;
-  if (cfg->math != DLRM_MATH_FP32 && cfg->math != DLRM_MATH_TF32 &&
-      cfg->math != DLRM_MATH_BF16 && cfg->math != DLRM_MATH_TF32X3)
-    return DLRM_ERR_INVALID_ARG;
-  // fused plans: fp32 (SIMT) and the TF32 / BF16 tensor-core modes; TF32X3 is
-  // layer-wise only
-  if (cfg->math == DLRM_MATH_TF32X3 && cfg->path == DLRM_PATH_FUSED) return DLRM_ERR_UNSUPPORTED;
-  if (dlrm::interaction_smem_per_sample(cfg->n_tables, cfg->emb_dim) >
-      dlrm::device_max_smem_optin())
-    return DLRM_ERR_UNSUPPORTED;
 
   dlrm_handle_t h = new (std::nothrow) dlrm_handle_s();
   if (!h) return DLRM_ERR_OOM;
@@ -318,51 +391,23 @@ dlrm_status_t dlrm_create(const dlrm_config_t* cfg, const float* const* tables,
   // Kernel plan.
   dlrm::FusedPlan fplan;
   dlrm::FusedTcPlan tplan;
-  bool fused_fits = false;
-  const bool tc_math = h->math == DLRM_MATH_TF32 || h->math == DLRM_MATH_BF16;
-  if (cfg->path != DLRM_PATH_LAYERWISE && (h->math == DLRM_MATH_FP32 || tc_math)) {
-    std::vector<std::vector<float>> hw, hb;
-    if (!host_params(h, bot_w, bot_b, top_w, top_b, &hw, &hb)) {
-      cudaGetLastError();
-      delete h;
-      return DLRM_ERR_CUDA;
-    }
-    if (tc_math) {
-      fused_fits = dlrm::fused_tc_plan(h->n_dense, h->k, h->d, h->bag, h->ln_bot, h->ln_top, hw,
-                                       hb, h->tabs, static_cast<int>(h->math),
-                                       dlrm::device_max_smem_optin(), &tplan);
-      h->fused_tc = fused_fits;
-      h->fused_bm = dlrm::kTcTile;
-    } else {
-      const int cw = 8;   // computing warps of the fused kernel
-      fused_fits = dlrm::fused_plan(h->n_dense, h->k, h->d, h->bag, h->ln_bot, h->ln_top, hw,
-                                    hb, h->tabs, h->max_batch, dlrm::device_sm_count(),
-                                    dlrm::device_max_smem_optin(), cw, &fplan);
-      h->fused_bm = fplan.bm;
-    }
-  }
-  const int64_t tiles = fused_fits ? (h->max_batch + h->fused_bm - 1) / h->fused_bm : 0;
-  if (cfg->path == DLRM_PATH_FUSED) {
-    if (!fused_fits) {
-      delete h;
-      return DLRM_ERR_UNSUPPORTED;
-    }
-    h->path = DLRM_PATH_FUSED;
-  } else if (cfg->path == DLRM_PATH_AUTO) {
-    // The fp32 fused kernel is persistent and beats the layer-wise launches at
-    // every batch when bags hold one row (8192 samples: 171 vs 238 us); with
-    // longer bags, gathered one row at a time inside the kernel, and for the
-    // tensor-core kernel (one CTA per tile), it is kept to two waves of tiles.
-    const bool persistent = !tc_math && h->bag == 1;
-    h->path = (fused_fits && (persistent || tiles <= 2 * dlrm::device_sm_count()))
-                  ? DLRM_PATH_FUSED
-                  : DLRM_PATH_LAYERWISE;
-  } else if (cfg->path == DLRM_PATH_LAYERWISE) {
-    h->path = DLRM_PATH_LAYERWISE;
-  } else {
+  std::vector<std::vector<float>> hw, hb;
+  if (wants_fused_plan(cfg) && !host_params(h, bot_w, bot_b, top_w, top_b, &hw, &hb)) {
+    cudaGetLastError();
     delete h;
-    return DLRM_ERR_INVALID_ARG;
+    return DLRM_ERR_CUDA;
   }
+  PlanChoice choice;
+  const dlrm_status_t planned =
+      choose_plan(cfg, hw, hb, h->tabs, dlrm::device_sm_count(), dlrm::device_max_smem_optin(),
+                  &fplan, &tplan, &choice);
+  if (planned != DLRM_OK) {
+    delete h;
+    return planned;
+  }
+  h->path = choice.path;
+  h->fused_tc = choice.fused_tc;
+  h->fused_bm = choice.fused_bm;
   if (h->path == DLRM_PATH_FUSED) {
     h->stage_names.push_back("fused");
   } else {
@@ -505,6 +550,49 @@ dlrm_status_t dlrm_create(const dlrm_config_t* cfg, const float* const* tables,
     h->report_on_destroy = true;
   }
   *out = h;
+  return DLRM_OK;
+}
+
+dlrm_status_t dlrm_plan_query(const dlrm_config_t* cfg, int32_t sm_count, int64_t smem_per_block,
+                              dlrm_plan_info_t* info) {
+  if (!cfg || !info || sm_count < 1 || smem_per_block < 1) return DLRM_ERR_INVALID_ARG;
+  const size_t smem = static_cast<size_t>(smem_per_block);
+  const dlrm_status_t checked = check_config(cfg, smem);
+  if (checked != DLRM_OK) return checked;
+  // zero weights of the model's shapes: the plan depends on shapes alone
+  std::vector<std::vector<float>> hw, hb;
+  if (wants_fused_plan(cfg)) {
+    for (int side = 0; side < 2; ++side) {
+      const int32_t* ln = side == 0 ? cfg->ln_bot : cfg->ln_top;
+      const int n = side == 0 ? cfg->n_bot : cfg->n_top;
+      for (int l = 0; l < n; ++l) {
+        hw.emplace_back(static_cast<size_t>(ln[l]) * ln[l + 1], 0.f);
+        hb.emplace_back(ln[l + 1], 0.f);
+      }
+    }
+  }
+  dlrm::GatherTables tabs{};   // null table pointers pass the 16-byte alignment test
+  dlrm::FusedPlan fplan;
+  dlrm::FusedTcPlan tplan;
+  PlanChoice c;
+  const dlrm_status_t planned = choose_plan(cfg, hw, hb, tabs, sm_count, smem, &fplan, &tplan, &c);
+  if (planned != DLRM_OK) return planned;
+  dlrm_plan_info_t r{};
+  r.path = c.path;
+  r.fused_fits = c.fused_fits ? 1 : 0;
+  if (c.fused_fits) {
+    const bool tc = tensor_core_math(cfg->math);
+    r.tensor_core = tc ? 1 : 0;
+    r.tile_samples = c.fused_bm;
+    r.tiles = c.tiles;
+    r.grid = static_cast<int32_t>(tc ? c.tiles : std::min<int64_t>(c.tiles, sm_count));
+    r.smem_bytes = tc ? tplan.params.smem_bytes : fplan.params.smem_bytes;
+    r.ring_stages = tc ? tplan.params.stages : fplan.params.stages;
+    r.stream_copies = tc ? tplan.params.n_tiles : fplan.params.n_stages;
+    r.stream_bytes = tc ? static_cast<int64_t>(tplan.wstream.size())
+                        : static_cast<int64_t>(fplan.wstream.size() * sizeof(float));
+  }
+  *info = r;
   return DLRM_OK;
 }
 

@@ -72,9 +72,10 @@ struct FusedPlan {
 
 // Builds the plan from host copies of the (out, in) weights and biases;
 // false when the model does not fit the fused kernel.
-// The tile height is the smallest of 4, 8, 12, 14, 16 rows whose tiles of
-// max_batch fit one wave on `sms` SMs (16 past that), falling back to smaller
-// tiles when the shared-memory carve does not fit.
+// The tile height is the one of 4, 8, 12, 14, 16 rows with the least
+// rounds x (rows + 12), rounds = ceil(tiles of max_batch / sms) (the launch is
+// persistent, and a tile costs about 12 rows' worth more than its rows),
+// falling back to smaller tiles when the shared-memory carve does not fit.
 bool fused_plan(int n_dense, int k_tables, int d, int bag, const std::vector<int>& ln_bot,
                 const std::vector<int>& ln_top, const std::vector<std::vector<float>>& w,
                 const std::vector<std::vector<float>>& b, const GatherTables& tabs,

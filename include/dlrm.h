@@ -137,6 +137,31 @@ dlrm_status_t dlrm_create(const dlrm_config_t* cfg, const float* const* tables,
                           const float* const* top_w, const float* const* top_b,
                           dlrm_handle_t* out);
 
+/* The kernel plan dlrm_create would take for cfg on a device with sm_count
+ * SMs and smem_per_block bytes of opt-in shared memory per block (GB300: 152
+ * and 232448), assuming 16-byte aligned tables. Host-only: touches no device,
+ * needs no weights (the plan depends on shapes alone). Returns the status
+ * dlrm_create would return for the config's shape (INVALID_ARG, UNSUPPORTED
+ * as documented there, UNSUPPORTED for path FUSED when the model does not fit
+ * the fused kernel), and INVALID_ARG for a null cfg or info, sm_count < 1 or
+ * smem_per_block < 1. On DLRM_OK, *info holds the plan. */
+typedef struct {
+  int32_t path;            /* DLRM_PATH_FUSED or DLRM_PATH_LAYERWISE */
+  int32_t fused_fits;      /* 1: the model fits the fused kernel of its math */
+  int32_t tensor_core;     /* 1: that fused kernel runs its GEMMs on tcgen05 */
+  int32_t tile_samples;    /* samples per fused tile (0 unless fused_fits) */
+  int64_t tiles;           /* fused tiles of max_batch samples */
+  int32_t grid;            /* CTAs of one fused launch at max_batch (fp32: at
+                              most one per SM, each looping over tiles) */
+  int32_t smem_bytes;      /* dynamic shared memory per fused CTA */
+  int32_t ring_stages;     /* depth of the fused weight ring */
+  int32_t stream_copies;   /* bulk copies in one pass over the weight stream */
+  int64_t stream_bytes;    /* packed MLP weight stream of the fused kernel */
+} dlrm_plan_info_t;
+
+dlrm_status_t dlrm_plan_query(const dlrm_config_t* cfg, int32_t sm_count,
+                              int64_t smem_per_block, dlrm_plan_info_t* info);
+
 /* One forward pass for `batch` samples ([P4] dlrm_megakernel.rs steps 1-6).
  *   dense    (batch, ln_bot[0]) fp32
  *   indices  (n_tables, batch * bag_size) int64, table-major
