@@ -6,6 +6,7 @@ reported (tile rows from the fused kernel's phase trace, CTAs and shared memory
 from the launch), and the weight stream is counted by hand from the stage
 layout. The rest are properties every plan must have.
 """
+import numpy as np
 import pytest
 
 import dlrm_embedding_interaction_gb300 as dl
@@ -172,3 +173,36 @@ def test_query_checks_its_arguments_like_create():
         dl.dlrm_plan_query([13, 4], [4 + f * (f - 1) // 2, 1], rows, 4, 1, 8)
     assert e.value.status == dl.ERR_UNSUPPORTED
     assert dl.lib().dlrm_plan_query(None, SMS, SMEM, None) == dl.ERR_INVALID_ARG
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name,math", [
+    ("tiny_b64_k3", dl.MATH_FP32), ("b2048_k3", dl.MATH_FP32), ("b2048_k3", dl.MATH_BF16),
+    ("b2048_k32", dl.MATH_FP32), ("b2048_k32", dl.MATH_BF16), ("sweep_b8192_k3", dl.MATH_FP32),
+    ("sweep_b8192_k3", dl.MATH_TF32), ("sweep_b300_k16", dl.MATH_TF32),
+    ("b2048_k3", dl.MATH_TF32X3)])
+def test_query_matches_create_on_the_device(name, math):
+    """The host query, given this device's SM count and shared memory, names
+    the path and tile height the handle built on the device took."""
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.fail("the gpu tests need a CUDA device")
+    props = torch.cuda.get_device_properties(0)
+    smem = getattr(props, "shared_memory_per_block_optin", SMEM)
+    cfg = synth.get_config(name)
+    q = query(cfg, math, sms=props.multi_processor_count, smem=smem)
+    inp = synth.make_inputs(cfg, seed=1)
+
+    def cu(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+    model = dl.DlrmModel(cfg.ln_bot, cfg.ln_top, [cu(t) for t in inp["tables"]],
+                         [cu(w) for w in inp["bot_w"]], [cu(v) for v in inp["bot_b"]],
+                         [cu(w) for w in inp["top_w"]], [cu(v) for v in inp["top_b"]],
+                         cfg.bag_size, cfg.batch, math)
+    try:
+        assert model.path == q["path"]
+        if q["path"] == dl.PATH_FUSED:
+            assert model.set_phase_trace(None) == q["tile_samples"]
+    finally:
+        model.close()
