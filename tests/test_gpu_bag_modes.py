@@ -83,6 +83,7 @@ CASES = [
     ((80,), 1024, 5, 70),
     ((64, 64), 13, 41, 8),
     ((10,), 1, 17, 3),
+    ((20,) * 128, 8, 40, 6),          # DLRM_MAX_TABLES tables in one launch
 ]
 
 

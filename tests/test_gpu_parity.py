@@ -120,7 +120,7 @@ def test_gather_non_uniform_offsets_flagged_and_zeroed():
 
 INTERACT_CASES = [
     (64, 3, 16), (2048, 3, 64), (2048, 32, 64), (300, 26, 128), (5, 0, 8),
-    (17, 7, 13), (3, 127, 4), (1, 1, 1), (33, 5, 6), (1000, 1, 64),
+    (17, 7, 13), (3, 127, 4), (1, 1, 1), (33, 5, 6), (1000, 1, 64), (9, 128, 8),
 ]
 
 
@@ -260,6 +260,55 @@ def test_forward_odd_widths_matches_oracle(path):
     inp = synth.make_inputs(cfg, seed=99)
     model = make_model(cfg, inp, path=path)
     close(run_forward(model, inp), oracle.forward(inp))
+    model.close()
+
+
+def test_forward_at_the_table_limit():
+    """DLRM_MAX_TABLES = 128 tables: F = 129 feature vectors, 8256 pairs and a
+    top MLP 8264 wide. Too wide for a fused tile, so AUTO takes the layer-wise
+    launches, with the gather's table list at its full length. Table values in
+    (-0.5, 0.5) make the pair dots of the same order as x."""
+    k = dl.MAX_TABLES
+    f = k + 1
+    cfg = synth.DlrmConfig("k128_b37", 37, (13, 16, 8), (100,) * k, 8, 2,
+                           (8 + f * (f - 1) // 2, 32, 1), 0.5)
+    inp = synth.make_inputs(cfg, seed=5)
+    model = make_model(cfg, inp)
+    assert model.path == dl.PATH_LAYERWISE
+    close(run_forward(model, inp), oracle.forward(inp))
+    model.close()
+
+
+def _deep_model_inputs():
+    """DLRM_MAX_LAYERS = 16 Linear layers on each side, 32 wide: 31 GEMMs plus
+    the sigmoid dot. The weights are scaled by sqrt(6), to the Kaiming range
+    that keeps ReLU activations at one size through the depth."""
+    n = dl.MAX_LAYERS
+    cfg = synth.DlrmConfig("layers16_b300", 300, (13,) + (32,) * (n - 1) + (16,), (1000,) * 3,
+                           16, 1, (16 + 6,) + (32,) * (n - 1) + (1,), 0.5)
+    inp = synth.make_inputs(cfg, seed=6)
+    for key in ("bot_w", "top_w"):
+        inp[key] = [w * np.float32(np.sqrt(6.0)) for w in inp[key]]
+    return cfg, inp
+
+
+@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
+def test_forward_at_the_layer_limit(path):
+    cfg, inp = _deep_model_inputs()
+    model = make_model(cfg, inp, path=path)
+    close(run_forward(model, inp), oracle.forward(inp))
+    model.close()
+
+
+@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
+def test_forward_at_the_layer_limit_tf32(path):
+    """The same 32-layer model with TF32 operands: within rel 2e-2 (a plain
+    tf32-rounding model of it errs by 2e-3). BF16 is left out: its 8-bit
+    mantissa, rounded at each of 31 layers, takes the same model to ~4e-2,
+    past the bar set for the workload models of 3 to 5 layers."""
+    cfg, inp = _deep_model_inputs()
+    model = make_model(cfg, inp, math=dl.MATH_TF32, path=path)
+    np.testing.assert_allclose(run_forward(model, inp), oracle.forward(inp), rtol=2e-2, atol=0)
     model.close()
 
 
