@@ -130,34 +130,53 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
             out = ""
-        rows = []
-        for rec in csv.reader(io.StringIO(out)):
-            if len(rec) < 10:
-                continue
-            try:
-                ts = time.mktime(time.strptime(rec[0].strip().split(".")[0],
-                                               "%Y/%m/%d %H:%M:%S"))
-                frac = float("0." + rec[0].strip().split(".")[1]) if "." in rec[0] else 0.0
-                rows.append(dict(t=ts + frac, sm=float(rec[2]), smax=float(rec[3]),
-                                 power=float(rec[4]) if rec[4].strip() not in ("", "[N/A]") else None,
-                                 hw=rec[6].strip(), hwt=rec[7].strip(), swt=rec[8].strip(),
-                                 swp=rec[9].strip()))
-            except Exception:
-                continue
-        inside = [r for r in rows if any(a - 0.15 <= r["t"] <= b + 0.15 for a, b in self.windows)]
-        used = inside if inside else rows
-        if not used:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        reasons = set()
-        for r in used:
-            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
-                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
-                if r[key].lower().startswith("active"):
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(r["sm"] for r in used),
-                "sm_max_mhz": max(r["smax"] for r in used),
-                "reasons": sorted(reasons), "samples": len(used),
-                "samples_in_timed_region": len(inside)}
+        return summarise_clocks(out, self.windows)
+
+
+THROTTLES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
+
+
+def summarise_clocks(text: str, windows) -> dict:
+    """SM clocks and active throttle reasons from `nvidia-smi --query-gpu=
+    ClockSampler.FIELDS --format=csv,noheader,nounits` rows, keeping the samples
+    inside the timed windows (epoch seconds, +-0.15 s; all samples when none
+    fall inside). `verdict` names a run these clocks would reject: a hardware or
+    thermal slowdown, or a median SM clock below 90% of max with no reason
+    active (a clock lock left by someone); sw_power_cap is kept and noted."""
+    rows = []
+    for rec in csv.reader(io.StringIO(text)):
+        if len(rec) < 10:
+            continue
+        try:
+            ts = time.mktime(time.strptime(rec[0].strip().split(".")[0], "%Y/%m/%d %H:%M:%S"))
+            frac = float("0." + rec[0].strip().split(".")[1]) if "." in rec[0] else 0.0
+            rows.append(dict(t=ts + frac, sm=float(rec[2]), smax=float(rec[3]),
+                             power=float(rec[4]) if rec[4].strip() not in ("", "[N/A]") else None,
+                             hw=rec[6].strip(), hwt=rec[7].strip(), swt=rec[8].strip(),
+                             swp=rec[9].strip()))
+        except Exception:
+            continue
+    inside = [r for r in rows if any(a - 0.15 <= r["t"] <= b + 0.15 for a, b in windows)]
+    used = inside if inside else rows
+    if not used:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+    reasons = set()
+    for r in used:
+        for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                          ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+            if r[key].lower().startswith("active"):
+                reasons.add(name)
+    med = statistics.median(r["sm"] for r in used)
+    smax = max(r["smax"] for r in used)
+    bad = [name for name in THROTTLES if name in reasons]
+    if bad:
+        verdict = "rejected: " + ", ".join(bad)
+    elif med < 0.9 * smax and "sw_power_cap" not in reasons:
+        verdict = "rejected: SM clock below max with no reason active (a clock lock?)"
+    else:
+        verdict = "ok"
+    return {"sm_mhz": med, "sm_max_mhz": smax, "reasons": sorted(reasons), "verdict": verdict,
+            "samples": len(used), "samples_in_timed_region": len(inside)}
 
 
 # ---------------------------------------------------------------- oracle timing
