@@ -524,3 +524,33 @@ def test_generator_distributions():
     head = w[:10_000].sum() / w.sum()
     assert abs((z < 10_000).mean() - head) < 0.005
     assert z.min() >= 0 and z.max() < 1_000_000
+
+
+def test_generator_variable_bags_structure():
+    """The general-offsets input recipe: table 0's lengths uniform on 0..max_len,
+    every table the same lengths in its own order (the same N indices, no
+    remainder bag), offsets the running sum from 0, indices inside each table,
+    and the bench's 0..40 mixture averaging 20 rows with empty bags present."""
+    cfg = synth.DlrmConfig("vb", 20000, (13, 8), (1000, 50, 7), 8, 1, (8 + 6,), 0.05)
+    idx, off, lens = synth.make_variable_bags(cfg, seed=3, max_len=40)
+    k, b = 3, 20000
+    assert lens.shape == off.shape == (k, b) and idx.shape == (k, int(lens[0].sum()))
+    for t in range(k):
+        assert sorted(lens[t]) == sorted(lens[0])
+        assert off[t, 0] == 0 and np.array_equal(np.diff(off[t]), lens[t, :-1])
+        assert off[t, -1] + lens[t, -1] == idx.shape[1]
+        assert idx[t].min() >= 0 and idx[t].max() < cfg.rows[t]
+    assert not np.array_equal(lens[1], lens[0])         # a different order per table
+    assert lens.min() == 0 and lens.max() == 40
+    assert abs(lens[0].mean() - 20.0) < 0.3
+    counts = np.bincount(lens[0], minlength=41)
+    assert counts.min() > 0.8 * b / 41                  # every length 0..40 drawn evenly
+    again = synth.make_variable_bags(cfg, seed=3, max_len=40)
+    assert all(np.array_equal(x, y) for x, y in zip((idx, off, lens), again))
+
+
+def test_generator_bag_weights():
+    w = synth.make_bag_weights((2, 1 << 16), seed=5)
+    assert w.dtype == np.float32 and w.min() >= -2.0 and w.max() < 2.0
+    assert abs(w.mean()) < 0.02 and not np.array_equal(w[0], w[1])
+    assert np.array_equal(w, synth.make_bag_weights((2, 1 << 16), seed=5))
