@@ -217,14 +217,20 @@ dlrm_status_t dlrm_set_profiling(dlrm_handle_t h, int32_t enable);
 
 /* Phase trace of the fused plan (profiling; off by default). With a non-null
  * device buffer of `capacity` uint64 words, every later dlrm_forward on a
- * fused handle writes, per tile t of 16 (or 8) samples, the %globaltimer
+ * fused handle writes, per tile t of *tile_rows samples (the plan's tile
+ * height: 4, 8, 12, 14 or 16 rows in fp32, 16 in TF32/BF16), the %globaltimer
  * nanoseconds at which the tile finished each phase to
- * buf[t * DLRM_TRACE_SLOTS + s]: s = 0 kernel start, 1 prologue (biases and
- * inputs loaded), 2 .. 1+n_bot the bottom layers, 2+n_bot the interaction,
- * 3+n_bot .. 1+n_bot+n_top the top layers but the last, 2+n_bot+n_top the end
- * (sigmoid layer written). Needs capacity >= tiles(max_batch) *
- * DLRM_TRACE_SLOTS (INVALID_ARG otherwise; UNSUPPORTED on a layer-wise
- * handle); NULL switches it off. Returns the tile height in *tile_rows. */
+ * buf[t * DLRM_TRACE_SLOTS + s]: s = 0 the tile's start (the kernel's start
+ * for a CTA's first tile), 1 prologue (biases and inputs loaded), 2 .. 1+n_bot
+ * the bottom layers, 2+n_bot the interaction, 3+n_bot .. 1+n_bot+n_top the top
+ * layers but the last, 2+n_bot+n_top the end (sigmoid layer written). While
+ * those slots end below 20, the slots from 20 on profile each GEMM layer g
+ * (bottom layers, then top layers but the last): fp32, slot 20 + g = when its
+ * k-loop ended; TF32/BF16, slots 20 + 2g and 21 + 2g = nanoseconds the MMA
+ * thread waited for the layer's input activations and for its weight tiles.
+ * Needs capacity >= tiles(max_batch) * DLRM_TRACE_SLOTS (INVALID_ARG
+ * otherwise; UNSUPPORTED on a layer-wise handle); NULL switches it off.
+ * Returns the tile height in *tile_rows. */
 #define DLRM_TRACE_SLOTS 40
 dlrm_status_t dlrm_set_phase_trace(dlrm_handle_t h, uint64_t* buf, int64_t capacity,
                                    int32_t* tile_rows);
