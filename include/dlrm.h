@@ -129,9 +129,13 @@ const char* dlrm_status_string(int32_t status);
  *           own device memory; the caller may free them afterwards.
  * Allocates the handle's workspace for max_batch samples (bag sums, hidden
  * activations, the interaction output, staging for dlrm_forward_host) and
- * synchronises the device once. Returns INVALID_ARG for any shape violation
- * of [P4] validate(), OOM if an allocation fails, UNSUPPORTED for
- * n_tables > DLRM_MAX_TABLES or a math mode not built. */
+ * synchronises the device once. Returns INVALID_ARG for a null pointer, any
+ * shape violation of [P4] validate(), an unknown math mode or path; OOM if an
+ * allocation fails; UNSUPPORTED for n_tables > DLRM_MAX_TABLES, more than
+ * DLRM_MAX_LAYERS layers a side, max_batch * bag_size > 2^31, an interaction
+ * that needs more shared memory per sample than the device has, or path
+ * FUSED when the model does not fit the fused kernel of its math (always for
+ * TF32X3). dlrm_plan_query gives the same answer on the host. */
 dlrm_status_t dlrm_create(const dlrm_config_t* cfg, const float* const* tables,
                           const float* const* bot_w, const float* const* bot_b,
                           const float* const* top_w, const float* const* top_b,
