@@ -181,13 +181,14 @@ def summarise_clocks(text: str, windows) -> dict:
 
 # ---------------------------------------------------------------- oracle timing
 
-def time_oracle(inp, batch, budget_s, max_samples=None):
+def time_oracle(inp, batch, budget_s, max_samples=None, threads=None):
     """Oracle samples/s on a bounded sample: whole batches (or a prefix of one)
-    repeated until budget_s of CPU time has run."""
+    repeated until budget_s of CPU time has run, on `threads` host threads (all
+    cores by default)."""
     import numpy as np
     import oracle
     lib = oracle.load()
-    threads = os.cpu_count() or 1
+    threads = threads or os.cpu_count() or 1
     probe_ids = np.arange(min(batch, 64))
     t0 = time.perf_counter()
     oracle.forward(inp, sample_ids=probe_ids, threads=threads, lib=lib)
@@ -207,7 +208,7 @@ def time_oracle(inp, batch, budget_s, max_samples=None):
     dt = time.perf_counter() - t_start
     return dict(value=done / dt, unit=UNIT, cores=threads, kind="oracle",
                 sample=f"{n} of {batch} samples x {reps} repetitions ({dt:.1f} s, fp64, "
-                       f"{threads} threads)")
+                       f"{threads} thread{'s' if threads != 1 else ''})")
 
 
 # ---------------------------------------------------------------- ranks
@@ -714,6 +715,9 @@ def run_ours(args, rank, world, local_rank):
             torch.cuda.empty_cache()
         if not args.no_cpu_baseline:
             cpu = time_oracle(inp, cfg.batch, args.cpu_seconds)
+            # the same oracle on one thread, a short sample beside the all-core figure
+            one = time_oracle(inp, cfg.batch, min(3.0, args.cpu_seconds), threads=1)
+            cpu["single_thread"] = {k: one[k] for k in ("value", "unit", "cores", "sample")}
 
     model.close()
     if rank != 0:
