@@ -339,6 +339,13 @@ dlrm_status_t choose_plan(const dlrm_config_t* cfg, const std::vector<std::vecto
   return DLRM_OK;
 }
 
+// Inputs and output of a forward at their elements' natural alignment.
+bool forward_args_aligned(const void* dense, const void* indices, const void* offsets,
+                          const void* out) {
+  return dlrm::aligned_to(dense, sizeof(float)) && dlrm::aligned_to(indices, sizeof(int64_t)) &&
+         dlrm::aligned_to(offsets, sizeof(int64_t)) && dlrm::aligned_to(out, sizeof(float));
+}
+
 }  // namespace
 
 extern "C" {
@@ -367,7 +374,8 @@ dlrm_status_t dlrm_create(const dlrm_config_t* cfg, const float* const* tables,
   if (!cfg || !tables || !bot_w || !bot_b || !top_w || !top_b) return DLRM_ERR_INVALID_ARG;
   const dlrm_status_t checked = check_config(cfg, dlrm::device_max_smem_optin());
   if (checked != DLRM_OK) return checked;
-  for (int t = 0; t < cfg->n_tables; ++t) if (!tables[t]) return DLRM_ERR_INVALID_ARG;
+  for (int t = 0; t < cfg->n_tables; ++t)
+    if (!tables[t] || !dlrm::aligned_to(tables[t], sizeof(float))) return DLRM_ERR_INVALID_ARG;
   for (int l = 0; l < cfg->n_bot; ++l) if (!bot_w[l] || !bot_b[l]) return DLRM_ERR_INVALID_ARG;
   for (int l = 0; l < cfg->n_top; ++l) if (!top_w[l] || !top_b[l]) return DLRM_ERR_INVALID_ARG;
 
@@ -599,6 +607,7 @@ dlrm_status_t dlrm_plan_query(const dlrm_config_t* cfg, int32_t sm_count, int64_
 dlrm_status_t dlrm_forward(dlrm_handle_t h, const float* dense, const int64_t* indices,
                            const int64_t* offsets, float* out, int32_t batch, void* stream) {
   if (!h || !dense || !indices || !offsets || !out) return DLRM_ERR_INVALID_ARG;
+  if (!forward_args_aligned(dense, indices, offsets, out)) return DLRM_ERR_INVALID_ARG;
   if (batch < 1 || batch > h->max_batch) return DLRM_ERR_INVALID_ARG;
   return run_forward(h, dense, indices, offsets, out, batch, static_cast<cudaStream_t>(stream));
 }
@@ -622,6 +631,8 @@ dlrm_status_t dlrm_forward_host(dlrm_handle_t h, const float* dense_host,
                                 const int64_t* indices_host, const int64_t* offsets_host,
                                 float* out_host, int32_t batch, void* stream) {
   if (!h || !dense_host || !indices_host || !offsets_host || !out_host)
+    return DLRM_ERR_INVALID_ARG;
+  if (!forward_args_aligned(dense_host, indices_host, offsets_host, out_host))
     return DLRM_ERR_INVALID_ARG;
   if (batch < 1 || batch > h->max_batch) return DLRM_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -687,6 +698,7 @@ dlrm_status_t dlrm_set_phase_trace(dlrm_handle_t h, uint64_t* buf, int64_t capac
     h->trace = nullptr;
     return DLRM_OK;
   }
+  if (!dlrm::aligned_to(buf, sizeof(uint64_t))) return DLRM_ERR_INVALID_ARG;
   const int64_t tiles = (h->max_batch + h->fused_bm - 1) / h->fused_bm;
   if (capacity < tiles * DLRM_TRACE_SLOTS) return DLRM_ERR_INVALID_ARG;
   h->trace = reinterpret_cast<unsigned long long*>(buf);
@@ -752,10 +764,14 @@ dlrm_status_t embedding_bag_sum_multi(const float* const* tables, const int64_t*
   if (!tables || !rows) return DLRM_ERR_INVALID_ARG;
   if (B == 0) return DLRM_OK;
   if (!indices || !offsets || !out) return DLRM_ERR_INVALID_ARG;
+  if (!dlrm::aligned_to(indices, sizeof(int64_t)) || !dlrm::aligned_to(offsets, sizeof(int64_t)) ||
+      !dlrm::aligned_to(out, sizeof(float)) || !dlrm::aligned_to(err_flag, sizeof(int32_t)))
+    return DLRM_ERR_INVALID_ARG;
   if (static_cast<int64_t>(B) * L > (int64_t(1) << 31)) return DLRM_ERR_UNSUPPORTED;
   dlrm::GatherTables tabs{};
   for (int t = 0; t < K; ++t) {
-    if (!tables[t] || rows[t] < 0) return DLRM_ERR_INVALID_ARG;
+    if (!tables[t] || rows[t] < 0 || !dlrm::aligned_to(tables[t], sizeof(float)))
+      return DLRM_ERR_INVALID_ARG;
     tabs.ptr[t] = tables[t];
     tabs.rows[t] = rows[t];
   }
@@ -780,9 +796,15 @@ dlrm_status_t embedding_bag_multi_ex(const float* const* tables, const int64_t* 
   if (!tables || !rows) return DLRM_ERR_INVALID_ARG;
   if (B == 0) return DLRM_OK;
   if ((n_idx > 0 && !indices) || !offsets || !out) return DLRM_ERR_INVALID_ARG;
+  const size_t index_bytes = static_cast<size_t>(options->index_bits / 8);
+  if (!dlrm::aligned_to(indices, index_bytes) || !dlrm::aligned_to(offsets, index_bytes) ||
+      !dlrm::aligned_to(options->per_sample_weights, sizeof(float)) ||
+      !dlrm::aligned_to(out, sizeof(float)) || !dlrm::aligned_to(err_flag, sizeof(int32_t)))
+    return DLRM_ERR_INVALID_ARG;
   dlrm::GatherTables tabs{};
   for (int t = 0; t < K; ++t) {
-    if (!tables[t] || rows[t] < 0) return DLRM_ERR_INVALID_ARG;
+    if (!tables[t] || rows[t] < 0 || !dlrm::aligned_to(tables[t], sizeof(float)))
+      return DLRM_ERR_INVALID_ARG;
     tabs.ptr[t] = tables[t];
     tabs.rows[t] = rows[t];
   }
@@ -810,6 +832,9 @@ dlrm_status_t pairwise_dot_lower_tri(const float* dense, int32_t ld_dense, const
   if (ld_out < (copy_dense ? D : 0) + p) return DLRM_ERR_INVALID_ARG;
   if (B == 0) return DLRM_OK;
   if (!dense || !out || (K > 0 && !emb)) return DLRM_ERR_INVALID_ARG;
+  if (!dlrm::aligned_to(dense, sizeof(float)) || !dlrm::aligned_to(emb, sizeof(float)) ||
+      !dlrm::aligned_to(out, sizeof(float)))
+    return DLRM_ERR_INVALID_ARG;
   if (p > (int64_t(1) << 30)) return DLRM_ERR_UNSUPPORTED;
   if (dlrm::interaction_smem_per_sample(K, D) > dlrm::device_max_smem_optin())
     return DLRM_ERR_UNSUPPORTED;
@@ -820,6 +845,8 @@ dlrm_status_t pairwise_dot_lower_tri(const float* dense, int32_t ld_dense, const
 
 dlrm_status_t pairwise_pair_map(int32_t F, int32_t* i_out, int32_t* j_out, void* stream) {
   if (F < 2 || F > 46341 || !i_out || !j_out) return DLRM_ERR_INVALID_ARG;
+  if (!dlrm::aligned_to(i_out, sizeof(int32_t)) || !dlrm::aligned_to(j_out, sizeof(int32_t)))
+    return DLRM_ERR_INVALID_ARG;
   return cuda_status(dlrm::launch_pair_map(F, i_out, j_out, static_cast<cudaStream_t>(stream)));
 }
 
@@ -834,6 +861,9 @@ dlrm_status_t linear_bias_act(const float* x, int32_t ld_x, const float* W, cons
     return DLRM_ERR_INVALID_ARG;
   if (M == 0) return DLRM_OK;
   if (!x || !W || !y) return DLRM_ERR_INVALID_ARG;
+  if (!dlrm::aligned_to(x, sizeof(float)) || !dlrm::aligned_to(W, sizeof(float)) ||
+      !dlrm::aligned_to(bias, sizeof(float)) || !dlrm::aligned_to(y, sizeof(float)))
+    return DLRM_ERR_INVALID_ARG;
   const size_t ybytes = (static_cast<size_t>(M - 1) * ld_y + N) * sizeof(float);
   const size_t xbytes = (static_cast<size_t>(M - 1) * ld_x + K) * sizeof(float);
   const size_t wbytes = static_cast<size_t>(N) * K * sizeof(float);

@@ -123,4 +123,10 @@ cudaError_t launch_linear_tc(const float* x, int ld_x, const float* w, int ld_w,
 int device_sm_count();
 size_t device_max_smem_optin();
 
+// An element pointer's natural alignment (`bytes` = the element size). A null
+// pointer passes: null checks are made separately.
+inline bool aligned_to(const void* p, size_t bytes) {
+  return reinterpret_cast<uintptr_t>(p) % bytes == 0;
+}
+
 }  // namespace dlrm

@@ -65,13 +65,24 @@ extern "C" dlrm_status_t dlrm_forward_noalloc(
     return DLRM_ERR_INVALID_ARG;
   if (cfg->math != DLRM_MATH_FP32) return DLRM_ERR_UNSUPPORTED;
   dlrm::GatherTables tabs{};
+  if (!dlrm::aligned_to(dense, sizeof(float)) || !dlrm::aligned_to(indices, sizeof(int64_t)) ||
+      !dlrm::aligned_to(offsets, sizeof(int64_t)) || !dlrm::aligned_to(out, sizeof(float)) ||
+      !dlrm::aligned_to(err_flag, sizeof(int32_t)))
+    return DLRM_ERR_INVALID_ARG;
   for (int t = 0; t < k; ++t) {
-    if (!tables[t] || cfg->rows[t] < 1) return DLRM_ERR_INVALID_ARG;
+    if (!tables[t] || cfg->rows[t] < 1 || !dlrm::aligned_to(tables[t], sizeof(float)))
+      return DLRM_ERR_INVALID_ARG;
     tabs.ptr[t] = tables[t];
     tabs.rows[t] = cfg->rows[t];
   }
-  for (int l = 0; l < cfg->n_bot; ++l) if (!bot_w[l] || !bot_b[l]) return DLRM_ERR_INVALID_ARG;
-  for (int l = 0; l < cfg->n_top; ++l) if (!top_w[l] || !top_b[l]) return DLRM_ERR_INVALID_ARG;
+  for (int side = 0; side < 2; ++side) {
+    const float* const* ws = side == 0 ? bot_w : top_w;
+    const float* const* bs = side == 0 ? bot_b : top_b;
+    for (int l = 0; l < (side == 0 ? cfg->n_bot : cfg->n_top); ++l)
+      if (!ws[l] || !bs[l] || !dlrm::aligned_to(ws[l], sizeof(float)) ||
+          !dlrm::aligned_to(bs[l], sizeof(float)))
+        return DLRM_ERR_INVALID_ARG;
+  }
   if (static_cast<int64_t>(batch) * bag > (int64_t(1) << 31)) return DLRM_ERR_UNSUPPORTED;
   if (dlrm::interaction_smem_per_sample(k, d) > dlrm::device_max_smem_optin())
     return DLRM_ERR_UNSUPPORTED;

@@ -19,6 +19,9 @@
  *    stream). Every call only enqueues work on it and never synchronises it,
  *    except dlrm_get_error and dlrm_create/dlrm_destroy as documented.
  *  - All float data is fp32, row-major; integer indices/offsets are int64.
+ *  - Every pointer sits at its element's natural alignment (4 bytes for fp32
+ *    and int32, 8 for int64 and uint64); any other is DLRM_ERR_INVALID_ARG,
+ *    returned before anything is launched.
  *  - Argument problems detectable on the host are returned as a status
  *    before anything is launched. Problems only visible on the device (an
  *    index outside its table, offsets that are not the uniform stride) never

@@ -72,12 +72,13 @@ def test_host_side_argument_checks(lib):
     assert lib.pairwise_pair_map(1, null, null, null) == dl.ERR_INVALID_ARG
 
 
-def _create(lib, ln_bot, ln_top, rows, d, bag=1, max_batch=8, math=0, tables_ok=True):
+def _create(lib, ln_bot, ln_top, rows, d, bag=1, max_batch=8, math=0, tables_ok=True,
+            table=0x1000):
     k = len(rows)
     cfg = dl._Config(len(ln_bot) - 1, (ctypes.c_int32 * len(ln_bot))(*ln_bot), k,
                      (ctypes.c_int64 * k)(*rows), d, len(ln_top) - 1,
                      (ctypes.c_int32 * len(ln_top))(*ln_top), bag, max_batch, math, 0)
-    fake = ctypes.c_void_p(0x1000 if tables_ok else 0)
+    fake = ctypes.c_void_p(table if tables_ok else 0)
     tabs = (ctypes.c_void_p * k)(*([fake] * k))
     w = (ctypes.c_void_p * 16)(*([ctypes.c_void_p(0x1000)] * 16))
     h = ctypes.c_void_p()
@@ -167,3 +168,65 @@ def test_header_is_plain_c_and_links(tmp_path, lib):
     assert r.returncode == 0, r.stderr
     run = subprocess.run([str(exe)], capture_output=True, text=True)
     assert run.returncode == 0, run.stderr
+
+
+def test_misaligned_pointers_are_refused_before_any_launch(lib):
+    """Every pointer must sit at its element's natural alignment (4 bytes for
+    fp32 and int32, 8 for int64); the calls refuse others with INVALID_ARG on
+    the host instead of faulting on the device."""
+    vp = ctypes.c_void_p
+    f32, i64, odd = vp(0x1000), vp(0x1008), vp(0x1002)
+    i64_on_4 = vp(0x1004)                               # int64 on a 4-byte boundary
+    rows = (ctypes.c_int64 * 2)(10, 10)
+    tabs = (vp * 2)(f32, f32)
+    bad_tabs = (vp * 2)(f32, odd)
+    null = vp(0)
+    g = lib.embedding_bag_sum_multi
+    assert g(bad_tabs, rows, 2, 8, i64, i64, 4, 1, f32, null, null) == dl.ERR_INVALID_ARG
+    assert g(tabs, rows, 2, 8, i64_on_4, i64, 4, 1, f32, null, null) == dl.ERR_INVALID_ARG
+    assert g(tabs, rows, 2, 8, i64, i64_on_4, 4, 1, f32, null, null) == dl.ERR_INVALID_ARG
+    assert g(tabs, rows, 2, 8, i64, i64, 4, 1, odd, null, null) == dl.ERR_INVALID_ARG
+    assert g(tabs, rows, 2, 8, i64, i64, 4, 1, f32, odd, null) == dl.ERR_INVALID_ARG
+
+    ex = lib.embedding_bag_multi_ex
+    ex.argtypes = [vp, vp, ctypes.c_int32, ctypes.c_int32, vp, ctypes.c_int64, vp,
+                   ctypes.c_int32, ctypes.POINTER(dl._BagOptions), vp, vp, vp]
+    ex.restype = ctypes.c_int
+    o64 = dl._BagOptions(0, 64, None, -1)
+    o32 = dl._BagOptions(0, 32, None, -1)
+    assert ex(tabs, rows, 2, 8, i64_on_4, 8, i64, 4, ctypes.byref(o64), f32, null, null) == dl.ERR_INVALID_ARG
+    assert ex(tabs, rows, 2, 8, odd, 8, f32, 4, ctypes.byref(o32), f32, null, null) == dl.ERR_INVALID_ARG
+    assert ex(bad_tabs, rows, 2, 8, i64, 8, i64, 4, ctypes.byref(o64), f32, null, null) == dl.ERR_INVALID_ARG
+    ow = dl._BagOptions(0, 64, 0x1002, -1)               # per-sample weights off by 2 bytes
+    assert ex(tabs, rows, 2, 8, i64, 8, i64, 4, ctypes.byref(ow), f32, null, null) == dl.ERR_INVALID_ARG
+
+    assert lib.pairwise_dot_lower_tri(odd, 8, f32, 2, 3, 8, f32, 20, 1, null) == dl.ERR_INVALID_ARG
+    assert lib.pairwise_dot_lower_tri(f32, 8, odd, 2, 3, 8, f32, 20, 1, null) == dl.ERR_INVALID_ARG
+    assert lib.pairwise_dot_lower_tri(f32, 8, f32, 2, 3, 8, odd, 20, 1, null) == dl.ERR_INVALID_ARG
+    assert lib.pairwise_pair_map(4, odd, f32, null) == dl.ERR_INVALID_ARG
+    w, y = vp(0x2000), vp(0x3000)
+    assert lib.linear_bias_act(odd, 4, w, null, y, 4, 2, 4, 4, 0, 0, null) == dl.ERR_INVALID_ARG
+    assert lib.linear_bias_act(f32, 4, w, odd, y, 4, 2, 4, 4, 0, 0, null) == dl.ERR_INVALID_ARG
+    assert lib.linear_bias_act(f32, 4, w, null, vp(0x3001), 4, 2, 4, 4, 0, 0, null) == dl.ERR_INVALID_ARG
+
+    # the forward handle borrows its tables: a misaligned one is refused at create
+    assert _create(lib, [13, 8, 4], [10, 8, 1], [10, 20, 30], 4, table=0x1002)[0] == dl.ERR_INVALID_ARG
+
+
+def test_noalloc_forward_refuses_misaligned_inputs(lib):
+    vp = ctypes.c_void_p
+    ln_bot, ln_top, rows = [13, 8, 4], [10, 8, 1], [10, 20, 30]
+    cfg = dl._Config(2, (ctypes.c_int32 * 3)(*ln_bot), 3, (ctypes.c_int64 * 3)(*rows), 4, 2,
+                     (ctypes.c_int32 * 3)(*ln_top), 1, 8, 0, 0)
+    ok = vp(0x1000)
+    tabs = (vp * 3)(ok, ok, ok)
+    w = (vp * 16)(*([ok] * 16))
+    f = lib.dlrm_forward_noalloc
+    args = lambda dense, idx, off, out, wts=w: f(ctypes.byref(cfg), tabs, wts, wts, wts, wts, dense,
+                                                 idx, off, out, 4, None, None)
+    assert args(vp(0x1002), ok, ok, ok) == dl.ERR_INVALID_ARG
+    assert args(ok, vp(0x1004), ok, ok) == dl.ERR_INVALID_ARG
+    assert args(ok, ok, vp(0x1004), ok) == dl.ERR_INVALID_ARG
+    assert args(ok, ok, ok, vp(0x1001)) == dl.ERR_INVALID_ARG
+    bad_w = (vp * 16)(*([vp(0x1002)] * 16))
+    assert args(ok, ok, ok, ok, bad_w) == dl.ERR_INVALID_ARG
