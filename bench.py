@@ -65,6 +65,9 @@ def parse_args():
     ap.add_argument("--config", default="b2048_k3")
     ap.add_argument("--math", choices=["fp32", "tf32", "bf16", "tf32x3"], default="fp32",
                     help="arithmetic of the timed model's MLPs (fp32 is the parity mode)")
+    ap.add_argument("--config-math", choices=["fp32", "tf32", "bf16", "tf32x3"], default="fp32",
+                    help="arithmetic of the other workloads' forwards under `configs` (their "
+                         "roofline fraction stays against the FP32 FFMA peak)")
     ap.add_argument("--seed", type=int, default=1234)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -439,8 +442,10 @@ def run_ours(args, rank, world, local_rank):
     cfg = synth.get_config(args.config)
     inp = synth.make_inputs(cfg, seed=args.seed)
     cu = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
-    math = {"fp32": dl.MATH_FP32, "tf32": dl.MATH_TF32, "bf16": dl.MATH_BF16,
-            "tf32x3": dl.MATH_TF32X3}[args.math]
+    maths = {"fp32": dl.MATH_FP32, "tf32": dl.MATH_TF32, "bf16": dl.MATH_BF16,
+             "tf32x3": dl.MATH_TF32X3}
+    math = maths[args.math]
+    config_math = maths[args.config_math]
     plan = {"auto": dl.PATH_AUTO, "fused": dl.PATH_FUSED, "layerwise": dl.PATH_LAYERWISE}[args.path]
     model = dl.DlrmModel(cfg.ln_bot, cfg.ln_top, [cu(t) for t in inp["tables"]],
                          [cu(w) for w in inp["bot_w"]], [cu(b) for b in inp["bot_b"]],
@@ -663,7 +668,7 @@ def run_ours(args, rank, world, local_rank):
         m = dl.DlrmModel(c.ln_bot, c.ln_top, tabs,
                          [cu(w) for w in ci["bot_w"]], [cu(b) for b in ci["bot_b"]],
                          [cu(w) for w in ci["top_w"]], [cu(b) for b in ci["top_b"]],
-                         c.bag_size, c.batch)
+                         c.bag_size, c.batch, config_math)
         d_, i_, o_ = cu(ci["dense"]), cu(ci["indices"]), cu(ci["offsets"])
         y_ = torch.empty(c.batch, device=dev)
         ms_c, _ = timed(lambda: m.forward(d_, i_, o_, y_, stream=stream), steps, warmup)
@@ -677,6 +682,7 @@ def run_ours(args, rank, world, local_rank):
         t_alu, t_hbm = fl / (fp32_peak * 1e12), by / (pk["hbm_gbs"] * 1e9)
         return dict(us_per_batch=t * 1e6, us_median=statistics.median(ms_c) * 1e3,
                     samples_per_s=c.batch / t, steps=len(ms_c), plan=plan,
+                    math=args.config_math,
                     roofline_frac=max(t_alu, t_hbm) / t,
                     bound="alu (FP32 FFMA)" if t_alu >= t_hbm else "hbm")
 
