@@ -147,6 +147,91 @@ def _need(t, dtype, name, cuda=True):
         raise ValueError(f"{name}: must be a CUDA tensor")
 
 
+# Model shape of every handle dlrm_create returned in this process (the C
+# handle is opaque): the forward bindings check their tensors against it.
+_HANDLE_SHAPES: dict = {}
+
+
+def _check_forward_io(n_dense: int, k: int, bag: int, max_batch: Optional[int], dense,
+                      indices, offsets, out, where: str, on_cuda: bool) -> int:
+    """Checks a forward's inputs and output before the library sees them and
+    returns the batch. dense (B, n_dense) float32, indices (K, B * bag) and
+    offsets (K, B) int64, out float32 with at least B elements, all
+    contiguous; CUDA tensors when ``on_cuda``, else host (CPU) tensors. The
+    library reads and writes these buffers by the sizes the model implies, so
+    a short or mistyped tensor would be accessed past its end on the device:
+    refused here with TypeError / ValueError instead. Checks run in the order
+    dtype, shape, layout, device."""
+    import torch
+    for t, dt, name in ((dense, torch.float32, "dense"), (indices, torch.int64, "indices"),
+                        (offsets, torch.int64, "offsets"), (out, torch.float32, "out")):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{where}: {name} must be a torch.Tensor")
+        if t.dtype != dt:
+            raise TypeError(f"{where}: {name}: expected {dt}, got {t.dtype}")
+    if dense.dim() != 2 or dense.shape[1] != n_dense:
+        raise ValueError(f"{where}: dense: expected (batch, {n_dense}), got {tuple(dense.shape)}")
+    b = int(dense.shape[0])
+    if b < 1 or (max_batch is not None and b > max_batch):
+        raise ValueError(f"{where}: batch {b} outside [1, {max_batch}]")
+    if indices.numel() != k * b * bag or (indices.dim() == 2 and indices.shape[0] != k):
+        raise ValueError(f"{where}: indices: expected ({k}, {b * bag}) = {k * b * bag} "
+                         f"elements, got {tuple(indices.shape)}")
+    if offsets.numel() != k * b or (offsets.dim() == 2 and offsets.shape[0] != k):
+        raise ValueError(f"{where}: offsets: expected ({k}, {b}), got {tuple(offsets.shape)}")
+    if out.numel() < b:
+        raise ValueError(f"{where}: out: needs at least {b} elements, has {out.numel()}")
+    for t, name in ((dense, "dense"), (indices, "indices"), (offsets, "offsets"), (out, "out")):
+        if not t.is_contiguous():
+            raise ValueError(f"{where}: {name} must be contiguous")
+    for t, name in ((dense, "dense"), (indices, "indices"), (offsets, "offsets"), (out, "out")):
+        if on_cuda and not t.is_cuda:
+            raise ValueError(f"{where}: {name} must be a CUDA tensor")
+        if not on_cuda and t.device.type != "cpu":
+            raise ValueError(f"{where}: {name} must be a host (CPU) tensor")
+    if on_cuda and len({t.device for t in (dense, indices, offsets, out)}) != 1:
+        raise ValueError(f"{where}: dense, indices, offsets and out must be on one device")
+    return b
+
+
+def _check_model_params(ln_bot, ln_top, tables, bot_w, bot_b, top_w, top_b, where: str,
+                        on_cuda: bool) -> int:
+    """Checks the tables and Linear parameters against the layer widths and
+    returns the embedding width D: every table (rows, D) with one D, W[l]
+    (ln[l+1], ln[l]) and b[l] (ln[l+1],) per side, all float32 and
+    contiguous, and CUDA tensors when ``on_cuda`` (checked last, after every
+    dtype and shape). Raises TypeError / ValueError."""
+    import torch
+    if len(tables) < 1:
+        raise ValueError(f"{where}: need at least one table")
+    if len(bot_w) != len(ln_bot) - 1 or len(bot_b) != len(ln_bot) - 1:
+        raise ValueError(f"{where}: expected {len(ln_bot) - 1} bottom weights and biases")
+    if len(top_w) != len(ln_top) - 1 or len(top_b) != len(ln_top) - 1:
+        raise ValueError(f"{where}: expected {len(ln_top) - 1} top weights and biases")
+    d = int(tables[0].shape[1]) if tables[0].dim() == 2 else -1
+    named = [(t, f"tables[{i}]", None) for i, t in enumerate(tables)]
+    for side, ln, ws, bs in (("bot", ln_bot, bot_w, bot_b), ("top", ln_top, top_w, top_b)):
+        for l in range(len(ln) - 1):
+            named.append((ws[l], f"{side}_w[{l}]", (ln[l + 1], ln[l])))
+            named.append((bs[l], f"{side}_b[{l}]", (ln[l + 1],)))
+    for t, name, shape in named:
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{where}: {name} must be a torch.Tensor")
+        if t.dtype != torch.float32:
+            raise TypeError(f"{where}: {name}: expected torch.float32, got {t.dtype}")
+        if shape is None:
+            if t.dim() != 2 or t.shape[1] != d or t.shape[0] < 1:
+                raise ValueError(f"{where}: {name}: expected (rows, {d}), got {tuple(t.shape)}")
+        elif tuple(t.shape) != tuple(shape):
+            raise ValueError(f"{where}: {name}: expected {tuple(shape)}, got {tuple(t.shape)}")
+        if not t.is_contiguous():
+            raise ValueError(f"{where}: {name} must be contiguous")
+    for t, name, _ in named:
+        if on_cuda and not t.is_cuda:
+            raise ValueError(f"{where}: {name} must be a CUDA tensor")
+    return d
+
+
 def _row_stride(t, name) -> int:
     if t.dim() != 2 or t.stride(1) != 1:
         raise ValueError(f"{name}: expected a 2-D tensor with unit column stride")
@@ -301,7 +386,11 @@ def dlrm_create(ln_bot: Sequence[int], ln_top: Sequence[int], tables: Sequence,
     parameters may be CPU or CUDA float32 tensors and are copied.
     """
     k = len(tables)
-    d = int(tables[0].shape[1])
+    d = _check_model_params(ln_bot, ln_top, tables, bot_w, bot_b, top_w, top_b, "dlrm_create",
+                            on_cuda=False)
+    for i, t in enumerate(tables):
+        if not t.is_cuda:
+            raise ValueError(f"dlrm_create: tables[{i}] must be a CUDA tensor (borrowed)")
     lb = (ctypes.c_int32 * len(ln_bot))(*ln_bot)
     lt = (ctypes.c_int32 * len(ln_top))(*ln_top)
     rows = (ctypes.c_int64 * k)(*[int(t.shape[0]) for t in tables])
@@ -309,14 +398,12 @@ def dlrm_create(ln_bot: Sequence[int], ln_top: Sequence[int], tables: Sequence,
                   math, path)
 
     def arr(ts):
-        for t in ts:
-            if not t.is_contiguous():
-                raise ValueError("parameters must be contiguous")
         return (ctypes.c_void_p * len(ts))(*[t.data_ptr() for t in ts])
 
     h = ctypes.c_void_p()
     _check(lib().dlrm_create(ctypes.byref(cfg), arr(tables), arr(bot_w), arr(bot_b),
                              arr(top_w), arr(top_b), ctypes.byref(h)), "dlrm_create")
+    _HANDLE_SHAPES[h.value] = (int(ln_bot[0]), k, int(bag_size), int(max_batch))
     return h.value
 
 
@@ -344,15 +431,29 @@ def dlrm_plan_query(ln_bot: Sequence[int], ln_top: Sequence[int], rows: Sequence
     return {name: getattr(info, name) for name, _ in _PlanInfo._fields_}
 
 
+def _handle_shape(h: int, where: str):
+    shape = _HANDLE_SHAPES.get(h)
+    if shape is None:
+        raise ValueError(f"{where}: {h!r} is not a live handle from dlrm_create")
+    return shape
+
+
 def dlrm_forward(h: int, dense, indices, offsets, out, stream=None) -> None:
-    batch = dense.shape[0]
+    """One forward on CUDA tensors: dense (B, n_dense) float32, indices (K, B*L)
+    and offsets (K, B) int64, out (>= B) float32; asynchronous on ``stream``."""
+    n_dense, k, bag, max_batch = _handle_shape(h, "dlrm_forward")
+    batch = _check_forward_io(n_dense, k, bag, max_batch, dense, indices, offsets, out,
+                              "dlrm_forward", on_cuda=True)
     _check(lib().dlrm_forward(ctypes.c_void_p(h), _ptr(dense), _ptr(indices), _ptr(offsets),
                               _ptr(out), batch, _stream(stream)), "dlrm_forward")
 
 
 def dlrm_forward_host(h: int, dense, indices, offsets, out, stream=None) -> None:
-    """Host-buffer forward (pinned CPU tensors); asynchronous on ``stream``."""
-    batch = dense.shape[0]
+    """Host-buffer forward (CPU tensors, pinned or not; shapes as dlrm_forward);
+    asynchronous on ``stream``."""
+    n_dense, k, bag, max_batch = _handle_shape(h, "dlrm_forward_host")
+    batch = _check_forward_io(n_dense, k, bag, max_batch, dense, indices, offsets, out,
+                              "dlrm_forward_host", on_cuda=False)
     _check(lib().dlrm_forward_host(ctypes.c_void_p(h), _ptr(dense), _ptr(indices),
                                    _ptr(offsets), _ptr(out), batch, _stream(stream)),
            "dlrm_forward_host")
@@ -368,23 +469,28 @@ def dlrm_forward_noalloc(ln_bot: Sequence[int], ln_top: Sequence[int], tables: S
     Every tensor is a CUDA tensor the caller owns; weights are (out, in)
     contiguous. Calls share one scratch array: serialise them (one stream).
     """
+    import torch
     k = len(tables)
-    d = int(tables[0].shape[1])
+    d = _check_model_params(ln_bot, ln_top, tables, bot_w, bot_b, top_w, top_b,
+                            "dlrm_forward_noalloc", on_cuda=True)
+    batch = _check_forward_io(int(ln_bot[0]), k, int(bag_size), None, dense, indices, offsets,
+                              out, "dlrm_forward_noalloc", on_cuda=True)
+    if err_flag is not None:
+        _need(err_flag, torch.int32, "err_flag")
+        if err_flag.numel() < 1:
+            raise ValueError("dlrm_forward_noalloc: err_flag needs one element")
     lb = (ctypes.c_int32 * len(ln_bot))(*ln_bot)
     lt = (ctypes.c_int32 * len(ln_top))(*ln_top)
     rows = (ctypes.c_int64 * k)(*[int(t.shape[0]) for t in tables])
-    cfg = _Config(len(ln_bot) - 1, lb, k, rows, d, len(ln_top) - 1, lt, bag_size,
-                  int(dense.shape[0]), MATH_FP32, PATH_AUTO)
+    cfg = _Config(len(ln_bot) - 1, lb, k, rows, d, len(ln_top) - 1, lt, bag_size, batch,
+                  MATH_FP32, PATH_AUTO)
 
     def arr(ts):
-        for t in ts:
-            if not (t.is_cuda and t.is_contiguous()):
-                raise ValueError("tables and parameters must be contiguous CUDA tensors")
         return (ctypes.c_void_p * len(ts))(*[t.data_ptr() for t in ts])
 
     _check(lib().dlrm_forward_noalloc(ctypes.byref(cfg), arr(tables), arr(bot_w), arr(bot_b),
                                       arr(top_w), arr(top_b), _ptr(dense), _ptr(indices),
-                                      _ptr(offsets), _ptr(out), int(dense.shape[0]),
+                                      _ptr(offsets), _ptr(out), batch,
                                       _ptr(err_flag), _stream(stream)),
            "dlrm_forward_noalloc")
 
@@ -426,6 +532,7 @@ def dlrm_stage_times(h: int):
 
 def dlrm_destroy(h: Optional[int]) -> None:
     if h:
+        _HANDLE_SHAPES.pop(h, None)
         lib().dlrm_destroy(ctypes.c_void_p(h))
 
 

@@ -2,8 +2,6 @@
 // allocation, for callers that cannot allocate when they run the model (see
 // include/dlrm.h). The working buffers (bag sums, two activation buffers, the
 // interaction output) are slices of one fixed file-scope device array.
-#include <atomic>
-
 #include "common.cuh"
 
 namespace {
@@ -14,23 +12,14 @@ constexpr size_t kScratchBytes = DLRM_NOALLOC_SCRATCH_BYTES;
 // symbol: kernels must be given the device address looked up below.
 __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::atomic<void*> g_scratch_addr[kMaxDevices];
-
-// Device address of the scratch on the current device, looked up once per
-// device (with that device current) and cached.
+// Device address of the scratch on the current device. Looked up on every
+// call (cudaGetSymbolAddress is cheap): an address cached across calls would
+// dangle after a device reset, which reloads the module elsewhere.
 cudaError_t scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
-  if (!p) {
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return e;
-    if (!p) return cudaErrorInvalidSymbol;
-    g_scratch_addr[dev].store(p, std::memory_order_release);
-  }
+  if (!p) return cudaErrorInvalidSymbol;
   *out = p;
   return cudaSuccess;
 }

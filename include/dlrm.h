@@ -279,10 +279,11 @@ void dlrm_destroy(dlrm_handle_t h);
  * array, so calls whose work overlaps on the GPU (different streams, or
  * different host threads, without ordering between them) race and corrupt
  * each other's results: serialise them, e.g. on one stream.
- * Set-up: the first call on a device looks up the array's device address
- * (cudaGetSymbolAddress, once per device, with that device current); make
- * that first call before any stream capture. The call allocates nothing:
- * no cudaMalloc, cudaFree or allocating library routine. */
+ * Set-up: every call looks up the array's device address on the current
+ * device (cudaGetSymbolAddress), so calls stay valid after a device reset.
+ * The first call on a device may load the library's device code: make that
+ * first call before any stream capture. The call allocates nothing: no
+ * cudaMalloc, cudaFree or allocating library routine. */
 dlrm_status_t dlrm_forward_noalloc(const dlrm_config_t* cfg, const float* const* tables,
                                    const float* const* bot_w, const float* const* bot_b,
                                    const float* const* top_w, const float* const* top_b,

@@ -402,12 +402,19 @@ def test_forward_reports_device_errors_and_clears_them(path):
 
 
 def test_forward_rejects_batch_above_max():
+    """Refused twice over: by the binding's shape check (ValueError) and, called
+    through the C ABI directly, by the library (INVALID_ARG, nothing launched)."""
+    import ctypes
     cfg = synth.get_config("tiny_b64_k3")
     inp = synth.make_inputs(cfg, seed=8)
     model = make_model(cfg, inp, max_batch=32)
-    with pytest.raises(dl.DlrmError) as ei:
-        model.forward(cu(inp["dense"]), cu(inp["indices"]), cu(inp["offsets"]))
-    assert ei.value.status == dl.ERR_INVALID_ARG
+    dense, idx, off = cu(inp["dense"]), cu(inp["indices"]), cu(inp["offsets"])
+    out = torch.empty(cfg.batch, device="cuda")
+    with pytest.raises(ValueError):
+        model.forward(dense, idx, off, out)
+    st = dl.lib().dlrm_forward(ctypes.c_void_p(model.handle), dl._ptr(dense), dl._ptr(idx),
+                               dl._ptr(off), dl._ptr(out), cfg.batch, dl._stream(None))
+    assert st == dl.ERR_INVALID_ARG
     model.close()
 
 
