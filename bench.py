@@ -574,8 +574,8 @@ def run_ours(args, rank, world, local_rank):
         # (slot 20 + g) while the phase stamps end below slot 20
         n_bot = len(cfg.ln_bot) - 1
         n_gemm = n_bot + len(cfg.ln_top) - 2
-        split = args.math == "fp32" and n_gemm + 3 < 20
-        kacc = np.zeros((n_gemm, 2))
+        split = args.math == "fp32" and n_gemm + 3 < 20 and n_gemm <= 10
+        kacc = np.zeros((n_gemm, 3))
         span = 0.0
         reps = 20
         with torch.cuda.stream(stream):
@@ -594,6 +594,8 @@ def run_ours(args, rank, world, local_rank):
                         kend = full[:, 20 + g]
                         kacc[g, 0] += (kend - full[:, first]).mean() / 1e3
                         kacc[g, 1] += (full[:, first + 1] - kend).mean() / 1e3
+                        # cycles warp 0 waited for weight stages, as us at the max clock
+                        kacc[g, 2] += full[:, 30 + g].mean() / pk["sm_max_mhz"]
         model.set_phase_trace(None)
         phases_us = {n: float(v / reps) for n, v in zip(pnames, acc)}
         phases_us["kernel_span"] = span / reps
@@ -601,6 +603,8 @@ def run_ours(args, rank, world, local_rank):
             names_g = [pnames[1 + g] if g < n_bot else pnames[2 + g] for g in range(n_gemm)]
             phases_us["gemm_kloop_epilogue"] = {
                 n: [float(kacc[g, 0] / reps), float(kacc[g, 1] / reps)] for g, n in enumerate(names_g)}
+            phases_us["gemm_weight_wait"] = {
+                n: float(kacc[g, 2] / reps) for g, n in enumerate(names_g)}
     dom = max(stage_us, key=stage_us.get)
     flops, byts = stage_work(cfg, dom, cfg.batch)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count

@@ -19,12 +19,13 @@
 //    producer warp that each copy a quarter of every stage (one thread's
 //    copies are serialised), running ahead across layer boundaries while
 //    eight warps compute.
-//  * a computing warp owns TM rows (the whole tile up to 8 rows, else half
-//    of it: 7 at 14-row tiles), broadcast-read from the activation buffer,
-//    and 32 * TN columns (one column per lane, TN per thread) of one 16-wide
-//    k-slice of each stage; the register tile (7 x 4 at 14 rows)
-//    accumulates with packed fma.rn.f32x2, and the k-slices' partial sums
-//    meet in shared memory.
+//  * a computing warp covers all BM rows of the tile and 64 columns (fewer
+//    in layers of 32 columns) of one k-slice of each stage: lane bit 0
+//    picks the row parity and the other bits a group of columns, so each
+//    128-bit shared load reads two activation rows or eight weight columns
+//    per half-warp, one wavefront each. The lane's register tile (BM / 2
+//    rows x 4 columns: 7 x 4 at 14-row tiles) accumulates with packed
+//    fma.rn.f32x2, and the k-slices' partial sums meet in shared memory.
 //  * biases and the last layer's weights are fetched with cp.async once per
 //    CTA; per tile, one round of global loads checks the bags and fetches
 //    the dense rows, and (bag size 1) the tile's embedding rows follow by
@@ -62,10 +63,11 @@ __device__ __forceinline__ uint64_t global_ns() {
 // Phase trace (profiling): the consumer leader stamps when tile `tile`
 // finishes phase `slot`.
 // Profiling: where GEMM layer g's leader stamps the end of its k-loop
-// (trace slot 20 + g), or null.
+// (trace slot 20 + g; slot 30 + g then receives the SM cycles warp 0 spent
+// waiting for the layer's weight stages), or null.
 __device__ __forceinline__ unsigned long long* kloop_stamp(const FusedParams& p, int tile, int g) {
   // slots 20.. are free only while the phase stamps (up to n_gemm + 3) end below
-  return (p.trace && p.n_gemm + 3 < 20 && 20 + g < kFusedTraceSlots)
+  return (p.trace && p.n_gemm + 3 < 20 && 30 + g < kFusedTraceSlots)
              ? p.trace + static_cast<size_t>(tile) * kFusedTraceSlots + 20 + g
              : nullptr;
 }
@@ -305,54 +307,66 @@ __device__ void produce(const Ring& r, const float* wstream, const uint2* tab, u
 // C (BM x n_pad; zero beyond n) = act(A (BM x k_pad) W^T + b). `pos` is the
 // warp's place in the stage sequence shared with the producer.
 //
-// Warp roles: the BM rows form RG = BM / TM row groups of TM rows; warp w
-// takes row group w % RG and slot w / RG of the SLOTS = 8 / RG slots of its
-// group. A slot is a (column group, k-slice) pair: a stage holds KS = 16 *
-// ksplit values of k for `gemm_rows` output columns; it is cut into KSLICES =
-// KS / KSL slices of KSL k (KSL / 4 steps of 4) and SLOTS / KSLICES column
-// groups of 32 * TN columns. Every tile height reads the same packed stream.
-// All 32 lanes of a warp read the same activation rows, so those 128-bit
-// shared loads are broadcasts (2 wavefronts); lane l owns columns l + 32 j
-// (j < TN), whose staged weight rows are consecutive across lanes (the chunk
-// swizzle puts 8 consecutive rows on 8 distinct bank groups: 4 wavefronts per
-// load). Per 4-wide k step a thread issues TM + TN loads for 4 * TM * TN FMAs
-// as packed fma.rn.f32x2 (the even-k and odd-k partial sums of an output in
-// one float2). Shared-memory wavefronts, not FMA issue, bound this loop: per
-// packed FMA 2 / TM (weights) + 1 / TN (activations) + 1 / (2 BM) (the bulk
-// copy writing the stage), against 1/2 SM cycle of FMA pipe; TM = TN = 8
-// balances the two at BM = 16.
-// The k-slices' partial sums meet in shared memory (the output buffer and,
-// once every warp is done reading it, the input buffer) and all threads add
-// them, the bias and the activation.
-template <int BM, int TM, int TN, int KSL, int KSPLIT, int CW>
-__device__ void gemm_layer(const FusedGemm& L, float* a_s, float* c_s, int lda,
+// Lane roles: every warp covers all BM rows. Lane bit 0 picks a row parity
+// (the lane's TM = BM / 2 rows are rg, rg + 2, ...) and the other lane bits
+// one of 16 lane column groups: lane column group lcg = lane / 2 owns the
+// warp's columns lcg + 16 j (j < TN), WCOLS = 16 TN columns in all.
+// Warp roles: warp w takes column group w % CGS of a pass (CGS = the pass's
+// columns / WCOLS) and k-slice w / CGS of every stage (KSLICES = CW / CGS
+// slices of KSL = KS / KSLICES values of k, KSL / 4 steps of 4).
+// Shared-memory cost: a 128-bit load is served per half-warp, in one
+// wavefront when the half-warp's distinct 16-byte words sit in distinct bank
+// groups. A half-warp's activation load reads two rows (adjacent rows are
+// four banks apart: lda = 4 mod 32) and its weight load eight consecutive
+// staged columns (the chunk swizzle puts eight consecutive rows of a stage
+// in eight bank groups), so every load costs two wavefronts per warp: per
+// 4-wide k step (TM + TN) loads, 2 (TM + TN) wavefronts, for 2 TM TN packed
+// FMAs (the even-k and odd-k partial sums of an output in one float2):
+// 0.39 wavefronts per packed FMA at 7 x 4, against 1/2 SM cycle of FMA
+// pipe; the bulk copy that writes the stage adds 2 / BM.
+// The k-slices' partial sums meet in the output buffer (set q at columns
+// q * n_pad of each row) and, for the sets past lda / n_pad, the input
+// buffer (the planner makes lda >= ceil(KSLICES / 2) * n_pad), where all threads add
+// them, the bias and the activation. Layers split into several k-slices have
+// a single pass (n_pad <= 256).
+constexpr int kDoubleBufferMax = 56;   // lane tile outputs that leave room for it
+
+template <int BM, int TN, int CGS, int KSPLIT, int CW, int LDA>
+__device__ void gemm_layer(const FusedGemm& L, float* a_s, float* c_s, int lda_rt,
                            const float* __restrict__ bias_s, int act, const Ring& r, RingPos& pos,
                            unsigned long long* kstamp) {
-  constexpr int RG = BM / TM;
-  constexpr int SLOTS = CW / RG;               // warp slots per row group
+  // the activation row stride: a compile-time constant for the common
+  // widths (row addresses become immediate offsets), else the plan's
+  const int lda = LDA > 0 ? LDA : lda_rt;
+  constexpr int R = 2;                         // row parities per warp
+  constexpr int TM = BM / R;                   // rows per lane
+  constexpr int LCG = kWarp / R;               // lane column groups
+  constexpr int WCOLS = LCG * TN;              // columns of one warp
+  constexpr int KSLICES = CW / CGS;
   constexpr int KS = 16 * KSPLIT;              // k per stage
-  constexpr int KSLICES = KS / KSL;
-  constexpr int CGS = SLOTS / KSLICES;         // column groups per pass
-  static_assert(CW == 8 && BM % TM == 0 && CGS >= 1 && KS % KSL == 0, "warp slots");
-  static_assert(KSLICES <= 2 * KSPLIT, "partial sets fit the output and input buffers");
-  constexpr int STEPS = KSL / 4;               // 4-wide k steps per stage
+  constexpr int KSL = KS / KSLICES;            // k per warp per stage
+  constexpr int STEPS = KSL / 4;               // 4-wide k steps per warp per stage
   constexpr int CPR = KS / 4;                  // 16-byte chunks per staged row
-  constexpr int WCOLS = 32 * TN;               // columns of one warp
+  static_assert(BM % R == 0 && CW % CGS == 0 && KS % KSLICES == 0 && STEPS >= 1, "warp slots");
+  static_assert(KSLICES == 1 || KSPLIT == 2, "k-sliced layers are the single-pass ones");
   // fragments of step s + 1 load while step s computes, when registers allow
-  constexpr bool kDoubleBuffer = TM * TN <= 32;
+  constexpr bool kDoubleBuffer = TM * TN <= kDoubleBufferMax;
   const int tid = threadIdx.x;
   const int warp = tid / kWarp;
   const int lane = tid % kWarp;
-  const int rg = warp % RG;
-  const int slot = warp / RG;
-  const int cg = slot % CGS;
-  const int kslice = slot / CGS;
-  const int sw = CPR == 4 ? ((lane >> 1) & 3) : (lane & 7);   // swizzle of rows lane + 32 j
+  const int rg = lane % R;
+  const int lcg = lane / R;
+  const int cg = warp % CGS;
+  const int kslice = warp / CGS;
+  // chunk swizzle of the lane's staged rows cg * WCOLS + 16 j + lcg: the
+  // same for every j (16 j and cg * WCOLS are multiples of 8)
+  const int sw = CPR == 4 ? ((lcg >> 1) & 3) : (lcg & 7);
   int ph[STEPS];
 #pragma unroll
   for (int s = 0; s < STEPS; ++s) ph[s] = ((kslice * STEPS + s) ^ sw) * 4;
-  const float* a_base = a_s + rg * TM * lda + kslice * KSL;
+  const float* a_base = a_s + rg * lda + kslice * KSL;
   const int per_pass = CGS * WCOLS;
+  long long waited = 0;   // profiling: cycles spent waiting for stages
 
   for (int pass = 0; pass < L.passes; ++pass) {
     const bool active = cg * WCOLS < gemm_rows(L, pass);
@@ -364,17 +378,24 @@ __device__ void gemm_layer(const FusedGemm& L, float* a_s, float* c_s, int lda,
 
     for (int kst = 0; kst < L.n_kst; ++kst, pos.advance(r.s_count)) {
       const uint32_t st = pos.slot;
-      wait_phase<true>(smem_u32(&r.full[st]), pos.phase, r.abort_flag, r.err);
+      if (kstamp) {   // profiling (uniform): time the wait
+        const long long t0 = clock64();
+        wait_phase<true>(smem_u32(&r.full[st]), pos.phase, r.abort_flag, r.err);
+        waited += clock64() - t0;
+      } else {
+        wait_phase<true>(smem_u32(&r.full[st]), pos.phase, r.abort_flag, r.err);
+      }
       if (active) {
-        const float* ws = r.stages + st * kFusedStageFloats + (cg * WCOLS + lane) * KS;
+        const float* ws = r.stages + st * kFusedStageFloats + (cg * WCOLS + lcg) * KS;
         const float* as = a_base + kst * KS;
         if (kDoubleBuffer) {
           float4 wv[2][TN], av[2][TM];
 #pragma unroll
           for (int j = 0; j < TN; ++j)
-            wv[0][j] = *reinterpret_cast<const float4*>(ws + 32 * j * KS + ph[0]);
+            wv[0][j] = *reinterpret_cast<const float4*>(ws + LCG * j * KS + ph[0]);
 #pragma unroll
-          for (int i = 0; i < TM; ++i) av[0][i] = *reinterpret_cast<const float4*>(as + i * lda);
+          for (int i = 0; i < TM; ++i)
+            av[0][i] = *reinterpret_cast<const float4*>(as + R * i * lda);
 #pragma unroll
           for (int step = 0; step < STEPS; ++step) {
             const int cur = step & 1;
@@ -382,10 +403,11 @@ __device__ void gemm_layer(const FusedGemm& L, float* a_s, float* c_s, int lda,
 #pragma unroll
               for (int j = 0; j < TN; ++j)
                 wv[cur ^ 1][j] =
-                    *reinterpret_cast<const float4*>(ws + 32 * j * KS + ph[step + 1]);
+                    *reinterpret_cast<const float4*>(ws + LCG * j * KS + ph[step + 1]);
 #pragma unroll
               for (int i = 0; i < TM; ++i)
-                av[cur ^ 1][i] = *reinterpret_cast<const float4*>(as + i * lda + 4 * (step + 1));
+                av[cur ^ 1][i] =
+                    *reinterpret_cast<const float4*>(as + R * i * lda + 4 * (step + 1));
             }
             // component-outer: TM * TN independent accumulators between the
             // two dependent updates of each
@@ -408,10 +430,10 @@ __device__ void gemm_layer(const FusedGemm& L, float* a_s, float* c_s, int lda,
             float4 wf[TN];
 #pragma unroll
             for (int j = 0; j < TN; ++j)
-              wf[j] = *reinterpret_cast<const float4*>(ws + 32 * j * KS + ph[step]);
+              wf[j] = *reinterpret_cast<const float4*>(ws + LCG * j * KS + ph[step]);
 #pragma unroll
             for (int i = 0; i < TM; ++i) {
-              const float4 a = *reinterpret_cast<const float4*>(as + i * lda + 4 * step);
+              const float4 a = *reinterpret_cast<const float4*>(as + R * i * lda + 4 * step);
 #pragma unroll
               for (int j = 0; j < TN; ++j)
                 acc[i][j] = __ffma2_rn(make_float2(a.x, a.y), make_float2(wf[j].x, wf[j].y),
@@ -427,121 +449,93 @@ __device__ void gemm_layer(const FusedGemm& L, float* a_s, float* c_s, int lda,
       ring_release(r, st);
     }
 
-    // profiling: the leader stamps the end of the layer's k-loop
-    if (kstamp && pass + 1 == L.passes && threadIdx.x == 0) *kstamp = global_ns();
-    const int c0 = pass * per_pass + cg * WCOLS + lane;
+    // profiling: the leader stamps the end of the layer's k-loop and the
+    // cycles it waited for weight stages
+    if (kstamp && pass + 1 == L.passes && threadIdx.x == 0) {
+      kstamp[0] = global_ns();
+      kstamp[10] = static_cast<unsigned long long>(waited);
+    }
+    const int c0 = pass * per_pass + cg * WCOLS + lcg;   // the lane's first column
     if (KSLICES == 1) {
       if (active) {
 #pragma unroll
         for (int j = 0; j < TN; ++j) {
-          const int n = c0 + 32 * j;
+          const int n = c0 + LCG * j;
           const float bv = bias_s[L.b_off + n];
 #pragma unroll
           for (int i = 0; i < TM; ++i) {
             const float v = apply_act((acc[i][j].x + acc[i][j].y) + bv, act);
-            c_s[(rg * TM + i) * lda + n] = (n < L.n) ? v : 0.f;
+            c_s[(rg + R * i) * lda + n] = (n < L.n) ? v : 0.f;
           }
         }
       }
       consumer_sync<CW>();
-    } else if (pass + 1 == L.passes) {
-      // Parallel reduction. Once every warp is past its k-loop the layer's
-      // input is dead: partial set q goes to the output buffer (q < KSPLIT)
-      // or the input buffer (q >= KSPLIT), at columns (q % KSPLIT) * n_pad
-      // + the pass's column; then all threads add the sets, add the bias and
-      // apply the activation. Single-pass layers have n_pad = per_pass and
-      // rows of lda >= KSPLIT * n_pad floats.
-      if (KSLICES > KSPLIT) consumer_sync<CW>();   // the input becomes scratch
+    } else {
+      // Parallel reduction (one pass: c0 is the column within n_pad). The
+      // k-slices' partial sums go to the output buffer, set q at columns
+      // q * n_pad for q < qo = lda / n_pad, and the rest to the input buffer
+      // (dead once every warp is past its k-loop) at columns (q - qo) *
+      // n_pad; then all threads add the sets, the bias and the activation,
+      // writing over set 0.
+      const int np = L.n_pad;
+      const int qo = lda / np;
+      if (KSLICES > qo) consumer_sync<CW>();   // the input becomes scratch
       if (active) {
-        float* dst = kslice < KSPLIT ? c_s + kslice * L.n_pad + c0
-                                     : a_s + (kslice - KSPLIT) * L.n_pad + c0 - pass * per_pass;
+        float* dst = (kslice < qo ? c_s + kslice * np : a_s + (kslice - qo) * np) + c0;
 #pragma unroll
         for (int i = 0; i < TM; ++i)
 #pragma unroll
-          for (int j = 0; j < TN; ++j) dst[(rg * TM + i) * lda + 32 * j] = acc[i][j].x + acc[i][j].y;
+          for (int j = 0; j < TN; ++j)
+            dst[(rg + R * i) * lda + LCG * j] = acc[i][j].x + acc[i][j].y;
       }
       consumer_sync<CW>();
-      const int np = gemm_rows(L, pass);
-      const int col0 = pass * per_pass;
       const int q_shift = 31 - __clz(np >> 2);          // np / 4 is a power of two
       for (int e = tid; e < BM * (np >> 2); e += CW * kWarp) {
         const int m = e >> q_shift;
         const int n = (e - (m << q_shift)) << 2;
-        const float* base_c = c_s + m * lda + n;
+        const float* base = c_s + m * lda + n;
         const float* base_a = a_s + m * lda + n;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 v = *reinterpret_cast<const float4*>(base);
 #pragma unroll
-        for (int q = 0; q < KSLICES; ++q) {
-          const float4 u = *reinterpret_cast<const float4*>(
-              (q < KSPLIT ? base_c : base_a) + (q % KSPLIT) * L.n_pad + (q < KSPLIT ? col0 : 0));
+        for (int q = 1; q < KSLICES; ++q) {
+          const float4 u =
+              *reinterpret_cast<const float4*>(q < qo ? base + q * np : base_a + (q - qo) * np);
           v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w;
         }
-        const int nn = col0 + n;
-        const float4 bv = *reinterpret_cast<const float4*>(bias_s + L.b_off + nn);
-        v.x = (nn + 0 < L.n) ? apply_act(v.x + bv.x, act) : 0.f;
-        v.y = (nn + 1 < L.n) ? apply_act(v.y + bv.y, act) : 0.f;
-        v.z = (nn + 2 < L.n) ? apply_act(v.z + bv.z, act) : 0.f;
-        v.w = (nn + 3 < L.n) ? apply_act(v.w + bv.w, act) : 0.f;
-        *reinterpret_cast<float4*>(c_s + m * lda + nn) = v;
+        const float4 bv = *reinterpret_cast<const float4*>(bias_s + L.b_off + n);
+        v.x = (n + 0 < L.n) ? apply_act(v.x + bv.x, act) : 0.f;
+        v.y = (n + 1 < L.n) ? apply_act(v.y + bv.y, act) : 0.f;
+        v.z = (n + 2 < L.n) ? apply_act(v.z + bv.z, act) : 0.f;
+        v.w = (n + 3 < L.n) ? apply_act(v.w + bv.w, act) : 0.f;
+        *reinterpret_cast<float4*>(c_s + m * lda + n) = v;
       }
       consumer_sync<CW>();
-    } else {
-      // A pass before the last of a multi-pass layer (the input is still
-      // live): k-slice q adds its partial sums to those of slices 0 .. q-1
-      // in place, the last one adding the bias and applying the activation.
-#pragma unroll 1
-      for (int q = 0; q < KSLICES; ++q) {
-        if (kslice == q && active) {
-#pragma unroll
-          for (int j = 0; j < TN; ++j) {
-            const int n = c0 + 32 * j;
-            const float bv = bias_s[L.b_off + n];
-#pragma unroll
-            for (int i = 0; i < TM; ++i) {
-              float* dst = c_s + (rg * TM + i) * lda + n;
-              float v = acc[i][j].x + acc[i][j].y;
-              if (q > 0) v += *dst;
-              if (q == KSLICES - 1) v = (n < L.n) ? apply_act(v + bv, act) : 0.f;
-              *dst = v;
-            }
-          }
-        }
-        consumer_sync<CW>();
-      }
     }
   }
 }
 
-template <int BM, int CW>
+template <int BM, int CW, int LDA>
 __device__ void gemm_dispatch(const FusedGemm& L, float* a_s, float* c_s, int lda,
                               const float* bias_s, int act, int zero_to, const Ring& r,
                               RingPos& pos, unsigned long long* kstamp) {
-  // TM rows per warp (the whole tile up to 8 rows, else two row groups of
-  // BM / 2), k-slices of KSL. A pass covers 64 * tn / ksplit columns with
-  // SLOTS / (16 * ksplit / KSL) column groups, which fixes the lane width TN
-  // (at least 1). (8-wide k-slices for layers of 64 columns or fewer, where
-  // every warp spans all columns, measured slower at 14-row tiles.)
-  constexpr int TM = BM <= 8 ? BM : BM / 2;
-  constexpr int SLOTS = CW * TM / BM;
-#define DLRM_GEMM_TN(TN16_, KS_, KSL_)                                               \
-  ((2 * (TN16_) / (KS_)) / (SLOTS / (16 * (KS_) / (KSL_))) > 0                       \
-       ? (2 * (TN16_) / (KS_)) / (SLOTS / (16 * (KS_) / (KSL_)))                     \
-       : 1)
-#define DLRM_GEMM_CASE(TN16_, KS_, KSL_)                                             \
-  gemm_layer<BM, TM, DLRM_GEMM_TN(TN16_, KS_, KSL_), KSL_, KS_, CW>(L, a_s, c_s, lda, bias_s, \
-                                                                    act, r, pos, kstamp)
+  // Stage geometry (fused_plan): wider than 256 columns, 512 columns x 16 k
+  // per stage (8 warp column groups of 64); 256 columns x 32 k, 2 column
+  // groups of 128 (lane tiles BM / 2 x 8) x 4 k-slices; else n_pad = 32 * tn
+  // columns x 32 k, cut into n_pad / 64 column groups (at least one) and the
+  // rest of the warps as k-slices.
+#define DLRM_GEMM_CASE(TN_, CGS_, KSPLIT_) \
+  gemm_layer<BM, TN_, CGS_, KSPLIT_, CW, LDA>(L, a_s, c_s, lda, bias_s, act, r, pos, kstamp)
   if (L.ksplit == 1) {
-    DLRM_GEMM_CASE(8, 1, 16);
+    DLRM_GEMM_CASE(4, 8, 1);
   } else {
     switch (L.tn) {
-      case 8: DLRM_GEMM_CASE(8, 2, 16); break;
-      case 4: DLRM_GEMM_CASE(4, 2, 16); break;
-      case 2: DLRM_GEMM_CASE(2, 2, 16); break;
-      default: DLRM_GEMM_CASE(1, 2, 16); break;
+      case 8: DLRM_GEMM_CASE(8, 2, 2); break;     // 256 columns
+      case 4: DLRM_GEMM_CASE(4, 2, 2); break;     // 128
+      case 2: DLRM_GEMM_CASE(4, 1, 2); break;     // 64
+      default: DLRM_GEMM_CASE(2, 1, 2); break;    // 32
     }
   }
 #undef DLRM_GEMM_CASE
-#undef DLRM_GEMM_TN
   const int extra = zero_to - L.n_pad;
   for (int e = threadIdx.x; e < BM * extra; e += CW * kWarp) {
     const int m = e / extra;
@@ -554,11 +548,12 @@ __device__ void gemm_dispatch(const FusedGemm& L, float* a_s, float* c_s, int ld
 // tile, which also fetches the biases and last-layer weights (they stay in
 // shared memory for the CTA's later tiles). `pos` carries the CTA's place in
 // the weight stream from tile to tile.
-template <int BM, int CW>
+template <int BM, int CW, int LDA>
 __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, float* act1, float* zs,
                         int* rowidx_s, float* bias_s, float* wlast_s, int tile, bool first,
                         RingPos& pos) {
   constexpr int kConsumers = CW * kWarp;
+  const int lda = LDA > 0 ? LDA : p.lda;   // activation row stride
   const int tid = threadIdx.x;
   const int m0 = tile * BM;
   const int rows = min(BM, p.batch - m0);
@@ -621,7 +616,7 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
         }
         if (e < n_dense) {
           const int m = e / kp;
-          act0[m * p.lda + (e - m * kp)] = dv[h];
+          act0[m * lda + (e - m * kp)] = dv[h];
         }
       }
     }
@@ -671,7 +666,7 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
   float* out = act1;
   for (int g = 0; g < p.n_bot; ++g) {
     const int zero_to = (g + 1 < p.n_bot) ? p.gemm[g + 1].k_pad : p.gemm[g].n_pad;
-    gemm_dispatch<BM, CW>(p.gemm[g], in, out, p.lda, bias_s, DLRM_ACT_RELU, zero_to, ring, pos,
+    gemm_dispatch<BM, CW, LDA>(p.gemm[g], in, out, lda, bias_s, DLRM_ACT_RELU, zero_to, ring, pos,
                           kloop_stamp(p, tile, g));
     float* t = in; in = out; out = t;
     stamp(p, tile, 2 + g);
@@ -684,8 +679,8 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
   for (int e = tid; e < BM * rk; e += kConsumers) {
     const int m = e / rk;
     const int c = e - m * rk;
-    if (c < d) r[m * p.lda + c] = x[m * p.lda + c];
-    else if (c >= d + pairs) r[m * p.lda + c] = 0.f;
+    if (c < d) r[m * lda + c] = x[m * lda + c];
+    else if (c >= d + pairs) r[m * lda + c] = 0.f;
   }
   if (p.prefetch_z) cp_async_wait<0>();
   // zbuf == 2: groups 0 and 1 were issued in the prologue; group g + 2
@@ -735,13 +730,13 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
       for (int e = tid; e < ns * nblk; e += kConsumers) {
         const int s = e / nblk;
         const int q = e - s * nblk;
-        const float* xrow = x + (g0 + s) * p.lda;
+        const float* xrow = x + (g0 + s) * lda;
         const float* zsam = zg + s * k * p.ldz;
         float acc[4][4];
         int bi, bj;
         gram_block([&](int rr) { return rr == 0 ? xrow : zsam + (rr - 1) * p.ldz; }, f, d4, q,
                    bi, bj, acc);
-        float* o = r + (g0 + s) * p.lda + d;
+        float* o = r + (g0 + s) * lda + d;
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
           const int i = 4 * bi + a;
@@ -758,8 +753,8 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
         const int q = e - s * pairs;
         int i, j;
         pair_from_index(q, i, j);
-        const float* vi = (i == 0) ? x + (g0 + s) * p.lda : zg + (s * k + i - 1) * p.ldz;
-        const float* vj = (j == 0) ? x + (g0 + s) * p.lda : zg + (s * k + j - 1) * p.ldz;
+        const float* vi = (i == 0) ? x + (g0 + s) * lda : zg + (s * k + i - 1) * p.ldz;
+        const float* vj = (j == 0) ? x + (g0 + s) * lda : zg + (s * k + j - 1) * p.ldz;
         float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
         for (int c4 = 0; c4 < d4; ++c4) {
@@ -770,7 +765,7 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
           a.z = fmaf(u.z, w.z, a.z);
           a.w = fmaf(u.w, w.w, a.w);
         }
-        r[(g0 + s) * p.lda + d + q] = (a.x + a.y) + (a.z + a.w);
+        r[(g0 + s) * lda + d + q] = (a.x + a.y) + (a.z + a.w);
       }
     }
     consumer_sync<CW>();
@@ -790,7 +785,7 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
   out = (r == act0) ? act1 : act0;
   for (int g = p.n_bot; g < p.n_gemm; ++g) {
     const int zero_to = (g + 1 < p.n_gemm) ? p.gemm[g + 1].k_pad : p.k_last;
-    gemm_dispatch<BM, CW>(p.gemm[g], in, out, p.lda, bias_s, DLRM_ACT_RELU, zero_to, ring, pos,
+    gemm_dispatch<BM, CW, LDA>(p.gemm[g], in, out, lda, bias_s, DLRM_ACT_RELU, zero_to, ring, pos,
                           kloop_stamp(p, tile, g));
     float* t = in; in = out; out = t;
     stamp(p, tile, 3 + g);
@@ -801,7 +796,7 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
   for (int m = warp; m < rows; m += CW) {
     float acc = 0.f;
     for (int q = lane; q < k4; q += kWarp) {
-      const float4 a = *reinterpret_cast<const float4*>(in + m * p.lda + 4 * q);
+      const float4 a = *reinterpret_cast<const float4*>(in + m * lda + 4 * q);
       const float4 w = *reinterpret_cast<const float4*>(wlast_s + 4 * q);
       acc = fmaf(a.x, w.x, acc);
       acc = fmaf(a.y, w.y, acc);
@@ -817,8 +812,25 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
   stamp(p, tile, 2 + p.n_gemm + 1);
 }
 
-template <int BM, int CW>
-__global__ void __launch_bounds__((CW + 1) * 32, 1)
+// Warps: CW = 8 computing warps (warpgroups 0 and 1) and a producer
+// warpgroup (warps 8-11) of which warp 8 streams the weights. At launch
+// every thread has kLaunchRegs registers (the cap for 12 warps: three share
+// one sub-partition's 16K); the producer warpgroup then gives most of its
+// registers back (setmaxnreg.dec to kProducerRegs) and the computing
+// warpgroups take them (setmaxnreg.inc to kComputeRegs), so a computing
+// thread holds a BM / 2 x 8 lane tile with double-buffered operands. The
+// split adds up exactly to the launch allocation (checked below); the host
+// refuses an instance that ptxas built with a different launch count.
+constexpr int kFusedWarps = 12;
+constexpr int kLaunchRegs = 168;
+constexpr int kProducerRegs = 40;
+constexpr int kComputeRegs = 232;
+static_assert(8 * kWarp * kComputeRegs + 4 * kWarp * kProducerRegs <=
+                  kFusedWarps * kWarp * kLaunchRegs,
+              "register split exceeds the launch allocation");
+
+template <int BM, int CW, int LDA>
+__global__ void __launch_bounds__(kFusedWarps * 32, 1)
 fused_forward_kernel(const __grid_constant__ FusedParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   float* stages = reinterpret_cast<float*>(smem_raw);
@@ -846,7 +858,10 @@ fused_forward_kernel(const __grid_constant__ FusedParams p) {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   __syncthreads();
-  if (warp == CW) {
+  static_assert(CW == 8, "two computing warpgroups");
+  if (warp >= CW) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs) : "memory");
+    if (warp > CW) return;
     // the L2 prefetch from a lane that issues no copies: a thread's bulk
     // operations run one after another
     if (threadIdx.x % kWarp == kWarp - 1) prefetch_stream_l2(p.wstream, p.stream_floats);
@@ -854,13 +869,14 @@ fused_forward_kernel(const __grid_constant__ FusedParams p) {
             static_cast<uint32_t>(my_tiles));
     return;
   }
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kComputeRegs) : "memory");
   RingPos pos;
   for (int i = 0; i < my_tiles; ++i)
-    consume<BM, CW>(p, r, act0, act1, zs, rowidx_s, bias_s, wlast_s,
+    consume<BM, CW, LDA>(p, r, act0, act1, zs, rowidx_s, bias_s, wlast_s,
                     static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x), i == 0, pos);
 }
 
-template <int BM, int CW>
+template <int BM, int CW, int LDA>
 cudaError_t enable_smem() {
   static std::atomic<uint64_t> done{0};
   int dev = 0;
@@ -868,7 +884,13 @@ cudaError_t enable_smem() {
   if (e != cudaSuccess) return e;
   const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
   if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
-  e = cudaFuncSetAttribute(fused_forward_kernel<BM, CW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  // the register split in the kernel assumes exactly kLaunchRegs per thread
+  // at launch: any other count could leave setmaxnreg.inc waiting forever
+  cudaFuncAttributes attr{};
+  e = cudaFuncGetAttributes(&attr, fused_forward_kernel<BM, CW, LDA>);
+  if (e != cudaSuccess) return e;
+  if (attr.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(fused_forward_kernel<BM, CW, LDA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(device_max_smem_optin()));
   if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
   return e;
@@ -876,16 +898,35 @@ cudaError_t enable_smem() {
 
 }  // namespace
 
-cudaError_t fused_prepare(int bm, int cw) {
-  if (cw != 8) return cudaErrorInvalidValue;
-  switch (bm) {
-    case 16: return enable_smem<16, 8>();
-    case 14: return enable_smem<14, 8>();
-    case 12: return enable_smem<12, 8>();
-    case 8: return enable_smem<8, 8>();
-    case 4: return enable_smem<4, 8>();
-    default: return cudaErrorInvalidValue;
+// Kernel instances: every tile height with a run-time activation row stride,
+// and the tile heights of 8 rows and more with the strides the workload
+// models take (516: widest layer or interaction row <= 512 floats; 612: the
+// 32-table models' 592-wide interaction rows) as compile-time constants.
+#define DLRM_FUSED_SWITCH(BM_VAR, LDA_VAR, CALL)                                     \
+  switch ((BM_VAR) * 10000 + (((BM_VAR) >= 8 && ((LDA_VAR) == 516 || (LDA_VAR) == 612)) \
+                                  ? (LDA_VAR)                                          \
+                                  : 0)) {                                              \
+    case 16 * 10000 + 516: CALL(16, 516); break;                                       \
+    case 16 * 10000 + 612: CALL(16, 612); break;                                       \
+    case 16 * 10000: CALL(16, 0); break;                                               \
+    case 14 * 10000 + 516: CALL(14, 516); break;                                       \
+    case 14 * 10000 + 612: CALL(14, 612); break;                                       \
+    case 14 * 10000: CALL(14, 0); break;                                               \
+    case 12 * 10000 + 516: CALL(12, 516); break;                                       \
+    case 12 * 10000 + 612: CALL(12, 612); break;                                       \
+    case 12 * 10000: CALL(12, 0); break;                                               \
+    case 8 * 10000 + 516: CALL(8, 516); break;                                         \
+    case 8 * 10000 + 612: CALL(8, 612); break;                                         \
+    case 8 * 10000: CALL(8, 0); break;                                                 \
+    case 4 * 10000: CALL(4, 0); break;                                                 \
+    default: return cudaErrorInvalidValue;                                             \
   }
+
+cudaError_t fused_prepare(int bm, int cw, int lda) {
+  if (cw != 8) return cudaErrorInvalidValue;
+#define DLRM_PREPARE(BM_, LDA_) return enable_smem<BM_, 8, LDA_>()
+  DLRM_FUSED_SWITCH(bm, lda, DLRM_PREPARE)
+#undef DLRM_PREPARE
 }
 
 cudaError_t launch_fused(const FusedParams& p, int bm, cudaStream_t stream) {
@@ -893,16 +934,13 @@ cudaError_t launch_fused(const FusedParams& p, int bm, cudaStream_t stream) {
   // persistent: at most one CTA per SM, each looping over its tiles
   const int64_t tiles = (p.batch + bm - 1) / bm;
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(tiles, device_sm_count()));
-  cudaError_t e = fused_prepare(bm, p.cw);
+  cudaError_t e = fused_prepare(bm, p.cw, p.lda);
   if (e != cudaSuccess) return e;
-  const unsigned threads = static_cast<unsigned>((p.cw + 1) * kWarp);
-  switch (bm) {
-    case 16: fused_forward_kernel<16, 8><<<grid, threads, p.smem_bytes, stream>>>(p); break;
-    case 14: fused_forward_kernel<14, 8><<<grid, threads, p.smem_bytes, stream>>>(p); break;
-    case 12: fused_forward_kernel<12, 8><<<grid, threads, p.smem_bytes, stream>>>(p); break;
-    case 8: fused_forward_kernel<8, 8><<<grid, threads, p.smem_bytes, stream>>>(p); break;
-    default: fused_forward_kernel<4, 8><<<grid, threads, p.smem_bytes, stream>>>(p); break;
-  }
+  const unsigned threads = static_cast<unsigned>(kFusedWarps * kWarp);
+#define DLRM_LAUNCH(BM_, LDA_) \
+  fused_forward_kernel<BM_, 8, LDA_><<<grid, threads, p.smem_bytes, stream>>>(p)
+  DLRM_FUSED_SWITCH(bm, p.lda, DLRM_LAUNCH)
+#undef DLRM_LAUNCH
   return cudaGetLastError();
 }
 
@@ -918,6 +956,15 @@ int swizzle_of(int row, int cpr) {
 
 size_t align128(size_t x) { return (x + 127) / 128 * 128; }
 
+// k-slices a stage of layer L is cut into among the 8 computing warps (the
+// partial-sum sets of each output): 1 for layers wider than 256 columns (8
+// column groups of 64 per pass), 4 for 256 columns (2 column groups of 128),
+// else 8 / column groups, with n_pad / 64 column groups (at least one).
+int fused_kslices(const FusedGemm& L) {
+  if (L.ksplit == 1) return 1;
+  return L.n_pad == 256 ? 4 : 8 / std::max(1, L.n_pad / 64);
+}
+
 }  // namespace
 
 bool fused_plan(int n_dense, int k_tables, int d, int bag, const std::vector<int>& ln_bot,
@@ -925,7 +972,7 @@ bool fused_plan(int n_dense, int k_tables, int d, int bag, const std::vector<int
                 const std::vector<std::vector<float>>& b, const GatherTables& tabs,
                 int max_batch, int sms, size_t smem_limit, int cw, FusedPlan* plan) {
   if (cw != 8) return false;
-  const int ksl = 16;           // k per warp slice per stage
+  const int ksl = 16;           // k per stage at ksplit 1 (32 at ksplit 2)
   const int n_bot = static_cast<int>(ln_bot.size()) - 1;
   const int n_top = static_cast<int>(ln_top.size()) - 1;
   const int n_gemm = n_bot + n_top - 1;
@@ -976,7 +1023,9 @@ bool fused_plan(int n_dense, int k_tables, int d, int bag, const std::vector<int
     L.n_kst = L.k_pad / (ksl * L.ksplit);
     L.b_off = bias_floats;
     bias_floats += L.n_pad;
-    widest = std::max({widest, L.k_pad, L.n_pad * L.ksplit});
+    // the k-slices' partial sums sit side by side in the rows of the two
+    // activation buffers
+    widest = std::max({widest, L.k_pad, L.n_pad * ((fused_kslices(L) + 1) / 2)});
   }
   p.k_last = static_cast<int>(round_up(ln_top[n_top - 1], 4));
   p.b_last = bias_floats;

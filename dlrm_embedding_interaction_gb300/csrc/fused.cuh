@@ -8,7 +8,8 @@
 
 namespace dlrm {
 
-// Warps per CTA: 8 computing warps and one producer warp.
+// Warps per CTA: 8 computing warps (two warpgroups) and a producer warpgroup
+// whose first warp streams the weights (fused.cu, fused_forward_kernel).
 constexpr int kFusedStageFloats = 8192;                        // 32 KB weight stage
 constexpr int kFusedMaxGemm = 2 * DLRM_MAX_LAYERS;
 
@@ -20,7 +21,8 @@ constexpr int kFusedMaxGemm = 2 * DLRM_MAX_LAYERS;
 // else r & 7).
 //   n      output width; wider than 256: n_pad = round_up(n, 256), tn = 8,
 //          ksplit = 1; else n_pad = 32 * tn (tn a power of two), ksplit = 2
-//   tn     columns per lane when the tile's rows form 4 row groups
+//   tn     the stage's columns per pass / 32 (each computing warp takes 64
+//          of them, or all 32 when tn = 1, for one k-slice)
 //   k_pad  input width padded to a multiple of KS (zero weights)
 //   b_off  offset of the layer's zero-padded bias in the bias block
 struct FusedGemm {
@@ -81,7 +83,7 @@ bool fused_plan(int n_dense, int k_tables, int d, int bag, const std::vector<int
                 const std::vector<std::vector<float>>& b, const GatherTables& tabs,
                 int max_batch, int sms, size_t smem_limit, int consumer_warps, FusedPlan* plan);
 
-cudaError_t fused_prepare(int bm, int consumer_warps);
+cudaError_t fused_prepare(int bm, int consumer_warps, int lda);
 cudaError_t launch_fused(const FusedParams& p, int bm, cudaStream_t stream);
 
 }  // namespace dlrm

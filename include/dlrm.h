@@ -232,9 +232,11 @@ dlrm_status_t dlrm_set_profiling(dlrm_handle_t h, int32_t enable);
  * the bottom layers, 2+n_bot the interaction, 3+n_bot .. 1+n_bot+n_top the top
  * layers but the last, 2+n_bot+n_top the end (sigmoid layer written). While
  * those slots end below 20, the slots from 20 on profile each GEMM layer g
- * (bottom layers, then top layers but the last): fp32, slot 20 + g = when its
- * k-loop ended; TF32/BF16, slots 20 + 2g and 21 + 2g = nanoseconds the MMA
- * thread waited for the layer's input activations and for its weight tiles.
+ * (bottom layers, then top layers but the last): fp32 (for g < 10), slot
+ * 20 + g = when its k-loop ended and slot 30 + g = the SM clock cycles
+ * computing warp 0 spent waiting for the layer's weight stages; TF32/BF16,
+ * slots 20 + 2g and 21 + 2g = nanoseconds the MMA thread waited for the
+ * layer's input activations and for its weight tiles.
  * Needs capacity >= tiles(max_batch) * DLRM_TRACE_SLOTS (INVALID_ARG
  * otherwise; UNSUPPORTED on a layer-wise handle); NULL switches it off.
  * Returns the tile height in *tile_rows. */
