@@ -30,7 +30,7 @@ EXPORTS = ("dlrm_version", "dlrm_status_string", "dlrm_create", "dlrm_forward",
            "dlrm_forward_noalloc", "dlrm_set_phase_trace", "dlrm_plan_query",
            "embedding_bag_sum_multi", "embedding_bag_multi", "embedding_bag_multi_ex",
            "pairwise_dot_lower_tri",
-           "pairwise_pair_map", "linear_bias_act")
+           "pairwise_pair_map", "linear_bias_act", "dlrm_test_stall")
 NOALLOC_SCRATCH_BYTES = 16 << 20
 TRACE_SLOTS = 40
 
@@ -75,6 +75,7 @@ def _bind(lib):
         "dlrm_forward": ([vp, vp, vp, vp, vp, i32, vp], st),
         "dlrm_forward_host": ([vp, vp, vp, vp, vp, i32, vp], st),
         "dlrm_get_error": ([vp, vp], st),
+        "dlrm_test_stall": ([vp, i64, i32], st),
         "dlrm_workspace_bytes": ([vp], i64),
         "dlrm_destroy": ([vp], None),
         "dlrm_path": ([vp], i32),
@@ -497,6 +498,17 @@ def dlrm_forward_noalloc(ln_bot: Sequence[int], ln_top: Sequence[int], tables: S
 
 def dlrm_get_error(h: int, stream=None) -> int:
     return int(lib().dlrm_get_error(ctypes.c_void_p(h), _stream(stream)))
+
+
+def dlrm_test_stall(h: int, wait_limit_ns: int = 0, withhold_last: bool = False) -> None:
+    """Failure-detection test hook: the limit of every bounded device wait of
+    later forwards on ``h`` (0: the default) and, with ``withhold_last``, each
+    kernel skips the last copy or tensor-core commit of its stream so that the
+    wait on it runs out (``dlrm_get_error`` then reports ERR_TIMEOUT).
+    ``dlrm_test_stall(h)`` restores normal operation."""
+    _handle_shape(h, "dlrm_test_stall")
+    _check(lib().dlrm_test_stall(ctypes.c_void_p(h), int(wait_limit_ns), 1 if withhold_last else 0),
+           "dlrm_test_stall")
 
 
 def dlrm_workspace_bytes(h: int) -> int:

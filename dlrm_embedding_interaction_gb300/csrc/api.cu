@@ -96,6 +96,7 @@ struct dlrm_handle_s {
   bool fused_tc = false;         // the fused plan runs on the tensor cores (TF32 / BF16)
   dlrm::FusedTcParams tcp{};
   unsigned long long* trace = nullptr;
+  dlrm::WaitCfg wait{};          // dlrm_test_stall: wait limit, withheld last copy
   // per-stage profiling (dlrm_set_profiling)
   std::vector<std::string> stage_names;
   std::vector<cudaEvent_t> events;      // stage boundaries, empty when off
@@ -143,6 +144,7 @@ dlrm_status_t run_forward(dlrm_handle_t h, const float* dense, const int64_t* in
     p.out = out;
     p.err = h->err;
     p.trace = h->trace;
+    p.wait = h->wait;
     if (h->fused_tc) {
       dlrm::FusedTcParams q = h->tcp;
       q.batch = batch;
@@ -152,6 +154,7 @@ dlrm_status_t run_forward(dlrm_handle_t h, const float* dense, const int64_t* in
       q.out = out;
       q.err = h->err;
       q.trace = h->trace;
+      q.wait = h->wait;
       e = dlrm::launch_fused_tc(q, s);
     } else {
       e = dlrm::launch_fused(p, h->fused_bm, s);
@@ -171,7 +174,7 @@ dlrm_status_t run_forward(dlrm_handle_t h, const float* dense, const int64_t* in
                       int ldy, int n, int k, int act) {
       if (h->math != DLRM_MATH_FP32 && n >= 16)
         return dlrm::launch_linear_tc(x, ldx, w, ldw, b, y, ldy, batch, n, k, act,
-                                      static_cast<int>(h->math), h->err, s);
+                                      static_cast<int>(h->math), h->err, s, h->wait);
       return dlrm::launch_linear_fp32(x, ldx, w, ldw, b, y, ldy, batch, n, k, act, s);
     };
     for (int l = 0; l < h->n_bot; ++l) {
@@ -679,6 +682,13 @@ dlrm_status_t dlrm_get_error(dlrm_handle_t h, void* stream) {
   if (bits & DLRM_ERRBIT_INDEX_OOB) return DLRM_ERR_INDEX_OOB;
   if (bits & DLRM_ERRBIT_OFFSETS) return DLRM_ERR_UNSUPPORTED;
   if (bits & DLRM_ERRBIT_TIMEOUT) return DLRM_ERR_TIMEOUT;
+  return DLRM_OK;
+}
+
+dlrm_status_t dlrm_test_stall(dlrm_handle_t h, int64_t wait_limit_ns, int32_t withhold_last) {
+  if (!h || wait_limit_ns < 0) return DLRM_ERR_INVALID_ARG;
+  h->wait.limit_ns = static_cast<uint64_t>(wait_limit_ns);
+  h->wait.withhold_last = withhold_last ? 1 : 0;
   return DLRM_OK;
 }
 

@@ -85,6 +85,21 @@ __device__ __forceinline__ void gram_block(const RowFn& row, int f, int d4, int 
   }
 }
 
+// Bounded waits of a launch. Every wait of a kernel on another party (a
+// weight stage or tile landing, a ring slot being released, tensor-core work
+// completing) gives up after limit_ns (0: the default of 2 s), sets
+// DLRM_ERRBIT_TIMEOUT and lets the kernel finish without the data. For
+// failure-detection tests, withhold_last makes the kernel skip the last copy
+// (or tensor-core commit) of its stream, so that the wait on it runs out.
+struct WaitCfg {
+  uint64_t limit_ns = 0;
+  int withhold_last = 0;
+};
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+__host__ __device__ __forceinline__ uint64_t wait_limit_ns(const WaitCfg& w) {
+  return w.limit_ns ? w.limit_ns : kDefaultWaitNs;
+}
+
 // Kernel-parameter table for the multi-table gather: K (pointer, rows) pairs
 // passed by value so a launch needs no device-side staging buffer.
 struct GatherTables {
@@ -118,7 +133,7 @@ cudaError_t launch_linear_fp32(const float* x, int ld_x, const float* w, int ld_
 // accumulation; err (nullable) receives DLRM_ERRBIT_TIMEOUT on a stuck wait.
 cudaError_t launch_linear_tc(const float* x, int ld_x, const float* w, int ld_w, const float* bias,
                              float* y, int ld_y, int m, int n, int k, int act, int mode,
-                             int32_t* err, cudaStream_t stream);
+                             int32_t* err, cudaStream_t stream, WaitCfg wait = WaitCfg{});
 
 int device_sm_count();
 size_t device_max_smem_optin();

@@ -32,9 +32,10 @@
 //    cp.async and land during the bottom MLP; bag sums and pair dots then run
 //    from shared memory and build R = [x, z] in place; the N = 1 sigmoid
 //    layer is a warp-per-row dot.
-// Every mbarrier wait is bounded (%globaltimer, 2 s): on expiry the kernel
-// sets DLRM_ERRBIT_TIMEOUT, stops waiting and finishes its control flow;
-// before exiting it waits (bounded) for any copies still in flight.
+// Every mbarrier wait is bounded (%globaltimer; 2 s unless the launch sets
+// another limit): on expiry the kernel sets DLRM_ERRBIT_TIMEOUT, stops
+// waiting and finishes its control flow; before exiting it waits (bounded)
+// for any copies still in flight.
 // Rows past the batch are computed on zeros and never stored.
 #include <atomic>
 
@@ -43,8 +44,6 @@
 
 namespace dlrm {
 namespace {
-
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -165,7 +164,7 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 constexpr uint32_t kSuspendNs = 20000;
 template <bool SPIN>
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                           int32_t* err) {
+                                           int32_t* err, uint64_t limit_ns) {
   if (mbar_test_wait(bar, parity)) return true;
   if (*abort_flag) return false;
   const uint64_t t0 = global_ns();
@@ -174,7 +173,7 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
       return true;
     if (!SPIN || (i & 63) == 0) {
       if (*abort_flag) return false;
-      if (global_ns() - t0 > kWaitLimitNs) {
+      if (global_ns() - t0 > limit_ns) {
         *abort_flag = 1;
         if (err) atomicOr(reinterpret_cast<unsigned int*>(err), DLRM_ERRBIT_TIMEOUT);
         return false;
@@ -209,6 +208,7 @@ struct Ring {
   volatile int* abort_flag;
   uint32_t s_count;
   int32_t* err;
+  uint64_t limit_ns;   // bound of every wait
 };
 
 // A consumer's place in the stream: the slot of its next stage (stage % S)
@@ -258,9 +258,11 @@ __device__ void prefetch_stream_l2(const float* wstream, size_t floats) {
 constexpr uint32_t kIssuers = 4;
 constexpr unsigned kIssuerMask = (1u << kIssuers) - 1;
 
-// The stage table runs once per tile of the CTA (n_tiles passes).
+// The stage table runs once per tile of the CTA (n_tiles passes). With
+// withhold_last (failure-detection tests) the stream's last stage is never
+// copied: the computing warps' wait on it runs out.
 __device__ void produce(const Ring& r, const float* wstream, const uint2* tab, uint32_t n_tab,
-                        uint32_t n_tiles) {
+                        uint32_t n_tiles, bool withhold_last) {
   const uint32_t lane = threadIdx.x % kWarp;
   if (lane >= kIssuers) return;
   const char* src0 = reinterpret_cast<const char*>(wstream);
@@ -268,9 +270,10 @@ __device__ void produce(const Ring& r, const float* wstream, const uint2* tab, u
   uint32_t j = 0, slot = 0, phase = 0;   // slot = j % S, phase = (j / S) & 1
   uint32_t jt = 0;                       // j % n_tab
   for (; j < n_stages; ++j) {
-    const bool ok = j < r.s_count ||
-                    wait_phase<false>(smem_u32(&r.empty[slot]), phase ^ 1, r.abort_flag, r.err);
+    const bool ok = j < r.s_count || wait_phase<false>(smem_u32(&r.empty[slot]), phase ^ 1,
+                                                         r.abort_flag, r.err, r.limit_ns);
     if (!__all_sync(kIssuerMask, ok)) break;
+    if (withhold_last && j + 1 == n_stages) break;   // not issued: not drained below
     const uint2 e = __ldg(tab + jt);
     if (++jt == n_tab) jt = 0;
     const uint32_t full = smem_u32(&r.full[slot]);
@@ -294,7 +297,7 @@ __device__ void produce(const Ring& r, const float* wstream, const uint2* tab, u
     const uint32_t bar = smem_u32(&r.full[q % r.s_count]);
     const uint64_t t0 = global_ns();
     while (!mbar_try_wait(bar, (q / r.s_count) & 1)) {
-      if (global_ns() - t0 > kWaitLimitNs) {
+      if (global_ns() - t0 > r.limit_ns) {
         if (r.err) atomicOr(reinterpret_cast<unsigned int*>(r.err), DLRM_ERRBIT_TIMEOUT);
         break;
       }
@@ -380,10 +383,10 @@ __device__ void gemm_layer(const FusedGemm& L, float* a_s, float* c_s, int lda_r
       const uint32_t st = pos.slot;
       if (kstamp) {   // profiling (uniform): time the wait
         const long long t0 = clock64();
-        wait_phase<true>(smem_u32(&r.full[st]), pos.phase, r.abort_flag, r.err);
+        wait_phase<true>(smem_u32(&r.full[st]), pos.phase, r.abort_flag, r.err, r.limit_ns);
         waited += clock64() - t0;
       } else {
-        wait_phase<true>(smem_u32(&r.full[st]), pos.phase, r.abort_flag, r.err);
+        wait_phase<true>(smem_u32(&r.full[st]), pos.phase, r.abort_flag, r.err, r.limit_ns);
       }
       if (active) {
         const float* ws = r.stages + st * kFusedStageFloats + (cg * WCOLS + lcg) * KS;
@@ -843,7 +846,8 @@ fused_forward_kernel(const __grid_constant__ FusedParams p) {
   uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw + p.off_bar);
   uint64_t* empty = full + p.stages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + p.stages);
-  const Ring r{stages, full, empty, abort_flag, static_cast<uint32_t>(p.stages), p.err};
+  const Ring r{stages, full, empty, abort_flag, static_cast<uint32_t>(p.stages), p.err,
+               wait_limit_ns(p.wait)};
   const int warp = threadIdx.x / kWarp;
   // persistent: CTA c runs tiles c, c + gridDim.x, ...
   const int n_tiles = (p.batch + BM - 1) / BM;
@@ -866,7 +870,7 @@ fused_forward_kernel(const __grid_constant__ FusedParams p) {
     // operations run one after another
     if (threadIdx.x % kWarp == kWarp - 1) prefetch_stream_l2(p.wstream, p.stream_floats);
     produce(r, p.wstream, p.stage_tab, static_cast<uint32_t>(p.n_stages),
-            static_cast<uint32_t>(my_tiles));
+            static_cast<uint32_t>(my_tiles), p.wait.withhold_last != 0);
     return;
   }
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kComputeRegs) : "memory");

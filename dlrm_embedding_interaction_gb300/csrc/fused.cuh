@@ -59,6 +59,7 @@ struct FusedParams {
   float* out;
   int32_t* err;
   unsigned long long* trace;   // optional phase stamps, kFusedTraceSlots per tile
+  WaitCfg wait;                // wait limit; failure tests: the last stage withheld
   GatherTables tabs;
 };
 

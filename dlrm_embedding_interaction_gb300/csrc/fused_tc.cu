@@ -27,9 +27,10 @@
 //    MMA warp, then fetch the bag rows (cp.async for bags of one row, sums in
 //    registers for longer bags); they compute the pair dots into R (fp32,
 //    from an fp32 copy of x) and the last layer's fp32 dot and sigmoid.
-// Every wait is bounded (%globaltimer, 2 s): on expiry the kernel sets
-// DLRM_ERRBIT_TIMEOUT, stops issuing and waiting, and still frees its tensor
-// memory and waits (bounded) for its copies in flight.
+// Every wait is bounded (%globaltimer; 2 s unless the launch sets another
+// limit): on expiry the kernel sets DLRM_ERRBIT_TIMEOUT, stops issuing and
+// waiting, waits (bounded) for its copies in flight and for every MMA it
+// issued, and still frees its tensor memory.
 #include <atomic>
 #include <cstring>
 
@@ -47,7 +48,6 @@ constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kThreads = 6 * kWarp;
 constexpr int kActBlock = kTcTile * 128;           // one K-block of the B operand (bytes)
-constexpr uint64_t kWaitNs = 2000000000ull;
 
 __device__ __forceinline__ void stamp(const FusedTcParams& p, int slot) {
   if (p.trace && threadIdx.x == 0)
@@ -102,7 +102,7 @@ __device__ __forceinline__ bool try_wait_suspend(uint32_t bar, uint32_t parity) 
 // sleep in the barrier between polls.
 template <bool SPIN>
 __device__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                             int32_t* err) {
+                             int32_t* err, uint64_t limit_ns) {
   if (test_wait(bar, parity)) return true;
   if (*abort_flag) return false;
   const uint64_t t0 = now_ns();
@@ -110,7 +110,7 @@ __device__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_
     if (SPIN ? test_wait(bar, parity) : try_wait_suspend(bar, parity)) return true;
     if (!SPIN || (i & 63) == 0) {
       if (*abort_flag) return false;
-      if (now_ns() - t0 > kWaitNs) {
+      if (now_ns() - t0 > limit_ns) {
         *abort_flag = 1;
         if (err) atomicOr(reinterpret_cast<unsigned int*>(err), DLRM_ERRBIT_TIMEOUT);
         return false;
@@ -219,10 +219,14 @@ __device__ void produce(const FusedTcParams& p, unsigned char* ring, uint64_t* f
   const uint32_t s_count = static_cast<uint32_t>(p.stages);
   const uint32_t n = static_cast<uint32_t>(p.n_tiles);
   uint32_t j = 0, slot = 0, phase = 0;   // slot = j % S, phase = (j / S) & 1
+  const uint64_t limit = wait_limit_ns(p.wait);
   for (; j < n; ++j) {
-    const bool ok =
-        j < s_count || wait_bounded<false>(smem_addr(&empty[slot]), phase ^ 1, abort_flag, p.err);
+    const bool ok = j < s_count || wait_bounded<false>(smem_addr(&empty[slot]), phase ^ 1,
+                                                       abort_flag, p.err, limit);
     if (!__all_sync(kIssuerMask, ok)) break;
+    // failure-detection tests: the last tile is never copied, so the MMA
+    // thread's wait on it runs out (not issued: not drained below)
+    if (p.wait.withhold_last && j + 1 == n) break;
     const uint32_t bar = smem_addr(&full[slot]);
     if (lane == 0) mbar_arrive_expect_tx(bar, kTcTileBytes);
     __syncwarp(kIssuerMask);
@@ -240,7 +244,7 @@ __device__ void produce(const FusedTcParams& p, unsigned char* ring, uint64_t* f
     const uint32_t bar = smem_addr(&full[q % s_count]);
     const uint64_t t0 = now_ns();
     while (!try_wait(bar, (q / s_count) & 1)) {
-      if (now_ns() - t0 > kWaitNs) {
+      if (now_ns() - t0 > limit) {
         if (p.err) atomicOr(reinterpret_cast<unsigned int*>(p.err), DLRM_ERRBIT_TIMEOUT);
         break;
       }
@@ -251,15 +255,17 @@ __device__ void produce(const FusedTcParams& p, unsigned char* ring, uint64_t* f
 template <bool BF16>
 __device__ void issue_mmas(const FusedTcParams& p, uint32_t tmem, unsigned char* ring,
                            unsigned char* const act[2], uint64_t* full, uint64_t* empty,
-                           uint64_t* acc_ready, uint64_t* act_ready, volatile int* abort_flag) {
+                           uint64_t* acc_ready, uint64_t* act_ready, uint64_t* drain,
+                           volatile int* abort_flag) {
   constexpr uint32_t kIdesc = instr_desc(BF16 ? 1u : 2u, kTcTile);
   const uint32_t s_count = static_cast<uint32_t>(p.stages);
+  const uint64_t limit = wait_limit_ns(p.wait);
   bool ok = true;
   uint32_t slot = 0, phase = 0;   // of stream tile j: j % S and (j / S) & 1
   for (int g = 0; g < p.n_gemm; ++g) {
     const TcGemm& L = p.gemm[g];
     const uint64_t ta = p.trace ? now_ns() : 0;
-    if (ok) ok = wait_bounded<true>(smem_addr(act_ready), g & 1, abort_flag, p.err);
+    if (ok) ok = wait_bounded<true>(smem_addr(act_ready), g & 1, abort_flag, p.err, limit);
     uint64_t act_wait = p.trace ? now_ns() - ta : 0, tile_wait = 0;
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t b_base = smem_addr(act[g & 1]);
@@ -268,7 +274,7 @@ __device__ void issue_mmas(const FusedTcParams& p, uint32_t tmem, unsigned char*
     for (int kb = 0; kb < L.kbs; ++kb) {
       for (int mt = 0; mt < L.mts; ++mt) {
         const uint64_t tw = p.trace ? now_ns() : 0;
-        if (ok) ok = wait_bounded<true>(smem_addr(&full[slot]), phase, abort_flag, p.err);
+        if (ok) ok = wait_bounded<true>(smem_addr(&full[slot]), phase, abort_flag, p.err, limit);
         if (p.trace) tile_wait += now_ns() - tw;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         if (ok) {
@@ -293,6 +299,18 @@ __device__ void issue_mmas(const FusedTcParams& p, uint32_t tmem, unsigned char*
       unsigned long long* t = p.trace + static_cast<size_t>(blockIdx.x) * kTcTraceSlots;
       t[20 + 2 * g] = act_wait;
       t[21 + 2 * g] = tile_wait;
+    }
+  }
+  // Every MMA must have run before the CTA frees its tensor memory, also when
+  // a wait gave up and the epilogue skipped its own waits: one more commit on
+  // a barrier of its own (a single phase, so its parity is unambiguous)
+  // tracks them all; wait for it, bounded.
+  mma_commit(smem_addr(drain));
+  const uint64_t t0 = now_ns();
+  while (!try_wait(smem_addr(drain), 0)) {
+    if (now_ns() - t0 > limit) {
+      if (p.err) atomicOr(reinterpret_cast<unsigned int*>(p.err), DLRM_ERRBIT_TIMEOUT);
+      break;
     }
   }
 }
@@ -421,7 +439,7 @@ __device__ void epilogue(const FusedTcParams& p, uint32_t tmem, unsigned char* c
     const TcGemm& L = p.gemm[g];
     const bool last_bottom = g == p.n_bot - 1;
     const bool last_hidden = g == p.n_gemm - 1;
-    wait_bounded<false>(smem_addr(acc_ready), g & 1, abort_flag, p.err);
+    wait_bounded<false>(smem_addr(acc_ready), g & 1, abort_flag, p.err, wait_limit_ns(p.wait));
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     unsigned char* out = act[(g + 1) & 1];
     for (int mt = 0; mt < L.mts; ++mt) {
@@ -555,7 +573,8 @@ fused_tc_kernel(const __grid_constant__ FusedTcParams p) {
   uint64_t* empty = full + p.stages;
   uint64_t* acc_ready = empty + p.stages;
   uint64_t* act_ready = acc_ready + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(act_ready + 1);
+  uint64_t* drain = act_ready + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const int warp = threadIdx.x / kWarp;
   stamp(p, 0);
@@ -573,6 +592,7 @@ fused_tc_kernel(const __grid_constant__ FusedTcParams p) {
     }
     mbar_init(smem_addr(acc_ready), 1);
     mbar_init(smem_addr(act_ready), 1);
+    mbar_init(smem_addr(drain), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -585,7 +605,8 @@ fused_tc_kernel(const __grid_constant__ FusedTcParams p) {
     produce(p, ring, full, empty, abort_flag);
   } else if (warp == kMmaWarp) {
     if (threadIdx.x % kWarp == 0)
-      issue_mmas<BF16>(p, tmem, ring, act, full, empty, acc_ready, act_ready, abort_flag);
+      issue_mmas<BF16>(p, tmem, ring, act, full, empty, acc_ready, act_ready, drain,
+                       abort_flag);
   } else {
     epilogue<BF16>(p, tmem, act, xf, hf, zs, rowidx_s, bias_s, wlast_s, acc_ready, act_ready,
                    abort_flag);
@@ -710,7 +731,7 @@ bool fused_tc_plan(int n_dense, int k_tables, int d, int bag, const std::vector<
       align_up(static_cast<size_t>(bias_floats) * 4, 128) + align_up(p.k_last * 4, 128);
   int stages = 0;
   for (int s = 12; s >= 2; --s) {         // the deepest ring that fits
-    const size_t bars = align_up((2 * s + 2) * 8 + 16, 128);
+    const size_t bars = align_up((2 * s + 3) * 8 + 16, 128);
     if (1024 + static_cast<size_t>(s) * kTcTileBytes + fixed_tail + bars <= smem_limit) {
       stages = s;
       break;
@@ -736,7 +757,7 @@ bool fused_tc_plan(int n_dense, int k_tables, int d, int bag, const std::vector<
   p.off_wlast = static_cast<int>(off);
   off += align_up(p.k_last * 4, 128);
   p.off_bar = static_cast<int>(off);
-  off += align_up((2 * stages + 2) * 8 + 16, 128);
+  off += align_up((2 * stages + 3) * 8 + 16, 128);   // full, empty, acc/act ready, drain
   p.smem_bytes = static_cast<int>(off + 1024);
   if (static_cast<size_t>(p.smem_bytes) > smem_limit) return false;
 

@@ -45,6 +45,7 @@ struct FusedTcParams {
   float* out;
   int32_t* err;
   unsigned long long* trace;      // optional phase stamps, kTcTraceSlots per tile
+  WaitCfg wait;                   // wait limit; failure tests: the last tile withheld
   GatherTables tabs;
 };
 

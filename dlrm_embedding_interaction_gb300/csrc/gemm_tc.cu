@@ -27,8 +27,9 @@
 //    about 2^-21 relative, inside the fp32 parity tolerance;
 //  * epilogue: each warp reads its 32 TMEM lanes (rows) with tcgen05.ld
 //    32x32b, adds the bias, applies ReLU/sigmoid and stores.
-// Every mbarrier wait is bounded (%globaltimer); on expiry the kernel sets
-// its error flag, stops issuing MMAs and still frees its TMEM.
+// Every mbarrier wait is bounded (%globaltimer; 2 s unless the launch sets
+// another limit); on expiry the kernel sets its error flag, stops issuing
+// MMAs, waits (bounded) for the MMAs it issued and still frees its TMEM.
 #include <atomic>
 
 #include "common.cuh"
@@ -41,16 +42,15 @@ using namespace tc;
 
 constexpr int kTcThreads = 128;
 constexpr int kTcM = tc::kM;
-constexpr uint64_t kTcWaitNs = 2000000000ull;
 
 enum TcMode { kTF32 = 0, kBF16 = 1, kTF32x3 = 2 };
 
 // Bounded wait; false on timeout (the caller sets the error flag).
-__device__ bool wait_bar(uint32_t bar, uint32_t parity) {
+__device__ bool wait_bar(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   if (try_wait(bar, parity)) return true;
   const uint64_t t0 = now_ns();
   while (!try_wait(bar, parity))
-    if (now_ns() - t0 > kTcWaitNs) return false;
+    if (now_ns() - t0 > limit_ns) return false;
   return true;
 }
 
@@ -153,7 +153,7 @@ template <int MODE, int NT>
 __global__ void __launch_bounds__(kTcThreads, 1)
 gemm_tc_kernel(const float* __restrict__ x, int ldx, const float* __restrict__ w, int ldw,
                const float* __restrict__ bias, float* __restrict__ y, int ldy, int m, int n, int k,
-               int act, int vec_x, int vec_w, int32_t* err) {
+               int act, int vec_x, int vec_w, int32_t* err, WaitCfg wait) {
   using Lay = TcLayout<MODE, NT>;
   constexpr int kStages = Lay::kStages;
   constexpr bool BF16 = MODE == kBF16;
@@ -172,6 +172,7 @@ gemm_tc_kernel(const float* __restrict__ x, int ldx, const float* __restrict__ w
   constexpr uint32_t kIdesc = instr_desc(BF16 ? 1u : 2u, NT);
   const int kb_count = (k + kBlockK - 1) / kBlockK;
   const bool async = !BF16 && vec_x && vec_w;
+  const uint64_t limit = wait_limit_ns(wait);
 
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -217,7 +218,8 @@ gemm_tc_kernel(const float* __restrict__ x, int ldx, const float* __restrict__ w
     // the MMAs of that older block (kStages - 2 iterations back)
     if (kb + 2 < kb_count) {
       const int old = kb + 2 - kStages;
-      if (old >= 0 && ok) ok = wait_bar(smem_addr(&bars[old % kStages]), (old / kStages) & 1);
+      if (old >= 0 && ok)
+        ok = wait_bar(smem_addr(&bars[old % kStages]), (old / kStages) & 1, limit);
       stage_block(kb + 2);
     } else {
       asm volatile("cp.async.commit_group;\n" ::: "memory");
@@ -249,15 +251,26 @@ gemm_tc_kernel(const float* __restrict__ x, int ldx, const float* __restrict__ w
           mma<false>(tmem, la + off, db + off, kIdesc, 1u);   // lo * hi
         }
       }
-      mma_commit(smem_addr(&bars[s]));
+      // failure-detection tests: the last block's commit is withheld, so
+      // the wait on it below runs out
+      if (!(wait.withhold_last && kb + 1 == kb_count)) mma_commit(smem_addr(&bars[s]));
     }
   }
   // all MMAs done: the last commit's stage barrier
   if (kb_count > 0 && ok) {
     const int last = kb_count - 1;
-    ok = wait_bar(smem_addr(&bars[last % kStages]), (last / kStages) & 1);
+    ok = wait_bar(smem_addr(&bars[last % kStages]), (last / kStages) & 1, limit);
   }
   if (!ok && threadIdx.x == 0 && err) atomicOr(reinterpret_cast<unsigned int*>(err), DLRM_ERRBIT_TIMEOUT);
+  // After a wait gave up, MMAs may still be running: before the tensor memory
+  // is read or freed, thread 0 commits once more on the spare barrier (one
+  // phase: its parity is unambiguous), which tracks every MMA it issued, and
+  // waits for it (bounded); the others meet it at the barrier below.
+  if (!ok && threadIdx.x == 0) {
+    mma_commit(smem_addr(&bars[kStages]));
+    wait_bar(smem_addr(&bars[kStages]), 0, limit);
+  }
+  __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 
   // Epilogue: warp w owns TMEM lanes (rows) 32w .. 32w+31.
@@ -294,7 +307,7 @@ gemm_tc_kernel(const float* __restrict__ x, int ldx, const float* __restrict__ w
 template <int MODE, int NT>
 cudaError_t launch_mode(const float* x, int ld_x, const float* w, int ld_w, const float* bias,
                         float* y, int ld_y, int m, int n, int k, int act, int vec_x, int vec_w,
-                        int32_t* err, cudaStream_t stream) {
+                        int32_t* err, cudaStream_t stream, WaitCfg wait) {
   static std::atomic<uint64_t> done{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -309,29 +322,30 @@ cudaError_t launch_mode(const float* x, int ld_x, const float* w, int ld_w, cons
   }
   const dim3 grid((m + kTcM - 1) / kTcM, (n + NT - 1) / NT);
   gemm_tc_kernel<MODE, NT><<<grid, kTcThreads, kSmem, stream>>>(x, ld_x, w, ld_w, bias, y, ld_y,
-                                                                m, n, k, act, vec_x, vec_w, err);
+                                                                m, n, k, act, vec_x, vec_w, err,
+                                                                wait);
   return cudaGetLastError();
 }
 
 template <int MODE>
 cudaError_t launch_tiles(const float* x, int ld_x, const float* w, int ld_w, const float* bias,
                          float* y, int ld_y, int m, int n, int k, int act, int vec_x, int vec_w,
-                         int32_t* err, cudaStream_t stream) {
+                         int32_t* err, cudaStream_t stream, WaitCfg wait) {
   const int64_t tiles128 = static_cast<int64_t>((m + kTcM - 1) / kTcM) * ((n + 127) / 128);
   if (tiles128 >= device_sm_count() || n <= 64)
     return n <= 64 ? launch_mode<MODE, 64>(x, ld_x, w, ld_w, bias, y, ld_y, m, n, k, act, vec_x,
-                                           vec_w, err, stream)
+                                           vec_w, err, stream, wait)
                    : launch_mode<MODE, 128>(x, ld_x, w, ld_w, bias, y, ld_y, m, n, k, act, vec_x,
-                                            vec_w, err, stream);
+                                            vec_w, err, stream, wait);
   return launch_mode<MODE, 64>(x, ld_x, w, ld_w, bias, y, ld_y, m, n, k, act, vec_x, vec_w, err,
-                               stream);
+                               stream, wait);
 }
 
 }  // namespace
 
 cudaError_t launch_linear_tc(const float* x, int ld_x, const float* w, int ld_w, const float* bias,
                              float* y, int ld_y, int m, int n, int k, int act, int mode,
-                             int32_t* err, cudaStream_t stream) {
+                             int32_t* err, cudaStream_t stream, WaitCfg wait) {
   if (m == 0) return cudaSuccess;
   auto aligned = [](const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; };
   const int vec_x = (ld_x % 4 == 0 && aligned(x)) ? 1 : 0;
@@ -339,13 +353,13 @@ cudaError_t launch_linear_tc(const float* x, int ld_x, const float* w, int ld_w,
   switch (mode) {
     case DLRM_MATH_BF16:
       return launch_tiles<kBF16>(x, ld_x, w, ld_w, bias, y, ld_y, m, n, k, act, vec_x, vec_w, err,
-                                 stream);
+                                 stream, wait);
     case DLRM_MATH_TF32X3:
       return launch_tiles<kTF32x3>(x, ld_x, w, ld_w, bias, y, ld_y, m, n, k, act, vec_x, vec_w,
-                                   err, stream);
+                                   err, stream, wait);
     default:
       return launch_tiles<kTF32>(x, ld_x, w, ld_w, bias, y, ld_y, m, n, k, act, vec_x, vec_w, err,
-                                 stream);
+                                 stream, wait);
   }
 }
 

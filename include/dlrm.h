@@ -198,6 +198,22 @@ dlrm_status_t dlrm_forward_host(dlrm_handle_t h, const float* dense_host,
  * none) and clears it. */
 dlrm_status_t dlrm_get_error(dlrm_handle_t h, void* stream);
 
+/* Test hook of the failure detection; no counterpart on the pages. Every
+ * wait of the library's kernels on another party (a weight stage or tile
+ * landing in shared memory, a ring slot being released, tensor-core work
+ * completing) is bounded: on expiry the kernel sets DLRM_ERRBIT_TIMEOUT in the
+ * handle's error word, stops waiting, waits (bounded) for the copies and
+ * tensor-core work it issued, frees its tensor memory and returns, so the
+ * context stays usable and dlrm_get_error reports DLRM_ERR_TIMEOUT. This call
+ * sets, for every later dlrm_forward on h, the limit of those waits in
+ * nanoseconds (0: the default, 2 s) and, with withhold_last != 0, makes each
+ * kernel skip the last copy or tensor-core commit of its stream (the fused
+ * kernels' last weight stage or tile, the layer-wise tensor-core GEMMs' last
+ * K block commit), so that the wait on it runs out after the limit. Results
+ * of such a forward are undefined. dlrm_test_stall(h, 0, 0) restores normal
+ * operation. INVALID_ARG for a null handle or a negative limit. */
+dlrm_status_t dlrm_test_stall(dlrm_handle_t h, int64_t wait_limit_ns, int32_t withhold_last);
+
 /* Bytes of device memory the handle owns (workspace + packed weights). */
 int64_t dlrm_workspace_bytes(dlrm_handle_t h);
 
