@@ -20,6 +20,7 @@
 #include "common.cuh"
 #include "fused.cuh"
 #include "fused_tc.cuh"
+#include "gemm_tma.cuh"
 
 namespace dlrm {
 
@@ -97,6 +98,10 @@ struct dlrm_handle_s {
   dlrm::FusedTcParams tcp{};
   unsigned long long* trace = nullptr;
   dlrm::WaitCfg wait{};          // dlrm_test_stall: wait limit, withheld last copy
+  // layer-wise TF32 / TF32X3: per layer (bottom, then top), the TMA plan of
+  // the warp-specialized tensor-core GEMM, or off (tma_on 0)
+  std::vector<dlrm::TmaLayer> tma;
+  std::vector<char> tma_on;
   // per-stage profiling (dlrm_set_profiling)
   std::vector<std::string> stage_names;
   std::vector<cudaEvent_t> events;      // stage boundaries, empty when off
@@ -168,18 +173,23 @@ dlrm_status_t run_forward(dlrm_handle_t h, const float* dense, const int64_t* in
     // [M1] bottom MLP, ReLU after every layer
     const float* in = dense;
     int ld_in = h->n_dense;
-    // GEMMs of the opt-in TF32/BF16 modes run on the tensor cores; the N = 1
-    // sigmoid layer (a dot product per row) stays on the fp32 GEMV.
-    auto linear = [&](const float* x, int ldx, const float* w, int ldw, const float* b, float* y,
-                      int ldy, int n, int k, int act) {
-      if (h->math != DLRM_MATH_FP32 && n >= 16)
+    // GEMMs of the opt-in modes run on the tensor cores: the warp-specialized
+    // TMA GEMM where the layer has a TMA plan (TF32 / TF32X3, input in a
+    // buffer of the handle), else the staged tcgen05 GEMM. The N = 1 sigmoid
+    // layer (a dot product per row) stays on the fp32 GEMV, and in TF32X3 so
+    // do layers of fewer than 64 inputs (fp32 is then both faster and exact).
+    auto linear = [&](int layer, const float* x, int ldx, const float* w, int ldw,
+                      const float* b, float* y, int ldy, int n, int k, int act) {
+      if (!h->tma_on.empty() && h->tma_on[layer])
+        return dlrm::launch_linear_tma(h->tma[layer], batch, b, y, ldy, act, h->err, s, h->wait);
+      if (h->math != DLRM_MATH_FP32 && n >= 16 && !(h->math == DLRM_MATH_TF32X3 && k < 64))
         return dlrm::launch_linear_tc(x, ldx, w, ldw, b, y, ldy, batch, n, k, act,
                                       static_cast<int>(h->math), h->err, s, h->wait);
       return dlrm::launch_linear_fp32(x, ldx, w, ldw, b, y, ldy, batch, n, k, act, s);
     };
     for (int l = 0; l < h->n_bot; ++l) {
       float* o = h->act[l & 1];
-      e = linear(in, ld_in, h->bot_w[l], h->bot_ldw[l], h->bot_b[l], o, h->ld_act,
+      e = linear(l, in, ld_in, h->bot_w[l], h->bot_ldw[l], h->bot_b[l], o, h->ld_act,
                  h->ln_bot[l + 1], h->ln_bot[l], DLRM_ACT_RELU);
       if (e != cudaSuccess || !mark()) return DLRM_ERR_CUDA;
       in = o;
@@ -195,8 +205,8 @@ dlrm_status_t run_forward(dlrm_handle_t h, const float* dense, const int64_t* in
       const bool last = (l == h->n_top - 1);
       float* o = last ? out : h->act[l & 1];
       const int ld_o = last ? 1 : h->ld_act;
-      e = linear(in, ld_in, h->top_w[l], h->top_ldw[l], h->top_b[l], o, ld_o, h->ln_top[l + 1],
-                 h->ln_top[l], last ? DLRM_ACT_SIGMOID : DLRM_ACT_RELU);
+      e = linear(h->n_bot + l, in, ld_in, h->top_w[l], h->top_ldw[l], h->top_b[l], o, ld_o,
+                 h->ln_top[l + 1], h->ln_top[l], last ? DLRM_ACT_SIGMOID : DLRM_ACT_RELU);
       if (e != cudaSuccess || !mark()) return DLRM_ERR_CUDA;
       in = o;
       ld_in = ld_o;
@@ -459,6 +469,35 @@ dlrm_status_t dlrm_create(const dlrm_config_t* cfg, const float* const* tables,
   const size_t off_idx = plan.take<int64_t>(mb * h->k * h->bag);
   const size_t off_off = plan.take<int64_t>(mb * h->k);
   const size_t off_out = plan.take<float>(mb);
+  // Layer-wise TF32 / TF32X3: the warp-specialized TMA GEMM for every
+  // tensor-core layer whose input is a buffer of the handle (all but the
+  // first bottom layer, which reads the caller's dense rows); in TF32X3 only
+  // for layers of 64 or more inputs, whose weights get two more copies: their
+  // tf32 head and the remainder.
+  const bool tma_math = h->path == DLRM_PATH_LAYERWISE &&
+                        (h->math == DLRM_MATH_TF32 || h->math == DLRM_MATH_TF32X3);
+  const int n_layers = h->n_bot + h->n_top;
+  std::vector<size_t> off_whi(n_layers, 0), off_wlo(n_layers, 0);
+  std::vector<char> want_tma(n_layers, 0);
+  auto layer_shape = [&](int g, int* n, int* k, int* ldw) {
+    const bool top = g >= h->n_bot;
+    const int l = top ? g - h->n_bot : g;
+    *n = top ? h->ln_top[l + 1] : h->ln_bot[l + 1];
+    *k = top ? h->ln_top[l] : h->ln_bot[l];
+    *ldw = top ? h->top_ldw[l] : h->bot_ldw[l];
+  };
+  if (tma_math) {
+    for (int g = 1; g < n_layers; ++g) {
+      int n, k, ldw;
+      layer_shape(g, &n, &k, &ldw);
+      if (n < 16 || (h->math == DLRM_MATH_TF32X3 && k < 64)) continue;
+      want_tma[g] = 1;
+      if (h->math == DLRM_MATH_TF32X3) {
+        off_whi[g] = plan.take<float>(static_cast<size_t>(n) * ldw);
+        off_wlo[g] = plan.take<float>(static_cast<size_t>(n) * ldw);
+      }
+    }
+  }
   // fused weight stream, its stage table, biases, last layer
   size_t off_fw = 0, off_ft = 0, off_fb = 0, off_fl = 0;
   if (h->path == DLRM_PATH_FUSED && h->fused_tc) {
@@ -550,6 +589,60 @@ dlrm_status_t dlrm_create(const dlrm_config_t* cfg, const float* const* tables,
   h->idx_stage = reinterpret_cast<int64_t*>(base + off_idx);
   h->off_stage = reinterpret_cast<int64_t*>(base + off_off);
   h->out_stage = at(off_out);
+  if (tma_math) {
+    // tensor maps of each TMA layer's input buffer (max_batch rows) and of
+    // its weights; a layer whose maps cannot be made keeps the staged GEMM
+    h->tma.resize(n_layers);
+    h->tma_on.assign(n_layers, 0);
+    for (int g = 1; g < n_layers && st == DLRM_OK; ++g) {
+      if (!want_tma[g]) continue;
+      int n, k, ldw;
+      layer_shape(g, &n, &k, &ldw);
+      const bool top = g >= h->n_bot;
+      const int l = top ? g - h->n_bot : g;
+      const float* in = (top && l == 0) ? h->r : h->act[(l - 1) & 1];
+      const int ld_in = (top && l == 0) ? h->ld_r : h->ld_act;
+      const float* w = top ? h->top_w[l] : h->bot_w[l];
+      dlrm::TmaLayer& T = h->tma[g];
+      T.n = n;
+      T.k = k;
+      T.split = h->math == DLRM_MATH_TF32X3 ? 1 : 0;
+      const float* w_head = w;
+      if (T.split) {
+        // w = head + rest: head keeps the top 10 mantissa bits (exact in
+        // tf32), rest = w - head is exact in fp32
+        const size_t count = static_cast<size_t>(n) * ldw;
+        std::vector<float> hw(count), hi(count), lo(count);
+        st = cuda_status(cudaMemcpy(hw.data(), w, count * sizeof(float), cudaMemcpyDeviceToHost));
+        if (st != DLRM_OK) break;
+        for (size_t i = 0; i < count; ++i) {
+          uint32_t bits;
+          std::memcpy(&bits, &hw[i], sizeof(bits));
+          bits &= 0xFFFFE000u;
+          std::memcpy(&hi[i], &bits, sizeof(bits));
+          lo[i] = hw[i] - hi[i];
+        }
+        st = cuda_status(cudaMemcpy(at(off_whi[g]), hi.data(), count * sizeof(float),
+                                    cudaMemcpyHostToDevice));
+        if (st == DLRM_OK)
+          st = cuda_status(cudaMemcpy(at(off_wlo[g]), lo.data(), count * sizeof(float),
+                                      cudaMemcpyHostToDevice));
+        if (st != DLRM_OK) break;
+        w_head = at(off_whi[g]);
+      }
+      const bool ok =
+          dlrm::encode_operand_map(T.map_x, in, k, h->max_batch, ld_in) &&
+          dlrm::encode_operand_map(T.map_w, w_head, k, n, ldw) &&
+          (!T.split || dlrm::encode_operand_map(T.map_wlo, at(off_wlo[g]), k, n, ldw));
+      h->tma_on[g] = ok ? 1 : 0;
+    }
+    if (st != DLRM_OK) {
+      cudaGetLastError();
+      cudaFree(h->arena);
+      delete h;
+      return st;
+    }
+  }
   // DLRM_PROFILE=1: per-stage timing from the first forward on, reported on
   // stderr by dlrm_destroy (the same counters dlrm_stage_times returns)
   const char* prof = std::getenv("DLRM_PROFILE");

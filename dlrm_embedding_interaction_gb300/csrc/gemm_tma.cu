@@ -1,0 +1,456 @@
+// Linear layers of many rows on the tensor cores, warp-specialized, with TMA
+// operand loads: the layer-wise plan's GEMM in the opt-in TF32 and TF32X3
+// (split-TF32, fp32-accurate) modes for batches of several 128-row tiles.
+//
+//   Y[m][n] = act(sum_k X[m][k] W[n][k] + b[n])   (Luminal compare
+//   modal_ci_ready...vanilla-pytorch, commit message: linear_bias_(relu|sigmoid))
+//
+// A persistent CTA (at most one per SM) walks output tiles of 128 rows x 128
+// columns, t = blockIdx.x, blockIdx.x + gridDim.x, ... with the column tile
+// fastest, so the CTAs running at one time share their rows of X through L2.
+// Per tile the K dimension flows in blocks of 32 values (128 bytes of fp32:
+// one 128-byte swizzle atom row) through a ring of shared-memory stages:
+//  * warp 0, one lane: loads each block's X tile (128 x 32) and weight tiles
+//    with cp.async.bulk.tensor (TMA, 128-byte swizzle: the canonical K-major
+//    layout the MMA descriptors read), completing on the stage's full
+//    mbarrier;
+//  * warps 2-3 (TF32X3): split the X tile in place into its tf32 head
+//    (hi = x with the low 13 mantissa bits cleared, exact in tf32) and write
+//    the remainder lo = x - hi (exact in fp32) beside it; the weights arrive
+//    already split (head and remainder streams made at create time);
+//  * warp 1, one lane: issues tcgen05.mma kind::tf32, M = 128, N = 128, four
+//    K steps of 8 per block (hi*hi + hi*lo + lo*hi in TF32X3), into one of
+//    two TMEM accumulators of 128 columns, and releases the stage with
+//    tcgen05.commit to its empty barrier;
+//  * warps 4-7: read the finished accumulator (tcgen05.ld 32x32b, warp w
+//    the TMEM lanes 32 (w % 4) ...), add the bias, apply the activation and
+//    store, then release the accumulator to the next tile but one.
+// Every wait is bounded (WaitCfg); on expiry the kernel sets
+// DLRM_ERRBIT_TIMEOUT, every role leaves its loop, the loads and MMAs in
+// flight are waited for (bounded) and the tensor memory is freed.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+
+#include "common.cuh"
+#include "gemm_tma.cuh"
+#include "tc.cuh"
+
+namespace dlrm {
+
+using namespace tc;
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kBM = 128;                 // rows of X per tile (the MMA M)
+constexpr int kBN = 128;                 // rows of W per tile (the MMA N)
+constexpr int kBK = 32;                  // k per block: 128 bytes of fp32
+constexpr int kTile = kBM * kBK * 4;     // 16 KB: one 128 x 32 fp32 tile
+constexpr int kAccCols = kBN;            // TMEM columns of one accumulator
+
+template <bool SPLIT>
+struct Layout {
+  // X, [X lo,] W (hi), [W lo]
+  static constexpr int kParts = SPLIT ? 4 : 2;
+  static constexpr int kStage = kParts * kTile;
+  static constexpr int kStages = SPLIT ? 3 : 6;
+  static constexpr int kBars = 3 * kStages + 5;      // full, split, empty; acc full/empty x2; drain
+  static constexpr int kSmem = 1024 + kStages * kStage + kBars * 8 + 16;
+};
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+// Bounded wait; false on timeout (which raises the abort flag and the error
+// bit) or when another thread has raised the abort flag.
+__device__ bool wait_for(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err,
+                         uint64_t limit) {
+  if (try_wait(bar, parity)) return true;
+  const uint64_t t0 = now_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (try_wait(bar, parity)) return true;
+    if ((i & 15) == 0) {
+      if (*abort_flag) return false;
+      if (now_ns() - t0 > limit) {
+        *abort_flag = 1;
+        if (err) atomicOr(reinterpret_cast<unsigned int*>(err), DLRM_ERRBIT_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// Bounded wait regardless of the abort flag (draining work in flight).
+__device__ void drain_wait(uint32_t bar, uint32_t parity, int32_t* err, uint64_t limit) {
+  const uint64_t t0 = now_ns();
+  while (!try_wait(bar, parity)) {
+    if (now_ns() - t0 > limit) {
+      if (err) atomicOr(reinterpret_cast<unsigned int*>(err), DLRM_ERRBIT_TIMEOUT);
+      return;
+    }
+  }
+}
+
+template <bool SPLIT>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_tma_kernel(const __grid_constant__ CUtensorMap tmap_x,
+                const __grid_constant__ CUtensorMap tmap_w,
+                const __grid_constant__ CUtensorMap tmap_wlo, const TmaGemmParams p) {
+  using Lay = Layout<SPLIT>;
+  constexpr int S = Lay::kStages;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* base = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + S * Lay::kStage);
+  uint64_t* full = bars;
+  uint64_t* split_done = bars + S;
+  uint64_t* empty = bars + 2 * S;
+  uint64_t* acc_full = bars + 3 * S;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // stage s: X at 0, [X lo at kTile,] W at (SPLIT ? 2 : 1) kTile, [W lo after it]
+  auto x_tile = [&](int s) { return base + s * Lay::kStage; };
+  auto xlo_tile = [&](int s) { return base + s * Lay::kStage + kTile; };
+  auto w_tile = [&](int s) { return base + s * Lay::kStage + (SPLIT ? 2 : 1) * kTile; };
+  auto wlo_tile = [&](int s) { return base + s * Lay::kStage + 3 * kTile; };
+
+  const int warp = threadIdx.x / kWarp;
+  const int lane = threadIdx.x % kWarp;
+  const uint64_t limit = wait_limit_ns(p.wait);
+  const int tiles = p.m_tiles * p.n_tiles;
+
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(tmem_slot)),
+                 "n"(2 * kAccCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (threadIdx.x == kWarp) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_addr(&full[s]), 1);
+      mbar_init(smem_addr(&split_done[s]), 2);          // the two split warps
+      mbar_init(smem_addr(&empty[s]), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(smem_addr(&acc_full[a]), 1);
+      mbar_init(smem_addr(&acc_empty[a]), 4);           // the four epilogue warps
+    }
+    mbar_init(smem_addr(drain), 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_x))
+                   : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_w))
+                   : "memory");
+      if (SPLIT)
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_wlo))
+                     : "memory");
+      constexpr uint32_t kBytes = (SPLIT ? 3 : 2) * kTile;
+      uint32_t stage = 0, phase = 0, it = 0;
+      bool ok = true;
+      const uint32_t total = static_cast<uint32_t>(
+          ((tiles - static_cast<int>(blockIdx.x) + gridDim.x - 1) / gridDim.x) * p.kb_count);
+      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        const int mt = t / p.n_tiles, nt = t % p.n_tiles;
+        for (int kb = 0; kb < p.kb_count; ++kb) {
+          if (it >= static_cast<uint32_t>(S) &&
+              !wait_for(smem_addr(&empty[stage]), phase ^ 1, abort_flag, p.err, limit)) {
+            ok = false;
+            break;
+          }
+          // failure-detection tests: the last block is never loaded, so the
+          // wait on it runs out (not issued: not drained below)
+          if (p.wait.withhold_last && it + 1 == total) {
+            ok = false;
+            break;
+          }
+          const uint32_t bar = smem_addr(&full[stage]);
+          mbar_expect_tx(bar, kBytes);
+          tma_load_2d(smem_addr(x_tile(stage)), &tmap_x, kb * kBK, mt * kBM, bar);
+          tma_load_2d(smem_addr(w_tile(stage)), &tmap_w, kb * kBK, nt * kBN, bar);
+          if (SPLIT) tma_load_2d(smem_addr(wlo_tile(stage)), &tmap_wlo, kb * kBK, nt * kBN, bar);
+          ++it;
+          if (++stage == static_cast<uint32_t>(S)) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // loads in flight must land before the shared memory is released
+      const uint32_t first = it > static_cast<uint32_t>(S) ? it - S : 0;
+      for (uint32_t q = first; q < it; ++q) drain_wait(smem_addr(&full[q % S]), (q / S) & 1, p.err, limit);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issue
+    if (lane == 0) {
+      constexpr uint32_t kIdesc = instr_desc(2u, kBN);   // tf32 x tf32 -> fp32, N = 128
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      int i = 0;
+      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++i) {
+        const int abuf = i & 1;
+        const uint32_t aphase = (i >> 1) & 1;
+        if (i >= 2 && !wait_for(smem_addr(&acc_empty[abuf]), aphase ^ 1, abort_flag, p.err, limit))
+          break;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t acc = tmem + static_cast<uint32_t>(abuf * kAccCols);
+        for (int kb = 0; kb < p.kb_count; ++kb) {
+          const uint32_t ready = smem_addr(SPLIT ? &split_done[stage] : &full[stage]);
+          if (!wait_for(ready, phase, abort_flag, p.err, limit)) {
+            ok = false;
+            break;
+          }
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          const uint64_t dx = smem_desc(smem_addr(x_tile(stage)));
+          const uint64_t dw = smem_desc(smem_addr(w_tile(stage)));
+          const uint64_t dxl = smem_desc(smem_addr(xlo_tile(stage)));
+          const uint64_t dwl = smem_desc(smem_addr(wlo_tile(stage)));
+#pragma unroll
+          for (int j = 0; j < kBK / 8; ++j) {
+            const uint64_t off = static_cast<uint64_t>((j * 32) >> 4);   // 32 bytes per K step
+            mma<false>(acc, dx + off, dw + off, kIdesc, (kb > 0 || j > 0) ? 1u : 0u);
+            if (SPLIT) {
+              mma<false>(acc, dx + off, dwl + off, kIdesc, 1u);   // hi * lo
+              mma<false>(acc, dxl + off, dw + off, kIdesc, 1u);   // lo * hi
+            }
+          }
+          mma_commit(smem_addr(&empty[stage]));     // the stage is free once these ran
+          if (++stage == static_cast<uint32_t>(S)) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        mma_commit(smem_addr(&acc_full[abuf]));     // the tile's accumulator is final
+      }
+      // every MMA must have run before the tensor memory is freed: one more
+      // commit on a barrier of its own (one phase) tracks them all
+      mma_commit(smem_addr(drain));
+      drain_wait(smem_addr(drain), 0, p.err, limit);
+    }
+  } else if (warp < 4) {
+    // ---------------------------------------------------------------- X split (TF32X3)
+    if (SPLIT) {
+      const int st = threadIdx.x - 2 * kWarp;            // 0 .. 63
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        for (int kb = 0; kb < p.kb_count; ++kb) {
+          if (!wait_for(smem_addr(&full[stage]), phase, abort_flag, p.err, limit)) {
+            ok = false;
+            break;
+          }
+          unsigned char* xs = x_tile(stage);
+          unsigned char* xl = xlo_tile(stage);
+#pragma unroll 4
+          for (int off = st * 16; off < kTile; off += 64 * 16) {
+            const uint4 v = *reinterpret_cast<const uint4*>(xs + off);
+            uint4 hi, lo;
+            hi.x = v.x & 0xFFFFE000u;
+            hi.y = v.y & 0xFFFFE000u;
+            hi.z = v.z & 0xFFFFE000u;
+            hi.w = v.w & 0xFFFFE000u;
+            lo.x = __float_as_uint(__uint_as_float(v.x) - __uint_as_float(hi.x));
+            lo.y = __float_as_uint(__uint_as_float(v.y) - __uint_as_float(hi.y));
+            lo.z = __float_as_uint(__uint_as_float(v.z) - __uint_as_float(hi.z));
+            lo.w = __float_as_uint(__uint_as_float(v.w) - __uint_as_float(hi.w));
+            *reinterpret_cast<uint4*>(xs + off) = hi;
+            *reinterpret_cast<uint4*>(xl + off) = lo;
+          }
+          // generic-proxy writes -> visible to the tensor core's async proxy
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_addr(&split_done[stage]));
+          if (++stage == static_cast<uint32_t>(S)) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    const int q = warp & 3;                              // TMEM lane quarter
+    int i = 0;
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
+      const int abuf = i & 1;
+      const uint32_t aphase = (i >> 1) & 1;
+      if (!wait_for(smem_addr(&acc_full[abuf]), aphase, abort_flag, p.err, limit)) break;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const int mt = t / p.n_tiles, nt = t % p.n_tiles;
+      const int row = mt * kBM + q * 32 + lane;
+      float* yrow = p.y + static_cast<int64_t>(row) * p.ldy;
+      for (int c0 = 0; c0 < kBN; c0 += 16) {
+        uint32_t r[16];
+        const uint32_t taddr =
+            tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(abuf * kAccCols + c0);
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+            "%11, %12, %13, %14, %15}, [%16];"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+              "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+              "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+            : "r"(taddr));
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        const int col0 = nt * kBN + c0;
+        if (row < p.m) {
+          if (p.vec_y && col0 + 16 <= p.n) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const float4 b = p.bias ? __ldg(reinterpret_cast<const float4*>(p.bias + col0) + v)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+              float4 o;
+              o.x = apply_act(__uint_as_float(r[4 * v + 0]) + b.x, p.act);
+              o.y = apply_act(__uint_as_float(r[4 * v + 1]) + b.y, p.act);
+              o.z = apply_act(__uint_as_float(r[4 * v + 2]) + b.z, p.act);
+              o.w = apply_act(__uint_as_float(r[4 * v + 3]) + b.w, p.act);
+              *reinterpret_cast<float4*>(yrow + col0 + 4 * v) = o;
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const int col = col0 + c;
+              if (col < p.n)
+                yrow[col] =
+                    apply_act(__uint_as_float(r[c]) + (p.bias ? __ldg(p.bias + col) : 0.f), p.act);
+            }
+          }
+        }
+      }
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&acc_empty[abuf]));
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 0) {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "n"(2 * kAccCols)
+                 : "memory");
+  }
+}
+
+template <bool SPLIT>
+cudaError_t prepare() {
+  static std::atomic<uint64_t> done{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(gemm_tma_kernel<SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Layout<SPLIT>::kSmem);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::atomic<void*> fn{nullptr};
+  void* f = fn.load(std::memory_order_acquire);
+  if (!f) {
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn.store(f, std::memory_order_release);
+  }
+  return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+}
+
+}  // namespace
+
+bool tma_operand_ok(const void* base, int ld) {
+  return base && reinterpret_cast<uintptr_t>(base) % 16 == 0 && ld > 0 && ld % 4 == 0;
+}
+
+bool encode_operand_map(void* map, const float* base, int inner, int rows, int ld) {
+  static_assert(sizeof(CUtensorMap) == kTensorMapBytes, "tensor map size");
+  if (!tma_operand_ok(base, ld) || inner < 1 || rows < 1 || inner > ld) return false;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * sizeof(float)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(kBM)};
+  const cuuint32_t estrides[2] = {1, 1};
+  const CUresult r = enc(reinterpret_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                         const_cast<float*>(base), dims, strides, box, estrides,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+cudaError_t launch_linear_tma(const TmaLayer& L, int m, const float* bias, float* y, int ldy,
+                              int act, int32_t* err, cudaStream_t stream, WaitCfg wait) {
+  if (m == 0) return cudaSuccess;
+  TmaGemmParams p{};
+  p.m = m;
+  p.n = L.n;
+  p.ldy = ldy;
+  p.y = y;
+  p.bias = bias;
+  p.act = act;
+  p.err = err;
+  p.wait = wait;
+  p.m_tiles = (m + kBM - 1) / kBM;
+  p.n_tiles = (L.n + kBN - 1) / kBN;
+  p.kb_count = (L.k + kBK - 1) / kBK;
+  p.vec_y = (ldy % 4 == 0 && reinterpret_cast<uintptr_t>(y) % 16 == 0 &&
+             (bias == nullptr || reinterpret_cast<uintptr_t>(bias) % 16 == 0))
+                ? 1
+                : 0;
+  const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(tiles, device_sm_count()));
+  const CUtensorMap* mx = reinterpret_cast<const CUtensorMap*>(L.map_x);
+  const CUtensorMap* mw = reinterpret_cast<const CUtensorMap*>(L.map_w);
+  const CUtensorMap* mwl = reinterpret_cast<const CUtensorMap*>(L.split ? L.map_wlo : L.map_w);
+  cudaError_t e;
+  if (L.split) {
+    e = prepare<true>();
+    if (e != cudaSuccess) return e;
+    gemm_tma_kernel<true><<<grid, kThreads, Layout<true>::kSmem, stream>>>(*mx, *mw, *mwl, p);
+  } else {
+    e = prepare<false>();
+    if (e != cudaSuccess) return e;
+    gemm_tma_kernel<false><<<grid, kThreads, Layout<false>::kSmem, stream>>>(*mx, *mw, *mwl, p);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace dlrm
