@@ -700,15 +700,17 @@ def run_ours(args, rank, world, local_rank):
                                               else "rel 2e-2 vs the fp64 oracle"))
         m2.close()
 
-    def forward_point(c, tabs, steps, warmup):
+    def forward_point(c, tabs, steps, warmup, math_name=None):
         """One workload's forward through the library, same timing rules as the
         headline: mean and median us per batch, samples/s, the plan taken and the
-        whole-forward roofline fraction."""
+        whole-forward roofline fraction (against the FP32 FFMA peak; in TF32X3
+        also against the tensor pipe doing the three products)."""
+        math_name = math_name or args.config_math
         ci = synth.make_inputs(c, seed=args.seed, with_tables=False)
         m = dl.DlrmModel(c.ln_bot, c.ln_top, tabs,
                          [cu(w) for w in ci["bot_w"]], [cu(b) for b in ci["bot_b"]],
                          [cu(w) for w in ci["top_w"]], [cu(b) for b in ci["top_b"]],
-                         c.bag_size, c.batch, config_math)
+                         c.bag_size, c.batch, maths[math_name])
         d_, i_, o_ = cu(ci["dense"]), cu(ci["indices"]), cu(ci["offsets"])
         y_ = torch.empty(c.batch, device=dev)
         ms_c, _ = timed(lambda: m.forward(d_, i_, o_, y_, stream=stream), steps, warmup)
@@ -720,11 +722,19 @@ def run_ours(args, rank, world, local_rank):
         t = sum(ms_c) / len(ms_c) * 1e-3
         fl, by = forward_work(c, c.batch)
         t_alu, t_hbm = fl / (fp32_peak * 1e12), by / (pk["hbm_gbs"] * 1e9)
-        return dict(us_per_batch=t * 1e6, us_median=statistics.median(ms_c) * 1e3,
-                    samples_per_s=c.batch / t, steps=len(ms_c), plan=plan,
-                    math=args.config_math,
-                    roofline_frac=max(t_alu, t_hbm) / t,
-                    bound="alu (FP32 FFMA)" if t_alu >= t_hbm else "hbm")
+        r = dict(us_per_batch=t * 1e6, us_median=statistics.median(ms_c) * 1e3,
+                 samples_per_s=c.batch / t, steps=len(ms_c), plan=plan,
+                 math=math_name,
+                 roofline_frac=max(t_alu, t_hbm) / t,
+                 bound="alu (FP32 FFMA)" if t_alu >= t_hbm else "hbm")
+        if math_name == "tf32x3":
+            # the MLPs on the tensor pipe: three tf32 products per fp32 one, at the
+            # TF32 rate taken as half the measured bf16 peak (the nominal ratio)
+            t_tc = 3 * fl / (pk["bf16_tflops"] * 0.5 * 1e12)
+            r["roofline_frac_tensor_or_hbm"] = max(t_tc, t_hbm) / t
+            r["bound_tensor_or_hbm"] = ("hbm" if t_hbm >= t_tc
+                                        else "tensor (3 tf32 products per fp32 product)")
+        return r
 
     configs = None
     gather = None
@@ -757,6 +767,9 @@ def run_ours(args, rank, world, local_rank):
             gather["general_bags"] = bag_modes_measure(torch, dl, synth, pk, tabs)
             if configs is not None:
                 configs[c4.name] = forward_point(c4, tabs, 5, 3)
+                # the same model with the MLPs as split-TF32 tensor-core GEMMs
+                # (opt-in, within the fp32 tolerance)
+                configs[c4.name + "_tf32x3"] = forward_point(c4, tabs, 5, 3, "tf32x3")
             del tabs
             torch.cuda.empty_cache()
         if not args.no_cpu_baseline:

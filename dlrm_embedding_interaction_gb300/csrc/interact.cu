@@ -13,7 +13,10 @@
 // padded to D + 4 floats so the 16-byte reads of different rows fall in
 // different banks), then thread w computes tasks w, w + T, ...: with D a
 // multiple of 4 a task is a 4 x 4 block of pairs held in registers
-// (gram_block), a quarter of the shared-memory reads of one pair per thread.
+// (gram_block), a quarter of the shared-memory reads of one pair per thread;
+// when the block's samples have too few such blocks for its threads, each
+// block is split over two adjacent lanes (alternate 16-byte chunks of D, one
+// shuffle to add).
 #include <atomic>
 
 #include "common.cuh"
@@ -91,7 +94,74 @@ interaction_kernel(const float* __restrict__ dense, int ld_dense, const float* _
     col0 = d;
   }
   const int nblk = gram_blocks(f);
-  if (VEC && use_blocks) {
+  if (VEC && use_blocks == 2) {
+    // 4 x 4 register blocks of pairs, each over half of D (alternate 16-byte
+    // chunks) on two adjacent lanes (w = 2 task + half), added with one
+    // shuffle per dot: twice the tasks when a block's samples have too few
+    // blocks for its threads
+    const int d4 = d / 4;
+    const int total = ns * nblk * 2;
+    for (int base = 0; base < total; base += blockDim.x) {   // uniform per warp
+      const int w = base + tid;
+      const bool active = w < total;
+      const int task = active ? (w >> 1) : 0;
+      const int half = w & 1;
+      const int s = task / nblk;
+      const int q = task - s * nblk;
+      const float* zsam = zs + s * f * ldz;
+      int ii, jj;
+      pair_from_index(q, ii, jj);
+      const int bi = ii - 1, bj = jj;
+      const float* ri[4];
+      const float* rj[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        ri[a] = zsam + min(4 * bi + a, f - 1) * ldz;
+        rj[a] = zsam + min(4 * bj + a, f - 1) * ldz;
+      }
+      float acc[4][4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[a][c] = 0.f;
+      // the two halves take alternate 16-byte chunks of the rows: the pair's
+      // loads fall in adjacent bank groups instead of colliding
+      const int c_end = active ? d4 : 0;
+      for (int c4 = half; c4 < c_end; c4 += 2) {
+        float4 u[4], v[4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          u[a] = *reinterpret_cast<const float4*>(ri[a] + 4 * c4);
+          v[a] = *reinterpret_cast<const float4*>(rj[a] + 4 * c4);
+        }
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            acc[a][c] = fmaf(u[a].x, v[c].x, acc[a][c]);
+            acc[a][c] = fmaf(u[a].y, v[c].y, acc[a][c]);
+            acc[a][c] = fmaf(u[a].z, v[c].z, acc[a][c]);
+            acc[a][c] = fmaf(u[a].w, v[c].w, acc[a][c]);
+          }
+      }
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[a][c] += __shfl_xor_sync(0xffffffffu, acc[a][c], 1);
+      if (active && half == 0) {
+        float* o = out + static_cast<int64_t>(b0 + s) * ld_out + col0;
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          const int i = 4 * bi + a;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int j = 4 * bj + c;
+            if (i < f && j < i) o[i * (i - 1) / 2 + j] = acc[a][c];
+          }
+        }
+      }
+    }
+  } else if (VEC && use_blocks) {
     // 4 x 4 register blocks of pairs (gram_block)
     const int d4 = d / 4;
     for (int w = tid; w < ns * nblk; w += blockDim.x) {
@@ -202,6 +272,10 @@ cudaError_t launch_interaction(const float* dense, int ld_dense, const float* em
   const int sms = device_sm_count();
   const int cap = std::max(1, (b + 2 * sms - 1) / (2 * sms));
   s = std::max(1, std::min(s, cap));
+  // half-D tasks on lane pairs when the block's pair blocks would leave more
+  // than a third of its threads idle (wide D only: each half keeps >= 8 steps)
+  int mode = use_blocks;
+  if (use_blocks && s * blocks4 * 3 < 2 * kInteractThreads && d >= 64) mode = 2;
   const size_t smem = per * s;
   const unsigned grid = static_cast<unsigned>((b + s - 1) / s);
   if (smem > 48 * 1024) {
@@ -211,7 +285,7 @@ cudaError_t launch_interaction(const float* dense, int ld_dense, const float* em
   }
   if (vec) {
     interaction_kernel<true><<<grid, kInteractThreads, smem, stream>>>(
-        dense, ld_dense, emb, b, k, d, out, ld_out, copy_dense, s, use_blocks);
+        dense, ld_dense, emb, b, k, d, out, ld_out, copy_dense, s, mode);
   } else {
     interaction_kernel<false><<<grid, kInteractThreads, smem, stream>>>(
         dense, ld_dense, emb, b, k, d, out, ld_out, copy_dense, s, 0);

@@ -121,6 +121,8 @@ def test_gather_non_uniform_offsets_flagged_and_zeroed():
 INTERACT_CASES = [
     (64, 3, 16), (2048, 3, 64), (2048, 32, 64), (300, 26, 128), (5, 0, 8),
     (17, 7, 13), (3, 127, 4), (1, 1, 1), (33, 5, 6), (1000, 1, 64), (9, 128, 8),
+    # pair blocks split over lane pairs (half of D each), several samples a block
+    (1200, 26, 128), (517, 12, 64),
 ]
 
 
