@@ -58,6 +58,9 @@ __device__ __forceinline__ void max4(float4& a, const float4& v) {
 // The weighted sum (per_sample_weights) is a fourth, internal reduction.
 constexpr int kBagWeightedSum = 3;
 
+// A row left out of its bag, in the vector kernel's 32-bit row numbers.
+constexpr uint32_t kSkip = 0xFFFFFFFFu;
+
 // Bag bounds: the uniform stride (GENERAL false: start must equal b * bag)
 // or consecutive offsets with the last bag running to N.
 template <bool GENERAL, typename IDX>
@@ -80,8 +83,10 @@ __device__ __forceinline__ bool bag_bounds(const IDX* offs, int b, int batch, in
 // sum; IDX: the index and offset type. An index equal to `padding`, when that
 // is >= 0, is left out of its bag without a flag (a negative `padding` is none).
 // Six CTAs of 256 threads per SM (at most 40 registers a thread) keep the
-// most rows in flight; ptxas spills a few bytes outside the row loop rather
-// than fall to five.
+// most rows in flight. Each index is checked once, by the lane that loads
+// it, and passed on as a 32-bit row number (tables of fewer than 2^32 - 1
+// rows; the scalar kernel takes larger ones), which keeps the row loop's
+// state within those registers.
 template <int TPB, int CHUNKS, int MODE, bool GENERAL, typename IDX>
 __global__ void __launch_bounds__(kGatherThreads, CHUNKS == 1 ? 6 : 1)
 gather_vec_kernel(const __grid_constant__ GatherTables tabs, int k_tables, int d4,
@@ -115,30 +120,44 @@ gather_vec_kernel(const __grid_constant__ GatherTables tabs, int k_tables, int d
     const int64_t base = static_cast<int64_t>(t) * n_idx + start;
     const IDX* idx = indices + base;
     const float4* table = reinterpret_cast<const float4*>(tabs.ptr[t]);
-    const int64_t rows = tabs.rows[t];
+    const uint64_t rows = static_cast<uint64_t>(tabs.rows[t]);   // < 2^32 - 1 (host check)
     bool oob = false;
     for (int l0 = 0; l0 < len; l0 += TPB) {
       const int cnt = min(TPB, len - l0);
-      const int64_t mine = (lane < cnt) ? static_cast<int64_t>(__ldg(idx + l0 + lane)) : 0;
-      const float mine_w = (kWeighted && lane < cnt) ? __ldg(psw + base + l0 + lane) : 1.f;
+      // The lane that owns an index checks it once: its row as a 32-bit
+      // number, or kSkip when the row is left out (past the bag, the padding
+      // row, out of range), so the unrolled loop below only shuffles,
+      // compares, loads and adds.
+      uint32_t mine = kSkip;
+      float mine_w = 1.f;
+      if (lane < cnt) {
+        const int64_t r = static_cast<int64_t>(__ldg(idx + l0 + lane));
+        const bool pad = GENERAL && padding >= 0 && r == padding;
+        const bool in = static_cast<uint64_t>(r) < rows;
+        oob |= !pad && !in;
+        if (in && !pad) mine = static_cast<uint32_t>(r);
+        if (kWeighted) mine_w = __ldg(psw + base + l0 + lane);
+      }
+      if (MODE == DLRM_BAG_MEAN || MODE == DLRM_BAG_MAX)
+        kept += __popc(__ballot_sync(gmask, mine != kSkip) & gmask);
       for (int u0 = 0; u0 < cnt; u0 += kUnroll) {
-        // a row left out (past the bag, padding or out of range) loads the
-        // identity of the reduction: 0 for sums, -inf for max
+        // a row left out loads the identity of the reduction: 0 for sums,
+        // -inf for max
         float4 v[kUnroll][CHUNKS];
         float wq[kUnroll];
 #pragma unroll
         for (int q = 0; q < kUnroll; ++q) {
-          const int64_t r = __shfl_sync(gmask, mine, (u0 + q) & (TPB - 1), TPB);
+          const uint32_t r = __shfl_sync(gmask, mine, (u0 + q) & (TPB - 1), TPB);
           if (kWeighted) wq[q] = __shfl_sync(gmask, mine_w, (u0 + q) & (TPB - 1), TPB);
-          const bool live = (u0 + q) < cnt && !(GENERAL && padding >= 0 && r == padding);
-          const bool ok = live && r >= 0 && r < rows;
-          oob |= live && !ok;
-          if (MODE == DLRM_BAG_MEAN || MODE == DLRM_BAG_MAX) kept += ok ? 1 : 0;
+          // (u0 + q) < cnt: for groups narrower than the unroll the source
+          // lane wraps around to a row already taken
+          const bool ok = r != kSkip && (u0 + q) < cnt;
 #pragma unroll
           for (int c = 0; c < CHUNKS; ++c) {
             const int col4 = lane + c * TPB;
-            v[q][c] = (ok && col4 < d4) ? __ldg(table + r * d4 + col4)
-                                        : make_float4(init, init, init, init);
+            v[q][c] = (ok && col4 < d4)
+                          ? __ldg(table + static_cast<uint64_t>(r) * static_cast<uint32_t>(d4) + col4)
+                          : make_float4(init, init, init, init);
           }
         }
 #pragma unroll
@@ -151,7 +170,7 @@ gather_vec_kernel(const __grid_constant__ GatherTables tabs, int k_tables, int d
           }
       }
     }
-    if (oob && lane == 0) flag_error(err, DLRM_ERRBIT_INDEX_OOB);
+    if (__any_sync(gmask, oob) && lane == 0) flag_error(err, DLRM_ERRBIT_INDEX_OOB);
   }
   // no rows kept: zeros in every mode (a sum of none is already zero); mean
   // divides by the rows kept
@@ -242,7 +261,9 @@ cudaError_t launch_any(const GatherTables& tabs, int k, int d, const IDX* indice
                        const IDX* offsets, const float* psw, int64_t padding, int b, int l,
                        int64_t n_idx, float* out, int32_t* err, cudaStream_t stream) {
   bool vec = (d % 4 == 0) && (reinterpret_cast<uintptr_t>(out) % 16 == 0);
-  for (int t = 0; t < k && vec; ++t) vec = reinterpret_cast<uintptr_t>(tabs.ptr[t]) % 16 == 0;
+  for (int t = 0; t < k && vec; ++t)
+    vec = reinterpret_cast<uintptr_t>(tabs.ptr[t]) % 16 == 0 &&
+          static_cast<uint64_t>(tabs.rows[t]) < static_cast<uint64_t>(kSkip);
   const int d4 = d / 4;
 #define DLRM_VEC(TPB_, CH_)                                                                     \
   launch_vec<TPB_, CH_, MODE, GENERAL, IDX>(tabs, k, d, indices, offsets, psw, padding, b, l, \
