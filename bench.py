@@ -86,6 +86,11 @@ def parse_args():
                          "smaller tables keep an ncu capture to a few GB)")
     ap.add_argument("--only-forward", action="store_true",
                     help="time the device forward only (for ncu launch lists)")
+    ap.add_argument("--rows", type=int, default=0,
+                    help="rows per table of the timed model (default: the workload's; "
+                         "smaller tables keep an ncu capture to a few GB)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="batch of the timed model (default: the workload's)")
     return ap.parse_args()
 
 
@@ -241,6 +246,12 @@ def run_reference(args, rank, world):
     import dlrm_synth as synth
     import oracle
     cfg = synth.get_config(args.config)
+    if args.batch > 0:
+        cfg = cfg.with_batch(args.batch)
+    if args.rows > 0:
+        cfg = synth.DlrmConfig(cfg.name, cfg.batch, cfg.ln_bot, (args.rows,) * cfg.n_tables,
+                               cfg.emb_dim, cfg.bag_size, cfg.ln_top, cfg.table_range,
+                               cfg.index_dist, cfg.zipf_s)
     inp = synth.make_inputs(cfg, seed=args.seed)
     lib = oracle.load()
     threads = os.cpu_count() or 1
@@ -447,6 +458,12 @@ def run_ours(args, rank, world, local_rank):
             dist.destroy_process_group()
         return 0
     cfg = synth.get_config(args.config)
+    if args.batch > 0:
+        cfg = cfg.with_batch(args.batch)
+    if args.rows > 0:
+        cfg = synth.DlrmConfig(cfg.name, cfg.batch, cfg.ln_bot, (args.rows,) * cfg.n_tables,
+                               cfg.emb_dim, cfg.bag_size, cfg.ln_top, cfg.table_range,
+                               cfg.index_dist, cfg.zipf_s)
     inp = synth.make_inputs(cfg, seed=args.seed)
     cu = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
     maths = {"fp32": dl.MATH_FP32, "tf32": dl.MATH_TF32, "bf16": dl.MATH_BF16,
