@@ -1066,7 +1066,9 @@ bool fused_plan(int n_dense, int k_tables, int d, int bag, const std::vector<int
     if (bm > first_bm) continue;
     for (int mode = 0; mode < 3 && !placed; ++mode) {
       if (bag != 1 && mode < 2) continue;
-      for (int stages : {4, 3}) {
+      // the deepest ring that fits: a CTA's weight feed is bounded by the
+      // bytes it keeps in flight (~80 GB/s per SM at four 32 KB stages)
+      for (int stages : {6, 5, 4, 3}) {
         const size_t off = static_cast<size_t>(stages) * kFusedStageFloats * sizeof(float);
         const size_t act = align128(static_cast<size_t>(bm) * p.lda * sizeof(float));
         const size_t rowidx = align128(static_cast<size_t>(bm) * k_tables * sizeof(int));
