@@ -63,11 +63,13 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="b2048_k3")
-    ap.add_argument("--math", choices=["fp32", "tf32", "bf16", "tf32x3"], default="fp32",
+    ap.add_argument("--math", choices=["fp32", "fp32_ffma", "tf32", "bf16", "tf32x3"],
+                    default="fp32",
                     help="arithmetic of the timed model's MLPs (fp32 is the parity mode)")
-    ap.add_argument("--config-math", choices=["fp32", "tf32", "bf16", "tf32x3"], default="fp32",
+    ap.add_argument("--config-math", choices=["fp32", "fp32_ffma", "tf32", "bf16", "tf32x3"],
+                    default="fp32",
                     help="arithmetic of the other workloads' forwards under `configs` (their "
-                         "roofline fraction stays against the FP32 FFMA peak)")
+                         "roofline fraction is against the pipes their plan uses)")
     ap.add_argument("--seed", type=int, default=1234)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -323,6 +325,36 @@ def forward_work(cfg, batch):
     return flops, byts
 
 
+def forward_roofline_parts(cfg, plan, math, fp32_peak_tflops, pk):
+    """Roofline time of one forward on the pipes its plan uses: the GEMM layers
+    the layer-wise plan runs on the tensor cores (plan["tensor_core_layers"])
+    at the tensor rate of their arithmetic (split-TF32: three tf32 products per
+    fp32 product; TF32 taken as half the measured bf16 peak, the nominal
+    ratio), every other flop at the FP32 FFMA peak, against the algorithmic
+    HBM bytes: max(tensor + FFMA time, HBM time)."""
+    import dlrm_embedding_interaction_gb300 as dl
+    flops, byts = forward_work(cfg, cfg.batch)
+    layers = list(zip(cfg.ln_bot[:-1], cfg.ln_bot[1:])) + list(zip(cfg.ln_top[:-1], cfg.ln_top[1:]))
+    mask = plan["tensor_core_layers"]
+    tc_flops = sum(2 * cfg.batch * k * n for g, (k, n) in enumerate(layers) if (mask >> g) & 1)
+    if plan["split_tf32"]:
+        tc_time, what = 3 * tc_flops / (pk["bf16_tflops"] * 0.5 * 1e12), "split-TF32"
+    elif math == dl.MATH_BF16:
+        tc_time, what = tc_flops / (pk["bf16_tflops"] * 1e12), "bf16"
+    else:
+        tc_time, what = tc_flops / (pk["bf16_tflops"] * 0.5 * 1e12), "tf32"
+    alu_time = (flops - tc_flops) / (fp32_peak_tflops * 1e12)
+    hbm_time = byts / (pk["hbm_gbs"] * 1e9)
+    if hbm_time >= tc_time + alu_time:
+        bound = "hbm"
+    elif tc_flops:
+        bound = f"tensor ({what} GEMM layers) + FP32 FFMA (the rest)"
+    else:
+        bound = "alu (FP32 FFMA)"
+    return dict(roofline_us=max(tc_time + alu_time, hbm_time) * 1e6, bound=bound,
+                tensor_core_layers=[g for g in range(len(layers)) if (mask >> g) & 1])
+
+
 def device_tables(torch, synth, cfg, seed, n=None):
     """The workload's first n tables from the seeded generator, filled on the host
     one at a time into a reused pinned buffer and copied to the current device."""
@@ -466,7 +498,8 @@ def run_ours(args, rank, world, local_rank):
                                cfg.index_dist, cfg.zipf_s)
     inp = synth.make_inputs(cfg, seed=args.seed)
     cu = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
-    maths = {"fp32": dl.MATH_FP32, "tf32": dl.MATH_TF32, "bf16": dl.MATH_BF16,
+    maths = {"fp32": dl.MATH_FP32, "fp32_ffma": dl.MATH_FP32_FFMA, "tf32": dl.MATH_TF32,
+             "bf16": dl.MATH_BF16,
              "tf32x3": dl.MATH_TF32X3}
     math = maths[args.math]
     config_math = maths[args.config_math]
@@ -655,7 +688,9 @@ def run_ours(args, rank, world, local_rank):
                 n: float(kacc[g, 2] / reps) for g, n in enumerate(names_g)}
     dom = max(stage_us, key=stage_us.get)
     flops, byts = stage_work(cfg, dom, cfg.batch)
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    props = torch.cuda.get_device_properties(dev)
+    sms = props.multi_processor_count
+    smem_optin = getattr(props, "shared_memory_per_block_optin", dl.GB300_SMEM_PER_BLOCK)
     fp32_peak = sms * FP32_LANES_PER_SM * 2 * pk["sm_max_mhz"] * 1e6 / 1e12
     # one launch per step (fused plan): the timed region's own CUDA-event time
     # is that launch's duration; else the library's per-stage event profile
@@ -720,8 +755,8 @@ def run_ours(args, rank, world, local_rank):
     def forward_point(c, tabs, steps, warmup, math_name=None):
         """One workload's forward through the library, same timing rules as the
         headline: mean and median us per batch, samples/s, the plan taken and the
-        whole-forward roofline fraction (against the FP32 FFMA peak; in TF32X3
-        also against the tensor pipe doing the three products)."""
+        whole-forward roofline fraction (forward_roofline_parts: the tensor pipe
+        for the GEMMs the plan runs there, the FP32 FFMA peak for the rest, HBM)."""
         math_name = math_name or args.config_math
         ci = synth.make_inputs(c, seed=args.seed, with_tables=False)
         m = dl.DlrmModel(c.ln_bot, c.ln_top, tabs,
@@ -737,20 +772,16 @@ def run_ours(args, rank, world, local_rank):
         if not ok:
             raise RuntimeError(f"device error in the {c.name} forward")
         t = sum(ms_c) / len(ms_c) * 1e-3
-        fl, by = forward_work(c, c.batch)
-        t_alu, t_hbm = fl / (fp32_peak * 1e12), by / (pk["hbm_gbs"] * 1e9)
+        plan_info = dl.dlrm_plan_query(c.ln_bot, c.ln_top, c.rows, c.emb_dim, c.bag_size,
+                                       c.batch, maths[math_name], dl.PATH_AUTO,
+                                       sms, smem_optin)
+        rf = forward_roofline_parts(c, plan_info, maths[math_name], fp32_peak, pk)
         r = dict(us_per_batch=t * 1e6, us_median=statistics.median(ms_c) * 1e3,
                  samples_per_s=c.batch / t, steps=len(ms_c), plan=plan,
-                 math=math_name,
-                 roofline_frac=max(t_alu, t_hbm) / t,
-                 bound="alu (FP32 FFMA)" if t_alu >= t_hbm else "hbm")
-        if math_name == "tf32x3":
-            # the MLPs on the tensor pipe: three tf32 products per fp32 one, at the
-            # TF32 rate taken as half the measured bf16 peak (the nominal ratio)
-            t_tc = 3 * fl / (pk["bf16_tflops"] * 0.5 * 1e12)
-            r["roofline_frac_tensor_or_hbm"] = max(t_tc, t_hbm) / t
-            r["bound_tensor_or_hbm"] = ("hbm" if t_hbm >= t_tc
-                                        else "tensor (3 tf32 products per fp32 product)")
+                 math=math_name, roofline_frac=rf["roofline_us"] * 1e-6 / t,
+                 bound=rf["bound"])
+        if rf["tensor_core_layers"]:
+            r["tensor_core_layers"] = rf["tensor_core_layers"]
         return r
 
     configs = None
@@ -784,9 +815,9 @@ def run_ours(args, rank, world, local_rank):
             gather["general_bags"] = bag_modes_measure(torch, dl, synth, pk, tabs)
             if configs is not None:
                 configs[c4.name] = forward_point(c4, tabs, 5, 3)
-                # the same model with the MLPs as split-TF32 tensor-core GEMMs
-                # (opt-in, within the fp32 tolerance)
-                configs[c4.name + "_tf32x3"] = forward_point(c4, tabs, 5, 3, "tf32x3")
+                # the same model with every GEMM on the FP32 FFMA pipe (the fp32
+                # layer-wise plan runs its large GEMMs as split-TF32)
+                configs[c4.name + "_fp32_ffma"] = forward_point(c4, tabs, 5, 3, "fp32_ffma")
             del tabs
             torch.cuda.empty_cache()
         if not args.no_cpu_baseline:
@@ -806,7 +837,8 @@ def run_ours(args, rank, world, local_rank):
         us_per_batch_median=statistics.median(ms) * 1e3,
         us_per_batch_p10_p90=[float(np.percentile(ms, 10) * 1e3), float(np.percentile(ms, 90) * 1e3)],
         higher_is_better=True, scaling="weak", vs_baseline=None,
-        dtype={"fp32": "f32", "tf32": "tf32", "bf16": "bf16", "tf32x3": "3xtf32"}[args.math],
+        dtype={"fp32": "f32", "fp32_ffma": "f32", "tf32": "tf32", "bf16": "bf16",
+               "tf32x3": "3xtf32"}[args.math],
         data="synthetic: seeded SplitMix64 inputs of the workload's shapes and distributions",
         config=dict(workload=cfg.name, global_batch=cfg.batch * world, batch_per_gpu=cfg.batch,
                     tables=cfg.n_tables, rows=cfg.rows[0], emb_dim=cfg.emb_dim,

@@ -15,7 +15,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libdlrm_gb300.so")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_OOM, ERR_INDEX_OOB, ERR_TIMEOUT = range(7)
-MATH_FP32, MATH_TF32, MATH_BF16, MATH_TF32X3 = 0, 1, 2, 3
+MATH_FP32, MATH_TF32, MATH_BF16, MATH_TF32X3, MATH_FP32_FFMA = 0, 1, 2, 3, 4
 PATH_AUTO, PATH_LAYERWISE, PATH_FUSED = 0, 1, 2
 ACT_NONE, ACT_RELU, ACT_SIGMOID = 0, 1, 2
 ERRBIT_INDEX_OOB = 1 << ERR_INDEX_OOB
@@ -62,7 +62,8 @@ class _PlanInfo(ctypes.Structure):
                 ("tensor_core", ctypes.c_int32), ("tile_samples", ctypes.c_int32),
                 ("tiles", ctypes.c_int64), ("grid", ctypes.c_int32),
                 ("smem_bytes", ctypes.c_int32), ("ring_stages", ctypes.c_int32),
-                ("stream_copies", ctypes.c_int32), ("stream_bytes", ctypes.c_int64)]
+                ("stream_copies", ctypes.c_int32), ("stream_bytes", ctypes.c_int64),
+                ("tensor_core_layers", ctypes.c_int32), ("split_tf32", ctypes.c_int32)]
 
 
 def _bind(lib):

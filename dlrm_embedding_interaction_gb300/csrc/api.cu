@@ -130,6 +130,26 @@ bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
   return a0 < b0 + nb && b0 < a0 + na;
 }
 
+bool tensor_core_math(int math) { return math == DLRM_MATH_TF32 || math == DLRM_MATH_BF16; }
+bool fp32_math(int math) { return math == DLRM_MATH_FP32 || math == DLRM_MATH_FP32_FFMA; }
+
+// Layer-wise plan, GEMM layer g (bottom layers, then top) of n outputs and k
+// inputs: on the TMA tensor-core GEMM (its input a buffer of the handle, so
+// not the first bottom layer; split-TF32 in FP32 and TF32X3, where it needs
+// 64 or more inputs to pay), ...
+bool tma_layer(int math, int g, int n, int k) {
+  if (g == 0 || n < 16) return false;
+  if (math == DLRM_MATH_TF32) return true;
+  return (math == DLRM_MATH_FP32 || math == DLRM_MATH_TF32X3) && k >= 64;
+}
+bool split_tf32_math(int math) { return math == DLRM_MATH_FP32 || math == DLRM_MATH_TF32X3; }
+// ... else on the staged tcgen05 GEMM (opt-in modes only), else on FFMA.
+bool staged_tc_layer(int math, int n, int k) {
+  if (n < 16) return false;
+  if (tensor_core_math(math)) return true;
+  return math == DLRM_MATH_TF32X3 && k >= 64;
+}
+
 dlrm_status_t run_forward(dlrm_handle_t h, const float* dense, const int64_t* indices,
                           const int64_t* offsets, float* out, int batch, cudaStream_t s) {
   cudaError_t e;
@@ -173,16 +193,16 @@ dlrm_status_t run_forward(dlrm_handle_t h, const float* dense, const int64_t* in
     // [M1] bottom MLP, ReLU after every layer
     const float* in = dense;
     int ld_in = h->n_dense;
-    // GEMMs of the opt-in modes run on the tensor cores: the warp-specialized
-    // TMA GEMM where the layer has a TMA plan (TF32 / TF32X3, input in a
-    // buffer of the handle), else the staged tcgen05 GEMM. The N = 1 sigmoid
-    // layer (a dot product per row) stays on the fp32 GEMV, and in TF32X3 so
-    // do layers of fewer than 64 inputs (fp32 is then both faster and exact).
+    // GEMMs on the tensor cores: the warp-specialized TMA GEMM where the
+    // layer has a TMA plan (TF32, and split-TF32 in FP32 / TF32X3; input in a
+    // buffer of the handle), else the staged tcgen05 GEMM in the opt-in
+    // modes. Everything else, among it the N = 1 sigmoid layer (a dot product
+    // per row), runs on the FFMA pipe.
     auto linear = [&](int layer, const float* x, int ldx, const float* w, int ldw,
                       const float* b, float* y, int ldy, int n, int k, int act) {
       if (!h->tma_on.empty() && h->tma_on[layer])
         return dlrm::launch_linear_tma(h->tma[layer], batch, b, y, ldy, act, h->err, s, h->wait);
-      if (h->math != DLRM_MATH_FP32 && n >= 16 && !(h->math == DLRM_MATH_TF32X3 && k < 64))
+      if (staged_tc_layer(h->math, n, k))
         return dlrm::launch_linear_tc(x, ldx, w, ldw, b, y, ldy, batch, n, k, act,
                                       static_cast<int>(h->math), h->err, s, h->wait);
       return dlrm::launch_linear_fp32(x, ldx, w, ldw, b, y, ldy, batch, n, k, act, s);
@@ -275,7 +295,8 @@ dlrm_status_t check_config(const dlrm_config_t* cfg, size_t smem_limit) {
   if (static_cast<int64_t>(cfg->max_batch) * cfg->bag_size > (int64_t(1) << 31))
     return DLRM_ERR_UNSUPPORTED;
   if (cfg->math != DLRM_MATH_FP32 && cfg->math != DLRM_MATH_TF32 &&
-      cfg->math != DLRM_MATH_BF16 && cfg->math != DLRM_MATH_TF32X3)
+      cfg->math != DLRM_MATH_BF16 && cfg->math != DLRM_MATH_TF32X3 &&
+      cfg->math != DLRM_MATH_FP32_FFMA)
     return DLRM_ERR_INVALID_ARG;
   if (cfg->path != DLRM_PATH_AUTO && cfg->path != DLRM_PATH_LAYERWISE &&
       cfg->path != DLRM_PATH_FUSED)
@@ -288,13 +309,10 @@ dlrm_status_t check_config(const dlrm_config_t* cfg, size_t smem_limit) {
   return DLRM_OK;
 }
 
-bool tensor_core_math(int math) { return math == DLRM_MATH_TF32 || math == DLRM_MATH_BF16; }
-
 // The fused planner is consulted unless the layer-wise plan was asked for or
 // the math has no fused kernel (TF32X3).
 bool wants_fused_plan(const dlrm_config_t* cfg) {
-  return cfg->path != DLRM_PATH_LAYERWISE &&
-         (cfg->math == DLRM_MATH_FP32 || tensor_core_math(cfg->math));
+  return cfg->path != DLRM_PATH_LAYERWISE && (fp32_math(cfg->math) || tensor_core_math(cfg->math));
 }
 
 struct PlanChoice {
@@ -469,13 +487,12 @@ dlrm_status_t dlrm_create(const dlrm_config_t* cfg, const float* const* tables,
   const size_t off_idx = plan.take<int64_t>(mb * h->k * h->bag);
   const size_t off_off = plan.take<int64_t>(mb * h->k);
   const size_t off_out = plan.take<float>(mb);
-  // Layer-wise TF32 / TF32X3: the warp-specialized TMA GEMM for every
-  // tensor-core layer whose input is a buffer of the handle (all but the
-  // first bottom layer, which reads the caller's dense rows); in TF32X3 only
-  // for layers of 64 or more inputs, whose weights get two more copies: their
-  // tf32 head and the remainder.
+  // Layer-wise plan: the warp-specialized TMA GEMM for the layers tma_layer
+  // picks; in split-TF32 (FP32, TF32X3) their weights get two more copies:
+  // their tf32 head and the remainder.
   const bool tma_math = h->path == DLRM_PATH_LAYERWISE &&
-                        (h->math == DLRM_MATH_TF32 || h->math == DLRM_MATH_TF32X3);
+                        (h->math == DLRM_MATH_TF32 || split_tf32_math(h->math));
+  const bool split = split_tf32_math(h->math);
   const int n_layers = h->n_bot + h->n_top;
   std::vector<size_t> off_whi(n_layers, 0), off_wlo(n_layers, 0);
   std::vector<char> want_tma(n_layers, 0);
@@ -490,9 +507,9 @@ dlrm_status_t dlrm_create(const dlrm_config_t* cfg, const float* const* tables,
     for (int g = 1; g < n_layers; ++g) {
       int n, k, ldw;
       layer_shape(g, &n, &k, &ldw);
-      if (n < 16 || (h->math == DLRM_MATH_TF32X3 && k < 64)) continue;
+      if (!tma_layer(h->math, g, n, k)) continue;
       want_tma[g] = 1;
-      if (h->math == DLRM_MATH_TF32X3) {
+      if (split) {
         off_whi[g] = plan.take<float>(static_cast<size_t>(n) * ldw);
         off_wlo[g] = plan.take<float>(static_cast<size_t>(n) * ldw);
       }
@@ -606,7 +623,7 @@ dlrm_status_t dlrm_create(const dlrm_config_t* cfg, const float* const* tables,
       dlrm::TmaLayer& T = h->tma[g];
       T.n = n;
       T.k = k;
-      T.split = h->math == DLRM_MATH_TF32X3 ? 1 : 0;
+      T.split = split ? 1 : 0;
       const float* w_head = w;
       if (T.split) {
         // w = head + rest: head keeps the top 10 mantissa bits (exact in
@@ -695,6 +712,17 @@ dlrm_status_t dlrm_plan_query(const dlrm_config_t* cfg, int32_t sm_count, int64_
     r.stream_copies = tc ? tplan.params.n_tiles : fplan.params.n_stages;
     r.stream_bytes = tc ? static_cast<int64_t>(tplan.wstream.size())
                         : static_cast<int64_t>(fplan.wstream.size() * sizeof(float));
+  }
+  if (c.path == DLRM_PATH_LAYERWISE) {
+    for (int g = 0; g < cfg->n_bot + cfg->n_top; ++g) {
+      const bool top = g >= cfg->n_bot;
+      const int l = top ? g - cfg->n_bot : g;
+      const int n = top ? cfg->ln_top[l + 1] : cfg->ln_bot[l + 1];
+      const int k = top ? cfg->ln_top[l] : cfg->ln_bot[l];
+      if (tma_layer(cfg->math, g, n, k) || staged_tc_layer(cfg->math, n, k))
+        r.tensor_core_layers |= 1 << g;
+    }
+    r.split_tf32 = (r.tensor_core_layers && split_tf32_math(cfg->math)) ? 1 : 0;
   }
   *info = r;
   return DLRM_OK;
@@ -960,7 +988,7 @@ dlrm_status_t linear_bias_act(const float* x, int32_t ld_x, const float* W, cons
   if (act != DLRM_ACT_NONE && act != DLRM_ACT_RELU && act != DLRM_ACT_SIGMOID)
     return DLRM_ERR_INVALID_ARG;
   if (math != DLRM_MATH_FP32 && math != DLRM_MATH_TF32 && math != DLRM_MATH_BF16 &&
-      math != DLRM_MATH_TF32X3)
+      math != DLRM_MATH_TF32X3 && math != DLRM_MATH_FP32_FFMA)
     return DLRM_ERR_INVALID_ARG;
   if (M == 0) return DLRM_OK;
   if (!x || !W || !y) return DLRM_ERR_INVALID_ARG;
@@ -972,7 +1000,7 @@ dlrm_status_t linear_bias_act(const float* x, int32_t ld_x, const float* W, cons
   const size_t wbytes = static_cast<size_t>(N) * K * sizeof(float);
   if (ranges_overlap(y, ybytes, x, xbytes) || ranges_overlap(y, ybytes, W, wbytes))
     return DLRM_ERR_INVALID_ARG;
-  if (math != DLRM_MATH_FP32)
+  if (!fp32_math(math))
     return cuda_status(dlrm::launch_linear_tc(x, ld_x, W, K, bias, y, ld_y, M, N, K, act,
                                               static_cast<int>(math), nullptr,
                                               static_cast<cudaStream_t>(stream)));

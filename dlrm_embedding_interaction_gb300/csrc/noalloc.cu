@@ -52,7 +52,7 @@ extern "C" dlrm_status_t dlrm_forward_noalloc(
   const int64_t p = f * (f - 1) / 2;
   if (cfg->ln_bot[cfg->n_bot] != d || cfg->ln_top[0] != d + p || cfg->ln_top[cfg->n_top] != 1)
     return DLRM_ERR_INVALID_ARG;
-  if (cfg->math != DLRM_MATH_FP32) return DLRM_ERR_UNSUPPORTED;
+  if (cfg->math != DLRM_MATH_FP32 && cfg->math != DLRM_MATH_FP32_FFMA) return DLRM_ERR_UNSUPPORTED;
   dlrm::GatherTables tabs{};
   if (!dlrm::aligned_to(dense, sizeof(float)) || !dlrm::aligned_to(indices, sizeof(int64_t)) ||
       !dlrm::aligned_to(offsets, sizeof(int64_t)) || !dlrm::aligned_to(out, sizeof(float)) ||

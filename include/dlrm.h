@@ -49,18 +49,26 @@ typedef enum {
   DLRM_ERR_TIMEOUT = 6       /* a bounded device wait gave up */
 } dlrm_status_t;
 
-/* Arithmetic of the MLP GEMMs. FP32 (SIMT FFMA) is the parity mode. TF32 and
- * BF16 run the MLPs on the tcgen05 tensor cores with fp32 accumulation in
- * TMEM (opt-in; results within rel 2e-2 of fp32). TF32X3 splits every fp32
- * operand into a tf32 head and its exact remainder and sums three tensor-core
- * products (head*head + head*rest + rest*head): opt-in, on the tensor cores,
- * with errors inside the fp32 parity tolerance (about 2^-21 relative per
- * product). */
+/* Arithmetic of the MLP GEMMs.
+ * FP32 is the parity mode: results within the fp32 tolerance. The fused plan
+ * and every small GEMM run on the FP32 FFMA pipe; the layer-wise plan runs
+ * each GEMM of 64 or more inputs and 16 or more outputs (but the first
+ * bottom layer, which reads the caller's buffer) as split-TF32 on the
+ * tcgen05 tensor cores: every fp32 operand is split into a tf32 head and
+ * its exact remainder and three products are summed in fp32 (head*head +
+ * head*rest + rest*head, about 2^-21 relative per product).
+ * FP32_FFMA is FP32 with every GEMM on the FFMA pipe.
+ * TF32 and BF16 run the MLPs on the tensor cores with fp32 accumulation in
+ * TMEM (opt-in; results within rel 2e-2 of fp32).
+ * TF32X3 is split-TF32 on the tensor cores for every GEMM of 64 or more
+ * inputs and 16 or more outputs, in the layer-wise plan and in
+ * linear_bias_act; it has no fused plan. */
 typedef enum {
   DLRM_MATH_FP32 = 0,
   DLRM_MATH_TF32 = 1,
   DLRM_MATH_BF16 = 2,
-  DLRM_MATH_TF32X3 = 3
+  DLRM_MATH_TF32X3 = 3,
+  DLRM_MATH_FP32_FFMA = 4
 } dlrm_math_t;
 
 /* Kernel plan of a forward handle. AUTO takes the fused single-launch forward
@@ -164,6 +172,11 @@ typedef struct {
   int32_t ring_stages;     /* depth of the fused weight ring */
   int32_t stream_copies;   /* bulk copies in one pass over the weight stream */
   int64_t stream_bytes;    /* packed MLP weight stream of the fused kernel */
+  int32_t tensor_core_layers;  /* layer-wise plan: bit g set when Linear layer g
+                                  (bottom layers first, then top) runs on the
+                                  tcgen05 tensor cores; 0 for a fused plan */
+  int32_t split_tf32;      /* 1: those layers compute split-TF32 (three tf32
+                              products per fp32 product) */
 } dlrm_plan_info_t;
 
 dlrm_status_t dlrm_plan_query(const dlrm_config_t* cfg, int32_t sm_count,
@@ -281,7 +294,8 @@ void dlrm_destroy(dlrm_handle_t h);
  * under a device-memory budget fixed at start-up.
  *
  * There is no handle: the caller passes the shape (cfg; cfg->math must be
- * DLRM_MATH_FP32, cfg->max_batch is ignored), the DEVICE pointers of the
+ * DLRM_MATH_FP32 or DLRM_MATH_FP32_FFMA, both the FFMA fused kernel here;
+ * cfg->max_batch is ignored), the DEVICE pointers of the
  * tables and of the Linear weights (PyTorch (out, in) layout, contiguous) and
  * biases, and the inputs and output exactly as for dlrm_forward. err_flag is
  * an optional device int32 word into which the DLRM_ERRBIT_* bits of this
@@ -411,7 +425,8 @@ dlrm_status_t pairwise_pair_map(int32_t F, int32_t* i_out, int32_t* j_out, void*
  *   bias  (N) fp32 or NULL (no bias)
  *   y     (M, N) fp32, row stride ld_y >= N; must not overlap x or W
  * act: DLRM_ACT_NONE / RELU / SIGMOID (1 / (1 + exp(-a))).
- * math: DLRM_MATH_FP32 (parity) or an opt-in tensor-core mode.
+ * math: DLRM_MATH_FP32 or DLRM_MATH_FP32_FFMA (both on the FFMA pipe here),
+ * or an opt-in tensor-core mode.
  * M >= 0 (0 is a no-op), N >= 1, K >= 1. */
 dlrm_status_t linear_bias_act(const float* x, int32_t ld_x, const float* W, const float* bias,
                               float* y, int32_t ld_y, int32_t M, int32_t N, int32_t K,

@@ -55,6 +55,10 @@ def test_host_side_argument_checks(lib):
     assert lib.linear_bias_act(null, 4, null, null, null, 4, 4, 4, 0, 0, 0, null) == dl.ERR_INVALID_ARG
     assert lib.linear_bias_act(null, 3, null, null, null, 4, 4, 4, 4, 0, 0, null) == dl.ERR_INVALID_ARG
     assert lib.linear_bias_act(null, 4, null, null, null, 4, 4, 4, 4, 7, 0, null) == dl.ERR_INVALID_ARG
+    # unknown math mode; every known one (FP32_FFMA = 4 the last) passes the check
+    assert lib.linear_bias_act(null, 4, null, null, null, 4, 0, 4, 4, 0, 5, null) == dl.ERR_INVALID_ARG
+    for math in (dl.MATH_FP32, dl.MATH_TF32, dl.MATH_BF16, dl.MATH_TF32X3, dl.MATH_FP32_FFMA):
+        assert lib.linear_bias_act(null, 4, null, null, null, 4, 0, 4, 4, 0, math, null) == dl.OK
     # M = 0 is a no-op
     assert lib.linear_bias_act(null, 4, null, null, null, 4, 0, 4, 4, 0, 0, null) == dl.OK
     # null pointers with M > 0

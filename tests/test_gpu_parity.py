@@ -253,6 +253,18 @@ def test_forward_matches_oracle(name, path):
     model.close()
 
 
+@pytest.mark.parametrize("name", ["tiny_b64_k3", "b2048_k3", "b2048_k32", "sweep_b1_k1",
+                                  "sweep_b1500_k3", "sweep_b4096_k8"])
+def test_forward_ffma_layerwise_matches_oracle(name):
+    """FP32_FFMA: the layer-wise plan with every GEMM on the FFMA pipe (plain
+    FP32 runs the large ones as split-TF32 on the tensor cores)."""
+    cfg = synth.get_config(name)
+    inp = synth.make_inputs(cfg, seed=1234)
+    model = make_model(cfg, inp, math=dl.MATH_FP32_FFMA, path=dl.PATH_LAYERWISE)
+    close(run_forward(model, inp), oracle.forward(inp))
+    model.close()
+
+
 @pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
 def test_forward_odd_widths_matches_oracle(path):
     """Layers wider than 512 (two column passes), and 128-, 100- and 32-wide

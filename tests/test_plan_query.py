@@ -127,6 +127,36 @@ def test_small_shared_memory_leaves_the_fused_kernel_out():
     assert e.value.status == dl.ERR_UNSUPPORTED
 
 
+def test_layerwise_tensor_core_layers():
+    """Which layer-wise GEMMs run on the tensor cores. The 26-table model has
+    bottom 13-512-256-128 and top 479-1024-1024-512-256-1 (layers 0-2, 3-7):
+    FP32 and TF32X3 take split-TF32 for every layer of >= 64 inputs and >= 16
+    outputs but the first bottom layer (13 inputs; it reads the caller's
+    buffer), FP32_FFMA none, TF32 and BF16 every layer of >= 16 outputs."""
+    big = synth.get_config("b65536_k26_zipf")
+    split_layers = 0b01111110            # layers 1..6; 7 is the N = 1 sigmoid layer
+    for math in (dl.MATH_FP32, dl.MATH_TF32X3):
+        p = query(big, math, path=dl.PATH_LAYERWISE)
+        assert (p["tensor_core_layers"], p["split_tf32"]) == (split_layers, 1)
+    p = query(big, dl.MATH_FP32_FFMA, path=dl.PATH_LAYERWISE)
+    assert (p["tensor_core_layers"], p["split_tf32"]) == (0, 0)
+    for math in (dl.MATH_TF32, dl.MATH_BF16):
+        p = query(big, math, path=dl.PATH_LAYERWISE)
+        assert (p["tensor_core_layers"], p["split_tf32"]) == (0b01111111, 0)
+    # AUTO takes the layer-wise plan for this model in fp32: the same layers
+    assert query(big)["tensor_core_layers"] == split_layers
+    # a fused plan reports none
+    cfg = synth.get_config("b2048_k3")
+    assert query(cfg)["tensor_core_layers"] == 0
+
+
+def test_ffma_mode_plans_like_fp32_when_fused():
+    """FP32_FFMA takes the same fused plan as FP32 (the fused kernel is FFMA)."""
+    for name in ("b2048_k3", "tiny_b64_k3", "sweep_b8192_k16"):
+        cfg = synth.get_config(name)
+        assert query(cfg, dl.MATH_FP32_FFMA) == query(cfg, dl.MATH_FP32)
+
+
 @pytest.mark.parametrize("math", [dl.MATH_FP32, dl.MATH_TF32, dl.MATH_BF16])
 def test_every_sweep_plan_is_consistent(math):
     """Over the 11 x 5 batch x tables sweep: a fused plan fits the device's
