@@ -30,7 +30,8 @@ EXPORTS = ("dlrm_version", "dlrm_status_string", "dlrm_create", "dlrm_forward",
            "dlrm_forward_noalloc", "dlrm_set_phase_trace", "dlrm_plan_query",
            "embedding_bag_sum_multi", "embedding_bag_multi", "embedding_bag_multi_ex",
            "pairwise_dot_lower_tri",
-           "pairwise_pair_map", "linear_bias_act", "dlrm_test_stall")
+           "pairwise_pair_map", "linear_bias_act", "dlrm_test_stall",
+           "dlrm_set_cluster_batch_limit", "dlrm_get_cluster_batch_limit")
 NOALLOC_SCRATCH_BYTES = 16 << 20
 TRACE_SLOTS = 40
 
@@ -77,6 +78,8 @@ def _bind(lib):
         "dlrm_forward_host": ([vp, vp, vp, vp, vp, i32, vp], st),
         "dlrm_get_error": ([vp, vp], st),
         "dlrm_test_stall": ([vp, i64, i32], st),
+        "dlrm_set_cluster_batch_limit": ([vp, i32], st),
+        "dlrm_get_cluster_batch_limit": ([vp, vp], st),
         "dlrm_workspace_bytes": ([vp], i64),
         "dlrm_destroy": ([vp], None),
         "dlrm_path": ([vp], i32),
@@ -512,6 +515,23 @@ def dlrm_test_stall(h: int, wait_limit_ns: int = 0, withhold_last: bool = False)
            "dlrm_test_stall")
 
 
+def dlrm_set_cluster_batch_limit(h: int, limit: int) -> None:
+    """Forwards of at most ``limit`` samples on ``h`` take the cluster-split
+    fused kernel (0: never; -1: the default)."""
+    _handle_shape(h, "dlrm_set_cluster_batch_limit")
+    _check(lib().dlrm_set_cluster_batch_limit(ctypes.c_void_p(h), int(limit)),
+           "dlrm_set_cluster_batch_limit")
+
+
+def dlrm_get_cluster_batch_limit(h: int) -> int:
+    """The largest batch ``h`` runs on the cluster-split kernel (0: none)."""
+    _handle_shape(h, "dlrm_get_cluster_batch_limit")
+    v = ctypes.c_int32(0)
+    _check(lib().dlrm_get_cluster_batch_limit(ctypes.c_void_p(h), ctypes.byref(v)),
+           "dlrm_get_cluster_batch_limit")
+    return int(v.value)
+
+
 def dlrm_workspace_bytes(h: int) -> int:
     return int(lib().dlrm_workspace_bytes(ctypes.c_void_p(h)))
 
@@ -583,6 +603,15 @@ class DlrmModel:
 
     def stage_names(self):
         return [dlrm_stage_name(self.handle, i) for i in range(dlrm_num_stages(self.handle))]
+
+    @property
+    def cluster_batch_limit(self) -> int:
+        """Forwards of at most this many samples take the cluster-split kernel."""
+        return dlrm_get_cluster_batch_limit(self.handle)
+
+    @cluster_batch_limit.setter
+    def cluster_batch_limit(self, limit: int) -> None:
+        dlrm_set_cluster_batch_limit(self.handle, limit)
 
     def set_profiling(self, enable: bool) -> None:
         dlrm_set_profiling(self.handle, enable)

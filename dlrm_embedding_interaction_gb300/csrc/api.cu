@@ -19,6 +19,7 @@
 
 #include "common.cuh"
 #include "fused.cuh"
+#include "fused_cluster.cuh"
 #include "fused_tc.cuh"
 #include "gemm_tma.cuh"
 
@@ -96,6 +97,12 @@ struct dlrm_handle_s {
   dlrm::FusedParams fused{};     // per-call fields filled by run_forward
   bool fused_tc = false;         // the fused plan runs on the tensor cores (TF32 / BF16)
   dlrm::FusedTcParams tcp{};
+  // fp32 fused plan, small batches: the cluster-split kernel (fused_cluster.cu)
+  bool cluster_on = false;
+  dlrm::ClusterParams cparams[3]{};   // per tile height (4, 8, 16 samples)
+  int cmax[3] = {0, 0, 0};            // clusters one wave holds (0: height unavailable)
+  int cluster_limit = 0;              // batches up to this run on the cluster kernel
+  int cluster_default = 0;
   unsigned long long* trace = nullptr;
   dlrm::WaitCfg wait{};          // dlrm_test_stall: wait limit, withheld last copy
   // layer-wise TF32 / TF32X3: per layer (bottom, then top), the TMA plan of
@@ -129,6 +136,21 @@ bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
   const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
   return a0 < b0 + nb && b0 < a0 + na;
 }
+
+// The cluster-split kernel for small batches of the fp32 fused plan: CTAs per
+// cluster, and the largest batch it takes by default (one wave of clusters
+// at most). Measured on the 13-512-256-64 / 512-256-1 models: it wins up to 64
+// samples at any table count (20-23 against 27-47 us), and up to 128 with 16
+// or more tables, whose wide interaction and top input slow the one-CTA tile
+// more (128 samples, 32 tables: 37 against 47 us); at 128 samples and 8
+// tables or fewer the one-CTA kernel is as fast.
+constexpr int kClusterSize = 8;
+int cluster_max_batch(int n_tables) { return n_tables >= 16 ? 128 : 64; }
+// It pays only for models whose weights the one-CTA tile streams for long:
+// a stream of 1 MiB (32 stages; 1.3 MB on those models) or more. The 20 KB
+// weights of a 64-wide model run in 14 us on one CTA per tile, against the
+// cluster kernel's ~20 us of exchanges.
+constexpr size_t kClusterMinStreamBytes = size_t(1) << 20;
 
 bool tensor_core_math(int math) { return math == DLRM_MATH_TF32 || math == DLRM_MATH_BF16; }
 bool fp32_math(int math) { return math == DLRM_MATH_FP32 || math == DLRM_MATH_FP32_FFMA; }
@@ -181,6 +203,25 @@ dlrm_status_t run_forward(dlrm_handle_t h, const float* dense, const int64_t* in
       q.trace = h->trace;
       q.wait = h->wait;
       e = dlrm::launch_fused_tc(q, s);
+    } else if (h->cluster_on && batch <= h->cluster_limit && !h->trace) {
+      // the smallest tile height whose tiles fit one wave of clusters,
+      // else the tallest available
+      int hi = -1;
+      for (int i = 0; i < 3 && hi < 0; ++i) {
+        const int bm = dlrm::kClusterTileRows[i];
+        if (h->cmax[i] > 0 && (batch + bm - 1) / bm <= h->cmax[i]) hi = i;
+      }
+      for (int i = 2; i >= 0 && hi < 0; --i)
+        if (h->cmax[i] > 0) hi = i;
+      dlrm::ClusterParams q = h->cparams[hi];
+      q.batch = batch;
+      q.dense = dense;
+      q.indices = indices;
+      q.offsets = offsets;
+      q.out = out;
+      q.err = h->err;
+      q.wait = h->wait;
+      e = dlrm::launch_fused_cluster(q, s);
     } else {
       e = dlrm::launch_fused(p, h->fused_bm, s);
     }
@@ -527,6 +568,22 @@ dlrm_status_t dlrm_create(const dlrm_config_t* cfg, const float* const* tables,
     off_fb = plan.take<float>(fplan.bias.size());
     off_fl = plan.take<float>(fplan.wlast.size());
   }
+  // the cluster-split kernel's weight streams, stage table, bias blocks
+  dlrm::ClusterPlan cplan;
+  bool cluster_planned = false;
+  size_t off_cw = 0, off_ct = 0, off_cb = 0, off_cl = 0;
+  if (h->path == DLRM_PATH_FUSED && !h->fused_tc &&
+      fplan.wstream.size() * sizeof(float) >= kClusterMinStreamBytes) {
+    cluster_planned = dlrm::fused_cluster_plan(h->n_dense, h->k, h->d, h->bag, h->ln_bot,
+                                               h->ln_top, hw, hb, h->tabs, kClusterSize,
+                                               dlrm::device_max_smem_optin(), &cplan);
+    if (cluster_planned) {
+      off_cw = plan.take<float>(cplan.wstream.size());
+      off_ct = plan.take<uint2>(cplan.stage_tab.size());
+      off_cb = plan.take<float>(cplan.bias.size());
+      off_cl = plan.take<float>(cplan.wlast.size());
+    }
+  }
 
   if (cudaMalloc(&h->arena, plan.bytes) != cudaSuccess) {
     cudaGetLastError();
@@ -589,6 +646,34 @@ dlrm_status_t dlrm_create(const dlrm_config_t* cfg, const float* const* tables,
     h->fused.bias = at(off_fb);
     h->fused.wlast = at(off_fl);
     if (st == DLRM_OK) st = cuda_status(dlrm::fused_prepare(h->fused_bm, h->fused.cw, h->fused.lda));
+  }
+  if (cluster_planned && st == DLRM_OK) {
+    st = cuda_status(cudaMemcpy(at(off_cw), cplan.wstream.data(),
+                                cplan.wstream.size() * sizeof(float), cudaMemcpyHostToDevice));
+    if (st == DLRM_OK)
+      st = cuda_status(cudaMemcpy(at(off_ct), cplan.stage_tab.data(),
+                                  cplan.stage_tab.size() * sizeof(uint2), cudaMemcpyHostToDevice));
+    if (st == DLRM_OK)
+      st = cuda_status(cudaMemcpy(at(off_cb), cplan.bias.data(), cplan.bias.size() * sizeof(float),
+                                  cudaMemcpyHostToDevice));
+    if (st == DLRM_OK)
+      st = cuda_status(cudaMemcpy(at(off_cl), cplan.wlast.data(),
+                                  cplan.wlast.size() * sizeof(float), cudaMemcpyHostToDevice));
+    int limit = 0;
+    for (int i = 0; i < 3 && st == DLRM_OK; ++i) {
+      if (!cplan.fits[i]) continue;
+      dlrm::ClusterParams& q = h->cparams[i];
+      q = cplan.params[i];
+      q.wstream = at(off_cw);
+      q.stage_tab = reinterpret_cast<const uint2*>(at(off_ct));
+      q.bias = at(off_cb);
+      q.wlast = at(off_cl);
+      h->cmax[i] = dlrm::fused_cluster_max_active(q.bm, q.csize, q.smem_bytes);
+      limit = std::max(limit, h->cmax[i] * q.bm);
+    }
+    h->cluster_default = std::min(limit, cluster_max_batch(h->k));
+    h->cluster_limit = h->cluster_default;
+    h->cluster_on = h->cluster_limit > 0;
   }
   if (st == DLRM_OK) st = cuda_status(cudaDeviceSynchronize());
   if (st != DLRM_OK) {
@@ -810,6 +895,25 @@ dlrm_status_t dlrm_test_stall(dlrm_handle_t h, int64_t wait_limit_ns, int32_t wi
   if (!h || wait_limit_ns < 0) return DLRM_ERR_INVALID_ARG;
   h->wait.limit_ns = static_cast<uint64_t>(wait_limit_ns);
   h->wait.withhold_last = withhold_last ? 1 : 0;
+  return DLRM_OK;
+}
+
+dlrm_status_t dlrm_set_cluster_batch_limit(dlrm_handle_t h, int32_t limit) {
+  if (!h || limit < -1) return DLRM_ERR_INVALID_ARG;
+  const bool planned = h->cluster_default > 0;
+  if (limit == -1) {
+    h->cluster_limit = h->cluster_default;
+  } else {
+    if (limit > 0 && !planned) return DLRM_ERR_UNSUPPORTED;
+    h->cluster_limit = limit;
+  }
+  h->cluster_on = planned && h->cluster_limit > 0;
+  return DLRM_OK;
+}
+
+dlrm_status_t dlrm_get_cluster_batch_limit(dlrm_handle_t h, int32_t* limit) {
+  if (!h || !limit) return DLRM_ERR_INVALID_ARG;
+  *limit = h->cluster_on ? h->cluster_limit : 0;
   return DLRM_OK;
 }
 

@@ -9,7 +9,9 @@ hangs: the launch returns, dlrm_get_error reports DLRM_ERR_TIMEOUT, and the
 next normal forward on the same handle matches the oracle.
 
 Covered: the fused fp32 kernel (one tile per CTA, and several tiles per CTA
-on the persistent path), the fused tensor-core kernel (BF16 and TF32), and
+on the persistent path), the cluster-split fp32 kernel of small batches
+(weight stages and the exchanges between the cluster's CTAs), the fused
+tensor-core kernel (BF16 and TF32), and
 the layer-wise tensor-core GEMM (TF32X3 and BF16).
 """
 import time
@@ -46,12 +48,13 @@ CASES = [
     # workload, math, path, tolerance (atol, rtol)
     ("b2048_k3", dl.MATH_FP32, dl.PATH_FUSED, (1e-5, 1e-4)),
     ("sweep_b8192_k3", dl.MATH_FP32, dl.PATH_FUSED, (1e-5, 1e-4)),   # several tiles per CTA
+    ("sweep_b64_k3", dl.MATH_FP32, dl.PATH_FUSED, (1e-5, 1e-4)),     # the cluster-split kernel
     ("b2048_k3", dl.MATH_BF16, dl.PATH_FUSED, (2e-2, 2e-2)),
     ("tiny_b64_k3", dl.MATH_TF32, dl.PATH_FUSED, (2e-2, 2e-2)),
     ("tiny_b64_k3", dl.MATH_TF32X3, dl.PATH_LAYERWISE, (1e-5, 1e-4)),
     ("b2048_k3", dl.MATH_BF16, dl.PATH_LAYERWISE, (2e-2, 2e-2)),
 ]
-IDS = ["fp32-fused", "fp32-fused-persistent", "bf16-fused", "tf32-fused", "tf32x3-layerwise",
+IDS = ["fp32-fused", "fp32-fused-persistent", "fp32-fused-cluster", "bf16-fused", "tf32-fused", "tf32x3-layerwise",
        "bf16-layerwise"]
 
 
