@@ -99,8 +99,10 @@ struct dlrm_handle_s {
   dlrm::FusedTcParams tcp{};
   // fp32 fused plan, small batches: the cluster-split kernel (fused_cluster.cu)
   bool cluster_on = false;
-  dlrm::ClusterParams cparams[3]{};   // per tile height (4, 8, 16 samples)
-  int cmax[3] = {0, 0, 0};            // clusters one wave holds (0: height unavailable)
+  // per cluster size (kClusterSizes) and tile height (4, 8, 16 samples): the
+  // parameter block, and the clusters one wave holds (0: unavailable)
+  dlrm::ClusterParams cparams[2][3]{};
+  int cmax[2][3] = {{0, 0, 0}, {0, 0, 0}};
   int cluster_limit = 0;              // batches up to this run on the cluster kernel
   int cluster_default = 0;
   unsigned long long* trace = nullptr;
@@ -144,8 +146,12 @@ bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
 // or more tables, whose wide interaction and top input slow the one-CTA tile
 // more (128 samples, 32 tables: 37 against 47 us); at 128 samples and 8
 // tables or fewer the one-CTA kernel is as fast.
-constexpr int kClusterSize = 8;
-int cluster_max_batch(int n_tables) { return n_tables >= 16 ? 128 : 64; }
+constexpr int kClusterSizes[2] = {8, 4};
+int cluster_max_batch(int n_tables) { return n_tables >= 16 ? 256 : 128; }
+// Clusters of 8 CTAs up to this batch (the fewest weights per CTA: 20 us at
+// 1-32 samples against 22.5 with 4), clusters of 4 above it (128 samples, 3
+// tables: 22.6 us against 28.8 with 8 and 26.7 on one CTA per tile).
+constexpr int kWideClusterMaxBatch = 32;
 // It pays only for models whose weights the one-CTA tile streams for long:
 // a stream of 1 MiB (32 stages; 1.3 MB on those models) or more. The 20 KB
 // weights of a 64-wide model run in 14 us on one CTA per tile, against the
@@ -204,16 +210,20 @@ dlrm_status_t run_forward(dlrm_handle_t h, const float* dense, const int64_t* in
       q.wait = h->wait;
       e = dlrm::launch_fused_tc(q, s);
     } else if (h->cluster_on && batch <= h->cluster_limit && !h->trace) {
-      // the smallest tile height whose tiles fit one wave of clusters,
+      // clusters of 8 for the smallest batches, else of 4 (when planned);
+      // then the smallest tile height whose tiles fit one wave of clusters,
       // else the tallest available
+      const bool have8 = h->cmax[0][0] + h->cmax[0][1] + h->cmax[0][2] > 0;
+      const bool have4 = h->cmax[1][0] + h->cmax[1][1] + h->cmax[1][2] > 0;
+      const int ci = (have4 && (batch > kWideClusterMaxBatch || !have8)) ? 1 : 0;
       int hi = -1;
       for (int i = 0; i < 3 && hi < 0; ++i) {
         const int bm = dlrm::kClusterTileRows[i];
-        if (h->cmax[i] > 0 && (batch + bm - 1) / bm <= h->cmax[i]) hi = i;
+        if (h->cmax[ci][i] > 0 && (batch + bm - 1) / bm <= h->cmax[ci][i]) hi = i;
       }
       for (int i = 2; i >= 0 && hi < 0; --i)
-        if (h->cmax[i] > 0) hi = i;
-      dlrm::ClusterParams q = h->cparams[hi];
+        if (h->cmax[ci][i] > 0) hi = i;
+      dlrm::ClusterParams q = h->cparams[ci][hi];
       q.batch = batch;
       q.dense = dense;
       q.indices = indices;
@@ -569,19 +579,21 @@ dlrm_status_t dlrm_create(const dlrm_config_t* cfg, const float* const* tables,
     off_fl = plan.take<float>(fplan.wlast.size());
   }
   // the cluster-split kernel's weight streams, stage table, bias blocks
-  dlrm::ClusterPlan cplan;
-  bool cluster_planned = false;
-  size_t off_cw = 0, off_ct = 0, off_cb = 0, off_cl = 0;
+  dlrm::ClusterPlan cplan[2];
+  bool cluster_planned[2] = {false, false};
+  size_t off_cw[2] = {0, 0}, off_ct[2] = {0, 0}, off_cb[2] = {0, 0}, off_cl[2] = {0, 0};
   if (h->path == DLRM_PATH_FUSED && !h->fused_tc &&
       fplan.wstream.size() * sizeof(float) >= kClusterMinStreamBytes) {
-    cluster_planned = dlrm::fused_cluster_plan(h->n_dense, h->k, h->d, h->bag, h->ln_bot,
-                                               h->ln_top, hw, hb, h->tabs, kClusterSize,
-                                               dlrm::device_max_smem_optin(), &cplan);
-    if (cluster_planned) {
-      off_cw = plan.take<float>(cplan.wstream.size());
-      off_ct = plan.take<uint2>(cplan.stage_tab.size());
-      off_cb = plan.take<float>(cplan.bias.size());
-      off_cl = plan.take<float>(cplan.wlast.size());
+    for (int ci = 0; ci < 2; ++ci) {
+      cluster_planned[ci] = dlrm::fused_cluster_plan(
+          h->n_dense, h->k, h->d, h->bag, h->ln_bot, h->ln_top, hw, hb, h->tabs,
+          kClusterSizes[ci], dlrm::device_max_smem_optin(), &cplan[ci]);
+      if (cluster_planned[ci]) {
+        off_cw[ci] = plan.take<float>(cplan[ci].wstream.size());
+        off_ct[ci] = plan.take<uint2>(cplan[ci].stage_tab.size());
+        off_cb[ci] = plan.take<float>(cplan[ci].bias.size());
+        off_cl[ci] = plan.take<float>(cplan[ci].wlast.size());
+      }
     }
   }
 
@@ -647,34 +659,36 @@ dlrm_status_t dlrm_create(const dlrm_config_t* cfg, const float* const* tables,
     h->fused.wlast = at(off_fl);
     if (st == DLRM_OK) st = cuda_status(dlrm::fused_prepare(h->fused_bm, h->fused.cw, h->fused.lda));
   }
-  if (cluster_planned && st == DLRM_OK) {
-    st = cuda_status(cudaMemcpy(at(off_cw), cplan.wstream.data(),
-                                cplan.wstream.size() * sizeof(float), cudaMemcpyHostToDevice));
+  int cluster_limit = 0;
+  for (int ci = 0; ci < 2 && st == DLRM_OK; ++ci) {
+    if (!cluster_planned[ci]) continue;
+    const dlrm::ClusterPlan& cp = cplan[ci];
+    st = cuda_status(cudaMemcpy(at(off_cw[ci]), cp.wstream.data(),
+                                cp.wstream.size() * sizeof(float), cudaMemcpyHostToDevice));
     if (st == DLRM_OK)
-      st = cuda_status(cudaMemcpy(at(off_ct), cplan.stage_tab.data(),
-                                  cplan.stage_tab.size() * sizeof(uint2), cudaMemcpyHostToDevice));
+      st = cuda_status(cudaMemcpy(at(off_ct[ci]), cp.stage_tab.data(),
+                                  cp.stage_tab.size() * sizeof(uint2), cudaMemcpyHostToDevice));
     if (st == DLRM_OK)
-      st = cuda_status(cudaMemcpy(at(off_cb), cplan.bias.data(), cplan.bias.size() * sizeof(float),
+      st = cuda_status(cudaMemcpy(at(off_cb[ci]), cp.bias.data(), cp.bias.size() * sizeof(float),
                                   cudaMemcpyHostToDevice));
     if (st == DLRM_OK)
-      st = cuda_status(cudaMemcpy(at(off_cl), cplan.wlast.data(),
-                                  cplan.wlast.size() * sizeof(float), cudaMemcpyHostToDevice));
-    int limit = 0;
+      st = cuda_status(cudaMemcpy(at(off_cl[ci]), cp.wlast.data(),
+                                  cp.wlast.size() * sizeof(float), cudaMemcpyHostToDevice));
     for (int i = 0; i < 3 && st == DLRM_OK; ++i) {
-      if (!cplan.fits[i]) continue;
-      dlrm::ClusterParams& q = h->cparams[i];
-      q = cplan.params[i];
-      q.wstream = at(off_cw);
-      q.stage_tab = reinterpret_cast<const uint2*>(at(off_ct));
-      q.bias = at(off_cb);
-      q.wlast = at(off_cl);
-      h->cmax[i] = dlrm::fused_cluster_max_active(q.bm, q.csize, q.smem_bytes);
-      limit = std::max(limit, h->cmax[i] * q.bm);
+      if (!cp.fits[i]) continue;
+      dlrm::ClusterParams& q = h->cparams[ci][i];
+      q = cp.params[i];
+      q.wstream = at(off_cw[ci]);
+      q.stage_tab = reinterpret_cast<const uint2*>(at(off_ct[ci]));
+      q.bias = at(off_cb[ci]);
+      q.wlast = at(off_cl[ci]);
+      h->cmax[ci][i] = dlrm::fused_cluster_max_active(q.bm, q.csize, q.smem_bytes);
+      cluster_limit = std::max(cluster_limit, h->cmax[ci][i] * q.bm);
     }
-    h->cluster_default = std::min(limit, cluster_max_batch(h->k));
-    h->cluster_limit = h->cluster_default;
-    h->cluster_on = h->cluster_limit > 0;
   }
+  h->cluster_default = std::min(cluster_limit, cluster_max_batch(h->k));
+  h->cluster_limit = h->cluster_default;
+  h->cluster_on = h->cluster_limit > 0;
   if (st == DLRM_OK) st = cuda_status(cudaDeviceSynchronize());
   if (st != DLRM_OK) {
     cudaGetLastError();

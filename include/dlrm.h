@@ -228,19 +228,20 @@ dlrm_status_t dlrm_get_error(dlrm_handle_t h, void* stream);
 dlrm_status_t dlrm_test_stall(dlrm_handle_t h, int64_t wait_limit_ns, int32_t withhold_last);
 
 /* Small batches of the fp32 fused plan of a model with 1 MiB or more of
- * packed MLP weights run on a second kernel: each layer's
- * output columns split over the 8 CTAs of a thread-block cluster, every CTA
- * streaming only its share of the weights and the layer's outputs exchanged
- * through distributed shared memory. A forward of at most `limit` samples
- * takes that kernel, a larger one the persistent single-CTA-per-tile kernel
- * (and so does every forward while a phase-trace buffer is set).
- * dlrm_set_cluster_batch_limit sets the limit: 0 turns the cluster kernel
- * off, -1 restores the default (the samples one wave of clusters holds at
- * the tallest tile that fits, at most 64, or 128 with 16 or more tables). UNSUPPORTED when the handle has
- * no cluster plan (layer-wise or tensor-core plans, or a model the kernel
- * does not take) and limit > 0; INVALID_ARG for a null handle or
- * limit < -1. dlrm_get_cluster_batch_limit reads the current limit (0 when
- * there is no cluster plan). */
+ * packed MLP weights run on a second kernel: each layer's output columns
+ * split over the CTAs of a thread-block cluster (8 CTAs up to 32 samples, 4
+ * above), every CTA streaming only its share of the weights and the layer's
+ * outputs exchanged through distributed shared memory. A forward of at most
+ * `limit` samples takes that kernel, a larger one the persistent
+ * single-CTA-per-tile kernel (and so does every forward while a phase-trace
+ * buffer is set). dlrm_set_cluster_batch_limit sets the limit: 0 turns the
+ * cluster kernel off, -1 restores the default (the samples one wave of
+ * clusters holds at the tallest tile that fits, at most 128, or 256 with 16
+ * or more tables). UNSUPPORTED when the handle has no cluster plan
+ * (layer-wise or tensor-core plans, or a model the kernel does not take) and
+ * limit > 0; INVALID_ARG for a null handle or limit < -1.
+ * dlrm_get_cluster_batch_limit reads the current limit (0 when there is no
+ * cluster plan). */
 dlrm_status_t dlrm_set_cluster_batch_limit(dlrm_handle_t h, int32_t limit);
 dlrm_status_t dlrm_get_cluster_batch_limit(dlrm_handle_t h, int32_t* limit);
 

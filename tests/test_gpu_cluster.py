@@ -1,8 +1,9 @@
 """The cluster-split fused forward (small batches of the fp32 fused plan)
 against the CPU oracle.
 
-Each layer's output columns are split over the 8 CTAs of a cluster and the
-outputs exchanged through distributed shared memory; the interaction and the
+Each layer's output columns are split over the CTAs of a cluster (8 up to
+32 samples, 4 above) and the outputs exchanged through distributed shared
+memory; the interaction and the
 sigmoid layer are split by samples. The cases cover every tile height (4, 8
 and 16 samples), partial tiles, one and several waves of clusters, column
 slices from 4 to 512 wide (layers of 16 to 1024 outputs), padded input
@@ -63,7 +64,7 @@ def test_default_limit_and_switch():
     inp = synth.make_inputs(cfg, seed=5)
     model = make_model(cfg, inp)
     default = model.cluster_batch_limit
-    assert default == 64                             # 3 tables
+    assert default == 128                            # 3 tables
     model.cluster_batch_limit = 0
     assert model.cluster_batch_limit == 0
     a, st = forward(model, inp, cfg.batch)           # the persistent kernel
@@ -98,14 +99,12 @@ SWEEP = [(b, k) for k in (1, 3, 8, 16, 32) for b in (1, 3, 8, 29, 64, 128)]
 
 @pytest.mark.parametrize("b,k", SWEEP, ids=[f"b{b}_k{k}" for b, k in SWEEP])
 def test_sweep_cells_match_oracle(b, k):
-    """The sweep's small cells (bottom 13-512-256-64, top 512-256-1), all on
-    the cluster kernel (the default limit is 64 samples, 128 with 16 or more
-    tables)."""
+    """The sweep's small cells (bottom 13-512-256-64, top 512-256-1) at the
+    default limit: clusters of 8 CTAs up to 32 samples, of 4 above."""
     cfg = synth.sweep_config(b, k)
     inp = synth.make_inputs(cfg, seed=100 + b + k)
     model = make_model(cfg, inp)
-    assert model.cluster_batch_limit == (128 if k >= 16 else 64)
-    model.cluster_batch_limit = 128                  # every cell on the cluster kernel
+    assert model.cluster_batch_limit == (256 if k >= 16 else 128)
     out, st = forward(model, inp, b)
     assert st == dl.OK
     close(out.cpu().numpy(), oracle.forward(inp))
@@ -114,9 +113,9 @@ def test_sweep_cells_match_oracle(b, k):
 
 @pytest.mark.parametrize("batch", [1, 4, 5, 17, 33, 61, 100, 255, 700])
 def test_tile_heights_and_waves(batch):
-    """With the limit raised every batch takes the cluster kernel: tiles of
-    4, 8 and 16 samples, partial last tiles, and more tiles than one wave of
-    clusters holds (255 and 700 samples)."""
+    """With the limit raised every batch takes the cluster kernel: clusters of
+    8 and of 4 CTAs, tiles of 4, 8 and 16 samples, partial last tiles, and
+    more tiles than one wave of clusters holds (700 samples)."""
     cfg = synth.sweep_config(batch, 3)
     inp = synth.make_inputs(cfg, seed=batch)
     model = make_model(cfg, inp, max_batch=1024)
