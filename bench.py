@@ -512,8 +512,11 @@ def run_ours(args, rank, world, local_rank):
     out = torch.empty(cfg.batch, device=dev)
     flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
-    n_stages = len(model.stage_names())
-    path_used = model.path
+    # the kernels the timed forward runs (an AUTO fp32 handle on the fused plan
+    # takes the layer-wise plan from its crossover batch)
+    kind = model.kernels(cfg.batch)
+    path_used = dl.PATH_LAYERWISE if kind == dl.KERNELS_LAYERWISE else dl.PATH_FUSED
+    n_stages = (len(cfg.ln_bot) + len(cfg.ln_top)) if path_used == dl.PATH_LAYERWISE else 1
 
     def barrier():
         if dist is not None:
@@ -767,7 +770,9 @@ def run_ours(args, rank, world, local_rank):
         y_ = torch.empty(c.batch, device=dev)
         ms_c, _ = timed(lambda: m.forward(d_, i_, o_, y_, stream=stream), steps, warmup)
         ok = m.error(stream) == dl.OK
-        plan = "fused" if m.path == dl.PATH_FUSED else "layer-wise"
+        plan = {dl.KERNELS_LAYERWISE: "layer-wise", dl.KERNELS_FUSED: "fused",
+                dl.KERNELS_FUSED_CLUSTER: "fused, cluster-split",
+                dl.KERNELS_FUSED_TC: "fused, tensor cores"}[m.kernels(c.batch)]
         m.close()
         if not ok:
             raise RuntimeError(f"device error in the {c.name} forward")

@@ -31,7 +31,8 @@ EXPORTS = ("dlrm_version", "dlrm_status_string", "dlrm_create", "dlrm_forward",
            "embedding_bag_sum_multi", "embedding_bag_multi", "embedding_bag_multi_ex",
            "pairwise_dot_lower_tri",
            "pairwise_pair_map", "linear_bias_act", "dlrm_test_stall",
-           "dlrm_set_cluster_batch_limit", "dlrm_get_cluster_batch_limit")
+           "dlrm_set_cluster_batch_limit", "dlrm_get_cluster_batch_limit",
+           "dlrm_forward_kernels")
 NOALLOC_SCRATCH_BYTES = 16 << 20
 TRACE_SLOTS = 40
 
@@ -64,7 +65,8 @@ class _PlanInfo(ctypes.Structure):
                 ("tiles", ctypes.c_int64), ("grid", ctypes.c_int32),
                 ("smem_bytes", ctypes.c_int32), ("ring_stages", ctypes.c_int32),
                 ("stream_copies", ctypes.c_int32), ("stream_bytes", ctypes.c_int64),
-                ("tensor_core_layers", ctypes.c_int32), ("split_tf32", ctypes.c_int32)]
+                ("tensor_core_layers", ctypes.c_int32), ("split_tf32", ctypes.c_int32),
+                ("layerwise_from", ctypes.c_int64)]
 
 
 def _bind(lib):
@@ -79,6 +81,7 @@ def _bind(lib):
         "dlrm_get_error": ([vp, vp], st),
         "dlrm_test_stall": ([vp, i64, i32], st),
         "dlrm_set_cluster_batch_limit": ([vp, i32], st),
+        "dlrm_forward_kernels": ([vp, i32], i32),
         "dlrm_get_cluster_batch_limit": ([vp, vp], st),
         "dlrm_workspace_bytes": ([vp], i64),
         "dlrm_destroy": ([vp], None),
@@ -515,6 +518,18 @@ def dlrm_test_stall(h: int, wait_limit_ns: int = 0, withhold_last: bool = False)
            "dlrm_test_stall")
 
 
+KERNELS_LAYERWISE, KERNELS_FUSED, KERNELS_FUSED_CLUSTER, KERNELS_FUSED_TC = 1, 2, 3, 4
+
+
+def dlrm_forward_kernels(h: int, batch: int) -> int:
+    """Which kernels a forward of ``batch`` samples on ``h`` runs (KERNELS_*)."""
+    _handle_shape(h, "dlrm_forward_kernels")
+    r = int(lib().dlrm_forward_kernels(ctypes.c_void_p(h), int(batch)))
+    if r < 0:
+        raise ValueError(f"dlrm_forward_kernels: batch {batch} outside [1, max_batch]")
+    return r
+
+
 def dlrm_set_cluster_batch_limit(h: int, limit: int) -> None:
     """Forwards of at most ``limit`` samples on ``h`` take the cluster-split
     fused kernel (0: never; -1: the default)."""
@@ -603,6 +618,10 @@ class DlrmModel:
 
     def stage_names(self):
         return [dlrm_stage_name(self.handle, i) for i in range(dlrm_num_stages(self.handle))]
+
+    def kernels(self, batch: int) -> int:
+        """Which kernels a forward of ``batch`` samples runs (KERNELS_*)."""
+        return dlrm_forward_kernels(self.handle, batch)
 
     @property
     def cluster_batch_limit(self) -> int:

@@ -8,6 +8,7 @@
 // memory of a handle is one arena allocated in dlrm_create; forward calls
 // allocate nothing and never synchronise.
 #include <algorithm>
+#include <cmath>
 #include <atomic>
 #include <cstdio>
 #include <cstdlib>
@@ -105,6 +106,9 @@ struct dlrm_handle_s {
   int cmax[2][3] = {{0, 0, 0}, {0, 0, 0}};
   int cluster_limit = 0;              // batches up to this run on the cluster kernel
   int cluster_default = 0;
+  // AUTO fp32 fused handles: forwards of at least this many samples take the
+  // layer-wise plan with split-TF32 GEMMs (0: never)
+  int64_t layerwise_from = 0;
   unsigned long long* trace = nullptr;
   dlrm::WaitCfg wait{};          // dlrm_test_stall: wait limit, withheld last copy
   // layer-wise TF32 / TF32X3: per layer (bottom, then top), the TMA plan of
@@ -178,6 +182,17 @@ bool staged_tc_layer(int math, int n, int k) {
   return math == DLRM_MATH_TF32X3 && k >= 64;
 }
 
+// The kernels one forward of `batch` samples runs (dlrm_forward_kernels).
+// Per-stage timing and the phase trace keep the handle's own plan and kernel.
+int forward_kind(const dlrm_handle_s* h, int batch) {
+  if (h->path != DLRM_PATH_FUSED) return DLRM_KERNELS_LAYERWISE;
+  const bool plain = h->events.empty() && !h->trace;
+  if (h->layerwise_from > 0 && batch >= h->layerwise_from && plain) return DLRM_KERNELS_LAYERWISE;
+  if (h->fused_tc) return DLRM_KERNELS_FUSED_TC;
+  if (h->cluster_on && batch <= h->cluster_limit && !h->trace) return DLRM_KERNELS_FUSED_CLUSTER;
+  return DLRM_KERNELS_FUSED;
+}
+
 dlrm_status_t run_forward(dlrm_handle_t h, const float* dense, const int64_t* indices,
                           const int64_t* offsets, float* out, int batch, cudaStream_t s) {
   cudaError_t e;
@@ -187,7 +202,8 @@ dlrm_status_t run_forward(dlrm_handle_t h, const float* dense, const int64_t* in
     return !prof || cudaEventRecord(h->events[stage++], s) == cudaSuccess;
   };
   if (!mark()) return DLRM_ERR_CUDA;
-  if (h->path == DLRM_PATH_FUSED) {
+  const int kind = forward_kind(h, batch);
+  if (kind != DLRM_KERNELS_LAYERWISE) {
     // the whole forward in one launch
     dlrm::FusedParams p = h->fused;
     p.batch = batch;
@@ -198,7 +214,7 @@ dlrm_status_t run_forward(dlrm_handle_t h, const float* dense, const int64_t* in
     p.err = h->err;
     p.trace = h->trace;
     p.wait = h->wait;
-    if (h->fused_tc) {
+    if (kind == DLRM_KERNELS_FUSED_TC) {
       dlrm::FusedTcParams q = h->tcp;
       q.batch = batch;
       q.dense = dense;
@@ -209,7 +225,7 @@ dlrm_status_t run_forward(dlrm_handle_t h, const float* dense, const int64_t* in
       q.trace = h->trace;
       q.wait = h->wait;
       e = dlrm::launch_fused_tc(q, s);
-    } else if (h->cluster_on && batch <= h->cluster_limit && !h->trace) {
+    } else if (kind == DLRM_KERNELS_FUSED_CLUSTER) {
       // clusters of 8 for the smallest batches, else of 4 (when planned);
       // then the smallest tile height whose tiles fit one wave of clusters,
       // else the tallest available
@@ -366,12 +382,40 @@ bool wants_fused_plan(const dlrm_config_t* cfg) {
   return cfg->path != DLRM_PATH_LAYERWISE && (fp32_math(cfg->math) || tensor_core_math(cfg->math));
 }
 
+// The batch from which the layer-wise plan, its large GEMMs as split-TF32
+// on the tensor cores, beats the fp32 fused kernel. A cost model fitted to
+// the 13-512-256-64 / (64 + P)-512-256-1 models with 1 to 32 tables at 2048
+// to 16384 samples (fused against layer-wise, L2 flushed): the fused kernel
+// takes ~3.13e-8 us per MLP flop plus ~2.04e-7 us per pair-dot flop of a
+// sample; the layer-wise launches ~78 us plus 0.44 of that per sample. The
+// crossover then falls near 6900 samples with 3 tables, 5100 with 16 and
+// 2800 with 32 (measured: between 6144 and 8192, near 6144, between 2048
+// and 4096). Zero when no layer runs split-TF32.
+int64_t layerwise_crossover(const dlrm_config_t* cfg) {
+  double mlp = 0.0;
+  bool split_layer = false;
+  for (int g = 0; g < cfg->n_bot + cfg->n_top; ++g) {
+    const bool top = g >= cfg->n_bot;
+    const int l = top ? g - cfg->n_bot : g;
+    const int n = top ? cfg->ln_top[l + 1] : cfg->ln_bot[l + 1];
+    const int k = top ? cfg->ln_top[l] : cfg->ln_bot[l];
+    mlp += 2.0 * n * k;
+    split_layer = split_layer || tma_layer(DLRM_MATH_FP32, g, n, k);
+  }
+  if (!split_layer) return 0;
+  const double f = cfg->n_tables + 1.0;
+  const double pair_flops = f * (f - 1.0) * cfg->emb_dim;
+  const double per_sample_us = 3.13e-8 * mlp + 2.04e-7 * pair_flops;
+  return static_cast<int64_t>(std::ceil(78.0 / (0.56 * per_sample_us)));
+}
+
 struct PlanChoice {
   int path = DLRM_PATH_LAYERWISE;
   bool fused_fits = false;
   bool fused_tc = false;    // the fused plan runs on the tensor cores
   int fused_bm = 0;         // samples per fused tile
   int64_t tiles = 0;        // fused tiles of max_batch
+  int64_t layerwise_from = 0;   // AUTO fp32 fused plan: the layer-wise plan from this batch
 };
 
 // The kernel plan of a checked config, from host copies of the weights and
@@ -414,6 +458,11 @@ dlrm_status_t choose_plan(const dlrm_config_t* cfg, const std::vector<std::vecto
     c->path = (c->fused_fits && (persistent || c->tiles <= 2 * static_cast<int64_t>(sms)))
                   ? DLRM_PATH_FUSED
                   : DLRM_PATH_LAYERWISE;
+    // large batches of the fp32 fused plan: the layer-wise split-TF32 plan
+    if (c->path == DLRM_PATH_FUSED && cfg->math == DLRM_MATH_FP32) {
+      const int64_t from = layerwise_crossover(cfg);
+      if (from > 0 && cfg->max_batch >= from) c->layerwise_from = from;
+    }
   } else {
     c->path = DLRM_PATH_LAYERWISE;
   }
@@ -498,6 +547,7 @@ dlrm_status_t dlrm_create(const dlrm_config_t* cfg, const float* const* tables,
   h->path = choice.path;
   h->fused_tc = choice.fused_tc;
   h->fused_bm = choice.fused_bm;
+  h->layerwise_from = choice.layerwise_from;
   if (h->path == DLRM_PATH_FUSED) {
     h->stage_names.push_back("fused");
   } else {
@@ -541,7 +591,7 @@ dlrm_status_t dlrm_create(const dlrm_config_t* cfg, const float* const* tables,
   // Layer-wise plan: the warp-specialized TMA GEMM for the layers tma_layer
   // picks; in split-TF32 (FP32, TF32X3) their weights get two more copies:
   // their tf32 head and the remainder.
-  const bool tma_math = h->path == DLRM_PATH_LAYERWISE &&
+  const bool tma_math = (h->path == DLRM_PATH_LAYERWISE || h->layerwise_from > 0) &&
                         (h->math == DLRM_MATH_TF32 || split_tf32_math(h->math));
   const bool split = split_tf32_math(h->math);
   const int n_layers = h->n_bot + h->n_top;
@@ -812,7 +862,8 @@ dlrm_status_t dlrm_plan_query(const dlrm_config_t* cfg, int32_t sm_count, int64_
     r.stream_bytes = tc ? static_cast<int64_t>(tplan.wstream.size())
                         : static_cast<int64_t>(fplan.wstream.size() * sizeof(float));
   }
-  if (c.path == DLRM_PATH_LAYERWISE) {
+  r.layerwise_from = c.layerwise_from;
+  if (c.path == DLRM_PATH_LAYERWISE || c.layerwise_from > 0) {
     for (int g = 0; g < cfg->n_bot + cfg->n_top; ++g) {
       const bool top = g >= cfg->n_bot;
       const int l = top ? g - cfg->n_bot : g;
@@ -910,6 +961,11 @@ dlrm_status_t dlrm_test_stall(dlrm_handle_t h, int64_t wait_limit_ns, int32_t wi
   h->wait.limit_ns = static_cast<uint64_t>(wait_limit_ns);
   h->wait.withhold_last = withhold_last ? 1 : 0;
   return DLRM_OK;
+}
+
+int32_t dlrm_forward_kernels(dlrm_handle_t h, int32_t batch) {
+  if (!h || batch < 1 || batch > h->max_batch) return -1;
+  return forward_kind(h, batch);
 }
 
 dlrm_status_t dlrm_set_cluster_batch_limit(dlrm_handle_t h, int32_t limit) {

@@ -177,6 +177,10 @@ typedef struct {
                                   tcgen05 tensor cores; 0 for a fused plan */
   int32_t split_tf32;      /* 1: those layers compute split-TF32 (three tf32
                               products per fp32 product) */
+  int64_t layerwise_from;  /* AUTO plan of fp32 math taking the fused kernel:
+                              forwards of at least this many samples run the
+                              layer-wise plan instead (its large GEMMs as
+                              split-TF32 on the tensor cores); 0: never */
 } dlrm_plan_info_t;
 
 dlrm_status_t dlrm_plan_query(const dlrm_config_t* cfg, int32_t sm_count,
@@ -226,6 +230,19 @@ dlrm_status_t dlrm_get_error(dlrm_handle_t h, void* stream);
  * of such a forward are undefined. dlrm_test_stall(h, 0, 0) restores normal
  * operation. INVALID_ARG for a null handle or a negative limit. */
 dlrm_status_t dlrm_test_stall(dlrm_handle_t h, int64_t wait_limit_ns, int32_t withhold_last);
+
+/* The kernels one forward of `batch` samples on h runs: */
+#define DLRM_KERNELS_LAYERWISE 1      /* one launch per step */
+#define DLRM_KERNELS_FUSED 2          /* the fused kernel, one CTA per tile */
+#define DLRM_KERNELS_FUSED_CLUSTER 3  /* the fused kernel on thread-block clusters */
+#define DLRM_KERNELS_FUSED_TC 4       /* the fused tensor-core kernel (TF32 / BF16) */
+/* -1 for a null handle or a batch outside [1, max_batch]. An AUTO handle of
+ * fp32 math on the fused plan runs the layer-wise plan from
+ * dlrm_plan_info_t.layerwise_from samples (large batches: split-TF32 GEMMs
+ * on the tensor cores beat the FFMA kernel), the cluster kernel up to the
+ * cluster batch limit below, the one-CTA-per-tile kernel between. While
+ * per-stage timing or a phase trace is on, a handle keeps its own plan. */
+int32_t dlrm_forward_kernels(dlrm_handle_t h, int32_t batch);
 
 /* Small batches of the fp32 fused plan of a model with 1 MiB or more of
  * packed MLP weights run on a second kernel: each layer's output columns

@@ -265,6 +265,35 @@ def test_forward_ffma_layerwise_matches_oracle(name):
     model.close()
 
 
+def test_auto_handle_picks_kernels_by_batch():
+    """One AUTO fp32 handle of the 512-wide model at max_batch 8192: the
+    cluster kernel for 32 samples, the one-CTA-per-tile fused kernel for
+    2048, the layer-wise split-TF32 plan for 8192 (from its crossover); each
+    forward matches the oracle."""
+    cfg = synth.sweep_config(8192, 3)
+    inp = synth.make_inputs(cfg, seed=77)
+    model = make_model(cfg, inp)
+    assert model.path == dl.PATH_FUSED
+    q = dl.dlrm_plan_query(cfg.ln_bot, cfg.ln_top, cfg.rows, cfg.emb_dim, 1, cfg.batch)
+    assert 0 < q["layerwise_from"] <= cfg.batch
+    want = {32: dl.KERNELS_FUSED_CLUSTER, 2048: dl.KERNELS_FUSED,
+            q["layerwise_from"]: dl.KERNELS_LAYERWISE, 8192: dl.KERNELS_LAYERWISE}
+    for b, kind in want.items():
+        assert model.kernels(b) == kind, b
+    assert model.kernels(q["layerwise_from"] - 1) == dl.KERNELS_FUSED
+    for b in (32, 2048, 8192):
+        sub = synth.make_inputs(cfg.with_batch(b), seed=77)
+        out = run_forward(model, sub)
+        ids = np.unique(np.concatenate([[0, b - 1], np.random.default_rng(b).integers(0, b, 40)]))
+        close(out[ids], oracle.forward(sub, sample_ids=ids))
+    model.set_profiling(True)           # per-stage timing keeps the handle's fused plan
+    assert model.kernels(8192) == dl.KERNELS_FUSED
+    model.set_profiling(False)
+    with pytest.raises(ValueError):
+        model.kernels(8193)
+    model.close()
+
+
 @pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
 def test_forward_odd_widths_matches_oracle(path):
     """Layers wider than 512 (two column passes), and 128-, 100- and 32-wide

@@ -151,10 +151,32 @@ def test_layerwise_tensor_core_layers():
 
 
 def test_ffma_mode_plans_like_fp32_when_fused():
-    """FP32_FFMA takes the same fused plan as FP32 (the fused kernel is FFMA)."""
+    """FP32_FFMA takes the same fused plan as FP32 (the fused kernel is FFMA),
+    but never the layer-wise split-TF32 plan at large batches."""
+    switch = ("layerwise_from", "tensor_core_layers", "split_tf32")
     for name in ("b2048_k3", "tiny_b64_k3", "sweep_b8192_k16"):
         cfg = synth.get_config(name)
-        assert query(cfg, dl.MATH_FP32_FFMA) == query(cfg, dl.MATH_FP32)
+        a, b = query(cfg, dl.MATH_FP32_FFMA), query(cfg, dl.MATH_FP32)
+        assert {k: v for k, v in a.items() if k not in switch} == \
+            {k: v for k, v in b.items() if k not in switch}
+        assert a["layerwise_from"] == 0
+
+
+@pytest.mark.parametrize("k,lo,hi", [(3, 6144, 8192), (16, 4096, 6144), (32, 2048, 4096)])
+def test_large_batches_switch_to_the_split_tf32_plan(k, lo, hi):
+    """AUTO fp32 on the fused plan runs the layer-wise split-TF32 plan from a
+    batch inside the measured crossover (the fused kernel was faster at `lo`
+    samples, the layer-wise plan at `hi`); a handle whose max_batch is below
+    it never switches, nor an explicit FUSED path or FFMA math."""
+    cfg = synth.sweep_config(16384, k)
+    p = query(cfg)
+    assert p["path"] == dl.PATH_FUSED
+    assert lo < p["layerwise_from"] <= hi
+    assert p["tensor_core_layers"] != 0 and p["split_tf32"] == 1
+    assert query(cfg, batch=lo)["layerwise_from"] == 0
+    assert query(cfg, path=dl.PATH_FUSED)["layerwise_from"] == 0
+    assert query(cfg, dl.MATH_FP32_FFMA)["layerwise_from"] == 0
+    assert query(synth.get_config("tiny_b64_k3"), batch=65536)["layerwise_from"] == 0
 
 
 @pytest.mark.parametrize("math", [dl.MATH_FP32, dl.MATH_TF32, dl.MATH_BF16])
