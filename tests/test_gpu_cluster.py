@@ -65,8 +65,10 @@ def test_default_limit_and_switch():
     model = make_model(cfg, inp)
     default = model.cluster_batch_limit
     assert default == 128                            # 3 tables
+    assert model.kernels(cfg.batch) == dl.KERNELS_FUSED_CLUSTER
     model.cluster_batch_limit = 0
     assert model.cluster_batch_limit == 0
+    assert model.kernels(cfg.batch) == dl.KERNELS_FUSED
     a, st = forward(model, inp, cfg.batch)           # the persistent kernel
     assert st == dl.OK
     model.cluster_batch_limit = -1
@@ -139,17 +141,18 @@ def test_odd_and_wide_layers():
     model.close()
 
 
-def test_long_bags():
+@pytest.mark.parametrize("batch", [20, 48])
+def test_long_bags(batch):
     """Bags of 20 rows (the 26-table model's shape, small tables): summed at
-    the interaction by the CTA that owns each sample."""
+    the interaction by the CTA that owns each sample (clusters of 8 CTAs at
+    20 samples, of 4 at 48)."""
     base = synth.get_config("b65536_k26_zipf")
-    cfg = synth.DlrmConfig("b48_k26_l20", 48, base.ln_bot, (5000,) * 26, base.emb_dim, 20,
-                           base.ln_top, index_dist="zipf", zipf_s=1.05)
+    cfg = synth.DlrmConfig(f"b{batch}_k26_l20", batch, base.ln_bot, (5000,) * 26, base.emb_dim,
+                           20, base.ln_top, index_dist="zipf", zipf_s=1.05)
     inp = synth.make_inputs(cfg, seed=12)
     model = make_model(cfg, inp)
     assert model.path == dl.PATH_FUSED
-    if model.cluster_batch_limit < cfg.batch:
-        pytest.skip("the model does not fit the cluster kernel")
+    assert model.kernels(cfg.batch) == dl.KERNELS_FUSED_CLUSTER
     out, st = forward(model, inp, cfg.batch)
     assert st == dl.OK
     close(out.cpu().numpy(), oracle.forward(inp))

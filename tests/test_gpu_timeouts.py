@@ -48,13 +48,15 @@ CASES = [
     # workload, math, path, tolerance (atol, rtol)
     ("b2048_k3", dl.MATH_FP32, dl.PATH_FUSED, (1e-5, 1e-4)),
     ("sweep_b8192_k3", dl.MATH_FP32, dl.PATH_FUSED, (1e-5, 1e-4)),   # several tiles per CTA
-    ("sweep_b64_k3", dl.MATH_FP32, dl.PATH_FUSED, (1e-5, 1e-4)),     # the cluster-split kernel
+    ("sweep_b64_k3", dl.MATH_FP32, dl.PATH_FUSED, (1e-5, 1e-4)),     # cluster kernel, 4 CTAs
+    ("sweep_b16_k3", dl.MATH_FP32, dl.PATH_FUSED, (1e-5, 1e-4)),     # cluster kernel, 8 CTAs
     ("b2048_k3", dl.MATH_BF16, dl.PATH_FUSED, (2e-2, 2e-2)),
     ("tiny_b64_k3", dl.MATH_TF32, dl.PATH_FUSED, (2e-2, 2e-2)),
     ("tiny_b64_k3", dl.MATH_TF32X3, dl.PATH_LAYERWISE, (1e-5, 1e-4)),
     ("b2048_k3", dl.MATH_BF16, dl.PATH_LAYERWISE, (2e-2, 2e-2)),
 ]
-IDS = ["fp32-fused", "fp32-fused-persistent", "fp32-fused-cluster", "bf16-fused", "tf32-fused", "tf32x3-layerwise",
+IDS = ["fp32-fused", "fp32-fused-persistent", "fp32-fused-cluster4", "fp32-fused-cluster8",
+       "bf16-fused", "tf32-fused", "tf32x3-layerwise",
        "bf16-layerwise"]
 
 
