@@ -14,7 +14,7 @@
 //    with cp.async.bulk.tensor (TMA, 128-byte swizzle: the canonical K-major
 //    layout the MMA descriptors read), completing on the stage's full
 //    mbarrier;
-//  * warps 2-3 (TF32X3): split the X tile in place into its tf32 head
+//  * warps 2-3 and 8-15 (TF32X3): split the X tile in place into its tf32 head
 //    (hi = x with the low 13 mantissa bits cleared, exact in tf32) and write
 //    the remainder lo = x - hi (exact in fp32) beside it; the weights arrive
 //    already split (head and remainder streams made at create time);
@@ -43,7 +43,8 @@ using namespace tc;
 
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;             // warps 8-15: more X split warps
+constexpr int kSplitWarps = 10;          // warps 2-3 and 8-15
 constexpr int kBM = 128;                 // rows of X per tile (the MMA M)
 constexpr int kBN = 128;                 // rows of W per tile (the MMA N)
 constexpr int kBK = 32;                  // k per block: 128 bytes of fp32
@@ -153,7 +154,7 @@ gemm_tma_kernel(const __grid_constant__ CUtensorMap tmap_x,
   if (threadIdx.x == kWarp) {
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_addr(&full[s]), 1);
-      mbar_init(smem_addr(&split_done[s]), 2);          // the two split warps
+      mbar_init(smem_addr(&split_done[s]), kSplitWarps);   // the split warps
       mbar_init(smem_addr(&empty[s]), 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -262,10 +263,10 @@ gemm_tma_kernel(const __grid_constant__ CUtensorMap tmap_x,
       mma_commit(smem_addr(drain));
       drain_wait(smem_addr(drain), 0, p.err, limit);
     }
-  } else if (warp < 4) {
+  } else if (warp < 4 || warp >= 8) {
     // ---------------------------------------------------------------- X split (TF32X3)
     if (SPLIT) {
-      const int st = threadIdx.x - 2 * kWarp;            // 0 .. 63
+      const int st = (warp < 4 ? warp - 2 : warp - 6) * kWarp + lane;   // 0 .. 191
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
@@ -277,7 +278,7 @@ gemm_tma_kernel(const __grid_constant__ CUtensorMap tmap_x,
           unsigned char* xs = x_tile(stage);
           unsigned char* xl = xlo_tile(stage);
 #pragma unroll 4
-          for (int off = st * 16; off < kTile; off += 64 * 16) {
+          for (int off = st * 16; off < kTile; off += kSplitWarps * kWarp * 16) {
             const uint4 v = *reinterpret_cast<const uint4*>(xs + off);
             uint4 hi, lo;
             hi.x = v.x & 0xFFFFE000u;
