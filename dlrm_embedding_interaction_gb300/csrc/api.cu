@@ -383,14 +383,15 @@ bool wants_fused_plan(const dlrm_config_t* cfg) {
 }
 
 // The batch from which the layer-wise plan, its large GEMMs as split-TF32
-// on the tensor cores, beats the fp32 fused kernel. A cost model fitted to
-// the 13-512-256-64 / (64 + P)-512-256-1 models with 1 to 32 tables at 2048
-// to 16384 samples (fused against layer-wise, L2 flushed): the fused kernel
-// takes ~3.13e-8 us per MLP flop plus ~2.04e-7 us per pair-dot flop of a
-// sample; the layer-wise launches ~78 us plus 0.44 of that per sample. The
-// crossover then falls near 6900 samples with 3 tables, 5100 with 16 and
-// 2800 with 32 (measured: between 6144 and 8192, near 6144, between 2048
-// and 4096). Zero when no layer runs split-TF32.
+// on the tensor cores and its launches overlapped (programmatic dependent
+// launch), beats the fp32 fused kernel. A cost model fitted to the
+// 13-512-256-64 / (64 + P)-512-256-1 models with 1 to 32 tables at 2048 to
+// 8192 samples (fused against layer-wise, L2 flushed): the fused kernel takes
+// ~3.13e-8 us per MLP flop plus ~2.04e-7 us per pair-dot flop of a sample;
+// the layer-wise launches ~75 us plus a third of that per sample. The
+// crossover then falls near 5600 samples with 3 tables, 4100 with 16 and 2200
+// with 32 (measured: between 4096 and 8192, near 4400, near 2500). Zero when
+// no layer runs split-TF32.
 int64_t layerwise_crossover(const dlrm_config_t* cfg) {
   double mlp = 0.0;
   bool split_layer = false;
@@ -406,7 +407,7 @@ int64_t layerwise_crossover(const dlrm_config_t* cfg) {
   const double f = cfg->n_tables + 1.0;
   const double pair_flops = f * (f - 1.0) * cfg->emb_dim;
   const double per_sample_us = 3.13e-8 * mlp + 2.04e-7 * pair_flops;
-  return static_cast<int64_t>(std::ceil(78.0 / (0.56 * per_sample_us)));
+  return static_cast<int64_t>(std::ceil(75.0 / (0.67 * per_sample_us)));
 }
 
 struct PlanChoice {

@@ -17,6 +17,33 @@ __host__ __device__ __forceinline__ int64_t round_up(int64_t x, int64_t m) {
   return (x + m - 1) / m * m;
 }
 
+// Programmatic dependent launch. A kernel launched by launch_pdl may start
+// while the kernel before it in the stream is still running: it must call
+// pdl_wait() before its first global-memory access (the wait returns once
+// the previous kernel has completed and its writes are visible; at once when
+// there is none), then pdl_trigger() lets the next kernel start its own
+// set-up early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 __device__ __forceinline__ float apply_act(float a, int act) {
   if (act == DLRM_ACT_RELU) return fmaxf(a, 0.0f);
   if (act == DLRM_ACT_SIGMOID) return 1.0f / (1.0f + expf(-a));

@@ -93,6 +93,9 @@ gather_vec_kernel(const __grid_constant__ GatherTables tabs, int k_tables, int d
                   const IDX* __restrict__ indices, const IDX* __restrict__ offsets,
                   const float* __restrict__ psw, int64_t padding, int batch, int bag,
                   int64_t n_idx, float* __restrict__ out, int32_t* err) {
+  pdl_wait();     // launched after the previous kernel may still run
+  pdl_trigger();
+
   constexpr bool kWeighted = MODE == kBagWeightedSum;
   const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t bag_id = gtid / TPB;
@@ -198,6 +201,9 @@ gather_scalar_kernel(const __grid_constant__ GatherTables tabs, int k_tables, in
                      const IDX* __restrict__ indices, const IDX* __restrict__ offsets,
                      const float* __restrict__ psw, int64_t padding, int batch, int bag,
                      int64_t n_idx, float* __restrict__ out, int32_t* err) {
+  pdl_wait();     // launched after the previous kernel may still run
+  pdl_trigger();
+
   const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t bag_id = gtid / kWarp;
   const int lane = threadIdx.x & (kWarp - 1);
@@ -249,10 +255,9 @@ cudaError_t launch_vec(const GatherTables& tabs, int k, int d, const IDX* indice
   const int64_t bags = static_cast<int64_t>(b) * k;
   const int64_t per_block = kGatherThreads / TPB;
   const int64_t grid = (bags + per_block - 1) / per_block;
-  gather_vec_kernel<TPB, CHUNKS, MODE, GENERAL, IDX>
-      <<<static_cast<unsigned>(grid), kGatherThreads, 0, stream>>>(
-          tabs, k, d / 4, indices, offsets, psw, padding, b, l, n_idx, out, err);
-  return cudaGetLastError();
+  return launch_pdl(gather_vec_kernel<TPB, CHUNKS, MODE, GENERAL, IDX>,
+                    dim3(static_cast<unsigned>(grid)), dim3(kGatherThreads), 0, stream, tabs, k,
+                    d / 4, indices, offsets, psw, padding, b, l, n_idx, out, err);
 }
 
 // Lane-group width and columns per lane by D, vector or scalar path.
@@ -283,10 +288,9 @@ cudaError_t launch_any(const GatherTables& tabs, int k, int d, const IDX* indice
   const int64_t bags = static_cast<int64_t>(b) * k;
   const int64_t per_block = kGatherThreads / kWarp;
   const int64_t grid = (bags + per_block - 1) / per_block;
-  gather_scalar_kernel<MODE, GENERAL, IDX><<<static_cast<unsigned>(grid), kGatherThreads, 0,
-                                             stream>>>(tabs, k, d, indices, offsets, psw, padding,
-                                                       b, l, n_idx, out, err);
-  return cudaGetLastError();
+  return launch_pdl(gather_scalar_kernel<MODE, GENERAL, IDX>, dim3(static_cast<unsigned>(grid)),
+                    dim3(kGatherThreads), 0, stream, tabs, k, d, indices, offsets, psw, padding, b,
+                    l, n_idx, out, err);
 }
 
 template <typename IDX>

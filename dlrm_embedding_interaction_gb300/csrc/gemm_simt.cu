@@ -93,6 +93,9 @@ __global__ void __launch_bounds__((BM / TM) * (BN / TN))
 sgemm_bias_act_kernel(const float* __restrict__ x, int ldx, const float* __restrict__ w, int ldw,
                       const float* __restrict__ bias, float* __restrict__ y, int ldy, int m,
                       int n, int k, int vec_y) {
+  pdl_wait();     // launched after the previous kernel may still run
+  pdl_trigger();
+
   constexpr int kThreads = (BM / TM) * (BN / TN);
   constexpr int kLdA = BM + 4;
   constexpr int kLdB = BN + 4;
@@ -203,6 +206,9 @@ __global__ void __launch_bounds__(kLmThreads, 2)
 sgemm_large_m_kernel(const float* __restrict__ x, int ldx, const float* __restrict__ w, int ldw,
                      const float* __restrict__ bias, float* __restrict__ y, int ldy, int m, int n,
                      int k) {
+  pdl_wait();     // launched after the previous kernel may still run
+  pdl_trigger();
+
   extern __shared__ __align__(16) float lm_smem[];
   const int tid = threadIdx.x;
   const int warp = tid / kWarp;
@@ -302,6 +308,9 @@ __global__ void __launch_bounds__(256)
 gemv_rows_kernel(const float* __restrict__ x, int ldx, const float* __restrict__ w, int ldw,
                  const float* __restrict__ bias, float* __restrict__ y, int ldy, int m, int n,
                  int k, int vec) {
+  pdl_wait();     // launched after the previous kernel may still run
+  pdl_trigger();
+
   const int row = blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp;
   const int lane = threadIdx.x & (kWarp - 1);
   if (row >= m) return;
@@ -339,17 +348,17 @@ cudaError_t launch_tile(const float* x, int ldx, const float* w, int ldw, const 
   constexpr int kThreads = (BM / TM) * (BN / TN);
   const dim3 grid((m + BM - 1) / BM, (n + BN - 1) / BN);
   if (va && vw)
-    sgemm_bias_act_kernel<BM, BN, TM, TN, ACT, true, true><<<grid, kThreads, 0, stream>>>(
-        x, ldx, w, ldw, bias, y, ldy, m, n, k, vy);
+    return launch_pdl(sgemm_bias_act_kernel<BM, BN, TM, TN, ACT, true, true>, grid, dim3(kThreads), 0,
+                      stream, x, ldx, w, ldw, bias, y, ldy, m, n, k, vy);
   else if (va)
-    sgemm_bias_act_kernel<BM, BN, TM, TN, ACT, true, false><<<grid, kThreads, 0, stream>>>(
-        x, ldx, w, ldw, bias, y, ldy, m, n, k, vy);
+    return launch_pdl(sgemm_bias_act_kernel<BM, BN, TM, TN, ACT, true, false>, grid, dim3(kThreads), 0,
+                      stream, x, ldx, w, ldw, bias, y, ldy, m, n, k, vy);
   else if (vw)
-    sgemm_bias_act_kernel<BM, BN, TM, TN, ACT, false, true><<<grid, kThreads, 0, stream>>>(
-        x, ldx, w, ldw, bias, y, ldy, m, n, k, vy);
+    return launch_pdl(sgemm_bias_act_kernel<BM, BN, TM, TN, ACT, false, true>, grid, dim3(kThreads), 0,
+                      stream, x, ldx, w, ldw, bias, y, ldy, m, n, k, vy);
   else
-    sgemm_bias_act_kernel<BM, BN, TM, TN, ACT, false, false><<<grid, kThreads, 0, stream>>>(
-        x, ldx, w, ldw, bias, y, ldy, m, n, k, vy);
+    return launch_pdl(sgemm_bias_act_kernel<BM, BN, TM, TN, ACT, false, false>, grid, dim3(kThreads), 0,
+                      stream, x, ldx, w, ldw, bias, y, ldy, m, n, k, vy);
   return cudaGetLastError();
 }
 
@@ -363,8 +372,8 @@ cudaError_t launch_act(const float* x, int ldx, const float* w, int ldw, const f
   if (n < 16) {
     const bool vec = va && vw;
     const unsigned grid = static_cast<unsigned>((m + 7) / 8);
-    gemv_rows_kernel<ACT><<<grid, 256, 0, stream>>>(x, ldx, w, ldw, bias, y, ldy, m, n, k, vec);
-    return cudaGetLastError();
+    return launch_pdl(gemv_rows_kernel<ACT>, dim3(grid), dim3(256), 0, stream, x, ldx, w, ldw, bias,
+                      y, ldy, m, n, k, vec);
   }
   const int64_t sms = device_sm_count();
   auto blocks = [&](int bm, int bn) {
@@ -384,9 +393,8 @@ cudaError_t launch_act(const float* x, int ldx, const float* w, int ldw, const f
       if (bit) done.fetch_or(bit, std::memory_order_acq_rel);
     }
     const dim3 grid((m + kLmBM - 1) / kLmBM, (n + kLmBN - 1) / kLmBN);
-    sgemm_large_m_kernel<ACT><<<grid, kLmThreads, kSmem, stream>>>(x, ldx, w, ldw, bias, y, ldy, m,
-                                                                  n, k);
-    return cudaGetLastError();
+    return launch_pdl(sgemm_large_m_kernel<ACT>, grid, dim3(kLmThreads), kSmem, stream, x, ldx, w,
+                      ldw, bias, y, ldy, m, n, k);
   }
   if (blocks(128, 128) >= sms)
     return launch_tile<128, 128, 8, 8, ACT>(x, ldx, w, ldw, bias, y, ldy, m, n, k, va, vw, vy, stream);

@@ -169,6 +169,11 @@ gemm_tma_kernel(const __grid_constant__ CUtensorMap tmap_x,
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tmem_slot;
+  // launched while the previous kernel may still run: its outputs (this
+  // layer's input) and its reads of this layer's output buffer are done
+  // after the wait
+  pdl_wait();
+  pdl_trigger();
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
@@ -445,11 +450,13 @@ cudaError_t launch_linear_tma(const TmaLayer& L, int m, const float* bias, float
   if (L.split) {
     e = prepare<true>();
     if (e != cudaSuccess) return e;
-    gemm_tma_kernel<true><<<grid, kThreads, Layout<true>::kSmem, stream>>>(*mx, *mw, *mwl, p);
+    return launch_pdl(gemm_tma_kernel<true>, dim3(grid), dim3(kThreads), Layout<true>::kSmem,
+                      stream, *mx, *mw, *mwl, p);
   } else {
     e = prepare<false>();
     if (e != cudaSuccess) return e;
-    gemm_tma_kernel<false><<<grid, kThreads, Layout<false>::kSmem, stream>>>(*mx, *mw, *mwl, p);
+    return launch_pdl(gemm_tma_kernel<false>, dim3(grid), dim3(kThreads), Layout<false>::kSmem,
+                      stream, *mx, *mw, *mwl, p);
   }
   return cudaGetLastError();
 }

@@ -44,6 +44,9 @@ __global__ void __launch_bounds__(kInteractThreads)
 interaction_kernel(const float* __restrict__ dense, int ld_dense, const float* __restrict__ emb,
                    int batch, int k_tables, int d, float* __restrict__ out, int ld_out,
                    int copy_dense, int samples_per_block, int use_blocks) {
+  pdl_wait();     // launched after the previous kernel may still run
+  pdl_trigger();
+
   extern __shared__ float4 smem_f4[];
   float* zs = reinterpret_cast<float*>(smem_f4);
   const int f = k_tables + 1;
@@ -283,14 +286,11 @@ cudaError_t launch_interaction(const float* dense, int ld_dense, const float* em
                         : enable_large_smem(interaction_kernel<false>, 1);
     if (e != cudaSuccess) return e;
   }
-  if (vec) {
-    interaction_kernel<true><<<grid, kInteractThreads, smem, stream>>>(
-        dense, ld_dense, emb, b, k, d, out, ld_out, copy_dense, s, mode);
-  } else {
-    interaction_kernel<false><<<grid, kInteractThreads, smem, stream>>>(
-        dense, ld_dense, emb, b, k, d, out, ld_out, copy_dense, s, 0);
-  }
-  return cudaGetLastError();
+  if (vec)
+    return launch_pdl(interaction_kernel<true>, dim3(grid), dim3(kInteractThreads), smem, stream,
+                      dense, ld_dense, emb, b, k, d, out, ld_out, copy_dense, s, mode);
+  return launch_pdl(interaction_kernel<false>, dim3(grid), dim3(kInteractThreads), smem, stream,
+                    dense, ld_dense, emb, b, k, d, out, ld_out, copy_dense, s, 0);
 }
 
 cudaError_t launch_pair_map(int f, int32_t* i_out, int32_t* j_out, cudaStream_t stream) {

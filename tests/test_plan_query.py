@@ -162,7 +162,7 @@ def test_ffma_mode_plans_like_fp32_when_fused():
         assert a["layerwise_from"] == 0
 
 
-@pytest.mark.parametrize("k,lo,hi", [(3, 6144, 8192), (16, 4096, 6144), (32, 2048, 4096)])
+@pytest.mark.parametrize("k,lo,hi", [(3, 4096, 6144), (16, 3072, 6144), (32, 2048, 4096)])
 def test_large_batches_switch_to_the_split_tf32_plan(k, lo, hi):
     """AUTO fp32 on the fused plan runs the layer-wise split-TF32 plan from a
     batch inside the measured crossover (the fused kernel was faster at `lo`
