@@ -23,8 +23,9 @@
 //    two TMEM accumulators of 128 columns, and releases the stage with
 //    tcgen05.commit to its empty barrier;
 //  * warps 4-7: read the finished accumulator (tcgen05.ld 32x32b, warp w
-//    the TMEM lanes 32 (w % 4) ...), add the bias, apply the activation and
-//    store, then release the accumulator to the next tile but one.
+//    the TMEM lanes 32 (w % 4) ...), release it to the next tile but one,
+//    add the bias, apply the activation and store through a shared-memory
+//    transpose, so that every store instruction writes 128 bytes of a row.
 // Every wait is bounded (WaitCfg); on expiry the kernel sets
 // DLRM_ERRBIT_TIMEOUT, every role leaves its loop, the loads and MMAs in
 // flight are waited for (bounded) and the tensor memory is freed.
@@ -58,8 +59,12 @@ struct Layout {
   static constexpr int kStage = kParts * kTile;
   static constexpr int kStages = SPLIT ? 3 : 6;
   static constexpr int kBars = 3 * kStages + 5;      // full, split, empty; acc full/empty x2; drain
-  static constexpr int kSmem = 1024 + kStages * kStage + kBars * 8 + 16;
+  // epilogue: per epilogue warp a 32 x 32 staging block (stride 33 floats)
+  static constexpr int kEpiFloats = 4 * 32 * 33;
+  static constexpr int kSmem = 1024 + kStages * kStage + kBars * 8 + 16 + kEpiFloats * 4;
 };
+static_assert(Layout<true>::kSmem <= 232448 && Layout<false>::kSmem <= 232448,
+              "shared memory of one CTA");
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -133,6 +138,7 @@ gemm_tma_kernel(const __grid_constant__ CUtensorMap tmap_x,
   uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* epi_s = reinterpret_cast<float*>(bars + Lay::kBars + 2);   // after the flag words
   // stage s: X at 0, [X lo at kTile,] W at (SPLIT ? 2 : 1) kTile, [W lo after it]
   auto x_tile = [&](int s) { return base + s * Lay::kStage; };
   auto xlo_tile = [&](int s) { return base + s * Lay::kStage + kTile; };
@@ -310,56 +316,64 @@ gemm_tma_kernel(const __grid_constant__ CUtensorMap tmap_x,
     }
   } else {
     // ---------------------------------------------------------------- epilogue
+    // Warp q reads TMEM lanes 32 q .. 32 q + 31 (the tile's rows) 32 columns
+    // at a time, stages the 32 x 32 block in shared memory and writes it back
+    // row by row: each store instruction writes 32 consecutive floats (128
+    // bytes) of one row.
     const int q = warp & 3;                              // TMEM lane quarter
+    float* blk = epi_s + q * 32 * 33;
     int i = 0;
     for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
       const int abuf = i & 1;
       const uint32_t aphase = (i >> 1) & 1;
+      const int mt = t / p.n_tiles, nt = t % p.n_tiles;
+      // the bias of the lane's column in each 32-column chunk, loaded while
+      // the accumulator is still being made
+      float bv[kBN / 32];
+#pragma unroll
+      for (int c = 0; c < kBN / 32; ++c) {
+        const int col = nt * kBN + 32 * c + lane;
+        bv[c] = (p.bias && col < p.n) ? __ldg(p.bias + col) : 0.f;
+      }
       if (!wait_for(smem_addr(&acc_full[abuf]), aphase, abort_flag, p.err, limit)) break;
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const int mt = t / p.n_tiles, nt = t % p.n_tiles;
-      const int row = mt * kBM + q * 32 + lane;
-      float* yrow = p.y + static_cast<int64_t>(row) * p.ldy;
-      for (int c0 = 0; c0 < kBN; c0 += 16) {
-        uint32_t r[16];
+      const int row0 = mt * kBM + q * 32;
+#pragma unroll
+      for (int c0 = 0; c0 < kBN; c0 += 32) {
+        uint32_t r[32];
         const uint32_t taddr =
             tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(abuf * kAccCols + c0);
         asm volatile(
-            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-            "%11, %12, %13, %14, %15}, [%16];"
+            "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+            "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, "
+            "%27, %28, %29, %30, %31}, [%32];"
             : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
               "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
-              "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+              "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]),
+              "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+              "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+              "=r"(r[30]), "=r"(r[31])
             : "r"(taddr));
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        const int col0 = nt * kBN + c0;
-        if (row < p.m) {
-          if (p.vec_y && col0 + 16 <= p.n) {
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              const float4 b = p.bias ? __ldg(reinterpret_cast<const float4*>(p.bias + col0) + v)
-                                      : make_float4(0.f, 0.f, 0.f, 0.f);
-              float4 o;
-              o.x = apply_act(__uint_as_float(r[4 * v + 0]) + b.x, p.act);
-              o.y = apply_act(__uint_as_float(r[4 * v + 1]) + b.y, p.act);
-              o.z = apply_act(__uint_as_float(r[4 * v + 2]) + b.z, p.act);
-              o.w = apply_act(__uint_as_float(r[4 * v + 3]) + b.w, p.act);
-              *reinterpret_cast<float4*>(yrow + col0 + 4 * v) = o;
-            }
-          } else {
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              const int col = col0 + c;
-              if (col < p.n)
-                yrow[col] =
-                    apply_act(__uint_as_float(r[c]) + (p.bias ? __ldg(p.bias + col) : 0.f), p.act);
-            }
-          }
+        if (c0 + 32 == kBN) {
+          // every TMEM read of this accumulator is done: release it
+          asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_addr(&acc_empty[abuf]));
         }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) blk[lane * 33 + j] = __uint_as_float(r[j]);
+        __syncwarp();
+        const int col = nt * kBN + c0 + lane;
+        const float b = bv[c0 / 32];
+        const int rows = min(32, p.m - row0);
+        if (col < p.n) {
+          float* ycol = p.y + static_cast<int64_t>(row0) * p.ldy + col;
+          for (int rr = 0; rr < rows; ++rr)
+            ycol[static_cast<int64_t>(rr) * p.ldy] = apply_act(blk[rr * 33 + lane] + b, p.act);
+        }
+        __syncwarp();
       }
-      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&acc_empty[abuf]));
     }
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
