@@ -382,17 +382,21 @@ bool wants_fused_plan(const dlrm_config_t* cfg) {
   return cfg->path != DLRM_PATH_LAYERWISE && (fp32_math(cfg->math) || tensor_core_math(cfg->math));
 }
 
-// The batch from which the layer-wise plan, its large GEMMs as split-TF32
-// on the tensor cores and its launches overlapped (programmatic dependent
-// launch), beats the fp32 fused kernel. A cost model fitted to the
-// 13-512-256-64 / (64 + P)-512-256-1 models with 1 to 32 tables at 2048 to
-// 8192 samples (fused against layer-wise, L2 flushed): the fused kernel takes
-// ~3.13e-8 us per MLP flop plus ~2.04e-7 us per pair-dot flop of a sample;
-// the layer-wise launches ~75 us plus a third of that per sample. The
-// crossover then falls near 5600 samples with 3 tables, 4100 with 16 and 2200
-// with 32 (measured: between 4096 and 8192, near 4400, near 2500). Zero when
-// no layer runs split-TF32.
-int64_t layerwise_crossover(const dlrm_config_t* cfg) {
+// The batch from which the layer-wise plan (its large GEMMs as split-TF32 on
+// the tensor cores, launches overlapped) replaces the fp32 fused kernel. The
+// fused kernel is persistent: one wave of `sms` tiles of `bm` samples runs in
+// the time of one tile, and the next sample starts a second round. Measured
+// on the 13-512-256-64 / (64 + P)-512-256-1 models (L2 flushed), the
+// layer-wise plan takes ~70-90 us from 1024 to 4096 samples, while the fused
+// kernel's round takes ~3.13e-8 us per MLP flop plus ~2.04e-7 us per pair-dot
+// flop per sample of the wave (41.5 us at 3 tables, 104 at 32). So the switch
+// is at the first sample of the second round, when the estimated layer-wise
+// time (70 us plus a third of the fused per-sample cost per sample) is below
+// two fused rounds there; never for models whose fused round is short (the
+// 64-wide model) or that have no split-TF32 layer. Measured crossovers: ~3000
+// samples with 3 tables (2200: layer-wise 74 against fused ~75), ~2800 with 16,
+// ~2100 with 32.
+int64_t layerwise_crossover(const dlrm_config_t* cfg, int bm, int sms) {
   double mlp = 0.0;
   bool split_layer = false;
   for (int g = 0; g < cfg->n_bot + cfg->n_top; ++g) {
@@ -403,11 +407,14 @@ int64_t layerwise_crossover(const dlrm_config_t* cfg) {
     mlp += 2.0 * n * k;
     split_layer = split_layer || tma_layer(DLRM_MATH_FP32, g, n, k);
   }
-  if (!split_layer) return 0;
+  if (!split_layer || bm < 1 || sms < 1) return 0;
   const double f = cfg->n_tables + 1.0;
   const double pair_flops = f * (f - 1.0) * cfg->emb_dim;
   const double per_sample_us = 3.13e-8 * mlp + 2.04e-7 * pair_flops;
-  return static_cast<int64_t>(std::ceil(75.0 / (0.67 * per_sample_us)));
+  const int64_t wave = static_cast<int64_t>(sms) * bm;
+  const double fused_two_rounds = 4.5 + 2.0 * static_cast<double>(wave) * per_sample_us;
+  const double layerwise = 70.0 + per_sample_us / 3.0 * static_cast<double>(wave + 1);
+  return layerwise < fused_two_rounds ? wave + 1 : 0;
 }
 
 struct PlanChoice {
@@ -461,7 +468,7 @@ dlrm_status_t choose_plan(const dlrm_config_t* cfg, const std::vector<std::vecto
                   : DLRM_PATH_LAYERWISE;
     // large batches of the fp32 fused plan: the layer-wise split-TF32 plan
     if (c->path == DLRM_PATH_FUSED && cfg->math == DLRM_MATH_FP32) {
-      const int64_t from = layerwise_crossover(cfg);
+      const int64_t from = layerwise_crossover(cfg, c->fused_bm, sms);
       if (from > 0 && cfg->max_batch >= from) c->layerwise_from = from;
     }
   } else {

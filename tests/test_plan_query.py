@@ -162,18 +162,21 @@ def test_ffma_mode_plans_like_fp32_when_fused():
         assert a["layerwise_from"] == 0
 
 
-@pytest.mark.parametrize("k,lo,hi", [(3, 4096, 6144), (16, 3072, 6144), (32, 2048, 4096)])
-def test_large_batches_switch_to_the_split_tf32_plan(k, lo, hi):
-    """AUTO fp32 on the fused plan runs the layer-wise split-TF32 plan from a
-    batch inside the measured crossover (the fused kernel was faster at `lo`
-    samples, the layer-wise plan at `hi`); a handle whose max_batch is below
-    it never switches, nor an explicit FUSED path or FFMA math."""
-    cfg = synth.sweep_config(16384, k)
+@pytest.mark.parametrize("k", [1, 3, 16, 32])
+@pytest.mark.parametrize("max_batch", [4096, 16384])
+def test_large_batches_switch_to_the_split_tf32_plan(k, max_batch):
+    """AUTO fp32 on the fused plan runs the layer-wise split-TF32 plan from the
+    first sample of a second round of fused tiles (one wave = SMs x tile
+    samples); a handle whose max_batch fits one wave never switches, nor an
+    explicit FUSED path, FFMA math or a model whose fused round is short."""
+    cfg = synth.sweep_config(max_batch, k)
     p = query(cfg)
     assert p["path"] == dl.PATH_FUSED
-    assert lo < p["layerwise_from"] <= hi
+    wave = SMS * p["tile_samples"]
+    assert p["layerwise_from"] == wave + 1
     assert p["tensor_core_layers"] != 0 and p["split_tf32"] == 1
-    assert query(cfg, batch=lo)["layerwise_from"] == 0
+    one_wave = query(cfg, batch=wave)
+    assert one_wave["layerwise_from"] == 0 or one_wave["layerwise_from"] > wave
     assert query(cfg, path=dl.PATH_FUSED)["layerwise_from"] == 0
     assert query(cfg, dl.MATH_FP32_FFMA)["layerwise_from"] == 0
     assert query(synth.get_config("tiny_b64_k3"), batch=65536)["layerwise_from"] == 0
