@@ -499,9 +499,12 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
     const float* zg = zs + (p.prefetch_z ? g0 * k * p.ldz
                                          : (p.zbuf == 2 ? (gi & 1) * p.sg * k * p.ldz : 0));
     // Pair dots; row 0 is x. In 4 x 4 register blocks (gram_block) when the
-    // group has a block task for every thread, else one pair per thread.
+    // group has a block task for at least every other thread, else one pair
+    // per thread: a block reads 8 rows for 16 dots where single pairs read
+    // 32, so blocks win on shared-memory traffic even with half the threads
+    // idle.
     const int nblk = gram_blocks(f);
-    if (ns * nblk >= kConsumers) {
+    if (2 * ns * nblk >= kConsumers) {
       for (int e = tid; e < ns * nblk; e += kConsumers) {
         const int s = e / nblk;
         const int q = e - s * nblk;
@@ -856,6 +859,12 @@ bool fused_plan(int n_dense, int k_tables, int d, int bag, const std::vector<int
         } else if (mode == 1) {
           sg = static_cast<int>(std::min<size_t>(bm, room / (2 * per_sample_z)));
           zbuf = 2;
+          // groups of one or two samples leave the pair dots one pair per
+          // thread (four times the shared-memory reads of 4 x 4 blocks) and
+          // cost a sync and copy round trip per sample: a weight stage is
+          // given up for groups of three (32 tables at 14-row tiles: the
+          // interaction 38.6 -> ~9 us)
+          if (sg < std::min(bm, 3) && stages > 3) continue;
         } else {
           sg = static_cast<int>(std::min<size_t>(bm, room / per_sample_z));
         }
