@@ -62,17 +62,36 @@ __device__ __forceinline__ void pair_from_index(int p, int& i, int& j) {
   j = p - ii * (ii - 1) / 2;
 }
 
-// Pair dots in 4 x 4 register blocks. The lower triangle of one sample's
-// Gram matrix Z Z^T (Z = F rows of d4 float4, in shared memory) is cut into
-// blocks (bi, bj), bi >= bj, of rows i in [4 bi, 4 bi + 4) and j in
-// [4 bj, 4 bj + 4), numbered i-major with the diagonal included: block q is
-// the strict pair (bi + 1, bj) of the same closed form. One thread computes
+// Pair dots in 4 x 4 register blocks. The F rows of one sample's Z (d4
+// float4 each, in shared memory) are dealt into nb = ceil(F / 4) residue
+// classes, class b holding rows b, b + nb, b + 2 nb, b + 3 nb; block (bi, bj),
+// bi >= bj, is the 4 x 4 grid of dots between the rows of classes bi and bj,
+// and the blocks are numbered i-major with the diagonal included (block q is
+// the strict pair (bi + 1, bj) of the same closed form). Every unordered pair
+// of distinct rows falls in exactly one block: the one of its two rows'
+// classes (gram_block_pair names the pair of each entry). One thread computes
 // the 16 dots of a block from 8 128-bit shared loads per 4-wide step (64
-// FMA), against 2 loads per 4 FMA one pair at a time. Rows past F are
-// clamped to F - 1 (computed, never stored).
+// FMA), against 2 loads per 4 FMA one pair at a time. Dealing rows by residue
+// rather than in runs of four puts the threads of a warp, which take
+// consecutive blocks, on consecutive rows: with a row stride of an odd number
+// of 16-byte words those fall in distinct bank groups, where runs of four
+// rows meet in two. Rows past F are clamped to F - 1 (computed, never stored).
 __host__ __device__ __forceinline__ int gram_blocks(int f) {
   const int nb = (f + 3) / 4;
   return nb * (nb + 1) / 2;
+}
+
+// The strict-lower-triangle index of entry (a, c) of block (bi, bj): rows
+// i = bi + a nb and j = bj + c nb, stored as (max, min); -1 when the entry has
+// no pair of its own (a row past F, the diagonal, or, in a diagonal block,
+// the upper copy of a pair).
+__host__ __device__ __forceinline__ int gram_block_pair(int f, int bi, int bj, int a, int c) {
+  const int nb = (f + 3) / 4;
+  const int i = bi + a * nb, j = bj + c * nb;
+  if (i >= f || j >= f || i == j || (bi == bj && a < c)) return -1;
+  const int hi = i > j ? i : j;
+  const int lo = i + j - hi;
+  return hi * (hi - 1) / 2 + lo;
 }
 
 template <class RowFn>
@@ -84,10 +103,11 @@ __device__ __forceinline__ void gram_block(const RowFn& row, int f, int d4, int 
   bj = jj;
   const float* ri[4];
   const float* rj[4];
+  const int nb = (f + 3) / 4;
 #pragma unroll
   for (int a = 0; a < 4; ++a) {
-    ri[a] = row(min(4 * bi + a, f - 1));
-    rj[a] = row(min(4 * bj + a, f - 1));
+    ri[a] = row(min(bi + a * nb, f - 1));
+    rj[a] = row(min(bj + a * nb, f - 1));
   }
 #pragma unroll
   for (int a = 0; a < 4; ++a)

@@ -450,12 +450,19 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
   float* r = out;            // R = [x, z]
 
   // Interaction: R[m] = [x[m], z[m]], zero to the next layer's k_pad.
+  // x by 16-byte words, and the padding past d + pairs zeroed; the pair dots
+  // fill the columns between.
   const int rk = (p.n_top > 1) ? p.gemm[p.n_bot].k_pad : p.k_last;
-  for (int e = tid; e < BM * rk; e += kConsumers) {
-    const int m = e / rk;
-    const int c = e - m * rk;
-    if (c < d) r[m * lda + c] = x[m * lda + c];
-    else if (c >= d + pairs) r[m * lda + c] = 0.f;
+  for (int e = tid; e < BM * d4; e += kConsumers) {
+    const int m = e / d4;
+    const int c4 = e - m * d4;
+    *reinterpret_cast<float4*>(r + m * lda + 4 * c4) =
+        *reinterpret_cast<const float4*>(x + m * lda + 4 * c4);
+  }
+  const int r_pad = rk - d - pairs;
+  for (int e = tid; e < BM * r_pad; e += kConsumers) {
+    const int m = e / r_pad;
+    r[m * lda + d + pairs + (e - m * r_pad)] = 0.f;
   }
   if (p.prefetch_z) cp_async_wait<0>();
   // zbuf == 2: groups 0 and 1 were issued in the prologue; group g + 2
@@ -516,14 +523,12 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
                    bi, bj, acc);
         float* o = r + (g0 + s) * lda + d;
 #pragma unroll
-        for (int a = 0; a < 4; ++a) {
-          const int i = 4 * bi + a;
+        for (int a = 0; a < 4; ++a)
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            const int j = 4 * bj + c;
-            if (i < f && j < i) o[i * (i - 1) / 2 + j] = acc[a][c];
+            const int q2 = gram_block_pair(f, bi, bj, a, c);
+            if (q2 >= 0) o[q2] = acc[a][c];
           }
-        }
       }
     } else {
       for (int e = tid; e < ns * pairs; e += kConsumers) {

@@ -409,14 +409,12 @@ __device__ void cluster_consume(const ClusterParams& p, const Cta& c, const Ring
                  bi, bj, acc);
       float* o = scratch + j * ld_r + d;
 #pragma unroll
-      for (int a = 0; a < 4; ++a) {
-        const int i = 4 * bi + a;
+      for (int a = 0; a < 4; ++a)
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
-          const int jj = 4 * bj + cc;
-          if (i < f && jj < i) o[i * (i - 1) / 2 + jj] = acc[a][cc];
+          const int q2 = gram_block_pair(f, bi, bj, a, cc);
+          if (q2 >= 0) o[q2] = acc[a][cc];
         }
-      }
     }
   } else {
     const int gl = tid & (gsz - 1);

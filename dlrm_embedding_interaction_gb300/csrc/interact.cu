@@ -117,10 +117,11 @@ interaction_kernel(const float* __restrict__ dense, int ld_dense, const float* _
       const int bi = ii - 1, bj = jj;
       const float* ri[4];
       const float* rj[4];
+      const int nb = (f + 3) / 4;   // rows dealt by residue class (gram_block)
 #pragma unroll
       for (int a = 0; a < 4; ++a) {
-        ri[a] = zsam + min(4 * bi + a, f - 1) * ldz;
-        rj[a] = zsam + min(4 * bj + a, f - 1) * ldz;
+        ri[a] = zsam + min(bi + a * nb, f - 1) * ldz;
+        rj[a] = zsam + min(bj + a * nb, f - 1) * ldz;
       }
       float acc[4][4];
 #pragma unroll
@@ -154,14 +155,12 @@ interaction_kernel(const float* __restrict__ dense, int ld_dense, const float* _
       if (active && half == 0) {
         float* o = out + static_cast<int64_t>(b0 + s) * ld_out + col0;
 #pragma unroll
-        for (int a = 0; a < 4; ++a) {
-          const int i = 4 * bi + a;
+        for (int a = 0; a < 4; ++a)
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            const int j = 4 * bj + c;
-            if (i < f && j < i) o[i * (i - 1) / 2 + j] = acc[a][c];
+            const int q2 = gram_block_pair(f, bi, bj, a, c);
+            if (q2 >= 0) o[q2] = acc[a][c];
           }
-        }
       }
     }
   } else if (VEC && use_blocks) {
@@ -176,14 +175,12 @@ interaction_kernel(const float* __restrict__ dense, int ld_dense, const float* _
       gram_block([&](int r) { return zsam + r * ldz; }, f, d4, q, bi, bj, acc);
       float* o = out + static_cast<int64_t>(b0 + s) * ld_out + col0;
 #pragma unroll
-      for (int a = 0; a < 4; ++a) {
-        const int i = 4 * bi + a;
+      for (int a = 0; a < 4; ++a)
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          const int j = 4 * bj + c;
-          if (i < f && j < i) o[i * (i - 1) / 2 + j] = acc[a][c];
+          const int q2 = gram_block_pair(f, bi, bj, a, c);
+          if (q2 >= 0) o[q2] = acc[a][c];
         }
-      }
     }
   } else if (VEC) {
     const int d4 = d / 4;
