@@ -182,6 +182,20 @@ def test_large_batches_switch_to_the_split_tf32_plan(k, max_batch):
     assert query(synth.get_config("tiny_b64_k3"), batch=65536)["layerwise_from"] == 0
 
 
+def test_many_tables_trade_a_weight_stage_for_bag_row_groups():
+    """32 tables at 14-row tiles: the bag rows (14 x 32 rows of 68 floats,
+    122 KB) stream in groups; a 4-stage ring leaves room for groups of one
+    sample, so the plan takes 3 stages and two 3-sample groups: 3 x 32,768
+    (stages) + 2 x 34,304 (14 x 612-float activation buffers) + 9,472 (row
+    indices, biases, last layer, barriers) + 2 x 3 x 8,704 (groups of 32
+    rows of 68 floats) = 228,608 bytes. 16 tables keep every bag row
+    resident (3 stages, no streaming) and 3 tables a 4-stage ring."""
+    assert (query(synth.get_config("b2048_k32"))["ring_stages"],
+            query(synth.get_config("b2048_k32"))["smem_bytes"]) == (3, 228608)
+    assert query(synth.get_config("sweep_b2048_k16"))["ring_stages"] == 3
+    assert query(synth.get_config("b2048_k3"))["ring_stages"] == 4
+
+
 @pytest.mark.parametrize("math", [dl.MATH_FP32, dl.MATH_TF32, dl.MATH_BF16])
 def test_every_sweep_plan_is_consistent(math):
     """Over the 11 x 5 batch x tables sweep: a fused plan fits the device's
