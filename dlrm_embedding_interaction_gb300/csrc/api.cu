@@ -805,9 +805,9 @@ dlrm_status_t dlrm_create(const dlrm_config_t* cfg, const float* const* tables,
         w_head = at(off_whi[g]);
       }
       const bool ok =
-          dlrm::encode_operand_map(T.map_x, in, k, h->max_batch, ld_in) &&
-          dlrm::encode_operand_map(T.map_w, w_head, k, n, ldw) &&
-          (!T.split || dlrm::encode_operand_map(T.map_wlo, at(off_wlo[g]), k, n, ldw));
+          dlrm::encode_operand_map(T.map_x, in, k, h->max_batch, ld_in, 128) &&
+          dlrm::encode_operand_map(T.map_w, w_head, k, n, ldw, 64) &&
+          (!T.split || dlrm::encode_operand_map(T.map_wlo, at(off_wlo[g]), k, n, ldw, 64));
       h->tma_on[g] = ok ? 1 : 0;
     }
     if (st != DLRM_OK) {

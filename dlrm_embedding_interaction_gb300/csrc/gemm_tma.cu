@@ -5,9 +5,12 @@
 //   Y[m][n] = act(sum_k X[m][k] W[n][k] + b[n])   (Luminal compare
 //   modal_ci_ready...vanilla-pytorch, commit message: linear_bias_(relu|sigmoid))
 //
-// A persistent CTA (at most one per SM) walks output tiles of 128 rows x 128
-// columns, t = blockIdx.x, blockIdx.x + gridDim.x, ... with the column tile
-// fastest, so the CTAs running at one time share their rows of X through L2.
+// A persistent CTA (at most one per SM) walks output tiles of 128 rows x BN
+// columns (BN = 128, or 64 when that still gives one tile per SM, or the
+// layer has at most 64 outputs: with one tile per CTA a tile's time is its K
+// loop, and halving BN halves the MMA work per block on twice the SMs),
+// t = blockIdx.x, blockIdx.x + gridDim.x, ... with the column tile fastest,
+// so the CTAs running at one time share their rows of X through L2.
 // Per tile the K dimension flows in blocks of 32 values (128 bytes of fp32:
 // one 128-byte swizzle atom row) through a ring of shared-memory stages:
 //  * warp 0, one lane: loads each block's X tile (128 x 32) and weight tiles
@@ -18,9 +21,9 @@
 //    (hi = x with the low 13 mantissa bits cleared, exact in tf32) and write
 //    the remainder lo = x - hi (exact in fp32) beside it; the weights arrive
 //    already split (head and remainder streams made at create time);
-//  * warp 1, one lane: issues tcgen05.mma kind::tf32, M = 128, N = 128, four
+//  * warp 1, one lane: issues tcgen05.mma kind::tf32, M = 128, N = BN, four
 //    K steps of 8 per block (hi*hi + hi*lo + lo*hi in TF32X3), into one of
-//    two TMEM accumulators of 128 columns, and releases the stage with
+//    two TMEM accumulators of BN columns, and releases the stage with
 //    tcgen05.commit to its empty barrier;
 //  * warps 4-7: read the finished accumulator (tcgen05.ld 32x32b, warp w
 //    the TMEM lanes 32 (w % 4) ...), release it to the next tile but one,
@@ -47,24 +50,24 @@ namespace {
 constexpr int kThreads = 512;             // warps 8-15: more X split warps
 constexpr int kSplitWarps = 10;          // warps 2-3 and 8-15
 constexpr int kBM = 128;                 // rows of X per tile (the MMA M)
-constexpr int kBN = 128;                 // rows of W per tile (the MMA N)
 constexpr int kBK = 32;                  // k per block: 128 bytes of fp32
 constexpr int kTile = kBM * kBK * 4;     // 16 KB: one 128 x 32 fp32 tile
-constexpr int kAccCols = kBN;            // TMEM columns of one accumulator
+constexpr int kWBox = 64;                // weight rows per TMA load (the maps' box)
+constexpr int kWBoxBytes = kWBox * kBK * 4;
 
-template <bool SPLIT>
+template <bool SPLIT, int BN>
 struct Layout {
-  // X, [X lo,] W (hi), [W lo]
-  static constexpr int kParts = SPLIT ? 4 : 2;
-  static constexpr int kStage = kParts * kTile;
-  static constexpr int kStages = SPLIT ? 3 : 6;
+  // X, [X lo,] W (hi), [W lo]; BN weight rows of 128 bytes per W tile
+  static constexpr int kWTile = BN * kBK * 4;
+  static constexpr int kStage = (SPLIT ? 2 : 1) * (kTile + kWTile);
+  static constexpr int kStages = SPLIT ? (BN == 128 ? 3 : 4) : (BN == 128 ? 6 : 8);
   static constexpr int kBars = 3 * kStages + 5;      // full, split, empty; acc full/empty x2; drain
   // epilogue: per epilogue warp a 32 x 32 staging block (stride 33 floats)
   static constexpr int kEpiFloats = 4 * 32 * 33;
   static constexpr int kSmem = 1024 + kStages * kStage + kBars * 8 + 16 + kEpiFloats * 4;
+  static_assert(BN % kWBox == 0 && kWTile % 1024 == 0 && kStage % 1024 == 0, "swizzle atoms");
+  static_assert(kSmem <= 232448, "shared memory of one CTA");
 };
-static_assert(Layout<true>::kSmem <= 232448 && Layout<false>::kSmem <= 232448,
-              "shared memory of one CTA");
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -119,12 +122,13 @@ __device__ void drain_wait(uint32_t bar, uint32_t parity, int32_t* err, uint64_t
   }
 }
 
-template <bool SPLIT>
+template <bool SPLIT, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tma_kernel(const __grid_constant__ CUtensorMap tmap_x,
                 const __grid_constant__ CUtensorMap tmap_w,
                 const __grid_constant__ CUtensorMap tmap_wlo, const TmaGemmParams p) {
-  using Lay = Layout<SPLIT>;
+  using Lay = Layout<SPLIT, BN>;
+  constexpr int kAccCols = BN;   // TMEM columns of one accumulator
   constexpr int S = Lay::kStages;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>(
@@ -143,7 +147,7 @@ gemm_tma_kernel(const __grid_constant__ CUtensorMap tmap_x,
   auto x_tile = [&](int s) { return base + s * Lay::kStage; };
   auto xlo_tile = [&](int s) { return base + s * Lay::kStage + kTile; };
   auto w_tile = [&](int s) { return base + s * Lay::kStage + (SPLIT ? 2 : 1) * kTile; };
-  auto wlo_tile = [&](int s) { return base + s * Lay::kStage + 3 * kTile; };
+  auto wlo_tile = [&](int s) { return base + s * Lay::kStage + 2 * kTile + Lay::kWTile; };
 
   const int warp = threadIdx.x / kWarp;
   const int lane = threadIdx.x % kWarp;
@@ -191,7 +195,7 @@ gemm_tma_kernel(const __grid_constant__ CUtensorMap tmap_x,
       if (SPLIT)
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_wlo))
                      : "memory");
-      constexpr uint32_t kBytes = (SPLIT ? 3 : 2) * kTile;
+      constexpr uint32_t kBytes = kTile + (SPLIT ? 2 : 1) * Lay::kWTile;
       uint32_t stage = 0, phase = 0, it = 0;
       bool ok = true;
       const uint32_t total = static_cast<uint32_t>(
@@ -213,8 +217,14 @@ gemm_tma_kernel(const __grid_constant__ CUtensorMap tmap_x,
           const uint32_t bar = smem_addr(&full[stage]);
           mbar_expect_tx(bar, kBytes);
           tma_load_2d(smem_addr(x_tile(stage)), &tmap_x, kb * kBK, mt * kBM, bar);
-          tma_load_2d(smem_addr(w_tile(stage)), &tmap_w, kb * kBK, nt * kBN, bar);
-          if (SPLIT) tma_load_2d(smem_addr(wlo_tile(stage)), &tmap_wlo, kb * kBK, nt * kBN, bar);
+#pragma unroll
+          for (int h = 0; h < BN / kWBox; ++h) {   // 64-row boxes, 8 swizzle atoms each
+            tma_load_2d(smem_addr(w_tile(stage)) + h * kWBoxBytes, &tmap_w, kb * kBK,
+                        nt * BN + h * kWBox, bar);
+            if (SPLIT)
+              tma_load_2d(smem_addr(wlo_tile(stage)) + h * kWBoxBytes, &tmap_wlo, kb * kBK,
+                          nt * BN + h * kWBox, bar);
+          }
           ++it;
           if (++stage == static_cast<uint32_t>(S)) {
             stage = 0;
@@ -229,7 +239,7 @@ gemm_tma_kernel(const __grid_constant__ CUtensorMap tmap_x,
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issue
     if (lane == 0) {
-      constexpr uint32_t kIdesc = instr_desc(2u, kBN);   // tf32 x tf32 -> fp32, N = 128
+      constexpr uint32_t kIdesc = instr_desc(2u, BN);    // tf32 x tf32 -> fp32, N = BN
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       int i = 0;
@@ -329,17 +339,17 @@ gemm_tma_kernel(const __grid_constant__ CUtensorMap tmap_x,
       const int mt = t / p.n_tiles, nt = t % p.n_tiles;
       // the bias of the lane's column in each 32-column chunk, loaded while
       // the accumulator is still being made
-      float bv[kBN / 32];
+      float bv[BN / 32];
 #pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) {
-        const int col = nt * kBN + 32 * c + lane;
+      for (int c = 0; c < BN / 32; ++c) {
+        const int col = nt * BN + 32 * c + lane;
         bv[c] = (p.bias && col < p.n) ? __ldg(p.bias + col) : 0.f;
       }
       if (!wait_for(smem_addr(&acc_full[abuf]), aphase, abort_flag, p.err, limit)) break;
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       const int row0 = mt * kBM + q * 32;
 #pragma unroll
-      for (int c0 = 0; c0 < kBN; c0 += 32) {
+      for (int c0 = 0; c0 < BN; c0 += 32) {
         uint32_t r[32];
         const uint32_t taddr =
             tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(abuf * kAccCols + c0);
@@ -355,7 +365,7 @@ gemm_tma_kernel(const __grid_constant__ CUtensorMap tmap_x,
               "=r"(r[30]), "=r"(r[31])
             : "r"(taddr));
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        if (c0 + 32 == kBN) {
+        if (c0 + 32 == BN) {
           // every TMEM read of this accumulator is done: release it
           asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
           __syncwarp();
@@ -364,7 +374,7 @@ gemm_tma_kernel(const __grid_constant__ CUtensorMap tmap_x,
 #pragma unroll
         for (int j = 0; j < 32; ++j) blk[lane * 33 + j] = __uint_as_float(r[j]);
         __syncwarp();
-        const int col = nt * kBN + c0 + lane;
+        const int col = nt * BN + c0 + lane;
         const float b = bv[c0 / 32];
         const int rows = min(32, p.m - row0);
         if (col < p.n) {
@@ -386,7 +396,7 @@ gemm_tma_kernel(const __grid_constant__ CUtensorMap tmap_x,
   }
 }
 
-template <bool SPLIT>
+template <bool SPLIT, int BN>
 cudaError_t prepare() {
   static std::atomic<uint64_t> done{0};
   int dev = 0;
@@ -394,8 +404,8 @@ cudaError_t prepare() {
   if (e != cudaSuccess) return e;
   const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
   if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
-  e = cudaFuncSetAttribute(gemm_tma_kernel<SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Layout<SPLIT>::kSmem);
+  e = cudaFuncSetAttribute(gemm_tma_kernel<SPLIT, BN>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<SPLIT, BN>::kSmem);
   if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
   return e;
 }
@@ -420,14 +430,15 @@ bool tma_operand_ok(const void* base, int ld) {
   return base && reinterpret_cast<uintptr_t>(base) % 16 == 0 && ld > 0 && ld % 4 == 0;
 }
 
-bool encode_operand_map(void* map, const float* base, int inner, int rows, int ld) {
+bool encode_operand_map(void* map, const float* base, int inner, int rows, int ld, int box_rows) {
   static_assert(sizeof(CUtensorMap) == kTensorMapBytes, "tensor map size");
   if (!tma_operand_ok(base, ld) || inner < 1 || rows < 1 || inner > ld) return false;
+  if (box_rows != kBM && box_rows != kWBox) return false;
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * sizeof(float)};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(kBM)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estrides[2] = {1, 1};
   const CUresult r = enc(reinterpret_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
                          const_cast<float*>(base), dims, strides, box, estrides,
@@ -449,30 +460,42 @@ cudaError_t launch_linear_tma(const TmaLayer& L, int m, const float* bias, float
   p.err = err;
   p.wait = wait;
   p.m_tiles = (m + kBM - 1) / kBM;
-  p.n_tiles = (L.n + kBN - 1) / kBN;
   p.kb_count = (L.k + kBK - 1) / kBK;
   p.vec_y = (ldy % 4 == 0 && reinterpret_cast<uintptr_t>(y) % 16 == 0 &&
              (bias == nullptr || reinterpret_cast<uintptr_t>(bias) % 16 == 0))
                 ? 1
                 : 0;
+  // 64-column tiles when they still fit one tile per SM (each CTA's K loop
+  // then does half the MMA work), or when the layer has at most 64 outputs
+  const int sms = device_sm_count();
+  const int64_t tiles64 = static_cast<int64_t>(p.m_tiles) * ((L.n + 63) / 64);
+  const bool narrow = L.n <= 64 || tiles64 <= sms;
+  const int bn = narrow ? 64 : 128;
+  p.n_tiles = (L.n + bn - 1) / bn;
   const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
-  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(tiles, device_sm_count()));
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(tiles, sms));
   const CUtensorMap* mx = reinterpret_cast<const CUtensorMap*>(L.map_x);
   const CUtensorMap* mw = reinterpret_cast<const CUtensorMap*>(L.map_w);
   const CUtensorMap* mwl = reinterpret_cast<const CUtensorMap*>(L.split ? L.map_wlo : L.map_w);
   cudaError_t e;
   if (L.split) {
-    e = prepare<true>();
-    if (e != cudaSuccess) return e;
-    return launch_pdl(gemm_tma_kernel<true>, dim3(grid), dim3(kThreads), Layout<true>::kSmem,
-                      stream, *mx, *mw, *mwl, p);
-  } else {
-    e = prepare<false>();
-    if (e != cudaSuccess) return e;
-    return launch_pdl(gemm_tma_kernel<false>, dim3(grid), dim3(kThreads), Layout<false>::kSmem,
-                      stream, *mx, *mw, *mwl, p);
+    if (narrow) {
+      if ((e = prepare<true, 64>()) != cudaSuccess) return e;
+      return launch_pdl(gemm_tma_kernel<true, 64>, dim3(grid), dim3(kThreads),
+                        Layout<true, 64>::kSmem, stream, *mx, *mw, *mwl, p);
+    }
+    if ((e = prepare<true, 128>()) != cudaSuccess) return e;
+    return launch_pdl(gemm_tma_kernel<true, 128>, dim3(grid), dim3(kThreads),
+                      Layout<true, 128>::kSmem, stream, *mx, *mw, *mwl, p);
   }
-  return cudaGetLastError();
+  if (narrow) {
+    if ((e = prepare<false, 64>()) != cudaSuccess) return e;
+    return launch_pdl(gemm_tma_kernel<false, 64>, dim3(grid), dim3(kThreads),
+                      Layout<false, 64>::kSmem, stream, *mx, *mw, *mwl, p);
+  }
+  if ((e = prepare<false, 128>()) != cudaSuccess) return e;
+  return launch_pdl(gemm_tma_kernel<false, 128>, dim3(grid), dim3(kThreads),
+                    Layout<false, 128>::kSmem, stream, *mx, *mw, *mwl, p);
 }
 
 }  // namespace dlrm

@@ -35,10 +35,12 @@ struct TmaGemmParams {
 bool tma_operand_ok(const void* base, int ld);
 
 // Encodes a 2-D fp32 tensor map of `rows` rows of `inner` values, row stride
-// `ld` floats, read in 32 x 128 boxes with the 128-byte swizzle; zeros past
-// the inner width. `map` points to kTensorMapBytes, 64-byte aligned. false
-// when the operand is not TMA-able or the driver's encoder is unavailable.
-bool encode_operand_map(void* map, const float* base, int inner, int rows, int ld);
+// `ld` floats, read in boxes of 32 values x box_rows rows (128 for an input
+// X, 64 for weights: a 128-row weight tile is two loads) with the 128-byte
+// swizzle; zeros past the inner width and the last row. `map` points to
+// kTensorMapBytes, 64-byte aligned. false when the operand is not TMA-able,
+// box_rows is neither 128 nor 64, or the driver's encoder is unavailable.
+bool encode_operand_map(void* map, const float* base, int inner, int rows, int ld, int box_rows);
 
 // Y (m x L.n, row stride ldy) = act(X W^T + bias) for the first m rows of the
 // layer's input buffer.
