@@ -145,13 +145,13 @@ bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
 
 // The cluster-split kernel for small batches of the fp32 fused plan: CTAs per
 // cluster, and the largest batch it takes by default (one wave of clusters
-// at most). Measured on the 13-512-256-64 / 512-256-1 models: it wins up to 64
-// samples at any table count (20-23 against 27-47 us), and up to 128 with 16
-// or more tables, whose wide interaction and top input slow the one-CTA tile
-// more (128 samples, 32 tables: 37 against 47 us); at 128 samples and 8
-// tables or fewer the one-CTA kernel is as fast.
+// at most). Measured on the 13-512-256-64 / 512-256-1 models (flushed L2):
+// it wins at any table count up to 256 samples (128 samples: 22.3-29.9
+// against 26.4-43.2 us for one CTA per tile; 256 samples: 25.8-35.2 against
+// 26.5-43.1) and loses from 384 on (32.5-47.3 against 26.5-43.1), where the
+// tiles of 16 samples make the per-layer k-loops long.
 constexpr int kClusterSizes[2] = {8, 4};
-int cluster_max_batch(int n_tables) { return n_tables >= 16 ? 256 : 128; }
+int cluster_max_batch(int n_tables) { (void)n_tables; return 256; }
 // Clusters of 8 CTAs up to this batch (the fewest weights per CTA: 20 us at
 // 1-32 samples against 22.5 with 4), clusters of 4 above it (128 samples, 3
 // tables: 22.6 us against 28.8 with 8 and 26.7 on one CTA per tile).

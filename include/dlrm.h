@@ -253,8 +253,7 @@ int32_t dlrm_forward_kernels(dlrm_handle_t h, int32_t batch);
  * single-CTA-per-tile kernel (and so does every forward while a phase-trace
  * buffer is set). dlrm_set_cluster_batch_limit sets the limit: 0 turns the
  * cluster kernel off, -1 restores the default (the samples one wave of
- * clusters holds at the tallest tile that fits, at most 128, or 256 with 16
- * or more tables). UNSUPPORTED when the handle has no cluster plan
+ * clusters holds at the tallest tile that fits, at most 256). UNSUPPORTED when the handle has no cluster plan
  * (layer-wise or tensor-core plans, or a model the kernel does not take) and
  * limit > 0; INVALID_ARG for a null handle or limit < -1.
  * dlrm_get_cluster_batch_limit reads the current limit (0 when there is no

@@ -64,7 +64,7 @@ def test_default_limit_and_switch():
     inp = synth.make_inputs(cfg, seed=5)
     model = make_model(cfg, inp)
     default = model.cluster_batch_limit
-    assert default == 128                            # 3 tables
+    assert default == 256
     assert model.kernels(cfg.batch) == dl.KERNELS_FUSED_CLUSTER
     model.cluster_batch_limit = 0
     assert model.cluster_batch_limit == 0
@@ -96,7 +96,7 @@ def test_default_limit_and_switch():
     small.close()
 
 
-SWEEP = [(b, k) for k in (1, 3, 8, 16, 32) for b in (1, 3, 8, 29, 64, 128)]
+SWEEP = [(b, k) for k in (1, 3, 8, 16, 32) for b in (1, 3, 8, 29, 64, 128, 256)]
 
 
 @pytest.mark.parametrize("b,k", SWEEP, ids=[f"b{b}_k{k}" for b, k in SWEEP])
@@ -106,7 +106,7 @@ def test_sweep_cells_match_oracle(b, k):
     cfg = synth.sweep_config(b, k)
     inp = synth.make_inputs(cfg, seed=100 + b + k)
     model = make_model(cfg, inp)
-    assert model.cluster_batch_limit == (256 if k >= 16 else 128)
+    assert model.cluster_batch_limit == 256
     out, st = forward(model, inp, b)
     assert st == dl.OK
     close(out.cpu().numpy(), oracle.forward(inp))
