@@ -15,8 +15,11 @@
 //  * bag indices are loaded once per group (one lane per index) and
 //    broadcast by shuffle; rows are fetched U at a time before any add, so a
 //    warp keeps U * 512 bytes outstanding per group;
-//  * bags are numbered b * K + t so consecutive groups write consecutive
-//    output rows (coalesced stores of the (B, K, D) result);
+//  * bags are numbered t * B + b (table-major): the groups in flight at one
+//    time work on one or two tables, so with skewed (Zipf) indices the hot
+//    rows of the current table share all of L2 instead of every table's hot
+//    rows competing for it, and consecutive groups read consecutive indices;
+//    each group still writes its whole output row (D * 4 bytes) at once;
 //  * no shared-memory staging: each row is read exactly once and consumed in
 //    registers, so a TMA or cp.async copy would only add a round trip.
 // Bounds: every index is checked against rows[t]; a bad index contributes
@@ -104,8 +107,8 @@ gather_vec_kernel(const __grid_constant__ GatherTables tabs, int k_tables, int d
   const unsigned gmask = (TPB == 32) ? 0xffffffffu
                                      : (((1u << TPB) - 1u) << (lane_in_warp & ~(TPB - 1u)));
   if (bag_id >= static_cast<int64_t>(batch) * k_tables) return;  // whole group leaves
-  const int b = static_cast<int>(bag_id / k_tables);
-  const int t = static_cast<int>(bag_id - static_cast<int64_t>(b) * k_tables);
+  const int t = static_cast<int>(bag_id / batch);                 // table-major
+  const int b = static_cast<int>(bag_id - static_cast<int64_t>(t) * batch);
 
   const float init = MODE == DLRM_BAG_MAX ? -INFINITY : 0.f;
   float4 acc[CHUNKS];
@@ -177,7 +180,7 @@ gather_vec_kernel(const __grid_constant__ GatherTables tabs, int k_tables, int d
   }
   // no rows kept: zeros in every mode (a sum of none is already zero); mean
   // divides by the rows kept
-  float4* dst = reinterpret_cast<float4*>(out) + bag_id * d4;
+  float4* dst = reinterpret_cast<float4*>(out) + (static_cast<int64_t>(b) * k_tables + t) * d4;
 #pragma unroll
   for (int c = 0; c < CHUNKS; ++c) {
     const int col4 = lane + c * TPB;
@@ -208,9 +211,9 @@ gather_scalar_kernel(const __grid_constant__ GatherTables tabs, int k_tables, in
   const int64_t bag_id = gtid / kWarp;
   const int lane = threadIdx.x & (kWarp - 1);
   if (bag_id >= static_cast<int64_t>(batch) * k_tables) return;
-  const int b = static_cast<int>(bag_id / k_tables);
-  const int t = static_cast<int>(bag_id - static_cast<int64_t>(b) * k_tables);
-  float* dst = out + bag_id * d;
+  const int t = static_cast<int>(bag_id / batch);                 // table-major
+  const int b = static_cast<int>(bag_id - static_cast<int64_t>(t) * batch);
+  float* dst = out + (static_cast<int64_t>(b) * k_tables + t) * d;
   int64_t start;
   int len;
   if (!bag_bounds<GENERAL>(offsets + static_cast<int64_t>(t) * batch, b, batch, bag, n_idx, start,
