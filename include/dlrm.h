@@ -59,7 +59,9 @@ typedef enum {
  * head*rest + rest*head, about 2^-21 relative per product).
  * FP32_FFMA is FP32 with every GEMM on the FFMA pipe.
  * TF32 and BF16 run the MLPs on the tensor cores with fp32 accumulation in
- * TMEM (opt-in; results within rel 2e-2 of fp32).
+ * TMEM (opt-in; results within rel 2e-2 of fp32). In the layer-wise plan BF16
+ * runs every layer but the first with tf32 operands on the TMA tensor-core
+ * GEMM, which has no bf16 form (tf32 keeps more precision than bf16).
  * TF32X3 is split-TF32 on the tensor cores for every GEMM of 64 or more
  * inputs and 16 or more outputs, in the layer-wise plan and in
  * linear_bias_act; it has no fused plan. */
