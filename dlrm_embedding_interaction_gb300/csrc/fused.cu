@@ -350,7 +350,10 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
   }
   cp_async_commit();
   {
-    const int n_bag = (p.prefetch_z || p.zbuf == 2) ? BM * k : 0;
+    // bag rows to fetch: one per bag, or (bag_rows) every row of every bag,
+    // element e = (sample * k + table) * L + l
+    const int lb = p.bag_rows ? p.bag : 1;
+    const int n_bag = (p.prefetch_z || p.zbuf == 2) ? BM * k * lb : 0;
     const int kp = p.gemm[0].k_pad;
     const int n_dense = BM * kp;
     const int n_all = n_bag > n_dense ? n_bag : n_dense;
@@ -364,10 +367,12 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
         start[h] = row[h] = 0;
         dv[h] = 0.f;
         if (e < n_bag) {
-          const int s = e / k, t = e - s * k;
+          const int sk = e / lb, l = e - sk * lb;
+          const int s = sk / k, t = sk - s * k;
           if (s < rows) {
-            start[h] = __ldg(p.offsets + static_cast<int64_t>(t) * p.batch + m0 + s);
-            row[h] = __ldg(p.indices + static_cast<int64_t>(t) * p.batch + m0 + s);
+            const int64_t b = m0 + s;
+            start[h] = __ldg(p.offsets + static_cast<int64_t>(t) * p.batch + b);
+            row[h] = __ldg(p.indices + (static_cast<int64_t>(t) * p.batch + b) * lb + l);
           }
         }
         if (e < n_dense) {
@@ -380,10 +385,13 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
       for (int h = 0; h < 2; ++h) {
         const int e = e0 + h * kConsumers + tid;
         if (e < n_bag) {
-          const int s = e / k, t = e - s * k;
+          const int sk = e / lb;
+          const int s = sk / k, t = sk - s * k;
           int row32 = -1;
           if (s < rows) {
-            if (start[h] != m0 + s) bad_off = true;
+            // a bag that does not start at b * L is zeros (every one of its
+            // rows sees the same start)
+            if (start[h] != static_cast<int64_t>(m0 + s) * lb) bad_off = true;
             else if (row[h] < 0 || row[h] >= p.tabs.rows[t]) oob = true;
             else row32 = static_cast<int>(row[h]);
           }
@@ -398,10 +406,11 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
   }
   consumer_sync<CW>();
   if (p.prefetch_z) {
-    for (int e = tid; e < BM * k * d4; e += kConsumers) {
-      const int sk = e / d4;              // sample * k + table
+    const int lb = p.bag_rows ? p.bag : 1;
+    for (int e = tid; e < BM * k * lb * d4; e += kConsumers) {
+      const int sk = e / d4;              // (sample * k + table) * L + l
       const int c4 = e - sk * d4;
-      const float* table = p.tabs.ptr[sk % k];
+      const float* table = p.tabs.ptr[(sk / lb) % k];
       float* dst = zs + sk * p.ldz + 4 * c4;
       const int row = rowidx_s[sk];
       if (row >= 0) cp_async16(dst, table + static_cast<int64_t>(row) * d + 4 * c4);
@@ -465,6 +474,36 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
     r[m * lda + d + pairs + (e - m * r_pad)] = 0.f;
   }
   if (p.prefetch_z) cp_async_wait<0>();
+  if (p.bag_rows) {
+    // every row of every bag landed at [(sample * k + table) * L + l]: sum
+    // each bag's L rows (in order) into registers, then, once all have read,
+    // write the sums to rows sample * k + table, the layout of bags of one row
+    consumer_sync<CW>();
+    constexpr int kMaxSums = kFusedBagRowSums;
+    float4 sums[kMaxSums];
+    const int lb = p.bag;
+#pragma unroll
+    for (int i = 0; i < kMaxSums; ++i) {
+      const int e = tid + i * kConsumers;
+      sums[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (e < BM * k * d4) {
+        const int sk = e / d4, c4 = e - sk * d4;
+        for (int l = 0; l < lb; ++l) {
+          const float4 u = *reinterpret_cast<const float4*>(zs + (sk * lb + l) * p.ldz + 4 * c4);
+          sums[i].x += u.x; sums[i].y += u.y; sums[i].z += u.z; sums[i].w += u.w;
+        }
+      }
+    }
+    consumer_sync<CW>();
+#pragma unroll
+    for (int i = 0; i < kMaxSums; ++i) {
+      const int e = tid + i * kConsumers;
+      if (e < BM * k * d4) {
+        const int sk = e / d4, c4 = e - sk * d4;
+        *reinterpret_cast<float4*>(zs + sk * p.ldz + 4 * c4) = sums[i];
+      }
+    }
+  }
   // zbuf == 2: groups 0 and 1 were issued in the prologue; group g + 2
   // streams into buffer g % 2 once group g's pair dots are done.
   for (int g0 = 0, gi = 0; g0 < BM; g0 += p.sg, ++gi) {
@@ -820,9 +859,11 @@ bool fused_plan(int n_dense, int k_tables, int d, int bag, const std::vector<int
   p.ldz = static_cast<int>(round_up(d, 4)) + 4;
 
   // shared-memory carve: stages | act0 | act1 | z | rowidx | bias | wlast | barriers
-  // Preference: every bag row of the tile prefetched at kernel start (bag 1);
-  // else two group buffers streamed with cp.async (bag 1); else one group
-  // buffer filled with summed loads (bags of L > 1). The 16-row tile is kept
+  // Preference: every bag row of the tile prefetched at kernel start (bags of
+  // one row, or every row of bags of L > 1 rows when they fit: the rows land
+  // during the bottom MLP and are summed at the interaction); else two group
+  // buffers streamed with cp.async (bag 1); else one group buffer filled with
+  // summed loads at the interaction (bags of L > 1). The 16-row tile is kept
   // first (one wave of tiles), then a weight stage is given up.
   const size_t per_sample_z = static_cast<size_t>(k_tables) * p.ldz * sizeof(float);
   bool placed = false;
@@ -845,13 +886,20 @@ bool fused_plan(int n_dense, int k_tables, int d, int bag, const std::vector<int
   for (int bm : {16, 14, 12, 8, 4}) {
     if (bm > first_bm) continue;
     for (int mode = 0; mode < 3 && !placed; ++mode) {
-      if (bag != 1 && mode < 2) continue;
+      // bags of several rows: every row prefetched (mode 0) when they fit and
+      // each computing thread holds at most kFusedBagRowSums bag sums, else
+      // summed by loads at the interaction (mode 2)
+      const int lb = (bag > 1 && mode == 0) ? bag : 1;
+      if (bag != 1 && mode == 1) continue;
+      if (lb > 1 && static_cast<int64_t>(bm) * k_tables * (d / 4) >
+                        static_cast<int64_t>(kFusedBagRowSums) * cw * kWarp)
+        continue;
       // the deepest ring that fits: a CTA's weight feed is bounded by the
       // bytes it keeps in flight (~80 GB/s per SM at four 32 KB stages)
       for (int stages : {6, 5, 4, 3}) {
         const size_t off = static_cast<size_t>(stages) * kFusedStageFloats * sizeof(float);
         const size_t act = align128(static_cast<size_t>(bm) * p.lda * sizeof(float));
-        const size_t rowidx = align128(static_cast<size_t>(bm) * k_tables * sizeof(int));
+        const size_t rowidx = align128(static_cast<size_t>(bm) * k_tables * lb * sizeof(int));
         const size_t tail = rowidx + align128(bias_floats * sizeof(float)) +
                             align128(p.k_last * sizeof(float)) + align128(2 * stages * 8 + 16);
         const size_t fixed = off + 2 * act + tail;
@@ -859,7 +907,7 @@ bool fused_plan(int n_dense, int k_tables, int d, int bag, const std::vector<int
         const size_t room = smem_limit - fixed;
         int sg = 0, zbuf = 1;
         if (mode == 0) {
-          if (room < bm * per_sample_z) continue;
+          if (room < bm * per_sample_z * lb) continue;
           sg = bm;
         } else if (mode == 1) {
           sg = static_cast<int>(std::min<size_t>(bm, room / (2 * per_sample_z)));
@@ -878,7 +926,7 @@ bool fused_plan(int n_dense, int k_tables, int d, int bag, const std::vector<int
         p.off_act0 = static_cast<int>(off);
         p.off_act1 = static_cast<int>(off + act);
         p.off_z = static_cast<int>(off + 2 * act);
-        const size_t zbytes = align128(static_cast<size_t>(zbuf) * sg * per_sample_z);
+        const size_t zbytes = align128(static_cast<size_t>(zbuf) * sg * per_sample_z * lb);
         p.off_rowidx = static_cast<int>(p.off_z + zbytes);
         p.off_bias = static_cast<int>(p.off_rowidx + rowidx);
         p.off_wlast = static_cast<int>(p.off_bias + align128(bias_floats * sizeof(float)));
@@ -886,6 +934,7 @@ bool fused_plan(int n_dense, int k_tables, int d, int bag, const std::vector<int
         p.smem_bytes = static_cast<int>(p.off_bar + align128(2 * stages * 8 + 16));
         p.sg = sg;
         p.prefetch_z = mode == 0 ? 1 : 0;
+        p.bag_rows = lb > 1 ? 1 : 0;
         p.zbuf = zbuf;
         plan->bm = bm;
         placed = true;

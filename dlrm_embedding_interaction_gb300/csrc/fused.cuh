@@ -12,6 +12,9 @@ namespace dlrm {
 // whose first warp streams the weights (fused.cu, fused_forward_kernel).
 constexpr int kFusedStageFloats = 8192;                        // 32 KB weight stage
 constexpr int kFusedMaxGemm = 2 * DLRM_MAX_LAYERS;
+// Bags of several rows prefetched whole: at most this many float4 bag sums
+// per computing thread (tile samples x tables x D / 4 <= 8 x 256).
+constexpr int kFusedBagRowSums = 8;
 
 // One GEMM layer of the weight stream. Its weights occupy `passes * n_kst`
 // consecutive stages of the packed stream: pass p covers output columns
@@ -36,7 +39,9 @@ struct FusedParams {
   int lda;           // activation row stride (floats), >= 516, = 4 mod 32
   int ldz;           // bag-sum row stride, round_up(d, 4) + 4
   int sg;            // samples per gather/interaction group
-  int prefetch_z;    // 1: all BM samples' rows are fetched at kernel start (bag 1)
+  int prefetch_z;    // 1: all BM samples' rows are fetched at kernel start (bag 1, or
+                     //    every row of every bag when bag_rows is set)
+  int bag_rows;      // 1: bags of bag > 1 rows, all rows prefetched, summed at the interaction
   int zbuf;          // bag 1 without prefetch: 2 group buffers, rows streamed with cp.async
   int stages;        // weight ring depth
   int n_stages;      // stages of the whole weight stream

@@ -538,6 +538,35 @@ def test_forward_flags_non_uniform_offsets_and_zeroes_the_bag(path):
 
 
 @pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
+def test_forward_bags_of_two_flag_offsets_and_zero_the_bag(path):
+    """Bags of two rows (the 64-wide model; the fused kernel prefetches every
+    row of every bag and sums them at the interaction): a bag start other
+    than b * L is flagged and that bag contributes zeros, an index out of
+    range leaves its row out; every other sample is the oracle's."""
+    cfg = synth.get_config("tiny_b64_k3")
+    inp = synth.make_inputs(cfg, seed=23)
+    model = make_model(cfg, inp, path=path)
+    off = inp["offsets"].copy()
+    off[2, 4] += 1                                  # sample 4, table 2
+    out = model.forward(cu(inp["dense"]), cu(inp["indices"]), cu(off)).cpu().numpy()
+    assert model.error() == dl.ERR_UNSUPPORTED
+    keep = np.arange(cfg.batch) != 4
+    close(out[keep], oracle.forward(inp)[keep])
+    bad = dict(inp)
+    bad["tables"] = list(inp["tables"])
+    bad["tables"][2] = np.concatenate([inp["tables"][2], np.zeros((1, cfg.emb_dim), np.float32)])
+    bad["indices"] = inp["indices"].copy()
+    bad["indices"][2, 8:10] = cfg.rows[2]           # both rows of the bag: the zero row
+    close(out[4:5], oracle.forward(bad, sample_ids=np.array([4])))
+    oob = inp["indices"].copy()
+    oob[0, 2 * 9 + 1] = cfg.rows[0] + 3             # sample 9, table 0, second row
+    out = model.forward(cu(inp["dense"]), cu(oob), cu(inp["offsets"])).cpu().numpy()
+    assert model.error() == dl.ERR_INDEX_OOB
+    close(out, oracle.forward(dict(inp, indices=oob), allow_oob=True))
+    model.close()
+
+
+@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
 def test_profile_environment_switch(path, monkeypatch, capfd):
     """DLRM_PROFILE=1 at create turns per-stage timing on; destroy reports it on stderr."""
     monkeypatch.setenv("DLRM_PROFILE", "1")
