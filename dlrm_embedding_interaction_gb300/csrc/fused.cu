@@ -328,6 +328,12 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
                         int* rowidx_s, float* bias_s, float* wlast_s, int tile, bool first,
                         RingPos& pos) {
   constexpr int kConsumers = CW * kWarp;
+  // Whole-bag prefetch (bags of a few rows) is compiled into the instances
+  // with a run-time row stride only: the workload models' instances (bags
+  // of one row) keep the exact code they had, which matters here because
+  // this kernel's instructions are fetched cold after every L2 flush (the
+  // 2048-sample, 3-table forward ran 4 us slower with the extra code inline).
+  constexpr bool kBagRows = LDA == 0;
   const int lda = LDA > 0 ? LDA : p.lda;   // activation row stride
   const int tid = threadIdx.x;
   const int m0 = tile * BM;
@@ -352,7 +358,7 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
   {
     // bag rows to fetch: one per bag, or (bag_rows) every row of every bag,
     // element e = (sample * k + table) * L + l
-    const int lb = p.bag_rows ? p.bag : 1;
+    const int lb = (kBagRows && p.bag_rows) ? p.bag : 1;
     const int n_bag = (p.prefetch_z || p.zbuf == 2) ? BM * k * lb : 0;
     const int kp = p.gemm[0].k_pad;
     const int n_dense = BM * kp;
@@ -406,7 +412,7 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
   }
   consumer_sync<CW>();
   if (p.prefetch_z) {
-    const int lb = p.bag_rows ? p.bag : 1;
+    const int lb = (kBagRows && p.bag_rows) ? p.bag : 1;
     for (int e = tid; e < BM * k * lb * d4; e += kConsumers) {
       const int sk = e / d4;              // (sample * k + table) * L + l
       const int c4 = e - sk * d4;
@@ -474,7 +480,7 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
     r[m * lda + d + pairs + (e - m * r_pad)] = 0.f;
   }
   if (p.prefetch_z) cp_async_wait<0>();
-  if (p.bag_rows) {
+  if (kBagRows && p.bag_rows) {
     // every row of every bag landed at [(sample * k + table) * L + l]: sum
     // each bag's L rows (in order) into registers, then, once all have read,
     // write the sums to rows sample * k + table, the layout of bags of one row
@@ -889,8 +895,12 @@ bool fused_plan(int n_dense, int k_tables, int d, int bag, const std::vector<int
       // bags of several rows: every row prefetched (mode 0) when they fit and
       // each computing thread holds at most kFusedBagRowSums bag sums, else
       // summed by loads at the interaction (mode 2)
+      // (only the instances with a run-time activation stride carry that code:
+      // tiles of 4 rows, or strides other than 516 and 612)
+      const bool rt_stride = bm < 8 || (p.lda != 516 && p.lda != 612);
       const int lb = (bag > 1 && mode == 0) ? bag : 1;
       if (bag != 1 && mode == 1) continue;
+      if (lb > 1 && !rt_stride) continue;
       if (lb > 1 && static_cast<int64_t>(bm) * k_tables * (d / 4) >
                         static_cast<int64_t>(kFusedBagRowSums) * cw * kWarp)
         continue;
