@@ -91,5 +91,9 @@ bool fused_plan(int n_dense, int k_tables, int d, int bag, const std::vector<int
 
 cudaError_t fused_prepare(int bm, int consumer_warps, int lda);
 cudaError_t launch_fused(const FusedParams& p, int bm, cudaStream_t stream);
+// The instances with phase-trace stamps (fused_trace.cu): launch_fused takes
+// them while p.trace is set.
+cudaError_t fused_prepare_traced(int bm, int consumer_warps, int lda);
+cudaError_t launch_fused_traced(const FusedParams& p, int bm, cudaStream_t stream);
 
 }  // namespace dlrm

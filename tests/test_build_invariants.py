@@ -17,13 +17,16 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 CSRC = os.path.join(ROOT, "dlrm_embedding_interaction_gb300", "csrc")
 
 
-def test_every_fused_kernel_instance_launches_with_168_registers(tmp_path):
+@pytest.mark.parametrize("source", ["fused.cu", "fused_trace.cu"])
+def test_every_fused_kernel_instance_launches_with_168_registers(tmp_path, source):
+    """Both translation units of the kernel: the plain instances and the ones
+    with phase-trace stamps."""
     from dlrm_embedding_interaction_gb300 import build
     nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
     if not os.path.exists(nvcc):
         pytest.skip("nvcc not available")
     cmd = [nvcc, *build.ARCH, *build.NVCC_FLAGS, "-Xptxas", "-v", "-c",
-           os.path.join(CSRC, "fused.cu"), "-o", str(tmp_path / "fused.o")]
+           os.path.join(CSRC, source), "-o", str(tmp_path / "fused.o")]
     r = subprocess.run(cmd, capture_output=True, text=True)
     assert r.returncode == 0, r.stderr[-2000:]
     regs = {}
@@ -37,5 +40,5 @@ def test_every_fused_kernel_instance_launches_with_168_registers(tmp_path):
         if m and current:
             regs[current] = int(m.group(1))
             current = None
-    assert len(regs) >= 5, regs          # every tile height at least once
+    assert len(regs) == 13, regs         # every tile height and stride instance
     assert set(regs.values()) == {168}, regs
