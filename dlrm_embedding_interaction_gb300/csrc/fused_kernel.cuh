@@ -115,7 +115,7 @@ __host__ __device__ __forceinline__ int gemm_rows(const FusedGemm& L, int pass) 
 // a single pass (n_pad <= 256).
 constexpr int kDoubleBufferMax = 56;   // lane tile outputs that leave room for it
 
-template <int BM, int TN, int CGS, int KSPLIT, int CW, int LDA>
+template <int BM, int TN, int CGS, int KSPLIT, int CW, int LDA, bool TRACE>
 __device__ void gemm_layer(const FusedGemm& L, float* a_s, float* c_s, int lda_rt,
                            const float* __restrict__ bias_s, int act, const Ring& r, RingPos& pos,
                            unsigned long long* kstamp) {
@@ -162,7 +162,7 @@ __device__ void gemm_layer(const FusedGemm& L, float* a_s, float* c_s, int lda_r
 
     for (int kst = 0; kst < L.n_kst; ++kst, pos.advance(r.s_count)) {
       const uint32_t st = pos.slot;
-      if (kstamp) {   // profiling (uniform): time the wait
+      if (TRACE && kstamp) {   // profiling (uniform): time the wait
         const long long t0 = clock64();
         wait_phase<true>(smem_u32(&r.full[st]), pos.phase, r.abort_flag, r.err, r.limit_ns);
         waited += clock64() - t0;
@@ -235,7 +235,7 @@ __device__ void gemm_layer(const FusedGemm& L, float* a_s, float* c_s, int lda_r
 
     // profiling: the leader stamps the end of the layer's k-loop and the
     // cycles it waited for weight stages
-    if (kstamp && pass + 1 == L.passes && threadIdx.x == 0) {
+    if (TRACE && kstamp && pass + 1 == L.passes && threadIdx.x == 0) {
       kstamp[0] = global_ns();
       kstamp[10] = static_cast<unsigned long long>(waited);
     }
@@ -298,7 +298,7 @@ __device__ void gemm_layer(const FusedGemm& L, float* a_s, float* c_s, int lda_r
   }
 }
 
-template <int BM, int CW, int LDA>
+template <int BM, int CW, int LDA, bool TRACE>
 __device__ void gemm_dispatch(const FusedGemm& L, float* a_s, float* c_s, int lda,
                               const float* bias_s, int act, int zero_to, const Ring& r,
                               RingPos& pos, unsigned long long* kstamp) {
@@ -308,7 +308,7 @@ __device__ void gemm_dispatch(const FusedGemm& L, float* a_s, float* c_s, int ld
   // columns x 32 k, cut into n_pad / 64 column groups (at least one) and the
   // rest of the warps as k-slices.
 #define DLRM_GEMM_CASE(TN_, CGS_, KSPLIT_) \
-  gemm_layer<BM, TN_, CGS_, KSPLIT_, CW, LDA>(L, a_s, c_s, lda, bias_s, act, r, pos, kstamp)
+  gemm_layer<BM, TN_, CGS_, KSPLIT_, CW, LDA, TRACE>(L, a_s, c_s, lda, bias_s, act, r, pos, kstamp)
   if (L.ksplit == 1) {
     DLRM_GEMM_CASE(4, 8, 1);
   } else {
@@ -465,7 +465,7 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
   float* out = act1;
   for (int g = 0; g < p.n_bot; ++g) {
     const int zero_to = (g + 1 < p.n_bot) ? p.gemm[g + 1].k_pad : p.gemm[g].n_pad;
-    gemm_dispatch<BM, CW, LDA>(p.gemm[g], in, out, lda, bias_s, DLRM_ACT_RELU, zero_to, ring, pos,
+    gemm_dispatch<BM, CW, LDA, TRACE>(p.gemm[g], in, out, lda, bias_s, DLRM_ACT_RELU, zero_to, ring, pos,
                           kloop_stamp<TRACE>(p, tile, g));
     float* t = in; in = out; out = t;
     stamp<TRACE>(p, tile, 2 + g);
@@ -622,7 +622,7 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
   out = (r == act0) ? act1 : act0;
   for (int g = p.n_bot; g < p.n_gemm; ++g) {
     const int zero_to = (g + 1 < p.n_gemm) ? p.gemm[g + 1].k_pad : p.k_last;
-    gemm_dispatch<BM, CW, LDA>(p.gemm[g], in, out, lda, bias_s, DLRM_ACT_RELU, zero_to, ring, pos,
+    gemm_dispatch<BM, CW, LDA, TRACE>(p.gemm[g], in, out, lda, bias_s, DLRM_ACT_RELU, zero_to, ring, pos,
                           kloop_stamp<TRACE>(p, tile, g));
     float* t = in; in = out; out = t;
     stamp<TRACE>(p, tile, 3 + g);
