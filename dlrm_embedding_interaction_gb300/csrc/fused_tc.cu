@@ -49,8 +49,11 @@ constexpr int kMmaWarp = 5;
 constexpr int kThreads = 6 * kWarp;
 constexpr int kActBlock = kTcTile * 128;           // one K-block of the B operand (bytes)
 
+// Phase stamps and wait timers exist only in the TRACE instances (launched
+// while a trace buffer is set), so the plain instances carry no trace code.
+template <bool TRACE>
 __device__ __forceinline__ void stamp(const FusedTcParams& p, int slot) {
-  if (p.trace && threadIdx.x == 0)
+  if (TRACE && p.trace && threadIdx.x == 0)
     p.trace[static_cast<size_t>(blockIdx.x) * kTcTraceSlots + slot] = now_ns();
 }
 
@@ -252,7 +255,7 @@ __device__ void produce(const FusedTcParams& p, unsigned char* ring, uint64_t* f
   }
 }
 
-template <bool BF16>
+template <bool BF16, bool TRACE>
 __device__ void issue_mmas(const FusedTcParams& p, uint32_t tmem, unsigned char* ring,
                            unsigned char* const act[2], uint64_t* full, uint64_t* empty,
                            uint64_t* acc_ready, uint64_t* act_ready, uint64_t* drain,
@@ -264,18 +267,18 @@ __device__ void issue_mmas(const FusedTcParams& p, uint32_t tmem, unsigned char*
   uint32_t slot = 0, phase = 0;   // of stream tile j: j % S and (j / S) & 1
   for (int g = 0; g < p.n_gemm; ++g) {
     const TcGemm& L = p.gemm[g];
-    const uint64_t ta = p.trace ? now_ns() : 0;
+    const uint64_t ta = (TRACE && p.trace) ? now_ns() : 0;
     if (ok) ok = wait_bounded<true>(smem_addr(act_ready), g & 1, abort_flag, p.err, limit);
-    uint64_t act_wait = p.trace ? now_ns() - ta : 0, tile_wait = 0;
+    uint64_t act_wait = (TRACE && p.trace) ? now_ns() - ta : 0, tile_wait = 0;
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t b_base = smem_addr(act[g & 1]);
     // Tiles arrive K-block-major; each (M-tile, K step) pair accumulates into
     // its own 16 columns, so consecutive MMAs never wait on one another.
     for (int kb = 0; kb < L.kbs; ++kb) {
       for (int mt = 0; mt < L.mts; ++mt) {
-        const uint64_t tw = p.trace ? now_ns() : 0;
+        const uint64_t tw = (TRACE && p.trace) ? now_ns() : 0;
         if (ok) ok = wait_bounded<true>(smem_addr(&full[slot]), phase, abort_flag, p.err, limit);
-        if (p.trace) tile_wait += now_ns() - tw;
+        if (TRACE && p.trace) tile_wait += now_ns() - tw;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         if (ok) {
           const uint64_t da = smem_desc(smem_addr(ring + slot * kTcTileBytes));
@@ -295,7 +298,7 @@ __device__ void issue_mmas(const FusedTcParams& p, uint32_t tmem, unsigned char*
     mma_commit(smem_addr(acc_ready));             // the layer's accumulators are final
     // profiling: per layer, ns the MMA thread waited for its input
     // activations (slot 20 + 2g) and for landed weight tiles (21 + 2g)
-    if (p.trace && p.n_gemm + 3 < 20 && 21 + 2 * g < kTcTraceSlots) {
+    if (TRACE && p.trace && p.n_gemm + 3 < 20 && 21 + 2 * g < kTcTraceSlots) {
       unsigned long long* t = p.trace + static_cast<size_t>(blockIdx.x) * kTcTraceSlots;
       t[20 + 2 * g] = act_wait;
       t[21 + 2 * g] = tile_wait;
@@ -315,7 +318,7 @@ __device__ void issue_mmas(const FusedTcParams& p, uint32_t tmem, unsigned char*
   }
 }
 
-template <bool BF16>
+template <bool BF16, bool TRACE>
 __device__ void epilogue(const FusedTcParams& p, uint32_t tmem, unsigned char* const act[2],
                          float* xf, float* hf, float* zs, int* rowidx_s, float* bias_s,
                          float* wlast_s, uint64_t* acc_ready, uint64_t* act_ready,
@@ -432,7 +435,7 @@ __device__ void epilogue(const FusedTcParams& p, uint32_t tmem, unsigned char* c
   // biases, last-layer weights and bag rows land while layer 0 runs
   asm volatile("cp.async.wait_all;\n" ::: "memory");
   epi_sync();
-  stamp(p, 1);
+  stamp<TRACE>(p, 1);
 
   // ---- layers
   for (int g = 0; g < p.n_gemm; ++g) {
@@ -483,7 +486,7 @@ __device__ void epilogue(const FusedTcParams& p, uint32_t tmem, unsigned char* c
       // top MLP's input, zeros up to its padded width
       asm volatile("cp.async.wait_all;\n" ::: "memory");
       epi_sync();
-      stamp(p, 2 + g);
+      stamp<TRACE>(p, 2 + g);
       // one (sample, pair) dot per thread, then zeros to the padded width
       const int kw = p.gemm[g + 1].kbs * KB;
       for (int e = tid; e < kTcTile * pairs; e += kEpiWarps * kWarp) {
@@ -513,10 +516,10 @@ __device__ void epilogue(const FusedTcParams& p, uint32_t tmem, unsigned char* c
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       epi_sync();
       if (tid == 0) mbar_arrive(smem_addr(act_ready));
-      stamp(p, last_bottom ? 2 + p.n_bot : (g < p.n_bot ? 2 + g : 3 + g));
+      stamp<TRACE>(p, last_bottom ? 2 + p.n_bot : (g < p.n_bot ? 2 + g : 3 + g));
     } else {
       epi_sync();
-      stamp(p, 3 + g);
+      stamp<TRACE>(p, 3 + g);
     }
   }
 
@@ -549,13 +552,13 @@ __device__ void epilogue(const FusedTcParams& p, uint32_t tmem, unsigned char* c
     if (oob) atomicOr(reinterpret_cast<unsigned int*>(p.err), DLRM_ERRBIT_INDEX_OOB);
     if (bad_off) atomicOr(reinterpret_cast<unsigned int*>(p.err), DLRM_ERRBIT_OFFSETS);
   }
-  if (p.trace) {
+  if (TRACE && p.trace) {
     epi_sync();
-    stamp(p, 2 + p.n_gemm + 1);
+    stamp<TRACE>(p, 2 + p.n_gemm + 1);
   }
 }
 
-template <bool BF16>
+template <bool BF16, bool TRACE>
 __global__ void __launch_bounds__(kThreads, 1)
 fused_tc_kernel(const __grid_constant__ FusedTcParams p) {
   extern __shared__ unsigned char smem_raw[];
@@ -577,7 +580,7 @@ fused_tc_kernel(const __grid_constant__ FusedTcParams p) {
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const int warp = threadIdx.x / kWarp;
-  stamp(p, 0);
+  stamp<TRACE>(p, 0);
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_addr(tmem_slot)),
@@ -605,10 +608,10 @@ fused_tc_kernel(const __grid_constant__ FusedTcParams p) {
     produce(p, ring, full, empty, abort_flag);
   } else if (warp == kMmaWarp) {
     if (threadIdx.x % kWarp == 0)
-      issue_mmas<BF16>(p, tmem, ring, act, full, empty, acc_ready, act_ready, drain,
+      issue_mmas<BF16, TRACE>(p, tmem, ring, act, full, empty, acc_ready, act_ready, drain,
                        abort_flag);
   } else {
-    epilogue<BF16>(p, tmem, act, xf, hf, zs, rowidx_s, bias_s, wlast_s, acc_ready, act_ready,
+    epilogue<BF16, TRACE>(p, tmem, act, xf, hf, zs, rowidx_s, bias_s, wlast_s, acc_ready, act_ready,
                    abort_flag);
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -621,7 +624,7 @@ fused_tc_kernel(const __grid_constant__ FusedTcParams p) {
   }
 }
 
-template <bool BF16>
+template <bool BF16, bool TRACE>
 cudaError_t enable_smem() {
   static std::atomic<uint64_t> done{0};
   int dev = 0;
@@ -629,7 +632,7 @@ cudaError_t enable_smem() {
   if (e != cudaSuccess) return e;
   const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
   if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
-  e = cudaFuncSetAttribute(fused_tc_kernel<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(fused_tc_kernel<BF16, TRACE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(device_max_smem_optin()));
   if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
   return e;
@@ -648,17 +651,24 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 }  // namespace
 
-cudaError_t fused_tc_prepare(int bf16) { return bf16 ? enable_smem<true>() : enable_smem<false>(); }
+cudaError_t fused_tc_prepare(int bf16) {
+  cudaError_t e = bf16 ? enable_smem<true, false>() : enable_smem<false, false>();
+  if (e == cudaSuccess) e = bf16 ? enable_smem<true, true>() : enable_smem<false, true>();
+  return e;
+}
 
 cudaError_t launch_fused_tc(const FusedTcParams& p, cudaStream_t stream) {
   if (p.batch == 0) return cudaSuccess;
   cudaError_t e = fused_tc_prepare(p.bf16);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>((p.batch + kTcTile - 1) / kTcTile);
-  if (p.bf16)
-    fused_tc_kernel<true><<<grid, kThreads, p.smem_bytes, stream>>>(p);
-  else
-    fused_tc_kernel<false><<<grid, kThreads, p.smem_bytes, stream>>>(p);
+  if (p.bf16) {
+    if (p.trace) fused_tc_kernel<true, true><<<grid, kThreads, p.smem_bytes, stream>>>(p);
+    else fused_tc_kernel<true, false><<<grid, kThreads, p.smem_bytes, stream>>>(p);
+  } else {
+    if (p.trace) fused_tc_kernel<false, true><<<grid, kThreads, p.smem_bytes, stream>>>(p);
+    else fused_tc_kernel<false, false><<<grid, kThreads, p.smem_bytes, stream>>>(p);
+  }
   return cudaGetLastError();
 }
 
