@@ -53,13 +53,14 @@ namespace {
 static_assert(kFusedStageFloats == kRingStageFloats, "one stage size for the plan and the ring");
 
 // Phase trace (profiling): the consumer leader stamps when tile `tile`
-// finishes phase `slot`.
-// Profiling: where GEMM layer g's leader stamps the end of its k-loop
-// (trace slot 20 + g; slot 30 + g then receives the SM cycles warp 0 spent
-// waiting for the layer's weight stages), or null.
-// The stamps exist only in the TRACE instances of the kernel (launched while
-// a trace buffer is set): compiled into the others they cost the 2048-sample,
-// 3-table forward 1.8 us (45.2 against 47.0 us), although never taken.
+// finishes phase `slot`, and (kloop_stamp) where GEMM layer g's leader stamps
+// the end of its k-loop (trace slot 20 + g; slot 30 + g then receives the SM
+// cycles warp 0 spent waiting for the layer's weight stages), or null.
+// The stamps and the k-loop's wait timer exist only in the TRACE instances
+// of the kernel (fused_trace.cu, launched while a trace buffer is set):
+// compiled into the plain instances, untaken, they cost the 2048-sample,
+// 3-table forward 3.6 us (47.0 against 43.4 us), most of it the timer branch
+// inside every k-loop stage.
 template <bool TRACE>
 __device__ __forceinline__ unsigned long long* kloop_stamp(const FusedParams& p, int tile, int g) {
   // slots 20.. are free only while the phase stamps (up to n_gemm + 3) end below
