@@ -170,7 +170,14 @@ __device__ void gemm_layer(const FusedGemm& L, float* a_s, float* c_s, int lda_r
       } else {
         wait_phase<true>(smem_u32(&r.full[st]), pos.phase, r.abort_flag, r.err, r.limit_ns);
       }
-      if (active) {
+      // In the instances with a compile-time row stride (the workload
+      // models') every warp runs the k-loop, also one whose column group lies
+      // past the pass's staged rows (the last pass of a layer wider than 512):
+      // it reads stale rows inside the stage buffer and its sums are never
+      // stored (the epilogue checks `active`). A branch here cost the
+      // 2048-sample forward 0.7-1 us although always taken there; the run-time
+      // stride instances (the 64-wide model: 0.5 us the other way) keep it.
+      if (LDA > 0 || active) {
         const float* ws = r.stages + st * kFusedStageFloats + (cg * WCOLS + lcg) * KS;
         const float* as = a_base + kst * KS;
         if (kDoubleBuffer) {
