@@ -718,7 +718,7 @@ dlrm_status_t dlrm_create(const dlrm_config_t* cfg, const float* const* tables,
     h->fused.stage_tab = reinterpret_cast<const uint2*>(at(off_ft));
     h->fused.bias = at(off_fb);
     h->fused.wlast = at(off_fl);
-    if (st == DLRM_OK) st = cuda_status(dlrm::fused_prepare(h->fused_bm, h->fused.cw, h->fused.lda));
+    if (st == DLRM_OK) st = cuda_status(dlrm::fused_prepare(h->fused_bm, h->fused.cw, dlrm::fused_instance_lda(h->fused)));
   }
   int cluster_limit = 0;
   for (int ci = 0; ci < 2 && st == DLRM_OK; ++ci) {

@@ -138,12 +138,10 @@ bool fused_plan(int n_dense, int k_tables, int d, int bag, const std::vector<int
       // bags of several rows: every row prefetched (mode 0) when they fit and
       // each computing thread holds at most kFusedBagRowSums bag sums, else
       // summed by loads at the interaction (mode 2)
-      // (only the instances with a run-time activation stride carry that code:
-      // tiles of 4 rows, or strides other than 516 and 612)
-      const bool rt_stride = bm < 8 || (p.lda != 516 && p.lda != 612);
+      // (they run on the instances with a run-time activation stride, which
+      // carry that code: fused_instance_lda)
       const int lb = (bag > 1 && mode == 0) ? bag : 1;
       if (bag != 1 && mode == 1) continue;
-      if (lb > 1 && !rt_stride) continue;
       if (lb > 1 && static_cast<int64_t>(bm) * k_tables * (d / 4) >
                         static_cast<int64_t>(kFusedBagRowSums) * cw * kWarp)
         continue;

@@ -89,6 +89,15 @@ bool fused_plan(int n_dense, int k_tables, int d, int bag, const std::vector<int
                 const std::vector<std::vector<float>>& b, const GatherTables& tabs,
                 int max_batch, int sms, size_t smem_limit, int consumer_warps, FusedPlan* plan);
 
+// The activation stride of the kernel instance a plan runs on: 516 or 612
+// (compile-time strides, one bag-row mode each) when the plan's stride and
+// mode match those instances, else 0 (the run-time-stride instances).
+inline int fused_instance_lda(const FusedParams& p) {
+  if (p.lda == 516 && p.prefetch_z && !p.bag_rows) return 516;
+  if (p.lda == 612 && p.zbuf == 2) return 612;
+  return 0;
+}
+// lda: fused_instance_lda of the plan.
 cudaError_t fused_prepare(int bm, int consumer_warps, int lda);
 cudaError_t launch_fused(const FusedParams& p, int bm, cudaStream_t stream);
 // The instances with phase-trace stamps (fused_trace.cu): launch_fused takes

@@ -351,6 +351,12 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
   // this kernel's instructions are fetched cold after every L2 flush (the
   // 2048-sample, 3-table forward ran 4 us slower with the extra code inline).
   constexpr bool kBagRows = LDA == 0;
+  // Bag-row mode: each compile-time-stride instance takes one mode (516: every
+  // bag row prefetched at tile start; 612: rows streamed through two group
+  // buffers), so the other modes' code is not in it; fused_instance_lda sends
+  // every other plan to the run-time-stride instances, which take any mode.
+  const bool pz = LDA == 516 ? true : (LDA == 612 ? false : p.prefetch_z != 0);
+  const bool zb2 = LDA == 612 ? true : (LDA == 516 ? false : p.zbuf == 2);
   const int lda = LDA > 0 ? LDA : p.lda;   // activation row stride
   const int tid = threadIdx.x;
   const int m0 = tile * BM;
@@ -376,7 +382,7 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
     // bag rows to fetch: one per bag, or (bag_rows) every row of every bag,
     // element e = (sample * k + table) * L + l
     const int lb = (kBagRows && p.bag_rows) ? p.bag : 1;
-    const int n_bag = (p.prefetch_z || p.zbuf == 2) ? BM * k * lb : 0;
+    const int n_bag = (pz || zb2) ? BM * k * lb : 0;
     const int kp = p.gemm[0].k_pad;
     const int n_dense = BM * kp;
     const int n_all = n_bag > n_dense ? n_bag : n_dense;
@@ -428,7 +434,7 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
     }
   }
   consumer_sync<CW>();
-  if (p.prefetch_z) {
+  if (pz) {
     const int lb = (kBagRows && p.bag_rows) ? p.bag : 1;
     for (int e = tid; e < BM * k * lb * d4; e += kConsumers) {
       const int sk = e / d4;              // (sample * k + table) * L + l
@@ -462,7 +468,7 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
     }
     cp_async_commit();
   };
-  if (p.zbuf == 2) {
+  if (zb2) {
     // the first two groups land while the bottom MLP runs
     issue_group(0, 0);
     if (p.sg < BM) issue_group(p.sg, 1);
@@ -496,7 +502,7 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
     const int m = e / r_pad;
     r[m * lda + d + pairs + (e - m * r_pad)] = 0.f;
   }
-  if (p.prefetch_z) cp_async_wait<0>();
+  if (pz) cp_async_wait<0>();
   if (kBagRows && p.bag_rows) {
     // every row of every bag landed at [(sample * k + table) * L + l]: sum
     // each bag's L rows (in order) into registers, then, once all have read,
@@ -531,9 +537,9 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
   // streams into buffer g % 2 once group g's pair dots are done.
   for (int g0 = 0, gi = 0; g0 < BM; g0 += p.sg, ++gi) {
     const int ns = min(p.sg, BM - g0);
-    if (p.zbuf == 2) {
+    if (zb2) {
       cp_async_wait<1>();   // group gi has landed (only gi + 1 may be pending)
-    } else if (!p.prefetch_z) {
+    } else if (!pz) {
       for (int e = tid; e < ns * k * d4; e += kConsumers) {
         const int s = e / (k * d4);
         const int rem = e - s * k * d4;
@@ -565,8 +571,7 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
       }
     }
     consumer_sync<CW>();
-    const float* zg = zs + (p.prefetch_z ? g0 * k * p.ldz
-                                         : (p.zbuf == 2 ? (gi & 1) * p.sg * k * p.ldz : 0));
+    const float* zg = zs + (pz ? g0 * k * p.ldz : (zb2 ? (gi & 1) * p.sg * k * p.ldz : 0));
     // Pair dots; row 0 is x. In 4 x 4 register blocks (gram_block) when the
     // group has a block task for at least every other thread, else one pair
     // per thread: a block reads 8 rows for 16 dots where single pairs read
@@ -614,7 +619,7 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
       }
     }
     consumer_sync<CW>();
-    if (p.zbuf == 2) {
+    if (zb2) {
       if (g0 + 2 * p.sg < BM) issue_group(g0 + 2 * p.sg, gi & 1);
       else cp_async_commit();
     }
@@ -788,12 +793,13 @@ cudaError_t launch_fused_instances(const FusedParams& p, int bm, cudaStream_t st
   // persistent: at most one CTA per SM, each looping over its tiles
   const int64_t tiles = (p.batch + bm - 1) / bm;
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(tiles, device_sm_count()));
-  cudaError_t e = prepare_fused_instances<TRACE>(bm, p.cw, p.lda);
+  const int ilda = fused_instance_lda(p);
+  cudaError_t e = prepare_fused_instances<TRACE>(bm, p.cw, ilda);
   if (e != cudaSuccess) return e;
   const unsigned threads = static_cast<unsigned>(kFusedWarps * kWarp);
 #define DLRM_LAUNCH(BM_, LDA_) \
   fused_forward_kernel<BM_, 8, LDA_, TRACE><<<grid, threads, p.smem_bytes, stream>>>(p)
-  DLRM_FUSED_SWITCH(bm, p.lda, DLRM_LAUNCH)
+  DLRM_FUSED_SWITCH(bm, ilda, DLRM_LAUNCH)
 #undef DLRM_LAUNCH
   return cudaGetLastError();
 }
