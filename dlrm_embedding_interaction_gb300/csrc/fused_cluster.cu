@@ -158,6 +158,9 @@ __device__ void cluster_gemm(const ClusterParams& p, const Cta& c, int g, const 
   const int cg = tid % half;
   const int ks = tid / half;
   const int k4v = (L.k + 3) >> 2;
+  // kslices = 512 / s is a power of two: shifts, not divisions, per stage
+  // (k_here and the inputs left are non-negative multiples of it)
+  const int kshift = 31 - __clz(L.kslices);
   float2 acc[BM][2];
 #pragma unroll
   for (int m = 0; m < BM; ++m) acc[m][0] = acc[m][1] = make_float2(0.f, 0.f);
@@ -166,10 +169,10 @@ __device__ void cluster_gemm(const ClusterParams& p, const Cta& c, int g, const 
     wait_phase<true>(smem_u32(&r.full[pos.slot]), pos.phase, r.abort_flag, r.err, r.limit_ns);
     const float4* w = reinterpret_cast<const float4*>(r.stages + pos.slot * kRingStageFloats);
     const int k_here = min(L.kst_k, L.k_pad - kst * L.kst_k);
-    const int steps = k_here / (4 * L.kslices);
+    const int steps = k_here >> (2 + kshift);
     const int k4_0 = kst * (L.kst_k >> 2) + ks;
     // the thread's steps that reach inputs below k (k4_0 + kslices i < k4v)
-    const int n = k4_0 < k4v ? min(steps, (k4v - k4_0 + L.kslices - 1) / L.kslices) : 0;
+    const int n = k4_0 < k4v ? min(steps, (k4v - k4_0 + L.kslices - 1) >> kshift) : 0;
     const float* a0 = a_s + 4 * k4_0;
 #pragma unroll 4
     for (int i = 0; i < n; ++i) {
