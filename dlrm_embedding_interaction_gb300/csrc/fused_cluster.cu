@@ -154,9 +154,9 @@ __device__ void cluster_gemm(const ClusterParams& p, const Cta& c, int g, const 
   const ClusterGemm& L = p.gemm[g];
   const int tid = threadIdx.x;
   const int lda = p.lda;
-  const int half = L.s >> 1;
-  const int cg = tid % half;
-  const int ks = tid / half;
+  const int half = L.s >> 1;               // a power of two
+  const int cg = tid & (half - 1);
+  const int ks = tid >> (31 - __clz(half));
   const int k4v = (L.k + 3) >> 2;
   // kslices = 512 / s is a power of two: shifts, not divisions, per stage
   // (k_here and the inputs left are non-negative multiples of it)
@@ -202,18 +202,20 @@ __device__ void cluster_gemm(const ClusterParams& p, const Cta& c, int g, const 
   // consecutive lanes (G a power of two: 32 when the outputs are few), then
   // the group's lanes push it to the cluster's ranks between them.
   const int s4 = L.s >> 2;
+  const int s4shift = 31 - __clz(s4);
   const int outs = BM * s4;
   int gsz = kClusterThreads / outs;
   gsz = gsz >= 32 ? 32 : (gsz >= 16 ? 16 : (gsz >= 8 ? 8 : (gsz >= 4 ? 4 : (gsz >= 2 ? 2 : 1))));
   if (gsz > L.kslices) gsz = L.kslices;
+  const int gshift = 31 - __clz(gsz);
   const int gl = tid & (gsz - 1);
   const uint32_t bar = c.xbar(e);
   const uint32_t base = smem_u32(out_s) + 4u * (c.q * L.s);
   for (int t0 = 0; t0 < outs * gsz; t0 += kClusterThreads) {
-    const int o = (t0 + tid) / gsz;
+    const int o = (t0 + tid) >> gshift;
     const bool live = o < outs;
-    const int m = live ? o / s4 : 0;
-    const int c4 = live ? o - m * s4 : 0;
+    const int m = live ? o >> s4shift : 0;
+    const int c4 = live ? o & (s4 - 1) : 0;
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
     if (live) {
       for (int kk = gl; kk < L.kslices; kk += gsz) {
@@ -455,9 +457,10 @@ __device__ void cluster_consume(const ClusterParams& p, const Cta& c, const Ring
     const uint32_t bar = c.xbar(e_int);
     const uint32_t base = smem_u32(rbuf);
     const int r4 = ld_r / 4;
+    const int cshift = 31 - __clz(C);       // clusters of 4 or 8 CTAs
     // each float4 of R by C consecutive threads, one rank each
     for (int e = tid; e < nmine * r4 * C; e += kClusterThreads) {
-      const int o = e / C, rk = e - o * C;
+      const int o = e >> cshift, rk = e & (C - 1);
       const int j = o / r4, c4 = o - j * r4;
       const int m = static_cast<int>(c.q) + C * j;
       const float4 v = *reinterpret_cast<const float4*>(scratch + j * ld_r + 4 * c4);
