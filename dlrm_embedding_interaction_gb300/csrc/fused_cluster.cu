@@ -108,6 +108,19 @@ __device__ __forceinline__ bool wait_exchange(uint32_t bar, uint32_t parity,
   }
 }
 
+// a / b for 0 <= a < 2^17 and 1 <= b < 2^14, given rb = __frcp_rn(b): the
+// rounded product a rb is within one of the quotient, and one correction
+// step each way makes it exact (checked over that whole range on the host).
+// Shorter than the integer division sequence on the kernel's latency-bound
+// paths; every divisor here is a loop invariant.
+__device__ __forceinline__ int quot(int a, int b, float rb) {
+  int q = __float2int_rz(__fmul_rn(__int2float_rn(a), rb));
+  const int r = a - q * b;
+  q += r >= b ? 1 : 0;
+  q -= r < 0 ? 1 : 0;
+  return q;
+}
+
 // Bytes exchange e brings every CTA of the cluster.
 __device__ __forceinline__ uint32_t exchange_bytes(const ClusterParams& p, int e) {
   if (e == p.n_bot) return static_cast<uint32_t>(p.bm * p.ld_r * 4);
@@ -203,9 +216,11 @@ __device__ void cluster_gemm(const ClusterParams& p, const Cta& c, int g, const 
   // the group's lanes push it to the cluster's ranks between them.
   const int s4 = L.s >> 2;
   const int s4shift = 31 - __clz(s4);
-  const int outs = BM * s4;
-  int gsz = kClusterThreads / outs;
-  gsz = gsz >= 32 ? 32 : (gsz >= 16 ? 16 : (gsz >= 8 ? 8 : (gsz >= 4 ? 4 : (gsz >= 2 ? 2 : 1))));
+  static_assert(BM == 4 || BM == 8 || BM == 16, "tile heights");
+  constexpr int kLog2BM = BM == 4 ? 2 : (BM == 8 ? 3 : 4);
+  const int oshift = kLog2BM + s4shift;     // outs = BM * s4, a power of two
+  const int outs = 1 << oshift;
+  int gsz = oshift >= 8 ? 1 : min(kClusterThreads >> oshift, 32);
   if (gsz > L.kslices) gsz = L.kslices;
   const int gshift = 31 - __clz(gsz);
   const int gl = tid & (gsz - 1);
@@ -252,9 +267,12 @@ __device__ void cluster_consume(const ClusterParams& p, const Cta& c, const Ring
   const int C = p.csize;
   const int m0 = static_cast<int>(cluster_id()) * BM;
   const int rows = min(BM, p.batch - m0);
-  const int k = p.k_tables, d = p.d, d4 = d / 4;
+  const int k = p.k_tables, d = p.d, d4 = d >> 2;
   const int f = k + 1;
   const int pairs = f * (f - 1) / 2;
+  const int cshift = 31 - __clz(C);       // clusters of 2 to 16 CTAs
+  const float r_k = __frcp_rn(static_cast<float>(k));
+  const float r_d4 = __frcp_rn(static_cast<float>(d4));
   bool oob = false, bad_off = false;
 
   // Prologue: this rank's bias block and the last layer's weights (group
@@ -268,6 +286,7 @@ __device__ void cluster_consume(const ClusterParams& p, const Cta& c, const Ring
   // One round of global loads, both elements of a thread in flight before
   // either is used: dense features and (bags of one row) bag starts and rows.
   const int kd = (p.n_dense + 3) & ~3;
+  const float r_kd = __frcp_rn(static_cast<float>(kd));
   const int n_dense = BM * kd;
   const int n_bag = p.bag == 1 ? p.zrows * k : 0;
   const int n_all = max(n_dense, n_bag);
@@ -280,12 +299,12 @@ __device__ void cluster_consume(const ClusterParams& p, const Cta& c, const Ring
       dv[h] = 0.f;
       start[h] = row[h] = 0;
       if (e < n_dense) {
-        const int m = e / kd, col = e - m * kd;
+        const int m = quot(e, kd, r_kd), col = e - m * kd;
         if (m < rows && col < p.n_dense)
           dv[h] = __ldg(p.dense + static_cast<int64_t>(m0 + m) * p.n_dense + col);
       }
       if (e < n_bag) {
-        const int j = e / k, t = e - j * k;
+        const int j = quot(e, k, r_k), t = e - j * k;
         const int m = static_cast<int>(c.q) + C * j;
         if (m < rows) {
           start[h] = __ldg(p.offsets + static_cast<int64_t>(t) * p.batch + m0 + m);
@@ -297,11 +316,11 @@ __device__ void cluster_consume(const ClusterParams& p, const Cta& c, const Ring
     for (int h = 0; h < 2; ++h) {
       const int e = e0 + h * kClusterThreads + tid;
       if (e < n_dense) {
-        const int m = e / kd;
+        const int m = quot(e, kd, r_kd);
         act0[m * lda + (e - m * kd)] = dv[h];
       }
       if (e < n_bag) {
-        const int j = e / k, t = e - j * k;
+        const int j = quot(e, k, r_k), t = e - j * k;
         const int m = static_cast<int>(c.q) + C * j;
         int row32 = -1;
         if (m < rows) {
@@ -316,9 +335,9 @@ __device__ void cluster_consume(const ClusterParams& p, const Cta& c, const Ring
   if (p.bag == 1) {
     consumer_sync<kClusterWarps>();
     for (int e = tid; e < p.zrows * k * d4; e += kClusterThreads) {
-      const int jt = e / d4;              // row * k + table
+      const int jt = quot(e, d4, r_d4);   // row * k + table
       const int c4 = e - jt * d4;
-      const float* table = p.tabs.ptr[jt % k];
+      const float* table = p.tabs.ptr[jt - quot(jt, k, r_k) * k];
       float* dst = zs + jt * p.ldz + 4 * c4;
       const int rw = rowidx_s[jt];
       if (rw >= 0) cp_async16(dst, table + static_cast<int64_t>(rw) * d + 4 * c4);
@@ -347,9 +366,9 @@ __device__ void cluster_consume(const ClusterParams& p, const Cta& c, const Ring
     cp_async_wait<0>();
   } else {
     for (int e = tid; e < p.zrows * k * d4; e += kClusterThreads) {
-      const int jt = e / d4;
+      const int jt = quot(e, d4, r_d4);
       const int c4 = e - jt * d4;
-      const int j = jt / k, t = jt - j * k;
+      const int j = quot(jt, k, r_k), t = jt - j * k;
       const int m = static_cast<int>(c.q) + C * j;
       float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
       if (m < rows) {
@@ -377,13 +396,12 @@ __device__ void cluster_consume(const ClusterParams& p, const Cta& c, const Ring
   }
   consumer_sync<kClusterWarps>();
   const int ld_r = p.ld_r;
-  const int nmine = (BM - static_cast<int>(c.q) + C - 1) / C;   // rows q, q + C, ... below BM
-  for (int e = tid; e < nmine * ld_r; e += kClusterThreads) {
-    const int j = e / ld_r, col = e - j * ld_r;
+  // rows q, q + C, ... below BM
+  const int nmine = max(BM - static_cast<int>(c.q) + C - 1, 0) >> cshift;
+  for (int j = 0; j < nmine; ++j) {
     const int m = static_cast<int>(c.q) + C * j;
-    float v = 0.f;
-    if (col < d) v = x[m * lda + col];
-    scratch[j * ld_r + col] = v;          // pairs overwrite [d, d + pairs) below
+    for (int col = tid; col < ld_r; col += kClusterThreads)
+      scratch[j * ld_r + col] = col < d ? x[m * lda + col] : 0.f;   // pairs overwrite [d, d + pairs) below
   }
   consumer_sync<kClusterWarps>();
   // Pair dots (row 0 is x) of this CTA's rows: in 4 x 4 register blocks
@@ -393,17 +411,19 @@ __device__ void cluster_consume(const ClusterParams& p, const Cta& c, const Ring
   const int nblk = gram_blocks(f);
   const int block_cost = (nmine * nblk + kClusterThreads - 1) / kClusterThreads * d4 * 64;
   int gsz = 0, lane_cost = block_cost;
-  for (int gg = 1; gg <= 32 && gg <= d4; gg *= 2) {
+  for (int lg = 0; lg <= 5 && (1 << lg) <= d4; ++lg) {
+    const int gg = 1 << lg;
     const int rounds = (nmine * pairs * gg + kClusterThreads - 1) / kClusterThreads;
-    const int cost = rounds * ((d4 + gg - 1) / gg * 40 + 120);
+    const int cost = rounds * (((d4 + gg - 1) >> lg) * 40 + 120);
     if (cost < lane_cost) {
       lane_cost = cost;
       gsz = gg;
     }
   }
   if (gsz == 0) {
+    const float r_nblk = __frcp_rn(static_cast<float>(nblk));
     for (int e = tid; e < nmine * nblk; e += kClusterThreads) {
-      const int j = e / nblk;
+      const int j = quot(e, nblk, r_nblk);
       const int qb = e - j * nblk;
       const int m = static_cast<int>(c.q) + C * j;
       const float* xrow = x + m * lda;
@@ -423,13 +443,15 @@ __device__ void cluster_consume(const ClusterParams& p, const Cta& c, const Ring
     }
   } else {
     const int gl = tid & (gsz - 1);
+    const int gshift = 31 - __clz(gsz);
+    const float r_pairs = __frcp_rn(static_cast<float>(pairs));
     const int tasks = nmine * pairs;
     for (int t0 = 0; t0 < tasks * gsz; t0 += kClusterThreads) {
-      const int task = (t0 + tid) / gsz;
+      const int task = (t0 + tid) >> gshift;
       float a = 0.f;
       int j = 0, q = 0;
       if (task < tasks) {
-        j = task / pairs;
+        j = quot(task, pairs, r_pairs);
         q = task - j * pairs;
         int i, jj;
         pair_from_index(q, i, jj);
@@ -456,15 +478,15 @@ __device__ void cluster_consume(const ClusterParams& p, const Cta& c, const Ring
     consumer_sync<kClusterWarps>();
     const uint32_t bar = c.xbar(e_int);
     const uint32_t base = smem_u32(rbuf);
-    const int r4 = ld_r / 4;
-    const int cshift = 31 - __clz(C);       // clusters of 4 or 8 CTAs
+    const int r4 = ld_r >> 2;
     // each float4 of R by C consecutive threads, one rank each
-    for (int e = tid; e < nmine * r4 * C; e += kClusterThreads) {
-      const int o = e >> cshift, rk = e & (C - 1);
-      const int j = o / r4, c4 = o - j * r4;
+    for (int j = 0; j < nmine; ++j) {
       const int m = static_cast<int>(c.q) + C * j;
-      const float4 v = *reinterpret_cast<const float4*>(scratch + j * ld_r + 4 * c4);
-      push_ranks(base + 4u * (m * lda + 4 * c4), bar, v, rk, C, C);
+      for (int e = tid; e < r4 * C; e += kClusterThreads) {
+        const int c4 = e >> cshift, rk = e & (C - 1);
+        const float4 v = *reinterpret_cast<const float4*>(scratch + j * ld_r + 4 * c4);
+        push_ranks(base + 4u * (m * lda + 4 * c4), bar, v, rk, C, C);
+      }
     }
     wait_exchange(bar, (e_int >> 1) & 1, c.abort_flag, p.err, c.limit_ns);
   }
