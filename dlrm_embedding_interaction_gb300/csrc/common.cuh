@@ -50,6 +50,20 @@ __device__ __forceinline__ float apply_act(float a, int act) {
   return a;
 }
 
+// a / b for 0 <= a < 2^20 and 1 <= b < 2^14, given rb = __frcp_rn(b): the
+// rounded product a rb is within one of the quotient (its relative error is
+// below 2^-22), and one correction step each way makes it exact (also
+// checked over that whole range on the host). Shorter than the integer
+// division sequence on the fused kernels' latency-bound tile paths, where
+// every divisor is a loop invariant whose reciprocal is taken once.
+__device__ __forceinline__ int quot(int a, int b, float rb) {
+  int q = __float2int_rz(__fmul_rn(__int2float_rn(a), rb));
+  const int r = a - q * b;
+  q += r >= b ? 1 : 0;
+  q -= r < 0 ? 1 : 0;
+  return q;
+}
+
 // Pair index p -> (i, j) of the strict lower triangle, i-major:
 // p = i(i-1)/2 + j with 0 <= j < i. The closed form i = floor((1+sqrt(1+8p))/2)
 // (Luminal PairwiseDotLowerTriStackedKernel) is evaluated in fp32, then fixed

@@ -108,19 +108,6 @@ __device__ __forceinline__ bool wait_exchange(uint32_t bar, uint32_t parity,
   }
 }
 
-// a / b for 0 <= a < 2^17 and 1 <= b < 2^14, given rb = __frcp_rn(b): the
-// rounded product a rb is within one of the quotient, and one correction
-// step each way makes it exact (checked over that whole range on the host).
-// Shorter than the integer division sequence on the kernel's latency-bound
-// paths; every divisor here is a loop invariant.
-__device__ __forceinline__ int quot(int a, int b, float rb) {
-  int q = __float2int_rz(__fmul_rn(__int2float_rn(a), rb));
-  const int r = a - q * b;
-  q += r >= b ? 1 : 0;
-  q -= r < 0 ? 1 : 0;
-  return q;
-}
-
 // Bytes exchange e brings every CTA of the cluster.
 __device__ __forceinline__ uint32_t exchange_bytes(const ClusterParams& p, int e) {
   if (e == p.n_bot) return static_cast<uint32_t>(p.bm * p.ld_r * 4);

@@ -361,9 +361,12 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
   const int tid = threadIdx.x;
   const int m0 = tile * BM;
   const int rows = min(BM, p.batch - m0);
-  const int k = p.k_tables, d = p.d, d4 = d / 4;
+  const int k = p.k_tables, d = p.d, d4 = d >> 2;
   const int f = k + 1;
   const int pairs = f * (f - 1) / 2;
+  // quotients by these on the tile's paths come from quot (no divisions)
+  const float r_k = __frcp_rn(static_cast<float>(k));
+  const float r_d4 = __frcp_rn(static_cast<float>(d4));
   bool oob = false, bad_off = false;
 
   // Prologue: bias block + last-layer weights (group 0); global loads, two
@@ -384,6 +387,8 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
     const int lb = (kBagRows && p.bag_rows) ? p.bag : 1;
     const int n_bag = (pz || zb2) ? BM * k * lb : 0;
     const int kp = p.gemm[0].k_pad;
+    const float r_kp = __frcp_rn(static_cast<float>(kp));
+    const float r_lb = kBagRows ? __frcp_rn(static_cast<float>(lb)) : 1.f;
     const int n_dense = BM * kp;
     const int n_all = n_bag > n_dense ? n_bag : n_dense;
     // two elements per thread, both loads in flight before either is used
@@ -396,8 +401,8 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
         start[h] = row[h] = 0;
         dv[h] = 0.f;
         if (e < n_bag) {
-          const int sk = e / lb, l = e - sk * lb;
-          const int s = sk / k, t = sk - s * k;
+          const int sk = kBagRows ? quot(e, lb, r_lb) : e, l = e - sk * lb;
+          const int s = quot(sk, k, r_k), t = sk - s * k;
           if (s < rows) {
             const int64_t b = m0 + s;
             start[h] = __ldg(p.offsets + static_cast<int64_t>(t) * p.batch + b);
@@ -405,7 +410,7 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
           }
         }
         if (e < n_dense) {
-          const int m = e / kp, c = e - m * kp;
+          const int m = quot(e, kp, r_kp), c = e - m * kp;
           if (m < rows && c < p.n_dense)
             dv[h] = __ldg(p.dense + static_cast<int64_t>(m0 + m) * p.n_dense + c);
         }
@@ -414,8 +419,8 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
       for (int h = 0; h < 2; ++h) {
         const int e = e0 + h * kConsumers + tid;
         if (e < n_bag) {
-          const int sk = e / lb;
-          const int s = sk / k, t = sk - s * k;
+          const int sk = kBagRows ? quot(e, lb, r_lb) : e;
+          const int s = quot(sk, k, r_k), t = sk - s * k;
           int row32 = -1;
           if (s < rows) {
             // a bag that does not start at b * L is zeros (every one of its
@@ -427,7 +432,7 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
           rowidx_s[e] = row32;
         }
         if (e < n_dense) {
-          const int m = e / kp;
+          const int m = quot(e, kp, r_kp);
           act0[m * lda + (e - m * kp)] = dv[h];
         }
       }
@@ -436,10 +441,12 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
   consumer_sync<CW>();
   if (pz) {
     const int lb = (kBagRows && p.bag_rows) ? p.bag : 1;
+    const float r_lb = kBagRows ? __frcp_rn(static_cast<float>(lb)) : 1.f;
     for (int e = tid; e < BM * k * lb * d4; e += kConsumers) {
-      const int sk = e / d4;              // (sample * k + table) * L + l
+      const int sk = quot(e, d4, r_d4);   // (sample * k + table) * L + l
       const int c4 = e - sk * d4;
-      const float* table = p.tabs.ptr[(sk / lb) % k];
+      const int sb = kBagRows ? quot(sk, lb, r_lb) : sk;
+      const float* table = p.tabs.ptr[sb - quot(sb, k, r_k) * k];
       float* dst = zs + sk * p.ldz + 4 * c4;
       const int row = rowidx_s[sk];
       if (row >= 0) cp_async16(dst, table + static_cast<int64_t>(row) * d + 4 * c4);
@@ -452,13 +459,14 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
   stamp<TRACE>(p, tile, 1);
 
   // Bag-size-1 rows streamed by sample group into two buffers (zbuf == 2).
+  const float r_kd4 = __frcp_rn(static_cast<float>(k * d4));
   auto issue_group = [&](int g0, int buf) {
     float* zb = zs + buf * p.sg * k * p.ldz;
     const int ns = min(p.sg, BM - g0);
     for (int e = tid; e < ns * k * d4; e += kConsumers) {
-      const int s = e / (k * d4);
+      const int s = quot(e, k * d4, r_kd4);
       const int rem = e - s * k * d4;
-      const int t = rem / d4;
+      const int t = quot(rem, d4, r_d4);
       const int c4 = rem - t * d4;
       const int row = rowidx_s[(g0 + s) * k + t];
       float* dst = zb + (s * k + t) * p.ldz + 4 * c4;
@@ -492,14 +500,15 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
   // fill the columns between.
   const int rk = (p.n_top > 1) ? p.gemm[p.n_bot].k_pad : p.k_last;
   for (int e = tid; e < BM * d4; e += kConsumers) {
-    const int m = e / d4;
+    const int m = quot(e, d4, r_d4);
     const int c4 = e - m * d4;
     *reinterpret_cast<float4*>(r + m * lda + 4 * c4) =
         *reinterpret_cast<const float4*>(x + m * lda + 4 * c4);
   }
   const int r_pad = rk - d - pairs;
+  const float r_rpad = __frcp_rn(static_cast<float>(max(r_pad, 1)));
   for (int e = tid; e < BM * r_pad; e += kConsumers) {
-    const int m = e / r_pad;
+    const int m = quot(e, r_pad, r_rpad);
     r[m * lda + d + pairs + (e - m * r_pad)] = 0.f;
   }
   if (pz) cp_async_wait<0>();
@@ -516,7 +525,7 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
       const int e = tid + i * kConsumers;
       sums[i] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (e < BM * k * d4) {
-        const int sk = e / d4, c4 = e - sk * d4;
+        const int sk = quot(e, d4, r_d4), c4 = e - sk * d4;
         for (int l = 0; l < lb; ++l) {
           const float4 u = *reinterpret_cast<const float4*>(zs + (sk * lb + l) * p.ldz + 4 * c4);
           sums[i].x += u.x; sums[i].y += u.y; sums[i].z += u.z; sums[i].w += u.w;
@@ -528,7 +537,7 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
     for (int i = 0; i < kMaxSums; ++i) {
       const int e = tid + i * kConsumers;
       if (e < BM * k * d4) {
-        const int sk = e / d4, c4 = e - sk * d4;
+        const int sk = quot(e, d4, r_d4), c4 = e - sk * d4;
         *reinterpret_cast<float4*>(zs + sk * p.ldz + 4 * c4) = sums[i];
       }
     }
@@ -541,9 +550,9 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
       cp_async_wait<1>();   // group gi has landed (only gi + 1 may be pending)
     } else if (!pz) {
       for (int e = tid; e < ns * k * d4; e += kConsumers) {
-        const int s = e / (k * d4);
+        const int s = quot(e, k * d4, r_kd4);
         const int rem = e - s * k * d4;
-        const int t = rem / d4;
+        const int t = quot(rem, d4, r_d4);
         const int c4 = rem - t * d4;
         const int m = g0 + s;
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -579,8 +588,9 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
     // idle.
     const int nblk = gram_blocks(f);
     if (2 * ns * nblk >= kConsumers) {
+      const float r_nblk = __frcp_rn(static_cast<float>(nblk));
       for (int e = tid; e < ns * nblk; e += kConsumers) {
-        const int s = e / nblk;
+        const int s = quot(e, nblk, r_nblk);
         const int q = e - s * nblk;
         const float* xrow = x + (g0 + s) * lda;
         const float* zsam = zg + s * k * p.ldz;
@@ -598,8 +608,9 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
           }
       }
     } else {
+      const float r_pairs = __frcp_rn(static_cast<float>(pairs));
       for (int e = tid; e < ns * pairs; e += kConsumers) {
-        const int s = e / pairs;
+        const int s = quot(e, pairs, r_pairs);
         const int q = e - s * pairs;
         int i, j;
         pair_from_index(q, i, j);
