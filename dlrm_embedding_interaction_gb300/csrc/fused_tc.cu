@@ -165,18 +165,25 @@ __device__ void zero_operand(unsigned char* buf, int f0, int f1, int tid, int nt
   constexpr int KB = BF16 ? 64 : 32;
   const int c0 = (f0 + EPC - 1) / EPC, c1 = f1 / EPC;   // whole chunks [c0, c1)
   if (c0 >= c1) {
-    for (int e = tid; e < kTcTile * (f1 - f0); e += nthreads)
-      put_operand<BF16>(buf, e / (f1 - f0), f0 + e % (f1 - f0), 0.f);
+    const int w = f1 - f0;
+    const float rw = __frcp_rn(static_cast<float>(max(w, 1)));
+    for (int e = tid; e < kTcTile * w; e += nthreads) {
+      const int s = quot(e, w, rw);
+      put_operand<BF16>(buf, s, f0 + (e - s * w), 0.f);
+    }
     return;
   }
   const int head = c0 * EPC - f0, tail = f1 - c1 * EPC;
-  for (int e = tid; e < kTcTile * (head + tail); e += nthreads) {
-    const int s = e / (head + tail), q = e % (head + tail);
+  const int ht = head + tail;
+  const float rht = __frcp_rn(static_cast<float>(max(ht, 1)));
+  for (int e = tid; e < kTcTile * ht; e += nthreads) {
+    const int s = quot(e, ht, rht), q = e - s * ht;
     put_operand<BF16>(buf, s, q < head ? f0 + q : c1 * EPC + (q - head), 0.f);
   }
   const int nch = c1 - c0;
+  const float rnch = __frcp_rn(static_cast<float>(nch));
   for (int e = tid; e < kTcTile * nch; e += nthreads) {
-    const int s = e / nch, c = c0 + e % nch;      // chunk c of the feature axis
+    const int s = quot(e, nch, rnch), c = c0 + (e - s * nch);   // chunk c of the feature axis
     const int f = c * EPC;
     *reinterpret_cast<uint4*>(buf + (f / KB) * kActBlock + swz_offset(s, (f % KB) * (BF16 ? 2 : 4) >> 4)) =
         make_uint4(0u, 0u, 0u, 0u);
@@ -329,9 +336,13 @@ __device__ void epilogue(const FusedTcParams& p, uint32_t tmem, unsigned char* c
   const int lane = tid % kWarp;
   const int m0 = blockIdx.x * kTcTile;
   const int rows = min(kTcTile, p.batch - m0);
-  const int k = p.k_tables, d = p.d, d4 = d / 4;
+  const int k = p.k_tables, d = p.d, d4 = d >> 2;
   const int f = k + 1;
   const int pairs = f * (f - 1) / 2;
+  // quotients by these on the tile's paths come from quot (no divisions)
+  const float r_k = __frcp_rn(static_cast<float>(k));
+  const float r_d4 = __frcp_rn(static_cast<float>(d4));
+  const float r_dn = __frcp_rn(static_cast<float>(max(p.n_dense, 1)));
   bool oob = false, bad_off = false;
 
   // ---- prologue. Biases and last-layer weights by cp.async. Then global
@@ -356,14 +367,14 @@ __device__ void epilogue(const FusedTcParams& p, uint32_t tmem, unsigned char* c
         start[h] = row[h] = 0;
         dv[h] = 0.f;
         if (e < n_bag) {
-          const int s = e / k, t = e - s * k;
+          const int s = quot(e, k, r_k), t = e - s * k;
           if (s < rows) {
             start[h] = __ldg(p.offsets + static_cast<int64_t>(t) * p.batch + m0 + s);
             row[h] = __ldg(p.indices + static_cast<int64_t>(t) * p.batch + m0 + s);
           }
         }
         if (e < n_dn) {
-          const int s = e / p.n_dense;
+          const int s = quot(e, p.n_dense, r_dn);
           if (s < rows) dv[h] = __ldg(p.dense + static_cast<int64_t>(m0) * p.n_dense + e);
         }
       }
@@ -371,7 +382,7 @@ __device__ void epilogue(const FusedTcParams& p, uint32_t tmem, unsigned char* c
       for (int h = 0; h < 2; ++h) {
         const int e = e0 + h * kEpi + tid;
         if (e < n_bag) {
-          const int s = e / k, t = e - s * k;
+          const int s = quot(e, k, r_k), t = e - s * k;
           int row32 = -1;
           if (s < rows) {
             if (start[h] != m0 + s) bad_off = true;
@@ -381,7 +392,7 @@ __device__ void epilogue(const FusedTcParams& p, uint32_t tmem, unsigned char* c
           rowidx_s[e] = row32;
         }
         if (e < n_dn) {
-          const int s = e / p.n_dense;
+          const int s = quot(e, p.n_dense, r_dn);
           put_operand<BF16>(act[0], s, e - s * p.n_dense, dv[h]);
         }
       }
@@ -394,9 +405,9 @@ __device__ void epilogue(const FusedTcParams& p, uint32_t tmem, unsigned char* c
   if (tid == 0) mbar_arrive(smem_addr(act_ready));
   if (p.bag == 1) {
     for (int e = tid; e < kTcTile * k * d4; e += kEpi) {
-      const int sk = e / d4;                    // sample * k + table
+      const int sk = quot(e, d4, r_d4);         // sample * k + table
       const int c4 = e - sk * d4;
-      const float* table = p.tabs.ptr[sk % k];
+      const float* table = p.tabs.ptr[sk - quot(sk, k, r_k) * k];
       const int row = rowidx_s[sk];
       cp_async16(zs + sk * p.ldz + 4 * c4,
                  row >= 0 ? table + static_cast<int64_t>(row) * d + 4 * c4 : table, row >= 0 ? 16 : 0);
@@ -405,9 +416,9 @@ __device__ void epilogue(const FusedTcParams& p, uint32_t tmem, unsigned char* c
     // bags of p.bag rows at offsets b * bag: summed in registers (an
     // out-of-range row adds nothing and raises the flag)
     for (int e = tid; e < kTcTile * k * d4; e += kEpi) {
-      const int sk = e / d4;
+      const int sk = quot(e, d4, r_d4);
       const int c4 = e - sk * d4;
-      const int s = sk / k, t = sk - s * k;
+      const int s = quot(sk, k, r_k), t = sk - s * k;
       float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
       if (s < rows) {
         const int64_t b = m0 + s;
@@ -489,8 +500,9 @@ __device__ void epilogue(const FusedTcParams& p, uint32_t tmem, unsigned char* c
       stamp<TRACE>(p, 2 + g);
       // one (sample, pair) dot per thread, then zeros to the padded width
       const int kw = p.gemm[g + 1].kbs * KB;
+      const float r_pairs = __frcp_rn(static_cast<float>(pairs));
       for (int e = tid; e < kTcTile * pairs; e += kEpiWarps * kWarp) {
-        const int s = e / pairs;
+        const int s = quot(e, pairs, r_pairs);
         const int q = e - s * pairs;
         int i, jj;
         pair_from_index(q, i, jj);
