@@ -52,10 +52,11 @@ __device__ __forceinline__ float apply_act(float a, int act) {
 
 // a / b for 0 <= a < 2^20 and 1 <= b < 2^14, given rb = __frcp_rn(b): the
 // rounded product a rb is within one of the quotient (its relative error is
-// below 2^-22), and one correction step each way makes it exact (also
-// checked over that whole range on the host). Shorter than the integer
-// division sequence on the fused kernels' latency-bound tile paths, where
-// every divisor is a loop invariant whose reciprocal is taken once.
+// below 2^-22), and one correction step each way makes it exact
+// (tests/test_quot.py restates it in float32 and checks it next to every
+// multiple in that range). Shorter than the integer division sequence on the
+// fused kernels' latency-bound tile paths, where every divisor is a loop
+// invariant whose reciprocal is taken once.
 __device__ __forceinline__ int quot(int a, int b, float rb) {
   int q = __float2int_rz(__fmul_rn(__int2float_rn(a), rb));
   const int r = a - q * b;
