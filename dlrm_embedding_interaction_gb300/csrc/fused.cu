@@ -104,7 +104,7 @@ bool fused_plan(int n_dense, int k_tables, int d, int bag, const std::vector<int
   bias_floats += 4;
   p.bias_floats = bias_floats;
   widest = std::max({widest, p.k_last, d + pairs});
-  p.lda = static_cast<int>(round_up(widest, 32)) + 4;
+  p.lda = static_cast<int>(round_up(widest, 32)) + 16;
   p.ldz = static_cast<int>(round_up(d, 4)) + 4;
 
   // shared-memory carve: stages | act0 | act1 | z | rowidx | bias | wlast | barriers

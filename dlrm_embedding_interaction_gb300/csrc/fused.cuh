@@ -36,7 +36,7 @@ struct FusedParams {
   int batch, n_dense, k_tables, d, bag, n_bot, n_top;
   int n_gemm;        // n_bot + n_top - 1 (the last top layer is the N = 1 dot)
   int cw;            // computing warps (8)
-  int lda;           // activation row stride (floats), >= 516, = 4 mod 32
+  int lda;           // activation row stride (floats), >= 528, = 16 mod 32
   int ldz;           // bag-sum row stride, round_up(d, 4) + 4
   int sg;            // samples per gather/interaction group
   int prefetch_z;    // 1: all BM samples' rows are fetched at kernel start (bag 1, or
@@ -89,12 +89,12 @@ bool fused_plan(int n_dense, int k_tables, int d, int bag, const std::vector<int
                 const std::vector<std::vector<float>>& b, const GatherTables& tabs,
                 int max_batch, int sms, size_t smem_limit, int consumer_warps, FusedPlan* plan);
 
-// The activation stride of the kernel instance a plan runs on: 516 or 612
+// The activation stride of the kernel instance a plan runs on: 528 or 624
 // (compile-time strides, one bag-row mode each) when the plan's stride and
 // mode match those instances, else 0 (the run-time-stride instances).
 inline int fused_instance_lda(const FusedParams& p) {
-  if (p.lda == 516 && p.prefetch_z && !p.bag_rows) return 516;
-  if (p.lda == 612 && p.zbuf == 2) return 612;
+  if (p.lda == 528 && p.prefetch_z && !p.bag_rows) return 528;
+  if (p.lda == 624 && p.zbuf == 2) return 624;
   return 0;
 }
 // lda: fused_instance_lda of the plan.

@@ -102,7 +102,7 @@ __host__ __device__ __forceinline__ int gemm_rows(const FusedGemm& L, int pass) 
 // Shared-memory cost: a 128-bit load is served per half-warp, in one
 // wavefront when the half-warp's distinct 16-byte words sit in distinct bank
 // groups. A half-warp's activation load reads two rows (adjacent rows are
-// four banks apart: lda = 4 mod 32) and its weight load eight consecutive
+// sixteen banks apart: lda = 16 mod 32) and its weight load eight consecutive
 // staged columns (the chunk swizzle puts eight consecutive rows of a stage
 // in eight bank groups), so every load costs two wavefronts per warp: per
 // 4-wide k step (TM + TN) loads, 2 (TM + TN) wavefronts, for 2 TM TN packed
@@ -247,6 +247,9 @@ __device__ void gemm_layer(const FusedGemm& L, float* a_s, float* c_s, int lda_r
       kstamp[0] = global_ns();
       kstamp[10] = static_cast<unsigned long long>(waited);
     }
+    // The lanes' scalar stores below hit row parities rg = 0, 1 at columns
+    // lcg + 16 j: with lda = 16 mod 32 the two parities' 16 banks are
+    // disjoint, one wavefront per store (two at lda = 4 mod 32).
     const int c0 = pass * per_pass + cg * WCOLS + lcg;   // the lane's first column
     if (KSLICES == 1) {
       if (active) {
@@ -351,12 +354,12 @@ __device__ void consume(const FusedParams& p, const Ring& ring, float* act0, flo
   // this kernel's instructions are fetched cold after every L2 flush (the
   // 2048-sample, 3-table forward ran 4 us slower with the extra code inline).
   constexpr bool kBagRows = LDA == 0;
-  // Bag-row mode: each compile-time-stride instance takes one mode (516: every
-  // bag row prefetched at tile start; 612: rows streamed through two group
+  // Bag-row mode: each compile-time-stride instance takes one mode (528: every
+  // bag row prefetched at tile start; 624: rows streamed through two group
   // buffers), so the other modes' code is not in it; fused_instance_lda sends
   // every other plan to the run-time-stride instances, which take any mode.
-  const bool pz = LDA == 516 ? true : (LDA == 612 ? false : p.prefetch_z != 0);
-  const bool zb2 = LDA == 612 ? true : (LDA == 516 ? false : p.zbuf == 2);
+  const bool pz = LDA == 528 ? true : (LDA == 624 ? false : p.prefetch_z != 0);
+  const bool zb2 = LDA == 624 ? true : (LDA == 528 ? false : p.zbuf == 2);
   const int lda = LDA > 0 ? LDA : p.lda;   // activation row stride
   const int tid = threadIdx.x;
   const int m0 = tile * BM;
@@ -766,23 +769,23 @@ cudaError_t enable_smem() {
 
 // Kernel instances: every tile height with a run-time activation row stride,
 // and the tile heights of 8 rows and more with the strides the workload
-// models take (516: widest layer or interaction row <= 512 floats; 612: the
+// models take (528: widest layer or interaction row <= 512 floats; 624: the
 // 32-table models' 592-wide interaction rows) as compile-time constants.
 #define DLRM_FUSED_SWITCH(BM_VAR, LDA_VAR, CALL)                                     \
-  switch ((BM_VAR) * 10000 + (((BM_VAR) >= 8 && ((LDA_VAR) == 516 || (LDA_VAR) == 612)) \
+  switch ((BM_VAR) * 10000 + (((BM_VAR) >= 8 && ((LDA_VAR) == 528 || (LDA_VAR) == 624)) \
                                   ? (LDA_VAR)                                          \
                                   : 0)) {                                              \
-    case 16 * 10000 + 516: CALL(16, 516); break;                                       \
-    case 16 * 10000 + 612: CALL(16, 612); break;                                       \
+    case 16 * 10000 + 528: CALL(16, 528); break;                                       \
+    case 16 * 10000 + 624: CALL(16, 624); break;                                       \
     case 16 * 10000: CALL(16, 0); break;                                               \
-    case 14 * 10000 + 516: CALL(14, 516); break;                                       \
-    case 14 * 10000 + 612: CALL(14, 612); break;                                       \
+    case 14 * 10000 + 528: CALL(14, 528); break;                                       \
+    case 14 * 10000 + 624: CALL(14, 624); break;                                       \
     case 14 * 10000: CALL(14, 0); break;                                               \
-    case 12 * 10000 + 516: CALL(12, 516); break;                                       \
-    case 12 * 10000 + 612: CALL(12, 612); break;                                       \
+    case 12 * 10000 + 528: CALL(12, 528); break;                                       \
+    case 12 * 10000 + 624: CALL(12, 624); break;                                       \
     case 12 * 10000: CALL(12, 0); break;                                               \
-    case 8 * 10000 + 516: CALL(8, 516); break;                                         \
-    case 8 * 10000 + 612: CALL(8, 612); break;                                         \
+    case 8 * 10000 + 528: CALL(8, 528); break;                                         \
+    case 8 * 10000 + 624: CALL(8, 624); break;                                         \
     case 8 * 10000: CALL(8, 0); break;                                                 \
     case 4 * 10000: CALL(4, 0); break;                                                 \
     default: return cudaErrorInvalidValue;                                             \
