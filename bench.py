@@ -53,7 +53,7 @@ SM_MAX_MHZ_DEFAULT = 2070.0
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
 # capture of the kernel as built now on the named workload; a kernel change
 # invalidates the entry.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {("fused", "b2048_k3"): 3175168}
 # DRAM bytes (read + write) of one standalone gather launch on the full 26 x 1M x 128
 # tables, bags of 20 (ncu dram__bytes_read.sum + dram__bytes_write.sum, one pass):
 # table-major bag order lets repeats of a row within a table's pass hit L2, so the
