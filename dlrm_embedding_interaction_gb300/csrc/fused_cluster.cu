@@ -190,10 +190,14 @@ __device__ void cluster_gemm(const ClusterParams& p, const Cta& c, int g, const 
     }
     ring_release(r, pos.slot);
   }
-  // k-slice partial sums: scratch[(slice * BM + m) * s + column]
+  // k-slice partial sums: scratch[slice * kstride + m * s + column]. The
+  // slices sit kstride = BM s + 4 floats apart: BM s is a multiple of 32
+  // floats, and without the skew the G lanes that sum one output float4
+  // (consecutive slices) would read one bank group, G ways conflicted.
+  const int kstride = BM * L.s + 4;
 #pragma unroll
   for (int m = 0; m < BM; ++m)
-    *reinterpret_cast<float2*>(scratch + (ks * BM + m) * L.s + 2 * cg) =
+    *reinterpret_cast<float2*>(scratch + ks * kstride + m * L.s + 2 * cg) =
         make_float2(acc[m][0].x + acc[m][0].y, acc[m][1].x + acc[m][1].y);
   const int e = exchange_of_gemm(p, g);
   arm_exchange(p, c, e + 1);   // before any byte of exchange e leaves this CTA
@@ -222,7 +226,7 @@ __device__ void cluster_gemm(const ClusterParams& p, const Cta& c, int g, const 
     if (live) {
       for (int kk = gl; kk < L.kslices; kk += gsz) {
         const float4 u =
-            *reinterpret_cast<const float4*>(scratch + (kk * BM + m) * L.s + 4 * c4);
+            *reinterpret_cast<const float4*>(scratch + kk * kstride + m * L.s + 4 * c4);
         v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w;
       }
     }
@@ -784,7 +788,9 @@ bool fused_cluster_plan(int n_dense, int k_tables, int d, int bag, const std::ve
     p.bm = bm;
     p.zrows = (bm + csize - 1) / csize;
     const size_t act = align128(static_cast<size_t>(bm) * p.lda * sizeof(float));
-    const size_t scratch = align128(std::max<size_t>(static_cast<size_t>(512) * bm,
+    // k-slice partial sums (512 / s slices of bm s floats, each skewed by 4)
+    // or the interaction rows staged for the exchange
+    const size_t scratch = align128(std::max<size_t>(static_cast<size_t>(512) * bm + 4 * 128,
                                                      static_cast<size_t>(p.zrows) * p.ld_r) *
                                     sizeof(float));
     const size_t z = align128(static_cast<size_t>(p.zrows) * k_tables * p.ldz * sizeof(float));
