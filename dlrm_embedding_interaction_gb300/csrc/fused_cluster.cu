@@ -159,7 +159,8 @@ __device__ void cluster_gemm(const ClusterParams& p, const Cta& c, int g, const 
   const int ks = tid >> (31 - __clz(half));
   const int k4v = (L.k + 3) >> 2;
   // kslices = 512 / s is a power of two: shifts, not divisions, per stage
-  // (k_here and the inputs left are non-negative multiples of it)
+  // (k_here is a multiple of 4 kslices; the inputs left are rounded up by
+  // the shift, every operand non-negative)
   const int kshift = 31 - __clz(L.kslices);
   float2 acc[BM][2];
 #pragma unroll
