@@ -56,7 +56,11 @@ __device__ __forceinline__ float apply_act(float a, int act) {
 // (tests/test_quot.py restates it in float32 and checks it next to every
 // multiple in that range). Shorter than the integer division sequence on the
 // fused kernels' latency-bound tile paths, where every divisor is a loop
-// invariant whose reciprocal is taken once.
+// invariant whose reciprocal is taken once. The dividends there are element
+// or task indices of one tile (at most 16 samples x 8,256 pairs, below 2^18),
+// and the divisors widths of arrays that one tile keeps in 227 KB of shared
+// memory (a sample's k x D/4 bag-row chunks, a row of activations) or the
+// pair count (8,256 at the 128-table limit): all below 2^14.
 __device__ __forceinline__ int quot(int a, int b, float rb) {
   int q = __float2int_rz(__fmul_rn(__int2float_rn(a), rb));
   const int r = a - q * b;
