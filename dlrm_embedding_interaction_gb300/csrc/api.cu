@@ -158,8 +158,9 @@ int cluster_max_batch(int n_tables) { (void)n_tables; return 256; }
 constexpr int kWideClusterMaxBatch = 32;
 // It pays only for models whose weights the one-CTA tile streams for long:
 // a stream of 1 MiB (32 stages; 1.3 MB on those models) or more. The 20 KB
-// weights of a 64-wide model run in 14 us on one CTA per tile, against the
-// cluster kernel's ~20 us of exchanges.
+// weights of a 64-wide model ran in 14 us on one CTA per tile against 18.6
+// on the cluster kernel, whose per-layer exchanges cost more than the
+// stream they save (12.3 us on one CTA per tile now).
 constexpr size_t kClusterMinStreamBytes = size_t(1) << 20;
 
 bool tensor_core_math(int math) { return math == DLRM_MATH_TF32 || math == DLRM_MATH_BF16; }
